@@ -1,0 +1,179 @@
+"""fp64 CPU oracle for masked second-order Higher-order Linear Attention.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py`` may import this package.  The CUDA library
+never loads it, and it shares no code with the CUDA path.
+
+The arithmetic lives in ``hla_oracle.c`` (plain loops in the order of the formulas
+on the gist.science technical summary of "Higher-order Linear Attention",
+section 1 "Tweede-orde HLA" and section 4 "Parallelle training via associatieve
+scans").  This module compiles it with gcc and marshals numpy arrays to it.
+
+Pins (what the oracle is checked against, all in ``tests/test_oracle_pins.py``):
+brute-force triple sum over key <= query/value index <= t, the dense masked-matrix
+form, hand-derived integer fixtures in ``tests/golden/``, closed forms for constant
+inputs, n = 1 / d = 1 / decay 0 / decay 1 special cases, chunk-size invariance of
+the chunked scan, associativity and identity of segment concatenation, strict
+causality, split resume, and the unmasked identity.  The decay variant's formula is
+not printed on the pages; its pins are internal consistency only (see the decay
+reading in hla_oracle.c).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "hla_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "libhla_oracle.so")
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile hla_oracle.c into a shared library (gcc, -O2, no fast-math)."""
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(build())
+        dp = ctypes.POINTER(ctypes.c_double)
+        i = ctypes.c_int
+        d = ctypes.c_double
+        _lib.hla_oracle_forward.argtypes = [i, i, i, i, i, dp, dp, dp, dp, i, d] + [dp] * 5 + [dp] + [dp] * 5 + [i]
+        _lib.hla_oracle_forward_chunked.argtypes = [i, i, i, i, i, i, dp, dp, dp, dp, i, d] + [dp] * 5 + [dp] + [dp] * 5 + [i]
+        _lib.hla_oracle_decode_step.argtypes = [i, i, i, i, dp, i, d] + [dp] * 5 + [dp, dp, dp, dp, i]
+        _lib.hla_oracle_combine.argtypes = [i, i, i] + [dp] * 10 + [dp] + [dp] * 5
+        for f in (_lib.hla_oracle_forward, _lib.hla_oracle_forward_chunked,
+                  _lib.hla_oracle_decode_step, _lib.hla_oracle_combine):
+            f.restype = ctypes.c_int
+    return _lib
+
+
+def _p(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _f64(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float64)
+
+
+@dataclass
+class State:
+    """The five summaries of every (b,h): S [BH,d,d], C [BH,d,dv], m [BH,d],
+    G [BH,d,dv], h [BH,d], fp64."""
+    S: np.ndarray
+    C: np.ndarray
+    m: np.ndarray
+    G: np.ndarray
+    h: np.ndarray
+
+    @staticmethod
+    def zeros(units: int, d: int, dv: int) -> "State":
+        return State(np.zeros((units, d, d)), np.zeros((units, d, dv)), np.zeros((units, d)),
+                     np.zeros((units, d, dv)), np.zeros((units, d)))
+
+    def copy(self) -> "State":
+        return State(*(np.array(x, dtype=np.float64, copy=True) for x in self.astuple()))
+
+    def astuple(self):
+        return (self.S, self.C, self.m, self.G, self.h)
+
+
+def _state_ptrs(st):
+    if st is None:
+        return [None] * 5
+    return [_p(x) for x in st.astuple()]
+
+
+def _as_state(st, units, d, dv):
+    if st is None:
+        return None
+    s = State(*(_f64(x) for x in st.astuple()))
+    assert s.S.size == units * d * d and s.C.size == units * d * dv and s.m.size == units * d
+    return s
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def forward(q, k, v, gamma=None, normalize=False, eps=0.0, state_in=None,
+            want_state=True, chunk=None, nthreads=None):
+    """Masked 2nd-order HLA forward in fp64.
+
+    q, k: [B,H,n,d]; v: [B,H,n,dv]; gamma: [H] or None.  chunk=None runs the serial
+    recurrence; chunk=c runs the chunked scan (per-chunk summaries folded with the
+    segment-concatenation rule).  Returns (o [B,H,n,dv], State or None).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, n, d = q.shape
+    dv = v.shape[-1]
+    assert k.shape == q.shape and v.shape[:3] == q.shape[:3]
+    g = _f64(gamma)
+    if g is not None:
+        assert g.shape == (H,)
+    sin = _as_state(state_in, B * H, d, dv)
+    o = np.zeros((B, H, n, dv))
+    sout = State.zeros(B * H, d, dv) if want_state else None
+    lib = _load()
+    nt = nthreads or default_threads()
+    args_tail = [_p(q), _p(k), _p(v), _p(g), int(bool(normalize)), float(eps)] + _state_ptrs(sin) + \
+        [_p(o)] + _state_ptrs(sout) + [nt]
+    if chunk is None:
+        rc = lib.hla_oracle_forward(B, H, n, d, dv, *args_tail)
+    else:
+        rc = lib.hla_oracle_forward_chunked(B, H, n, d, dv, int(chunk), *args_tail)
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return o, sout
+
+
+def decode_step(state: State, q, k, v, H, gamma=None, normalize=False, eps=0.0, nthreads=None):
+    """One decode step for N (sequence, head) pairs, in place on ``state``.
+    q, k: [N,d]; v: [N,dv]; pair u uses gamma[u % H].  Returns o [N,dv]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    N, d = q.shape
+    dv = v.shape[-1]
+    g = _f64(gamma)
+    for x in state.astuple():
+        assert x.dtype == np.float64 and x.flags.c_contiguous
+    o = np.zeros((N, dv))
+    rc = _load().hla_oracle_decode_step(N, H, d, dv, _p(g), int(bool(normalize)), float(eps),
+                                        *_state_ptrs(state), _p(q), _p(k), _p(v), _p(o),
+                                        nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return o
+
+
+def combine(A: State, Bst: State, decay_pow=None) -> State:
+    """Segment concatenation out = A (+) B for every item (A earlier than B)."""
+    A = State(*(_f64(x) for x in A.astuple()))
+    Bst = State(*(_f64(x) for x in Bst.astuple()))
+    count, d, dv = A.C.shape
+    out = State.zeros(count, d, dv)
+    f = _f64(decay_pow)
+    rc = _load().hla_oracle_combine(count, d, dv, *_state_ptrs(A), *_state_ptrs(Bst), _p(f),
+                                    *_state_ptrs(out))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out

@@ -1,0 +1,423 @@
+/*
+ * hla_oracle.c -- fp64 CPU oracle for masked second-order Higher-order Linear
+ * Attention (HLA).
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke check
+ * and the CPU-baseline leg of the benchmark load this file.  It shares no code,
+ * header, table or helper with the CUDA library, and the CUDA library never
+ * loads it.
+ *
+ * What it computes (sources: "Higher-order Linear Attention", gist.science
+ * technical summary, section 1 "Tweede-orde HLA", bullets "Onderhoud van de
+ * toestand", "Strenge causaliteit", "Outputformulering", "Normalisatie";
+ * section 4 "Parallelle training via associatieve scans", bullets
+ * "Associatieve operatoren" and "Scan-equivalentie"; "Belangrijkste
+ * bijdragen" item 2 for the exponential-decay variant):
+ *
+ *   prefix summaries   S_t = sum_{i<=t} k_i k_i^T        (d x d)
+ *                      C_t = sum_{i<=t} q_i v_i^T        (d x dv)
+ *                      m_t = sum_{i<=t} q_i              (d)
+ *   cross summaries    G_t = G_{t-1} + k_t (k_t^T C_{t-1})   (d x dv)
+ *                      h_t = h_{t-1} + k_t (k_t^T m_{t-1})   (d)
+ *   masked output      o_t = q_t^T (S_t C_t - G_t)
+ *   ratio-normalised   o_t = q_t^T (S_t C_t - G_t) / (q_t^T (S_t m_t - h_t) + eps)
+ *
+ * Exponential decay (per head, factor g in [0,1]): every prefix statistic decays
+ * by g per step, S_t = g S_{t-1} + k k^T, C_t = g C_{t-1} + q v^T,
+ * m_t = g m_{t-1} + q, and the cross summaries take the factors that keep
+ * q_t^T(S_t C_t - G_t) equal to the masked sum of decayed pairs:
+ * G_t = g^2 G_{t-1} + g k_t (k_t^T C_{t-1}),  h_t = g^2 h_{t-1} + g k_t (k_t^T m_{t-1}).
+ * The pages name the decayed operators without printing them; this is the
+ * plainest reading that the undecayed formulas support.  With g = 1 every
+ * formula above reduces to the undecayed one.
+ *
+ * Segment concatenation (semidirect product), segment A before segment B,
+ * f = g^{len(B)}:
+ *   S = f S_A + S_B,  C = f C_A + C_B,  m = f m_A + m_B,
+ *   G = f^2 G_A + G_B + f S_B C_A,   h = f^2 h_A + h_B + f S_B m_A.
+ * The cross term S_B C_A is the one the pages name.
+ *
+ * Layout: q, k [B][H][n][d]; v, o [B][H][n][dv]; row-major, fp64.
+ * State, one block per (b,h): S [BH][d][d], C [BH][d][dv], m [BH][d],
+ * G [BH][d][dv], h [BH][d].
+ *
+ * Everything is a plain loop in the order the formulas are written; no
+ * blocking, no fusion.  Independent (b,h) pairs run on separate threads.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    double *S, *C, *m, *G, *h;
+} ostate;
+
+/* one (b,h) stream: the five summaries of one head, plus its decay factor */
+typedef struct {
+    int d, dv;
+    double g;
+    double *S, *C, *m, *G, *h; /* views into caller state for this (b,h) */
+    double *kc;                /* scratch: k^T C_{t-1}, length dv        */
+    double *qs;                /* scratch: q^T S_t, length d             */
+} stream_t;
+
+/* One token of the serial recurrence.  The cross summaries are updated from
+ * the previous C and m first, then the prefix summaries take the new token.
+ * If o != NULL the (optionally normalised) output of this token is written. */
+static void step_token(stream_t *st, const double *q, const double *k,
+                       const double *v, int normalize, double eps, double *o)
+{
+    const int d = st->d, dv = st->dv;
+    const double g = st->g, g2 = g * g;
+    double *S = st->S, *C = st->C, *m = st->m, *G = st->G, *h = st->h;
+
+    /* k^T C_{t-1} and k^T m_{t-1} */
+    for (int j = 0; j < dv; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i) acc += k[i] * C[i * dv + j];
+        st->kc[j] = acc;
+    }
+    double km = 0.0;
+    for (int i = 0; i < d; ++i) km += k[i] * m[i];
+
+    /* G_t = g^2 G_{t-1} + g k (k^T C_{t-1}),  h_t = g^2 h_{t-1} + g k (k^T m_{t-1}) */
+    for (int i = 0; i < d; ++i) {
+        for (int j = 0; j < dv; ++j)
+            G[i * dv + j] = g2 * G[i * dv + j] + g * k[i] * st->kc[j];
+        h[i] = g2 * h[i] + g * k[i] * km;
+    }
+    /* S_t = g S_{t-1} + k k^T */
+    for (int i = 0; i < d; ++i)
+        for (int j = 0; j < d; ++j)
+            S[i * d + j] = g * S[i * d + j] + k[i] * k[j];
+    /* C_t = g C_{t-1} + q v^T,  m_t = g m_{t-1} + q */
+    for (int i = 0; i < d; ++i) {
+        for (int j = 0; j < dv; ++j)
+            C[i * dv + j] = g * C[i * dv + j] + q[i] * v[j];
+        m[i] = g * m[i] + q[i];
+    }
+    if (!o) return;
+
+    /* o_t = q^T (S_t C_t - G_t), evaluated as (q^T S_t) C_t - q^T G_t so that
+     * the cost per token is O(d^2 + d dv) as the pages state. */
+    for (int j = 0; j < d; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i) acc += q[i] * S[i * d + j];
+        st->qs[j] = acc;
+    }
+    double den = 0.0;
+    if (normalize) {
+        /* q^T (S_t m_t - h_t) */
+        for (int i = 0; i < d; ++i) den += st->qs[i] * m[i] - q[i] * h[i];
+        den += eps;
+    }
+    for (int j = 0; j < dv; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i) acc += st->qs[i] * C[i * dv + j] - q[i] * G[i * dv + j];
+        o[j] = normalize ? acc / den : acc;
+    }
+}
+
+/* R7: out = A (+) B, A earlier in time than B, f = g^{len(B)}.
+ * out may alias A or B: every output is formed in a private buffer first. */
+static void combine_one(int d, int dv, double f,
+                        const double *SA, const double *CA, const double *mA,
+                        const double *GA, const double *hA,
+                        const double *SB, const double *CB, const double *mB,
+                        const double *GB, const double *hB,
+                        double *S, double *C, double *m, double *G, double *h)
+{
+    const double f2 = f * f;
+    double *tG = (double *)malloc(sizeof(double) * (size_t)d * dv);
+    double *th = (double *)malloc(sizeof(double) * (size_t)d);
+    for (int i = 0; i < d; ++i) {
+        for (int j = 0; j < dv; ++j) {
+            double cross = 0.0; /* (S_B C_A)[i][j] */
+            for (int l = 0; l < d; ++l) cross += SB[i * d + l] * CA[l * dv + j];
+            tG[i * dv + j] = f2 * GA[i * dv + j] + GB[i * dv + j] + f * cross;
+        }
+        double crossm = 0.0; /* (S_B m_A)[i] */
+        for (int l = 0; l < d; ++l) crossm += SB[i * d + l] * mA[l];
+        th[i] = f2 * hA[i] + hB[i] + f * crossm;
+    }
+    for (int i = 0; i < d * d; ++i) S[i] = f * SA[i] + SB[i];
+    for (int i = 0; i < d * dv; ++i) C[i] = f * CA[i] + CB[i];
+    for (int i = 0; i < d; ++i) m[i] = f * mA[i] + mB[i];
+    memcpy(G, tG, sizeof(double) * (size_t)d * dv);
+    memcpy(h, th, sizeof(double) * (size_t)d);
+    free(tG);
+    free(th);
+}
+
+/* ------------------------------------------------------------------------- */
+/* work distribution over (b,h) pairs                                        */
+
+typedef struct {
+    int B, H, n, d, dv, chunk;
+    const double *q, *k, *v, *gamma;
+    int normalize;
+    double eps;
+    ostate in, out;
+    double *o;
+    int next; /* next unit to take, guarded by lock */
+    pthread_mutex_t lock;
+    int mode; /* 0 serial forward, 1 chunked-scan forward, 2 decode step */
+} job_t;
+
+static int take_unit(job_t *J, int total)
+{
+    pthread_mutex_lock(&J->lock);
+    int u = J->next < total ? J->next++ : -1;
+    pthread_mutex_unlock(&J->lock);
+    return u;
+}
+
+static void load_state(stream_t *st, const ostate *in, size_t u)
+{
+    const int d = st->d, dv = st->dv;
+    if (in && in->S) {
+        memcpy(st->S, in->S + u * d * d, sizeof(double) * d * d);
+        memcpy(st->C, in->C + u * d * dv, sizeof(double) * d * dv);
+        memcpy(st->m, in->m + u * d, sizeof(double) * d);
+        memcpy(st->G, in->G + u * d * dv, sizeof(double) * d * dv);
+        memcpy(st->h, in->h + u * d, sizeof(double) * d);
+    } else {
+        memset(st->S, 0, sizeof(double) * d * d);
+        memset(st->C, 0, sizeof(double) * d * dv);
+        memset(st->m, 0, sizeof(double) * d);
+        memset(st->G, 0, sizeof(double) * d * dv);
+        memset(st->h, 0, sizeof(double) * d);
+    }
+}
+
+static void store_state(const stream_t *st, ostate *out, size_t u)
+{
+    const int d = st->d, dv = st->dv;
+    if (!out || !out->S) return;
+    memcpy(out->S + u * d * d, st->S, sizeof(double) * d * d);
+    memcpy(out->C + u * d * dv, st->C, sizeof(double) * d * dv);
+    memcpy(out->m + u * d, st->m, sizeof(double) * d);
+    memcpy(out->G + u * d * dv, st->G, sizeof(double) * d * dv);
+    memcpy(out->h + u * d, st->h, sizeof(double) * d);
+}
+
+static stream_t stream_new(int d, int dv)
+{
+    stream_t st;
+    st.d = d;
+    st.dv = dv;
+    st.g = 1.0;
+    st.S = (double *)calloc((size_t)d * d, sizeof(double));
+    st.C = (double *)calloc((size_t)d * dv, sizeof(double));
+    st.m = (double *)calloc((size_t)d, sizeof(double));
+    st.G = (double *)calloc((size_t)d * dv, sizeof(double));
+    st.h = (double *)calloc((size_t)d, sizeof(double));
+    st.kc = (double *)calloc((size_t)dv, sizeof(double));
+    st.qs = (double *)calloc((size_t)d, sizeof(double));
+    return st;
+}
+
+static void stream_free(stream_t *st)
+{
+    free(st->S); free(st->C); free(st->m); free(st->G); free(st->h);
+    free(st->kc); free(st->qs);
+}
+
+/* serial recurrence over all n tokens of unit u = b*H + hh */
+static void run_serial(job_t *J, stream_t *st, int u)
+{
+    const int n = J->n, d = J->d, dv = J->dv;
+    const size_t qo = (size_t)u * n * d, vo = (size_t)u * n * dv;
+    load_state(st, &J->in, u);
+    for (int t = 0; t < n; ++t)
+        step_token(st, J->q + qo + (size_t)t * d, J->k + qo + (size_t)t * d,
+                   J->v + vo + (size_t)t * dv, J->normalize, J->eps,
+                   J->o ? J->o + vo + (size_t)t * dv : NULL);
+    store_state(st, &J->out, u);
+}
+
+/* Chunked scan: each chunk's own summary is built from zero by the token
+ * recurrence (no outputs), the running prefix is the left fold of the
+ * preceding summaries with the segment-concatenation rule, and the chunk's
+ * outputs are produced by continuing the recurrence from that prefix.  Equal
+ * to run_serial up to rounding whenever the concatenation rule is exact. */
+static void run_chunked(job_t *J, stream_t *st, int u)
+{
+    const int n = J->n, d = J->d, dv = J->dv, c = J->chunk;
+    const size_t qo = (size_t)u * n * d, vo = (size_t)u * n * dv;
+    stream_t loc = stream_new(d, dv);
+    loc.g = st->g;
+    /* prefix state lives in st */
+    load_state(st, &J->in, u);
+    for (int t0 = 0; t0 < n; t0 += c) {
+        const int len = (n - t0 < c) ? (n - t0) : c;
+        /* local summary of this chunk, from zero */
+        load_state(&loc, NULL, 0);
+        for (int t = t0; t < t0 + len; ++t)
+            step_token(&loc, J->q + qo + (size_t)t * d, J->k + qo + (size_t)t * d,
+                       J->v + vo + (size_t)t * dv, 0, 0.0, NULL);
+        /* outputs of this chunk: continue from the prefix in a copy */
+        stream_t run = stream_new(d, dv);
+        run.g = st->g;
+        memcpy(run.S, st->S, sizeof(double) * d * d);
+        memcpy(run.C, st->C, sizeof(double) * d * dv);
+        memcpy(run.m, st->m, sizeof(double) * d);
+        memcpy(run.G, st->G, sizeof(double) * d * dv);
+        memcpy(run.h, st->h, sizeof(double) * d);
+        for (int t = t0; t < t0 + len; ++t)
+            step_token(&run, J->q + qo + (size_t)t * d, J->k + qo + (size_t)t * d,
+                       J->v + vo + (size_t)t * dv, J->normalize, J->eps,
+                       J->o ? J->o + vo + (size_t)t * dv : NULL);
+        stream_free(&run);
+        /* prefix <- prefix (+) local */
+        combine_one(d, dv, pow(st->g, (double)len),
+                    st->S, st->C, st->m, st->G, st->h,
+                    loc.S, loc.C, loc.m, loc.G, loc.h,
+                    st->S, st->C, st->m, st->G, st->h);
+    }
+    store_state(st, &J->out, u);
+    stream_free(&loc);
+}
+
+/* one decode step for pair u (seq*H + head): state in place, one token */
+static void run_decode(job_t *J, stream_t *st, int u)
+{
+    const int d = J->d, dv = J->dv;
+    load_state(st, &J->in, u);
+    step_token(st, J->q + (size_t)u * d, J->k + (size_t)u * d, J->v + (size_t)u * dv,
+               J->normalize, J->eps, J->o + (size_t)u * dv);
+    store_state(st, &J->out, u);
+}
+
+static void *worker(void *arg)
+{
+    job_t *J = (job_t *)arg;
+    stream_t st = stream_new(J->d, J->dv);
+    const int total = J->B * J->H;
+    for (;;) {
+        int u = take_unit(J, total);
+        if (u < 0) break;
+        st.g = J->gamma ? J->gamma[u % J->H] : 1.0;
+        if (J->mode == 0) run_serial(J, &st, u);
+        else if (J->mode == 1) run_chunked(J, &st, u);
+        else run_decode(J, &st, u);
+    }
+    stream_free(&st);
+    return NULL;
+}
+
+static int run_job(job_t *J, int nthreads)
+{
+    const int total = J->B * J->H;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > total) nthreads = total > 0 ? total : 1;
+    J->next = 0;
+    pthread_mutex_init(&J->lock, NULL);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * nthreads);
+    int started = 0;
+    for (int i = 1; i < nthreads; ++i)
+        if (pthread_create(&th[started], NULL, worker, J) == 0) ++started;
+    worker(J);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&J->lock);
+    return 0;
+}
+
+static int check_dims(int B, int H, int n, int d, int dv)
+{
+    return (B < 0 || H < 1 || n < 0 || d < 1 || dv < 1) ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* exported entry points (ctypes)                                            */
+
+/* Serial recurrence over n tokens for every (b,h).  gamma: [H] or NULL (no
+ * decay).  state_in / state_out: pointers may be NULL (zeros / skip). */
+int hla_oracle_forward(int B, int H, int n, int d, int dv,
+                       const double *q, const double *k, const double *v,
+                       const double *gamma, int normalize, double eps,
+                       double *Si, double *Ci, double *mi, double *Gi, double *hi,
+                       double *o,
+                       double *So, double *Co, double *mo, double *Go, double *ho,
+                       int nthreads)
+{
+    if (check_dims(B, H, n, d, dv)) return -1;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.B = B; J.H = H; J.n = n; J.d = d; J.dv = dv; J.chunk = 0;
+    J.q = q; J.k = k; J.v = v; J.gamma = gamma;
+    J.normalize = normalize; J.eps = eps;
+    J.in = (ostate){Si, Ci, mi, Gi, hi};
+    J.out = (ostate){So, Co, mo, Go, ho};
+    J.o = o;
+    J.mode = 0;
+    return run_job(&J, nthreads);
+}
+
+/* Chunked-scan forward (chunk >= 1): see run_chunked. */
+int hla_oracle_forward_chunked(int B, int H, int n, int d, int dv, int chunk,
+                               const double *q, const double *k, const double *v,
+                               const double *gamma, int normalize, double eps,
+                               double *Si, double *Ci, double *mi, double *Gi, double *hi,
+                               double *o,
+                               double *So, double *Co, double *mo, double *Go, double *ho,
+                               int nthreads)
+{
+    if (check_dims(B, H, n, d, dv) || chunk < 1) return -1;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.B = B; J.H = H; J.n = n; J.d = d; J.dv = dv; J.chunk = chunk;
+    J.q = q; J.k = k; J.v = v; J.gamma = gamma;
+    J.normalize = normalize; J.eps = eps;
+    J.in = (ostate){Si, Ci, mi, Gi, hi};
+    J.out = (ostate){So, Co, mo, Go, ho};
+    J.o = o;
+    J.mode = 1;
+    return run_job(&J, nthreads);
+}
+
+/* One decode step for N independent (sequence, head) pairs, pair u using
+ * gamma[u % H].  The state arrays are read and written in place.
+ * q, k: [N][d]; v, o: [N][dv]. */
+int hla_oracle_decode_step(int N, int H, int d, int dv,
+                           const double *gamma, int normalize, double eps,
+                           double *S, double *C, double *m, double *G, double *h,
+                           const double *q, const double *k, const double *v,
+                           double *o, int nthreads)
+{
+    if (check_dims(1, H, 1, d, dv) || N < 0) return -1;
+    if (N % H) return -1;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.B = N / H; J.H = H; J.n = 1; J.d = d; J.dv = dv;
+    J.q = q; J.k = k; J.v = v; J.gamma = gamma;
+    J.normalize = normalize; J.eps = eps;
+    J.in = (ostate){S, C, m, G, h};
+    J.out = (ostate){S, C, m, G, h};
+    J.o = o;
+    J.mode = 2;
+    return run_job(&J, nthreads);
+}
+
+/* Segment concatenation for `count` independent items: out_i = A_i (+) B_i
+ * with f_i = decay_pow[i] (NULL: f = 1).  out may alias A or B. */
+int hla_oracle_combine(int count, int d, int dv,
+                       const double *SA, const double *CA, const double *mA,
+                       const double *GA, const double *hA,
+                       const double *SB, const double *CB, const double *mB,
+                       const double *GB, const double *hB,
+                       const double *decay_pow,
+                       double *S, double *C, double *m, double *G, double *h)
+{
+    if (count < 0 || d < 1 || dv < 1) return -1;
+    for (int i = 0; i < count; ++i) {
+        const size_t a = (size_t)i * d * d, b = (size_t)i * d * dv, c = (size_t)i * d;
+        combine_one(d, dv, decay_pow ? decay_pow[i] : 1.0,
+                    SA + a, CA + b, mA + c, GA + b, hA + c,
+                    SB + a, CB + b, mB + c, GB + b, hB + c,
+                    S + a, C + b, m + c, G + b, h + c);
+    }
+    return 0;
+}

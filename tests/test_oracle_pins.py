@@ -1,0 +1,309 @@
+"""Pins for the fp64 oracle against what the pages and mathematics fix.
+
+Source of the definitions: gist.science technical summary of "Higher-order Linear
+Attention", section 1 (prefix summaries S^K, C^QV, m^Q; cross summaries G, h;
+masked output; ratio normalisation), section 4 (segment concatenation with cross
+term S_B C_A; exclusive scan equals the serial recurrence), "Resultaten en claims"
+(exactness, strict causality).
+
+Every check here compares the oracle with something computed another way: a
+brute-force sum over index triples, the dense masked-matrix form, integer
+fixtures derived by hand, closed forms, or a structural property.
+"""
+import glob
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rand_inputs(rng, B, H, n, d, dv, positive=False):
+    q = rng.standard_normal((B, H, n, d))
+    k = rng.standard_normal((B, H, n, d))
+    v = rng.standard_normal((B, H, n, dv))
+    if positive:
+        q, k = np.abs(q) + 0.1, np.abs(k) + 0.1
+    return q, k, v
+
+
+def brute_force(q, k, v, g=1.0, normalize=False, eps=0.0):
+    """o_t = sum_{a<=b<=t} g^{(t-a)+(t-b)} (q_t.k_a)(k_a.q_b) v_b, straight triple loop."""
+    n, dv = q.shape[0], v.shape[1]
+    o = np.zeros((n, dv))
+    for t in range(n):
+        num = np.zeros(dv)
+        den = 0.0
+        for b in range(t + 1):
+            for a in range(b + 1):
+                w = (g ** ((t - a) + (t - b))) * (q[t] @ k[a]) * (k[a] @ q[b])
+                num += w * v[b]
+                den += w
+        o[t] = num / (den + eps) if normalize else num
+    return o
+
+
+def brute_state(q, k, v, g=1.0):
+    """The five summaries after the last token, each from its own definition."""
+    n, d = q.shape
+    dv = v.shape[1]
+    T = n - 1
+    S = sum(g ** (T - a) * np.outer(k[a], k[a]) for a in range(n))
+    C = sum(g ** (T - b) * np.outer(q[b], v[b]) for b in range(n))
+    m = sum(g ** (T - b) * q[b] for b in range(n))
+    G = np.zeros((d, dv))
+    h = np.zeros(d)
+    for a in range(n):
+        for b in range(a):  # strictly earlier query/value index: the "future" pairs
+            w = g ** ((T - a) + (T - b)) * (k[a] @ q[b])
+            G += w * np.outer(k[a], v[b])
+            h += w * k[a]
+    return S, C, m, G, h
+
+
+def rel(a, b):
+    return np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300)
+
+
+# --------------------------------------------------------------------------- T1
+@pytest.mark.parametrize("decay", [False, True])
+@pytest.mark.parametrize("normalize", [False, True])
+@pytest.mark.parametrize("n,d,dv", [(1, 1, 1), (7, 3, 2), (19, 4, 3), (24, 2, 4)])
+def test_brute_force_outputs(decay, normalize, n, d, dv):
+    rng = np.random.default_rng(100 + n * 7 + d)
+    B, H = 2, 2
+    q, k, v = rand_inputs(rng, B, H, n, d, dv, positive=normalize)
+    gamma = np.array([0.9, 0.6]) if decay else None
+    eps = 1e-3 if normalize else 0.0
+    o, st = oracle.forward(q, k, v, gamma=gamma, normalize=normalize, eps=eps)
+    for b in range(B):
+        for h in range(H):
+            g = gamma[h] if decay else 1.0
+            ref = brute_force(q[b, h], k[b, h], v[b, h], g, normalize, eps)
+            assert rel(o[b, h], ref) < 1e-12
+            S, C, m, G, hh = brute_state(q[b, h], k[b, h], v[b, h], g)
+            u = b * H + h
+            for got, want in zip((st.S[u], st.C[u], st.m[u], st.G[u], st.h[u]), (S, C, m, G, hh)):
+                assert rel(got, want) < 1e-12
+
+
+# --------------------------------------------------------------------------- T2
+def test_dense_matrix_form():
+    """No decay: O = [L o ((L o QK^T)(L o QK^T)^T)] V with L the lower-triangular ones."""
+    rng = np.random.default_rng(7)
+    n, d, dv = 40, 5, 3
+    q, k, v = rand_inputs(rng, 1, 1, n, d, dv)
+    L = np.tril(np.ones((n, n)))
+    A = L * (q[0, 0] @ k[0, 0].T)
+    ref = (L * (A @ A.T)) @ v[0, 0]
+    o, _ = oracle.forward(q, k, v)
+    assert rel(o[0, 0], ref) < 1e-12
+    # normalised: the denominator is the row sum of the same masked weights
+    qp, kp = np.abs(q) + 0.1, np.abs(k) + 0.1
+    A = L * (qp[0, 0] @ kp[0, 0].T)
+    W = L * (A @ A.T)
+    ref = (W @ v[0, 0]) / (W.sum(axis=1, keepdims=True) + 1e-6)
+    o, _ = oracle.forward(qp, kp, v, normalize=True, eps=1e-6)
+    assert rel(o[0, 0], ref) < 1e-12
+
+
+# ---------------------------------------------------------------------- golden
+@pytest.mark.parametrize("path", sorted(glob.glob(os.path.join(GOLDEN, "*.json"))))
+def test_hand_fixtures(path):
+    fx = json.load(open(path))
+    q = np.array(fx["q"], dtype=np.float64)[None, None]
+    k = np.array(fx["k"], dtype=np.float64)[None, None]
+    v = np.array(fx["v"], dtype=np.float64)[None, None]
+    gamma = None if fx["gamma"] is None else np.array([fx["gamma"]])
+    o, _ = oracle.forward(q, k, v, gamma=gamma, normalize=fx["normalize"], eps=fx["eps"])
+    np.testing.assert_allclose(o[0, 0], np.array(fx["o"], dtype=np.float64), rtol=1e-14, atol=1e-14)
+
+
+# ------------------------------------------------------------------ closed forms
+def test_constant_inputs_closed_form():
+    """Constant q,k,v: every triple contributes (q.k)^2 v and there are t(t+1)/2 pairs."""
+    rng = np.random.default_rng(3)
+    n, d, dv = 50, 6, 4
+    q1, k1, v1 = rng.standard_normal(d), rng.standard_normal(d), rng.standard_normal(dv)
+    q = np.broadcast_to(q1, (1, 1, n, d)).copy()
+    k = np.broadcast_to(k1, (1, 1, n, d)).copy()
+    v = np.broadcast_to(v1, (1, 1, n, dv)).copy()
+    o, _ = oracle.forward(q, k, v)
+    t = np.arange(1, n + 1)[:, None]
+    ref = (q1 @ k1) ** 2 * t * (t + 1) / 2 * v1[None, :]
+    assert rel(o[0, 0], ref) < 1e-13
+
+
+def test_single_token():
+    rng = np.random.default_rng(4)
+    q, k, v = rand_inputs(rng, 3, 2, 1, 5, 3)
+    o, _ = oracle.forward(q, k, v)
+    ref = np.einsum("bhnd,bhnd->bhn", q, k)[..., None] ** 2 * v
+    assert rel(o, ref) < 1e-14
+    o, _ = oracle.forward(q, k, v, normalize=True, eps=0.5)
+    s = np.einsum("bhnd,bhnd->bhn", q, k)[..., None] ** 2
+    assert rel(o, s * v / (s + 0.5)) < 1e-14
+
+
+def test_scalar_d1_cumulative_form():
+    """d = 1: o_t = q_t * cumsum_b( cumsum_a(k_a^2)_b * q_b * v_b )_t."""
+    rng = np.random.default_rng(5)
+    n, dv = 64, 3
+    q, k, v = rand_inputs(rng, 1, 1, n, 1, dv)
+    K2 = np.cumsum(k[0, 0, :, 0] ** 2)
+    inner = np.cumsum((K2 * q[0, 0, :, 0])[:, None] * v[0, 0], axis=0)
+    ref = q[0, 0, :, 0][:, None] * inner
+    o, _ = oracle.forward(q, k, v)
+    assert rel(o[0, 0], ref) < 1e-12
+
+
+def test_decay_zero_and_one():
+    rng = np.random.default_rng(6)
+    q, k, v = rand_inputs(rng, 1, 2, 30, 4, 3)
+    # gamma = 1 is the undecayed operator
+    o1, s1 = oracle.forward(q, k, v, gamma=np.array([1.0, 1.0]))
+    o0, s0 = oracle.forward(q, k, v)
+    assert rel(o1, o0) < 1e-14 and rel(s1.G, s0.G) < 1e-14
+    # gamma = 0 keeps only a = b = t: o_t = (q_t.k_t)^2 v_t
+    oz, _ = oracle.forward(q, k, v, gamma=np.array([0.0, 0.0]))
+    ref = np.einsum("bhnd,bhnd->bhn", q, k)[..., None] ** 2 * v
+    assert rel(oz, ref) < 1e-14
+
+
+# --------------------------------------------------------------------------- T3
+@pytest.mark.parametrize("decay", [False, True])
+@pytest.mark.parametrize("normalize", [False, True])
+def test_chunked_scan_equals_serial_every_chunk(decay, normalize):
+    """Exactness claim: the chunk-parallel scan reproduces the serial activations,
+    for every chunk size including ones that do not divide n."""
+    rng = np.random.default_rng(11)
+    B, H, n, d, dv = 1, 2, 23, 3, 2
+    q, k, v = rand_inputs(rng, B, H, n, d, dv, positive=normalize)
+    gamma = np.array([0.95, 0.7]) if decay else None
+    # a non-zero incoming state, itself from a real prefix
+    qp, kp, vp = rand_inputs(rng, B, H, 9, d, dv, positive=normalize)
+    _, st0 = oracle.forward(qp, kp, vp, gamma=gamma)
+    o_ser, s_ser = oracle.forward(q, k, v, gamma=gamma, normalize=normalize, eps=1e-3, state_in=st0)
+    for c in range(1, n + 2):
+        o_c, s_c = oracle.forward(q, k, v, gamma=gamma, normalize=normalize, eps=1e-3, state_in=st0, chunk=c)
+        assert rel(o_c, o_ser) < 1e-12, c
+        for a, b in zip(s_c.astuple(), s_ser.astuple()):
+            assert rel(a, b) < 1e-12, c
+
+
+# --------------------------------------------------------------------------- T4
+def _rand_state(rng, units, d, dv):
+    return oracle.State(rng.standard_normal((units, d, d)), rng.standard_normal((units, d, dv)),
+                        rng.standard_normal((units, d)), rng.standard_normal((units, d, dv)),
+                        rng.standard_normal((units, d)))
+
+
+def test_combine_associative_identity_noncommutative():
+    rng = np.random.default_rng(12)
+    u, d, dv = 5, 4, 3
+    A, Bs, Cs = (_rand_state(rng, u, d, dv) for _ in range(3))
+    fB, fC = rng.uniform(0.2, 1.0, u), rng.uniform(0.2, 1.0, u)
+    left = oracle.combine(oracle.combine(A, Bs, fB), Cs, fC)
+    right = oracle.combine(A, oracle.combine(Bs, Cs, fC), fB * fC)
+    for a, b in zip(left.astuple(), right.astuple()):
+        assert rel(a, b) < 1e-13
+    Z = oracle.State.zeros(u, d, dv)
+    for a, b in zip(oracle.combine(A, Z).astuple(), A.astuple()):
+        assert rel(a, b) < 1e-15
+    for a, b in zip(oracle.combine(Z, A).astuple(), A.astuple()):
+        assert rel(a, b) < 1e-15
+    AB, BA = oracle.combine(A, Bs), oracle.combine(Bs, A)
+    assert rel(AB.G, BA.G) > 1e-3
+
+
+def test_combine_equals_concatenated_sequence():
+    """State of seq_A ++ seq_B equals state(A) (+) state(B) with f = gamma^len(B)."""
+    rng = np.random.default_rng(13)
+    d, dv, na, nb = 4, 3, 11, 6
+    gamma = np.array([0.8, 1.0])
+    qa, ka, va = rand_inputs(rng, 1, 2, na, d, dv)
+    qb, kb, vb = rand_inputs(rng, 1, 2, nb, d, dv)
+    _, sa = oracle.forward(qa, ka, va, gamma=gamma)
+    _, sb = oracle.forward(qb, kb, vb, gamma=gamma)
+    _, sab = oracle.forward(np.concatenate([qa, qb], 2), np.concatenate([ka, kb], 2),
+                            np.concatenate([va, vb], 2), gamma=gamma)
+    comb = oracle.combine(sa, sb, gamma ** nb)
+    for a, b in zip(comb.astuple(), sab.astuple()):
+        assert rel(a, b) < 1e-12
+
+
+# --------------------------------------------------------------------------- T5
+@pytest.mark.parametrize("normalize", [False, True])
+def test_strict_causality(normalize):
+    rng = np.random.default_rng(14)
+    n, d, dv = 30, 4, 3
+    q, k, v = rand_inputs(rng, 1, 2, n, d, dv, positive=normalize)
+    gamma = np.array([0.9, 1.0])
+    o, _ = oracle.forward(q, k, v, gamma=gamma, normalize=normalize, eps=1e-3)
+    for t in (0, 7, 20):
+        q2, k2, v2 = q.copy(), k.copy(), v.copy()
+        q2[:, :, t + 1:] += 1.0
+        k2[:, :, t + 1:] -= 2.0
+        v2[:, :, t + 1:] *= 3.0
+        o2, _ = oracle.forward(q2, k2, v2, gamma=gamma, normalize=normalize, eps=1e-3)
+        assert np.array_equal(o2[:, :, : t + 1], o[:, :, : t + 1])
+        assert not np.allclose(o2[:, :, t + 1:], o[:, :, t + 1:])
+
+
+# --------------------------------------------------------------------------- T7
+def test_unmasked_identity():
+    """q_t^T S_t C_t equals the sum over all key/value index pairs, and the masked
+    output is that minus q_t^T G_t."""
+    rng = np.random.default_rng(15)
+    n, d, dv = 12, 3, 2
+    q, k, v = rand_inputs(rng, 1, 1, n, d, dv)
+    o, _ = oracle.forward(q, k, v)
+    for t in (0, 5, 11):
+        _, st = oracle.forward(q[:, :, : t + 1], k[:, :, : t + 1], v[:, :, : t + 1])
+        qt = q[0, 0, t]
+        unmasked = qt @ st.S[0] @ st.C[0]
+        allpairs = sum((qt @ k[0, 0, a]) * (k[0, 0, a] @ q[0, 0, b]) * v[0, 0, b]
+                       for a in range(t + 1) for b in range(t + 1))
+        assert rel(unmasked, allpairs) < 1e-12
+        assert rel(unmasked - qt @ st.G[0], o[0, 0, t]) < 1e-12
+
+
+# --------------------------------------------------------------------------- T8
+def test_split_resume_and_decode_continuation():
+    rng = np.random.default_rng(16)
+    B, H, n, d, dv = 2, 2, 21, 4, 3
+    q, k, v = rand_inputs(rng, B, H, n, d, dv, positive=True)
+    gamma = np.array([0.9, 0.99])
+    for normalize in (False, True):
+        o, s = oracle.forward(q, k, v, gamma=gamma, normalize=normalize, eps=1e-3)
+        n1 = 13
+        o1, s1 = oracle.forward(q[:, :, :n1], k[:, :, :n1], v[:, :, :n1], gamma=gamma,
+                                normalize=normalize, eps=1e-3)
+        o2, s2 = oracle.forward(q[:, :, n1:], k[:, :, n1:], v[:, :, n1:], gamma=gamma,
+                                normalize=normalize, eps=1e-3, state_in=s1)
+        assert rel(np.concatenate([o1, o2], 2), o) < 1e-13
+        for a, b in zip(s2.astuple(), s.astuple()):
+            assert rel(a, b) < 1e-13
+        # decode steps from s1 reproduce the remaining outputs
+        st = s1.copy()
+        for t in range(n1, n):
+            od = oracle.decode_step(st, q[:, :, t].reshape(B * H, d), k[:, :, t].reshape(B * H, d),
+                                    v[:, :, t].reshape(B * H, dv), H, gamma=gamma,
+                                    normalize=normalize, eps=1e-3)
+            assert rel(od.reshape(B, H, dv), o[:, :, t]) < 1e-13
+        for a, b in zip(st.astuple(), s.astuple()):
+            assert rel(a, b) < 1e-13
+
+
+def test_empty_sequence_keeps_state():
+    rng = np.random.default_rng(17)
+    q, k, v = rand_inputs(rng, 1, 1, 5, 3, 2)
+    _, s = oracle.forward(q, k, v)
+    o, s2 = oracle.forward(q[:, :, :0], k[:, :, :0], v[:, :, :0], state_in=s)
+    assert o.shape == (1, 1, 0, 2)
+    for a, b in zip(s2.astuple(), s.astuple()):
+        assert np.array_equal(a, b)
