@@ -1,0 +1,542 @@
+#!/usr/bin/env python
+"""Benchmark of the masked second-order HLA forward (and the decode step) on GB300.
+
+Prints ONE JSON line (rank 0).  A step is one hla_forward_chunked call over one
+batch of the workload (all hot-path stages: chunk products, segment summaries,
+exclusive scan, outputs, final-state export), inputs resident in HBM.  Timing:
+W eager warm-up steps, then K steps replayed from CUDA graphs, bracketed by
+CUDA events on the launching stream (barrier + synchronize on both sides, max
+over ranks).  The steps cycle over enough input sets that the bytes touched
+between reuses exceed the 129 MB L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Multi-GPU: the path does not shard (every (b,h) pair is independent), so N ranks
+run N independent replicas ("replicas only"); value = tokens of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from causal_prefix_scan_gb300 import workloads as W  # noqa: E402
+
+METRIC = "masked 2nd-order HLA forward tokens/s and % roofline on 1 GB300"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+FWD_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd_tc.cu")
+DECODE_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_decode.cu")
+
+
+# ----------------------------------------------------------------- arithmetic
+def alg_flops_per_token_head(w: W.Workload) -> float:
+    """c(3d+dv) + 4d^2 + 6 d dv + 2 d^2 dv / c, triangular products at half."""
+    c, d, dv = w.chunk, w.d, w.dv
+    return c * (3 * d + dv) + 4 * d * d + 6 * d * dv + 2 * d * d * dv / c
+
+
+def alg_bytes_per_launch(w: W.Workload, with_state: bool = True) -> float:
+    s = 2 if w.dtype == "bf16" else 4
+    per_th = (2 * w.d + w.dv) * s + w.dv * s
+    state = (w.d * w.d + 2 * w.d * w.dv + 2 * w.d) * 4 if with_state else 0
+    return w.token_heads * per_th + w.B * w.H * state
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0), "fallback"
+
+
+def file_hash(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str, src: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[kernel][workload]
+        if e.get("source_sha256_16") == file_hash(src):
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", self.gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.06)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def gpu_selector(dev_index: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        if u:
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis:
+        return vis.split(",")[dev_index]
+    return str(dev_index)
+
+
+# ----------------------------------------------------------------- dist
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        return dist
+    return None
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- oracle timing
+def oracle_rate(w: W.Workload, x, batch_rows: int, n_tokens: int, nthreads: int):
+    """Time the fp64 oracle on the first `batch_rows` rows (all heads) over the first
+    `n_tokens` tokens; returns (seconds, tokens)."""
+    import oracle
+    sl = lambda a: np.ascontiguousarray(a[:batch_rows, :, :n_tokens], dtype=np.float64)
+    q, k, v = sl(x["q"]), sl(x["k"]), sl(x["v"])
+    g = None if x["gamma"] is None else np.asarray(x["gamma"], np.float64)
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, gamma=g, normalize=w.normalize, eps=w.eps, want_state=True, nthreads=nthreads)
+    return time.perf_counter() - t0, batch_rows * n_tokens
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline_forward(w: W.Workload, x):
+    """The oracle on the whole workload when that takes at most ~20 s, else on its
+    first batch rows (all heads, all tokens) sized to ~20 s."""
+    cores = cpu_threads()
+    rows = max(1, min(w.B, -(-cores // w.H)))
+    secs, toks = oracle_rate(w, x, rows, w.n, min(cores, rows * w.H))
+    if rows < w.B:
+        more = int(rows * 20.0 / max(secs, 1e-9))
+        rows = max(rows, min(w.B, more))
+        if rows > max(1, -(-cores // w.H)):
+            secs, toks = oracle_rate(w, x, rows, w.n, min(cores, rows * w.H))
+    used = min(cores, rows * w.H)
+    return {"value": toks / secs, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"fp64 serial recurrence over {rows} of {w.B} batch row(s) x {w.H} heads x {w.n} tokens "
+                      f"of the same inputs, threads over (b,h)", "seconds": secs}
+
+
+# ----------------------------------------------------------------- forward bench
+def workload_by_name(name: str):
+    if name in W.WORKLOADS:
+        return W.WORKLOADS[name]
+    if name == W.DECODE.name:
+        return W.DECODE
+    raise SystemExit(f"unknown workload {name}; choose from {list(W.WORKLOADS) + [W.DECODE.name]}")
+
+
+def config_dict(w: W.Workload, nsets: int, set_bytes: int, world: int):
+    variant = "normalised" if w.normalize else ("decay" if w.decay else "unnormalised")
+    return {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d, "dv": w.dv, "chunk": w.chunk,
+            "variant": variant, "inputs": f"q,k {w.qk}, v N(0,1), seed {w.seed}",
+            "l2": f"inputs larger than L2: {nsets} rotating input sets, {nsets * set_bytes / 2**20:.0f} MiB",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def bench_forward(args, w: W.Workload, rank, world, local, dist):
+    import torch
+    import causal_prefix_scan_gb300 as hla
+    from causal_prefix_scan_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = W.make_inputs(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    host = {k: torch.from_numpy(x[k]).to(tdt).pin_memory() for k in ("q", "k", "v")}
+    gamma = torch.from_numpy(x["gamma"]).to(dev) if x["gamma"] is not None else None
+    esz = 2 if w.dtype == "bf16" else 4
+    set_bytes = w.token_heads * (2 * w.d + 2 * w.dv) * esz  # q, k, v, o
+    nsets = max(1, min(16, -(-2 * L2_BYTES // set_bytes)))
+    sets = []
+    for _ in range(nsets):
+        q, k, v = (host[n].to(dev, non_blocking=True) for n in ("q", "k", "v"))
+        o = torch.empty(q.shape[:3] + (w.dv,), dtype=tdt, device=dev)
+        sets.append((q, k, v, o))
+    params = hla.make_params(sets[0][0], sets[0][2], w.chunk, gamma, w.normalize, w.eps)
+    ws_bytes = hla.hla_forward_workspace_size(params)
+    ws = hla.new_workspace(ws_bytes, dev)
+    st = hla.State.empty(w.B * w.H, w.d, w.dv, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, s=None):
+        q, k, v, o = sets[i % nsets]
+        hla.hla_forward_chunked(params, q, k, v, o, None, st, ws, ws_bytes, s or stream)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    hla.hla_sync_status(stream)
+
+    # graphs of R steps (+ a remainder graph) replayed to make exactly K steps
+    K = args.steps
+    R = min(K, max(nsets, 50))
+    graphs = []
+
+    def capture(nsteps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for i in range(nsteps):
+                step(i, torch.cuda.current_stream())
+        return g
+
+    g_main = capture(R)
+    reps = K // R
+    g_rem = capture(K % R) if K % R else None
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        g_main.replay()  # untimed warm replay
+    stream.synchronize()
+    hla.hla_sync_status(stream)
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_selector(local)) as clk, torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    barrier(dist)
+    hla.hla_sync_status(stream)
+    t_ms = ev0.elapsed_time(ev1)
+    t_max = max_over_ranks(dist, t_ms)
+    ms_per_step = t_max / K
+    value = world * w.tokens * K / (t_max / 1e3)
+
+    # ---- end to end: host buffers, copies inside the timed region
+    Ke = min(K, 200)
+    q, k, v, o = sets[0]
+    o_host = torch.empty(o.shape, dtype=tdt).pin_memory()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            q.copy_(host["q"], non_blocking=True); k.copy_(host["k"], non_blocking=True)
+            v.copy_(host["v"], non_blocking=True)
+            hla.hla_forward_chunked(params, q, k, v, o, None, st, ws, ws_bytes, stream)
+            o_host.copy_(o, non_blocking=True)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(Ke):
+            q.copy_(host["q"], non_blocking=True); k.copy_(host["k"], non_blocking=True)
+            v.copy_(host["v"], non_blocking=True)
+            hla.hla_forward_chunked(params, q, k, v, o, None, st, ws, ws_bytes, stream)
+            o_host.copy_(o, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    barrier(dist)
+    hla.hla_sync_status(stream)
+    te = max_over_ranks(dist, e0.elapsed_time(e1))
+    e2e = {"value": world * w.tokens * Ke / (te / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(sum(host[n].numel() * host[n].element_size() for n in ("q", "k", "v"))),
+           "d2h_bytes_per_step": int(o_host.numel() * o_host.element_size()), "steps": Ke}
+
+    # ---- roofline of the (only) kernel of the step
+    peaks, peak_kind = load_peaks()
+    bytes_launch = alg_bytes_per_launch(w)
+    flops_launch = alg_flops_per_token_head(w) * w.token_heads
+    t_launch = ms_per_step / 1e3
+    t_hbm = bytes_launch / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops_launch / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        ach, peak, unit, bound = bytes_launch / t_launch / 1e9, peaks["hbm_gbs"], "GB/s", "hbm"
+    else:
+        ach, peak, unit, bound = flops_launch / t_launch / 1e12, peaks["bf16_tflops"], "TFLOP/s", "tensor"
+    roofline = {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback",
+                "traffic": traffic_for("fwd_tc_kernel", w.name, FWD_KERNEL_SRC),
+                "kernel": "fwd_tc_kernel" if w.dtype == "bf16" else "fwd_simt_kernel",
+                "alg_bytes_per_launch": bytes_launch, "alg_flops_per_launch": flops_launch,
+                "tensor_frac": (flops_launch / t_launch / 1e12) / peaks["bf16_tflops"],
+                "roofline_time_us": max(t_hbm, t_tc) * 1e6, "launch_time_us": t_launch * 1e6}
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": config_dict(w, nsets, set_bytes, world), "roofline": roofline,
+            "e2e": e2e, "gpu_launches": K, "clocks": clk.summary(),
+            "token_heads_per_s": world * w.token_heads * K / (t_max / 1e3)}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_forward(w, x)
+    return line
+
+
+# ----------------------------------------------------------------- decode bench
+def bench_decode(args, dw: W.DecodeWorkload, rank, world, local, dist):
+    import torch
+    import causal_prefix_scan_gb300 as hla
+    from causal_prefix_scan_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    N, d, dv = dw.seqs * dw.H, dw.d, dw.dv
+    # prefill the state with the forward over a seeded prefix (drawn on the device)
+    pw = W.Workload("decode_prefix", dw.seqs, dw.H, dw.prefix, d, dv, dw.chunk, "bf16", "l2", seed=dw.seed)
+    st = hla.State.empty(N, d, dv, device=dev)
+    rows = 32
+    for b0 in range(0, dw.seqs, rows):
+        px = W.make_inputs_device(pw.with_(B=min(rows, dw.seqs - b0), seed=dw.seed * 1000 + b0), device=dev)
+        sub = hla.State(*(a[b0 * dw.H:(b0 + px["q"].shape[0]) * dw.H] for a in st.astuple()))
+        p = hla.make_params(px["q"], px["v"], dw.chunk)
+        need = hla.hla_forward_workspace_size(p)
+        ws = hla.new_workspace(need, dev)
+        o = torch.empty_like(px["v"])
+        hla.hla_forward_chunked(p, px["q"], px["k"], px["v"], o, None, sub, ws, need)
+        del px, o, ws
+    torch.cuda.synchronize()
+    hla.hla_sync_status()
+    steps = args.steps
+    T = min(steps, 64)  # distinct token sets cycled through
+    g = torch.Generator(device=dev)
+    g.manual_seed(dw.seed)
+    def draw(shape):
+        x = torch.randn(shape, generator=g, device=dev)
+        return (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    toks = [(draw((N, d)), draw((N, d)), torch.randn((N, dv), generator=g, device=dev).to(torch.bfloat16))
+            for _ in range(T)]
+    o = torch.empty((N, dv), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, s):
+        q, k, v = toks[i % T]
+        hla.hla_decode_step(N, dw.H, d, dv, hla.HLA_BF16, 0, 0.0, None, st, q, k, v, o, s)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i, stream)
+    stream.synchronize()
+    R = min(steps, 64)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream, capture_error_mode="thread_local"):
+        for i in range(R):
+            step(i, torch.cuda.current_stream())
+    g_rem = None
+    if steps % R:
+        g_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_rem, stream=stream, capture_error_mode="thread_local"):
+            for i in range(steps % R):
+                step(i, torch.cuda.current_stream())
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_selector(local)) as clk, torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(steps // R):
+            gr.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+        stream.synchronize()
+    barrier(dist)
+    hla.hla_sync_status(stream)
+    t_max = max_over_ranks(dist, ev0.elapsed_time(ev1))
+    ms = t_max / steps
+    value = world * dw.seqs * steps / (t_max / 1e3)
+    state_bytes = (d * d + 2 * d * dv + 2 * d) * 4
+    bytes_step = N * (2 * state_bytes + (2 * d + 2 * dv) * 2)
+    peaks, peak_kind = load_peaks()
+    ach = bytes_step / (ms / 1e3) / 1e9
+    # e2e: q,k,v host->device and o device->host every step
+    hq, hk, hv = (toks[0][i].cpu().pin_memory() for i in range(3))
+    ho = torch.empty((N, dv), dtype=torch.bfloat16).pin_memory()
+    q, k, v = (torch.empty_like(t) for t in toks[0])
+    Ke = min(steps, 100)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(Ke):
+            q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True); v.copy_(hv, non_blocking=True)
+            hla.hla_decode_step(N, dw.H, d, dv, hla.HLA_BF16, 0, 0.0, None, st, q, k, v, o, stream)
+            ho.copy_(o, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    te = max_over_ranks(dist, e0.elapsed_time(e1))
+    line = {"metric": "HLA decode step tokens/s and % HBM roofline on 1 GB300", "value": value,
+            "unit": "tokens/s", "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": dw.name, "seqs": dw.seqs, "H": dw.H, "d": d, "dv": dv, "prefix": dw.prefix,
+                       "l2": f"state {N * state_bytes / 2**30:.2f} GiB >> L2"},
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"], "traffic": traffic_for("decode_kernel", dw.name,
+                                                                                   DECODE_KERNEL_SRC),
+                         "kernel": "decode_kernel", "alg_bytes_per_launch": bytes_step,
+                         "peak_source": peak_kind},
+            "e2e": {"value": world * dw.seqs * Ke / (te / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": 3 * N * d * 2, "d2h_bytes_per_step": N * dv * 2, "steps": Ke},
+            "gpu_launches": steps, "clocks": clk.summary()}
+    return line
+
+
+# ----------------------------------------------------------------- reference arm
+def bench_reference(args, w, rank, world):
+    """The oracle as it stands, on the host cores: each step one bounded sample of
+    the workload (one batch row, all heads, a window of tokens)."""
+    if isinstance(w, W.DecodeWorkload):
+        return {"impl": "reference", "unavailable": "the oracle arm is defined for the forward workloads"}
+    x = W.make_inputs(w)
+    cores = min(cpu_threads(), w.H)
+    secs, _ = oracle_rate(w, x, 1, min(w.n, 128), cores)
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    n_s = int(max(16, min(w.n, 128 * budget / max(secs, 1e-9))))
+    import oracle
+    sl = lambda a, t0: np.ascontiguousarray(a[:1, :, t0:t0 + n_s], dtype=np.float64)
+    g = None if x["gamma"] is None else np.asarray(x["gamma"], np.float64)
+    offs = list(range(0, max(1, w.n - n_s + 1), max(1, n_s)))
+
+    def one(i):
+        t0 = offs[i % len(offs)]
+        oracle.forward(sl(x["q"], t0), sl(x["k"], t0), sl(x["v"], t0), gamma=g, normalize=w.normalize,
+                       eps=w.eps, nthreads=cores)
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(i)
+    dt = time.perf_counter() - t0
+    value = n_s * args.steps / dt
+    sample = f"fp64 serial recurrence on 1 batch row x {w.H} heads x {n_s}-token windows per step"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(w, 1, 0, world),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=W.FWD_BF16.name)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    w = workload_by_name(args.workload)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(bench_reference(args, w, rank, world)), flush=True)
+        return
+    dist = dist_init(world)
+    if isinstance(w, W.DecodeWorkload):
+        line = bench_decode(args, w, rank, world, local, dist)
+    else:
+        line = bench_forward(args, w, rank, world, local, dist)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

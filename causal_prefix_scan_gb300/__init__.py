@@ -1,0 +1,229 @@
+"""GB300-native masked second-order Higher-order Linear Attention (HLA).
+
+Thin ctypes binding over the C ABI in ``include/hla.h`` (library
+``_lib/libhla_gb300.so``, built for sm_103a by ``_build.build()``).  Functions named
+like the C entry points take device pointers (ints) or torch CUDA tensors and only
+marshal arguments; every step of the computation runs in the library's kernels.
+PyTorch is used for device memory and streams only.
+
+If the library has not been built, every call raises ``RuntimeError``: there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+from ._build import LIB_PATH
+
+HLA_OK, HLA_ERR_ARG, HLA_ERR_UNSUPPORTED, HLA_ERR_CUDA, HLA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+HLA_F32, HLA_BF16 = 0, 1
+HLA_NORMALIZE, HLA_DECAY = 1, 2
+
+__all__ = [
+    "HLA_OK", "HLA_ERR_ARG", "HLA_ERR_UNSUPPORTED", "HLA_ERR_CUDA", "HLA_ERR_TIMEOUT",
+    "HLA_F32", "HLA_BF16", "HLA_NORMALIZE", "HLA_DECAY",
+    "HlaError", "hla_params", "hla_state", "library", "EXPORTS",
+    "hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combine", "hla_decode_step",
+    "hla_sync_status", "hla_status_string", "hla_last_error",
+    "State", "new_workspace", "forward", "state_combine", "decode_step",
+]
+
+# Every symbol include/hla.h declares.
+EXPORTS = ("hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combine", "hla_decode_step",
+           "hla_sync_status", "hla_status_string", "hla_last_error")
+
+
+class HlaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+class hla_params(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("n", ctypes.c_int), ("d", ctypes.c_int),
+                ("dv", ctypes.c_int), ("chunk", ctypes.c_int), ("in_dtype", ctypes.c_int),
+                ("flags", ctypes.c_uint), ("eps", ctypes.c_float), ("gamma", ctypes.c_void_p)]
+
+
+class hla_state(ctypes.Structure):
+    _fields_ = [("S", ctypes.c_void_p), ("C", ctypes.c_void_p), ("m", ctypes.c_void_p),
+                ("G", ctypes.c_void_p), ("h", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def library(path: str | None = None):
+    """Load libhla_gb300.so (raises RuntimeError if it was never built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing; run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, S, vp, sz = ctypes.POINTER(hla_params), ctypes.POINTER(hla_state), ctypes.c_void_p, ctypes.c_size_t
+    i, u, f = ctypes.c_int, ctypes.c_uint, ctypes.c_float
+    lib.hla_forward_workspace_size.argtypes = [P]
+    lib.hla_forward_workspace_size.restype = sz
+    lib.hla_forward_chunked.argtypes = [P, vp, vp, vp, vp, S, S, vp, sz, vp]
+    lib.hla_state_combine.argtypes = [i, i, i, S, S, S, vp, vp]
+    lib.hla_decode_step.argtypes = [i, i, i, i, i, u, f, vp, S, vp, vp, vp, vp, vp]
+    lib.hla_sync_status.argtypes = [vp]
+    for fn in (lib.hla_forward_chunked, lib.hla_state_combine, lib.hla_decode_step, lib.hla_sync_status):
+        fn.restype = ctypes.c_int
+    lib.hla_status_string.argtypes = [ctypes.c_int]
+    lib.hla_status_string.restype = ctypes.c_char_p
+    lib.hla_last_error.argtypes = []
+    lib.hla_last_error.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int):
+    if status != HLA_OK:
+        lib = library()
+        raise HlaError(status, lib.hla_last_error().decode() or lib.hla_status_string(status).decode())
+
+
+def _state_struct(st):
+    if st is None:
+        return None
+    if isinstance(st, hla_state):
+        return ctypes.pointer(st)
+    return ctypes.pointer(hla_state(_ptr(st.S), _ptr(st.C), _ptr(st.m), _ptr(st.G), _ptr(st.h)))
+
+
+# --------------------------------------------------------------------- raw ABI
+def hla_status_string(status: int) -> str:
+    return library().hla_status_string(status).decode()
+
+
+def hla_last_error() -> str:
+    return library().hla_last_error().decode()
+
+
+def hla_forward_workspace_size(params: hla_params) -> int:
+    return library().hla_forward_workspace_size(ctypes.byref(params))
+
+
+def hla_forward_chunked(params: hla_params, q, k, v, o, state_in=None, state_out=None, workspace=None,
+                        workspace_bytes: int = 0, stream=None) -> None:
+    _check(library().hla_forward_chunked(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                         _state_struct(state_in), _state_struct(state_out), _ptr(workspace),
+                                         workspace_bytes, _stream(stream)))
+
+
+def hla_state_combine(count: int, d: int, dv: int, A, B, out, decay_pow=None, stream=None) -> None:
+    _check(library().hla_state_combine(count, d, dv, _state_struct(A), _state_struct(B), _state_struct(out),
+                                       _ptr(decay_pow), _stream(stream)))
+
+
+def hla_decode_step(N: int, H: int, d: int, dv: int, dtype: int, flags: int, eps: float, gamma, state,
+                    q, k, v, o, stream=None) -> None:
+    _check(library().hla_decode_step(N, H, d, dv, dtype, flags, eps, _ptr(gamma), _state_struct(state),
+                                     _ptr(q), _ptr(k), _ptr(v), _ptr(o), _stream(stream)))
+
+
+def hla_sync_status(stream=None) -> None:
+    _check(library().hla_sync_status(_stream(stream)))
+
+
+# ------------------------------------------------------- tensor-level helpers
+@dataclass
+class State:
+    """Five fp32 summaries of `units` pairs: S [U,d,d], C [U,d,dv], m [U,d], G [U,d,dv], h [U,d]."""
+    S: object
+    C: object
+    m: object
+    G: object
+    h: object
+
+    @staticmethod
+    def empty(units: int, d: int, dv: int, device="cuda") -> "State":
+        import torch
+        z = lambda *s: torch.empty(*s, dtype=torch.float32, device=device)
+        return State(z(units, d, d), z(units, d, dv), z(units, d), z(units, d, dv), z(units, d))
+
+    @staticmethod
+    def zeros(units: int, d: int, dv: int, device="cuda") -> "State":
+        import torch
+        z = lambda *s: torch.zeros(*s, dtype=torch.float32, device=device)
+        return State(z(units, d, d), z(units, d, dv), z(units, d), z(units, d, dv), z(units, d))
+
+    def astuple(self):
+        return (self.S, self.C, self.m, self.G, self.h)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return HLA_F32
+    if t.dtype == torch.bfloat16:
+        return HLA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def make_params(q, v, chunk: int, gamma=None, normalize: bool = False, eps: float = 0.0) -> hla_params:
+    B, H, n, d = q.shape
+    flags = (HLA_NORMALIZE if normalize else 0) | (HLA_DECAY if gamma is not None else 0)
+    return hla_params(B, H, n, d, v.shape[-1], chunk, _dtype_code(q), flags, float(eps), _ptr(gamma))
+
+
+def new_workspace(nbytes: int, device="cuda"):
+    """A zeroed device workspace of `nbytes` (the forward call keeps it zeroed between calls)."""
+    import torch
+    return torch.zeros(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def forward(q, k, v, chunk: int, gamma=None, normalize: bool = False, eps: float = 0.0, state_in=None,
+            return_state: bool = False, out=None, workspace=None, stream=None):
+    """Masked 2nd-order HLA forward.  q, k [B,H,n,d], v [B,H,n,dv] contiguous CUDA tensors
+    (bf16 or fp32); gamma [H] fp32 or None.  Returns o (and the final State)."""
+    import torch
+    p = make_params(q, v, chunk, gamma, normalize, eps)
+    o = out if out is not None else torch.empty(q.shape[:3] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    need = hla_forward_workspace_size(p)
+    if workspace is None and need:
+        workspace = new_workspace(need, q.device)
+    st = State.empty(p.B * p.H, p.d, p.dv, device=q.device) if return_state else None
+    hla_forward_chunked(p, q, k, v, o, state_in, st, workspace, need if workspace is not None else 0, stream)
+    return (o, st) if return_state else o
+
+
+def state_combine(A: State, B: State, decay_pow=None, out: State | None = None, stream=None) -> State:
+    count, d, dv = A.C.shape
+    out = out if out is not None else State.empty(count, d, dv, device=A.S.device)
+    hla_state_combine(count, d, dv, A, B, out, decay_pow, stream)
+    return out
+
+
+def decode_step(state: State, q, k, v, H: int, gamma=None, normalize: bool = False, eps: float = 0.0,
+                out=None, stream=None):
+    """One decode step for N pairs (q, k [N,d], v [N,dv]); state updated in place."""
+    import torch
+    N, d = q.shape
+    dv = v.shape[-1]
+    o = out if out is not None else torch.empty((N, dv), dtype=q.dtype, device=q.device)
+    flags = (HLA_NORMALIZE if normalize else 0) | (HLA_DECAY if gamma is not None else 0)
+    hla_decode_step(N, H, d, dv, _dtype_code(q), flags, float(eps), gamma, state, q, k, v, o, stream)
+    return o

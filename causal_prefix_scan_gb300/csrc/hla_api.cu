@@ -1,0 +1,209 @@
+// hla_api.cu -- the C ABI declared in hla.h: argument validation, workspace
+// sizing, the sticky device status word, and dispatch to the kernels.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include "hla_internal.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+// Sticky device status word (DEV_OK / DEV_TIMEOUT), one per device.
+__device__ unsigned g_dev_status = 0u;
+
+hla_status fail(hla_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+hla_status fail(hla_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+hla_status cuda_fail(cudaError_t e, const char *where) {
+    return fail(HLA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool width_ok(int x) { return x == 16 || x == 32 || x == 64 || x == 128; }
+
+// Device address of the status word for the current device.
+cudaError_t status_ptr(unsigned **p) {
+    void *a = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&a, g_dev_status);
+    *p = static_cast<unsigned *>(a);
+    return e;
+}
+
+int num_sms_current() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+    return n;
+}
+
+hla_status check_state(const hla_state *s, const char *name) {
+    if (!s) return HLA_OK;
+    if (!s->S || !s->C || !s->m || !s->G || !s->h) return fail(HLA_ERR_ARG, "%s: all five pointers must be set", name);
+    if (!aligned16(s->S) || !aligned16(s->C) || !aligned16(s->m) || !aligned16(s->G) || !aligned16(s->h))
+        return fail(HLA_ERR_ARG, "%s: pointers must be 16-byte aligned", name);
+    return HLA_OK;
+}
+
+hla_status check_params(const hla_params *p) {
+    if (!p) return fail(HLA_ERR_ARG, "params is NULL");
+    if (p->B < 1 || p->H < 1 || p->n < 0) return fail(HLA_ERR_ARG, "need B >= 1, H >= 1, n >= 0");
+    if (p->d < 1 || p->dv < 1 || p->chunk < 1) return fail(HLA_ERR_ARG, "need d, dv, chunk >= 1");
+    if (p->in_dtype != HLA_F32 && p->in_dtype != HLA_BF16) return fail(HLA_ERR_ARG, "unknown in_dtype");
+    if (p->flags & ~(unsigned)(HLA_NORMALIZE | HLA_DECAY)) return fail(HLA_ERR_ARG, "unknown flag bits");
+    if ((p->flags & HLA_DECAY) && !p->gamma) return fail(HLA_ERR_ARG, "HLA_DECAY needs gamma");
+    if ((p->flags & HLA_NORMALIZE) && !(p->eps >= 0.f)) return fail(HLA_ERR_ARG, "eps must be >= 0");
+    if ((long long)p->B * p->H * (long long)p->n * (p->d > p->dv ? p->d : p->dv) > (1LL << 40))
+        return fail(HLA_ERR_ARG, "problem too large");
+    if (!hla::fwd_tc_supported(*p) && !hla::fwd_simt_supported(*p))
+        return fail(HLA_ERR_UNSUPPORTED, "unsupported shape: dtype=%d d=%d dv=%d chunk=%d", (int)p->in_dtype, p->d,
+                    p->dv, p->chunk);
+    if (p->in_dtype == HLA_F32 && !hla::fwd_simt_supported(*p))
+        return fail(HLA_ERR_UNSUPPORTED, "fp32 inputs need d, dv, chunk in {16,32,64}");
+    return HLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *hla_status_string(hla_status s) {
+    switch (s) {
+        case HLA_OK: return "ok";
+        case HLA_ERR_ARG: return "invalid argument";
+        case HLA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case HLA_ERR_CUDA: return "CUDA error";
+        case HLA_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+const char *hla_last_error(void) { return g_msg; }
+
+size_t hla_forward_workspace_size(const hla_params *p) {
+    if (check_params(p) != HLA_OK) return 0;
+    if (hla::fwd_tc_supported(*p)) return hla::fwd_tc_workspace(*p, num_sms_current());
+    return 0;
+}
+
+hla_status hla_forward_chunked(const hla_params *p, const void *q, const void *k, const void *v, void *o,
+                               const hla_state *state_in, const hla_state *state_out, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+    hla_status s = check_params(p);
+    if (s != HLA_OK) return s;
+    if ((s = check_state(state_in, "state_in")) != HLA_OK) return s;
+    if ((s = check_state(state_out, "state_out")) != HLA_OK) return s;
+    if (state_in && state_out &&
+        (state_in->S == state_out->S || state_in->C == state_out->C || state_in->G == state_out->G))
+        return fail(HLA_ERR_ARG, "state_out may not alias state_in");
+    if (p->n > 0) {
+        if (!q || !k || !v || !o) return fail(HLA_ERR_ARG, "q, k, v, o must be set when n > 0");
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+            return fail(HLA_ERR_ARG, "q, k, v, o must be 16-byte aligned");
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool tc = hla::fwd_tc_supported(*p);
+    const int nsm = num_sms_current();
+    if (tc && p->n > 0) {
+        const size_t need = hla::fwd_tc_workspace(*p, nsm);
+        if (!workspace || workspace_bytes < need)
+            return fail(HLA_ERR_ARG, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return fail(HLA_ERR_ARG, "workspace must be 256-byte aligned");
+    }
+    if (p->n == 0) {  // no tokens: state_out = state_in (or zeros)
+        if (!state_out) return HLA_OK;
+        const size_t BH = (size_t)p->B * p->H, D = p->d, DV = p->dv;
+        const size_t sz[5] = {BH * D * D * 4, BH * D * DV * 4, BH * D * 4, BH * D * DV * 4, BH * D * 4};
+        float *dst[5] = {state_out->S, state_out->C, state_out->m, state_out->G, state_out->h};
+        for (int i = 0; i < 5; ++i) {
+            cudaError_t e;
+            if (state_in) {
+                const float *src[5] = {state_in->S, state_in->C, state_in->m, state_in->G, state_in->h};
+                e = cudaMemcpyAsync(dst[i], src[i], sz[i], cudaMemcpyDeviceToDevice, st);
+            } else {
+                e = cudaMemsetAsync(dst[i], 0, sz[i], st);
+            }
+            if (e != cudaSuccess) return cuda_fail(e, "state copy");
+        }
+        return HLA_OK;
+    }
+    hla::FwdArgs a;
+    a.B = p->B; a.H = p->H; a.n = p->n; a.d = p->d; a.dv = p->dv; a.chunk = p->chunk;
+    a.in_dtype = p->in_dtype; a.flags = p->flags; a.eps = p->eps; a.gamma = p->gamma;
+    a.q = q; a.k = k; a.v = v; a.o = o;
+    a.sin = hla::to_ptrs(state_in);
+    a.sout = hla::to_ptrs(state_out);
+    a.workspace = workspace;
+    a.ws_bytes = workspace_bytes;
+    cudaError_t e = status_ptr(&a.err);
+    if (e != cudaSuccess) return cuda_fail(e, "status word");
+    e = tc ? hla::fwd_tc_launch(a, st, nsm) : hla::fwd_simt_launch(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return HLA_OK;
+}
+
+hla_status hla_state_combine(int count, int d, int dv, const hla_state *A, const hla_state *B,
+                             const hla_state *out, const float *decay_pow, void *stream) {
+    if (count < 0) return fail(HLA_ERR_ARG, "count must be >= 0");
+    if (!width_ok(d) || !width_ok(dv)) return fail(HLA_ERR_UNSUPPORTED, "d, dv must be in {16,32,64,128}");
+    if (!A || !B || !out) return fail(HLA_ERR_ARG, "A, B, out must be set");
+    hla_status s;
+    if ((s = check_state(A, "A")) != HLA_OK || (s = check_state(B, "B")) != HLA_OK ||
+        (s = check_state(out, "out")) != HLA_OK)
+        return s;
+    hla::CombineArgs a;
+    a.count = count; a.d = d; a.dv = dv;
+    a.A = hla::to_ptrs(A); a.B = hla::to_ptrs(B); a.out = hla::to_ptrs(out);
+    a.decay_pow = decay_pow;
+    cudaError_t e = hla::combine_launch(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    return HLA_OK;
+}
+
+hla_status hla_decode_step(int N, int H, int d, int dv, hla_dtype dtype, unsigned flags, float eps,
+                           const float *gamma, const hla_state *state, const void *q, const void *k,
+                           const void *v, void *o, void *stream) {
+    if (N < 0 || H < 1 || (N % H) != 0) return fail(HLA_ERR_ARG, "need N >= 0, H >= 1, N %% H == 0");
+    if (!width_ok(d) || !width_ok(dv)) return fail(HLA_ERR_UNSUPPORTED, "d, dv must be in {16,32,64,128}");
+    if (dtype != HLA_F32 && dtype != HLA_BF16) return fail(HLA_ERR_ARG, "unknown dtype");
+    if (flags & ~(unsigned)(HLA_NORMALIZE | HLA_DECAY)) return fail(HLA_ERR_ARG, "unknown flag bits");
+    if ((flags & HLA_DECAY) && !gamma) return fail(HLA_ERR_ARG, "HLA_DECAY needs gamma");
+    if (!state) return fail(HLA_ERR_ARG, "state must be set");
+    hla_status s = check_state(state, "state");
+    if (s != HLA_OK) return s;
+    if (N > 0 && (!q || !k || !v || !o)) return fail(HLA_ERR_ARG, "q, k, v, o must be set");
+    hla::DecodeArgs a;
+    a.N = N; a.H = H; a.d = d; a.dv = dv; a.dtype = dtype; a.flags = flags; a.eps = eps; a.gamma = gamma;
+    a.st = hla::to_ptrs(state);
+    a.q = q; a.k = k; a.v = v; a.o = o;
+    cudaError_t e = hla::decode_launch(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return HLA_OK;
+}
+
+hla_status hla_sync_status(void *stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    unsigned v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_dev_status, sizeof v);
+    if (e != cudaSuccess) return cuda_fail(e, "read status word");
+    if (v != 0u) {
+        const unsigned zero = 0u;
+        e = cudaMemcpyToSymbol(g_dev_status, &zero, sizeof zero);
+        if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+        return fail(HLA_ERR_TIMEOUT, "a bounded device wait expired (status 0x%x)", v);
+    }
+    return HLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,257 @@
+// hla_fwd_simt.cu -- chunked masked second-order HLA forward on CUDA cores, fp32
+// arithmetic, for fp32 inputs and for widths d, dv <= 64 (any input dtype).
+//
+// One CTA per (b,h) pair walks the chunks in order, keeping the pair's state on
+// chip.  Instead of G and h it carries X = S C - G (d x dv) and Y = S m - h (d),
+// which obey X_t = g^2 X_{t-1} + u_t v_t^T and Y_t = g^2 Y_{t-1} + u_t with
+// u_t = S_t q_t, and give o_t = q_t^T X_t, den_t = q_t^T Y_t.  (Both identities
+// follow from the recurrence of the gist.science summary, section 1: expand
+// S_t C_t - G_t with the updates of S, C and G.)  Per chunk of L tokens with
+// local positions tau = 1..L after the prefix position p:
+//   A[t,a] = g^{t-a} q_t.k_a            (a <= t)
+//   u_b    = g^{tau_b} S_p q_b + sum_{a<=b} A[b,a] k_a        (= S_b q_b)
+//   M[t,b] = g^{2(t-b)} q_t.u_b         (b <= t)
+//   o_t    = sum_b M[t,b] v_b + g^{2 tau_t} q_t^T X_p
+//   den_t  = sum_b M[t,b]     + g^{2 tau_t} q_t^T Y_p
+// and the state moves to the chunk end with weights w_b = g^{L - tau_b}.
+#include "hla_internal.h"
+
+namespace hla {
+namespace {
+
+template <typename T>
+__device__ __forceinline__ float ld_in(const T *p, size_t i);
+template <>
+__device__ __forceinline__ float ld_in<float>(const float *p, size_t i) { return p[i]; }
+template <>
+__device__ __forceinline__ float ld_in<__nv_bfloat16>(const __nv_bfloat16 *p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+template <typename T>
+__device__ __forceinline__ void st_out(T *p, size_t i, float x);
+template <>
+__device__ __forceinline__ void st_out<float>(float *p, size_t i, float x) { p[i] = x; }
+template <>
+__device__ __forceinline__ void st_out<__nv_bfloat16>(__nv_bfloat16 *p, size_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+constexpr int kThreads = 256;
+constexpr int kMaxChunk = 64;
+
+template <typename T, int D, int DV>
+__global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
+    extern __shared__ float sm[];
+    const int c = a.chunk;
+    float *S = sm;                  // D*D
+    float *X = S + D * D;           // D*DV
+    float *Cs = X + D * DV;         // D*DV
+    float *m = Cs + D * DV;         // D
+    float *Y = m + D;               // D
+    float *Q = Y + D;               // c*D
+    float *K = Q + kMaxChunk * D;   // c*D
+    float *V = K + kMaxChunk * D;   // c*DV
+    float *U = V + kMaxChunk * DV;  // c*D
+    float *A = U + kMaxChunk * D;   // c*c (A, then M)
+    float *gp = A + kMaxChunk * kMaxChunk;  // g^x, x = 0..2c+1
+
+    const int tid = threadIdx.x;
+    const int u = blockIdx.x;  // pair index b*H + h
+    const int hh = u % a.H;
+    const bool decay = (a.flags & HLA_DECAY) != 0;
+    const bool norm = (a.flags & HLA_NORMALIZE) != 0;
+    const float g = decay ? a.gamma[hh] : 1.f;
+    const float lg = log2f(g);
+    const T *q = static_cast<const T *>(a.q) + (size_t)u * a.n * D;
+    const T *k = static_cast<const T *>(a.k) + (size_t)u * a.n * D;
+    const T *v = static_cast<const T *>(a.v) + (size_t)u * a.n * DV;
+    T *o = static_cast<T *>(a.o) + (size_t)u * a.n * DV;
+
+    for (int x = tid; x <= 2 * c + 1; x += kThreads) gp[x] = decay ? gpow(lg, (float)x) : 1.f;
+
+    // ---- prefix state
+    if (a.sin.S) {
+        const float *Si = a.sin.S + (size_t)u * D * D, *Ci = a.sin.C + (size_t)u * D * DV;
+        const float *mi = a.sin.m + (size_t)u * D, *Gi = a.sin.G + (size_t)u * D * DV, *hi = a.sin.h + (size_t)u * D;
+        for (int e = tid; e < D * D; e += kThreads) S[e] = Si[e];
+        for (int e = tid; e < D * DV; e += kThreads) Cs[e] = Ci[e];
+        for (int e = tid; e < D; e += kThreads) m[e] = mi[e];
+        __syncthreads();
+        for (int e = tid; e < D * DV; e += kThreads) {  // X = S C - G
+            const int i = e / DV, j = e % DV;
+            float acc = 0.f;
+            for (int l = 0; l < D; ++l) acc += S[i * D + l] * Cs[l * DV + j];
+            X[e] = acc - Gi[e];
+        }
+        for (int i = tid; i < D; i += kThreads) {  // Y = S m - h
+            float acc = 0.f;
+            for (int l = 0; l < D; ++l) acc += S[i * D + l] * m[l];
+            Y[i] = acc - hi[i];
+        }
+    } else {
+        for (int e = tid; e < D * D; e += kThreads) S[e] = 0.f;
+        for (int e = tid; e < D * DV; e += kThreads) X[e] = Cs[e] = 0.f;
+        for (int e = tid; e < D; e += kThreads) m[e] = Y[e] = 0.f;
+    }
+    __syncthreads();
+
+    for (int t0 = 0; t0 < a.n; t0 += c) {
+        const int L = min(c, a.n - t0);
+        for (int e = tid; e < c * D; e += kThreads) {
+            const int t = e / D;
+            Q[e] = t < L ? ld_in(q, (size_t)t0 * D + e) : 0.f;
+            K[e] = t < L ? ld_in(k, (size_t)t0 * D + e) : 0.f;
+        }
+        for (int e = tid; e < c * DV; e += kThreads) {
+            const int t = e / DV;
+            V[e] = t < L ? ld_in(v, (size_t)t0 * DV + e) : 0.f;
+        }
+        __syncthreads();
+        // A[t,a] = g^{t-a} q_t.k_a, a <= t
+        for (int e = tid; e < c * c; e += kThreads) {
+            const int t = e / c, s = e % c;
+            float acc = 0.f;
+            if (s <= t) {
+                for (int i = 0; i < D; ++i) acc += Q[t * D + i] * K[s * D + i];
+                acc *= gp[t - s];
+            }
+            A[e] = acc;
+        }
+        __syncthreads();
+        // u_b = g^{b+1} (S_p q_b) + sum_{a<=b} A[b,a] k_a   (S symmetric)
+        for (int e = tid; e < c * D; e += kThreads) {
+            const int b = e / D, i = e % D;
+            float ps = 0.f;
+            for (int j = 0; j < D; ++j) ps += S[i * D + j] * Q[b * D + j];
+            float acc = gp[b + 1] * ps;
+            for (int s = 0; s <= b; ++s) acc += A[b * c + s] * K[s * D + i];
+            U[e] = acc;
+        }
+        __syncthreads();
+        // M[t,b] = g^{2(t-b)} q_t.u_b, b <= t  (overwrites A)
+        for (int e = tid; e < c * c; e += kThreads) {
+            const int t = e / c, b = e % c;
+            float acc = 0.f;
+            if (b <= t) {
+                for (int i = 0; i < D; ++i) acc += Q[t * D + i] * U[b * D + i];
+                acc *= gp[2 * (t - b)];
+            }
+            A[e] = acc;
+        }
+        __syncthreads();
+        // outputs
+        for (int e = tid; e < L * DV; e += kThreads) {
+            const int t = e / DV, j = e % DV;
+            float num = 0.f;
+            for (int b = 0; b <= t; ++b) num += A[t * c + b] * V[b * DV + j];
+            float px = 0.f;
+            for (int i = 0; i < D; ++i) px += Q[t * D + i] * X[i * DV + j];
+            const float gt = gp[2 * (t + 1)];
+            num += gt * px;
+            if (norm) {
+                float den = 0.f;
+                for (int b = 0; b <= t; ++b) den += A[t * c + b];
+                float py = 0.f;
+                for (int i = 0; i < D; ++i) py += Q[t * D + i] * Y[i];
+                den += gt * py;
+                num = num / (den + a.eps);
+            }
+            st_out(o, (size_t)t0 * DV + e, num);
+        }
+        __syncthreads();
+        // state to the chunk end, weights w_b = g^{L-1-b}
+        const float gL = gp[L], g2L = gp[2 * L];
+        for (int e = tid; e < D * D; e += kThreads) {
+            const int i = e / D, j = e % D;
+            float acc = 0.f;
+            for (int s = 0; s < L; ++s) acc += gp[L - 1 - s] * K[s * D + i] * K[s * D + j];
+            S[e] = gL * S[e] + acc;
+        }
+        for (int e = tid; e < D * DV; e += kThreads) {
+            const int i = e / DV, j = e % DV;
+            float ax = 0.f, ac = 0.f;
+            for (int b = 0; b < L; ++b) {
+                ax += gp[2 * (L - 1 - b)] * U[b * D + i] * V[b * DV + j];
+                ac += gp[L - 1 - b] * Q[b * D + i] * V[b * DV + j];
+            }
+            X[e] = g2L * X[e] + ax;
+            Cs[e] = gL * Cs[e] + ac;
+        }
+        for (int i = tid; i < D; i += kThreads) {
+            float am = 0.f, ay = 0.f;
+            for (int b = 0; b < L; ++b) {
+                am += gp[L - 1 - b] * Q[b * D + i];
+                ay += gp[2 * (L - 1 - b)] * U[b * D + i];
+            }
+            m[i] = gL * m[i] + am;
+            Y[i] = g2L * Y[i] + ay;
+        }
+        __syncthreads();
+        // re-tabulate is unnecessary: gp depends only on g
+    }
+
+    if (a.sout.S) {
+        float *So = a.sout.S + (size_t)u * D * D, *Co = a.sout.C + (size_t)u * D * DV;
+        float *mo = a.sout.m + (size_t)u * D, *Go = a.sout.G + (size_t)u * D * DV, *ho = a.sout.h + (size_t)u * D;
+        for (int e = tid; e < D * D; e += kThreads) So[e] = S[e];
+        for (int e = tid; e < D * DV; e += kThreads) {
+            const int i = e / DV, j = e % DV;
+            float acc = 0.f;  // (S C)[i][j]
+            for (int l = 0; l < D; ++l) acc += S[i * D + l] * Cs[l * DV + j];
+            Co[e] = Cs[e];
+            Go[e] = acc - X[e];
+        }
+        for (int i = tid; i < D; i += kThreads) {
+            float acc = 0.f;
+            for (int l = 0; l < D; ++l) acc += S[i * D + l] * m[l];
+            mo[i] = m[i];
+            ho[i] = acc - Y[i];
+        }
+    }
+}
+
+template <typename T, int D, int DV>
+cudaError_t launch_t(const FwdArgs &a, cudaStream_t st) {
+    const size_t floats = (size_t)D * D + 2 * (size_t)D * DV + 2 * D + (size_t)kMaxChunk * (3 * D + DV) +
+                          (size_t)kMaxChunk * kMaxChunk + 2 * kMaxChunk + 2;
+    const size_t bytes = floats * sizeof(float);
+    auto kern = fwd_simt_kernel<T, D, DV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<a.B * a.H, kThreads, bytes, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_dv(const FwdArgs &a, cudaStream_t st) {
+    switch (a.dv) {
+        case 16: return launch_t<T, D, 16>(a, st);
+        case 32: return launch_t<T, D, 32>(a, st);
+        case 64: return launch_t<T, D, 64>(a, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename T>
+cudaError_t launch_d(const FwdArgs &a, cudaStream_t st) {
+    switch (a.d) {
+        case 16: return launch_dv<T, 16>(a, st);
+        case 32: return launch_dv<T, 32>(a, st);
+        case 64: return launch_dv<T, 64>(a, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool fwd_simt_supported(const hla_params &p) {
+    auto ok = [](int x) { return x == 16 || x == 32 || x == 64; };
+    return ok(p.d) && ok(p.dv) && ok(p.chunk) && p.chunk <= kMaxChunk;
+}
+
+cudaError_t fwd_simt_launch(const FwdArgs &a, cudaStream_t st) {
+    if (a.n == 0 && !a.sout.S) return cudaSuccess;
+    return a.in_dtype == HLA_F32 ? launch_d<float>(a, st) : launch_d<__nv_bfloat16>(a, st);
+}
+
+}  // namespace hla

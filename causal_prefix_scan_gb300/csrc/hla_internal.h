@@ -1,0 +1,65 @@
+// hla_internal.h -- argument bundles and launcher declarations shared by the
+// C-ABI layer (hla_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "hla.h"
+#include "hla_common.cuh"
+
+namespace hla {
+
+struct StatePtrs {
+    float *S = nullptr, *C = nullptr, *m = nullptr, *G = nullptr, *h = nullptr;
+};
+
+inline StatePtrs to_ptrs(const hla_state *s) {
+    StatePtrs p;
+    if (s) { p.S = s->S; p.C = s->C; p.m = s->m; p.G = s->G; p.h = s->h; }
+    return p;
+}
+
+struct FwdArgs {
+    int B, H, n, d, dv, chunk;
+    hla_dtype in_dtype;
+    unsigned flags;
+    float eps;
+    const float *gamma;
+    const void *q, *k, *v;
+    void *o;
+    StatePtrs sin, sout;
+    void *workspace;
+    size_t ws_bytes;
+    unsigned *err;  // sticky device status word
+};
+
+// CUDA-core path (fp32 arithmetic; d, dv, chunk in {16,32,64}).
+bool fwd_simt_supported(const hla_params &p);
+cudaError_t fwd_simt_launch(const FwdArgs &a, cudaStream_t st);
+
+// Tensor-core path (bf16 inputs; d, dv, chunk in {64,128}).
+bool fwd_tc_supported(const hla_params &p);
+size_t fwd_tc_workspace(const hla_params &p, int num_sms);
+cudaError_t fwd_tc_launch(const FwdArgs &a, cudaStream_t st, int num_sms);
+
+struct CombineArgs {
+    int count, d, dv;
+    StatePtrs A, B, out;
+    const float *decay_pow;
+};
+cudaError_t combine_launch(const CombineArgs &a, cudaStream_t st);
+
+struct DecodeArgs {
+    int N, H, d, dv;
+    hla_dtype dtype;
+    unsigned flags;
+    float eps;
+    const float *gamma;
+    StatePtrs st;
+    const void *q, *k, *v;
+    void *o;
+};
+cudaError_t decode_launch(const DecodeArgs &a, cudaStream_t st);
+
+}  // namespace hla

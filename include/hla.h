@@ -1,0 +1,175 @@
+/*
+ * hla.h -- C ABI of the GB300 (sm_103a) library for the masked second-order
+ * Higher-order Linear Attention (HLA) forward, its segment concatenation and
+ * its single-token decode step.
+ *
+ * Definitions (gist.science technical summary of "Higher-order Linear
+ * Attention"):
+ *   section 1, bullet "Onderhoud van de toestand": prefix summaries
+ *       S_t = sum_{i<=t} k_i k_i^T (d x d), C_t = sum_{i<=t} q_i v_i^T (d x dv),
+ *       m_t = sum_{i<=t} q_i (d);
+ *   section 1, bullet "Strenge causaliteit": cross summaries
+ *       G_t = G_{t-1} + k_t (k_t^T C_{t-1}) (d x dv), h_t = h_{t-1} + k_t (k_t^T m_{t-1}) (d);
+ *   section 1, bullet "Outputformulering": o_t = q_t^T (S_t C_t - G_t);
+ *   section 1, bullet "Normalisatie": ratio-normalised output
+ *       o_t = q_t^T (S_t C_t - G_t) / (q_t^T (S_t m_t - h_t) + eps);
+ *   section 4, bullets "Associatieve operatoren" and "Scan-equivalentie":
+ *       segments combine by a semidirect product with cross term S_B C_A, and
+ *       an exclusive scan over segment summaries reproduces the serial outputs;
+ *   "Belangrijkste bijdragen", item 2: the same operators with exponential
+ *       decay.  Decay reading used here: every prefix statistic decays by the
+ *       head's factor g per token (S_t = g S_{t-1} + k k^T, C_t = g C_{t-1} +
+ *       q v^T, m_t = g m_{t-1} + q), and G_t = g^2 G_{t-1} + g k_t (k_t^T C_{t-1}),
+ *       h_t = g^2 h_{t-1} + g k_t (k_t^T m_{t-1}); g = 1 is the undecayed case.
+ *
+ * Conventions shared by every call
+ *   - All tensors are caller-owned device memory; the library never allocates
+ *     or frees device memory.  Inputs are read-only.
+ *   - Every call is asynchronous on the given CUDA stream (`stream` is a
+ *     cudaStream_t passed as void*; NULL is the legacy default stream).  The
+ *     returned status covers argument validation and launch errors only.  A
+ *     device-side failure (a bounded wait that expired) is recorded in a sticky
+ *     device flag that hla_sync_status() reports.
+ *   - On any status other than HLA_OK nothing was launched, except HLA_ERR_CUDA
+ *     from a failed launch; hla_last_error() gives a message.
+ *   - Layout: q, k are [B][H][n][d]; v, o are [B][H][n][dv]; all contiguous,
+ *     row-major, 16-byte aligned, element type `in_dtype` (o has the input type;
+ *     accumulation is fp32, the store rounds to nearest even).
+ *   - State (one block per (b,h) pair, pair index u = b*H + h, fp32, contiguous,
+ *     16-byte aligned): S [BH][d][d], C [BH][d][dv], m [BH][d], G [BH][d][dv],
+ *     h [BH][d].
+ */
+#ifndef HLA_H
+#define HLA_H
+
+#include <stddef.h>
+
+/* Exported entry points keep default visibility in a -fvisibility=hidden build. */
+#if defined(__GNUC__)
+#define HLA_API __attribute__((visibility("default")))
+#else
+#define HLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    HLA_OK = 0,
+    HLA_ERR_ARG = 1,          /* null pointer, bad size, misalignment, short workspace */
+    HLA_ERR_UNSUPPORTED = 2,  /* valid arguments outside the supported shape set      */
+    HLA_ERR_CUDA = 3,         /* a CUDA runtime call failed                           */
+    HLA_ERR_TIMEOUT = 4       /* a bounded device-side wait expired (sticky flag)     */
+} hla_status;
+
+typedef enum { HLA_F32 = 0, HLA_BF16 = 1 } hla_dtype;
+
+enum {
+    HLA_NORMALIZE = 1u,  /* ratio-normalised output (section 1, "Normalisatie")          */
+    HLA_DECAY = 2u       /* per-head exponential decay ("Belangrijkste bijdragen", item 2) */
+};
+
+typedef struct {
+    int B, H, n;          /* batch, heads, tokens per sequence (n >= 0)               */
+    int d, dv;            /* query/key width, value width                              */
+    int chunk;            /* chunk length of the chunk-parallel scheme                 */
+    hla_dtype in_dtype;   /* element type of q, k, v, o                                */
+    unsigned flags;       /* HLA_NORMALIZE | HLA_DECAY                                 */
+    float eps;            /* added to the denominator when HLA_NORMALIZE               */
+    const float *gamma;   /* [H] device fp32 decay factors in [0,1]; required with
+                             HLA_DECAY, ignored otherwise                               */
+} hla_params;
+
+/* The five summaries of B*H (or N) pairs; all five pointers set, or the whole
+ * struct pointer passed as NULL where a call allows it. */
+typedef struct {
+    float *S, *C, *m, *G, *h;
+} hla_state;
+
+/*
+ * Supported shapes of hla_forward_chunked
+ *   in_dtype HLA_BF16, d in {64,128}, dv in {64,128}, chunk in {64,128}:
+ *       tensor-core path (tcgen05 MMA, TMEM accumulators, TMA tile loads).
+ *   in_dtype HLA_F32 or HLA_BF16 with d, dv in {16,32,64} and chunk in
+ *       {16,32,64}: CUDA-core fp32 path (fp32 inputs keep full precision).
+ *   Anything else: HLA_ERR_UNSUPPORTED.  Any n >= 0; a final partial chunk is
+ *   handled exactly (decay is applied only over the tokens present).
+ */
+
+/* Bytes of device workspace hla_forward_chunked needs for these parameters
+ * (0 if none).  Returns 0 as well for unsupported parameters; the forward call
+ * itself reports the error.  The workspace holds the per-segment summaries of
+ * the exclusive scan and the flags that order it. */
+HLA_API size_t hla_forward_workspace_size(const hla_params *p);
+
+/*
+ * Masked second-order forward over n tokens for every (b,h) pair, by the
+ * chunk-parallel scheme of section 4: per-segment summaries are combined with
+ * the semidirect-product rule in an exclusive scan, and each chunk's outputs are
+ * formed from its exact prefix state.  The result equals the serial recurrence
+ * of section 1 up to floating-point rounding.
+ *
+ *   q, k, v   inputs as described above (read only);
+ *   o         output [B][H][n][dv], in_dtype;
+ *   state_in  state before the first token, or NULL for zeros;
+ *   state_out state after the last token (S, C, m, G, h), or NULL to skip; may
+ *             not alias state_in;
+ *   workspace device scratch of at least hla_forward_workspace_size(p) bytes,
+ *             256-byte aligned, set to zero before its first use; every call
+ *             (also one that ends in HLA_ERR_TIMEOUT) leaves its header and flags
+ *             zero again, so it can be reused without clearing.  Calls sharing
+ *             one workspace must not overlap in time.
+ */
+HLA_API hla_status hla_forward_chunked(const hla_params *p, const void *q, const void *k,
+                               const void *v, void *o, const hla_state *state_in,
+                               const hla_state *state_out, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/*
+ * Segment concatenation (section 4, "Associatieve operatoren"): for each of
+ * `count` items, out = A (+) B where segment A precedes segment B in time:
+ *   S = f S_A + S_B,  C = f C_A + C_B,  m = f m_A + m_B,
+ *   G = f^2 G_A + G_B + f S_B C_A,  h = f^2 h_A + h_B + f S_B m_A,
+ * with f = decay_pow[i] (= g^{len(B)}), or f = 1 when decay_pow is NULL.
+ * A, B, out: states of `count` items with widths d, dv (any d, dv in
+ * {16,32,64,128}).  out may be A or B (all five pointers equal); partial
+ * aliasing between different arrays is not allowed.  The product S_B C_A is
+ * formed in fp32.
+ */
+HLA_API hla_status hla_state_combine(int count, int d, int dv, const hla_state *A,
+                             const hla_state *B, const hla_state *out,
+                             const float *decay_pow, void *stream);
+
+/*
+ * One decode step (section 1 recurrence applied to a single new token) for N
+ * independent (sequence, head) pairs; pair u uses gamma[u % H] when
+ * HLA_DECAY is set.  The fp32 state is updated in place: the cross summaries
+ * from C_{t-1}, m_{t-1}, then S, C, m; the output is
+ * o = q^T (S_t C_t - G_t) (divided by q^T (S_t m_t - h_t) + eps with
+ * HLA_NORMALIZE).
+ *   q, k: [N][d]; v, o: [N][dv]; element type `dtype` (HLA_F32 or HLA_BF16);
+ *   state: N pairs, read and written in place;
+ *   d, dv in {16,32,64,128}; N % H == 0.
+ */
+HLA_API hla_status hla_decode_step(int N, int H, int d, int dv, hla_dtype dtype, unsigned flags,
+                           float eps, const float *gamma, const hla_state *state,
+                           const void *q, const void *k, const void *v, void *o,
+                           void *stream);
+
+/* Synchronise `stream`, then report and clear the sticky device flag: HLA_OK,
+ * HLA_ERR_TIMEOUT if a bounded device wait expired since the last call, or
+ * HLA_ERR_CUDA if the stream reported an error. */
+HLA_API hla_status hla_sync_status(void *stream);
+
+/* Static description of a status code. */
+HLA_API const char *hla_status_string(hla_status s);
+
+/* Message describing the most recent non-OK status returned on this thread. */
+HLA_API const char *hla_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HLA_H */

@@ -1,0 +1,110 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function that
+include/hla.h declares, and rejects bad arguments with a status code before any
+CUDA work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import causal_prefix_scan_gb300 as hla
+from causal_prefix_scan_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "hla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return hla.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hla_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(hla.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_has_no_oracle_symbols(lib):
+    for name in ("hla_oracle_forward", "hla_oracle_combine"):
+        with pytest.raises(AttributeError):
+            getattr(lib, name)
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert hla.hla_status_string(s)
+
+
+def _params(**kw):
+    base = dict(B=1, H=2, n=128, d=64, dv=64, chunk=64, in_dtype=hla.HLA_BF16, flags=0, eps=0.0, gamma=None)
+    base.update(kw)
+    return hla.hla_params(**base)
+
+
+def _call(p, q=16, k=16, v=16, o=16, sin=None, sout=None, ws=None, ws_bytes=0):
+    return hla.library().hla_forward_chunked(ctypes.byref(p) if p is not None else None, q, k, v, o, sin, sout,
+                                             ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), hla.HLA_ERR_ARG),
+    (dict(H=0), hla.HLA_ERR_ARG),
+    (dict(n=-1), hla.HLA_ERR_ARG),
+    (dict(in_dtype=7), hla.HLA_ERR_ARG),
+    (dict(flags=8), hla.HLA_ERR_ARG),
+    (dict(flags=hla.HLA_DECAY), hla.HLA_ERR_ARG),          # decay without gamma
+    (dict(flags=hla.HLA_NORMALIZE, eps=-1.0), hla.HLA_ERR_ARG),
+    (dict(d=48), hla.HLA_ERR_UNSUPPORTED),
+    (dict(chunk=256), hla.HLA_ERR_UNSUPPORTED),
+    (dict(in_dtype=hla.HLA_F32, d=128, dv=128, chunk=128), hla.HLA_ERR_UNSUPPORTED),
+])
+def test_forward_rejects_bad_params(lib, kw, status):
+    assert _call(_params(**kw)) == status
+    assert hla.hla_last_error()
+
+
+def test_forward_rejects_null_and_misaligned(lib):
+    assert _call(None) == hla.HLA_ERR_ARG
+    assert _call(_params(), q=None) == hla.HLA_ERR_ARG
+    assert _call(_params(), v=8) == hla.HLA_ERR_ARG  # not 16-byte aligned
+    # tensor-core shape with no workspace
+    assert _call(_params()) == hla.HLA_ERR_ARG
+    assert "workspace" in hla.hla_last_error()
+    bad = hla.hla_state(16, 16, None, 16, 16)
+    assert _call(_params(), sout=ctypes.pointer(bad)) == hla.HLA_ERR_ARG
+
+
+def test_combine_and_decode_reject_bad_args(lib):
+    L = hla.library()
+    st = hla.hla_state(16, 16, 16, 16, 16)
+    sp = ctypes.pointer(st)
+    assert L.hla_state_combine(-1, 64, 64, sp, sp, sp, None, None) == hla.HLA_ERR_ARG
+    assert L.hla_state_combine(1, 48, 64, sp, sp, sp, None, None) == hla.HLA_ERR_UNSUPPORTED
+    assert L.hla_state_combine(1, 64, 64, None, sp, sp, None, None) == hla.HLA_ERR_ARG
+    assert L.hla_decode_step(5, 2, 64, 64, hla.HLA_BF16, 0, 0.0, None, sp, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
+    assert L.hla_decode_step(4, 2, 64, 64, hla.HLA_BF16, hla.HLA_DECAY, 0.0, None, sp, 16, 16, 16, 16,
+                             None) == hla.HLA_ERR_ARG
+    assert L.hla_decode_step(4, 2, 64, 64, 9, 0, 0.0, None, sp, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
+    assert L.hla_decode_step(4, 2, 64, 64, hla.HLA_BF16, 0, 0.0, None, None, 16, 16, 16, 16,
+                             None) == hla.HLA_ERR_ARG
+
+
+def test_workspace_size_zero_for_invalid(lib):
+    assert hla.hla_forward_workspace_size(_params(d=48)) == 0
+    assert hla.hla_forward_workspace_size(_params(in_dtype=hla.HLA_F32, d=16, dv=16, chunk=32)) == 0
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(hla, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        hla.library(str(tmp_path / "nope.so"))
