@@ -26,13 +26,13 @@ __all__ = [
     "HLA_F32", "HLA_BF16", "HLA_NORMALIZE", "HLA_DECAY",
     "HlaError", "hla_params", "hla_state", "library", "EXPORTS",
     "hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combine", "hla_decode_step",
-    "hla_sync_status", "hla_status_string", "hla_last_error",
+    "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
     "State", "new_workspace", "forward", "state_combine", "decode_step",
 ]
 
 # Every symbol include/hla.h declares.
 EXPORTS = ("hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combine", "hla_decode_step",
-           "hla_sync_status", "hla_status_string", "hla_last_error")
+           "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc")
 
 
 class HlaError(RuntimeError):
@@ -69,6 +69,8 @@ def library(path: str | None = None):
     lib.hla_forward_workspace_size.argtypes = [P]
     lib.hla_forward_workspace_size.restype = sz
     lib.hla_forward_chunked.argtypes = [P, vp, vp, vp, vp, S, S, vp, sz, vp]
+    lib.hla_forward_chunked_noalloc.argtypes = [P, vp, vp, vp, vp, S, S, vp]
+    lib.hla_forward_chunked_noalloc.restype = ctypes.c_int
     lib.hla_state_combine.argtypes = [i, i, i, S, S, S, vp, vp]
     lib.hla_decode_step.argtypes = [i, i, i, i, i, u, f, vp, S, vp, vp, vp, vp, vp]
     lib.hla_sync_status.argtypes = [vp]
@@ -131,6 +133,15 @@ def hla_forward_chunked(params: hla_params, q, k, v, o, state_in=None, state_out
     _check(library().hla_forward_chunked(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                                          _state_struct(state_in), _state_struct(state_out), _ptr(workspace),
                                          workspace_bytes, _stream(stream)))
+
+
+def hla_forward_chunked_noalloc(params: hla_params, q, k, v, o, state_in=None, state_out=None,
+                                stream=None) -> None:
+    """The forward without a caller workspace, for callers that cannot allocate
+    device memory (the scratch is a fixed array inside the library; see hla.h)."""
+    _check(library().hla_forward_chunked_noalloc(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                                 _state_struct(state_in), _state_struct(state_out),
+                                                 _stream(stream)))
 
 
 def hla_state_combine(count: int, d: int, dv: int, A, B, out, decay_pow=None, stream=None) -> None:

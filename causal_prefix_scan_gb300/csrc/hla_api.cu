@@ -74,6 +74,12 @@ hla_status check_params(const hla_params *p) {
 
 }  // namespace
 
+namespace hla {
+// Record `msg` as this thread's last error and return `s` (used by entry points
+// defined in other translation units).
+hla_status report(hla_status s, const char *msg) { return fail(s, "%s", msg); }
+}  // namespace hla
+
 extern "C" {
 
 const char *hla_status_string(hla_status s) {

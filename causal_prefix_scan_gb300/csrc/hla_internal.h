@@ -62,4 +62,7 @@ struct DecodeArgs {
 };
 cudaError_t decode_launch(const DecodeArgs &a, cudaStream_t st);
 
+// Set this thread's last-error message and return `s`.
+hla_status report(hla_status s, const char *msg);
+
 }  // namespace hla

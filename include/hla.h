@@ -168,6 +168,33 @@ HLA_API const char *hla_status_string(hla_status s);
 /* Message describing the most recent non-OK status returned on this thread. */
 HLA_API const char *hla_last_error(void);
 
+/*
+ * Forward pass for callers that cannot allocate device memory.  The paper has
+ * no counterpart to this entry point; it exists for the library's users.
+ *
+ * Some callers cannot call cudaMalloc while they run: code executing inside a
+ * host allocator hook or an allocation-free real-time loop, or a host that
+ * hands out device memory only up front.  They cannot provide the workspace
+ * that hla_forward_chunked needs.  This call computes exactly what
+ * hla_forward_chunked computes (same arguments, same kernels) but takes its
+ * scratch from one array of HLA_NOALLOC_SCRATCH_BYTES bytes that the library
+ * keeps in device memory; it allocates nothing.  Every GPU that loads the
+ * library holds that array until the process exits.
+ *
+ *   - The first call on a device looks up the array's device address while
+ *     that device is current; make that first call before any stream capture.
+ *   - Every call shares the one array.  Calls that may overlap on the GPU
+ *     (different streams, or different host threads on one device) race and
+ *     corrupt each other's results: serialise them.
+ *   - Parameters whose scratch need (hla_forward_workspace_size) exceeds
+ *     HLA_NOALLOC_SCRATCH_BYTES are rejected with HLA_ERR_UNSUPPORTED before any
+ *     device work.  Shapes served by the CUDA-core path need no scratch.
+ */
+#define HLA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+HLA_API hla_status hla_forward_chunked_noalloc(const hla_params *p, const void *q, const void *k,
+                                               const void *v, void *o, const hla_state *state_in,
+                                               const hla_state *state_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
