@@ -55,8 +55,8 @@ HLA_DEVICE bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // (and raises the sticky flag) if it never does.
 HLA_DEVICE bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err) {
     for (uint32_t i = 0; i < kWaitLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (i > 64) __nanosleep(64);
+        if (mbar_try_wait(bar, parity)) return true;  // try_wait itself suspends briefly
+        if (i > 4096) __nanosleep(64);
     }
     atomicOr(err, DEV_TIMEOUT);
     return false;

@@ -1,0 +1,1061 @@
+// hla_fwd_tc.cuh -- chunk-parallel masked second-order HLA forward on the
+// sm_103a tensor cores (tcgen05 MMA, TMEM accumulators, TMA tile loads), bf16
+// inputs, fp32 accumulation and fp32 state.  Included by one translation unit
+// per (decay, normalise) combination.
+//
+// Method (gist.science summary of "Higher-order Linear Attention", section 1 for
+// the summaries and the masked output, section 4 for the segment concatenation
+// and the exclusive scan).  Working form: instead of the cross summaries G, h
+// the kernel carries X = S C - G and Y = S m - h, for which
+//   X_t = g^2 X_{t-1} + u_t v_t^T,  Y_t = g^2 Y_{t-1} + u_t,  u_t = S_t q_t,
+//   o_t = q_t^T X_t,  den_t = q_t^T Y_t
+// (expand S_t C_t - G_t with the updates of S, C and G).  In this form the
+// concatenation of segment A before B (f = g^{len B}) reads
+//   S = f S_A + S_B, C = f C_A + C_B, m = f m_A + m_B,
+//   X = f^2 X_A + X_B + f S_A C_B,  Y = f^2 Y_A + Y_B + f S_A m_B,
+// which is the pages' rule with G = S C - X substituted.
+//
+// Per chunk of c tokens (local positions tau = 1..L after prefix position p),
+// with state (S_p, X_p, Y_p) at the chunk start:
+//   A   = tril(Gamma1 o Q K^T),   Gamma1[t,a] = g^{t-a}             (MMA + epilogue)
+//   U   = diag(g^tau) Q S_p + A K                                     (rows u_b = S_b q_b)
+//   M   = tril(Gamma2 o Q U^T),   Gamma2[t,b] = g^{2(t-b)}
+//   O   = M V + diag(g^{2 tau}) Q X_p,  den = rowsum(M) + diag(g^{2 tau}) Q Y_p
+//   S  <- g^L S + K^T W K,  X <- g^{2L} X + U^T W^2 V,  C <- g^L C + Q^T W V,
+//   with W = diag(g^{L - tau}).
+//
+// Parallel structure (one launch): the (b,h) sequence is cut into `nseg`
+// segments of whole chunks; one CTA per (b,h,segment), CTAs ordered by a ticket
+// so that a CTA only ever waits for CTAs that started before it.
+//   pass 1: the segment's own summary (S, C, X, m, Y from zero) -> workspace,
+//           then a release flag;
+//   scan:   the CTA folds state_in and the summaries of all earlier segments of
+//           its sequence (exclusive scan by the concatenation rule);
+//   pass 2: the chunk loop again from that exact prefix, writing O.
+// The last segment exports state_out (S, C, m, G = S C - X, h = S m - Y).
+//
+// Each CTA: 256 threads (8 warps).  Thread 0 issues TMA and MMAs.  TMEM
+// epilogues: warp w reads lane quadrant w % 4 and column half w / 4 of an
+// accumulator.  TMEM (512 columns): work W [0,128), S [128,256), X [256,384),
+// C (pass 1 / scan) or spare (pass 2) [384,512).  Token-row accumulators use
+// M = c rows, state accumulators M = d rows.  The next chunk's Q, K, V tiles
+// are prefetched into a second input stage when shared memory allows.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+#include "hla_internal.h"
+
+namespace hla {
+namespace tc {
+
+constexpr int kThreads = 256;
+constexpr uint32_t TW = 0, TS = 128, TX = 256, T4 = 384, kTmemCols = 512;
+
+__host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
+
+struct TcParams {
+    CUtensorMap tmQ, tmK, tmV;
+    int B, H, n, BH;
+    int nchunks, nseg, cps;
+    float eps;
+    const float *gamma;
+    void *o;
+    StatePtrs sin, sout;
+    unsigned *ticket;   // workspace header: [0] ticket counter, [1] finished CTAs
+    unsigned *flagsw;   // [BH][nseg] release flags
+    float *summ;        // [BH][nseg][SUM] segment summaries
+    float *save;        // [BH][SAVE] prefix copy for the state export
+    unsigned *err;
+};
+
+template <int C, int D, int DV>
+struct Cfg {
+    static constexpr int SUM = D * D + 2 * D * DV + 2 * D;  // S, X, C, m, Y
+    static constexpr int SAVE = D * D + D * DV + 2 * D;     // S, X, m, Y
+    // operand tiles (bytes)
+    static constexpr int SZ_Q = C * D * 2, SZ_K = C * D * 2, SZ_V = C * DV * 2;
+    static constexpr int SZ_TA = cmax(C * C, C * D) * 2;
+    static constexpr int SZ_TU = C * D * 2;
+    static constexpr int SZ_TS = cmax(cmax(D * D, C * D), C * DV) * 2;
+    static constexpr int SZ_TQ = cmax(C * D, D * DV) * 2;
+    static constexpr int SZ_IN = SZ_Q + SZ_K + SZ_V;  // one input stage
+    static constexpr int WORK = SZ_TA + SZ_TU + SZ_TS + SZ_TQ;
+    // scan / export phase operands (alias the tiles)
+    static constexpr int FOLD = 2 * D * D * 2 + 2 * D * DV * 2;
+    // fp32 vectors: m, Y [D]; a shared region R1 (scan: m_L, two partial rows [D];
+    // pass 2: row sums [2C], q.Y [C]); g^j and g^{2j} for j < 16
+    static constexpr int R1 = cmax(3 * D, 3 * C);
+    static constexpr int NVEC = 2 * D + R1 + 32;
+    static constexpr int SMALL = NVEC * 4 + 64;
+    static constexpr int LIMIT = 227 * 1024;
+    // two input stages (prefetch of the next chunk) when they fit
+    static constexpr int NSTAGE = (2 * SZ_IN + WORK + SMALL <= LIMIT) ? 2 : 1;
+    static constexpr int OFF_IN = 0;
+    static constexpr int OFF_TA = NSTAGE * SZ_IN, OFF_TU = OFF_TA + SZ_TA, OFF_TS = OFF_TU + SZ_TU,
+                         OFF_TQ = OFF_TS + SZ_TS, TILES = OFF_TQ + SZ_TQ;
+    static constexpr int ARENA = cmax(TILES, FOLD);
+    static constexpr int OFF_VEC = ARENA;
+    static constexpr int OFF_BAR = ARENA + NVEC * 4;
+    static constexpr int SMEM = OFF_BAR + 64;
+    static constexpr int SMEM_LAUNCH = cmax(SMEM, 120 * 1024);  // one CTA per SM
+    static_assert(SMEM <= LIMIT, "shared memory budget");
+    static_assert(C == 64 || C == 128, "chunk");
+    static_assert(D == 64 || D == 128, "d");
+    static_assert(DV == 64 || DV == 128, "dv");
+};
+
+// Split 16 fp32 values into bf16 hi + lo parts and store both rows.
+__device__ __forceinline__ void store_hilo(uint8_t *hi, uint8_t *lo, int rows, int r, int c0, const float (&v)[16]) {
+    float h[16], l[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        h[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+        l[i] = v[i] - h[i];
+    }
+    tile_store_row16(hi, rows, r, c0, h);
+    tile_store_row16(lo, rows, r, c0, l);
+}
+
+__device__ __forceinline__ float4 ldcg4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
+
+__device__ __forceinline__ void st_row16(float *dst, const float (&v)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 4)
+        *reinterpret_cast<float4 *>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+}
+
+// Row of an accumulator with MR rows held by (quadrant q, lane l), or -1.
+template <int MR>
+__device__ __forceinline__ int row_of(int q, int l) {
+    if constexpr (MR == 128) return 32 * q + l;
+    else return l < 16 ? 16 * q + l : -1;
+}
+
+template <int C, int D, int DV, bool DECAY, bool NORM>
+struct Kern {
+    using K_ = Cfg<C, D, DV>;
+    const TcParams &P;
+    uint8_t *base;
+    uint8_t *sTA, *sTU, *sTS, *sTQ;
+    uint8_t *sShi, *sSlo, *sChi, *sClo;
+    float *mrun, *Yrun;          // [D]
+    float *mL, *part0, *part1;   // scan phase, [D] each (alias R1)
+    float *rsum, *den;           // pass 2, [2C] and [C] (alias R1)
+    float *g16;                  // g^j, j < 16, then g^{2j}
+    uint64_t *tma_bar, *mma_bar;
+    uint32_t tb, tph, mph;
+    int tid, warp, lane, quad, half;
+    int rowC, rowD;  // rows this thread owns in token-row / state accumulators (-1: none)
+    int bh;
+    float lg;
+    bool need_mY;
+
+    __device__ Kern(const TcParams &p, uint8_t *b) : P(p), base(b) {}
+
+    __device__ uint8_t *sQ(int s) const { return base + K_::OFF_IN + s * K_::SZ_IN; }
+    __device__ uint8_t *sK(int s) const { return sQ(s) + K_::SZ_Q; }
+    __device__ uint8_t *sV(int s) const { return sK(s) + K_::SZ_K; }
+
+    // g^x for x >= 0 (1 without decay)
+    __device__ __forceinline__ float gp(int x) const {
+        if constexpr (DECAY) return gpow(lg, (float)x);
+        else return 1.f;
+    }
+    __device__ __forceinline__ uint32_t taddr(uint32_t slot, int col) const {
+        return tb + slot + ((uint32_t)(32 * quad) << 16) + (uint32_t)col;
+    }
+
+    // ---- synchronisation; false = abort (a bounded wait expired)
+    __device__ bool wait_mma() {
+        bool ok = mbar_wait(mma_bar, mph, P.err);
+        mph ^= 1u;
+        tc_fence_after();
+        return !__syncthreads_or(!ok);
+    }
+    __device__ bool wait_tma(int s) {
+        bool ok = mbar_wait(tma_bar + s, (tph >> s) & 1u, P.err);
+        tph ^= (1u << s);
+        return !__syncthreads_or(!ok);
+    }
+    // Make shared-memory and TMEM writes of all threads visible to the MMAs issued next.
+    __device__ void publish() {
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    __device__ void commit() {
+        if (tid == 0) umma_commit(mma_bar);
+    }
+
+    // ---- MMA groups (thread 0 only)
+    // token-row product, A K-major [C x KD], B K-major [N x KD]
+    __device__ void mma_kk(uint32_t slot, const uint8_t *a, const uint8_t *b, int N, int KD, bool acc) {
+        const uint32_t id = make_idesc(C, N, false, false);
+        const uint32_t sa = smem_u32(a), sb = smem_u32(b);
+#pragma unroll 4
+        for (int k = 0; k < KD; k += 16) {
+            const uint32_t ko = (uint32_t)(k & 63) * 2u;
+            umma_f16(tb + slot, make_sdesc(sa + (uint32_t)(k >> 6) * C * 128u + ko, 16u, 1024u),
+                     make_sdesc(sb + (uint32_t)(k >> 6) * N * 128u + ko, 16u, 1024u), id, (acc || k > 0) ? 1u : 0u);
+        }
+    }
+    // token-row product, A K-major [C x KD], B MN-major [KD x N]
+    __device__ void mma_km(uint32_t slot, const uint8_t *a, const uint8_t *b, int N, int KD, bool acc) {
+        const uint32_t id = make_idesc(C, N, false, true);
+        const uint32_t sa = smem_u32(a), sb = smem_u32(b);
+#pragma unroll 4
+        for (int k = 0; k < KD; k += 16)
+            umma_f16(tb + slot,
+                     make_sdesc(sa + (uint32_t)(k >> 6) * C * 128u + (uint32_t)(k & 63) * 2u, 16u, 1024u),
+                     make_sdesc(sb + (uint32_t)k * 128u, (uint32_t)KD * 128u, 1024u), id, (acc || k > 0) ? 1u : 0u);
+    }
+    // state product over tokens: A MN-major [C x D] (as D x C), B MN-major [C x N]
+    __device__ void mma_mm(uint32_t slot, const uint8_t *a, const uint8_t *b, int N, bool acc) {
+        const uint32_t id = make_idesc(D, N, true, true);
+        const uint32_t sa = smem_u32(a), sb = smem_u32(b);
+#pragma unroll 4
+        for (int k = 0; k < C; k += 16)
+            umma_f16(tb + slot, make_sdesc(sa + (uint32_t)k * 128u, (uint32_t)C * 128u, 1024u),
+                     make_sdesc(sb + (uint32_t)k * 128u, (uint32_t)C * 128u, 1024u), id, (acc || k > 0) ? 1u : 0u);
+    }
+    // state x state: A K-major [D x D] (rows = M), B MN-major [D x DV]
+    __device__ void mma_ss(uint32_t slot, const uint8_t *a, const uint8_t *b, bool acc) {
+        const uint32_t id = make_idesc(D, DV, false, true);
+        const uint32_t sa = smem_u32(a), sb = smem_u32(b);
+#pragma unroll 4
+        for (int k = 0; k < D; k += 16)
+            umma_f16(tb + slot,
+                     make_sdesc(sa + (uint32_t)(k >> 6) * D * 128u + (uint32_t)(k & 63) * 2u, 16u, 1024u),
+                     make_sdesc(sb + (uint32_t)k * 128u, (uint32_t)D * 128u, 1024u), id, (acc || k > 0) ? 1u : 0u);
+    }
+
+    __device__ void tma_chunk(int jj, int s) {
+        if (tid == 0) {
+            fence_async_smem();  // earlier generic reads of the stage precede the overwrite
+            mbar_expect_tx(tma_bar + s, K_::SZ_IN);
+            const int t0 = jj * C;
+#pragma unroll
+            for (int kb = 0; kb < D / 64; ++kb) {
+                tma_load_3d(sQ(s) + kb * C * 128, &P.tmQ, tma_bar + s, kb * 64, t0, bh);
+                tma_load_3d(sK(s) + kb * C * 128, &P.tmK, tma_bar + s, kb * 64, t0, bh);
+            }
+#pragma unroll
+            for (int kb = 0; kb < DV / 64; ++kb) tma_load_3d(sV(s) + kb * C * 128, &P.tmV, tma_bar + s, kb * 64, t0, bh);
+        }
+    }
+
+    // ---- TMEM row access: this thread's row (of quadrant `quad`) and column half
+    // `half` of an accumulator with NC columns, 32 columns per TMEM round trip.
+    // f(c0, v[16]) is called for c0 = first column of each 16-column group.
+    template <int NC, typename F>
+    __device__ __forceinline__ void for_row(uint32_t slot, F &&f) {
+        constexpr int HALF = NC / 2;
+        float a[16], b[16];
+#pragma unroll
+        for (int c0 = 0; c0 < HALF; c0 += 32) {
+            const int c = half * HALF + c0;
+            tmem_ld16(taddr(slot, c), a);
+            tmem_ld16(taddr(slot, c + 16), b);
+            tmem_wait_ld();
+            f(c, a);
+            f(c + 16, b);
+        }
+    }
+    template <int NC, typename F>
+    __device__ __forceinline__ void rmw_row(uint32_t slot, F &&f) {
+        constexpr int HALF = NC / 2;
+        float a[16], b[16];
+#pragma unroll
+        for (int c0 = 0; c0 < HALF; c0 += 32) {
+            const int c = half * HALF + c0;
+            tmem_ld16(taddr(slot, c), a);
+            tmem_ld16(taddr(slot, c + 16), b);
+            tmem_wait_ld();
+            f(c, a);
+            f(c + 16, b);
+            tmem_st16(taddr(slot, c), a);
+            tmem_st16(taddr(slot, c + 16), b);
+        }
+        tmem_wait_st();
+    }
+    // Two accumulators with the same row layout, read together.
+    template <int NC, typename F>
+    __device__ __forceinline__ void for_row2(uint32_t s1, uint32_t s2, F &&f) {
+        constexpr int HALF = NC / 2;
+        float a[16], b[16];
+#pragma unroll
+        for (int c0 = 0; c0 < HALF; c0 += 16) {
+            const int c = half * HALF + c0;
+            tmem_ld16(taddr(s1, c), a);
+            tmem_ld16(taddr(s2, c), b);
+            tmem_wait_ld();
+            f(c, a, b);
+        }
+    }
+    template <int NC>
+    __device__ void zero_slot(uint32_t slot) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < NC / 2; c0 += 16) tmem_st16(taddr(slot, half * (NC / 2) + c0), v);
+        tmem_wait_st();
+    }
+
+    // Per-half row partials: the two column halves of a row write separate arrays.
+    __device__ void put_partial(float *dst0, float *dst1, int row, float v) {
+        if (row >= 0) (half ? dst1 : dst0)[row] = v;
+    }
+
+    // Row-scaled copy of a [C x W] tile: dst[r] = scale(r) * src[r] (all threads).
+    template <int Wd, typename F>
+    __device__ void scaled_tile_copy(const uint8_t *src, uint8_t *dst, F &&scale) {
+        constexpr int GROUPS = Wd / 16;
+        for (int e = tid; e < C * GROUPS; e += kThreads) {
+            const int r = e / GROUPS, c0 = (e % GROUPS) * 16;
+            const float s = scale(r);
+            float a[8], b[8], v[16];
+            tile_load_row8(src, C, r, c0, a);
+            tile_load_row8(src, C, r, c0 + 8, b);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { v[i] = s * a[i]; v[8 + i] = s * b[i]; }
+            tile_store_row16(dst, C, r, c0, v);
+        }
+    }
+
+    // Masked, decayed row of a c x c score tile: v[i] (column c0+i of row `row`)
+    // becomes 0 above the diagonal and is scaled by g^{P (row - col)} below it
+    // (P = 1 for A-tilde, 2 for M).  Off-diagonal groups use one exp2 per group.
+    template <int POW>
+    __device__ __forceinline__ void mask_row(int row, int c0, float (&v)[16]) const {
+        if (c0 + 15 <= row) {
+            if constexpr (DECAY) {
+                const float b = gp(POW * (row - c0 - 15));
+                const float *t = g16 + (POW == 2 ? 16 : 0);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] *= b * t[15 - i];
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int dlt = row - c0 - i;
+                v[i] = dlt >= 0 ? (DECAY ? v[i] * gp(POW * dlt) : v[i]) : 0.f;
+            }
+        }
+    }
+
+    // m <- g^L m + sum_b w_b q_b and Y <- g^{2L} Y + sum_b ycol_b over the rows of
+    // two [C x D] tiles (ycol already carries its weights); all threads.
+    // Two row groups (even / odd rows) per column, combined in a fixed order so
+    // that results do not depend on thread timing.
+    __device__ void column_sums(const uint8_t *tq, const uint8_t *ty, int L) {
+        const int i = tid % D, g = tid / D;
+        float am = 0.f, ay = 0.f;
+        if (g < 2) {
+            for (int b = g; b < L; b += 2) {
+                am += gp(L - 1 - b) * tile_load(tq, C, b, i);
+                ay += tile_load(ty, C, b, i);
+            }
+        }
+        if (g == 1) { part0[i] = am; part1[i] = ay; }
+        __syncthreads();
+        if (g == 0) {
+            mrun[i] = gp(L) * mrun[i] + (am + part0[i]);
+            Yrun[i] = gp(2 * L) * Yrun[i] + (ay + part1[i]);
+        }
+        __syncthreads();
+    }
+
+    // A-tilde = tril(Gamma1 o A) from TMEM W -> sTA
+    __device__ void epi_atilde() {
+        for_row<C>(TW, [&](int c0, float (&v)[16]) {
+            if (rowC < 0) return;
+            mask_row<1>(rowC, c0, v);
+            tile_store_row16(sTA, C, rowC, c0, v);
+        });
+    }
+
+    // ======================================================================== pass 1
+    // Segment summary from zero state over chunks [jb, je): TMEM S, X, C and
+    // mrun / Yrun hold (S, X, C, m, Y) of the segment afterwards.
+    __device__ bool pass1(int jb, int je) {
+        for (int i = tid; i < D; i += kThreads) mrun[i] = Yrun[i] = 0.f;
+        int stage = 0;
+        tma_chunk(jb, 0);
+        for (int jj = jb; jj < je; ++jj) {
+            const bool first = (jj == jb);
+            const int L = min(C, P.n - jj * C);
+            if (K_::NSTAGE == 1 && !first) tma_chunk(jj, 0);
+            uint8_t *Q = sQ(stage), *Kt = sK(stage), *V = sV(stage);
+            // state at the chunk start -> bf16 operand copy of S; decay the state
+            if (!first) {
+                const float gL = gp(L), g2L = gp(2 * L);
+                rmw_row<D>(TS, [&](int c0, float (&v)[16]) {
+                    if (rowD >= 0) tile_store_row16(sTS, D, rowD, c0, v);
+                    if constexpr (DECAY) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= gL;
+                    }
+                });
+                if constexpr (DECAY) {
+                    rmw_row<DV>(TX, [&](int, float (&v)[16]) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= g2L;
+                    });
+                    rmw_row<DV>(T4, [&](int, float (&v)[16]) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= gL;
+                    });
+                }
+            }
+            if (!wait_tma(stage)) return false;
+            if (K_::NSTAGE == 2 && jj + 1 < je) tma_chunk(jj + 1, stage ^ 1);
+            if constexpr (DECAY) {
+                if (!first) scaled_tile_copy<D>(Q, sTQ, [&](int r) { return gp(r + 1); });  // diag(g^tau) Q
+            }
+            publish();
+            if (tid == 0) mma_kk(TW, Q, Kt, C, D, false);  // A = Q K^T
+            commit();
+            if (!wait_mma()) return false;
+            epi_atilde();
+            publish();
+            if (tid == 0) {
+                if (!first) mma_kk(TW, DECAY ? sTQ : Q, sTS, D, D, false);  // diag(g^tau) Q S_p
+                mma_km(TW, sTA, Kt, D, C, !first);                          // + A-tilde K
+            }
+            commit();
+            if (!wait_mma()) return false;
+            // U weighted by w^2 (the X update's left operand); K_w, V_w for decay
+            {
+                const float w2 = (DECAY && rowC >= 0) ? (rowC < L ? gp(2 * (L - 1 - rowC)) : 0.f) : 1.f;
+                for_row<D>(TW, [&](int c0, float (&v)[16]) {
+                    if (rowC < 0) return;
+                    if constexpr (DECAY) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= w2;
+                    }
+                    tile_store_row16(sTU, C, rowC, c0, v);
+                });
+            }
+            if constexpr (DECAY) {
+                auto w = [&](int r) { return r < L ? gp(L - 1 - r) : 0.f; };
+                scaled_tile_copy<D>(Kt, sTA, w);
+                scaled_tile_copy<DV>(V, sTS, w);
+            }
+            publish();
+            if (tid == 0) {
+                mma_mm(TS, Kt, DECAY ? sTA : Kt, D, !first);  // S += K^T W K
+                mma_mm(TX, sTU, V, DV, !first);               // X += (W^2 U)^T V
+                mma_mm(T4, Q, DECAY ? sTS : V, DV, !first);   // C += Q^T W V
+            }
+            commit();
+            if (need_mY) column_sums(Q, sTU, L);  // overlaps the MMAs
+            if (!wait_mma()) return false;
+            stage ^= (K_::NSTAGE - 1);
+        }
+        return true;
+    }
+
+    // Write the TMEM/SMEM summary (S, X, C, m, Y) of this CTA to `dst`.
+    __device__ void store_summary(float *dst) {
+        float *S = dst, *X = S + D * D, *Cc = X + D * DV, *m = Cc + D * DV, *Y = m + D;
+        for_row<D>(TS, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(S + rowD * D + c0, v); });
+        for_row<DV>(TX, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(X + rowD * DV + c0, v); });
+        for_row<DV>(T4, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(Cc + rowD * DV + c0, v); });
+        for (int i = tid; i < D; i += kThreads) { m[i] = mrun[i]; Y[i] = Yrun[i]; }
+    }
+
+    // ======================================================================== scan
+    __device__ bool prefix_init() {
+        if (!P.sin.S) {
+            zero_slot<D>(TS);
+            zero_slot<DV>(TX);
+            zero_slot<DV>(T4);
+            for (int i = tid; i < D; i += kThreads) mrun[i] = Yrun[i] = 0.f;
+            publish();
+            return true;
+        }
+        const float *Si = P.sin.S + (size_t)bh * D * D, *Ci = P.sin.C + (size_t)bh * D * DV;
+        const float *mi = P.sin.m + (size_t)bh * D, *Gi = P.sin.G + (size_t)bh * D * DV,
+                    *hi = P.sin.h + (size_t)bh * D;
+        for (int i = tid; i < D; i += kThreads) mrun[i] = mi[i];
+        __syncthreads();
+        float sm = 0.f;
+        rmw_row<D>(TS, [&](int c0, float (&v)[16]) {
+            if (rowD < 0) return;
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+                const float4 s = *reinterpret_cast<const float4 *>(Si + rowD * D + c0 + i);
+                v[i] = s.x; v[i + 1] = s.y; v[i + 2] = s.z; v[i + 3] = s.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sm += v[i] * mrun[c0 + i];
+            store_hilo(sShi, sSlo, D, rowD, c0, v);
+        });
+        rmw_row<DV>(T4, [&](int c0, float (&v)[16]) {
+            if (rowD < 0) return;
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+                const float4 s = *reinterpret_cast<const float4 *>(Ci + rowD * DV + c0 + i);
+                v[i] = s.x; v[i + 1] = s.y; v[i + 2] = s.z; v[i + 3] = s.w;
+            }
+            store_hilo(sChi, sClo, D, rowD, c0, v);
+        });
+        put_partial(part0, part1, rowD, sm);
+        publish();
+        if (tid == 0) {  // X = S C (three bf16 products approximate the fp32 one)
+            mma_ss(TX, sShi, sChi, false);
+            mma_ss(TX, sShi, sClo, true);
+            mma_ss(TX, sSlo, sChi, true);
+        }
+        commit();
+        for (int i = tid; i < D; i += kThreads) Yrun[i] = part0[i] + part1[i] - hi[i];
+        if (!wait_mma()) return false;
+        rmw_row<DV>(TX, [&](int c0, float (&v)[16]) {
+            if (rowD < 0) return;
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+                const float4 g = *reinterpret_cast<const float4 *>(Gi + rowD * DV + c0 + i);
+                v[i] -= g.x; v[i + 1] -= g.y; v[i + 2] -= g.z; v[i + 3] -= g.w;
+            }
+        });
+        publish();
+        return true;
+    }
+
+    // prefix <- prefix (+) L, with L a summary (S, X, C, m, Y) and f = g^{len L}.
+    __device__ bool fold(const float *Lsum, float f) {
+        const float *SL = Lsum, *XL = SL + D * D, *CL = XL + D * DV, *mLg = CL + D * DV, *YL = mLg + D;
+        const float f2 = f * f;
+        for (int i = tid; i < D; i += kThreads) mL[i] = __ldcg(mLg + i);
+        __syncthreads();
+        float sm = 0.f;
+        rmw_row<D>(TS, [&](int c0, float (&v)[16]) {
+            if (rowD < 0) return;
+            store_hilo(sShi, sSlo, D, rowD, c0, v);
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+                const float4 s = ldcg4(SL + rowD * D + c0 + i);
+                sm += v[i] * mL[c0 + i] + v[i + 1] * mL[c0 + i + 1] + v[i + 2] * mL[c0 + i + 2] +
+                      v[i + 3] * mL[c0 + i + 3];
+                v[i] = f * v[i] + s.x; v[i + 1] = f * v[i + 1] + s.y;
+                v[i + 2] = f * v[i + 2] + s.z; v[i + 3] = f * v[i + 3] + s.w;
+            }
+        });
+        rmw_row<DV>(TX, [&](int c0, float (&v)[16]) {
+            if (rowD < 0) return;
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+                const float4 s = ldcg4(XL + rowD * DV + c0 + i);
+                v[i] = f2 * v[i] + s.x; v[i + 1] = f2 * v[i + 1] + s.y;
+                v[i + 2] = f2 * v[i + 2] + s.z; v[i + 3] = f2 * v[i + 3] + s.w;
+            }
+        });
+        rmw_row<DV>(T4, [&](int c0, float (&v)[16]) {
+            if (rowD < 0) return;
+            float cl[16];
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+                const float4 s = ldcg4(CL + rowD * DV + c0 + i);
+                cl[i] = f * s.x; cl[i + 1] = f * s.y; cl[i + 2] = f * s.z; cl[i + 3] = f * s.w;
+                v[i] = f * v[i] + s.x; v[i + 1] = f * v[i + 1] + s.y;
+                v[i + 2] = f * v[i + 2] + s.z; v[i + 3] = f * v[i + 3] + s.w;
+            }
+            store_hilo(sChi, sClo, D, rowD, c0, cl);
+        });
+        put_partial(part0, part1, rowD, sm);
+        publish();
+        if (tid == 0) {  // X += S_P (f C_L)
+            mma_ss(TX, sShi, sChi, true);
+            mma_ss(TX, sShi, sClo, true);
+            mma_ss(TX, sSlo, sChi, true);
+        }
+        commit();
+        for (int i = tid; i < D; i += kThreads) {
+            Yrun[i] = f2 * Yrun[i] + __ldcg(YL + i) + f * (part0[i] + part1[i]);
+            mrun[i] = f * mrun[i] + mL[i];
+        }
+        return wait_mma();
+    }
+
+    // Spin (bounded) until segment j of this sequence has published its summary.
+    __device__ bool wait_flag(int j) {
+        bool ok = true;
+        if (tid == 0) {
+            const unsigned *f = P.flagsw + (size_t)bh * P.nseg + j;
+            ok = false;
+            for (uint32_t it = 0; it < kWaitLimit; ++it) {
+                unsigned v;
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+                if (v) { ok = true; break; }
+                if (it > 256) __nanosleep(128);
+            }
+            if (!ok) atomicOr(P.err, DEV_TIMEOUT);
+        }
+        return !__syncthreads_or(!ok);
+    }
+
+    // ======================================================================== export
+    // state_out from the prefix in TMEM (S, X, C, m, Y): G = S C - X, h = S m - Y.
+    __device__ bool export_state() {
+        float *So = P.sout.S + (size_t)bh * D * D, *Co = P.sout.C + (size_t)bh * D * DV;
+        float *mo = P.sout.m + (size_t)bh * D, *Go = P.sout.G + (size_t)bh * D * DV, *ho = P.sout.h + (size_t)bh * D;
+        float sm = 0.f;
+        for_row<D>(TS, [&](int c0, float (&v)[16]) {
+            if (rowD < 0) return;
+            store_hilo(sShi, sSlo, D, rowD, c0, v);
+            st_row16(So + rowD * D + c0, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sm += v[i] * mrun[c0 + i];
+        });
+        for_row<DV>(T4, [&](int c0, float (&v)[16]) {
+            if (rowD < 0) return;
+            store_hilo(sChi, sClo, D, rowD, c0, v);
+            st_row16(Co + rowD * DV + c0, v);
+        });
+        put_partial(part0, part1, rowD, sm);
+        publish();
+        if (tid == 0) {  // W = S C
+            mma_ss(TW, sShi, sChi, false);
+            mma_ss(TW, sShi, sClo, true);
+            mma_ss(TW, sSlo, sChi, true);
+        }
+        commit();
+        for (int i = tid; i < D; i += kThreads) {
+            mo[i] = mrun[i];
+            ho[i] = part0[i] + part1[i] - Yrun[i];
+        }
+        if (!wait_mma()) return false;
+        for_row2<DV>(TW, TX, [&](int c0, float (&sc)[16], float (&xv)[16]) {
+            if (rowD < 0) return;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sc[i] -= xv[i];
+            st_row16(Go + rowD * DV + c0, sc);
+        });
+        return true;
+    }
+
+    // Save / restore the parts of the prefix that pass 2 needs (S, X, m, Y).
+    __device__ void save_prefix(float *sv) {
+        float *S = sv, *X = S + D * D, *m = X + D * DV, *Y = m + D;
+        for_row<D>(TS, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(S + rowD * D + c0, v); });
+        for_row<DV>(TX, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(X + rowD * DV + c0, v); });
+        for (int i = tid; i < D; i += kThreads) { m[i] = mrun[i]; Y[i] = Yrun[i]; }
+    }
+    __device__ void restore_prefix(const float *sv) {
+        const float *S = sv, *X = S + D * D, *m = X + D * DV, *Y = m + D;
+        __syncthreads();
+        rmw_row<D>(TS, [&](int c0, float (&v)[16]) {
+            if (rowD >= 0)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = S[rowD * D + c0 + i];
+        });
+        rmw_row<DV>(TX, [&](int c0, float (&v)[16]) {
+            if (rowD >= 0)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = X[rowD * DV + c0 + i];
+        });
+        for (int i = tid; i < D; i += kThreads) { mrun[i] = m[i]; Yrun[i] = Y[i]; }
+    }
+
+    // ======================================================================== pass 2
+    __device__ bool pass2(int jb, int je) {
+        __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(P.o) + (size_t)bh * P.n * DV;
+        int stage = 0;
+        tma_chunk(jb, 0);
+        for (int jj = jb; jj < je; ++jj) {
+            const int t0 = jj * C;
+            const int L = min(C, P.n - t0);
+            if (K_::NSTAGE == 1 && jj != jb) tma_chunk(jj, 0);
+            uint8_t *Q = sQ(stage), *Kt = sK(stage), *V = sV(stage);
+            // state at the chunk start -> bf16 operands; then decay it to the chunk end
+            {
+                const float gL = gp(L), g2L = gp(2 * L);
+                rmw_row<D>(TS, [&](int c0, float (&v)[16]) {
+                    if (rowD >= 0) tile_store_row16(sTS, D, rowD, c0, v);
+                    if constexpr (DECAY) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= gL;
+                    }
+                });
+                rmw_row<DV>(TX, [&](int c0, float (&v)[16]) {
+                    if (rowD >= 0) tile_store_row16(sTQ, D, rowD, c0, v);
+                    if constexpr (DECAY) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= g2L;
+                    }
+                });
+            }
+            if (!wait_tma(stage)) return false;
+            if (K_::NSTAGE == 2 && jj + 1 < je) tma_chunk(jj + 1, stage ^ 1);
+            if constexpr (NORM) {  // q_t . Y_p, before Y moves on (one thread per row)
+                if (tid < C) {
+                    float acc = 0.f;
+                    for (int i = 0; i < D; ++i) acc += tile_load(Q, C, tid, i) * Yrun[i];
+                    den[tid] = acc;
+                }
+            }
+            publish();
+            if (tid == 0) mma_kk(TW, Q, Kt, C, D, false);  // A = Q K^T
+            commit();
+            if (!wait_mma()) return false;
+            epi_atilde();
+            publish();
+            if (tid == 0) {
+                if constexpr (DECAY) {
+                    mma_kk(T4, Q, sTS, D, D, false);   // spare = Q S_p
+                    mma_km(TW, sTA, Kt, D, C, false);  // W = A-tilde K
+                } else {
+                    mma_kk(TW, Q, sTS, D, D, false);
+                    mma_km(TW, sTA, Kt, D, C, true);
+                }
+            }
+            commit();
+            if (!wait_mma()) return false;
+            // U = g^tau Q S_p + A-tilde K -> sTU; W^2 U -> sTS (decay)
+            if constexpr (DECAY) {
+                const float gt = rowC >= 0 ? gp(rowC + 1) : 0.f;
+                const float w2 = (rowC >= 0 && rowC < L) ? gp(2 * (L - 1 - rowC)) : 0.f;
+                for_row2<D>(TW, T4, [&](int c0, float (&v)[16], float (&sp)[16]) {
+                    if (rowC < 0) return;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] += gt * sp[i];
+                    tile_store_row16(sTU, C, rowC, c0, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] *= w2;
+                    tile_store_row16(sTS, C, rowC, c0, v);
+                });
+                scaled_tile_copy<D>(Kt, sTA, [&](int r) { return r < L ? gp(L - 1 - r) : 0.f; });
+            } else {
+                for_row<D>(TW, [&](int c0, float (&v)[16]) {
+                    if (rowC >= 0) tile_store_row16(sTU, C, rowC, c0, v);
+                });
+            }
+            publish();
+            if (tid == 0) {
+                mma_kk(TW, Q, sTU, C, D, false);                        // M = Q U^T
+                mma_mm(TX, DECAY ? sTS : sTU, V, DV, true);             // X += (W^2 U)^T V
+                mma_mm(TS, Kt, DECAY ? sTA : Kt, D, true);              // S += K^T W K
+                if constexpr (DECAY) mma_km(T4, Q, sTQ, DV, D, false);  // spare = Q X_p
+            }
+            commit();
+            float ay = 0.f;        // Y <- g^{2L} Y + sum_b w_b^2 u_b (weights on the tile),
+            float *ysc = rsum;     // two row groups; rsum is free until the M epilogue
+            if constexpr (NORM) {
+                const int i = tid % D, g = tid / D;
+                const uint8_t *ty = DECAY ? sTS : sTU;
+                if (g < 2)
+                    for (int b = g; b < L; b += 2) ay += tile_load(ty, C, b, i);
+                if (g == 1) ysc[i] = ay;
+            }
+            if (!wait_mma()) return false;
+            if constexpr (NORM) {
+                if (tid < D) Yrun[tid] = gp(2 * L) * Yrun[tid] + (ay + ysc[tid]);
+                __syncthreads();  // rsum is rewritten by the M epilogue
+            }
+            // M = tril(Gamma2 o Q U^T) -> sTA, row sums for the denominator
+            float rs = 0.f;
+            for_row<C>(TW, [&](int c0, float (&v)[16]) {
+                if (rowC < 0) return;
+                mask_row<2>(rowC, c0, v);
+                if constexpr (NORM) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) rs += v[i];
+                }
+                tile_store_row16(sTA, C, rowC, c0, v);
+            });
+            if constexpr (NORM) put_partial(rsum, rsum + C, rowC, rs);
+            publish();
+            if (tid == 0) {
+                mma_km(TW, sTA, V, DV, C, false);                      // O = M V
+                if constexpr (!DECAY) mma_km(TW, Q, sTQ, DV, D, true);  // + Q X_p
+            }
+            commit();
+            if (!wait_mma()) return false;
+            {
+                const float g2t = (DECAY && rowC >= 0) ? gp(2 * (rowC + 1)) : 1.f;
+                float inv = 1.f;
+                if constexpr (NORM) {
+                    if (rowC >= 0) inv = 1.f / (rsum[rowC] + rsum[C + rowC] + g2t * den[rowC] + P.eps);
+                }
+                auto out = [&](int c0, float (&v)[16]) {
+                    if (rowC < 0 || rowC >= L) return;
+                    if constexpr (NORM) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= inv;
+                    }
+                    uint4 a, b;
+                    a.x = pack_bf16(v[0], v[1]); a.y = pack_bf16(v[2], v[3]);
+                    a.z = pack_bf16(v[4], v[5]); a.w = pack_bf16(v[6], v[7]);
+                    b.x = pack_bf16(v[8], v[9]); b.y = pack_bf16(v[10], v[11]);
+                    b.z = pack_bf16(v[12], v[13]); b.w = pack_bf16(v[14], v[15]);
+                    uint4 *dst = reinterpret_cast<uint4 *>(O + (size_t)(t0 + rowC) * DV + c0);
+                    dst[0] = a;
+                    dst[1] = b;
+                };
+                if constexpr (DECAY) {
+                    for_row2<DV>(TW, T4, [&](int c0, float (&v)[16], float (&sp)[16]) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] += g2t * sp[i];
+                        out(c0, v);
+                    });
+                } else {
+                    for_row<DV>(TW, out);
+                }
+            }
+            __syncthreads();
+            stage ^= (K_::NSTAGE - 1);
+        }
+        return true;
+    }
+};
+
+// The last CTA to finish returns the workspace header and flags to zero, so the
+// next call needs no separate clearing launch.  Every CTA counts itself done
+// only after its last read of a flag.  Called by one thread per CTA.
+__device__ __forceinline__ void finish_cta(const TcParams &P) {
+    __threadfence();
+    const unsigned done = atomicAdd(P.ticket + 1, 1u);
+    if (done == gridDim.x - 1) {
+        for (int i = 0; i < P.BH * P.nseg; ++i) P.flagsw[i] = 0u;
+        P.ticket[0] = 0u;
+        P.ticket[1] = 0u;
+        __threadfence();
+    }
+}
+
+template <int C, int D, int DV, bool DECAY, bool NORM>
+__global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ TcParams P) {
+    using K_ = Cfg<C, D, DV>;
+    // No static shared memory: the dynamic block starts at the (1024-byte
+    // aligned) base of the CTA's shared window, which the swizzled tiles need.
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *base = smem_raw;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + K_::OFF_BAR);
+    uint32_t *tmem_base_p = reinterpret_cast<uint32_t *>(base + K_::OFF_BAR + 24);
+    int *ticket_p = reinterpret_cast<int *>(base + K_::OFF_BAR + 28);
+    int *misalign_p = reinterpret_cast<int *>(base + K_::OFF_BAR + 32);
+
+    Kern<C, D, DV, DECAY, NORM> x(P, base);
+    x.tid = threadIdx.x;
+    x.warp = threadIdx.x >> 5;
+    x.lane = threadIdx.x & 31;
+    x.quad = x.warp & 3;
+    x.half = x.warp >> 2;
+    x.rowC = row_of<C>(x.quad, x.lane);
+    x.rowD = row_of<D>(x.quad, x.lane);
+    x.sTA = base + K_::OFF_TA; x.sTU = base + K_::OFF_TU; x.sTS = base + K_::OFF_TS; x.sTQ = base + K_::OFF_TQ;
+    x.sShi = base; x.sSlo = base + D * D * 2; x.sChi = base + 2 * D * D * 2; x.sClo = x.sChi + D * DV * 2;
+    float *vec = reinterpret_cast<float *>(base + K_::OFF_VEC);
+    x.mrun = vec; x.Yrun = vec + D;
+    float *r1 = vec + 2 * D;
+    x.mL = r1; x.part0 = r1 + D; x.part1 = r1 + 2 * D;
+    x.rsum = r1; x.den = r1 + 2 * C;
+    x.g16 = r1 + K_::R1;
+    x.tma_bar = &bars[0];  // [0], [1]: input stages
+    x.mma_bar = &bars[2];
+    x.tph = x.mph = 0;
+
+    if (x.tid == 0) {
+        *misalign_p = (smem_u32(base) & 1023u) != 0;
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_init(&bars[2], 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&P.tmQ);
+        tma_prefetch_desc(&P.tmK);
+        tma_prefetch_desc(&P.tmV);
+        *ticket_p = (int)atomicAdd(P.ticket, 1u);
+    }
+    __syncthreads();
+    if (*misalign_p) {  // cannot happen with no static shared memory; refuse rather than corrupt
+        if (x.tid == 0) {
+            atomicOr(P.err, DEV_TIMEOUT);
+            finish_cta(P);
+        }
+        return;
+    }
+    if (x.warp == 0) {
+        tmem_alloc(tmem_base_p, kTmemCols);
+        tmem_relinquish();
+    }
+    const int ticket = *ticket_p;
+    const int seg = ticket / P.BH;
+    x.bh = ticket % P.BH;
+    const int h = x.bh % P.H;
+    float g = 1.f;
+    if constexpr (DECAY) g = P.gamma[h];
+    x.lg = log2f(g);
+    if (x.tid < 32) x.g16[x.tid] = DECAY ? gpow(x.lg, (float)((x.tid & 15) * (x.tid < 16 ? 1 : 2))) : 1.f;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    x.tb = *tmem_base_p;
+
+    const int jb = seg * P.cps;
+    const int je = min(P.nchunks, jb + P.cps);
+    const bool last = (seg == P.nseg - 1);
+    const bool want_out = P.sout.S != nullptr;
+    x.need_mY = NORM || want_out;
+    auto seg_len = [&](int s) {  // tokens in segment s
+        const int b0 = s * P.cps * C;
+        return min(P.n, (s + 1) * P.cps * C) - b0;
+    };
+    auto seg_pow = [&](int s) { return DECAY ? gpow(x.lg, (float)seg_len(s)) : 1.f; };
+    bool ok = true;
+    do {
+        // ---- pass 1: own summary (needed by later segments, and by the export)
+        if (!last || want_out) {
+            if (!(ok = x.pass1(jb, je))) break;
+            x.store_summary(P.summ + ((size_t)x.bh * P.nseg + seg) * K_::SUM);
+            __threadfence();
+            __syncthreads();
+            if (!last && x.tid == 0) {
+                unsigned *f = P.flagsw + (size_t)x.bh * P.nseg + seg;
+                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
+            }
+        }
+        // ---- exclusive scan: prefix = state_in (+) L_0 (+) ... (+) L_{seg-1}
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (!(ok = x.prefix_init())) break;
+        for (int j = 0; j < seg; ++j) {
+            if (!(ok = x.wait_flag(j))) break;
+            if (!(ok = x.fold(P.summ + ((size_t)x.bh * P.nseg + j) * K_::SUM, seg_pow(j)))) break;
+        }
+        if (!ok) break;
+        // ---- state export from prefix (+) own summary
+        if (last && want_out) {
+            float *sv = P.save + (size_t)x.bh * K_::SAVE;
+            x.save_prefix(sv);
+            __threadfence_block();
+            if (!(ok = x.fold(P.summ + ((size_t)x.bh * P.nseg + seg) * K_::SUM, seg_pow(seg)))) break;
+            if (!(ok = x.export_state())) break;
+            x.restore_prefix(sv);
+            x.publish();
+        }
+        // ---- pass 2: outputs from the exact prefix
+        if (!(ok = x.pass2(jb, je))) break;
+    } while (0);
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (x.warp == 0) tmem_dealloc(x.tb, kTmemCols);
+    if (x.tid == 0) finish_cta(P);
+}
+
+// ============================================================================ host side
+inline PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+inline bool encode_3d(CUtensorMap *tm, const void *ptr, int width, int n, int BH, int box_rows) {
+    auto enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t gdim[3] = {(cuuint64_t)width, (cuuint64_t)n, (cuuint64_t)BH};
+    cuuint64_t gstr[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * (cuuint64_t)n};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), gdim, gstr, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Plan {
+    int nchunks, nseg, cps;
+};
+inline Plan make_plan(const hla_params &p, int num_sms) {
+    Plan pl;
+    const int BH = p.B * p.H;
+    pl.nchunks = (p.n + p.chunk - 1) / p.chunk;
+    int nseg = num_sms / (BH > 0 ? BH : 1);
+    nseg = nseg < 1 ? 1 : nseg;
+    if (nseg > pl.nchunks) nseg = pl.nchunks > 0 ? pl.nchunks : 1;
+    pl.cps = (pl.nchunks + nseg - 1) / nseg;
+    if (pl.cps < 1) pl.cps = 1;
+    pl.nseg = (pl.nchunks + pl.cps - 1) / pl.cps;
+    if (pl.nseg < 1) pl.nseg = 1;
+    return pl;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+    size_t off_flags, off_summ, off_save, total;
+};
+inline WsLayout ws_layout(const hla_params &p, const Plan &pl) {
+    const size_t BH = (size_t)p.B * p.H;
+    const size_t D = p.d, DV = p.dv;
+    const size_t SUM = D * D + 2 * D * DV + 2 * D, SAVE = D * D + D * DV + 2 * D;
+    WsLayout w;
+    w.off_flags = 256;
+    w.off_summ = align256(w.off_flags + BH * pl.nseg * 4);
+    w.off_save = align256(w.off_summ + BH * pl.nseg * SUM * 4);
+    w.total = align256(w.off_save + BH * SAVE * 4);
+    return w;
+}
+
+template <int C, int D, int DV, bool DECAY, bool NORM>
+cudaError_t launch_cfg(const FwdArgs &a, cudaStream_t st, int num_sms) {
+    using K_ = Cfg<C, D, DV>;
+    hla_params p{a.B, a.H, a.n, a.d, a.dv, a.chunk, a.in_dtype, a.flags, a.eps, a.gamma};
+    const Plan pl = make_plan(p, num_sms);
+    const WsLayout wl = ws_layout(p, pl);
+    TcParams P;
+    memset(&P, 0, sizeof P);
+    const int BH = a.B * a.H;
+    if (!encode_3d(&P.tmQ, a.q, D, a.n, BH, C) || !encode_3d(&P.tmK, a.k, D, a.n, BH, C) ||
+        !encode_3d(&P.tmV, a.v, DV, a.n, BH, C))
+        return cudaErrorInvalidValue;
+    P.B = a.B; P.H = a.H; P.n = a.n; P.BH = BH;
+    P.nchunks = pl.nchunks; P.nseg = pl.nseg; P.cps = pl.cps;
+    P.eps = a.eps; P.gamma = a.gamma;
+    P.o = a.o; P.sin = a.sin; P.sout = a.sout;
+    uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+    P.ticket = reinterpret_cast<unsigned *>(ws);
+    P.flagsw = reinterpret_cast<unsigned *>(ws + wl.off_flags);
+    P.summ = reinterpret_cast<float *>(ws + wl.off_summ);
+    P.save = reinterpret_cast<float *>(ws + wl.off_save);
+    P.err = a.err;
+    auto kern = fwd_tc_kernel<C, D, DV, DECAY, NORM>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K_::SMEM_LAUNCH);
+    if (e != cudaSuccess) return e;
+    kern<<<BH * pl.nseg, kThreads, K_::SMEM_LAUNCH, st>>>(P);
+    return cudaGetLastError();
+}
+
+// Launcher for one (decay, normalise) combination over all supported shapes;
+// explicitly instantiated in hla_fwd_tc_f<flags>.cu.
+template <bool DECAY, bool NORM>
+cudaError_t launch_flags(const FwdArgs &a, cudaStream_t st, int ns) {
+    const int key = (a.chunk == 128 ? 4 : 0) | (a.d == 128 ? 2 : 0) | (a.dv == 128 ? 1 : 0);
+    switch (key) {
+        case 0: return launch_cfg<64, 64, 64, DECAY, NORM>(a, st, ns);
+        case 1: return launch_cfg<64, 64, 128, DECAY, NORM>(a, st, ns);
+        case 2: return launch_cfg<64, 128, 64, DECAY, NORM>(a, st, ns);
+        case 3: return launch_cfg<64, 128, 128, DECAY, NORM>(a, st, ns);
+        case 4: return launch_cfg<128, 64, 64, DECAY, NORM>(a, st, ns);
+        case 5: return launch_cfg<128, 64, 128, DECAY, NORM>(a, st, ns);
+        case 6: return launch_cfg<128, 128, 64, DECAY, NORM>(a, st, ns);
+        default: return launch_cfg<128, 128, 128, DECAY, NORM>(a, st, ns);
+    }
+}
+
+}  // namespace tc
+}  // namespace hla
