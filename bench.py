@@ -36,7 +36,7 @@ from causal_prefix_scan_gb300 import workloads as W  # noqa: E402
 METRIC = "masked 2nd-order HLA forward tokens/s and % roofline on 1 GB300"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
-FWD_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd_tc.cu")
+FWD_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd_tc.cuh")
 DECODE_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_decode.cu")
 
 
