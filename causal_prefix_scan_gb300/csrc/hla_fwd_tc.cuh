@@ -53,9 +53,17 @@ namespace hla {
 namespace tc {
 
 constexpr int kThreads = 256;
-constexpr uint32_t TW = 0, TS = 128, TX = 256, T4 = 384, kTmemCols = 512;
 
 __host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
+__host__ __device__ constexpr int pow2ceil(int x) { return x <= 32 ? 32 : (x <= 64 ? 64 : (x <= 128 ? 128 : (x <= 256 ? 256 : 512))); }
+
+// TMEM columns: work W (max(c, d, dv)), S (d), X (dv), fourth slot: C in pass 1
+// and the scan (dv), spare in pass 2 (d or dv).  Shapes that fit in 256 columns
+// run two CTAs per SM.
+__host__ __device__ constexpr int tmem_cols(int C, int D, int DV) {
+    return pow2ceil(cmax(cmax(C, D), DV) + D + DV + cmax(D, DV));
+}
+inline int ctas_per_sm(const hla_params &p) { return tmem_cols(p.chunk, p.d, p.dv) <= 256 ? 2 : 1; }
 
 struct TcParams {
     CUtensorMap tmQ, tmK, tmV;
@@ -86,9 +94,15 @@ struct Cfg {
     static constexpr int WORK = SZ_TA + SZ_TU + SZ_TS + SZ_TQ;
     // scan / export phase operands (alias the tiles)
     static constexpr int FOLD = 2 * D * D * 2 + 2 * D * DV * 2;
-    // fp32 vectors: m, Y [D]; a shared region R1 (scan: m_L, two partial rows [D];
-    // pass 2: row sums [2C], q.Y [C]); g^j and g^{2j} for j < 16
-    static constexpr int R1 = cmax(3 * D, 3 * C);
+    // TMEM slots
+    static constexpr uint32_t TW = 0, TS = cmax(cmax(C, D), DV), TX = TS + D, T4 = TX + DV;
+    static constexpr int TCOLS = tmem_cols(C, D, DV);
+    static constexpr int CTAS = TCOLS <= 256 ? 2 : 1;
+    // row partial sums: one slot per column part of an accumulator row
+    static constexpr int NP_C = C == 128 ? 2 : 4, NP_D = D == 128 ? 2 : 4;
+    // fp32 vectors: m, Y [D]; a shared region R1 (scan: m_L [D] + row partials
+    // [NP_D x D]; pass 2: row sums [NP_C x C], q.Y [C]); g^j and g^{2j} for j < 16
+    static constexpr int R1 = cmax(D + NP_D * D, NP_C * C + C);
     static constexpr int NVEC = 2 * D + R1 + 32;
     static constexpr int SMALL = NVEC * 4 + 64;
     static constexpr int LIMIT = 227 * 1024;
@@ -101,7 +115,9 @@ struct Cfg {
     static constexpr int OFF_VEC = ARENA;
     static constexpr int OFF_BAR = ARENA + NVEC * 4;
     static constexpr int SMEM = OFF_BAR + 64;
-    static constexpr int SMEM_LAUNCH = cmax(SMEM, 120 * 1024);  // one CTA per SM
+    // CTAs per SM set by the shared-memory request (and TMEM / registers)
+    static constexpr int SMEM_LAUNCH = CTAS == 2 ? cmax(SMEM, 78 * 1024) : cmax(SMEM, 120 * 1024);
+    static_assert(CTAS == 1 || SMEM <= 112 * 1024, "two CTAs per SM need <= 112 KB each");
     static_assert(SMEM <= LIMIT, "shared memory budget");
     static_assert(C == 64 || C == 128, "chunk");
     static_assert(D == 64 || D == 128, "d");
@@ -132,22 +148,37 @@ __device__ __forceinline__ void st_row16(float *dst, const float (&v)[16]) {
 template <int MR>
 __device__ __forceinline__ int row_of(int q, int l) {
     if constexpr (MR == 128) return 32 * q + l;
-    else return l < 16 ? 16 * q + l : -1;
+    else return 16 * q + (l & 15);
 }
 
 template <int C, int D, int DV, bool DECAY, bool NORM>
 struct Kern {
     using K_ = Cfg<C, D, DV>;
+    static constexpr uint32_t TW = K_::TW, TS = K_::TS, TX = K_::TX, T4 = K_::T4;
     const TcParams &P;
     uint8_t *base;
-    uint8_t *sTA, *sTU, *sTS, *sTQ;
-    uint8_t *sShi, *sSlo, *sChi, *sClo;
-    float *mrun, *Yrun;          // [D]
-    float *mL, *part0, *part1;   // scan phase, [D] each (alias R1)
-    float *rsum, *den;           // pass 2, [2C] and [C] (alias R1)
-    float *g16;                  // g^j, j < 16, then g^{2j}
-    uint64_t *tma_bar, *mma_bar;
-    uint32_t tb, tph, mph;
+    // Work tiles, scan operands and small fp32 vectors, all at fixed offsets from
+    // `base` (computed on use, so they occupy no registers).
+    __device__ __forceinline__ uint8_t *tA() const { return base + K_::OFF_TA; }
+    __device__ __forceinline__ uint8_t *tU() const { return base + K_::OFF_TU; }
+    __device__ __forceinline__ uint8_t *tS() const { return base + K_::OFF_TS; }
+    __device__ __forceinline__ uint8_t *tQ() const { return base + K_::OFF_TQ; }
+    __device__ __forceinline__ uint8_t *tShi() const { return base; }
+    __device__ __forceinline__ uint8_t *tSlo() const { return base + D * D * 2; }
+    __device__ __forceinline__ uint8_t *tChi() const { return base + 2 * D * D * 2; }
+    __device__ __forceinline__ uint8_t *tClo() const { return base + 2 * D * D * 2 + D * DV * 2; }
+    __device__ __forceinline__ float *vec() const { return reinterpret_cast<float *>(base + K_::OFF_VEC); }
+    __device__ __forceinline__ float *mrun() const { return vec(); }              // [D]
+    __device__ __forceinline__ float *Yrun() const { return vec() + D; }          // [D]
+    __device__ __forceinline__ float *mL() const { return vec() + 2 * D; }        // scan: [D]
+    __device__ __forceinline__ float *part() const { return vec() + 3 * D; }      // scan: [NP_D x D]
+    __device__ __forceinline__ float *part0() const { return part(); }            // [D]
+    __device__ __forceinline__ float *part1() const { return part() + D; }        // [D]
+    __device__ __forceinline__ float *rsum() const { return vec() + 2 * D; }      // pass 2: [NP_C x C]
+    __device__ __forceinline__ float *den() const { return vec() + 2 * D + K_::NP_C * C; }  // pass 2: [C]
+    __device__ __forceinline__ float *g16() const { return vec() + 2 * D + K_::R1; }  // g^j, g^{2j}
+    uint64_t *tma_bar, *mma_bar, *mma_bar2;
+    uint32_t tb, tph, mph, mph2;
     int tid, warp, lane, quad, half;
     int rowC, rowD;  // rows this thread owns in token-row / state accumulators (-1: none)
     int bh;
@@ -176,6 +207,23 @@ struct Kern {
         tc_fence_after();
         return !__syncthreads_or(!ok);
     }
+    // Second completion barrier: MMAs committed to it run on while the block
+    // works on results committed to the first one.
+    __device__ bool wait_mma2() {
+        bool ok = mbar_wait(mma_bar2, mph2, P.err);
+        mph2 ^= 1u;
+        tc_fence_after();
+        return !__syncthreads_or(!ok);
+    }
+    __device__ void commit2() {
+        if (tid == 0) umma_commit(mma_bar2);
+    }
+    // Block barrier that also orders this thread's TMEM accesses around it.
+    __device__ void tc_sync() {
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
     __device__ bool wait_tma(int s) {
         bool ok = mbar_wait(tma_bar + s, (tph >> s) & 1u, P.err);
         tph ^= (1u << s);
@@ -192,46 +240,50 @@ struct Kern {
         if (tid == 0) umma_commit(mma_bar);
     }
 
-    // ---- MMA groups (thread 0 only)
+    // ---- MMA groups (thread 0 only).  Shapes are compile-time, the K loop is
+    // unrolled, and each step adds a constant byte offset (>> 4) to descriptors
+    // built once per group, so issuing costs a few instructions per MMA.
     // token-row product, A K-major [C x KD], B K-major [N x KD]
-    __device__ void mma_kk(uint32_t slot, const uint8_t *a, const uint8_t *b, int N, int KD, bool acc) {
-        const uint32_t id = make_idesc(C, N, false, false);
-        const uint32_t sa = smem_u32(a), sb = smem_u32(b);
-#pragma unroll 4
+    template <int N, int KD>
+    __device__ __forceinline__ void mma_kk(uint32_t slot, const uint8_t *a, const uint8_t *b, bool acc) {
+        constexpr uint32_t id = make_idesc(C, N, false, false);
+        const uint64_t da = make_sdesc(smem_u32(a), 16u, 1024u), db = make_sdesc(smem_u32(b), 16u, 1024u);
+#pragma unroll 1
         for (int k = 0; k < KD; k += 16) {
-            const uint32_t ko = (uint32_t)(k & 63) * 2u;
-            umma_f16(tb + slot, make_sdesc(sa + (uint32_t)(k >> 6) * C * 128u + ko, 16u, 1024u),
-                     make_sdesc(sb + (uint32_t)(k >> 6) * N * 128u + ko, 16u, 1024u), id, (acc || k > 0) ? 1u : 0u);
+            const uint32_t ka = ((uint32_t)(k >> 6) * C * 128u + (uint32_t)(k & 63) * 2u) >> 4;
+            const uint32_t kb = ((uint32_t)(k >> 6) * N * 128u + (uint32_t)(k & 63) * 2u) >> 4;
+            umma_f16(tb + slot, da + ka, db + kb, id, (acc || k > 0) ? 1u : 0u);
         }
     }
     // token-row product, A K-major [C x KD], B MN-major [KD x N]
-    __device__ void mma_km(uint32_t slot, const uint8_t *a, const uint8_t *b, int N, int KD, bool acc) {
-        const uint32_t id = make_idesc(C, N, false, true);
-        const uint32_t sa = smem_u32(a), sb = smem_u32(b);
-#pragma unroll 4
-        for (int k = 0; k < KD; k += 16)
-            umma_f16(tb + slot,
-                     make_sdesc(sa + (uint32_t)(k >> 6) * C * 128u + (uint32_t)(k & 63) * 2u, 16u, 1024u),
-                     make_sdesc(sb + (uint32_t)k * 128u, (uint32_t)KD * 128u, 1024u), id, (acc || k > 0) ? 1u : 0u);
+    template <int N, int KD>
+    __device__ __forceinline__ void mma_km(uint32_t slot, const uint8_t *a, const uint8_t *b, bool acc) {
+        constexpr uint32_t id = make_idesc(C, N, false, true);
+        const uint64_t da = make_sdesc(smem_u32(a), 16u, 1024u), db = make_sdesc(smem_u32(b), KD * 128u, 1024u);
+#pragma unroll 1
+        for (int k = 0; k < KD; k += 16) {
+            const uint32_t ka = ((uint32_t)(k >> 6) * C * 128u + (uint32_t)(k & 63) * 2u) >> 4;
+            umma_f16(tb + slot, da + ka, db + (uint32_t)(k * 8), id, (acc || k > 0) ? 1u : 0u);
+        }
     }
     // state product over tokens: A MN-major [C x D] (as D x C), B MN-major [C x N]
-    __device__ void mma_mm(uint32_t slot, const uint8_t *a, const uint8_t *b, int N, bool acc) {
-        const uint32_t id = make_idesc(D, N, true, true);
-        const uint32_t sa = smem_u32(a), sb = smem_u32(b);
-#pragma unroll 4
+    template <int N>
+    __device__ __forceinline__ void mma_mm(uint32_t slot, const uint8_t *a, const uint8_t *b, bool acc) {
+        constexpr uint32_t id = make_idesc(D, N, true, true);
+        const uint64_t da = make_sdesc(smem_u32(a), C * 128u, 1024u), db = make_sdesc(smem_u32(b), C * 128u, 1024u);
+#pragma unroll 1
         for (int k = 0; k < C; k += 16)
-            umma_f16(tb + slot, make_sdesc(sa + (uint32_t)k * 128u, (uint32_t)C * 128u, 1024u),
-                     make_sdesc(sb + (uint32_t)k * 128u, (uint32_t)C * 128u, 1024u), id, (acc || k > 0) ? 1u : 0u);
+            umma_f16(tb + slot, da + (uint32_t)(k * 8), db + (uint32_t)(k * 8), id, (acc || k > 0) ? 1u : 0u);
     }
     // state x state: A K-major [D x D] (rows = M), B MN-major [D x DV]
-    __device__ void mma_ss(uint32_t slot, const uint8_t *a, const uint8_t *b, bool acc) {
-        const uint32_t id = make_idesc(D, DV, false, true);
-        const uint32_t sa = smem_u32(a), sb = smem_u32(b);
-#pragma unroll 4
-        for (int k = 0; k < D; k += 16)
-            umma_f16(tb + slot,
-                     make_sdesc(sa + (uint32_t)(k >> 6) * D * 128u + (uint32_t)(k & 63) * 2u, 16u, 1024u),
-                     make_sdesc(sb + (uint32_t)k * 128u, (uint32_t)D * 128u, 1024u), id, (acc || k > 0) ? 1u : 0u);
+    __device__ __forceinline__ void mma_ss(uint32_t slot, const uint8_t *a, const uint8_t *b, bool acc) {
+        constexpr uint32_t id = make_idesc(D, DV, false, true);
+        const uint64_t da = make_sdesc(smem_u32(a), 16u, 1024u), db = make_sdesc(smem_u32(b), D * 128u, 1024u);
+#pragma unroll 1
+        for (int k = 0; k < D; k += 16) {
+            const uint32_t ka = ((uint32_t)(k >> 6) * D * 128u + (uint32_t)(k & 63) * 2u) >> 4;
+            umma_f16(tb + slot, da + ka, db + (uint32_t)(k * 8), id, (acc || k > 0) ? 1u : 0u);
+        }
     }
 
     __device__ void tma_chunk(int jj, int s) {
@@ -249,67 +301,147 @@ struct Kern {
         }
     }
 
-    // ---- TMEM row access: this thread's row (of quadrant `quad`) and column half
-    // `half` of an accumulator with NC columns, 32 columns per TMEM round trip.
-    // f(c0, v[16]) is called for c0 = first column of each 16-column group.
-    template <int NC, typename F>
+    // ---- TMEM row access.  An accumulator with MR = 128 rows keeps row r in lane r:
+    // warp w reads lane quadrant w % 4, and the two warps of a quadrant split the
+    // columns in halves.  One with MR = 64 keeps its rows in lanes 0-15 of each
+    // quadrant: the 16x32bx2 shape lets both half-warps read, so the columns split
+    // in quarters.  f(c0, v[16]) gets 16 consecutive columns starting at c0.
+    template <int MR>
+    __device__ __forceinline__ int colpart() const { return MR == 128 ? half : half * 2 + (lane >> 4); }
+    template <int MR, int NC, typename F>
     __device__ __forceinline__ void for_row(uint32_t slot, F &&f) {
-        constexpr int HALF = NC / 2;
         float a[16], b[16];
+        if constexpr (MR == 128) {
+            constexpr int HALF = NC / 2;
 #pragma unroll
-        for (int c0 = 0; c0 < HALF; c0 += 32) {
-            const int c = half * HALF + c0;
-            tmem_ld16(taddr(slot, c), a);
-            tmem_ld16(taddr(slot, c + 16), b);
-            tmem_wait_ld();
-            f(c, a);
-            f(c + 16, b);
+            for (int c0 = 0; c0 < HALF; c0 += 32) {
+                const int c = half * HALF + c0;
+                tmem_ld16(taddr(slot, c), a);
+                tmem_ld16(taddr(slot, c + 16), b);
+                tmem_wait_ld();
+                f(c, a);
+                f(c + 16, b);
+            }
+        } else {
+            constexpr int QC = NC / 4;
+            const int cw = half * (NC / 2), cme = cw + (lane >> 4) * QC;
+            if constexpr (QC == 16) {
+                tmem_ld16x2<QC>(taddr(slot, cw), a);
+                tmem_wait_ld();
+                f(cme, a);
+            } else {
+                tmem_ld16x2<QC>(taddr(slot, cw), a);
+                tmem_ld16x2<QC>(taddr(slot, cw + 16), b);
+                tmem_wait_ld();
+                f(cme, a);
+                f(cme + 16, b);
+            }
         }
     }
-    template <int NC, typename F>
+    // Read-modify-write: values changed by f are stored back.
+    template <int MR, int NC, typename F>
     __device__ __forceinline__ void rmw_row(uint32_t slot, F &&f) {
-        constexpr int HALF = NC / 2;
         float a[16], b[16];
+        if constexpr (MR == 128) {
+            constexpr int HALF = NC / 2;
 #pragma unroll
-        for (int c0 = 0; c0 < HALF; c0 += 32) {
-            const int c = half * HALF + c0;
-            tmem_ld16(taddr(slot, c), a);
-            tmem_ld16(taddr(slot, c + 16), b);
-            tmem_wait_ld();
-            f(c, a);
-            f(c + 16, b);
-            tmem_st16(taddr(slot, c), a);
-            tmem_st16(taddr(slot, c + 16), b);
+            for (int c0 = 0; c0 < HALF; c0 += 32) {
+                const int c = half * HALF + c0;
+                tmem_ld16(taddr(slot, c), a);
+                tmem_ld16(taddr(slot, c + 16), b);
+                tmem_wait_ld();
+                f(c, a);
+                f(c + 16, b);
+                tmem_st16(taddr(slot, c), a);
+                tmem_st16(taddr(slot, c + 16), b);
+            }
+        } else {
+            constexpr int QC = NC / 4;
+            const int cw = half * (NC / 2), cme = cw + (lane >> 4) * QC;
+            if constexpr (QC == 16) {
+                tmem_ld16x2<QC>(taddr(slot, cw), a);
+                tmem_wait_ld();
+                f(cme, a);
+                tmem_st16x2<QC>(taddr(slot, cw), a);
+            } else {
+                tmem_ld16x2<QC>(taddr(slot, cw), a);
+                tmem_ld16x2<QC>(taddr(slot, cw + 16), b);
+                tmem_wait_ld();
+                f(cme, a);
+                f(cme + 16, b);
+                tmem_st16x2<QC>(taddr(slot, cw), a);
+                tmem_st16x2<QC>(taddr(slot, cw + 16), b);
+            }
         }
         tmem_wait_st();
     }
     // Two accumulators with the same row layout, read together.
-    template <int NC, typename F>
+    template <int MR, int NC, typename F>
     __device__ __forceinline__ void for_row2(uint32_t s1, uint32_t s2, F &&f) {
-        constexpr int HALF = NC / 2;
         float a[16], b[16];
+        if constexpr (MR == 128) {
+            constexpr int HALF = NC / 2;
 #pragma unroll
-        for (int c0 = 0; c0 < HALF; c0 += 16) {
-            const int c = half * HALF + c0;
-            tmem_ld16(taddr(s1, c), a);
-            tmem_ld16(taddr(s2, c), b);
-            tmem_wait_ld();
-            f(c, a, b);
+            for (int c0 = 0; c0 < HALF; c0 += 16) {
+                const int c = half * HALF + c0;
+                tmem_ld16(taddr(s1, c), a);
+                tmem_ld16(taddr(s2, c), b);
+                tmem_wait_ld();
+                f(c, a, b);
+            }
+        } else {
+            constexpr int QC = NC / 4;
+            const int cw = half * (NC / 2), cme = cw + (lane >> 4) * QC;
+#pragma unroll
+            for (int c0 = 0; c0 < QC; c0 += 16) {
+                tmem_ld16x2<QC>(taddr(s1, cw + c0), a);
+                tmem_ld16x2<QC>(taddr(s2, cw + c0), b);
+                tmem_wait_ld();
+                f(cme + c0, a, b);
+            }
         }
     }
-    template <int NC>
+    template <int MR, int NC>
     __device__ void zero_slot(uint32_t slot) {
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        if constexpr (MR == 128) {
 #pragma unroll
-        for (int c0 = 0; c0 < NC / 2; c0 += 16) tmem_st16(taddr(slot, half * (NC / 2) + c0), v);
+            for (int c0 = 0; c0 < NC / 2; c0 += 16) tmem_st16(taddr(slot, half * (NC / 2) + c0), v);
+        } else {
+            constexpr int QC = NC / 4;
+#pragma unroll
+            for (int c0 = 0; c0 < QC; c0 += 16) tmem_st16x2<QC>(taddr(slot, half * (NC / 2) + c0), v);
+        }
         tmem_wait_st();
     }
 
-    // Per-half row partials: the two column halves of a row write separate arrays.
-    __device__ void put_partial(float *dst0, float *dst1, int row, float v) {
-        if (row >= 0) (half ? dst1 : dst0)[row] = v;
+    // Copy state accumulator `slot` (rows D, NC columns) to the bf16 tile `dst`;
+    // with decay, also scale the accumulator by `scale` in place.
+    template <int NC>
+    __device__ __forceinline__ void extract_state(uint32_t slot, uint8_t *dst, float scale) {
+        auto f = [&](int c0, float (&v)[16]) {
+            tile_store_row16(dst, D, rowD, c0, v);
+            if constexpr (DECAY) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] *= scale;
+            }
+        };
+        if constexpr (DECAY) rmw_row<D, NC>(slot, f);
+        else for_row<D, NC>(slot, f);
+    }
+
+    // Row partial sums: each column part of a row writes its own slot.
+    template <int MR>
+    __device__ void put_partial(float *dst, int row, float v) {
+        dst[colpart<MR>() * MR + row] = v;
+    }
+    template <int MR>
+    __device__ float sum_partials(const float *src, int row) const {
+        float s = src[row] + src[MR + row];
+        if constexpr (MR == 64) s += src[2 * MR + row] + src[3 * MR + row];
+        return s;
     }
 
     // Row-scaled copy of a [C x W] tile: dst[r] = scale(r) * src[r] (all threads).
@@ -330,15 +462,18 @@ struct Kern {
 
     // Masked, decayed row of a c x c score tile: v[i] (column c0+i of row `row`)
     // becomes 0 above the diagonal and is scaled by g^{P (row - col)} below it
-    // (P = 1 for A-tilde, 2 for M).  Off-diagonal groups use one exp2 per group.
+    // (P = 1 for A-tilde, 2 for M).  Off-diagonal groups use one exp2 per group
+    // and the factors g^{P j} held in gt.
     template <int POW>
-    __device__ __forceinline__ void mask_row(int row, int c0, float (&v)[16]) const {
-        if (c0 + 15 <= row) {
+    __device__ __forceinline__ void mask_row(int row, int c0, float (&v)[16], const float (&gt)[16]) const {
+        if (c0 > row) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        } else if (c0 + 15 <= row) {
             if constexpr (DECAY) {
                 const float b = gp(POW * (row - c0 - 15));
-                const float *t = g16 + (POW == 2 ? 16 : 0);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] *= b * t[15 - i];
+                for (int i = 0; i < 16; ++i) v[i] *= b * gt[15 - i];
             }
         } else {
 #pragma unroll
@@ -348,113 +483,113 @@ struct Kern {
             }
         }
     }
+    // g^{P j}, j < 16, into registers (only with decay)
+    template <int POW>
+    __device__ __forceinline__ void load_g16(float (&gt)[16]) const {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) gt[i] = DECAY ? g16()[(POW == 2 ? 16 : 0) + i] : 1.f;
+    }
 
-    // m <- g^L m + sum_b w_b q_b and Y <- g^{2L} Y + sum_b ycol_b over the rows of
-    // two [C x D] tiles (ycol already carries its weights); all threads.
-    // Two row groups (even / odd rows) per column, combined in a fixed order so
-    // that results do not depend on thread timing.
-    __device__ void column_sums(const uint8_t *tq, const uint8_t *ty, int L) {
+    // m <- m + sum_b wm(b) q_b and Y <- Y + sum_b ycol_b over the rows b < L of
+    // two [C x D] tiles (ycol already carries its weights).  wm(b) = wlast * g^{L-1-b}
+    // is produced by repeated multiplication from the last row down.  Two row groups
+    // (even / odd rows) per column, combined in a fixed order (deterministic).
+    __device__ void column_sums(const uint8_t *tq, const uint8_t *ty, int L, float wlast) {
         const int i = tid % D, g = tid / D;
         float am = 0.f, ay = 0.f;
-        if (g < 2) {
-            for (int b = g; b < L; b += 2) {
-                am += gp(L - 1 - b) * tile_load(tq, C, b, i);
-                ay += tile_load(ty, C, b, i);
+        if (g < 2 && L > g) {
+            const uint32_t colb = (uint32_t)(i >> 6) * C * 128u + (uint32_t)(i & 7) * 2u;
+            const uint32_t j = (uint32_t)((i & 63) >> 3);
+            const int blast = ((L - 1 - g) & ~1) + g;  // last row of this parity below L
+            float w = wlast * gp(L - 1 - blast);
+            const float g2 = gp(2);
+            for (int b = blast; b >= 0; b -= 2) {
+                const uint32_t off = colb + (uint32_t)b * 128u + ((j ^ (uint32_t)(b & 7)) << 4);
+                am += w * __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(tq + off) << 16);
+                ay += __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(ty + off) << 16);
+                w *= g2;
             }
         }
-        if (g == 1) { part0[i] = am; part1[i] = ay; }
+        if (g == 1) { part0()[i] = am; part1()[i] = ay; }
         __syncthreads();
         if (g == 0) {
-            mrun[i] = gp(L) * mrun[i] + (am + part0[i]);
-            Yrun[i] = gp(2 * L) * Yrun[i] + (ay + part1[i]);
+            mrun()[i] += am + part0()[i];
+            Yrun()[i] += ay + part1()[i];
         }
         __syncthreads();
     }
 
-    // A-tilde = tril(Gamma1 o A) from TMEM W -> sTA
+    // A-tilde = tril(Gamma1 o A) from TMEM W -> tA()
     __device__ void epi_atilde() {
-        for_row<C>(TW, [&](int c0, float (&v)[16]) {
+        float gt[16];
+        load_g16<1>(gt);
+        for_row<C, C>(TW, [&](int c0, float (&v)[16]) {
             if (rowC < 0) return;
-            mask_row<1>(rowC, c0, v);
-            tile_store_row16(sTA, C, rowC, c0, v);
+            mask_row<1>(rowC, c0, v, gt);
+            tile_store_row16(tA(), C, rowC, c0, v);
         });
     }
 
     // ======================================================================== pass 1
     // Segment summary from zero state over chunks [jb, je): TMEM S, X, C and
-    // mrun / Yrun hold (S, X, C, m, Y) of the segment afterwards.
+    // mrun() / Yrun() hold (S, X, C, m, Y) of the segment afterwards.  X, C, m, Y take
+    // their decay weights relative to the segment end, g^{LB - tau} (<= 1, tau
+    // the token's position in the segment), so they need no per-chunk rescaling;
+    // S is rescaled per chunk because its bf16 copy feeds the next chunk.
     __device__ bool pass1(int jb, int je) {
-        for (int i = tid; i < D; i += kThreads) mrun[i] = Yrun[i] = 0.f;
+        for (int i = tid; i < D; i += kThreads) mrun()[i] = Yrun()[i] = 0.f;
+        const int LB = min(P.n, je * C) - jb * C;  // tokens in the segment
         int stage = 0;
         tma_chunk(jb, 0);
         for (int jj = jb; jj < je; ++jj) {
             const bool first = (jj == jb);
             const int L = min(C, P.n - jj * C);
+            const int rest = LB - (jj - jb) * C - L;  // segment tokens after this chunk
             if (K_::NSTAGE == 1 && !first) tma_chunk(jj, 0);
             uint8_t *Q = sQ(stage), *Kt = sK(stage), *V = sV(stage);
-            // state at the chunk start -> bf16 operand copy of S; decay the state
-            if (!first) {
-                const float gL = gp(L), g2L = gp(2 * L);
-                rmw_row<D>(TS, [&](int c0, float (&v)[16]) {
-                    if (rowD >= 0) tile_store_row16(sTS, D, rowD, c0, v);
-                    if constexpr (DECAY) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] *= gL;
-                    }
-                });
-                if constexpr (DECAY) {
-                    rmw_row<DV>(TX, [&](int, float (&v)[16]) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] *= g2L;
-                    });
-                    rmw_row<DV>(T4, [&](int, float (&v)[16]) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] *= gL;
-                    });
-                }
-            }
             if (!wait_tma(stage)) return false;
             if (K_::NSTAGE == 2 && jj + 1 < je) tma_chunk(jj + 1, stage ^ 1);
-            if constexpr (DECAY) {
-                if (!first) scaled_tile_copy<D>(Q, sTQ, [&](int r) { return gp(r + 1); });  // diag(g^tau) Q
-            }
-            publish();
-            if (tid == 0) mma_kk(TW, Q, Kt, C, D, false);  // A = Q K^T
+            if (tid == 0) mma_kk<C, D>(TW, Q, Kt, false);  // A = Q K^T
             commit();
+            // meanwhile: state at the chunk start -> bf16 copy of S, then decay S
+            if (!first) {
+                extract_state<D>(TS, tS(), gp(L));
+                if constexpr (DECAY)  // diag(g^tau) Q
+                    scaled_tile_copy<D>(Q, tQ(), [&](int r) { return gp(r + 1); });
+            }
             if (!wait_mma()) return false;
             epi_atilde();
             publish();
             if (tid == 0) {
-                if (!first) mma_kk(TW, DECAY ? sTQ : Q, sTS, D, D, false);  // diag(g^tau) Q S_p
-                mma_km(TW, sTA, Kt, D, C, !first);                          // + A-tilde K
+                if (!first) mma_kk<D, D>(TW, DECAY ? tQ() : Q, tS(), false);  // diag(g^tau) Q S_p
+                mma_km<D, C>(TW, tA(), Kt, !first);                          // + A-tilde K
             }
             commit();
             if (!wait_mma()) return false;
-            // U weighted by w^2 (the X update's left operand); K_w, V_w for decay
+            // U weighted by g^{2(LB - tau)} (the X update's left operand); K_w, V_w for decay
             {
-                const float w2 = (DECAY && rowC >= 0) ? (rowC < L ? gp(2 * (L - 1 - rowC)) : 0.f) : 1.f;
-                for_row<D>(TW, [&](int c0, float (&v)[16]) {
+                const float w2 = (DECAY && rowC >= 0) ? (rowC < L ? gp(2 * (rest + L - 1 - rowC)) : 0.f) : 1.f;
+                for_row<C, D>(TW, [&](int c0, float (&v)[16]) {
                     if (rowC < 0) return;
                     if constexpr (DECAY) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) v[i] *= w2;
                     }
-                    tile_store_row16(sTU, C, rowC, c0, v);
+                    tile_store_row16(tU(), C, rowC, c0, v);
                 });
             }
             if constexpr (DECAY) {
-                auto w = [&](int r) { return r < L ? gp(L - 1 - r) : 0.f; };
-                scaled_tile_copy<D>(Kt, sTA, w);
-                scaled_tile_copy<DV>(V, sTS, w);
+                scaled_tile_copy<D>(Kt, tA(), [&](int r) { return r < L ? gp(L - 1 - r) : 0.f; });
+                scaled_tile_copy<DV>(V, tS(), [&](int r) { return r < L ? gp(rest + L - 1 - r) : 0.f; });
             }
             publish();
             if (tid == 0) {
-                mma_mm(TS, Kt, DECAY ? sTA : Kt, D, !first);  // S += K^T W K
-                mma_mm(TX, sTU, V, DV, !first);               // X += (W^2 U)^T V
-                mma_mm(T4, Q, DECAY ? sTS : V, DV, !first);   // C += Q^T W V
+                mma_mm<D>(TS, Kt, DECAY ? tA() : Kt, !first);  // S += K^T W K
+                mma_mm<DV>(TX, tU(), V, !first);               // X += (W^2 U)^T V
+                mma_mm<DV>(T4, Q, DECAY ? tS() : V, !first);   // C += Q^T W V
             }
             commit();
-            if (need_mY) column_sums(Q, sTU, L);  // overlaps the MMAs
+            if (need_mY) column_sums(Q, tU(), L, gp(rest));  // overlaps the MMAs
             if (!wait_mma()) return false;
             stage ^= (K_::NSTAGE - 1);
         }
@@ -464,29 +599,29 @@ struct Kern {
     // Write the TMEM/SMEM summary (S, X, C, m, Y) of this CTA to `dst`.
     __device__ void store_summary(float *dst) {
         float *S = dst, *X = S + D * D, *Cc = X + D * DV, *m = Cc + D * DV, *Y = m + D;
-        for_row<D>(TS, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(S + rowD * D + c0, v); });
-        for_row<DV>(TX, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(X + rowD * DV + c0, v); });
-        for_row<DV>(T4, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(Cc + rowD * DV + c0, v); });
-        for (int i = tid; i < D; i += kThreads) { m[i] = mrun[i]; Y[i] = Yrun[i]; }
+        for_row<D, D>(TS, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(S + rowD * D + c0, v); });
+        for_row<D, DV>(TX, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(X + rowD * DV + c0, v); });
+        for_row<D, DV>(T4, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(Cc + rowD * DV + c0, v); });
+        for (int i = tid; i < D; i += kThreads) { m[i] = mrun()[i]; Y[i] = Yrun()[i]; }
     }
 
     // ======================================================================== scan
     __device__ bool prefix_init() {
         if (!P.sin.S) {
-            zero_slot<D>(TS);
-            zero_slot<DV>(TX);
-            zero_slot<DV>(T4);
-            for (int i = tid; i < D; i += kThreads) mrun[i] = Yrun[i] = 0.f;
+            zero_slot<D, D>(TS);
+            zero_slot<D, DV>(TX);
+            zero_slot<D, DV>(T4);
+            for (int i = tid; i < D; i += kThreads) mrun()[i] = Yrun()[i] = 0.f;
             publish();
             return true;
         }
         const float *Si = P.sin.S + (size_t)bh * D * D, *Ci = P.sin.C + (size_t)bh * D * DV;
         const float *mi = P.sin.m + (size_t)bh * D, *Gi = P.sin.G + (size_t)bh * D * DV,
                     *hi = P.sin.h + (size_t)bh * D;
-        for (int i = tid; i < D; i += kThreads) mrun[i] = mi[i];
+        for (int i = tid; i < D; i += kThreads) mrun()[i] = mi[i];
         __syncthreads();
         float sm = 0.f;
-        rmw_row<D>(TS, [&](int c0, float (&v)[16]) {
+        rmw_row<D, D>(TS, [&](int c0, float (&v)[16]) {
             if (rowD < 0) return;
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
@@ -494,29 +629,29 @@ struct Kern {
                 v[i] = s.x; v[i + 1] = s.y; v[i + 2] = s.z; v[i + 3] = s.w;
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sm += v[i] * mrun[c0 + i];
-            store_hilo(sShi, sSlo, D, rowD, c0, v);
+            for (int i = 0; i < 16; ++i) sm += v[i] * mrun()[c0 + i];
+            store_hilo(tShi(), tSlo(), D, rowD, c0, v);
         });
-        rmw_row<DV>(T4, [&](int c0, float (&v)[16]) {
+        rmw_row<D, DV>(T4, [&](int c0, float (&v)[16]) {
             if (rowD < 0) return;
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
                 const float4 s = *reinterpret_cast<const float4 *>(Ci + rowD * DV + c0 + i);
                 v[i] = s.x; v[i + 1] = s.y; v[i + 2] = s.z; v[i + 3] = s.w;
             }
-            store_hilo(sChi, sClo, D, rowD, c0, v);
+            store_hilo(tChi(), tClo(), D, rowD, c0, v);
         });
-        put_partial(part0, part1, rowD, sm);
+        put_partial<D>(part(), rowD, sm);
         publish();
         if (tid == 0) {  // X = S C (three bf16 products approximate the fp32 one)
-            mma_ss(TX, sShi, sChi, false);
-            mma_ss(TX, sShi, sClo, true);
-            mma_ss(TX, sSlo, sChi, true);
+            mma_ss(TX, tShi(), tChi(), false);
+            mma_ss(TX, tShi(), tClo(), true);
+            mma_ss(TX, tSlo(), tChi(), true);
         }
         commit();
-        for (int i = tid; i < D; i += kThreads) Yrun[i] = part0[i] + part1[i] - hi[i];
+        for (int i = tid; i < D; i += kThreads) Yrun()[i] = sum_partials<D>(part(), i) - hi[i];
         if (!wait_mma()) return false;
-        rmw_row<DV>(TX, [&](int c0, float (&v)[16]) {
+        rmw_row<D, DV>(TX, [&](int c0, float (&v)[16]) {
             if (rowD < 0) return;
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
@@ -532,22 +667,22 @@ struct Kern {
     __device__ bool fold(const float *Lsum, float f) {
         const float *SL = Lsum, *XL = SL + D * D, *CL = XL + D * DV, *mLg = CL + D * DV, *YL = mLg + D;
         const float f2 = f * f;
-        for (int i = tid; i < D; i += kThreads) mL[i] = __ldcg(mLg + i);
+        for (int i = tid; i < D; i += kThreads) mL()[i] = __ldcg(mLg + i);
         __syncthreads();
         float sm = 0.f;
-        rmw_row<D>(TS, [&](int c0, float (&v)[16]) {
+        rmw_row<D, D>(TS, [&](int c0, float (&v)[16]) {
             if (rowD < 0) return;
-            store_hilo(sShi, sSlo, D, rowD, c0, v);
+            store_hilo(tShi(), tSlo(), D, rowD, c0, v);
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
                 const float4 s = ldcg4(SL + rowD * D + c0 + i);
-                sm += v[i] * mL[c0 + i] + v[i + 1] * mL[c0 + i + 1] + v[i + 2] * mL[c0 + i + 2] +
-                      v[i + 3] * mL[c0 + i + 3];
+                sm += v[i] * mL()[c0 + i] + v[i + 1] * mL()[c0 + i + 1] + v[i + 2] * mL()[c0 + i + 2] +
+                      v[i + 3] * mL()[c0 + i + 3];
                 v[i] = f * v[i] + s.x; v[i + 1] = f * v[i + 1] + s.y;
                 v[i + 2] = f * v[i + 2] + s.z; v[i + 3] = f * v[i + 3] + s.w;
             }
         });
-        rmw_row<DV>(TX, [&](int c0, float (&v)[16]) {
+        rmw_row<D, DV>(TX, [&](int c0, float (&v)[16]) {
             if (rowD < 0) return;
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
@@ -556,7 +691,7 @@ struct Kern {
                 v[i + 2] = f2 * v[i + 2] + s.z; v[i + 3] = f2 * v[i + 3] + s.w;
             }
         });
-        rmw_row<DV>(T4, [&](int c0, float (&v)[16]) {
+        rmw_row<D, DV>(T4, [&](int c0, float (&v)[16]) {
             if (rowD < 0) return;
             float cl[16];
 #pragma unroll
@@ -566,19 +701,19 @@ struct Kern {
                 v[i] = f * v[i] + s.x; v[i + 1] = f * v[i + 1] + s.y;
                 v[i + 2] = f * v[i + 2] + s.z; v[i + 3] = f * v[i + 3] + s.w;
             }
-            store_hilo(sChi, sClo, D, rowD, c0, cl);
+            store_hilo(tChi(), tClo(), D, rowD, c0, cl);
         });
-        put_partial(part0, part1, rowD, sm);
+        put_partial<D>(part(), rowD, sm);
         publish();
         if (tid == 0) {  // X += S_P (f C_L)
-            mma_ss(TX, sShi, sChi, true);
-            mma_ss(TX, sShi, sClo, true);
-            mma_ss(TX, sSlo, sChi, true);
+            mma_ss(TX, tShi(), tChi(), true);
+            mma_ss(TX, tShi(), tClo(), true);
+            mma_ss(TX, tSlo(), tChi(), true);
         }
         commit();
         for (int i = tid; i < D; i += kThreads) {
-            Yrun[i] = f2 * Yrun[i] + __ldcg(YL + i) + f * (part0[i] + part1[i]);
-            mrun[i] = f * mrun[i] + mL[i];
+            Yrun()[i] = f2 * Yrun()[i] + __ldcg(YL + i) + f * (sum_partials<D>(part(), i));
+            mrun()[i] = f * mrun()[i] + mL()[i];
         }
         return wait_mma();
     }
@@ -606,32 +741,32 @@ struct Kern {
         float *So = P.sout.S + (size_t)bh * D * D, *Co = P.sout.C + (size_t)bh * D * DV;
         float *mo = P.sout.m + (size_t)bh * D, *Go = P.sout.G + (size_t)bh * D * DV, *ho = P.sout.h + (size_t)bh * D;
         float sm = 0.f;
-        for_row<D>(TS, [&](int c0, float (&v)[16]) {
+        for_row<D, D>(TS, [&](int c0, float (&v)[16]) {
             if (rowD < 0) return;
-            store_hilo(sShi, sSlo, D, rowD, c0, v);
+            store_hilo(tShi(), tSlo(), D, rowD, c0, v);
             st_row16(So + rowD * D + c0, v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sm += v[i] * mrun[c0 + i];
+            for (int i = 0; i < 16; ++i) sm += v[i] * mrun()[c0 + i];
         });
-        for_row<DV>(T4, [&](int c0, float (&v)[16]) {
+        for_row<D, DV>(T4, [&](int c0, float (&v)[16]) {
             if (rowD < 0) return;
-            store_hilo(sChi, sClo, D, rowD, c0, v);
+            store_hilo(tChi(), tClo(), D, rowD, c0, v);
             st_row16(Co + rowD * DV + c0, v);
         });
-        put_partial(part0, part1, rowD, sm);
+        put_partial<D>(part(), rowD, sm);
         publish();
         if (tid == 0) {  // W = S C
-            mma_ss(TW, sShi, sChi, false);
-            mma_ss(TW, sShi, sClo, true);
-            mma_ss(TW, sSlo, sChi, true);
+            mma_ss(TW, tShi(), tChi(), false);
+            mma_ss(TW, tShi(), tClo(), true);
+            mma_ss(TW, tSlo(), tChi(), true);
         }
         commit();
         for (int i = tid; i < D; i += kThreads) {
-            mo[i] = mrun[i];
-            ho[i] = part0[i] + part1[i] - Yrun[i];
+            mo[i] = mrun()[i];
+            ho[i] = sum_partials<D>(part(), i) - Yrun()[i];
         }
         if (!wait_mma()) return false;
-        for_row2<DV>(TW, TX, [&](int c0, float (&sc)[16], float (&xv)[16]) {
+        for_row2<D, DV>(TW, TX, [&](int c0, float (&sc)[16], float (&xv)[16]) {
             if (rowD < 0) return;
 #pragma unroll
             for (int i = 0; i < 16; ++i) sc[i] -= xv[i];
@@ -643,27 +778,59 @@ struct Kern {
     // Save / restore the parts of the prefix that pass 2 needs (S, X, m, Y).
     __device__ void save_prefix(float *sv) {
         float *S = sv, *X = S + D * D, *m = X + D * DV, *Y = m + D;
-        for_row<D>(TS, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(S + rowD * D + c0, v); });
-        for_row<DV>(TX, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(X + rowD * DV + c0, v); });
-        for (int i = tid; i < D; i += kThreads) { m[i] = mrun[i]; Y[i] = Yrun[i]; }
+        for_row<D, D>(TS, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(S + rowD * D + c0, v); });
+        for_row<D, DV>(TX, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(X + rowD * DV + c0, v); });
+        for (int i = tid; i < D; i += kThreads) { m[i] = mrun()[i]; Y[i] = Yrun()[i]; }
     }
+    // Prefix <- a stored summary (S, X, C, m, Y): the fold of that summary into a
+    // zero prefix.
+    __device__ void load_summary(const float *src) {
+        const float *S = src, *X = S + D * D, *Cc = X + D * DV, *m = Cc + D * DV, *Y = m + D;
+        rmw_row<D, D>(TS, [&](int c0, float (&v)[16]) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+                const float4 a = ldcg4(S + rowD * D + c0 + i);
+                v[i] = a.x; v[i + 1] = a.y; v[i + 2] = a.z; v[i + 3] = a.w;
+            }
+        });
+        rmw_row<D, DV>(TX, [&](int c0, float (&v)[16]) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+                const float4 a = ldcg4(X + rowD * DV + c0 + i);
+                v[i] = a.x; v[i + 1] = a.y; v[i + 2] = a.z; v[i + 3] = a.w;
+            }
+        });
+        rmw_row<D, DV>(T4, [&](int c0, float (&v)[16]) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+                const float4 a = ldcg4(Cc + rowD * DV + c0 + i);
+                v[i] = a.x; v[i + 1] = a.y; v[i + 2] = a.z; v[i + 3] = a.w;
+            }
+        });
+        for (int i = tid; i < D; i += kThreads) { mrun()[i] = __ldcg(m + i); Yrun()[i] = __ldcg(Y + i); }
+        tc_sync();
+    }
+
     __device__ void restore_prefix(const float *sv) {
         const float *S = sv, *X = S + D * D, *m = X + D * DV, *Y = m + D;
         __syncthreads();
-        rmw_row<D>(TS, [&](int c0, float (&v)[16]) {
+        rmw_row<D, D>(TS, [&](int c0, float (&v)[16]) {
             if (rowD >= 0)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = S[rowD * D + c0 + i];
         });
-        rmw_row<DV>(TX, [&](int c0, float (&v)[16]) {
+        rmw_row<D, DV>(TX, [&](int c0, float (&v)[16]) {
             if (rowD >= 0)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = X[rowD * DV + c0 + i];
         });
-        for (int i = tid; i < D; i += kThreads) { mrun[i] = m[i]; Yrun[i] = Y[i]; }
+        for (int i = tid; i < D; i += kThreads) { mrun()[i] = m[i]; Yrun()[i] = Y[i]; }
     }
 
     // ======================================================================== pass 2
+    // Outputs from the exact prefix.  Q S_p and Q X_p go to the spare columns so
+    // that they overlap the epilogues; two completion barriers let the block work
+    // on one group of MMA results while the next group runs.
     __device__ bool pass2(int jb, int je) {
         __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(P.o) + (size_t)bh * P.n * DV;
         int stage = 0;
@@ -673,122 +840,105 @@ struct Kern {
             const int L = min(C, P.n - t0);
             if (K_::NSTAGE == 1 && jj != jb) tma_chunk(jj, 0);
             uint8_t *Q = sQ(stage), *Kt = sK(stage), *V = sV(stage);
-            // state at the chunk start -> bf16 operands; then decay it to the chunk end
-            {
-                const float gL = gp(L), g2L = gp(2 * L);
-                rmw_row<D>(TS, [&](int c0, float (&v)[16]) {
-                    if (rowD >= 0) tile_store_row16(sTS, D, rowD, c0, v);
-                    if constexpr (DECAY) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] *= gL;
-                    }
-                });
-                rmw_row<DV>(TX, [&](int c0, float (&v)[16]) {
-                    if (rowD >= 0) tile_store_row16(sTQ, D, rowD, c0, v);
-                    if constexpr (DECAY) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] *= g2L;
-                    }
-                });
-            }
             if (!wait_tma(stage)) return false;
             if (K_::NSTAGE == 2 && jj + 1 < je) tma_chunk(jj + 1, stage ^ 1);
-            if constexpr (NORM) {  // q_t . Y_p, before Y moves on (one thread per row)
+            if (tid == 0) mma_kk<C, D>(TW, Q, Kt, false);  // A = Q K^T
+            commit();
+            // meanwhile: S_p -> bf16 operand, then decay S to the chunk end
+            extract_state<D>(TS, tS(), gp(L));
+            publish();
+            if (tid == 0) mma_kk<D, D>(T4, Q, tS(), false);  // spare = Q S_p
+            commit2();
+            // meanwhile: X_p -> bf16 operand, then decay X; q . Y_p for the denominator
+            extract_state<DV>(TX, tQ(), gp(2 * L));
+            if constexpr (NORM) {
                 if (tid < C) {
                     float acc = 0.f;
-                    for (int i = 0; i < D; ++i) acc += tile_load(Q, C, tid, i) * Yrun[i];
-                    den[tid] = acc;
+                    for (int i = 0; i < D; ++i) acc += tile_load(Q, C, tid, i) * Yrun()[i];
+                    den()[tid] = acc;
                 }
             }
-            publish();
-            if (tid == 0) mma_kk(TW, Q, Kt, C, D, false);  // A = Q K^T
-            commit();
-            if (!wait_mma()) return false;
+            if (!wait_mma()) return false;  // A
             epi_atilde();
             publish();
-            if (tid == 0) {
-                if constexpr (DECAY) {
-                    mma_kk(T4, Q, sTS, D, D, false);   // spare = Q S_p
-                    mma_km(TW, sTA, Kt, D, C, false);  // W = A-tilde K
-                } else {
-                    mma_kk(TW, Q, sTS, D, D, false);
-                    mma_km(TW, sTA, Kt, D, C, true);
-                }
-            }
+            if (tid == 0) mma_km<D, C>(TW, tA(), Kt, false);  // W = A-tilde K
             commit();
-            if (!wait_mma()) return false;
-            // U = g^tau Q S_p + A-tilde K -> sTU; W^2 U -> sTS (decay)
-            if constexpr (DECAY) {
-                const float gt = rowC >= 0 ? gp(rowC + 1) : 0.f;
+            if (!wait_mma2()) return false;  // Q S_p
+            if (!wait_mma()) return false;   // A-tilde K
+            // U = g^tau Q S_p + A-tilde K -> tU(); W^2 U -> tS() (decay)
+            {
+                const float gt = (DECAY && rowC >= 0) ? gp(rowC + 1) : 1.f;
                 const float w2 = (rowC >= 0 && rowC < L) ? gp(2 * (L - 1 - rowC)) : 0.f;
-                for_row2<D>(TW, T4, [&](int c0, float (&v)[16], float (&sp)[16]) {
+                for_row2<C, D>(TW, T4, [&](int c0, float (&v)[16], float (&sp)[16]) {
                     if (rowC < 0) return;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] += gt * sp[i];
-                    tile_store_row16(sTU, C, rowC, c0, v);
+                    tile_store_row16(tU(), C, rowC, c0, v);
+                    if constexpr (DECAY) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] *= w2;
-                    tile_store_row16(sTS, C, rowC, c0, v);
-                });
-                scaled_tile_copy<D>(Kt, sTA, [&](int r) { return r < L ? gp(L - 1 - r) : 0.f; });
-            } else {
-                for_row<D>(TW, [&](int c0, float (&v)[16]) {
-                    if (rowC >= 0) tile_store_row16(sTU, C, rowC, c0, v);
+                        for (int i = 0; i < 16; ++i) v[i] *= w2;
+                        tile_store_row16(tS(), C, rowC, c0, v);
+                    }
                 });
             }
+            if constexpr (DECAY)
+                scaled_tile_copy<D>(Kt, tA(), [&](int r) { return r < L ? gp(L - 1 - r) : 0.f; });
             publish();
             if (tid == 0) {
-                mma_kk(TW, Q, sTU, C, D, false);                        // M = Q U^T
-                mma_mm(TX, DECAY ? sTS : sTU, V, DV, true);             // X += (W^2 U)^T V
-                mma_mm(TS, Kt, DECAY ? sTA : Kt, D, true);              // S += K^T W K
-                if constexpr (DECAY) mma_km(T4, Q, sTQ, DV, D, false);  // spare = Q X_p
-            }
+                mma_kk<C, D>(TW, Q, tU(), false);             // M = Q U^T
+                mma_mm<D>(TS, Kt, DECAY ? tA() : Kt, true);   // S += K^T W K (reads tA(): done before
+            }                                                // the M epilogue rewrites tA())
             commit();
-            float ay = 0.f;        // Y <- g^{2L} Y + sum_b w_b^2 u_b (weights on the tile),
-            float *ysc = rsum;     // two row groups; rsum is free until the M epilogue
+            if (tid == 0) {
+                mma_mm<DV>(TX, DECAY ? tS() : tU(), V, true);  // X += (W^2 U)^T V
+                mma_km<DV, D>(T4, Q, tQ(), false);            // spare = Q X_p
+            }
+            commit2();
+            float ay = 0.f;     // Y <- g^{2L} Y + sum_b w_b^2 u_b (weights on the tile),
+            float *ysc = rsum();  // two row groups; rsum() is free until the M epilogue
             if constexpr (NORM) {
                 const int i = tid % D, g = tid / D;
-                const uint8_t *ty = DECAY ? sTS : sTU;
+                const uint8_t *ty = DECAY ? tS() : tU();
                 if (g < 2)
                     for (int b = g; b < L; b += 2) ay += tile_load(ty, C, b, i);
                 if (g == 1) ysc[i] = ay;
             }
-            if (!wait_mma()) return false;
+            if (!wait_mma()) return false;  // M and the S update
             if constexpr (NORM) {
-                if (tid < D) Yrun[tid] = gp(2 * L) * Yrun[tid] + (ay + ysc[tid]);
-                __syncthreads();  // rsum is rewritten by the M epilogue
+                if (tid < D) Yrun()[tid] = gp(2 * L) * Yrun()[tid] + (ay + ysc[tid]);
+                __syncthreads();  // rsum() is rewritten by the M epilogue
             }
-            // M = tril(Gamma2 o Q U^T) -> sTA, row sums for the denominator
-            float rs = 0.f;
-            for_row<C>(TW, [&](int c0, float (&v)[16]) {
-                if (rowC < 0) return;
-                mask_row<2>(rowC, c0, v);
-                if constexpr (NORM) {
+            // M = tril(Gamma2 o Q U^T) -> tA(), row sums for the denominator
+            {
+                float rs = 0.f;
+                float gt2[16];
+                load_g16<2>(gt2);
+                for_row<C, C>(TW, [&](int c0, float (&v)[16]) {
+                    if (rowC < 0) return;
+                    mask_row<2>(rowC, c0, v, gt2);
+                    if constexpr (NORM) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) rs += v[i];
-                }
-                tile_store_row16(sTA, C, rowC, c0, v);
-            });
-            if constexpr (NORM) put_partial(rsum, rsum + C, rowC, rs);
-            publish();
-            if (tid == 0) {
-                mma_km(TW, sTA, V, DV, C, false);                      // O = M V
-                if constexpr (!DECAY) mma_km(TW, Q, sTQ, DV, D, true);  // + Q X_p
+                        for (int i = 0; i < 16; ++i) rs += v[i];
+                    }
+                    tile_store_row16(tA(), C, rowC, c0, v);
+                });
+                if constexpr (NORM) put_partial<C>(rsum(), rowC, rs);
             }
+            publish();
+            if (tid == 0) mma_km<DV, C>(TW, tA(), V, false);  // O = M V
             commit();
-            if (!wait_mma()) return false;
+            if (!wait_mma2()) return false;  // X, S updates and Q X_p
+            if (!wait_mma()) return false;   // M V
             {
                 const float g2t = (DECAY && rowC >= 0) ? gp(2 * (rowC + 1)) : 1.f;
                 float inv = 1.f;
                 if constexpr (NORM) {
-                    if (rowC >= 0) inv = 1.f / (rsum[rowC] + rsum[C + rowC] + g2t * den[rowC] + P.eps);
+                    if (rowC >= 0) inv = 1.f / (sum_partials<C>(rsum(), rowC) + g2t * den()[rowC] + P.eps);
                 }
-                auto out = [&](int c0, float (&v)[16]) {
+                for_row2<C, DV>(TW, T4, [&](int c0, float (&v)[16], float (&sp)[16]) {
                     if (rowC < 0 || rowC >= L) return;
-                    if constexpr (NORM) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] *= inv;
-                    }
+                    for (int i = 0; i < 16; ++i) v[i] = (v[i] + g2t * sp[i]) * inv;
                     uint4 a, b;
                     a.x = pack_bf16(v[0], v[1]); a.y = pack_bf16(v[2], v[3]);
                     a.z = pack_bf16(v[4], v[5]); a.w = pack_bf16(v[6], v[7]);
@@ -797,18 +947,9 @@ struct Kern {
                     uint4 *dst = reinterpret_cast<uint4 *>(O + (size_t)(t0 + rowC) * DV + c0);
                     dst[0] = a;
                     dst[1] = b;
-                };
-                if constexpr (DECAY) {
-                    for_row2<DV>(TW, T4, [&](int c0, float (&v)[16], float (&sp)[16]) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] += g2t * sp[i];
-                        out(c0, v);
-                    });
-                } else {
-                    for_row<DV>(TW, out);
-                }
+                });
             }
-            __syncthreads();
+            tc_sync();  // all TMEM reads of W and the spare done before the next chunk's MMAs
             stage ^= (K_::NSTAGE - 1);
         }
         return true;
@@ -830,16 +971,16 @@ __device__ __forceinline__ void finish_cta(const TcParams &P) {
 }
 
 template <int C, int D, int DV, bool DECAY, bool NORM>
-__global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ TcParams P) {
+__global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(const __grid_constant__ TcParams P) {
     using K_ = Cfg<C, D, DV>;
     // No static shared memory: the dynamic block starts at the (1024-byte
     // aligned) base of the CTA's shared window, which the swizzled tiles need.
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *base = smem_raw;
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + K_::OFF_BAR);
-    uint32_t *tmem_base_p = reinterpret_cast<uint32_t *>(base + K_::OFF_BAR + 24);
-    int *ticket_p = reinterpret_cast<int *>(base + K_::OFF_BAR + 28);
-    int *misalign_p = reinterpret_cast<int *>(base + K_::OFF_BAR + 32);
+    uint32_t *tmem_base_p = reinterpret_cast<uint32_t *>(base + K_::OFF_BAR + 32);
+    int *ticket_p = reinterpret_cast<int *>(base + K_::OFF_BAR + 36);
+    int *misalign_p = reinterpret_cast<int *>(base + K_::OFF_BAR + 40);
 
     Kern<C, D, DV, DECAY, NORM> x(P, base);
     x.tid = threadIdx.x;
@@ -849,23 +990,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     x.half = x.warp >> 2;
     x.rowC = row_of<C>(x.quad, x.lane);
     x.rowD = row_of<D>(x.quad, x.lane);
-    x.sTA = base + K_::OFF_TA; x.sTU = base + K_::OFF_TU; x.sTS = base + K_::OFF_TS; x.sTQ = base + K_::OFF_TQ;
-    x.sShi = base; x.sSlo = base + D * D * 2; x.sChi = base + 2 * D * D * 2; x.sClo = x.sChi + D * DV * 2;
-    float *vec = reinterpret_cast<float *>(base + K_::OFF_VEC);
-    x.mrun = vec; x.Yrun = vec + D;
-    float *r1 = vec + 2 * D;
-    x.mL = r1; x.part0 = r1 + D; x.part1 = r1 + 2 * D;
-    x.rsum = r1; x.den = r1 + 2 * C;
-    x.g16 = r1 + K_::R1;
     x.tma_bar = &bars[0];  // [0], [1]: input stages
     x.mma_bar = &bars[2];
-    x.tph = x.mph = 0;
+    x.mma_bar2 = &bars[3];
+    x.tph = x.mph = x.mph2 = 0;
 
     if (x.tid == 0) {
         *misalign_p = (smem_u32(base) & 1023u) != 0;
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
         mbar_init(&bars[2], 1);
+        mbar_init(&bars[3], 1);
         fence_mbar_init();
         tma_prefetch_desc(&P.tmQ);
         tma_prefetch_desc(&P.tmK);
@@ -881,7 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         return;
     }
     if (x.warp == 0) {
-        tmem_alloc(tmem_base_p, kTmemCols);
+        tmem_alloc(tmem_base_p, K_::TCOLS);
         tmem_relinquish();
     }
     const int ticket = *ticket_p;
@@ -891,7 +1026,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     float g = 1.f;
     if constexpr (DECAY) g = P.gamma[h];
     x.lg = log2f(g);
-    if (x.tid < 32) x.g16[x.tid] = DECAY ? gpow(x.lg, (float)((x.tid & 15) * (x.tid < 16 ? 1 : 2))) : 1.f;
+    if (x.tid < 32) x.g16()[x.tid] = DECAY ? gpow(x.lg, (float)((x.tid & 15) * (x.tid < 16 ? 1 : 2))) : 1.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -924,8 +1059,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (!(ok = x.prefix_init())) break;
-        for (int j = 0; j < seg; ++j) {
+        int j0 = 0;
+        if (!P.sin.S && seg > 0) {  // zero initial state: the prefix starts as segment 0's summary
+            if (!(ok = x.wait_flag(0))) break;
+            x.load_summary(P.summ + ((size_t)x.bh * P.nseg) * K_::SUM);
+            j0 = 1;
+        } else if (!(ok = x.prefix_init())) {
+            break;
+        }
+        for (int j = j0; j < seg; ++j) {
             if (!(ok = x.wait_flag(j))) break;
             if (!(ok = x.fold(P.summ + ((size_t)x.bh * P.nseg + j) * K_::SUM, seg_pow(j)))) break;
         }
@@ -947,7 +1089,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (x.warp == 0) tmem_dealloc(x.tb, kTmemCols);
+    if (x.warp == 0) tmem_dealloc(x.tb, K_::TCOLS);
     if (x.tid == 0) finish_cta(P);
 }
 
@@ -984,7 +1126,7 @@ inline Plan make_plan(const hla_params &p, int num_sms) {
     Plan pl;
     const int BH = p.B * p.H;
     pl.nchunks = (p.n + p.chunk - 1) / p.chunk;
-    int nseg = num_sms / (BH > 0 ? BH : 1);
+    int nseg = num_sms * ctas_per_sm(p) / (BH > 0 ? BH : 1);
     nseg = nseg < 1 ? 1 : nseg;
     if (nseg > pl.nchunks) nseg = pl.nchunks > 0 ? pl.nchunks : 1;
     pl.cps = (pl.nchunks + nseg - 1) / nseg;
