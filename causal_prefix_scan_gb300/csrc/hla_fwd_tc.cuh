@@ -490,33 +490,87 @@ struct Kern {
         for (int i = 0; i < 16; ++i) gt[i] = DECAY ? g16()[(POW == 2 ? 16 : 0) + i] : 1.f;
     }
 
-    // m <- m + sum_b wm(b) q_b and Y <- Y + sum_b ycol_b over the rows b < L of
-    // two [C x D] tiles (ycol already carries its weights).  wm(b) = wlast * g^{L-1-b}
-    // is produced by repeated multiplication from the last row down.  Two row groups
-    // (even / odd rows) per column, combined in a fixed order (deterministic).
-    __device__ void column_sums(const uint8_t *tq, const uint8_t *ty, int L, float wlast) {
-        const int i = tid % D, g = tid / D;
-        float am = 0.f, ay = 0.f;
-        if (g < 2 && L > g) {
-            const uint32_t colb = (uint32_t)(i >> 6) * C * 128u + (uint32_t)(i & 7) * 2u;
-            const uint32_t j = (uint32_t)((i & 63) >> 3);
-            const int blast = ((L - 1 - g) & ~1) + g;  // last row of this parity below L
-            float w = wlast * gp(L - 1 - blast);
-            const float g2 = gp(2);
-            for (int b = blast; b >= 0; b -= 2) {
-                const uint32_t off = colb + (uint32_t)b * 128u + ((j ^ (uint32_t)(b & 7)) << 4);
-                am += w * __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(tq + off) << 16);
-                ay += __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(ty + off) << 16);
-                w *= g2;
+    // Column sums over the rows r < L of one or two [C x D] tiles, for all threads.
+    // Thread t takes an 8-column block (t % (D/8)) and every NG-th row; rows are
+    // read as 16-byte vectors.  Partials combine by warp shuffles and then across
+    // warps in a fixed order (deterministic), through `scr` (2 x 8 x D floats).
+    //   m-sum: wlast * g^{L-1-r} * tq[r]   (weight built by multiplication from the last row)
+    //   y-sum: ty[r]                       (its weights are already in the tile)
+    // Results: dm[i] = sm * dm[i] + msum[i], dy[i] = sy * dy[i] + ysum[i].
+    template <bool TWO>
+    __device__ void tile_colsums(const uint8_t *tq, const uint8_t *ty, int L, float wlast, float *scr,
+                                 float *dm, float sm, float *dy, float sy) {
+        constexpr int NB = D / 8, NG = kThreads / NB;
+        const int cb = tid % NB, rg = tid / NB;
+        float am[8], ay[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) am[j] = ay[j] = 0.f;
+        if (rg < L) {
+            const int rlast = rg + ((L - 1 - rg) / NG) * NG;
+            float w = wlast * gp(L - 1 - rlast);
+            const float gstep = gp(NG);
+            for (int r = rlast; r >= 0; r -= NG) {
+                float a[8];
+                tile_load_row8(tq, C, r, cb * 8, a);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) am[j] += w * a[j];
+                if constexpr (TWO) {
+                    tile_load_row8(ty, C, r, cb * 8, a);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) ay[j] += a[j];
+                }
+                w *= gstep;
             }
         }
-        if (g == 1) { part0()[i] = am; part1()[i] = ay; }
-        __syncthreads();
-        if (g == 0) {
-            mrun()[i] += am + part0()[i];
-            Yrun()[i] += ay + part1()[i];
+#pragma unroll
+        for (int off = NB; off < 32; off <<= 1) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                am[j] += __shfl_xor_sync(0xffffffffu, am[j], off);
+                if constexpr (TWO) ay[j] += __shfl_xor_sync(0xffffffffu, ay[j], off);
+            }
+        }
+        if (lane < NB) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                scr[warp * D + cb * 8 + j] = am[j];
+                if constexpr (TWO) scr[8 * D + warp * D + cb * 8 + j] = ay[j];
+            }
         }
         __syncthreads();
+        if (tid < D) {
+            float a = 0.f, b = 0.f;
+#pragma unroll
+            for (int w8 = 0; w8 < kThreads / 32; ++w8) {
+                a += scr[w8 * D + tid];
+                if constexpr (TWO) b += scr[8 * D + w8 * D + tid];
+            }
+            dm[tid] = sm * dm[tid] + a;
+            if constexpr (TWO) dy[tid] = sy * dy[tid] + b;
+        }
+        __syncthreads();
+    }
+
+    // den[t] = q_t . Y for every row t of the Q tile (all threads; partials in rsum).
+    __device__ void row_dot_Y(const uint8_t *Q) {
+        constexpr int NPR = kThreads / C, CPT = D / NPR;
+        const int r = tid % C, part = tid / C;
+        float acc = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < CPT; c0 += 8) {
+            float q8[8];
+            tile_load_row8(Q, C, r, part * CPT + c0, q8);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc += q8[j] * Yrun()[part * CPT + c0 + j];
+        }
+        rsum()[part * C + r] = acc;
+        __syncthreads();
+        if (tid < C) {
+            float sacc = 0.f;
+#pragma unroll
+            for (int pp = 0; pp < NPR; ++pp) sacc += rsum()[pp * C + tid];
+            den()[tid] = sacc;
+        }
     }
 
     // A-tilde = tril(Gamma1 o A) from TMEM W -> tA()
@@ -589,7 +643,8 @@ struct Kern {
                 mma_mm<DV>(T4, Q, DECAY ? tS() : V, !first);   // C += Q^T W V
             }
             commit();
-            if (need_mY) column_sums(Q, tU(), L, gp(rest));  // overlaps the MMAs
+            if (need_mY)  // overlaps the MMAs; scratch: tQ is free once Q S_p has run
+                tile_colsums<true>(Q, tU(), L, gp(rest), reinterpret_cast<float *>(tQ()), mrun(), 1.f, Yrun(), 1.f);
             if (!wait_mma()) return false;
             stage ^= (K_::NSTAGE - 1);
         }
@@ -851,13 +906,7 @@ struct Kern {
             commit2();
             // meanwhile: X_p -> bf16 operand, then decay X; q . Y_p for the denominator
             extract_state<DV>(TX, tQ(), gp(2 * L));
-            if constexpr (NORM) {
-                if (tid < C) {
-                    float acc = 0.f;
-                    for (int i = 0; i < D; ++i) acc += tile_load(Q, C, tid, i) * Yrun()[i];
-                    den()[tid] = acc;
-                }
-            }
+            if constexpr (NORM) row_dot_Y(Q);
             if (!wait_mma()) return false;  // A
             epi_atilde();
             publish();
@@ -894,19 +943,24 @@ struct Kern {
                 mma_km<DV, D>(T4, Q, tQ(), false);            // spare = Q X_p
             }
             commit2();
-            float ay = 0.f;     // Y <- g^{2L} Y + sum_b w_b^2 u_b (weights on the tile),
-            float *ysc = rsum();  // two row groups; rsum() is free until the M epilogue
-            if constexpr (NORM) {
+            // Y <- g^{2L} Y + sum_b w_b^2 u_b (weights already on the tile)
+            float ay = 0.f;
+            float *ysc = rsum();  // rsum is free until the M epilogue
+            if constexpr (NORM && !DECAY) {
+                // scratch: tS (S_p) is free once Q S_p has run
+                tile_colsums<false>(tU(), nullptr, L, 1.f, reinterpret_cast<float *>(tS()), Yrun(), gp(2 * L),
+                                    nullptr, 1.f);
+            } else if constexpr (NORM) {
+                // with decay tS holds W^2 U, read by the X update in flight: two row groups
                 const int i = tid % D, g = tid / D;
-                const uint8_t *ty = DECAY ? tS() : tU();
                 if (g < 2)
-                    for (int b = g; b < L; b += 2) ay += tile_load(ty, C, b, i);
+                    for (int b = g; b < L; b += 2) ay += tile_load(tS(), C, b, i);
                 if (g == 1) ysc[i] = ay;
             }
             if (!wait_mma()) return false;  // M and the S update
-            if constexpr (NORM) {
+            if constexpr (NORM && DECAY) {
                 if (tid < D) Yrun()[tid] = gp(2 * L) * Yrun()[tid] + (ay + ysc[tid]);
-                __syncthreads();  // rsum() is rewritten by the M epilogue
+                __syncthreads();  // rsum is rewritten by the M epilogue
             }
             // M = tril(Gamma2 o Q U^T) -> tA(), row sums for the denominator
             {
