@@ -254,7 +254,14 @@ HLA_DEVICE uint32_t tmem_warp_addr(uint32_t base, int warp, int col) {
 }
 
 // ---------------------------------------------------------------- math helpers
+// 2^y with the hardware approximation (PTX ex2.approx: relative error ~2^-22,
+// 2^-inf = 0).
+HLA_DEVICE float ex2_approx(float y) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+    return r;
+}
 // g^x for x >= 0 with g in [0,1]; lg = log2(g) (may be -inf).  0^0 = 1.
-HLA_DEVICE float gpow(float lg, float x) { return x == 0.f ? 1.f : exp2f(lg * x); }
+HLA_DEVICE float gpow(float lg, float x) { return x == 0.f ? 1.f : ex2_approx(lg * x); }
 
 }  // namespace hla

@@ -465,29 +465,38 @@ struct Kern {
     // (P = 1 for A-tilde, 2 for M).  Off-diagonal groups use one exp2 per group
     // and the factors g^{P j} held in gt.
     template <int POW>
-    __device__ __forceinline__ void mask_row(int row, int c0, float (&v)[16], const float (&gt)[16]) const {
+    __device__ __forceinline__ void mask_row(int row, int c0, float (&v)[16], const float (&gt)[3]) const {
         if (c0 > row) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = 0.f;
         } else if (c0 + 15 <= row) {
             if constexpr (DECAY) {
-                const float b = gp(POW * (row - c0 - 15));
+                // g^{P(row-c0-i)}: start at i = 15 and multiply by g^P towards i = 0
+                float f = gp(POW * (row - c0 - 15));
+                const float step = gt[POW];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] *= b * gt[15 - i];
+                for (int i = 15; i >= 0; --i) { v[i] *= f; f *= step; }
             }
-        } else {
+        } else {  // the group holding the diagonal: factor 1 on it, times g^P per column to the left
+            float f = 1.f;
+            const float step = gt[POW];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int dlt = row - c0 - i;
-                v[i] = dlt >= 0 ? (DECAY ? v[i] * gp(POW * dlt) : v[i]) : 0.f;
+            for (int i = 15; i >= 0; --i) {
+                const bool keep = (c0 + i <= row);
+                if constexpr (DECAY) {
+                    v[i] = keep ? v[i] * f : 0.f;
+                    f = keep ? f * step : f;
+                } else {
+                    v[i] = keep ? v[i] : 0.f;
+                }
             }
         }
     }
     // g^{P j}, j < 16, into registers (only with decay)
     template <int POW>
-    __device__ __forceinline__ void load_g16(float (&gt)[16]) const {
+    __device__ __forceinline__ void load_g16(float (&gt)[3]) const {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) gt[i] = DECAY ? g16()[(POW == 2 ? 16 : 0) + i] : 1.f;
+        for (int i = 0; i < 3; ++i) gt[i] = DECAY ? g16()[i] : 1.f;  // g^0, g^1, g^2
     }
 
     // Column sums over the rows r < L of one or two [C x D] tiles, for all threads.
@@ -575,7 +584,7 @@ struct Kern {
 
     // A-tilde = tril(Gamma1 o A) from TMEM W -> tA()
     __device__ void epi_atilde() {
-        float gt[16];
+        float gt[3];
         load_g16<1>(gt);
         for_row<C, C>(TW, [&](int c0, float (&v)[16]) {
             if (rowC < 0) return;
@@ -965,7 +974,7 @@ struct Kern {
             // M = tril(Gamma2 o Q U^T) -> tA(), row sums for the denominator
             {
                 float rs = 0.f;
-                float gt2[16];
+                float gt2[3];
                 load_g16<2>(gt2);
                 for_row<C, C>(TW, [&](int c0, float (&v)[16]) {
                     if (rowC < 0) return;
