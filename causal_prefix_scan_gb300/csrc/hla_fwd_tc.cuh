@@ -902,7 +902,6 @@ struct Kern {
         for (int jj = jb; jj < je; ++jj) {
             const int t0 = jj * C;
             const int L = min(C, P.n - t0);
-            if (K_::NSTAGE == 1 && jj != jb) tma_chunk(jj, 0);
             uint8_t *Q = sQ(stage), *Kt = sK(stage), *V = sV(stage);
             if (!wait_tma(stage)) return false;
             if (K_::NSTAGE == 2 && jj + 1 < je) tma_chunk(jj + 1, stage ^ 1);
@@ -992,6 +991,9 @@ struct Kern {
             commit();
             if (!wait_mma2()) return false;  // X, S updates and Q X_p
             if (!wait_mma()) return false;   // M V
+            // Q, K, V of this chunk are no longer read: with one input stage, start the
+            // next chunk's load now so that it overlaps the output epilogue
+            if (K_::NSTAGE == 1 && jj + 1 < je) tma_chunk(jj + 1, 0);
             {
                 const float g2t = (DECAY && rowC >= 0) ? gp(2 * (rowC + 1)) : 1.f;
                 float inv = 1.f;
