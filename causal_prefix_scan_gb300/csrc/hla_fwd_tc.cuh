@@ -30,9 +30,12 @@
 //   pass 1: the segment's own summary (S, C, X, m, Y from zero) -> workspace,
 //           then a release flag;
 //   scan:   the CTA folds state_in and the summaries of all earlier segments of
-//           its sequence (exclusive scan by the concatenation rule);
+//           its sequence (exclusive scan by the concatenation rule), in one
+//           pipelined pass whose only products, f S C_B, go to the tensor cores;
 //   pass 2: the chunk loop again from that exact prefix, writing O.
-// The last segment exports state_out (S, C, m, G = S C - X, h = S m - Y).
+// The last segment exports state_out (S, C, m, G = S C - X, h = S m - Y): C, m
+// (and Y without normalisation) before pass 2, the rest from the state that
+// pass 2 leaves at the sequence end.
 //
 // Each CTA: 256 threads (8 warps).  Thread 0 issues TMA and MMAs.  TMEM
 // epilogues: warp w reads lane quadrant w % 4 and column half w / 4 of an
@@ -76,14 +79,12 @@ struct TcParams {
     unsigned *ticket;   // workspace header: [0] ticket counter, [1] finished CTAs
     unsigned *flagsw;   // [BH][nseg] release flags
     float *summ;        // [BH][nseg][SUM] segment summaries
-    float *save;        // [BH][SAVE] prefix copy for the state export
     unsigned *err;
 };
 
 template <int C, int D, int DV>
 struct Cfg {
     static constexpr int SUM = D * D + 2 * D * DV + 2 * D;  // S, X, C, m, Y
-    static constexpr int SAVE = D * D + D * DV + 2 * D;     // S, X, m, Y
     // operand tiles (bytes)
     static constexpr int SZ_Q = C * D * 2, SZ_K = C * D * 2, SZ_V = C * DV * 2;
     static constexpr int SZ_TA = cmax(C * C, C * D) * 2;
@@ -92,7 +93,7 @@ struct Cfg {
     static constexpr int SZ_TQ = cmax(C * D, D * DV) * 2;
     static constexpr int SZ_IN = SZ_Q + SZ_K + SZ_V;  // one input stage
     static constexpr int WORK = SZ_TA + SZ_TU + SZ_TS + SZ_TQ;
-    // scan / export phase operands (alias the tiles)
+    // scan / export phase operands: S and C as bf16 hi + lo pairs (alias the tiles)
     static constexpr int FOLD = 2 * D * D * 2 + 2 * D * DV * 2;
     // TMEM slots
     static constexpr uint32_t TW = 0, TS = cmax(cmax(C, D), DV), TX = TS + D, T4 = TX + DV;
@@ -100,9 +101,9 @@ struct Cfg {
     static constexpr int CTAS = TCOLS <= 256 ? 2 : 1;
     // row partial sums: one slot per column part of an accumulator row
     static constexpr int NP_C = C == 128 ? 2 : 4, NP_D = D == 128 ? 2 : 4;
-    // fp32 vectors: m, Y [D]; a shared region R1 (scan: m_L [D] + row partials
-    // [NP_D x D]; pass 2: row sums [NP_C x C], q.Y [C]); g^j and g^{2j} for j < 16
-    static constexpr int R1 = cmax(D + NP_D * D, NP_C * C + C);
+    // fp32 vectors: m, Y [D]; pass 2's row sums [NP_C x C] and q.Y [C]; g^j and
+    // g^{2j} for j < 16
+    static constexpr int R1 = NP_C * C + C;
     static constexpr int NVEC = 2 * D + R1 + 32;
     static constexpr int SMALL = NVEC * 4 + 64;
     static constexpr int LIMIT = 227 * 1024;
@@ -111,7 +112,12 @@ struct Cfg {
     static constexpr int OFF_IN = 0;
     static constexpr int OFF_TA = NSTAGE * SZ_IN, OFF_TU = OFF_TA + SZ_TA, OFF_TS = OFF_TU + SZ_TU,
                          OFF_TQ = OFF_TS + SZ_TS, TILES = OFF_TQ + SZ_TQ;
-    static constexpr int ARENA = cmax(TILES, FOLD);
+    // two sets of scan operands when they fit in the tile arena
+    static constexpr int FBUF = 2 * FOLD <= TILES ? 2 : 1;
+    static constexpr int ARENA = cmax(TILES, FBUF * FOLD);
+    // scan / export: two sets of row partials [NP_D x D] after the operands
+    static constexpr int OFF_PART = FBUF * FOLD;
+    static_assert(OFF_PART + 2 * NP_D * D * 4 <= ARENA, "scan partials");
     static constexpr int OFF_VEC = ARENA;
     static constexpr int OFF_BAR = ARENA + NVEC * 4;
     static constexpr int SMEM = OFF_BAR + 64;
@@ -163,17 +169,20 @@ struct Kern {
     __device__ __forceinline__ uint8_t *tU() const { return base + K_::OFF_TU; }
     __device__ __forceinline__ uint8_t *tS() const { return base + K_::OFF_TS; }
     __device__ __forceinline__ uint8_t *tQ() const { return base + K_::OFF_TQ; }
-    __device__ __forceinline__ uint8_t *tShi() const { return base; }
-    __device__ __forceinline__ uint8_t *tSlo() const { return base + D * D * 2; }
-    __device__ __forceinline__ uint8_t *tChi() const { return base + 2 * D * D * 2; }
-    __device__ __forceinline__ uint8_t *tClo() const { return base + 2 * D * D * 2 + D * DV * 2; }
+    __device__ __forceinline__ uint8_t *fShi(int b) const { return base + b * K_::FOLD; }
+    __device__ __forceinline__ uint8_t *fSlo(int b) const { return fShi(b) + D * D * 2; }
+    __device__ __forceinline__ uint8_t *fChi(int b) const { return fShi(b) + 2 * D * D * 2; }
+    __device__ __forceinline__ uint8_t *fClo(int b) const { return fChi(b) + D * DV * 2; }
+    __device__ __forceinline__ uint8_t *tShi() const { return fShi(0); }
+    __device__ __forceinline__ uint8_t *tSlo() const { return fSlo(0); }
+    __device__ __forceinline__ uint8_t *tChi() const { return fChi(0); }
+    __device__ __forceinline__ uint8_t *tClo() const { return fClo(0); }
     __device__ __forceinline__ float *vec() const { return reinterpret_cast<float *>(base + K_::OFF_VEC); }
     __device__ __forceinline__ float *mrun() const { return vec(); }              // [D]
     __device__ __forceinline__ float *Yrun() const { return vec() + D; }          // [D]
-    __device__ __forceinline__ float *mL() const { return vec() + 2 * D; }        // scan: [D]
-    __device__ __forceinline__ float *part() const { return vec() + 3 * D; }      // scan: [NP_D x D]
-    __device__ __forceinline__ float *part0() const { return part(); }            // [D]
-    __device__ __forceinline__ float *part1() const { return part() + D; }        // [D]
+    __device__ __forceinline__ float *part(int b = 0) const {                     // scan: 2 x [NP_D x D]
+        return reinterpret_cast<float *>(base + K_::OFF_PART) + b * K_::NP_D * D;
+    }
     __device__ __forceinline__ float *rsum() const { return vec() + 2 * D; }      // pass 2: [NP_C x C]
     __device__ __forceinline__ float *den() const { return vec() + 2 * D + K_::NP_C * C; }  // pass 2: [C]
     __device__ __forceinline__ float *g16() const { return vec() + 2 * D + K_::R1; }  // g^j, g^{2j}
@@ -660,12 +669,55 @@ struct Kern {
         return true;
     }
 
-    // Write the TMEM/SMEM summary (S, X, C, m, Y) of this CTA to `dst`.
+    // ---- accumulator shares.  A thread owns row rowD of a [D x NC] state
+    // accumulator and share<NC>() consecutive columns of it, from share_col<NC>();
+    // share offset c (a multiple of 16) is column share_col<NC>() + c.
+    template <int NC>
+    __host__ __device__ static constexpr int share() { return D == 128 ? NC / 2 : NC / 4; }
+    template <int NC>
+    __device__ __forceinline__ int share_col() const {
+        return D == 128 ? half * (NC / 2) : half * (NC / 2) + (lane >> 4) * (NC / 4);
+    }
+    template <int NC>
+    __device__ __forceinline__ void ld_share(uint32_t slot, int c, float (&v)[16]) {
+        if constexpr (D == 128) tmem_ld16(taddr(slot, half * (NC / 2) + c), v);
+        else tmem_ld16x2<NC / 4>(taddr(slot, half * (NC / 2) + c), v);
+    }
+    template <int NC>
+    __device__ __forceinline__ void st_share(uint32_t slot, int c, const float (&v)[16]) {
+        if constexpr (D == 128) tmem_st16(taddr(slot, half * (NC / 2) + c), v);
+        else tmem_st16x2<NC / 4>(taddr(slot, half * (NC / 2) + c), v);
+    }
+    // Segment summaries keep each [D x NC] matrix in share order: the four values
+    // (r, c .. c+3) sit at float offset ((c / 4) D + r) 4, so the threads of a warp,
+    // which own consecutive rows, read and write consecutive 16-byte words.
+    static __device__ __forceinline__ int sofs(int r, int c) { return ((c >> 2) * D + r) * 4; }
+    static __device__ __forceinline__ void ld_sum16(const float *src, int r, int c, float *v) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+            const float4 a = ldcg4(src + sofs(r, c + i));
+            v[i] = a.x; v[i + 1] = a.y; v[i + 2] = a.z; v[i + 3] = a.w;
+        }
+    }
+    template <int NC>
+    __device__ void put_share(uint32_t slot, float *dst) {
+        constexpr int N = share<NC>();
+        float v[N];
+        const int c0 = share_col<NC>();
+#pragma unroll
+        for (int c = 0; c < N; c += 16) ld_share<NC>(slot, c, *reinterpret_cast<float(*)[16]>(v + c));
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < N; c += 4)
+            *reinterpret_cast<float4 *>(dst + sofs(rowD, c0 + c)) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+    }
+
+    // Write the summary (S, X, C, m, Y) of this CTA to `dst`.
     __device__ void store_summary(float *dst) {
         float *S = dst, *X = S + D * D, *Cc = X + D * DV, *m = Cc + D * DV, *Y = m + D;
-        for_row<D, D>(TS, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(S + rowD * D + c0, v); });
-        for_row<D, DV>(TX, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(X + rowD * DV + c0, v); });
-        for_row<D, DV>(T4, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(Cc + rowD * DV + c0, v); });
+        put_share<D>(TS, S);
+        put_share<DV>(TX, X);
+        put_share<DV>(T4, Cc);
         for (int i = tid; i < D; i += kThreads) { m[i] = mrun()[i]; Y[i] = Yrun()[i]; }
     }
 
@@ -727,96 +779,267 @@ struct Kern {
         return true;
     }
 
-    // prefix <- prefix (+) L, with L a summary (S, X, C, m, Y) and f = g^{len L}.
-    __device__ bool fold(const float *Lsum, float f) {
-        const float *SL = Lsum, *XL = SL + D * D, *CL = XL + D * DV, *mLg = CL + D * DV, *YL = mLg + D;
-        const float f2 = f * f;
-        for (int i = tid; i < D; i += kThreads) mL()[i] = __ldcg(mLg + i);
-        __syncthreads();
-        float sm = 0.f;
-        rmw_row<D, D>(TS, [&](int c0, float (&v)[16]) {
-            if (rowD < 0) return;
-            store_hilo(tShi(), tSlo(), D, rowD, c0, v);
-#pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-                const float4 s = ldcg4(SL + rowD * D + c0 + i);
-                sm += v[i] * mL()[c0 + i] + v[i + 1] * mL()[c0 + i + 1] + v[i + 2] * mL()[c0 + i + 2] +
-                      v[i + 3] * mL()[c0 + i + 3];
-                v[i] = f * v[i] + s.x; v[i + 1] = f * v[i + 1] + s.y;
-                v[i + 2] = f * v[i + 2] + s.z; v[i + 3] = f * v[i + 3] + s.w;
-            }
-        });
-        rmw_row<D, DV>(TX, [&](int c0, float (&v)[16]) {
-            if (rowD < 0) return;
-#pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-                const float4 s = ldcg4(XL + rowD * DV + c0 + i);
-                v[i] = f2 * v[i] + s.x; v[i + 1] = f2 * v[i + 1] + s.y;
-                v[i + 2] = f2 * v[i + 2] + s.z; v[i + 3] = f2 * v[i + 3] + s.w;
-            }
-        });
-        rmw_row<D, DV>(T4, [&](int c0, float (&v)[16]) {
-            if (rowD < 0) return;
-            float cl[16];
-#pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-                const float4 s = ldcg4(CL + rowD * DV + c0 + i);
-                cl[i] = f * s.x; cl[i + 1] = f * s.y; cl[i + 2] = f * s.z; cl[i + 3] = f * s.w;
-                v[i] = f * v[i] + s.x; v[i + 1] = f * v[i + 1] + s.y;
-                v[i + 2] = f * v[i + 2] + s.z; v[i + 3] = f * v[i + 3] + s.w;
-            }
-            store_hilo(tChi(), tClo(), D, rowD, c0, cl);
-        });
-        put_partial<D>(part(), rowD, sm);
-        publish();
-        if (tid == 0) {  // X += S_P (f C_L)
-            mma_ss(TX, tShi(), tChi(), true);
-            mma_ss(TX, tShi(), tClo(), true);
-            mma_ss(TX, tSlo(), tChi(), true);
-        }
-        commit();
-        for (int i = tid; i < D; i += kThreads) {
-            Yrun()[i] = f2 * Yrun()[i] + __ldcg(YL + i) + f * (sum_partials<D>(part(), i));
-            mrun()[i] = f * mrun()[i] + mL()[i];
-        }
-        return wait_mma();
-    }
-
-    // Spin (bounded) until segment j of this sequence has published its summary.
-    __device__ bool wait_flag(int j) {
+    // Spin (bounded) until segments j0 .. j1-1 of this sequence have published their
+    // summaries; the lanes of warp 0 poll the flags together.
+    __device__ bool wait_flags(int j0, int j1) {
         bool ok = true;
-        if (tid == 0) {
-            const unsigned *f = P.flagsw + (size_t)bh * P.nseg + j;
-            ok = false;
-            for (uint32_t it = 0; it < kWaitLimit; ++it) {
-                unsigned v;
-                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
-                if (v) { ok = true; break; }
-                if (it > 256) __nanosleep(128);
+        if (warp == 0) {
+            for (int j = j0 + lane; j < j1 && ok; j += 32) {
+                const unsigned *f = P.flagsw + (size_t)bh * P.nseg + j;
+                ok = false;
+                for (uint32_t it = 0; it < kWaitLimit; ++it) {
+                    unsigned v;
+                    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+                    if (v) { ok = true; break; }
+                    if (it > 256) __nanosleep(128);
+                }
             }
             if (!ok) atomicOr(P.err, DEV_TIMEOUT);
         }
         return !__syncthreads_or(!ok);
     }
 
-    // ======================================================================== export
-    // state_out from the prefix in TMEM (S, X, C, m, Y): G = S C - X, h = S m - Y.
-    __device__ bool export_state() {
-        float *So = P.sout.S + (size_t)bh * D * D, *Co = P.sout.C + (size_t)bh * D * DV;
-        float *mo = P.sout.m + (size_t)bh * D, *Go = P.sout.G + (size_t)bh * D * DV, *ho = P.sout.h + (size_t)bh * D;
-        float sm = 0.f;
-        for_row<D, D>(TS, [&](int c0, float (&v)[16]) {
-            if (rowD < 0) return;
-            store_hilo(tShi(), tSlo(), D, rowD, c0, v);
-            st_row16(So + rowD * D + c0, v);
+    __device__ bool wait_buf(int b) { return b == 0 ? wait_mma() : wait_mma2(); }
+    __device__ void commit_buf(int b) {
+        if (b == 0) commit();
+        else commit2();
+    }
+
+    // prefix <- prefix (+) L_0 (+) ... (+) L_{cnt-1}, for `cnt` summaries of full
+    // segments stored one after another at Lsum, each spanning `seg_tokens` tokens
+    // (decay factor f = g^seg_tokens).  One fold of a summary L into the prefix is
+    //   S <- f S + S_L,  C <- f C + C_L,  m <- f m + m_L,
+    //   X <- f^2 X + X_L + f S C_L,  Y <- f^2 Y + Y_L + f S m_L,
+    // with S the prefix before that fold.  Unrolled over the summaries, the product
+    // S C_L of step r reaches the result with weight f^{2(cnt-1-r)+1}.  The products
+    // accumulate, with that weight already on C_L, in the spare accumulator, which
+    // thus needs no rescaling between steps: step r+1 runs while the MMAs of step r
+    // do (two operand buffers when they fit), and its first loads are issued
+    // before those MMAs.  S, C and the product-free part of X are updated in place in TMEM; the
+    // sum of the products joins X at the end.  `zero_prefix`: the prefix is zero
+    // and TMEM / mrun() / Yrun() are not initialised; step 0 sets them.
+    __device__ bool fold_all(const float *Lsum, int cnt, int seg_tokens, bool zero_prefix) {
+        constexpr int NS = share<D>(), NV = share<DV>();
+        constexpr int GW = D == 128 ? 16 : 32;  // columns per load group (register budget)
+        constexpr int GS = NS < GW ? NS : GW, GV = NV < GW ? NV : GW;
+        constexpr int NG = cmax(NS / GS, NV / GV);
+        const int cs = share_col<D>(), cv = share_col<DV>();
+        const float f = gp(seg_tokens), f2 = f * f;
+        unsigned pend = 0u;  // bit b: MMAs committed to barrier b and not yet waited for
+        bool cross = false;  // the spare accumulator holds products
+        // one column group of a step: slices of S_L, m_L, C_L, X_L; m_L, Y_L entries
+        float s[GS], mv[GS], cl[GV], xl[GV];
+        float mLi = 0.f, YLi = 0.f;
+        auto load_s = [&](int r, int g) {  // S_L, m_L slices (and the vector entries)
+            const float *SL = Lsum + (size_t)r * K_::SUM, *mL = SL + D * D + 2 * D * DV;
+            if (g < NS / GS) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sm += v[i] * mrun()[c0 + i];
-        });
-        for_row<D, DV>(T4, [&](int c0, float (&v)[16]) {
-            if (rowD < 0) return;
-            store_hilo(tChi(), tClo(), D, rowD, c0, v);
-            st_row16(Co + rowD * DV + c0, v);
-        });
+                for (int c = 0; c < GS; c += 16) ld_sum16(SL, rowD, cs + g * GS + c, s + c);
+#pragma unroll
+                for (int c = 0; c < GS; c += 4) {
+                    const float4 a = ldcg4(mL + cs + g * GS + c);
+                    mv[c] = a.x; mv[c + 1] = a.y; mv[c + 2] = a.z; mv[c + 3] = a.w;
+                }
+            }
+            if (g == 0 && tid < D) {
+                mLi = __ldcg(mL + tid);
+                YLi = __ldcg(mL + D + tid);
+            }
+        };
+        auto load_v = [&](int r, int g) {  // C_L, X_L slices
+            const float *XL = Lsum + (size_t)r * K_::SUM + D * D, *CL = XL + D * DV;
+            if (g < NV / GV) {
+#pragma unroll
+                for (int c = 0; c < GV; c += 16) {
+                    ld_sum16(CL, rowD, cv + g * GV + c, cl + c);
+                    ld_sum16(XL, rowD, cv + g * GV + c, xl + c);
+                }
+            }
+        };
+        if (cnt > 0) load_s(0, 0);
+        for (int r = 0; r < cnt; ++r) {
+            const int b = K_::FBUF == 2 ? (r & 1) : 0;
+            const bool z = zero_prefix && r == 0;  // prefix zero: no TMEM reads, no product
+            const float coef = DECAY ? gp((2 * (cnt - 1 - r) + 1) * seg_tokens) : 1.f;
+            uint8_t *shi = fShi(b), *slo = fSlo(b), *chi = fChi(b), *clo = fClo(b);
+            float sm = 0.f;
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+                const bool hs = g < NS / GS, hv = g < NV / GV;
+                if (g > 0) load_s(r, g);
+                load_v(r, g);
+                // the operand buffer is free once the MMAs that read it have completed
+                if (g == 0 && (pend >> b & 1u)) {
+                    if (!wait_buf(b)) return false;
+                    pend &= ~(1u << b);
+                }
+                if (hs) {  // S: old value -> operand (hi + lo), S m_L row partials, update
+#pragma unroll
+                    for (int c = 0; c < GS; c += 16) {
+                        float v[16];
+                        if (!z) {
+                            ld_share<D>(TS, g * GS + c, v);
+                            tmem_wait_ld();
+                            store_hilo(shi, slo, D, rowD, cs + g * GS + c, v);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            sm += v[i] * mv[c + i];
+                            v[i] = f * v[i] + s[c + i];
+                        }
+                        st_share<D>(TS, g * GS + c, v);
+                    }
+                }
+                if (hv) {  // C: weighted C_L -> operand, update; X without the product
+#pragma unroll
+                    for (int c = 0; c < GV; c += 16) {
+                        float v[16], w[16];
+                        if (!z) {
+                            ld_share<DV>(T4, g * GV + c, v);
+                            ld_share<DV>(TX, g * GV + c, w);
+                            tmem_wait_ld();
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] = w[i] = 0.f;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            v[i] = f * v[i] + cl[c + i];
+                            w[i] = f2 * w[i] + xl[c + i];
+                            cl[c + i] *= coef;
+                        }
+                        if (!z) store_hilo(chi, clo, D, rowD, cv + g * GV + c, *reinterpret_cast<float(*)[16]>(cl + c));
+                        st_share<DV>(T4, g * GV + c, v);
+                        st_share<DV>(TX, g * GV + c, w);
+                    }
+                }
+            }
+            tmem_wait_st();
+            put_partial<D>(part(b), rowD, sm);
+            publish();
+            const float mLc = mLi, YLc = YLi;
+            if (r + 1 < cnt) load_s(r + 1, 0);  // in flight while the MMAs are issued
+            if (!z) {
+                if (tid == 0) {
+                    mma_ss(TW, shi, chi, cross);
+                    mma_ss(TW, shi, clo, true);
+                    mma_ss(TW, slo, chi, true);
+                }
+                commit_buf(b);
+                pend |= 1u << b;
+                cross = true;
+            }
+            if (tid < D) {
+                if (z) {
+                    Yrun()[tid] = YLc;
+                    mrun()[tid] = mLc;
+                } else {
+                    Yrun()[tid] = f2 * Yrun()[tid] + YLc + f * sum_partials<D>(part(b), tid);
+                    mrun()[tid] = f * mrun()[tid] + mLc;
+                }
+            }
+        }
+        if ((pend & 1u) && !wait_mma()) return false;
+        if ((pend & 2u) && !wait_mma2()) return false;
+        if (cross) {  // X += sum of the products
+            constexpr int N = share<DV>();
+#pragma unroll
+            for (int c = 0; c < N; c += 16) {
+                float v[16], w[16];
+                ld_share<DV>(TW, c, v);
+                ld_share<DV>(TX, c, w);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[i] += v[i];
+                st_share<DV>(TX, c, w);
+            }
+            tmem_wait_st();
+        }
+        tc_sync();
+        return true;
+    }
+
+    // ======================================================================== export
+    // state_out = prefix (+) own summary L (f = g^{len L}).  Pass 2 carries S, X
+    // (and Y with normalisation) of the prefix to the segment end, so those come
+    // from TMEM afterwards; C and m, which pass 2 does not carry, and Y without
+    // normalisation are combined here, before pass 2 moves the prefix on:
+    // C and m go to state_out, m also to mrun() and Y to Yrun(), which pass 2 leaves alone.
+    __device__ void export_pre(const float *Lown, float f) {
+        const float *SL = Lown, *XL = SL + D * D, *CL = XL + D * DV, *mL = CL + D * DV, *YL = mL + D;
+        (void)XL;
+        float *Co = P.sout.C + (size_t)bh * D * DV, *mo = P.sout.m + (size_t)bh * D;
+        constexpr int NV = share<DV>();
+        const int cv = share_col<DV>();
+#pragma unroll
+        for (int c = 0; c < NV; c += 16) {
+            float v[16], cl[16];
+            ld_sum16(CL, rowD, cv + c, cl);
+            ld_share<DV>(T4, c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = f * v[i] + cl[i];
+            st_row16(Co + rowD * DV + cv + c, v);
+        }
+        if constexpr (!NORM) {  // row partials of S_prefix m_L
+            constexpr int NS = share<D>();
+            const int cs = share_col<D>();
+            float sm = 0.f;
+#pragma unroll
+            for (int c = 0; c < NS; c += 16) {
+                float v[16];
+                ld_share<D>(TS, c, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; i += 4) {
+                    const float4 a = ldcg4(mL + cs + c + i);
+                    sm += v[i] * a.x + v[i + 1] * a.y + v[i + 2] * a.z + v[i + 3] * a.w;
+                }
+            }
+            put_partial<D>(part(), rowD, sm);
+        }
+        tc_sync();
+        if (tid < D) {
+            const float mLi = __ldcg(mL + tid);
+            if constexpr (!NORM)
+                Yrun()[tid] = f * f * Yrun()[tid] + __ldcg(YL + tid) + f * sum_partials<D>(part(), tid);
+            mrun()[tid] = mo[tid] = f * mrun()[tid] + mLi;
+        }
+        __syncthreads();
+    }
+
+    // After pass 2: G = S C - X and h = S m - Y from the final S, X (TMEM), m, Y
+    // (mrun(), Yrun()) and C (written to state_out by export_pre, read back here by
+    // the threads that wrote it); S, G, h go to state_out.
+    __device__ bool export_post() {
+        float *So = P.sout.S + (size_t)bh * D * D, *Co = P.sout.C + (size_t)bh * D * DV;
+        float *Go = P.sout.G + (size_t)bh * D * DV, *ho = P.sout.h + (size_t)bh * D;
+        constexpr int NS = share<D>(), NV = share<DV>();
+        const int cs = share_col<D>(), cv = share_col<DV>();
+        float sm = 0.f;
+#pragma unroll
+        for (int c = 0; c < NS; c += 16) {
+            float v[16];
+            ld_share<D>(TS, c, v);
+            tmem_wait_ld();
+            store_hilo(tShi(), tSlo(), D, rowD, cs + c, v);
+            st_row16(So + rowD * D + cs + c, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sm += v[i] * mrun()[cs + c + i];
+        }
+#pragma unroll
+        for (int c = 0; c < NV; c += 16) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+                const float4 a = *reinterpret_cast<const float4 *>(Co + rowD * DV + cv + c + i);
+                v[i] = a.x; v[i + 1] = a.y; v[i + 2] = a.z; v[i + 3] = a.w;
+            }
+            store_hilo(tChi(), tClo(), D, rowD, cv + c, v);
+        }
         put_partial<D>(part(), rowD, sm);
         publish();
         if (tid == 0) {  // W = S C
@@ -825,72 +1048,20 @@ struct Kern {
             mma_ss(TW, tSlo(), tChi(), true);
         }
         commit();
-        for (int i = tid; i < D; i += kThreads) {
-            mo[i] = mrun()[i];
-            ho[i] = sum_partials<D>(part(), i) - Yrun()[i];
-        }
+        if (tid < D) ho[tid] = sum_partials<D>(part(), tid) - Yrun()[tid];
         if (!wait_mma()) return false;
-        for_row2<D, DV>(TW, TX, [&](int c0, float (&sc)[16], float (&xv)[16]) {
-            if (rowD < 0) return;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sc[i] -= xv[i];
-            st_row16(Go + rowD * DV + c0, sc);
-        });
+        for (int c = 0; c < NV; c += 16) {
+            float v[16], w[16];
+            ld_share<DV>(TW, c, v);
+            ld_share<DV>(TX, c, w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] -= w[i];
+            st_row16(Go + rowD * DV + cv + c, v);
+        }
         return true;
     }
-
-    // Save / restore the parts of the prefix that pass 2 needs (S, X, m, Y).
-    __device__ void save_prefix(float *sv) {
-        float *S = sv, *X = S + D * D, *m = X + D * DV, *Y = m + D;
-        for_row<D, D>(TS, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(S + rowD * D + c0, v); });
-        for_row<D, DV>(TX, [&](int c0, float (&v)[16]) { if (rowD >= 0) st_row16(X + rowD * DV + c0, v); });
-        for (int i = tid; i < D; i += kThreads) { m[i] = mrun()[i]; Y[i] = Yrun()[i]; }
-    }
-    // Prefix <- a stored summary (S, X, C, m, Y): the fold of that summary into a
-    // zero prefix.
-    __device__ void load_summary(const float *src) {
-        const float *S = src, *X = S + D * D, *Cc = X + D * DV, *m = Cc + D * DV, *Y = m + D;
-        rmw_row<D, D>(TS, [&](int c0, float (&v)[16]) {
-#pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-                const float4 a = ldcg4(S + rowD * D + c0 + i);
-                v[i] = a.x; v[i + 1] = a.y; v[i + 2] = a.z; v[i + 3] = a.w;
-            }
-        });
-        rmw_row<D, DV>(TX, [&](int c0, float (&v)[16]) {
-#pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-                const float4 a = ldcg4(X + rowD * DV + c0 + i);
-                v[i] = a.x; v[i + 1] = a.y; v[i + 2] = a.z; v[i + 3] = a.w;
-            }
-        });
-        rmw_row<D, DV>(T4, [&](int c0, float (&v)[16]) {
-#pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-                const float4 a = ldcg4(Cc + rowD * DV + c0 + i);
-                v[i] = a.x; v[i + 1] = a.y; v[i + 2] = a.z; v[i + 3] = a.w;
-            }
-        });
-        for (int i = tid; i < D; i += kThreads) { mrun()[i] = __ldcg(m + i); Yrun()[i] = __ldcg(Y + i); }
-        tc_sync();
-    }
-
-    __device__ void restore_prefix(const float *sv) {
-        const float *S = sv, *X = S + D * D, *m = X + D * DV, *Y = m + D;
-        __syncthreads();
-        rmw_row<D, D>(TS, [&](int c0, float (&v)[16]) {
-            if (rowD >= 0)
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = S[rowD * D + c0 + i];
-        });
-        rmw_row<D, DV>(TX, [&](int c0, float (&v)[16]) {
-            if (rowD >= 0)
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = X[rowD * DV + c0 + i];
-        });
-        for (int i = tid; i < D; i += kThreads) { mrun()[i] = m[i]; Yrun()[i] = Y[i]; }
-    }
-
     // ======================================================================== pass 2
     // Outputs from the exact prefix.  Q S_p and Q X_p go to the spare columns so
     // that they overlap the epilogues; two completion barriers let the block work
@@ -1113,7 +1284,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
         if (!last || want_out) {
             if (!(ok = x.pass1(jb, je))) break;
             x.store_summary(P.summ + ((size_t)x.bh * P.nseg + seg) * K_::SUM);
-            __threadfence();
+            // the block barrier orders every thread's summary stores before the
+            // release store of the flag, which makes them visible at gpu scope
             __syncthreads();
             if (!last && x.tid == 0) {
                 unsigned *f = P.flagsw + (size_t)x.bh * P.nseg + seg;
@@ -1124,31 +1296,19 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        int j0 = 0;
-        if (!P.sin.S && seg > 0) {  // zero initial state: the prefix starts as segment 0's summary
-            if (!(ok = x.wait_flag(0))) break;
-            x.load_summary(P.summ + ((size_t)x.bh * P.nseg) * K_::SUM);
-            j0 = 1;
-        } else if (!(ok = x.prefix_init())) {
-            break;
+        if (P.sin.S || seg == 0) {
+            if (!(ok = x.prefix_init())) break;
         }
-        for (int j = j0; j < seg; ++j) {
-            if (!(ok = x.wait_flag(j))) break;
-            if (!(ok = x.fold(P.summ + ((size_t)x.bh * P.nseg + j) * K_::SUM, seg_pow(j)))) break;
+        if (seg > 0) {  // with a zero state_in the first fold step sets the prefix
+            if (!(ok = x.wait_flags(0, seg))) break;
+            if (!(ok = x.fold_all(P.summ + (size_t)x.bh * P.nseg * K_::SUM, seg, P.cps * C, !P.sin.S))) break;
         }
-        if (!ok) break;
-        // ---- state export from prefix (+) own summary
-        if (last && want_out) {
-            float *sv = P.save + (size_t)x.bh * K_::SAVE;
-            x.save_prefix(sv);
-            __threadfence_block();
-            if (!(ok = x.fold(P.summ + ((size_t)x.bh * P.nseg + seg) * K_::SUM, seg_pow(seg)))) break;
-            if (!(ok = x.export_state())) break;
-            x.restore_prefix(sv);
-            x.publish();
-        }
+        // ---- state export, part 1: what pass 2 does not carry to the segment end
+        if (last && want_out) x.export_pre(P.summ + ((size_t)x.bh * P.nseg + seg) * K_::SUM, seg_pow(seg));
         // ---- pass 2: outputs from the exact prefix
         if (!(ok = x.pass2(jb, je))) break;
+        // ---- state export, part 2: the final state at the sequence end
+        if (last && want_out && !(ok = x.export_post())) break;
     } while (0);
 
     tc_fence_before();
@@ -1204,17 +1364,16 @@ inline Plan make_plan(const hla_params &p, int num_sms) {
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-    size_t off_flags, off_summ, off_save, total;
+    size_t off_flags, off_summ, total;
 };
 inline WsLayout ws_layout(const hla_params &p, const Plan &pl) {
     const size_t BH = (size_t)p.B * p.H;
     const size_t D = p.d, DV = p.dv;
-    const size_t SUM = D * D + 2 * D * DV + 2 * D, SAVE = D * D + D * DV + 2 * D;
+    const size_t SUM = D * D + 2 * D * DV + 2 * D;
     WsLayout w;
     w.off_flags = 256;
     w.off_summ = align256(w.off_flags + BH * pl.nseg * 4);
-    w.off_save = align256(w.off_summ + BH * pl.nseg * SUM * 4);
-    w.total = align256(w.off_save + BH * SAVE * 4);
+    w.total = align256(w.off_summ + BH * pl.nseg * SUM * 4);
     return w;
 }
 
@@ -1238,7 +1397,6 @@ cudaError_t launch_cfg(const FwdArgs &a, cudaStream_t st, int num_sms) {
     P.ticket = reinterpret_cast<unsigned *>(ws);
     P.flagsw = reinterpret_cast<unsigned *>(ws + wl.off_flags);
     P.summ = reinterpret_cast<float *>(ws + wl.off_summ);
-    P.save = reinterpret_cast<float *>(ws + wl.off_save);
     P.err = a.err;
     auto kern = fwd_tc_kernel<C, D, DV, DECAY, NORM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K_::SMEM_LAUNCH);
