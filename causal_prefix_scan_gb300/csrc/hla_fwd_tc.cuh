@@ -24,18 +24,20 @@
 //   S  <- g^L S + K^T W K,  X <- g^{2L} X + U^T W^2 V,  C <- g^L C + Q^T W V,
 //   with W = diag(g^{L - tau}).
 //
-// Parallel structure (one launch): the (b,h) sequence is cut into `nseg`
-// segments of whole chunks; one CTA per (b,h,segment), CTAs ordered by a ticket
-// so that a CTA only ever waits for CTAs that started before it.
-//   pass 1: the segment's own summary (S, C, X, m, Y from zero) -> workspace,
+// Parallel structure (one launch): the chunks of all (b,h) sequences, laid end
+// to end, are cut into equal runs, one per CTA, as many CTAs as fit on the device
+// at once.  A run that crosses a sequence boundary holds a piece of each
+// sequence it touches.  CTAs take runs in ticket order, so a CTA only ever waits
+// for CTAs that started before it.
+//   pass 1: each piece's own summary (S, C, X, m, Y from zero) -> workspace,
 //           then a release flag;
-//   scan:   the CTA folds state_in and the summaries of all earlier segments of
-//           its sequence (exclusive scan by the concatenation rule), in one
-//           pipelined pass whose only products, f S C_B, go to the tensor cores;
+//   scan:   per piece, the CTA folds state_in and the summaries of all earlier
+//           pieces of its sequence (exclusive scan by the concatenation rule), in
+//           one pipelined pass whose only products, f S C_B, go to the tensor cores;
 //   pass 2: the chunk loop again from that exact prefix, writing O.
-// The last segment exports state_out (S, C, m, G = S C - X, h = S m - Y): C, m
-// (and Y without normalisation) before pass 2, the rest from the state that
-// pass 2 leaves at the sequence end.
+// The CTA holding a sequence's last piece exports state_out (S, C, m,
+// G = S C - X, h = S m - Y): C, m (and Y without normalisation) before pass 2,
+// the rest from the state that pass 2 leaves at the sequence end.
 //
 // Each CTA: 256 threads (8 warps).  Thread 0 issues TMA and MMAs.  TMEM
 // epilogues: warp w reads lane quadrant w % 4 and column half w / 4 of an
@@ -71,14 +73,21 @@ inline int ctas_per_sm(const hla_params &p) { return tmem_cols(p.chunk, p.d, p.d
 struct TcParams {
     CUtensorMap tmQ, tmK, tmV;
     int B, H, n, BH;
-    int nchunks, nseg, cps;
+    // work split: the BH sequences' chunks, laid end to end, are cut into runs of
+    // cpc chunks, one per CTA; a run that crosses a sequence boundary holds a
+    // piece of each sequence.  A sequence has at most kmax pieces.
+    int nchunks, cpc, kmax;
+    // > 0 when runs align with sequences (R runs each): tickets then go out level
+    // by level (piece 0 of every sequence, then piece 1, ...), so that the CTAs
+    // holding the last pieces, which fold the most, are the last to be placed
+    int runs_per_seq;
     float eps;
     const float *gamma;
     void *o;
     StatePtrs sin, sout;
     unsigned *ticket;   // workspace header: [0] ticket counter, [1] finished CTAs
-    unsigned *flagsw;   // [BH][nseg] release flags
-    float *summ;        // [BH][nseg][SUM] segment summaries
+    unsigned *flagsw;   // [BH][kmax] release flags
+    float *summ;        // [BH][kmax][SUM] piece summaries
     unsigned *err;
 };
 
@@ -779,13 +788,13 @@ struct Kern {
         return true;
     }
 
-    // Spin (bounded) until segments j0 .. j1-1 of this sequence have published their
+    // Spin (bounded) until pieces j0 .. j1-1 of this sequence have published their
     // summaries; the lanes of warp 0 poll the flags together.
     __device__ bool wait_flags(int j0, int j1) {
         bool ok = true;
         if (warp == 0) {
             for (int j = j0 + lane; j < j1 && ok; j += 32) {
-                const unsigned *f = P.flagsw + (size_t)bh * P.nseg + j;
+                const unsigned *f = P.flagsw + (size_t)bh * P.kmax + j;
                 ok = false;
                 for (uint32_t it = 0; it < kWaitLimit; ++it) {
                     unsigned v;
@@ -805,26 +814,30 @@ struct Kern {
         else commit2();
     }
 
-    // prefix <- prefix (+) L_0 (+) ... (+) L_{cnt-1}, for `cnt` summaries of full
-    // segments stored one after another at Lsum, each spanning `seg_tokens` tokens
-    // (decay factor f = g^seg_tokens).  One fold of a summary L into the prefix is
+    // prefix <- prefix (+) L_0 (+) ... (+) L_{cnt-1}, for the summaries of the first
+    // `cnt` pieces of this sequence, stored one after another at Lsum; piece r
+    // spans tokens [start(r), start(r+1)), with decay factor f_r = g^{len}.  One
+    // fold of a summary L (factor f) into the prefix is
     //   S <- f S + S_L,  C <- f C + C_L,  m <- f m + m_L,
     //   X <- f^2 X + X_L + f S C_L,  Y <- f^2 Y + Y_L + f S m_L,
     // with S the prefix before that fold.  Unrolled over the summaries, the product
-    // S C_L of step r reaches the result with weight f^{2(cnt-1-r)+1}.  The products
-    // accumulate, with that weight already on C_L, in the spare accumulator, which
-    // thus needs no rescaling between steps: step r+1 runs while the MMAs of step r
-    // do (two operand buffers when they fit), and its first loads are issued
-    // before those MMAs.  S, C and the product-free part of X are updated in place in TMEM; the
-    // sum of the products joins X at the end.  `zero_prefix`: the prefix is zero
-    // and TMEM / mrun() / Yrun() are not initialised; step 0 sets them.
-    __device__ bool fold_all(const float *Lsum, int cnt, int seg_tokens, bool zero_prefix) {
+    // S C_L of step r reaches the result with weight f_r F_r^2, F_r = g^{start(cnt)
+    // - start(r+1)} the decay from the end of piece r to the end of the last one.
+    // The products accumulate, with that weight already on C_L, in the spare
+    // accumulator, which thus needs no rescaling between steps: step r+1 runs while
+    // the MMAs of step r do (two operand buffers when they fit), and its first loads
+    // are issued before those MMAs.  S, C and the product-free part of X are updated
+    // in place in TMEM; the sum of the products joins X at the end.  `zero_prefix`:
+    // the prefix is zero and TMEM / mrun() / Yrun() are not initialised; step 0
+    // sets them.
+    template <typename Start>
+    __device__ bool fold_all(const float *Lsum, int cnt, Start &&start, bool zero_prefix) {
         constexpr int NS = share<D>(), NV = share<DV>();
         constexpr int GW = D == 128 ? 16 : 32;  // columns per load group (register budget)
         constexpr int GS = NS < GW ? NS : GW, GV = NV < GW ? NV : GW;
         constexpr int NG = cmax(NS / GS, NV / GV);
         const int cs = share_col<D>(), cv = share_col<DV>();
-        const float f = gp(seg_tokens), f2 = f * f;
+        const int t_end = start(cnt);
         unsigned pend = 0u;  // bit b: MMAs committed to barrier b and not yet waited for
         bool cross = false;  // the spare accumulator holds products
         // one column group of a step: slices of S_L, m_L, C_L, X_L; m_L, Y_L entries
@@ -860,7 +873,9 @@ struct Kern {
         for (int r = 0; r < cnt; ++r) {
             const int b = K_::FBUF == 2 ? (r & 1) : 0;
             const bool z = zero_prefix && r == 0;  // prefix zero: no TMEM reads, no product
-            const float coef = DECAY ? gp((2 * (cnt - 1 - r) + 1) * seg_tokens) : 1.f;
+            const int len = start(r + 1) - start(r);
+            const float f = gp(len), f2 = f * f;
+            const float coef = DECAY ? gp(len + 2 * (t_end - start(r + 1))) : 1.f;
             uint8_t *shi = fShi(b), *slo = fSlo(b), *chi = fChi(b), *clo = fClo(b);
             float sm = 0.f;
 #pragma unroll
@@ -1199,7 +1214,7 @@ __device__ __forceinline__ void finish_cta(const TcParams &P) {
     __threadfence();
     const unsigned done = atomicAdd(P.ticket + 1, 1u);
     if (done == gridDim.x - 1) {
-        for (int i = 0; i < P.BH * P.nseg; ++i) P.flagsw[i] = 0u;
+        for (int i = 0; i < P.BH * P.kmax; ++i) P.flagsw[i] = 0u;
         P.ticket[0] = 0u;
         P.ticket[1] = 0u;
         __threadfence();
@@ -1256,59 +1271,92 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
         tmem_relinquish();
     }
     const int ticket = *ticket_p;
-    const int seg = ticket / P.BH;
-    x.bh = ticket % P.BH;
-    const int h = x.bh % P.H;
-    float g = 1.f;
-    if constexpr (DECAY) g = P.gamma[h];
-    x.lg = log2f(g);
-    if (x.tid < 32) x.g16()[x.tid] = DECAY ? gpow(x.lg, (float)((x.tid & 15) * (x.tid < 16 ? 1 : 2))) : 1.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     x.tb = *tmem_base_p;
-
-    const int jb = seg * P.cps;
-    const int je = min(P.nchunks, jb + P.cps);
-    const bool last = (seg == P.nseg - 1);
     const bool want_out = P.sout.S != nullptr;
     x.need_mY = NORM || want_out;
-    auto seg_len = [&](int s) {  // tokens in segment s
-        const int b0 = s * P.cps * C;
-        return min(P.n, (s + 1) * P.cps * C) - b0;
+
+    // This CTA's run of chunks [g0, g1) in the end-to-end order of all sequences,
+    // and the pieces it holds: one per sequence that the run touches.  Pieces of a
+    // sequence get increasing tickets in either ticket order.
+    const long long NC = P.nchunks;
+    const int run = P.runs_per_seq > 0 ? (ticket % P.BH) * P.runs_per_seq + ticket / P.BH : ticket;
+    const long long g0 = (long long)run * P.cpc;
+    const long long g1 = min((long long)P.BH * NC, g0 + P.cpc);
+    const int bh_lo = (int)(g0 / NC), bh_hi = (int)((g1 - 1) / NC);
+    struct Piece {
+        int jb, je, k;  // chunks [jb, je) of the sequence; piece index k within it
+        long long first_run;
+        bool last;      // the sequence's last piece
     };
-    auto seg_pow = [&](int s) { return DECAY ? gpow(x.lg, (float)seg_len(s)) : 1.f; };
-    bool ok = true;
-    do {
-        // ---- pass 1: own summary (needed by later segments, and by the export)
-        if (!last || want_out) {
-            if (!(ok = x.pass1(jb, je))) break;
-            x.store_summary(P.summ + ((size_t)x.bh * P.nseg + seg) * K_::SUM);
-            // the block barrier orders every thread's summary stores before the
-            // release store of the flag, which makes them visible at gpu scope
-            __syncthreads();
-            if (!last && x.tid == 0) {
-                unsigned *f = P.flagsw + (size_t)x.bh * P.nseg + seg;
-                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
-            }
-        }
-        // ---- exclusive scan: prefix = state_in (+) L_0 (+) ... (+) L_{seg-1}
+    auto piece = [&](int bh) {
+        Piece pc;
+        pc.jb = (int)(max(g0, bh * NC) - bh * NC);
+        pc.je = (int)(min(g1, (bh + 1) * NC) - bh * NC);
+        pc.first_run = (bh * NC) / P.cpc;
+        pc.k = (int)(run - pc.first_run);
+        pc.last = (pc.je == P.nchunks);
+        return pc;
+    };
+    // Select sequence bh: its decay constant and the table of g^j, g^{2j}, j < 16.
+    x.bh = -1;
+    auto select = [&](int bh) {
+        if (bh == x.bh) return;
+        __syncthreads();  // every thread is done with the previous sequence's table
+        x.bh = bh;
+        float g = 1.f;
+        if constexpr (DECAY) g = P.gamma[bh % P.H];
+        x.lg = log2f(g);
+        if (x.tid < 32) x.g16()[x.tid] = DECAY ? gpow(x.lg, (float)((x.tid & 15) * (x.tid < 16 ? 1 : 2))) : 1.f;
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (P.sin.S || seg == 0) {
-            if (!(ok = x.prefix_init())) break;
+    };
+    bool ok = true;
+    do {
+        // ---- phase 1: the summary of every piece that a later piece, or the
+        // export, needs; a release flag publishes it to later pieces
+        for (int bh = bh_lo; bh <= bh_hi && ok; ++bh) {
+            const Piece pc = piece(bh);
+            if (pc.last && !want_out) continue;
+            select(bh);
+            if (!(ok = x.pass1(pc.jb, pc.je))) break;
+            x.store_summary(P.summ + ((size_t)bh * P.kmax + pc.k) * K_::SUM);
+            // the block barrier orders every thread's summary stores before the
+            // release store of the flag, which makes them visible at gpu scope
+            __syncthreads();
+            if (!pc.last && x.tid == 0) {
+                unsigned *f = P.flagsw + (size_t)bh * P.kmax + pc.k;
+                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
+            }
         }
-        if (seg > 0) {  // with a zero state_in the first fold step sets the prefix
-            if (!(ok = x.wait_flags(0, seg))) break;
-            if (!(ok = x.fold_all(P.summ + (size_t)x.bh * P.nseg * K_::SUM, seg, P.cps * C, !P.sin.S))) break;
+        if (!ok) break;
+        // ---- phase 2, per piece: exclusive scan (prefix = state_in (+) the
+        // summaries of the sequence's earlier pieces), then the outputs
+        for (int bh = bh_lo; bh <= bh_hi && ok; ++bh) {
+            const Piece pc = piece(bh);
+            select(bh);
+            // first token of piece r of this sequence
+            auto start = [&](int r) -> int {
+                return r == 0 ? 0 : (int)(((pc.first_run + r) * P.cpc - bh * NC) * C);
+            };
+            if (P.sin.S || pc.k == 0) {
+                if (!(ok = x.prefix_init())) break;
+            }
+            if (pc.k > 0) {  // with a zero state_in the first fold step sets the prefix
+                if (!(ok = x.wait_flags(0, pc.k))) break;
+                if (!(ok = x.fold_all(P.summ + (size_t)bh * P.kmax * K_::SUM, pc.k, start, !P.sin.S))) break;
+            }
+            // ---- state export, part 1: what pass 2 does not carry to the sequence end
+            if (pc.last && want_out)
+                x.export_pre(P.summ + ((size_t)bh * P.kmax + pc.k) * K_::SUM,
+                             DECAY ? gpow(x.lg, (float)(P.n - start(pc.k))) : 1.f);
+            if (!(ok = x.pass2(pc.jb, pc.je))) break;
+            // ---- state export, part 2: the final state at the sequence end
+            if (pc.last && want_out && !(ok = x.export_post())) break;
         }
-        // ---- state export, part 1: what pass 2 does not carry to the segment end
-        if (last && want_out) x.export_pre(P.summ + ((size_t)x.bh * P.nseg + seg) * K_::SUM, seg_pow(seg));
-        // ---- pass 2: outputs from the exact prefix
-        if (!(ok = x.pass2(jb, je))) break;
-        // ---- state export, part 2: the final state at the sequence end
-        if (last && want_out && !(ok = x.export_post())) break;
     } while (0);
 
     tc_fence_before();
@@ -1345,19 +1393,23 @@ inline bool encode_3d(CUtensorMap *tm, const void *ptr, int width, int n, int BH
 }
 
 struct Plan {
-    int nchunks, nseg, cps;
+    int nchunks;  // chunks per sequence
+    int cpc;      // chunks per CTA (a run in the end-to-end order of all sequences)
+    int ncta;     // CTAs: at most the number that fit on the device at once
+    int kmax;     // upper bound on the pieces (runs touched) of one sequence
 };
 inline Plan make_plan(const hla_params &p, int num_sms) {
     Plan pl;
-    const int BH = p.B * p.H;
+    const long long BH = (long long)p.B * p.H;
     pl.nchunks = (p.n + p.chunk - 1) / p.chunk;
-    int nseg = num_sms * ctas_per_sm(p) / (BH > 0 ? BH : 1);
-    nseg = nseg < 1 ? 1 : nseg;
-    if (nseg > pl.nchunks) nseg = pl.nchunks > 0 ? pl.nchunks : 1;
-    pl.cps = (pl.nchunks + nseg - 1) / nseg;
-    if (pl.cps < 1) pl.cps = 1;
-    pl.nseg = (pl.nchunks + pl.cps - 1) / pl.cps;
-    if (pl.nseg < 1) pl.nseg = 1;
+    const long long total = BH * pl.nchunks;
+    const long long slots = (long long)num_sms * ctas_per_sm(p);
+    long long cpc = (total + slots - 1) / (slots > 0 ? slots : 1);
+    if (cpc < 1) cpc = 1;
+    pl.cpc = (int)cpc;
+    pl.ncta = (int)((total + cpc - 1) / cpc);
+    if (pl.ncta < 1) pl.ncta = 1;
+    pl.kmax = (pl.nchunks + pl.cpc - 1) / pl.cpc + 1;
     return pl;
 }
 
@@ -1372,8 +1424,8 @@ inline WsLayout ws_layout(const hla_params &p, const Plan &pl) {
     const size_t SUM = D * D + 2 * D * DV + 2 * D;
     WsLayout w;
     w.off_flags = 256;
-    w.off_summ = align256(w.off_flags + BH * pl.nseg * 4);
-    w.total = align256(w.off_summ + BH * pl.nseg * SUM * 4);
+    w.off_summ = align256(w.off_flags + BH * pl.kmax * 4);
+    w.total = align256(w.off_summ + BH * pl.kmax * SUM * 4);
     return w;
 }
 
@@ -1390,7 +1442,8 @@ cudaError_t launch_cfg(const FwdArgs &a, cudaStream_t st, int num_sms) {
         !encode_3d(&P.tmV, a.v, DV, a.n, BH, C))
         return cudaErrorInvalidValue;
     P.B = a.B; P.H = a.H; P.n = a.n; P.BH = BH;
-    P.nchunks = pl.nchunks; P.nseg = pl.nseg; P.cps = pl.cps;
+    P.nchunks = pl.nchunks; P.cpc = pl.cpc; P.kmax = pl.kmax;
+    P.runs_per_seq = pl.nchunks % pl.cpc == 0 ? pl.nchunks / pl.cpc : 0;
     P.eps = a.eps; P.gamma = a.gamma;
     P.o = a.o; P.sin = a.sin; P.sout = a.sout;
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
@@ -1401,7 +1454,7 @@ cudaError_t launch_cfg(const FwdArgs &a, cudaStream_t st, int num_sms) {
     auto kern = fwd_tc_kernel<C, D, DV, DECAY, NORM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K_::SMEM_LAUNCH);
     if (e != cudaSuccess) return e;
-    kern<<<BH * pl.nseg, kThreads, K_::SMEM_LAUNCH, st>>>(P);
+    kern<<<pl.ncta, kThreads, K_::SMEM_LAUNCH, st>>>(P);
     return cudaGetLastError();
 }
 

@@ -83,12 +83,30 @@ def test_tc_short_sequences(n):
 
 
 def test_tc_many_pairs_single_segment():
-    # B*H above the SM count: one segment per sequence, several waves of CTAs
+    # B*H above the SM count: each CTA's run holds several whole sequences
     w = small("wide", B=20, H=10, n=150, d=64, dv=64)
     x = W.make_inputs(w)
     o, st = run_forward(x, "bf16", 64)
     o_ref, st_ref = run_oracle(x)
     assert_parity(o, o_ref, st, st_ref, what="B*H=200")
+
+
+@pytest.mark.parametrize("B,H,n,chunk,d,dv,decay,normalize", [
+    (1, 3, 8192, 64, 64, 128, False, True),    # long sequences; runs end inside sequences
+    (2, 40, 200, 64, 64, 128, True, False),    # 4 chunks per sequence, runs of a few chunks
+    (1, 400, 40, 64, 64, 64, True, True),      # one chunk per sequence: runs of several whole sequences
+    (1, 7, 4990, 128, 128, 128, True, False),  # 39 chunks per sequence
+])
+def test_tc_runs_cross_sequences(B, H, n, chunk, d, dv, decay, normalize):
+    # The chunks of all sequences, end to end, are split into equal runs, one per
+    # CTA; with these sizes (and any SM count) some runs hold pieces of two or more
+    # sequences, and some sequences start or end inside a run.
+    w = small("runs", B=B, H=H, n=n, chunk=chunk, d=d, dv=dv, decay=decay, qk="elu1" if normalize else "l2",
+              gamma_lo=0.9, gamma_hi=0.999)
+    x = W.make_inputs(w)
+    o, st = run_forward(x, "bf16", chunk, normalize=normalize, eps=1e-6)
+    o_ref, st_ref = run_oracle(x, normalize=normalize, eps=1e-6)
+    assert_parity(o, o_ref, st, st_ref, what=f"runs B{B}H{H}n{n}")
 
 
 def test_empty_sequence_passes_state_through():
