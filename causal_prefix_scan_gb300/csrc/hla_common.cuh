@@ -75,6 +75,19 @@ HLA_DEVICE void tma_load_3d(void *dst, const void *tmap, uint64_t *bar, int c0, 
         : "memory");
 }
 
+// 3-D tiled store of a shared-memory tile (coordinates innermost first); rows
+// outside the tensor are not written.  Tracked by the issuing thread's bulk groups.
+HLA_DEVICE void tma_store_3d(const void *src, const void *tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+HLA_DEVICE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the issuing thread's bulk stores have read their shared-memory source ...
+HLA_DEVICE void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... or have completed.
+HLA_DEVICE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Make generic-proxy shared-memory writes visible to the async proxy (tensor cores, TMA).
 HLA_DEVICE void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 

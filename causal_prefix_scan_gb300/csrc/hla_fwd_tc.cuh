@@ -71,7 +71,7 @@ __host__ __device__ constexpr int tmem_cols(int C, int D, int DV) {
 inline int ctas_per_sm(const hla_params &p) { return tmem_cols(p.chunk, p.d, p.dv) <= 256 ? 2 : 1; }
 
 struct TcParams {
-    CUtensorMap tmQ, tmK, tmV;
+    CUtensorMap tmQ, tmK, tmV, tmO;
     int B, H, n, BH;
     // work split: the BH sequences' chunks, laid end to end, are cut into runs of
     // cpc chunks, one per CTA; a run that crosses a sequence boundary holds a
@@ -1082,13 +1082,13 @@ struct Kern {
     // that they overlap the epilogues; two completion barriers let the block work
     // on one group of MMA results while the next group runs.
     __device__ bool pass2(int jb, int je) {
-        __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(P.o) + (size_t)bh * P.n * DV;
         int stage = 0;
         tma_chunk(jb, 0);
         for (int jj = jb; jj < je; ++jj) {
             const int t0 = jj * C;
             const int L = min(C, P.n - t0);
             uint8_t *Q = sQ(stage), *Kt = sK(stage), *V = sV(stage);
+            if (tid == 0) bulk_wait_read();  // the previous chunk's O store has left tS()
             if (!wait_tma(stage)) return false;
             if (K_::NSTAGE == 2 && jj + 1 < je) tma_chunk(jj + 1, stage ^ 1);
             if (tid == 0) mma_kk<C, D>(TW, Q, Kt, false);  // A = Q K^T
@@ -1186,23 +1186,25 @@ struct Kern {
                 if constexpr (NORM) {
                     if (rowC >= 0) inv = 1.f / (sum_partials<C>(rsum(), rowC) + g2t * den()[rowC] + P.eps);
                 }
+                // O tile -> tS() (free: its last reader, the X update, has completed),
+                // then one TMA store; rows past the sequence end are not written
                 for_row2<C, DV>(TW, T4, [&](int c0, float (&v)[16], float (&sp)[16]) {
-                    if (rowC < 0 || rowC >= L) return;
+                    if (rowC < 0) return;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] = (v[i] + g2t * sp[i]) * inv;
-                    uint4 a, b;
-                    a.x = pack_bf16(v[0], v[1]); a.y = pack_bf16(v[2], v[3]);
-                    a.z = pack_bf16(v[4], v[5]); a.w = pack_bf16(v[6], v[7]);
-                    b.x = pack_bf16(v[8], v[9]); b.y = pack_bf16(v[10], v[11]);
-                    b.z = pack_bf16(v[12], v[13]); b.w = pack_bf16(v[14], v[15]);
-                    uint4 *dst = reinterpret_cast<uint4 *>(O + (size_t)(t0 + rowC) * DV + c0);
-                    dst[0] = a;
-                    dst[1] = b;
+                    tile_store_row16(tS(), C, rowC, c0, v);
                 });
             }
-            tc_sync();  // all TMEM reads of W and the spare done before the next chunk's MMAs
+            publish();  // tile writes visible to the TMA; TMEM reads of W and the spare done
+            if (tid == 0) {
+#pragma unroll
+                for (int kb = 0; kb < DV / 64; ++kb) tma_store_3d(tS() + kb * C * 128, &P.tmO, kb * 64, t0, bh);
+                bulk_commit();
+            }
             stage ^= (K_::NSTAGE - 1);
         }
+        if (tid == 0) bulk_wait_read();  // tS() and the arena are free again after this barrier
+        __syncthreads();
         return true;
     }
 };
@@ -1256,6 +1258,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
         tma_prefetch_desc(&P.tmQ);
         tma_prefetch_desc(&P.tmK);
         tma_prefetch_desc(&P.tmV);
+        tma_prefetch_desc(&P.tmO);
         *ticket_p = (int)atomicAdd(P.ticket, 1u);
     }
     __syncthreads();
@@ -1363,7 +1366,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
     __syncthreads();
     tc_fence_after();
     if (x.warp == 0) tmem_dealloc(x.tb, K_::TCOLS);
-    if (x.tid == 0) finish_cta(P);
+    if (x.tid == 0) {
+        bulk_wait_all();  // the output stores are complete before the CTA counts itself done
+        finish_cta(P);
+    }
 }
 
 // ============================================================================ host side
@@ -1439,7 +1445,7 @@ cudaError_t launch_cfg(const FwdArgs &a, cudaStream_t st, int num_sms) {
     memset(&P, 0, sizeof P);
     const int BH = a.B * a.H;
     if (!encode_3d(&P.tmQ, a.q, D, a.n, BH, C) || !encode_3d(&P.tmK, a.k, D, a.n, BH, C) ||
-        !encode_3d(&P.tmV, a.v, DV, a.n, BH, C))
+        !encode_3d(&P.tmV, a.v, DV, a.n, BH, C) || !encode_3d(&P.tmO, a.o, DV, a.n, BH, C))
         return cudaErrorInvalidValue;
     P.B = a.B; P.H = a.H; P.n = a.n; P.BH = BH;
     P.nchunks = pl.nchunks; P.cpc = pl.cpc; P.kmax = pl.kmax;
