@@ -210,9 +210,13 @@ def cpu_baseline_forward(w: W.Workload, x):
         if rows > max(1, -(-cores // w.H)):
             secs, toks = oracle_rate(w, x, rows, w.n, min(cores, rows * w.H))
     used = min(cores, rows * w.H)
+    reps = 1
+    if secs < 5.0:  # a quick sample is repeated to about 10 s for a stable rate
+        reps = max(2, min(500, int(10.0 / max(secs, 1e-9))))
+        secs = (secs + sum(oracle_rate(w, x, rows, w.n, used)[0] for _ in range(reps - 1))) / reps
     return {"value": toks / secs, "unit": "tokens/s", "cores": used, "kind": "oracle",
             "sample": f"fp64 serial recurrence over {rows} of {w.B} batch row(s) x {w.H} heads x {w.n} tokens "
-                      f"of the same inputs, threads over (b,h)", "seconds": secs}
+                      f"of the same inputs, threads over (b,h); mean of {reps} run(s)", "seconds": secs}
 
 
 # ----------------------------------------------------------------- forward bench
@@ -306,35 +310,57 @@ def bench_forward(args, w: W.Workload, rank, world, local, dist):
     ms_per_step = t_max / K
     value = world * w.tokens * K / (t_max / 1e3)
 
-    # ---- end to end: host buffers, copies inside the timed region
+    # ---- end to end: host buffers, copies inside the timed region.  Every step
+    # copies its q, k, v from pinned host memory and reads its o back; as a
+    # streaming caller would, step i+1's upload and step i-1's download run on
+    # their own streams while step i computes (two device buffer sets).
     Ke = min(K, 200)
-    q, k, v, o = sets[0]
-    o_host = torch.empty(o.shape, dtype=tdt).pin_memory()
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            q.copy_(host["q"], non_blocking=True); k.copy_(host["k"], non_blocking=True)
-            v.copy_(host["v"], non_blocking=True)
+    o_host = [torch.empty(sets[0][3].shape, dtype=tdt).pin_memory() for _ in range(2)]
+    bufs = [sets[b % nsets] for b in range(2)] if nsets >= 2 else \
+        [sets[0], tuple(torch.empty_like(t) for t in sets[0])]
+    s_up, s_down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = {kk: [torch.cuda.Event() for _ in range(2)] for kk in ("up", "fwd", "down")}
+
+    def e2e_steps(n):
+        for i in range(n):
+            b = i % 2
+            q, k, v, o = bufs[b]
+            if i >= 2:
+                s_up.wait_event(ev["fwd"][b])       # step i-2 has finished reading buffer b
+            with torch.cuda.stream(s_up):
+                q.copy_(host["q"], non_blocking=True); k.copy_(host["k"], non_blocking=True)
+                v.copy_(host["v"], non_blocking=True)
+            ev["up"][b].record(s_up)
+            stream.wait_event(ev["up"][b])
+            if i >= 2:
+                stream.wait_event(ev["down"][b])    # o of step i-2 has been read back
             hla.hla_forward_chunked(params, q, k, v, o, None, st, ws, ws_bytes, stream)
-            o_host.copy_(o, non_blocking=True)
-    stream.synchronize()
+            ev["fwd"][b].record(stream)
+            s_down.wait_event(ev["fwd"][b])
+            with torch.cuda.stream(s_down):
+                o_host[b].copy_(o, non_blocking=True)
+            ev["down"][b].record(s_down)
+        stream.wait_stream(s_up)
+        stream.wait_stream(s_down)
+
+    e2e_steps(3)
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(Ke):
-            q.copy_(host["q"], non_blocking=True); k.copy_(host["k"], non_blocking=True)
-            v.copy_(host["v"], non_blocking=True)
-            hla.hla_forward_chunked(params, q, k, v, o, None, st, ws, ws_bytes, stream)
-            o_host.copy_(o, non_blocking=True)
-        e1.record(stream)
+    e0.record(stream)
+    s_up.wait_stream(stream)
+    s_down.wait_stream(stream)
+    e2e_steps(Ke)
+    e1.record(stream)
     stream.synchronize()
     barrier(dist)
     hla.hla_sync_status(stream)
     te = max_over_ranks(dist, e0.elapsed_time(e1))
     e2e = {"value": world * w.tokens * Ke / (te / 1e3), "unit": "tokens/s",
            "h2d_bytes_per_step": int(sum(host[n].numel() * host[n].element_size() for n in ("q", "k", "v"))),
-           "d2h_bytes_per_step": int(o_host.numel() * o_host.element_size()), "steps": Ke}
+           "d2h_bytes_per_step": int(o_host[0].numel() * o_host[0].element_size()), "steps": Ke,
+           "overlap": "upload of step i+1 and download of step i-1 on their own streams during step i"}
 
     # ---- roofline of the (only) kernel of the step
     peaks, peak_kind = load_peaks()
