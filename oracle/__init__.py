@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for masked second-order Higher-order Linear Attention.
+"""fp64 CPU oracle for second-order Higher-order Linear Attention (masked and unmasked).
 
 TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``, ``__graft_entry__.smoke()``
 and the CPU-baseline leg of ``bench.py`` may import this package.  The CUDA library
@@ -16,7 +16,11 @@ inputs, n = 1 / d = 1 / decay 0 / decay 1 special cases, chunk-size invariance o
 the chunked scan, associativity and identity of segment concatenation, strict
 causality, split resume, and the unmasked identity.  The decay variant's formula is
 not printed on the pages; its pins are internal consistency only (see the decay
-reading in hla_oracle.c).
+reading in hla_oracle.c).  The unmasked variant (o_t = q_t^T S_t C_t, skill card
+"Higher-order linear attention", bullet "Streaming Computation") is pinned by an
+all-pairs brute force, the dense form [L o ((L o QK^T)(QK^T)^T)]V, its relation to the
+masked output through G, chunk invariance, resume and decode continuation; shared
+key/value heads (bullet "Multi-Head Support") by equality with repeated heads.
 """
 from __future__ import annotations
 
@@ -53,9 +57,9 @@ def _load():
         dp = ctypes.POINTER(ctypes.c_double)
         i = ctypes.c_int
         d = ctypes.c_double
-        _lib.hla_oracle_forward.argtypes = [i, i, i, i, i, dp, dp, dp, dp, i, d] + [dp] * 5 + [dp] + [dp] * 5 + [i]
-        _lib.hla_oracle_forward_chunked.argtypes = [i, i, i, i, i, i, dp, dp, dp, dp, i, d] + [dp] * 5 + [dp] + [dp] * 5 + [i]
-        _lib.hla_oracle_decode_step.argtypes = [i, i, i, i, dp, i, d] + [dp] * 5 + [dp, dp, dp, dp, i]
+        _lib.hla_oracle_forward.argtypes = [i] * 7 + [dp, dp, dp, dp, i, d] + [dp] * 5 + [dp] + [dp] * 5 + [i]
+        _lib.hla_oracle_forward_chunked.argtypes = [i] * 8 + [dp, dp, dp, dp, i, d] + [dp] * 5 + [dp] + [dp] * 5 + [i]
+        _lib.hla_oracle_decode_step.argtypes = [i] * 6 + [dp, i, d] + [dp] * 5 + [dp, dp, dp, dp, i]
         _lib.hla_oracle_combine.argtypes = [i, i, i] + [dp] * 10 + [dp] + [dp] * 5
         for f in (_lib.hla_oracle_forward, _lib.hla_oracle_forward_chunked,
                   _lib.hla_oracle_decode_step, _lib.hla_oracle_combine):
@@ -117,17 +121,20 @@ def default_threads() -> int:
 
 
 def forward(q, k, v, gamma=None, normalize=False, eps=0.0, state_in=None,
-            want_state=True, chunk=None, nthreads=None):
-    """Masked 2nd-order HLA forward in fp64.
+            want_state=True, chunk=None, nthreads=None, unmasked=False):
+    """2nd-order HLA forward in fp64, masked (default) or unmasked.
 
-    q, k: [B,H,n,d]; v: [B,H,n,dv]; gamma: [H] or None.  chunk=None runs the serial
-    recurrence; chunk=c runs the chunked scan (per-chunk summaries folded with the
-    segment-concatenation rule).  Returns (o [B,H,n,dv], State or None).
+    q: [B,H,n,d]; k: [B,Hkv,n,d]; v: [B,Hkv,n,dv] with H a multiple of Hkv (query
+    head h reads key/value head h // (H // Hkv)); gamma: [H] or None.  chunk=None
+    runs the serial recurrence; chunk=c runs the chunked scan (per-chunk summaries
+    folded with the segment-concatenation rule).  The unmasked variant carries S, C,
+    m only and returns G, h as zeros.  Returns (o [B,H,n,dv], State or None).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, n, d = q.shape
+    Hkv = k.shape[1]
     dv = v.shape[-1]
-    assert k.shape == q.shape and v.shape[:3] == q.shape[:3]
+    assert k.shape == (B, Hkv, n, d) and v.shape[:3] == (B, Hkv, n) and H % Hkv == 0
     g = _f64(gamma)
     if g is not None:
         assert g.shape == (H,)
@@ -138,26 +145,31 @@ def forward(q, k, v, gamma=None, normalize=False, eps=0.0, state_in=None,
     nt = nthreads or default_threads()
     args_tail = [_p(q), _p(k), _p(v), _p(g), int(bool(normalize)), float(eps)] + _state_ptrs(sin) + \
         [_p(o)] + _state_ptrs(sout) + [nt]
+    um = int(bool(unmasked))
     if chunk is None:
-        rc = lib.hla_oracle_forward(B, H, n, d, dv, *args_tail)
+        rc = lib.hla_oracle_forward(B, H, Hkv, n, d, dv, um, *args_tail)
     else:
-        rc = lib.hla_oracle_forward_chunked(B, H, n, d, dv, int(chunk), *args_tail)
+        rc = lib.hla_oracle_forward_chunked(B, H, Hkv, n, d, dv, um, int(chunk), *args_tail)
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return o, sout
 
 
-def decode_step(state: State, q, k, v, H, gamma=None, normalize=False, eps=0.0, nthreads=None):
+def decode_step(state: State, q, k, v, H, gamma=None, normalize=False, eps=0.0, nthreads=None,
+                unmasked=False):
     """One decode step for N (sequence, head) pairs, in place on ``state``.
-    q, k: [N,d]; v: [N,dv]; pair u uses gamma[u % H].  Returns o [N,dv]."""
+    q: [N,d]; k: [N/H*Hkv,d]; v: [N/H*Hkv,dv]; pair u uses gamma[u % H] and key/value
+    row (u // H) * Hkv + (u % H) // (H // Hkv).  Returns o [N,dv]."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     N, d = q.shape
     dv = v.shape[-1]
+    Hkv = k.shape[0] * H // max(N, 1) if N else H
     g = _f64(gamma)
     for x in state.astuple():
         assert x.dtype == np.float64 and x.flags.c_contiguous
     o = np.zeros((N, dv))
-    rc = _load().hla_oracle_decode_step(N, H, d, dv, _p(g), int(bool(normalize)), float(eps),
+    rc = _load().hla_oracle_decode_step(N, H, Hkv, d, dv, int(bool(unmasked)), _p(g), int(bool(normalize)),
+                                        float(eps),
                                         *_state_ptrs(state), _p(q), _p(k), _p(v), _p(o),
                                         nthreads or default_threads())
     if rc != 0:

@@ -37,9 +37,23 @@
  *   G = f^2 G_A + G_B + f S_B C_A,   h = f^2 h_A + h_B + f S_B m_A.
  * The cross term S_B C_A is the one the pages name.
  *
- * Layout: q, k [B][H][n][d]; v, o [B][H][n][dv]; row-major, fp64.
- * State, one block per (b,h): S [BH][d][d], C [BH][d][dv], m [BH][d],
- * G [BH][d][dv], h [BH][d].
+ * Unmasked variant (the skill card "Higher-order linear attention", section
+ * "Linear-Time Higher-Order Interactions", bullet "Streaming Computation";
+ * gist.science "Belangrijkste bijdragen" item 2 for its scan operators):
+ *   o_t = q_t^T S_t C_t,   ratio-normalised  o_t = q_t^T S_t C_t / (q_t^T S_t m_t + eps),
+ * with the same decayed S, C, m.  Only S, C, m are carried; G and h are not
+ * part of this variant and are left at zero.  Its concatenation is the linear
+ * part of the rule above (S, C, m).
+ *
+ * Multi-query heads (skill card, section "Architecture Overview", bullet
+ * "Multi-Head Support"): k and v may have Hkv heads with H a multiple of Hkv;
+ * query head h reads key/value head h / (H / Hkv).  The summaries stay per query
+ * head (C = sum q v^T depends on the query head; S is the same for every head
+ * of a group).
+ *
+ * Layout: q [B][H][n][d], k [B][Hkv][n][d], v [B][Hkv][n][dv], o [B][H][n][dv];
+ * row-major, fp64.  State, one block per (b,h): S [BH][d][d], C [BH][d][dv],
+ * m [BH][d], G [BH][d][dv], h [BH][d].
  *
  * Everything is a plain loop in the order the formulas are written; no
  * blocking, no fusion.  Independent (b,h) pairs run on separate threads.
@@ -56,6 +70,7 @@ typedef struct {
 /* one (b,h) stream: the five summaries of one head, plus its decay factor */
 typedef struct {
     int d, dv;
+    int unmasked; /* 1: o = q^T S C, G and h not carried */
     double g;
     double *S, *C, *m, *G, *h; /* views into caller state for this (b,h) */
     double *kc;                /* scratch: k^T C_{t-1}, length dv        */
@@ -72,20 +87,22 @@ static void step_token(stream_t *st, const double *q, const double *k,
     const double g = st->g, g2 = g * g;
     double *S = st->S, *C = st->C, *m = st->m, *G = st->G, *h = st->h;
 
-    /* k^T C_{t-1} and k^T m_{t-1} */
-    for (int j = 0; j < dv; ++j) {
-        double acc = 0.0;
-        for (int i = 0; i < d; ++i) acc += k[i] * C[i * dv + j];
-        st->kc[j] = acc;
-    }
-    double km = 0.0;
-    for (int i = 0; i < d; ++i) km += k[i] * m[i];
+    if (!st->unmasked) {
+        /* k^T C_{t-1} and k^T m_{t-1} */
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i) acc += k[i] * C[i * dv + j];
+            st->kc[j] = acc;
+        }
+        double km = 0.0;
+        for (int i = 0; i < d; ++i) km += k[i] * m[i];
 
-    /* G_t = g^2 G_{t-1} + g k (k^T C_{t-1}),  h_t = g^2 h_{t-1} + g k (k^T m_{t-1}) */
-    for (int i = 0; i < d; ++i) {
-        for (int j = 0; j < dv; ++j)
-            G[i * dv + j] = g2 * G[i * dv + j] + g * k[i] * st->kc[j];
-        h[i] = g2 * h[i] + g * k[i] * km;
+        /* G_t = g^2 G_{t-1} + g k (k^T C_{t-1}),  h_t = g^2 h_{t-1} + g k (k^T m_{t-1}) */
+        for (int i = 0; i < d; ++i) {
+            for (int j = 0; j < dv; ++j)
+                G[i * dv + j] = g2 * G[i * dv + j] + g * k[i] * st->kc[j];
+            h[i] = g2 * h[i] + g * k[i] * km;
+        }
     }
     /* S_t = g S_{t-1} + k k^T */
     for (int i = 0; i < d; ++i)
@@ -100,7 +117,9 @@ static void step_token(stream_t *st, const double *q, const double *k,
     if (!o) return;
 
     /* o_t = q^T (S_t C_t - G_t), evaluated as (q^T S_t) C_t - q^T G_t so that
-     * the cost per token is O(d^2 + d dv) as the pages state. */
+     * the cost per token is O(d^2 + d dv) as the pages state; the unmasked
+     * variant has no G (and no h) term.  G and h are zero in that variant, so the
+     * same loops serve both. */
     for (int j = 0; j < d; ++j) {
         double acc = 0.0;
         for (int i = 0; i < d; ++i) acc += q[i] * S[i * d + j];
@@ -155,6 +174,8 @@ static void combine_one(int d, int dv, double f,
 
 typedef struct {
     int B, H, n, d, dv, chunk;
+    int Hkv;      /* key/value heads; query head h reads head h / (H / Hkv) */
+    int unmasked; /* variant: 0 masked, 1 unmasked */
     const double *q, *k, *v, *gamma;
     int normalize;
     double eps;
@@ -180,8 +201,13 @@ static void load_state(stream_t *st, const ostate *in, size_t u)
         memcpy(st->S, in->S + u * d * d, sizeof(double) * d * d);
         memcpy(st->C, in->C + u * d * dv, sizeof(double) * d * dv);
         memcpy(st->m, in->m + u * d, sizeof(double) * d);
-        memcpy(st->G, in->G + u * d * dv, sizeof(double) * d * dv);
-        memcpy(st->h, in->h + u * d, sizeof(double) * d);
+        if (st->unmasked) { /* not part of the unmasked state */
+            memset(st->G, 0, sizeof(double) * d * dv);
+            memset(st->h, 0, sizeof(double) * d);
+        } else {
+            memcpy(st->G, in->G + u * d * dv, sizeof(double) * d * dv);
+            memcpy(st->h, in->h + u * d, sizeof(double) * d);
+        }
     } else {
         memset(st->S, 0, sizeof(double) * d * d);
         memset(st->C, 0, sizeof(double) * d * dv);
@@ -207,6 +233,7 @@ static stream_t stream_new(int d, int dv)
     stream_t st;
     st.d = d;
     st.dv = dv;
+    st.unmasked = 0;
     st.g = 1.0;
     st.S = (double *)calloc((size_t)d * d, sizeof(double));
     st.C = (double *)calloc((size_t)d * dv, sizeof(double));
@@ -225,15 +252,23 @@ static void stream_free(stream_t *st)
 }
 
 /* serial recurrence over all n tokens of unit u = b*H + hh */
+/* key/value head of unit u = b*H + hh */
+static size_t kv_unit(const job_t *J, int u)
+{
+    const int b = u / J->H, hh = u % J->H;
+    return (size_t)b * J->Hkv + hh / (J->H / J->Hkv);
+}
+
 static void run_serial(job_t *J, stream_t *st, int u)
 {
     const int n = J->n, d = J->d, dv = J->dv;
-    const size_t qo = (size_t)u * n * d, vo = (size_t)u * n * dv;
+    const size_t qo = (size_t)u * n * d, oo = (size_t)u * n * dv;
+    const size_t ko = kv_unit(J, u) * n * d, vo = kv_unit(J, u) * n * dv;
     load_state(st, &J->in, u);
     for (int t = 0; t < n; ++t)
-        step_token(st, J->q + qo + (size_t)t * d, J->k + qo + (size_t)t * d,
+        step_token(st, J->q + qo + (size_t)t * d, J->k + ko + (size_t)t * d,
                    J->v + vo + (size_t)t * dv, J->normalize, J->eps,
-                   J->o ? J->o + vo + (size_t)t * dv : NULL);
+                   J->o ? J->o + oo + (size_t)t * dv : NULL);
     store_state(st, &J->out, u);
 }
 
@@ -245,9 +280,11 @@ static void run_serial(job_t *J, stream_t *st, int u)
 static void run_chunked(job_t *J, stream_t *st, int u)
 {
     const int n = J->n, d = J->d, dv = J->dv, c = J->chunk;
-    const size_t qo = (size_t)u * n * d, vo = (size_t)u * n * dv;
+    const size_t qo = (size_t)u * n * d, oo = (size_t)u * n * dv;
+    const size_t ko = kv_unit(J, u) * n * d, vo = kv_unit(J, u) * n * dv;
     stream_t loc = stream_new(d, dv);
     loc.g = st->g;
+    loc.unmasked = st->unmasked;
     /* prefix state lives in st */
     load_state(st, &J->in, u);
     for (int t0 = 0; t0 < n; t0 += c) {
@@ -255,26 +292,31 @@ static void run_chunked(job_t *J, stream_t *st, int u)
         /* local summary of this chunk, from zero */
         load_state(&loc, NULL, 0);
         for (int t = t0; t < t0 + len; ++t)
-            step_token(&loc, J->q + qo + (size_t)t * d, J->k + qo + (size_t)t * d,
+            step_token(&loc, J->q + qo + (size_t)t * d, J->k + ko + (size_t)t * d,
                        J->v + vo + (size_t)t * dv, 0, 0.0, NULL);
         /* outputs of this chunk: continue from the prefix in a copy */
         stream_t run = stream_new(d, dv);
         run.g = st->g;
+        run.unmasked = st->unmasked;
         memcpy(run.S, st->S, sizeof(double) * d * d);
         memcpy(run.C, st->C, sizeof(double) * d * dv);
         memcpy(run.m, st->m, sizeof(double) * d);
         memcpy(run.G, st->G, sizeof(double) * d * dv);
         memcpy(run.h, st->h, sizeof(double) * d);
         for (int t = t0; t < t0 + len; ++t)
-            step_token(&run, J->q + qo + (size_t)t * d, J->k + qo + (size_t)t * d,
+            step_token(&run, J->q + qo + (size_t)t * d, J->k + ko + (size_t)t * d,
                        J->v + vo + (size_t)t * dv, J->normalize, J->eps,
-                       J->o ? J->o + vo + (size_t)t * dv : NULL);
+                       J->o ? J->o + oo + (size_t)t * dv : NULL);
         stream_free(&run);
-        /* prefix <- prefix (+) local */
+        /* prefix <- prefix (+) local; the unmasked variant keeps G, h at zero */
         combine_one(d, dv, pow(st->g, (double)len),
                     st->S, st->C, st->m, st->G, st->h,
                     loc.S, loc.C, loc.m, loc.G, loc.h,
                     st->S, st->C, st->m, st->G, st->h);
+        if (st->unmasked) {
+            memset(st->G, 0, sizeof(double) * d * dv);
+            memset(st->h, 0, sizeof(double) * d);
+        }
     }
     store_state(st, &J->out, u);
     stream_free(&loc);
@@ -285,7 +327,7 @@ static void run_decode(job_t *J, stream_t *st, int u)
 {
     const int d = J->d, dv = J->dv;
     load_state(st, &J->in, u);
-    step_token(st, J->q + (size_t)u * d, J->k + (size_t)u * d, J->v + (size_t)u * dv,
+    step_token(st, J->q + (size_t)u * d, J->k + kv_unit(J, u) * d, J->v + kv_unit(J, u) * dv,
                J->normalize, J->eps, J->o + (size_t)u * dv);
     store_state(st, &J->out, u);
 }
@@ -299,6 +341,7 @@ static void *worker(void *arg)
         int u = take_unit(J, total);
         if (u < 0) break;
         st.g = J->gamma ? J->gamma[u % J->H] : 1.0;
+        st.unmasked = J->unmasked;
         if (J->mode == 0) run_serial(J, &st, u);
         else if (J->mode == 1) run_chunked(J, &st, u);
         else run_decode(J, &st, u);
@@ -330,12 +373,18 @@ static int check_dims(int B, int H, int n, int d, int dv)
     return (B < 0 || H < 1 || n < 0 || d < 1 || dv < 1) ? -1 : 0;
 }
 
+static int check_heads(int H, int Hkv, int unmasked)
+{
+    return (Hkv < 1 || H % Hkv || (unmasked != 0 && unmasked != 1)) ? -1 : 0;
+}
+
 /* ------------------------------------------------------------------------- */
 /* exported entry points (ctypes)                                            */
 
 /* Serial recurrence over n tokens for every (b,h).  gamma: [H] or NULL (no
- * decay).  state_in / state_out: pointers may be NULL (zeros / skip). */
-int hla_oracle_forward(int B, int H, int n, int d, int dv,
+ * decay).  state_in / state_out: pointers may be NULL (zeros / skip).  Hkv:
+ * key/value heads (H for ordinary multi-head); unmasked: 0 or 1 (variant). */
+int hla_oracle_forward(int B, int H, int Hkv, int n, int d, int dv, int unmasked,
                        const double *q, const double *k, const double *v,
                        const double *gamma, int normalize, double eps,
                        double *Si, double *Ci, double *mi, double *Gi, double *hi,
@@ -343,10 +392,11 @@ int hla_oracle_forward(int B, int H, int n, int d, int dv,
                        double *So, double *Co, double *mo, double *Go, double *ho,
                        int nthreads)
 {
-    if (check_dims(B, H, n, d, dv)) return -1;
+    if (check_dims(B, H, n, d, dv) || check_heads(H, Hkv, unmasked)) return -1;
     job_t J;
     memset(&J, 0, sizeof J);
     J.B = B; J.H = H; J.n = n; J.d = d; J.dv = dv; J.chunk = 0;
+    J.Hkv = Hkv; J.unmasked = unmasked;
     J.q = q; J.k = k; J.v = v; J.gamma = gamma;
     J.normalize = normalize; J.eps = eps;
     J.in = (ostate){Si, Ci, mi, Gi, hi};
@@ -357,7 +407,7 @@ int hla_oracle_forward(int B, int H, int n, int d, int dv,
 }
 
 /* Chunked-scan forward (chunk >= 1): see run_chunked. */
-int hla_oracle_forward_chunked(int B, int H, int n, int d, int dv, int chunk,
+int hla_oracle_forward_chunked(int B, int H, int Hkv, int n, int d, int dv, int unmasked, int chunk,
                                const double *q, const double *k, const double *v,
                                const double *gamma, int normalize, double eps,
                                double *Si, double *Ci, double *mi, double *Gi, double *hi,
@@ -365,10 +415,11 @@ int hla_oracle_forward_chunked(int B, int H, int n, int d, int dv, int chunk,
                                double *So, double *Co, double *mo, double *Go, double *ho,
                                int nthreads)
 {
-    if (check_dims(B, H, n, d, dv) || chunk < 1) return -1;
+    if (check_dims(B, H, n, d, dv) || check_heads(H, Hkv, unmasked) || chunk < 1) return -1;
     job_t J;
     memset(&J, 0, sizeof J);
     J.B = B; J.H = H; J.n = n; J.d = d; J.dv = dv; J.chunk = chunk;
+    J.Hkv = Hkv; J.unmasked = unmasked;
     J.q = q; J.k = k; J.v = v; J.gamma = gamma;
     J.normalize = normalize; J.eps = eps;
     J.in = (ostate){Si, Ci, mi, Gi, hi};
@@ -380,18 +431,19 @@ int hla_oracle_forward_chunked(int B, int H, int n, int d, int dv, int chunk,
 
 /* One decode step for N independent (sequence, head) pairs, pair u using
  * gamma[u % H].  The state arrays are read and written in place.
- * q, k: [N][d]; v, o: [N][dv]. */
-int hla_oracle_decode_step(int N, int H, int d, int dv,
+ * q: [N][d], o: [N][dv]; k: [N/H*Hkv][d], v: [N/H*Hkv][dv]. */
+int hla_oracle_decode_step(int N, int H, int Hkv, int d, int dv, int unmasked,
                            const double *gamma, int normalize, double eps,
                            double *S, double *C, double *m, double *G, double *h,
                            const double *q, const double *k, const double *v,
                            double *o, int nthreads)
 {
-    if (check_dims(1, H, 1, d, dv) || N < 0) return -1;
+    if (check_dims(1, H, 1, d, dv) || check_heads(H, Hkv, unmasked) || N < 0) return -1;
     if (N % H) return -1;
     job_t J;
     memset(&J, 0, sizeof J);
     J.B = N / H; J.H = H; J.n = 1; J.d = d; J.dv = dv;
+    J.Hkv = Hkv; J.unmasked = unmasked;
     J.q = q; J.k = k; J.v = v; J.gamma = gamma;
     J.normalize = normalize; J.eps = eps;
     J.in = (ostate){S, C, m, G, h};

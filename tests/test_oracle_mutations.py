@@ -43,7 +43,7 @@ def _build_mutant(tmp_path, name):
     L = ctypes.CDLL(str(lib))
     dp = ctypes.POINTER(ctypes.c_double)
     i, d = ctypes.c_int, ctypes.c_double
-    L.hla_oracle_forward.argtypes = [i, i, i, i, i, dp, dp, dp, dp, i, d] + [dp] * 5 + [dp] + [dp] * 5 + [i]
+    L.hla_oracle_forward.argtypes = [i] * 7 + [dp, dp, dp, dp, i, d] + [dp] * 5 + [dp] + [dp] * 5 + [i]
     return L
 
 
@@ -57,6 +57,56 @@ def test_pin_rejects_planted_mistake(tmp_path, name):
     o = np.zeros((1, 1, n, dv))
     P = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
     none = [None] * 5
-    assert L.hla_oracle_forward(1, 1, n, d, dv, P(q), P(k), P(v), P(g), 0, 0.0, *none, P(o), *none, 1) == 0
+    assert L.hla_oracle_forward(1, 1, 1, n, d, dv, 0, P(q), P(k), P(v), P(g), 0, 0.0, *none, P(o), *none, 1) == 0
     ref = brute_force(q[0, 0], k[0, 0], v[0, 0], 0.8)
     assert rel(o[0, 0], ref) > 1e-6, f"mutation {name} not caught by the brute-force pin"
+
+
+# mistakes in the unmasked variant and in the key/value head mapping, each caught by
+# its own pin (all-pairs brute force; repeated-head equivalence)
+MUTATIONS_VARIANTS = {
+    # the unmasked variant still subtracts the cross summary
+    "unmasked_keeps_cross": ("    if (!st->unmasked) {\n        /* k^T C_{t-1} and k^T m_{t-1} */",
+                             "    if (1) {\n        /* k^T C_{t-1} and k^T m_{t-1} */"),
+    # query heads mapped to key/value heads round-robin instead of in groups
+    "kv_round_robin": ("return (size_t)b * J->Hkv + hh / (J->H / J->Hkv);",
+                       "return (size_t)b * J->Hkv + hh % J->Hkv;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS_VARIANTS))
+def test_variant_pins_reject_planted_mistake(tmp_path, name):
+    from test_oracle_pins import brute_force_unmasked
+    text = open(SRC).read()
+    old, new = MUTATIONS_VARIANTS[name]
+    assert text.count(old) == 1, name
+    src = tmp_path / f"mut_{name}.c"
+    src.write_text(text.replace(old, new))
+    lib = tmp_path / f"libmut_{name}.so"
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", str(lib), str(src), "-lm"])
+    L = ctypes.CDLL(str(lib))
+    dp = ctypes.POINTER(ctypes.c_double)
+    i, d = ctypes.c_int, ctypes.c_double
+    L.hla_oracle_forward.argtypes = [i] * 7 + [dp, dp, dp, dp, i, d] + [dp] * 5 + [dp] + [dp] * 5 + [i]
+    P = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+    none = [None] * 5
+    rng = np.random.default_rng(2)
+    n, dd, dv = 8, 3, 2
+    if name == "unmasked_keeps_cross":
+        q, k, v = rand_inputs(rng, 1, 1, n, dd, dv)
+        o = np.zeros((1, 1, n, dv))
+        assert L.hla_oracle_forward(1, 1, 1, n, dd, dv, 1, P(q), P(k), P(v), None, 0, 0.0, *none, P(o), *none,
+                                    1) == 0
+        ref = brute_force_unmasked(q[0, 0], k[0, 0], v[0, 0])
+        assert rel(o[0, 0], ref) > 1e-6, f"mutation {name} not caught"
+    else:
+        H, Hkv = 4, 2
+        q = rng.standard_normal((1, H, n, dd))
+        k = rng.standard_normal((1, Hkv, n, dd))
+        v = rng.standard_normal((1, Hkv, n, dv))
+        o = np.zeros((1, H, n, dv))
+        assert L.hla_oracle_forward(1, H, Hkv, n, dd, dv, 0, P(q), P(k), P(v), None, 0, 0.0, *none, P(o), *none,
+                                    1) == 0
+        kr, vr = np.repeat(k, H // Hkv, axis=1), np.repeat(v, H // Hkv, axis=1)
+        ref = np.stack([brute_force(q[0, h], kr[0, h], vr[0, h]) for h in range(H)])
+        assert rel(o[0], ref) > 1e-6, f"mutation {name} not caught"

@@ -307,3 +307,123 @@ def test_empty_sequence_keeps_state():
     assert o.shape == (1, 1, 0, 2)
     for a, b in zip(s2.astuple(), s.astuple()):
         assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------- unmasked variant
+# Skill card "Higher-order linear attention", section "Linear-Time Higher-Order
+# Interactions", bullet "Streaming Computation": o_t = q_t^T S_t C_t; the ratio form
+# divides by q_t^T S_t m_t.  Its operators are the linear part of the concatenation
+# rule (gist.science "Belangrijkste bijdragen" item 2).
+def brute_force_unmasked(q, k, v, g=1.0, normalize=False, eps=0.0):
+    """o_t = sum_{a<=t} sum_{b<=t} g^{(t-a)+(t-b)} (q_t.k_a)(k_a.q_b) v_b: every key
+    index and every query/value index up to t, in any order."""
+    n, dv = q.shape[0], v.shape[1]
+    o = np.zeros((n, dv))
+    for t in range(n):
+        num = np.zeros(dv)
+        den = 0.0
+        for a in range(t + 1):
+            for b in range(t + 1):
+                w = (g ** ((t - a) + (t - b))) * (q[t] @ k[a]) * (k[a] @ q[b])
+                num += w * v[b]
+                den += w
+        o[t] = num / (den + eps) if normalize else num
+    return o
+
+
+@pytest.mark.parametrize("decay", [False, True])
+@pytest.mark.parametrize("normalize", [False, True])
+@pytest.mark.parametrize("n,d,dv", [(1, 1, 1), (9, 3, 2), (17, 4, 3)])
+def test_unmasked_brute_force_and_state(decay, normalize, n, d, dv):
+    rng = np.random.default_rng(300 + n + d)
+    B, H = 2, 2
+    q, k, v = rand_inputs(rng, B, H, n, d, dv, positive=normalize)
+    gamma = np.array([0.85, 0.5]) if decay else None
+    o, st = oracle.forward(q, k, v, gamma=gamma, normalize=normalize, eps=1e-3, unmasked=True)
+    for b in range(B):
+        for h in range(H):
+            g = gamma[h] if decay else 1.0
+            ref = brute_force_unmasked(q[b, h], k[b, h], v[b, h], g, normalize, 1e-3)
+            assert rel(o[b, h], ref) < 1e-12
+            S, C, m, _, _ = brute_state(q[b, h], k[b, h], v[b, h], g)
+            u = b * H + h
+            assert rel(st.S[u], S) < 1e-12 and rel(st.C[u], C) < 1e-12 and rel(st.m[u], m) < 1e-12
+    assert not st.G.any() and not st.h.any()  # not carried by this variant
+
+
+def test_unmasked_dense_form_and_masked_relation():
+    """O = [L o ((L o QK^T)(QK^T)^T)] V, and the masked output is the unmasked one
+    minus q_t^T G_t (G from the masked state after t)."""
+    rng = np.random.default_rng(31)
+    n, d, dv = 14, 3, 2
+    q, k, v = rand_inputs(rng, 1, 1, n, d, dv)
+    o, _ = oracle.forward(q, k, v, unmasked=True)
+    Q, K, V = q[0, 0], k[0, 0], v[0, 0]
+    L = np.tril(np.ones((n, n)))
+    A = Q @ K.T
+    assert rel(o[0, 0], (L * ((L * A) @ A.T)) @ V) < 1e-12
+    om, _ = oracle.forward(q, k, v)
+    for t in (0, 6, 13):
+        _, st = oracle.forward(q[:, :, : t + 1], k[:, :, : t + 1], v[:, :, : t + 1])
+        assert rel(o[0, 0, t] - Q[t] @ st.G[0], om[0, 0, t]) < 1e-12
+
+
+@pytest.mark.parametrize("decay", [False, True])
+def test_unmasked_chunked_resume_decode(decay):
+    rng = np.random.default_rng(32)
+    B, H, n, d, dv = 2, 2, 23, 3, 4
+    q, k, v = rand_inputs(rng, B, H, n, d, dv, positive=True)
+    gamma = np.array([0.9, 0.7]) if decay else None
+    kw = dict(gamma=gamma, normalize=True, eps=1e-3, unmasked=True)
+    o, s = oracle.forward(q, k, v, **kw)
+    for c in (1, 4, 7, 23, 40):
+        oc, sc = oracle.forward(q, k, v, chunk=c, **kw)
+        assert rel(oc, o) < 1e-12
+        for a, b in zip(sc.astuple(), s.astuple()):
+            assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
+    n1 = 11
+    _, s1 = oracle.forward(q[:, :, :n1], k[:, :, :n1], v[:, :, :n1], **kw)
+    o2, _ = oracle.forward(q[:, :, n1:], k[:, :, n1:], v[:, :, n1:], state_in=s1, **kw)
+    assert rel(o2, o[:, :, n1:]) < 1e-12
+    st = s1.copy()
+    for t in range(n1, n):
+        od = oracle.decode_step(st, q[:, :, t].reshape(B * H, d), k[:, :, t].reshape(B * H, d),
+                                v[:, :, t].reshape(B * H, dv), H, **kw)
+        assert rel(od.reshape(B, H, dv), o[:, :, t]) < 1e-12
+    for a, b in zip(st.astuple(), s.astuple()):
+        assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------- shared key/value heads
+# Skill card, section "Architecture Overview", bullet "Multi-Head Support": keys and
+# values shared by a group of query heads.  The result must equal ordinary
+# multi-head attention with each group's keys and values repeated per query head.
+@pytest.mark.parametrize("unmasked", [False, True])
+@pytest.mark.parametrize("H,Hkv", [(4, 1), (6, 2), (3, 3)])
+def test_shared_kv_heads_equal_repeated_heads(unmasked, H, Hkv):
+    rng = np.random.default_rng(40 + H * 3 + Hkv)
+    B, n, d, dv = 2, 10, 3, 2
+    q = rng.standard_normal((B, H, n, d))
+    k = rng.standard_normal((B, Hkv, n, d))
+    v = rng.standard_normal((B, Hkv, n, dv))
+    gamma = np.linspace(0.6, 0.95, H)
+    rep = lambda a: np.repeat(a, H // Hkv, axis=1)
+    kw = dict(gamma=gamma, unmasked=unmasked)
+    o, s = oracle.forward(q, k, v, **kw)
+    o_ref, s_ref = oracle.forward(q, rep(k), rep(v), **kw)
+    assert np.array_equal(o, o_ref)
+    for a, b in zip(s.astuple(), s_ref.astuple()):
+        assert np.array_equal(a, b)
+    oc, _ = oracle.forward(q, k, v, chunk=4, **kw)
+    assert rel(oc, o) < 1e-12
+    # decode: key/value rows per (sequence, key/value head)
+    st, st_ref = s.copy(), s.copy()
+    qd = rng.standard_normal((B * H, d))
+    kd = rng.standard_normal((B * Hkv, d))
+    vd = rng.standard_normal((B * Hkv, dv))
+    od = oracle.decode_step(st, qd, kd, vd, H, **kw)
+    rep2 = lambda a: np.repeat(a.reshape(B, Hkv, -1), H // Hkv, axis=1).reshape(B * H, -1)
+    od_ref = oracle.decode_step(st_ref, qd, rep2(kd), rep2(vd), H, **kw)
+    assert np.array_equal(od, od_ref)
+    for a, b in zip(st.astuple(), st_ref.astuple()):
+        assert np.array_equal(a, b)
