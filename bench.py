@@ -34,6 +34,10 @@ import numpy as np  # noqa: E402
 from causal_prefix_scan_gb300 import workloads as W  # noqa: E402
 
 METRIC = "masked 2nd-order HLA forward tokens/s and % roofline on 1 GB300"
+
+
+def metric_for(w) -> str:
+    return METRIC.replace("masked", "unmasked", 1) if getattr(w, "unmasked", False) else METRIC
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 FWD_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd_tc.cuh")
@@ -42,16 +46,24 @@ DECODE_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_
 
 # ----------------------------------------------------------------- arithmetic
 def alg_flops_per_token_head(w: W.Workload) -> float:
-    """c(3d+dv) + 4d^2 + 6 d dv + 2 d^2 dv / c, triangular products at half."""
+    """Masked: c(3d+dv) + 4d^2 + 6 d dv + 2 d^2 dv / c; unmasked (no X = S C - G):
+    c(3d+dv) + 4d^2 + 4 d dv; triangular products at half."""
     c, d, dv = w.chunk, w.d, w.dv
+    if w.unmasked:
+        return c * (3 * d + dv) + 4 * d * d + 4 * d * dv
     return c * (3 * d + dv) + 4 * d * d + 6 * d * dv + 2 * d * d * dv / c
 
 
 def alg_bytes_per_launch(w: W.Workload, with_state: bool = True) -> float:
+    """q read and o written once per token-head, k and v read once per token and
+    key/value head, the final state written once per (b,h): S, C, m, G, h (masked)
+    or S, C, m (unmasked)."""
     s = 2 if w.dtype == "bf16" else 4
-    per_th = (2 * w.d + w.dv) * s + w.dv * s
-    state = (w.d * w.d + 2 * w.d * w.dv + 2 * w.d) * 4 if with_state else 0
-    return w.token_heads * per_th + w.B * w.H * state
+    qo = (w.d + w.dv) * s * w.token_heads
+    kv = (w.d + w.dv) * s * w.B * w.kv_heads * w.n
+    per_pair = w.d * w.d + w.d * w.dv + w.d if w.unmasked else w.d * w.d + 2 * w.d * w.dv + 2 * w.d
+    state = per_pair * 4 if with_state else 0
+    return qo + kv + w.B * w.H * state
 
 
 def load_peaks():
@@ -187,7 +199,8 @@ def oracle_rate(w: W.Workload, x, batch_rows: int, n_tokens: int, nthreads: int)
     g = None if x["gamma"] is None else np.asarray(x["gamma"], np.float64)
     oracle.build()
     t0 = time.perf_counter()
-    oracle.forward(q, k, v, gamma=g, normalize=w.normalize, eps=w.eps, want_state=True, nthreads=nthreads)
+    oracle.forward(q, k, v, gamma=g, normalize=w.normalize, eps=w.eps, want_state=True, nthreads=nthreads,
+                   unmasked=w.unmasked)
     return time.perf_counter() - t0, batch_rows * n_tokens
 
 
@@ -230,7 +243,9 @@ def workload_by_name(name: str):
 
 def config_dict(w: W.Workload, nsets: int, set_bytes: int, world: int):
     variant = "normalised" if w.normalize else ("decay" if w.decay else "unnormalised")
-    return {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d, "dv": w.dv, "chunk": w.chunk,
+    variant = ("unmasked " if w.unmasked else "masked ") + variant
+    return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.kv_heads, "n": w.n, "d": w.d, "dv": w.dv,
+            "chunk": w.chunk,
             "variant": variant, "inputs": f"q,k {w.qk}, v N(0,1), seed {w.seed}",
             "l2": f"inputs larger than L2: {nsets} rotating input sets, {nsets * set_bytes / 2**20:.0f} MiB",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
@@ -248,14 +263,14 @@ def bench_forward(args, w: W.Workload, rank, world, local, dist):
     host = {k: torch.from_numpy(x[k]).to(tdt).pin_memory() for k in ("q", "k", "v")}
     gamma = torch.from_numpy(x["gamma"]).to(dev) if x["gamma"] is not None else None
     esz = 2 if w.dtype == "bf16" else 4
-    set_bytes = w.token_heads * (2 * w.d + 2 * w.dv) * esz  # q, k, v, o
+    set_bytes = (w.token_heads + w.B * w.kv_heads * w.n) * (w.d + w.dv) * esz  # q, o and k, v
     nsets = max(1, min(16, -(-2 * L2_BYTES // set_bytes)))
     sets = []
     for _ in range(nsets):
         q, k, v = (host[n].to(dev, non_blocking=True) for n in ("q", "k", "v"))
         o = torch.empty(q.shape[:3] + (w.dv,), dtype=tdt, device=dev)
         sets.append((q, k, v, o))
-    params = hla.make_params(sets[0][0], sets[0][2], w.chunk, gamma, w.normalize, w.eps)
+    params = hla.make_params(sets[0][0], sets[0][2], w.chunk, gamma, w.normalize, w.eps, w.unmasked)
     ws_bytes = hla.hla_forward_workspace_size(params)
     ws = hla.new_workspace(ws_bytes, dev)
     st = hla.State.empty(w.B * w.H, w.d, w.dv, device=dev)
@@ -380,7 +395,7 @@ def bench_forward(args, w: W.Workload, rank, world, local, dist):
                 "alg_bytes_per_launch": bytes_launch, "alg_flops_per_launch": flops_launch,
                 "tensor_frac": (flops_launch / t_launch / 1e12) / peaks["bf16_tflops"],
                 "roofline_time_us": max(t_hbm, t_tc) * 1e6, "launch_time_us": t_launch * 1e6}
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+    line = {"metric": metric_for(w), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": config_dict(w, nsets, set_bytes, world), "roofline": roofline,
@@ -429,7 +444,7 @@ def bench_decode(args, dw: W.DecodeWorkload, rank, world, local, dist):
 
     def step(i, s):
         q, k, v = toks[i % T]
-        hla.hla_decode_step(N, dw.H, d, dv, hla.HLA_BF16, 0, 0.0, None, st, q, k, v, o, s)
+        hla.hla_decode_step(N, dw.H, 0, d, dv, hla.HLA_BF16, 0, 0.0, None, st, q, k, v, o, s)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -476,7 +491,7 @@ def bench_decode(args, dw: W.DecodeWorkload, rank, world, local, dist):
         e0.record(stream)
         for _ in range(Ke):
             q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True); v.copy_(hv, non_blocking=True)
-            hla.hla_decode_step(N, dw.H, d, dv, hla.HLA_BF16, 0, 0.0, None, st, q, k, v, o, stream)
+            hla.hla_decode_step(N, dw.H, 0, d, dv, hla.HLA_BF16, 0, 0.0, None, st, q, k, v, o, stream)
             ho.copy_(o, non_blocking=True)
         e1.record(stream)
     stream.synchronize()
@@ -517,7 +532,7 @@ def bench_reference(args, w, rank, world):
     def one(i):
         t0 = offs[i % len(offs)]
         oracle.forward(sl(x["q"], t0), sl(x["k"], t0), sl(x["v"], t0), gamma=g, normalize=w.normalize,
-                       eps=w.eps, nthreads=cores)
+                       eps=w.eps, nthreads=cores, unmasked=w.unmasked)
 
     for i in range(args.warmup):
         one(i)
@@ -527,7 +542,7 @@ def bench_reference(args, w, rank, world):
     dt = time.perf_counter() - t0
     value = n_s * args.steps / dt
     sample = f"fp64 serial recurrence on 1 batch row x {w.H} heads x {n_s}-token windows per step"
-    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+    return {"impl": "reference", "metric": metric_for(w), "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_dict(w, 1, 0, world),

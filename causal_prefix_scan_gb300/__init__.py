@@ -1,4 +1,4 @@
-"""GB300-native masked second-order Higher-order Linear Attention (HLA).
+"""GB300-native second-order Higher-order Linear Attention (HLA): masked and unmasked.
 
 Thin ctypes binding over the C ABI in ``include/hla.h`` (library
 ``_lib/libhla_gb300.so``, built for sm_103a by ``_build.build()``).  Functions named
@@ -19,11 +19,11 @@ from ._build import LIB_PATH
 
 HLA_OK, HLA_ERR_ARG, HLA_ERR_UNSUPPORTED, HLA_ERR_CUDA, HLA_ERR_TIMEOUT = 0, 1, 2, 3, 4
 HLA_F32, HLA_BF16 = 0, 1
-HLA_NORMALIZE, HLA_DECAY = 1, 2
+HLA_NORMALIZE, HLA_DECAY, HLA_UNMASKED = 1, 2, 4
 
 __all__ = [
     "HLA_OK", "HLA_ERR_ARG", "HLA_ERR_UNSUPPORTED", "HLA_ERR_CUDA", "HLA_ERR_TIMEOUT",
-    "HLA_F32", "HLA_BF16", "HLA_NORMALIZE", "HLA_DECAY",
+    "HLA_F32", "HLA_BF16", "HLA_NORMALIZE", "HLA_DECAY", "HLA_UNMASKED",
     "HlaError", "hla_params", "hla_state", "library", "EXPORTS",
     "hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combine", "hla_decode_step",
     "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
@@ -44,7 +44,8 @@ class HlaError(RuntimeError):
 class hla_params(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("n", ctypes.c_int), ("d", ctypes.c_int),
                 ("dv", ctypes.c_int), ("chunk", ctypes.c_int), ("in_dtype", ctypes.c_int),
-                ("flags", ctypes.c_uint), ("eps", ctypes.c_float), ("gamma", ctypes.c_void_p)]
+                ("flags", ctypes.c_uint), ("eps", ctypes.c_float), ("gamma", ctypes.c_void_p),
+                ("Hkv", ctypes.c_int)]
 
 
 class hla_state(ctypes.Structure):
@@ -72,7 +73,7 @@ def library(path: str | None = None):
     lib.hla_forward_chunked_noalloc.argtypes = [P, vp, vp, vp, vp, S, S, vp]
     lib.hla_forward_chunked_noalloc.restype = ctypes.c_int
     lib.hla_state_combine.argtypes = [i, i, i, S, S, S, vp, vp]
-    lib.hla_decode_step.argtypes = [i, i, i, i, i, u, f, vp, S, vp, vp, vp, vp, vp]
+    lib.hla_decode_step.argtypes = [i, i, i, i, i, i, u, f, vp, S, vp, vp, vp, vp, vp]
     lib.hla_sync_status.argtypes = [vp]
     for fn in (lib.hla_forward_chunked, lib.hla_state_combine, lib.hla_decode_step, lib.hla_sync_status):
         fn.restype = ctypes.c_int
@@ -149,9 +150,9 @@ def hla_state_combine(count: int, d: int, dv: int, A, B, out, decay_pow=None, st
                                        _ptr(decay_pow), _stream(stream)))
 
 
-def hla_decode_step(N: int, H: int, d: int, dv: int, dtype: int, flags: int, eps: float, gamma, state,
-                    q, k, v, o, stream=None) -> None:
-    _check(library().hla_decode_step(N, H, d, dv, dtype, flags, eps, _ptr(gamma), _state_struct(state),
+def hla_decode_step(N: int, H: int, Hkv: int, d: int, dv: int, dtype: int, flags: int, eps: float, gamma,
+                    state, q, k, v, o, stream=None) -> None:
+    _check(library().hla_decode_step(N, H, Hkv, d, dv, dtype, flags, eps, _ptr(gamma), _state_struct(state),
                                      _ptr(q), _ptr(k), _ptr(v), _ptr(o), _stream(stream)))
 
 
@@ -194,10 +195,15 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
-def make_params(q, v, chunk: int, gamma=None, normalize: bool = False, eps: float = 0.0) -> hla_params:
+def make_params(q, v, chunk: int, gamma=None, normalize: bool = False, eps: float = 0.0,
+                unmasked: bool = False) -> hla_params:
+    """Parameters for q [B,H,n,d] and v [B,Hkv,n,dv] (Hkv = H, or a divisor of H when
+    key/value heads are shared)."""
     B, H, n, d = q.shape
-    flags = (HLA_NORMALIZE if normalize else 0) | (HLA_DECAY if gamma is not None else 0)
-    return hla_params(B, H, n, d, v.shape[-1], chunk, _dtype_code(q), flags, float(eps), _ptr(gamma))
+    flags = (HLA_NORMALIZE if normalize else 0) | (HLA_DECAY if gamma is not None else 0) | \
+        (HLA_UNMASKED if unmasked else 0)
+    return hla_params(B, H, n, d, v.shape[-1], chunk, _dtype_code(q), flags, float(eps), _ptr(gamma),
+                      v.shape[1])
 
 
 def new_workspace(nbytes: int, device="cuda"):
@@ -207,11 +213,12 @@ def new_workspace(nbytes: int, device="cuda"):
 
 
 def forward(q, k, v, chunk: int, gamma=None, normalize: bool = False, eps: float = 0.0, state_in=None,
-            return_state: bool = False, out=None, workspace=None, stream=None):
-    """Masked 2nd-order HLA forward.  q, k [B,H,n,d], v [B,H,n,dv] contiguous CUDA tensors
-    (bf16 or fp32); gamma [H] fp32 or None.  Returns o (and the final State)."""
+            return_state: bool = False, out=None, workspace=None, stream=None, unmasked: bool = False):
+    """2nd-order HLA forward (masked; unmasked with ``unmasked=True``).  q [B,H,n,d],
+    k [B,Hkv,n,d], v [B,Hkv,n,dv] contiguous CUDA tensors (bf16 or fp32; Hkv divides H);
+    gamma [H] fp32 or None.  Returns o (and the final State)."""
     import torch
-    p = make_params(q, v, chunk, gamma, normalize, eps)
+    p = make_params(q, v, chunk, gamma, normalize, eps, unmasked)
     o = out if out is not None else torch.empty(q.shape[:3] + (v.shape[-1],), dtype=q.dtype, device=q.device)
     need = hla_forward_workspace_size(p)
     if workspace is None and need:
@@ -229,12 +236,15 @@ def state_combine(A: State, B: State, decay_pow=None, out: State | None = None, 
 
 
 def decode_step(state: State, q, k, v, H: int, gamma=None, normalize: bool = False, eps: float = 0.0,
-                out=None, stream=None):
-    """One decode step for N pairs (q, k [N,d], v [N,dv]); state updated in place."""
+                out=None, stream=None, unmasked: bool = False):
+    """One decode step for N pairs (q [N,d]; k [N/H*Hkv,d], v [N/H*Hkv,dv]); state
+    updated in place."""
     import torch
     N, d = q.shape
     dv = v.shape[-1]
+    Hkv = k.shape[0] * H // N if N else H
     o = out if out is not None else torch.empty((N, dv), dtype=q.dtype, device=q.device)
-    flags = (HLA_NORMALIZE if normalize else 0) | (HLA_DECAY if gamma is not None else 0)
-    hla_decode_step(N, H, d, dv, _dtype_code(q), flags, float(eps), gamma, state, q, k, v, o, stream)
+    flags = (HLA_NORMALIZE if normalize else 0) | (HLA_DECAY if gamma is not None else 0) | \
+        (HLA_UNMASKED if unmasked else 0)
+    hla_decode_step(N, H, Hkv, d, dv, _dtype_code(q), flags, float(eps), gamma, state, q, k, v, o, stream)
     return o

@@ -59,8 +59,11 @@ hla_status check_params(const hla_params *p) {
     if (p->B < 1 || p->H < 1 || p->n < 0) return fail(HLA_ERR_ARG, "need B >= 1, H >= 1, n >= 0");
     if (p->d < 1 || p->dv < 1 || p->chunk < 1) return fail(HLA_ERR_ARG, "need d, dv, chunk >= 1");
     if (p->in_dtype != HLA_F32 && p->in_dtype != HLA_BF16) return fail(HLA_ERR_ARG, "unknown in_dtype");
-    if (p->flags & ~(unsigned)(HLA_NORMALIZE | HLA_DECAY)) return fail(HLA_ERR_ARG, "unknown flag bits");
+    if (p->flags & ~(unsigned)(HLA_NORMALIZE | HLA_DECAY | HLA_UNMASKED))
+        return fail(HLA_ERR_ARG, "unknown flag bits");
     if ((p->flags & HLA_DECAY) && !p->gamma) return fail(HLA_ERR_ARG, "HLA_DECAY needs gamma");
+    if (p->Hkv < 0 || (p->Hkv > 0 && p->H % p->Hkv != 0))
+        return fail(HLA_ERR_ARG, "Hkv must divide H (0 means Hkv = H)");
     if ((p->flags & HLA_NORMALIZE) && !(p->eps >= 0.f)) return fail(HLA_ERR_ARG, "eps must be >= 0");
     if ((long long)p->B * p->H * (long long)p->n * (p->d > p->dv ? p->d : p->dv) > (1LL << 40))
         return fail(HLA_ERR_ARG, "problem too large");
@@ -126,14 +129,15 @@ hla_status hla_forward_chunked(const hla_params *p, const void *q, const void *k
         if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
             return fail(HLA_ERR_ARG, "workspace must be 256-byte aligned");
     }
-    if (p->n == 0) {  // no tokens: state_out = state_in (or zeros)
+    if (p->n == 0) {  // no tokens: state_out = state_in (or zeros); unmasked: G, h zero
         if (!state_out) return HLA_OK;
         const size_t BH = (size_t)p->B * p->H, D = p->d, DV = p->dv;
         const size_t sz[5] = {BH * D * D * 4, BH * D * DV * 4, BH * D * 4, BH * D * DV * 4, BH * D * 4};
         float *dst[5] = {state_out->S, state_out->C, state_out->m, state_out->G, state_out->h};
+        const bool unmasked = (p->flags & HLA_UNMASKED) != 0;
         for (int i = 0; i < 5; ++i) {
             cudaError_t e;
-            if (state_in) {
+            if (state_in && !(unmasked && i >= 3)) {
                 const float *src[5] = {state_in->S, state_in->C, state_in->m, state_in->G, state_in->h};
                 e = cudaMemcpyAsync(dst[i], src[i], sz[i], cudaMemcpyDeviceToDevice, st);
             } else {
@@ -145,6 +149,7 @@ hla_status hla_forward_chunked(const hla_params *p, const void *q, const void *k
     }
     hla::FwdArgs a;
     a.B = p->B; a.H = p->H; a.n = p->n; a.d = p->d; a.dv = p->dv; a.chunk = p->chunk;
+    a.Hkv = p->Hkv > 0 ? p->Hkv : p->H;
     a.in_dtype = p->in_dtype; a.flags = p->flags; a.eps = p->eps; a.gamma = p->gamma;
     a.q = q; a.k = k; a.v = v; a.o = o;
     a.sin = hla::to_ptrs(state_in);
@@ -176,20 +181,29 @@ hla_status hla_state_combine(int count, int d, int dv, const hla_state *A, const
     return HLA_OK;
 }
 
-hla_status hla_decode_step(int N, int H, int d, int dv, hla_dtype dtype, unsigned flags, float eps,
+hla_status hla_decode_step(int N, int H, int Hkv, int d, int dv, hla_dtype dtype, unsigned flags, float eps,
                            const float *gamma, const hla_state *state, const void *q, const void *k,
                            const void *v, void *o, void *stream) {
     if (N < 0 || H < 1 || (N % H) != 0) return fail(HLA_ERR_ARG, "need N >= 0, H >= 1, N %% H == 0");
+    if (Hkv < 0 || (Hkv > 0 && H % Hkv != 0)) return fail(HLA_ERR_ARG, "Hkv must divide H (0 means Hkv = H)");
     if (!width_ok(d) || !width_ok(dv)) return fail(HLA_ERR_UNSUPPORTED, "d, dv must be in {16,32,64,128}");
     if (dtype != HLA_F32 && dtype != HLA_BF16) return fail(HLA_ERR_ARG, "unknown dtype");
-    if (flags & ~(unsigned)(HLA_NORMALIZE | HLA_DECAY)) return fail(HLA_ERR_ARG, "unknown flag bits");
+    if (flags & ~(unsigned)(HLA_NORMALIZE | HLA_DECAY | HLA_UNMASKED))
+        return fail(HLA_ERR_ARG, "unknown flag bits");
     if ((flags & HLA_DECAY) && !gamma) return fail(HLA_ERR_ARG, "HLA_DECAY needs gamma");
     if (!state) return fail(HLA_ERR_ARG, "state must be set");
-    hla_status s = check_state(state, "state");
-    if (s != HLA_OK) return s;
+    hla_status s;
+    if (flags & HLA_UNMASKED) {  // G, h are not part of the unmasked state
+        if (!state->S || !state->C || !state->m) return fail(HLA_ERR_ARG, "state: S, C, m must be set");
+        if (!aligned16(state->S) || !aligned16(state->C) || !aligned16(state->m))
+            return fail(HLA_ERR_ARG, "state: pointers must be 16-byte aligned");
+    } else if ((s = check_state(state, "state")) != HLA_OK) {
+        return s;
+    }
     if (N > 0 && (!q || !k || !v || !o)) return fail(HLA_ERR_ARG, "q, k, v, o must be set");
     hla::DecodeArgs a;
     a.N = N; a.H = H; a.d = d; a.dv = dv; a.dtype = dtype; a.flags = flags; a.eps = eps; a.gamma = gamma;
+    a.Hkv = Hkv > 0 ? Hkv : H;
     a.st = hla::to_ptrs(state);
     a.q = q; a.k = k; a.v = v; a.o = o;
     cudaError_t e = hla::decode_launch(a, static_cast<cudaStream_t>(stream));

@@ -11,6 +11,10 @@
 //   den = g (w.m_{t-1}) + w.q - g^2 (q.h_{t-1}) - g (q.k)(k.m_{t-1}).
 // So each of S, C, G is streamed once from HBM and written once: the kernel is
 // bound by HBM bandwidth (2 x 4 (d^2 + 2 d dv + 2 d) bytes per pair and step).
+// Unmasked variant (o = q^T S_t C_t, skill card "Higher-order linear attention",
+// bullet "Streaming Computation"): o = g z + (w.q) v, den = g (w.m_{t-1}) + w.q;
+// G and h are neither read nor written.  Shared key/value heads: pair u = s*H + h
+// reads key/value row s*Hkv + h/(H/Hkv).
 #include "hla_internal.h"
 
 namespace hla {
@@ -73,21 +77,23 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     const size_t u = blockIdx.x;
     const bool decay = (a.flags & HLA_DECAY) != 0;
     const bool norm = (a.flags & HLA_NORMALIZE) != 0;
+    const bool unm = (a.flags & HLA_UNMASKED) != 0;
     const float g = decay ? a.gamma[u % a.H] : 1.f;
     const float g2 = g * g;
+    const size_t kvu = (u / a.H) * a.Hkv + (u % a.H) / (a.H / a.Hkv);  // key/value row
 
     const T *q = static_cast<const T *>(a.q) + u * D;
-    const T *k = static_cast<const T *>(a.k) + u * D;
-    const T *v = static_cast<const T *>(a.v) + u * DV;
+    const T *k = static_cast<const T *>(a.k) + kvu * D;
+    const T *v = static_cast<const T *>(a.v) + kvu * DV;
     for (int i = tid; i < D; i += kThreads) { qs[i] = ldf(q, i); ks[i] = ldf(k, i); }
     for (int j = tid; j < DV; j += kThreads) vs[j] = ldf(v, j);
     __syncthreads();
 
     float4 *S = reinterpret_cast<float4 *>(a.st.S + u * D * D);
     float4 *C = reinterpret_cast<float4 *>(a.st.C + u * D * DV);
-    float4 *G = reinterpret_cast<float4 *>(a.st.G + u * D * DV);
+    float4 *G = unm ? nullptr : reinterpret_cast<float4 *>(a.st.G + u * D * DV);
     float *m = a.st.m + u * D;
-    float *h = a.st.h + u * D;
+    float *h = unm ? nullptr : a.st.h + u * D;
 
     // ---- S: S_t = g S + k k^T, w = S_t q  (rows of one lane group share a row)
     float4 sv[ITS];
@@ -171,17 +177,17 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     }
     __syncthreads();
 
-    // ---- G: y = G^T q from G_{t-1}; G_t = g^2 G + g k r^T
+    // ---- G: y = G^T q from G_{t-1}; G_t = g^2 G + g k r^T  (masked variant only)
     float4 yp = make_float4(0, 0, 0, 0);
 #pragma unroll
     for (int i = 0; i < ITC; ++i) {
         const int e = tid + i * kThreads;
-        if (e < NC) cv[i] = G[e];
+        if (e < NC && !unm) cv[i] = G[e];
     }
 #pragma unroll
     for (int i = 0; i < ITC; ++i) {
         const int e = tid + i * kThreads;
-        if (e < NC) {
+        if (e < NC && !unm) {
             const int row = e / CGV, cg = e % CGV;
             const float qr = qs[row], gk = g * ks[row];
             float4 x = cv[i];
@@ -208,7 +214,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     // ---- scalars and the m, h vectors
     float pwq = 0.f, pqk = 0.f, pkm = 0.f, pwm = 0.f, pqh = 0.f;
     for (int i = tid; i < D; i += kThreads) {
-        const float mo = m[i], ho = h[i];
+        const float mo = m[i], ho = unm ? 0.f : h[i];
         pwq += ws[i] * qs[i];
         pqk += qs[i] * ks[i];
         pkm += ks[i] * mo;
@@ -222,12 +228,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     if (norm) {
         const float wm = block_sum(pwm, red);
         const float qh = block_sum(pqh, red);
-        den = g * wm + wq - g2 * qh - g * qk * km + a.eps;
+        den = unm ? g * wm + wq + a.eps : g * wm + wq - g2 * qh - g * qk * km + a.eps;
     }
     __syncthreads();  // all reads of m, h done before they are overwritten
     for (int i = tid; i < D; i += kThreads) {
         const float mo = m[i];
-        h[i] = g2 * h[i] + g * ks[i] * km;
+        if (!unm) h[i] = g2 * h[i] + g * ks[i] * km;
         m[i] = g * mo + qs[i];
     }
     T *o = static_cast<T *>(a.o) + u * DV;
@@ -236,7 +242,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
         const float *r = reinterpret_cast<const float *>(&rsum[cg]);
         const float *z = reinterpret_cast<const float *>(&zsum[cg]);
         const float *y = reinterpret_cast<const float *>(&ysum[cg]);
-        const float num = g * z[c] + wq * vs[j] - g2 * y[c] - g * qk * r[c];
+        const float num = unm ? g * z[c] + wq * vs[j] : g * z[c] + wq * vs[j] - g2 * y[c] - g * qk * r[c];
         stf(o, j, norm ? num / den : num);
     }
 }

@@ -14,6 +14,12 @@
 //   o_t    = sum_b M[t,b] v_b + g^{2 tau_t} q_t^T X_p
 //   den_t  = sum_b M[t,b]     + g^{2 tau_t} q_t^T Y_p
 // and the state moves to the chunk end with weights w_b = g^{L - tau_b}.
+// Unmasked variant (o_t = q_t^T S_t C_t = u_t^T C_t; skill card "Higher-order
+// linear attention", bullet "Streaming Computation"): with the same u,
+//   M[t,b] = g^{t-b} u_t.q_b            (b <= t)
+//   o_t    = sum_b M[t,b] v_b + g^{tau_t} u_t^T C_p,  den_t = sum_b M[t,b] + g^{tau_t} u_t.m_p
+// and only S, C, m are carried.  Key/value heads may be shared: query head h
+// reads key/value head h / (H / Hkv).
 #include "hla_internal.h"
 
 namespace hla {
@@ -60,11 +66,13 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
     const int hh = u % a.H;
     const bool decay = (a.flags & HLA_DECAY) != 0;
     const bool norm = (a.flags & HLA_NORMALIZE) != 0;
+    const bool unm = (a.flags & HLA_UNMASKED) != 0;
     const float g = decay ? a.gamma[hh] : 1.f;
     const float lg = log2f(g);
+    const size_t kvu = (size_t)(u / a.H) * a.Hkv + hh / (a.H / a.Hkv);  // key/value head
     const T *q = static_cast<const T *>(a.q) + (size_t)u * a.n * D;
-    const T *k = static_cast<const T *>(a.k) + (size_t)u * a.n * D;
-    const T *v = static_cast<const T *>(a.v) + (size_t)u * a.n * DV;
+    const T *k = static_cast<const T *>(a.k) + kvu * a.n * D;
+    const T *v = static_cast<const T *>(a.v) + kvu * a.n * DV;
     T *o = static_cast<T *>(a.o) + (size_t)u * a.n * DV;
 
     for (int x = tid; x <= 2 * c + 1; x += kThreads) gp[x] = decay ? gpow(lg, (float)x) : 1.f;
@@ -77,13 +85,13 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
         for (int e = tid; e < D * DV; e += kThreads) Cs[e] = Ci[e];
         for (int e = tid; e < D; e += kThreads) m[e] = mi[e];
         __syncthreads();
-        for (int e = tid; e < D * DV; e += kThreads) {  // X = S C - G
+        for (int e = tid; e < D * DV && !unm; e += kThreads) {  // X = S C - G
             const int i = e / DV, j = e % DV;
             float acc = 0.f;
             for (int l = 0; l < D; ++l) acc += S[i * D + l] * Cs[l * DV + j];
             X[e] = acc - Gi[e];
         }
-        for (int i = tid; i < D; i += kThreads) {  // Y = S m - h
+        for (int i = tid; i < D && !unm; i += kThreads) {  // Y = S m - h
             float acc = 0.f;
             for (int l = 0; l < D; ++l) acc += S[i * D + l] * m[l];
             Y[i] = acc - hi[i];
@@ -128,31 +136,38 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
             U[e] = acc;
         }
         __syncthreads();
-        // M[t,b] = g^{2(t-b)} q_t.u_b, b <= t  (overwrites A)
+        // M[t,b] = g^{2(t-b)} q_t.u_b (unmasked: g^{t-b} u_t.q_b), b <= t  (overwrites A)
         for (int e = tid; e < c * c; e += kThreads) {
             const int t = e / c, b = e % c;
             float acc = 0.f;
             if (b <= t) {
-                for (int i = 0; i < D; ++i) acc += Q[t * D + i] * U[b * D + i];
-                acc *= gp[2 * (t - b)];
+                if (unm) {
+                    for (int i = 0; i < D; ++i) acc += U[t * D + i] * Q[b * D + i];
+                    acc *= gp[t - b];
+                } else {
+                    for (int i = 0; i < D; ++i) acc += Q[t * D + i] * U[b * D + i];
+                    acc *= gp[2 * (t - b)];
+                }
             }
             A[e] = acc;
         }
         __syncthreads();
-        // outputs
+        // outputs; the prefix term is g^{2 tau} q^T X_p (masked) or g^{tau} u^T C_p (unmasked)
         for (int e = tid; e < L * DV; e += kThreads) {
             const int t = e / DV, j = e % DV;
             float num = 0.f;
             for (int b = 0; b <= t; ++b) num += A[t * c + b] * V[b * DV + j];
+            const float *lhs = unm ? U + t * D : Q + t * D;
+            const float *Rx = unm ? Cs : X, *Ry = unm ? m : Y;
             float px = 0.f;
-            for (int i = 0; i < D; ++i) px += Q[t * D + i] * X[i * DV + j];
-            const float gt = gp[2 * (t + 1)];
+            for (int i = 0; i < D; ++i) px += lhs[i] * Rx[i * DV + j];
+            const float gt = unm ? gp[t + 1] : gp[2 * (t + 1)];
             num += gt * px;
             if (norm) {
                 float den = 0.f;
                 for (int b = 0; b <= t; ++b) den += A[t * c + b];
                 float py = 0.f;
-                for (int i = 0; i < D; ++i) py += Q[t * D + i] * Y[i];
+                for (int i = 0; i < D; ++i) py += lhs[i] * Ry[i];
                 den += gt * py;
                 num = num / (den + a.eps);
             }
@@ -171,20 +186,20 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
             const int i = e / DV, j = e % DV;
             float ax = 0.f, ac = 0.f;
             for (int b = 0; b < L; ++b) {
-                ax += gp[2 * (L - 1 - b)] * U[b * D + i] * V[b * DV + j];
+                if (!unm) ax += gp[2 * (L - 1 - b)] * U[b * D + i] * V[b * DV + j];
                 ac += gp[L - 1 - b] * Q[b * D + i] * V[b * DV + j];
             }
-            X[e] = g2L * X[e] + ax;
+            if (!unm) X[e] = g2L * X[e] + ax;
             Cs[e] = gL * Cs[e] + ac;
         }
         for (int i = tid; i < D; i += kThreads) {
             float am = 0.f, ay = 0.f;
             for (int b = 0; b < L; ++b) {
                 am += gp[L - 1 - b] * Q[b * D + i];
-                ay += gp[2 * (L - 1 - b)] * U[b * D + i];
+                if (!unm) ay += gp[2 * (L - 1 - b)] * U[b * D + i];
             }
             m[i] = gL * m[i] + am;
-            Y[i] = g2L * Y[i] + ay;
+            if (!unm) Y[i] = g2L * Y[i] + ay;
         }
         __syncthreads();
         // re-tabulate is unnecessary: gp depends only on g
@@ -197,15 +212,15 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
         for (int e = tid; e < D * DV; e += kThreads) {
             const int i = e / DV, j = e % DV;
             float acc = 0.f;  // (S C)[i][j]
-            for (int l = 0; l < D; ++l) acc += S[i * D + l] * Cs[l * DV + j];
+            for (int l = 0; l < D && !unm; ++l) acc += S[i * D + l] * Cs[l * DV + j];
             Co[e] = Cs[e];
-            Go[e] = acc - X[e];
+            Go[e] = unm ? 0.f : acc - X[e];  // G is not part of the unmasked state
         }
         for (int i = tid; i < D; i += kThreads) {
             float acc = 0.f;
-            for (int l = 0; l < D; ++l) acc += S[i * D + l] * m[l];
+            for (int l = 0; l < D && !unm; ++l) acc += S[i * D + l] * m[l];
             mo[i] = m[i];
-            ho[i] = acc - Y[i];
+            ho[i] = unm ? 0.f : acc - Y[i];
         }
     }
 }

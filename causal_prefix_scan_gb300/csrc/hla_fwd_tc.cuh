@@ -73,6 +73,7 @@ inline int ctas_per_sm(const hla_params &p) { return tmem_cols(p.chunk, p.d, p.d
 struct TcParams {
     CUtensorMap tmQ, tmK, tmV, tmO;
     int B, H, n, BH;
+    int Hkv;  // key/value heads: query head h reads key/value head h / (H / Hkv)
     // work split: the BH sequences' chunks, laid end to end, are cut into runs of
     // cpc chunks, one per CTA; a run that crosses a sequence boundary holds a
     // piece of each sequence.  A sequence has at most kmax pieces.
@@ -166,7 +167,7 @@ __device__ __forceinline__ int row_of(int q, int l) {
     else return 16 * q + (l & 15);
 }
 
-template <int C, int D, int DV, bool DECAY, bool NORM>
+template <int C, int D, int DV, bool DECAY, bool NORM, bool UNM>
 struct Kern {
     using K_ = Cfg<C, D, DV>;
     static constexpr uint32_t TW = K_::TW, TS = K_::TS, TX = K_::TX, T4 = K_::T4;
@@ -200,6 +201,7 @@ struct Kern {
     int tid, warp, lane, quad, half;
     int rowC, rowD;  // rows this thread owns in token-row / state accumulators (-1: none)
     int bh;
+    int kvh;  // key/value head (b * Hkv + h / (H / Hkv)) of pair bh
     float lg;
     bool need_mY;
 
@@ -312,10 +314,10 @@ struct Kern {
 #pragma unroll
             for (int kb = 0; kb < D / 64; ++kb) {
                 tma_load_3d(sQ(s) + kb * C * 128, &P.tmQ, tma_bar + s, kb * 64, t0, bh);
-                tma_load_3d(sK(s) + kb * C * 128, &P.tmK, tma_bar + s, kb * 64, t0, bh);
+                tma_load_3d(sK(s) + kb * C * 128, &P.tmK, tma_bar + s, kb * 64, t0, kvh);
             }
 #pragma unroll
-            for (int kb = 0; kb < DV / 64; ++kb) tma_load_3d(sV(s) + kb * C * 128, &P.tmV, tma_bar + s, kb * 64, t0, bh);
+            for (int kb = 0; kb < DV / 64; ++kb) tma_load_3d(sV(s) + kb * C * 128, &P.tmV, tma_bar + s, kb * 64, t0, kvh);
         }
     }
 
@@ -721,17 +723,50 @@ struct Kern {
             *reinterpret_cast<float4 *>(dst + sofs(rowD, c0 + c)) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
     }
 
-    // Write the summary (S, X, C, m, Y) of this CTA to `dst`.
+    // Write the summary (S, X, C, m, Y) of this CTA to `dst`.  The unmasked
+    // variant keeps its running C in the X slot of TMEM and has no X, Y.
     __device__ void store_summary(float *dst) {
         float *S = dst, *X = S + D * D, *Cc = X + D * DV, *m = Cc + D * DV, *Y = m + D;
         put_share<D>(TS, S);
-        put_share<DV>(TX, X);
-        put_share<DV>(T4, Cc);
-        for (int i = tid; i < D; i += kThreads) { m[i] = mrun()[i]; Y[i] = Yrun()[i]; }
+        if constexpr (UNM) {
+            put_share<DV>(TX, Cc);
+            for (int i = tid; i < D; i += kThreads) m[i] = mrun()[i];
+        } else {
+            put_share<DV>(TX, X);
+            put_share<DV>(T4, Cc);
+            for (int i = tid; i < D; i += kThreads) { m[i] = mrun()[i]; Y[i] = Yrun()[i]; }
+        }
     }
 
     // ======================================================================== scan
     __device__ bool prefix_init() {
+        if constexpr (UNM) {  // S -> TS, C -> TX, m -> mrun(); G, h are not part of the state
+            if (!P.sin.S) {
+                zero_slot<D, D>(TS);
+                zero_slot<D, DV>(TX);
+                for (int i = tid; i < D; i += kThreads) mrun()[i] = 0.f;
+            } else {
+                const float *Si = P.sin.S + (size_t)bh * D * D, *Ci = P.sin.C + (size_t)bh * D * DV;
+                const float *mi = P.sin.m + (size_t)bh * D;
+                rmw_row<D, D>(TS, [&](int c0, float (&v)[16]) {
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4) {
+                        const float4 a = *reinterpret_cast<const float4 *>(Si + rowD * D + c0 + i);
+                        v[i] = a.x; v[i + 1] = a.y; v[i + 2] = a.z; v[i + 3] = a.w;
+                    }
+                });
+                rmw_row<D, DV>(TX, [&](int c0, float (&v)[16]) {
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4) {
+                        const float4 a = *reinterpret_cast<const float4 *>(Ci + rowD * DV + c0 + i);
+                        v[i] = a.x; v[i + 1] = a.y; v[i + 2] = a.z; v[i + 3] = a.w;
+                    }
+                });
+                for (int i = tid; i < D; i += kThreads) mrun()[i] = mi[i];
+            }
+            publish();
+            return true;
+        }
         if (!P.sin.S) {
             zero_slot<D, D>(TS);
             zero_slot<D, DV>(TX);
@@ -1207,6 +1242,243 @@ struct Kern {
         __syncthreads();
         return true;
     }
+
+    // ======================================================================== unmasked variant
+    // o_t = q_t^T S_t C_t = u_t^T C_t with u_t = S_t q_t (skill card "Higher-order
+    // linear attention", bullet "Streaming Computation").  Per chunk, with U as in
+    // the masked path:
+    //   M' = tril(Gamma1 o U Q^T),   O = M' V + diag(g^tau) U C_p,
+    //   den = rowsum(M') + diag(g^tau) U m_p,
+    // and S, C, m move to the chunk end.  TMEM: work W, S, C (in the X slot), spare.
+
+    // Pass 1: the piece's S, C, m from zero; every weight is relative to the piece
+    // end (g^{LB - tau}), so nothing is rescaled per chunk and no U is needed.
+    __device__ bool pass1_unm(int jb, int je) {
+        for (int i = tid; i < D; i += kThreads) mrun()[i] = 0.f;
+        const int LB = min(P.n, je * C) - jb * C;
+        int stage = 0;
+        tma_chunk(jb, 0);
+        for (int jj = jb; jj < je; ++jj) {
+            const bool first = (jj == jb);
+            const int L = min(C, P.n - jj * C);
+            const int rest = LB - (jj - jb) * C - L;
+            if (K_::NSTAGE == 1 && !first) tma_chunk(jj, 0);
+            uint8_t *Q = sQ(stage), *Kt = sK(stage), *V = sV(stage);
+            if (!wait_tma(stage)) return false;
+            if (K_::NSTAGE == 2 && jj + 1 < je) tma_chunk(jj + 1, stage ^ 1);
+            if constexpr (DECAY) {  // K_w, V_w: rows weighted by g^{rest + L - 1 - tau}
+                scaled_tile_copy<D>(Kt, tA(), [&](int r) { return r < L ? gp(rest + L - 1 - r) : 0.f; });
+                scaled_tile_copy<DV>(V, tS(), [&](int r) { return r < L ? gp(rest + L - 1 - r) : 0.f; });
+            }
+            publish();
+            if (tid == 0) {
+                mma_mm<D>(TS, Kt, DECAY ? tA() : Kt, !first);  // S += K^T W K
+                mma_mm<DV>(TX, Q, DECAY ? tS() : V, !first);   // C += Q^T W V
+            }
+            commit();
+            if (need_mY)  // m += sum_tau g^{rest + L - 1 - tau} q_tau; scratch: tQ
+                tile_colsums<false>(Q, nullptr, L, gp(rest), reinterpret_cast<float *>(tQ()), mrun(), 1.f,
+                                    nullptr, 1.f);
+            if (!wait_mma()) return false;
+            stage ^= (K_::NSTAGE - 1);
+        }
+        return true;
+    }
+
+    // prefix <- prefix (+) L_0 (+) ... (+) L_{cnt-1} for the unmasked state: the
+    // linear part of the concatenation rule, S <- f S + S_L, C <- f C + C_L,
+    // m <- f m + m_L (f = g^{len L}).  `zero_prefix`: step 0 sets the prefix.
+    template <typename Start>
+    __device__ bool fold_unm(const float *Lsum, int cnt, Start &&start, bool zero_prefix) {
+        constexpr int NS = share<D>(), NV = share<DV>();
+        const int cs = share_col<D>(), cv = share_col<DV>();
+        for (int r = 0; r < cnt; ++r) {
+            const float *SL = Lsum + (size_t)r * K_::SUM, *CL = SL + D * D + D * DV, *mL = CL + D * DV;
+            const float f = gp(start(r + 1) - start(r));
+            const bool z = zero_prefix && r == 0;
+            const float mLi = tid < D ? __ldcg(mL + tid) : 0.f;
+#pragma unroll
+            for (int c = 0; c < NS; c += 16) {
+                float s[16], v[16];
+                ld_sum16(SL, rowD, cs + c, s);
+                if (!z) {
+                    ld_share<D>(TS, c, v);
+                    tmem_wait_ld();
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = z ? s[i] : f * v[i] + s[i];
+                st_share<D>(TS, c, v);
+            }
+#pragma unroll
+            for (int c = 0; c < NV; c += 16) {
+                float s[16], v[16];
+                ld_sum16(CL, rowD, cv + c, s);
+                if (!z) {
+                    ld_share<DV>(TX, c, v);
+                    tmem_wait_ld();
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = z ? s[i] : f * v[i] + s[i];
+                st_share<DV>(TX, c, v);
+            }
+            tmem_wait_st();
+            if (tid < D) mrun()[tid] = z ? mLi : f * mrun()[tid] + mLi;
+        }
+        tc_sync();
+        return true;
+    }
+
+    // State export, part 1 (unmasked): pass 2 carries S and C (and m with
+    // normalisation) to the sequence end; without normalisation m is combined
+    // here: m = f m_prefix + m_L -> mrun() and state_out.
+    __device__ void export_pre_unm(const float *Lown, float f) {
+        if constexpr (!NORM) {
+            const float *mL = Lown + D * D + 2 * D * DV;
+            float *mo = P.sout.m + (size_t)bh * D;
+            if (tid < D) mrun()[tid] = mo[tid] = f * mrun()[tid] + __ldcg(mL + tid);
+            __syncthreads();
+        }
+    }
+
+    // State export, part 2 (unmasked): S, C, m at the sequence end; G and h are
+    // not part of this variant and are written as zeros.
+    __device__ void export_post_unm() {
+        float *So = P.sout.S + (size_t)bh * D * D, *Co = P.sout.C + (size_t)bh * D * DV;
+        float *mo = P.sout.m + (size_t)bh * D, *Go = P.sout.G + (size_t)bh * D * DV, *ho = P.sout.h + (size_t)bh * D;
+        constexpr int NS = share<D>(), NV = share<DV>();
+        const int cs = share_col<D>(), cv = share_col<DV>();
+#pragma unroll
+        for (int c = 0; c < NS; c += 16) {
+            float v[16];
+            ld_share<D>(TS, c, v);
+            tmem_wait_ld();
+            st_row16(So + rowD * D + cs + c, v);
+        }
+#pragma unroll
+        for (int c = 0; c < NV; c += 16) {
+            float v[16], zero[16];
+            ld_share<DV>(TX, c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) zero[i] = 0.f;
+            st_row16(Co + rowD * DV + cv + c, v);
+            st_row16(Go + rowD * DV + cv + c, zero);
+        }
+        for (int i = tid; i < D; i += kThreads) { mo[i] = mrun()[i]; ho[i] = 0.f; }
+    }
+
+    // Pass 2 (unmasked): outputs from the exact prefix (S in TS, C in TX, m).
+    __device__ bool pass2_unm(int jb, int je) {
+        int stage = 0;
+        tma_chunk(jb, 0);
+        for (int jj = jb; jj < je; ++jj) {
+            const int t0 = jj * C;
+            const int L = min(C, P.n - t0);
+            uint8_t *Q = sQ(stage), *Kt = sK(stage), *V = sV(stage);
+            if (tid == 0) bulk_wait_read();  // the previous chunk's O store has left tS()
+            if (!wait_tma(stage)) return false;
+            if (K_::NSTAGE == 2 && jj + 1 < je) tma_chunk(jj + 1, stage ^ 1);
+            if (tid == 0) mma_kk<C, D>(TW, Q, Kt, false);  // A = Q K^T
+            commit();
+            // meanwhile: S_p -> bf16 operand, then decay S to the chunk end
+            extract_state<D>(TS, tS(), gp(L));
+            publish();
+            if (tid == 0) mma_kk<D, D>(T4, Q, tS(), false);  // spare = Q S_p
+            commit2();
+            // meanwhile: C_p -> bf16 operand (rows d, MN-major for U C_p), decay C
+            extract_state<DV>(TX, tQ(), gp(L));
+            if (!wait_mma()) return false;  // A
+            epi_atilde();
+            publish();
+            if (tid == 0) mma_km<D, C>(TW, tA(), Kt, false);  // W = A-tilde K
+            commit();
+            if (!wait_mma2()) return false;  // Q S_p
+            if (!wait_mma()) return false;   // A-tilde K
+            // U = g^tau Q S_p + A-tilde K -> tU(); with normalisation, row partials of
+            // u_t . m_p (into rsum(), free until the M' epilogue)
+            {
+                const float gt = (DECAY && rowC >= 0) ? gp(rowC + 1) : 1.f;
+                float um = 0.f;
+                for_row2<C, D>(TW, T4, [&](int c0, float (&v)[16], float (&sp)[16]) {
+                    if (rowC < 0) return;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        v[i] += gt * sp[i];
+                        if constexpr (NORM) um += v[i] * mrun()[c0 + i];
+                    }
+                    tile_store_row16(tU(), C, rowC, c0, v);
+                });
+                if constexpr (NORM) put_partial<C>(rsum(), rowC, um);
+            }
+            if constexpr (DECAY) {  // K_w, V_w: rows weighted by g^{L - 1 - tau}
+                scaled_tile_copy<D>(Kt, tA(), [&](int r) { return r < L ? gp(L - 1 - r) : 0.f; });
+                scaled_tile_copy<DV>(V, tS(), [&](int r) { return r < L ? gp(L - 1 - r) : 0.f; });
+            }
+            publish();
+            if (tid == 0) {
+                mma_kk<C, D>(TW, tU(), Q, false);             // M' = U Q^T
+                mma_mm<D>(TS, Kt, DECAY ? tA() : Kt, true);   // S += K^T W K (reads tA(): done before
+            }                                                // the M' epilogue rewrites tA())
+            commit();
+            if (tid == 0) {
+                mma_mm<DV>(TX, Q, DECAY ? tS() : V, true);    // C += Q^T W V
+                mma_km<DV, D>(T4, tU(), tQ(), false);         // spare = U C_p
+            }
+            commit2();
+            if constexpr (NORM) {  // den = u . m_p, before m moves on
+                if (tid < C) den()[tid] = sum_partials<C>(rsum(), tid);
+            }
+            if (!wait_mma()) return false;  // M' and the S update
+            // M' = tril(Gamma1 o U Q^T) -> tA(), row sums for the denominator
+            {
+                float rs = 0.f;
+                float gt1[3];
+                load_g16<1>(gt1);
+                for_row<C, C>(TW, [&](int c0, float (&v)[16]) {
+                    if (rowC < 0) return;
+                    mask_row<1>(rowC, c0, v, gt1);
+                    if constexpr (NORM) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) rs += v[i];
+                    }
+                    tile_store_row16(tA(), C, rowC, c0, v);
+                });
+                if constexpr (NORM) put_partial<C>(rsum(), rowC, rs);
+            }
+            publish();
+            if (tid == 0) mma_km<DV, C>(TW, tA(), V, false);  // O = M' V
+            commit();
+            if (!wait_mma2()) return false;  // C update and U C_p
+            if (!wait_mma()) return false;   // M' V
+            if constexpr (NORM)  // m <- g^L m + sum_tau g^{L - 1 - tau} q_tau (scratch: tQ, read by U C_p)
+                tile_colsums<false>(Q, nullptr, L, 1.f, reinterpret_cast<float *>(tQ()), mrun(), gp(L), nullptr,
+                                    1.f);
+            if (K_::NSTAGE == 1 && jj + 1 < je) tma_chunk(jj + 1, 0);
+            {
+                const float g1t = (DECAY && rowC >= 0) ? gp(rowC + 1) : 1.f;
+                float inv = 1.f;
+                if constexpr (NORM) {
+                    if (rowC >= 0) inv = 1.f / (sum_partials<C>(rsum(), rowC) + g1t * den()[rowC] + P.eps);
+                }
+                for_row2<C, DV>(TW, T4, [&](int c0, float (&v)[16], float (&sp)[16]) {
+                    if (rowC < 0) return;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = (v[i] + g1t * sp[i]) * inv;
+                    tile_store_row16(tS(), C, rowC, c0, v);
+                });
+            }
+            publish();
+            if (tid == 0) {
+#pragma unroll
+                for (int kb = 0; kb < DV / 64; ++kb) tma_store_3d(tS() + kb * C * 128, &P.tmO, kb * 64, t0, bh);
+                bulk_commit();
+            }
+            stage ^= (K_::NSTAGE - 1);
+        }
+        if (tid == 0) bulk_wait_read();
+        __syncthreads();
+        return true;
+    }
 };
 
 // The last CTA to finish returns the workspace header and flags to zero, so the
@@ -1223,7 +1495,7 @@ __device__ __forceinline__ void finish_cta(const TcParams &P) {
     }
 }
 
-template <int C, int D, int DV, bool DECAY, bool NORM>
+template <int C, int D, int DV, bool DECAY, bool NORM, bool UNM>
 __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(const __grid_constant__ TcParams P) {
     using K_ = Cfg<C, D, DV>;
     // No static shared memory: the dynamic block starts at the (1024-byte
@@ -1235,7 +1507,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
     int *ticket_p = reinterpret_cast<int *>(base + K_::OFF_BAR + 36);
     int *misalign_p = reinterpret_cast<int *>(base + K_::OFF_BAR + 40);
 
-    Kern<C, D, DV, DECAY, NORM> x(P, base);
+    Kern<C, D, DV, DECAY, NORM, UNM> x(P, base);
     x.tid = threadIdx.x;
     x.warp = threadIdx.x >> 5;
     x.lane = threadIdx.x & 31;
@@ -1309,6 +1581,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
         if (bh == x.bh) return;
         __syncthreads();  // every thread is done with the previous sequence's table
         x.bh = bh;
+        x.kvh = (bh / P.H) * P.Hkv + (bh % P.H) / (P.H / P.Hkv);
         float g = 1.f;
         if constexpr (DECAY) g = P.gamma[bh % P.H];
         x.lg = log2f(g);
@@ -1325,7 +1598,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
             const Piece pc = piece(bh);
             if (pc.last && !want_out) continue;
             select(bh);
-            if (!(ok = x.pass1(pc.jb, pc.je))) break;
+            if constexpr (UNM) ok = x.pass1_unm(pc.jb, pc.je);
+            else ok = x.pass1(pc.jb, pc.je);
+            if (!ok) break;
             x.store_summary(P.summ + ((size_t)bh * P.kmax + pc.k) * K_::SUM);
             // the block barrier orders every thread's summary stores before the
             // release store of the flag, which makes them visible at gpu scope
@@ -1350,15 +1625,27 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
             }
             if (pc.k > 0) {  // with a zero state_in the first fold step sets the prefix
                 if (!(ok = x.wait_flags(0, pc.k))) break;
-                if (!(ok = x.fold_all(P.summ + (size_t)bh * P.kmax * K_::SUM, pc.k, start, !P.sin.S))) break;
+                const float *Ls = P.summ + (size_t)bh * P.kmax * K_::SUM;
+                if constexpr (UNM) ok = x.fold_unm(Ls, pc.k, start, !P.sin.S);
+                else ok = x.fold_all(Ls, pc.k, start, !P.sin.S);
+                if (!ok) break;
             }
             // ---- state export, part 1: what pass 2 does not carry to the sequence end
-            if (pc.last && want_out)
-                x.export_pre(P.summ + ((size_t)bh * P.kmax + pc.k) * K_::SUM,
-                             DECAY ? gpow(x.lg, (float)(P.n - start(pc.k))) : 1.f);
-            if (!(ok = x.pass2(pc.jb, pc.je))) break;
+            if (pc.last && want_out) {
+                const float *Lown = P.summ + ((size_t)bh * P.kmax + pc.k) * K_::SUM;
+                const float fown = DECAY ? gpow(x.lg, (float)(P.n - start(pc.k))) : 1.f;
+                if constexpr (UNM) x.export_pre_unm(Lown, fown);
+                else x.export_pre(Lown, fown);
+            }
+            if constexpr (UNM) ok = x.pass2_unm(pc.jb, pc.je);
+            else ok = x.pass2(pc.jb, pc.je);
+            if (!ok) break;
             // ---- state export, part 2: the final state at the sequence end
-            if (pc.last && want_out && !(ok = x.export_post())) break;
+            if (pc.last && want_out) {
+                if constexpr (UNM) x.export_post_unm();
+                else ok = x.export_post();
+                if (!ok) break;
+            }
         }
     } while (0);
 
@@ -1435,7 +1722,7 @@ inline WsLayout ws_layout(const hla_params &p, const Plan &pl) {
     return w;
 }
 
-template <int C, int D, int DV, bool DECAY, bool NORM>
+template <int C, int D, int DV, bool DECAY, bool NORM, bool UNM>
 cudaError_t launch_cfg(const FwdArgs &a, cudaStream_t st, int num_sms) {
     using K_ = Cfg<C, D, DV>;
     hla_params p{a.B, a.H, a.n, a.d, a.dv, a.chunk, a.in_dtype, a.flags, a.eps, a.gamma};
@@ -1443,11 +1730,11 @@ cudaError_t launch_cfg(const FwdArgs &a, cudaStream_t st, int num_sms) {
     const WsLayout wl = ws_layout(p, pl);
     TcParams P;
     memset(&P, 0, sizeof P);
-    const int BH = a.B * a.H;
-    if (!encode_3d(&P.tmQ, a.q, D, a.n, BH, C) || !encode_3d(&P.tmK, a.k, D, a.n, BH, C) ||
-        !encode_3d(&P.tmV, a.v, DV, a.n, BH, C) || !encode_3d(&P.tmO, a.o, DV, a.n, BH, C))
+    const int BH = a.B * a.H, BHkv = a.B * a.Hkv;
+    if (!encode_3d(&P.tmQ, a.q, D, a.n, BH, C) || !encode_3d(&P.tmK, a.k, D, a.n, BHkv, C) ||
+        !encode_3d(&P.tmV, a.v, DV, a.n, BHkv, C) || !encode_3d(&P.tmO, a.o, DV, a.n, BH, C))
         return cudaErrorInvalidValue;
-    P.B = a.B; P.H = a.H; P.n = a.n; P.BH = BH;
+    P.B = a.B; P.H = a.H; P.n = a.n; P.BH = BH; P.Hkv = a.Hkv;
     P.nchunks = pl.nchunks; P.cpc = pl.cpc; P.kmax = pl.kmax;
     P.runs_per_seq = pl.nchunks % pl.cpc == 0 ? pl.nchunks / pl.cpc : 0;
     P.eps = a.eps; P.gamma = a.gamma;
@@ -1457,7 +1744,7 @@ cudaError_t launch_cfg(const FwdArgs &a, cudaStream_t st, int num_sms) {
     P.flagsw = reinterpret_cast<unsigned *>(ws + wl.off_flags);
     P.summ = reinterpret_cast<float *>(ws + wl.off_summ);
     P.err = a.err;
-    auto kern = fwd_tc_kernel<C, D, DV, DECAY, NORM>;
+    auto kern = fwd_tc_kernel<C, D, DV, DECAY, NORM, UNM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K_::SMEM_LAUNCH);
     if (e != cudaSuccess) return e;
     kern<<<pl.ncta, kThreads, K_::SMEM_LAUNCH, st>>>(P);
@@ -1466,18 +1753,18 @@ cudaError_t launch_cfg(const FwdArgs &a, cudaStream_t st, int num_sms) {
 
 // Launcher for one (decay, normalise) combination over all supported shapes;
 // explicitly instantiated in hla_fwd_tc_f<flags>.cu.
-template <bool DECAY, bool NORM>
+template <bool DECAY, bool NORM, bool UNM>
 cudaError_t launch_flags(const FwdArgs &a, cudaStream_t st, int ns) {
     const int key = (a.chunk == 128 ? 4 : 0) | (a.d == 128 ? 2 : 0) | (a.dv == 128 ? 1 : 0);
     switch (key) {
-        case 0: return launch_cfg<64, 64, 64, DECAY, NORM>(a, st, ns);
-        case 1: return launch_cfg<64, 64, 128, DECAY, NORM>(a, st, ns);
-        case 2: return launch_cfg<64, 128, 64, DECAY, NORM>(a, st, ns);
-        case 3: return launch_cfg<64, 128, 128, DECAY, NORM>(a, st, ns);
-        case 4: return launch_cfg<128, 64, 64, DECAY, NORM>(a, st, ns);
-        case 5: return launch_cfg<128, 64, 128, DECAY, NORM>(a, st, ns);
-        case 6: return launch_cfg<128, 128, 64, DECAY, NORM>(a, st, ns);
-        default: return launch_cfg<128, 128, 128, DECAY, NORM>(a, st, ns);
+        case 0: return launch_cfg<64, 64, 64, DECAY, NORM, UNM>(a, st, ns);
+        case 1: return launch_cfg<64, 64, 128, DECAY, NORM, UNM>(a, st, ns);
+        case 2: return launch_cfg<64, 128, 64, DECAY, NORM, UNM>(a, st, ns);
+        case 3: return launch_cfg<64, 128, 128, DECAY, NORM, UNM>(a, st, ns);
+        case 4: return launch_cfg<128, 64, 64, DECAY, NORM, UNM>(a, st, ns);
+        case 5: return launch_cfg<128, 64, 128, DECAY, NORM, UNM>(a, st, ns);
+        case 6: return launch_cfg<128, 128, 64, DECAY, NORM, UNM>(a, st, ns);
+        default: return launch_cfg<128, 128, 128, DECAY, NORM, UNM>(a, st, ns);
     }
 }
 

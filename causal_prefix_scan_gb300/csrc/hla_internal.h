@@ -22,6 +22,7 @@ inline StatePtrs to_ptrs(const hla_state *s) {
 
 struct FwdArgs {
     int B, H, n, d, dv, chunk;
+    int Hkv;  // key/value heads (H % Hkv == 0)
     hla_dtype in_dtype;
     unsigned flags;
     float eps;
@@ -52,6 +53,7 @@ cudaError_t combine_launch(const CombineArgs &a, cudaStream_t st);
 
 struct DecodeArgs {
     int N, H, d, dv;
+    int Hkv;  // key/value heads per sequence (H % Hkv == 0)
     hla_dtype dtype;
     unsigned flags;
     float eps;

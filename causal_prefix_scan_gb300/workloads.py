@@ -7,7 +7,8 @@ CUDA side (tests, benchmark) take their inputs from here, so they see the same
 values.
 
 Recipe: numpy ``default_rng(seed)``, draws in the order q, k, v, gamma, each as
-float32 standard normals of the full [B,H,n,d] / [B,H,n,dv] shape, then the
+float32 standard normals of the full [B,H,n,d] / [B,Hkv,n,d] / [B,Hkv,n,dv] shape
+(Hkv = H unless keys and values are shared by head groups), then the
 workload's preprocessing, then rounding to the input dtype (round to nearest
 even for bf16).  The oracle reads the rounded values exactly.
 """
@@ -36,6 +37,12 @@ class Workload:
     gamma_hi: float = 0.999
     seed: int = 0
     note: str = field(default="", compare=False)
+    unmasked: bool = False    # unmasked variant o = q^T S C
+    Hkv: int = 0              # key/value heads (0: H); query head h reads head h // (H // Hkv)
+
+    @property
+    def kv_heads(self) -> int:
+        return self.Hkv or self.H
 
     @property
     def tokens(self) -> int:
@@ -58,7 +65,12 @@ FWD_NORM = Workload("fwd_bf16_norm_B2H16n8192d64dv128", 2, 16, 8192, 64, 128, 64
                     normalize=True, eps=1e-6, seed=3)
 FWD_DECAY = Workload("fwd_bf16_decay_B1H32n32768d128", 1, 32, 32768, 128, 128, 128, "bf16", "l2",
                      decay=True, seed=4)
-WORKLOADS = {w.name: w for w in (SMALL_F32, FWD_BF16, FWD_NORM, FWD_DECAY)}
+# Widening beyond the masked forward: the unmasked variant, and keys/values shared
+# by groups of query heads, on the shape of the B4H8n2048d64 workload.
+FWD_UNMASKED = Workload("fwd_bf16_unmasked_B4H8n2048d64", 4, 8, 2048, 64, 64, 64, "bf16", "l2", seed=6,
+                        unmasked=True)
+FWD_SHARED_KV = Workload("fwd_bf16_kv2_B4H8n2048d64", 4, 8, 2048, 64, 64, 64, "bf16", "l2", seed=7, Hkv=2)
+WORKLOADS = {w.name: w for w in (SMALL_F32, FWD_BF16, FWD_NORM, FWD_DECAY, FWD_UNMASKED, FWD_SHARED_KV)}
 
 
 @dataclass(frozen=True)
@@ -109,8 +121,8 @@ def make_inputs(w: Workload):
     float32 or None."""
     rng = np.random.default_rng(w.seed)
     q = rng.standard_normal((w.B, w.H, w.n, w.d), dtype=np.float32)
-    k = rng.standard_normal((w.B, w.H, w.n, w.d), dtype=np.float32)
-    v = rng.standard_normal((w.B, w.H, w.n, w.dv), dtype=np.float32)
+    k = rng.standard_normal((w.B, w.kv_heads, w.n, w.d), dtype=np.float32)
+    v = rng.standard_normal((w.B, w.kv_heads, w.n, w.dv), dtype=np.float32)
     gamma = None
     if w.decay:
         lo, hi = np.log(w.gamma_lo), np.log(w.gamma_hi)
@@ -152,8 +164,8 @@ def make_inputs_device(w: Workload, device="cuda"):
         return x.to(dt)
 
     q = draw((w.B, w.H, w.n, w.d), w.qk, w.d)
-    k = draw((w.B, w.H, w.n, w.d), w.qk, w.d)
-    v = draw((w.B, w.H, w.n, w.dv), "none", w.dv)
+    k = draw((w.B, w.kv_heads, w.n, w.d), w.qk, w.d)
+    v = draw((w.B, w.kv_heads, w.n, w.dv), "none", w.dv)
     gamma = None
     if w.decay:
         u = torch.rand((w.H,), generator=g, device=device, dtype=torch.float64)

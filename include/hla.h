@@ -1,7 +1,7 @@
 /*
- * hla.h -- C ABI of the GB300 (sm_103a) library for the masked second-order
- * Higher-order Linear Attention (HLA) forward, its segment concatenation and
- * its single-token decode step.
+ * hla.h -- C ABI of the GB300 (sm_103a) library for the second-order
+ * Higher-order Linear Attention (HLA) forward (masked, and unmasked with
+ * HLA_UNMASKED), its segment concatenation and its single-token decode step.
  *
  * Definitions (gist.science technical summary of "Higher-order Linear
  * Attention"):
@@ -22,6 +22,15 @@
  *       q v^T, m_t = g m_{t-1} + q), and G_t = g^2 G_{t-1} + g k_t (k_t^T C_{t-1}),
  *       h_t = g^2 h_{t-1} + g k_t (k_t^T m_{t-1}); g = 1 is the undecayed case.
  *
+ * Unmasked variant (skill card "Higher-order linear attention", section
+ * "Linear-Time Higher-Order Interactions", bullet "Streaming Computation"):
+ *       o_t = q_t^T S_t C_t, ratio form o_t = q_t^T S_t C_t / (q_t^T S_t m_t + eps),
+ *   with the same decayed S, C, m; G and h are not part of this variant.
+ * Shared key/value heads (same card, section "Architecture Overview", bullet
+ *   "Multi-Head Support"): k and v may carry Hkv heads, H a multiple of Hkv;
+ *   query head h reads key/value head h / (H / Hkv).  The summaries stay per
+ *   query head.
+ *
  * Conventions shared by every call
  *   - All tensors are caller-owned device memory; the library never allocates
  *     or frees device memory.  Inputs are read-only.
@@ -32,7 +41,8 @@
  *     device flag that hla_sync_status() reports.
  *   - On any status other than HLA_OK nothing was launched, except HLA_ERR_CUDA
  *     from a failed launch; hla_last_error() gives a message.
- *   - Layout: q, k are [B][H][n][d]; v, o are [B][H][n][dv]; all contiguous,
+ *   - Layout: q is [B][H][n][d], k [B][Hkv][n][d], v [B][Hkv][n][dv], o
+ *     [B][H][n][dv] (Hkv = H unless key/value heads are shared); all contiguous,
  *     row-major, 16-byte aligned, element type `in_dtype` (o has the input type;
  *     accumulation is fp32, the store rounds to nearest even).
  *   - State (one block per (b,h) pair, pair index u = b*H + h, fp32, contiguous,
@@ -67,7 +77,9 @@ typedef enum { HLA_F32 = 0, HLA_BF16 = 1 } hla_dtype;
 
 enum {
     HLA_NORMALIZE = 1u,  /* ratio-normalised output (section 1, "Normalisatie")          */
-    HLA_DECAY = 2u       /* per-head exponential decay ("Belangrijkste bijdragen", item 2) */
+    HLA_DECAY = 2u,      /* per-head exponential decay ("Belangrijkste bijdragen", item 2) */
+    HLA_UNMASKED = 4u    /* unmasked output o = q^T S C (skill card, "Streaming Computation");
+                            state carries S, C, m; G and h are written as zeros          */
 };
 
 typedef struct {
@@ -79,6 +91,7 @@ typedef struct {
     float eps;            /* added to the denominator when HLA_NORMALIZE               */
     const float *gamma;   /* [H] device fp32 decay factors in [0,1]; required with
                              HLA_DECAY, ignored otherwise                               */
+    int Hkv;              /* key/value heads (H % Hkv == 0); 0 means H                  */
 } hla_params;
 
 /* The five summaries of B*H (or N) pairs; all five pointers set, or the whole
@@ -114,7 +127,8 @@ HLA_API size_t hla_forward_workspace_size(const hla_params *p);
  *   o         output [B][H][n][dv], in_dtype;
  *   state_in  state before the first token, or NULL for zeros;
  *   state_out state after the last token (S, C, m, G, h), or NULL to skip; may
- *             not alias state_in;
+ *             not alias state_in.  With HLA_UNMASKED, G and h of state_in are
+ *             ignored and those of state_out are written as zeros;
  *   workspace device scratch of at least hla_forward_workspace_size(p) bytes,
  *             256-byte aligned, set to zero before its first use; every call
  *             (also one that ends in HLA_ERR_TIMEOUT) leaves its header and flags
@@ -143,16 +157,19 @@ HLA_API hla_status hla_state_combine(int count, int d, int dv, const hla_state *
 
 /*
  * One decode step (section 1 recurrence applied to a single new token) for N
- * independent (sequence, head) pairs; pair u uses gamma[u % H] when
+ * independent (sequence, head) pairs, pair u = s*H + h; pair u uses gamma[h] when
  * HLA_DECAY is set.  The fp32 state is updated in place: the cross summaries
  * from C_{t-1}, m_{t-1}, then S, C, m; the output is
  * o = q^T (S_t C_t - G_t) (divided by q^T (S_t m_t - h_t) + eps with
- * HLA_NORMALIZE).
- *   q, k: [N][d]; v, o: [N][dv]; element type `dtype` (HLA_F32 or HLA_BF16);
+ * HLA_NORMALIZE).  With HLA_UNMASKED the output is o = q^T S_t C_t (divided by
+ * q^T S_t m_t + eps), and G, h are neither read nor written (they may be NULL).
+ *   q: [N][d], o: [N][dv]; k: [N/H*Hkv][d], v: [N/H*Hkv][dv] (row s*Hkv + h/(H/Hkv)
+ *   for pair u); element type `dtype` (HLA_F32 or HLA_BF16);
+ *   Hkv: key/value heads per sequence, H % Hkv == 0 (0 means H);
  *   state: N pairs, read and written in place;
  *   d, dv in {16,32,64,128}; N % H == 0.
  */
-HLA_API hla_status hla_decode_step(int N, int H, int d, int dv, hla_dtype dtype, unsigned flags,
+HLA_API hla_status hla_decode_step(int N, int H, int Hkv, int d, int dv, hla_dtype dtype, unsigned flags,
                            float eps, const float *gamma, const hla_state *state,
                            const void *q, const void *k, const void *v, void *o,
                            void *stream);

@@ -36,12 +36,12 @@ def state_to_np(st: "hla.State", units, d, dv):
     return oracle.State(*(x.double().cpu().numpy().reshape(s) for x, s in zip(st.astuple(), shapes)))
 
 
-def run_forward(x, dtype, chunk, normalize=False, eps=0.0, state_in=None, return_state=True):
+def run_forward(x, dtype, chunk, normalize=False, eps=0.0, state_in=None, return_state=True, unmasked=False):
     q, k, v = to_dev(x["q"], dtype), to_dev(x["k"], dtype), to_dev(x["v"], dtype)
     g = None if x.get("gamma") is None else torch.from_numpy(np.asarray(x["gamma"], np.float32)).cuda()
     sin = state_to_dev(state_in) if state_in is not None else None
     res = hla.forward(q, k, v, chunk=chunk, gamma=g, normalize=normalize, eps=eps, state_in=sin,
-                      return_state=return_state)
+                      return_state=return_state, unmasked=unmasked)
     hla.hla_sync_status()
     if return_state:
         o, st = res
@@ -50,9 +50,10 @@ def run_forward(x, dtype, chunk, normalize=False, eps=0.0, state_in=None, return
     return res.float().cpu().numpy(), None
 
 
-def run_oracle(x, normalize=False, eps=0.0, state_in=None):
+def run_oracle(x, normalize=False, eps=0.0, state_in=None, unmasked=False):
     g = None if x.get("gamma") is None else np.asarray(x["gamma"], np.float64)
-    return oracle.forward(x["q"], x["k"], x["v"], gamma=g, normalize=normalize, eps=eps, state_in=state_in)
+    return oracle.forward(x["q"], x["k"], x["v"], gamma=g, normalize=normalize, eps=eps, state_in=state_in,
+                          unmasked=unmasked)
 
 
 def assert_parity(o, o_ref, st=None, st_ref=None, tol=TOL_BF16, what=""):

@@ -46,7 +46,7 @@ def test_status_strings(lib):
 
 
 def _params(**kw):
-    base = dict(B=1, H=2, n=128, d=64, dv=64, chunk=64, in_dtype=hla.HLA_BF16, flags=0, eps=0.0, gamma=None)
+    base = dict(B=1, H=2, n=128, d=64, dv=64, chunk=64, in_dtype=hla.HLA_BF16, flags=0, eps=0.0, gamma=None, Hkv=0)
     base.update(kw)
     return hla.hla_params(**base)
 
@@ -62,6 +62,8 @@ def _call(p, q=16, k=16, v=16, o=16, sin=None, sout=None, ws=None, ws_bytes=0):
     (dict(n=-1), hla.HLA_ERR_ARG),
     (dict(in_dtype=7), hla.HLA_ERR_ARG),
     (dict(flags=8), hla.HLA_ERR_ARG),
+    (dict(H=6, Hkv=4), hla.HLA_ERR_ARG),                    # key/value heads must divide H
+    (dict(Hkv=-1), hla.HLA_ERR_ARG),
     (dict(flags=hla.HLA_DECAY), hla.HLA_ERR_ARG),          # decay without gamma
     (dict(flags=hla.HLA_NORMALIZE, eps=-1.0), hla.HLA_ERR_ARG),
     (dict(d=48), hla.HLA_ERR_UNSUPPORTED),
@@ -91,12 +93,19 @@ def test_combine_and_decode_reject_bad_args(lib):
     assert L.hla_state_combine(-1, 64, 64, sp, sp, sp, None, None) == hla.HLA_ERR_ARG
     assert L.hla_state_combine(1, 48, 64, sp, sp, sp, None, None) == hla.HLA_ERR_UNSUPPORTED
     assert L.hla_state_combine(1, 64, 64, None, sp, sp, None, None) == hla.HLA_ERR_ARG
-    assert L.hla_decode_step(5, 2, 64, 64, hla.HLA_BF16, 0, 0.0, None, sp, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
-    assert L.hla_decode_step(4, 2, 64, 64, hla.HLA_BF16, hla.HLA_DECAY, 0.0, None, sp, 16, 16, 16, 16,
+    assert L.hla_decode_step(5, 2, 0, 64, 64, hla.HLA_BF16, 0, 0.0, None, sp, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
+    assert L.hla_decode_step(4, 2, 0, 64, 64, hla.HLA_BF16, hla.HLA_DECAY, 0.0, None, sp, 16, 16, 16, 16,
                              None) == hla.HLA_ERR_ARG
-    assert L.hla_decode_step(4, 2, 64, 64, 9, 0, 0.0, None, sp, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
-    assert L.hla_decode_step(4, 2, 64, 64, hla.HLA_BF16, 0, 0.0, None, None, 16, 16, 16, 16,
+    assert L.hla_decode_step(4, 2, 0, 64, 64, 9, 0, 0.0, None, sp, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
+    assert L.hla_decode_step(4, 2, 0, 64, 64, hla.HLA_BF16, 0, 0.0, None, None, 16, 16, 16, 16,
                              None) == hla.HLA_ERR_ARG
+    # key/value heads must divide the query heads; flag bits above HLA_UNMASKED are unknown
+    assert L.hla_decode_step(6, 3, 2, 64, 64, hla.HLA_BF16, 0, 0.0, None, sp, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
+    assert L.hla_decode_step(4, 2, 0, 64, 64, hla.HLA_BF16, 8, 0.0, None, sp, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
+    # the unmasked state needs S, C, m only
+    um = hla.hla_state(16, 16, None, None, None)
+    assert L.hla_decode_step(4, 2, 0, 64, 64, hla.HLA_BF16, hla.HLA_UNMASKED, 0.0, None, ctypes.pointer(um),
+                             16, 16, 16, 16, None) == hla.HLA_ERR_ARG
 
 
 def test_workspace_size_zero_for_invalid(lib):

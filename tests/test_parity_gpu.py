@@ -142,6 +142,64 @@ def test_tc_deterministic():
         assert np.array_equal(p, q)
 
 
+# ------------------------------------------- unmasked variant, shared key/value heads
+@pytest.mark.parametrize("chunk,d,dv", TC_SHAPES)
+@pytest.mark.parametrize("decay,normalize", [(False, False), (False, True), (True, False), (True, True)])
+def test_tc_unmasked_variants(chunk, d, dv, decay, normalize):
+    n = 5 * chunk + 17
+    w = small("unm", d=d, dv=dv, chunk=chunk, n=n, decay=decay, qk="elu1" if normalize else "l2",
+              gamma_lo=0.9, gamma_hi=0.999, seed=23)
+    x = W.make_inputs(w)
+    o, st = run_forward(x, "bf16", chunk, normalize=normalize, eps=1e-6, unmasked=True)
+    o_ref, st_ref = run_oracle(x, normalize=normalize, eps=1e-6, unmasked=True)
+    assert_parity(o, o_ref, st, st_ref, what=f"unmasked c{chunk} d{d} dv{dv} decay={decay} norm={normalize}")
+
+
+@pytest.mark.parametrize("d,dv,chunk,n", [(16, 32, 16, 100), (64, 64, 64, 130), (32, 16, 32, 45)])
+@pytest.mark.parametrize("decay,normalize", [(False, False), (True, True)])
+def test_simt_unmasked(d, dv, chunk, n, decay, normalize):
+    for dtype in ("f32", "bf16"):
+        w = small("simt_unm", d=d, dv=dv, chunk=chunk, n=n, dtype=dtype, decay=decay,
+                  qk="elu1" if normalize else "l2")
+        x = W.make_inputs(w)
+        o, st = run_forward(x, dtype, chunk, normalize=normalize, eps=1e-6, unmasked=True)
+        o_ref, st_ref = run_oracle(x, normalize=normalize, eps=1e-6, unmasked=True)
+        assert_parity(o, o_ref, st, st_ref, tol=TOL_F32 if dtype == "f32" else TOL_BF16, what=f"simt unm {dtype}")
+
+
+@pytest.mark.parametrize("B,H,n,chunk,d,dv", [(1, 3, 8192, 64, 64, 128), (1, 400, 40, 64, 64, 64),
+                                              (1, 7, 4990, 128, 128, 128)])
+def test_tc_unmasked_runs_and_resume(B, H, n, chunk, d, dv):
+    w = small("unm_runs", B=B, H=H, n=n, chunk=chunk, d=d, dv=dv, decay=True, qk="elu1", seed=24)
+    x = W.make_inputs(w)
+    o, st = run_forward(x, "bf16", chunk, normalize=True, eps=1e-6, unmasked=True)
+    o_ref, st_ref = run_oracle(x, normalize=True, eps=1e-6, unmasked=True)
+    assert_parity(o, o_ref, st, st_ref, what=f"unmasked runs B{B}H{H}n{n}")
+    # resume from a state in the middle of the sequence
+    n1 = (n // 3) + 5
+    x1 = {kk: (vv[:, :, :n1] if kk != "gamma" else vv) for kk, vv in x.items()}
+    x2 = {kk: (vv[:, :, n1:] if kk != "gamma" else vv) for kk, vv in x.items()}
+    _, st1 = run_oracle(x1, normalize=True, eps=1e-6, unmasked=True)
+    o2, st2 = run_forward(x2, "bf16", chunk, normalize=True, eps=1e-6, state_in=st1, unmasked=True)
+    o2_ref, st2_ref = run_oracle(x2, normalize=True, eps=1e-6, state_in=st1, unmasked=True)
+    assert_parity(o2, o2_ref, st2, st2_ref, what="unmasked resume")
+
+
+@pytest.mark.parametrize("unmasked", [False, True])
+@pytest.mark.parametrize("chunk,d,dv,dtype", [(64, 64, 64, "bf16"), (128, 128, 128, "bf16"), (64, 64, 128, "bf16"),
+                                              (32, 32, 16, "f32")])
+def test_shared_kv_heads(unmasked, chunk, d, dv, dtype):
+    # 8 query heads reading 2 key/value heads; several pieces per sequence
+    w = small("kv2", B=2, H=8, Hkv=2, n=6 * chunk + 9, chunk=chunk, d=d, dv=dv, dtype=dtype, decay=True,
+              qk="elu1", seed=25)
+    x = W.make_inputs(w)
+    assert x["k"].shape[1] == 2 and x["v"].shape[1] == 2
+    o, st = run_forward(x, dtype, chunk, normalize=True, eps=1e-6, unmasked=unmasked)
+    o_ref, st_ref = run_oracle(x, normalize=True, eps=1e-6, unmasked=unmasked)
+    assert_parity(o, o_ref, st, st_ref, tol=TOL_F32 if dtype == "f32" else TOL_BF16,
+                  what=f"shared kv unmasked={unmasked} c{chunk} d{d} dv{dv}")
+
+
 # ------------------------------------------------------------------ combine
 @pytest.mark.parametrize("d,dv", [(64, 64), (128, 128), (16, 32), (64, 128)])
 def test_state_combine(d, dv):
@@ -194,11 +252,44 @@ def test_decode_steps(d, dv, decay, normalize):
     state_errors(state_to_np(dst, N, d, dv), ref, 1e-5, "decode state")
 
 
+@pytest.mark.parametrize("unmasked,Hkv", [(True, 4), (False, 2), (True, 1)])
+def test_decode_unmasked_and_shared_heads(unmasked, Hkv):
+    seqs, H, d, dv, steps = 6, 4, 128, 64, 3
+    N = seqs * H
+    rng = np.random.default_rng(19)
+    gamma = np.exp(rng.uniform(np.log(0.9), np.log(0.999), H))
+    pre = W.make_inputs(W.Workload("pre", seqs, H, 40, d, dv, 64, "bf16", "elu1", seed=33, Hkv=Hkv))
+    _, st = oracle.forward(pre["q"], pre["k"], pre["v"], gamma=gamma, unmasked=unmasked)
+    st32 = oracle.State(*(np.asarray(a, np.float32).astype(np.float64) for a in st.astuple()))
+    dst = state_to_dev(st32)
+    g = torch.from_numpy(gamma.astype(np.float32)).cuda()
+    g64 = gamma.astype(np.float32).astype(np.float64)
+    ref = st32.copy()
+    for s in range(steps):
+        toks = W.make_decode_tokens(seqs, H, d, dv, 1, seed=40 + s)
+        qn = np.abs(toks["q"][0])
+        kn = np.abs(toks["k"][0]).reshape(seqs, H, d)[:, :Hkv].reshape(seqs * Hkv, d)
+        vn = toks["v"][0].reshape(seqs, H, dv)[:, :Hkv].reshape(seqs * Hkv, dv)
+        kn, vn = np.ascontiguousarray(kn), np.ascontiguousarray(vn)
+        q, k, v = to_dev(qn, "bf16"), to_dev(kn, "bf16"), to_dev(vn, "bf16")
+        o = hla.decode_step(dst, q, k, v, H, gamma=g, normalize=True, eps=1e-6, unmasked=unmasked)
+        o_ref = oracle.decode_step(ref, qn, kn, vn, H, gamma=g64, normalize=True, eps=1e-6, unmasked=unmasked)
+        hla.hla_sync_status()
+        og = o.float().cpu().numpy()
+        assert max(rel_l2(og[u], o_ref[u]) for u in range(N)) <= TOL_BF16, f"step {s}"
+    got = state_to_np(dst, N, d, dv)
+    if unmasked:  # G, h are neither read nor written by the unmasked step
+        got.G[...] = ref.G
+        got.h[...] = ref.h
+    state_errors(got, ref, 1e-5, "decode state")
+
+
 # ---------------------------------------------------- full-size workloads
-@pytest.mark.parametrize("w", [W.FWD_BF16, W.FWD_NORM, W.FWD_DECAY], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [W.FWD_BF16, W.FWD_NORM, W.FWD_DECAY, W.FWD_UNMASKED, W.FWD_SHARED_KV],
+                         ids=lambda w: w.name)
 def test_full_workload(w):
     x = W.make_inputs(w)
-    o, st = run_forward(x, w.dtype, w.chunk, normalize=w.normalize, eps=w.eps)
-    o_ref, st_ref = run_oracle(x, normalize=w.normalize, eps=w.eps)
+    o, st = run_forward(x, w.dtype, w.chunk, normalize=w.normalize, eps=w.eps, unmasked=w.unmasked)
+    o_ref, st_ref = run_oracle(x, normalize=w.normalize, eps=w.eps, unmasked=w.unmasked)
     err = assert_parity(o, o_ref, st, st_ref, what=w.name)
     print(f"{w.name}: max per-(b,h) rel L2 {err:.3e}")
