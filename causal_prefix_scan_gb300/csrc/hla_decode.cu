@@ -59,8 +59,10 @@ __device__ __forceinline__ float block_sum(float x, float *red) {
     return s;
 }
 
-template <typename T, int D, int DV>
-__global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
+// Three CTAs per SM keep enough loads in flight; the register cap (85) is above what
+// the bf16 and fp32 instantiations need.
+template <typename T, int D, int DV, bool UNM>
+__global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeArgs a) {
     constexpr int CG = D / 4;           // float4 column groups of S
     constexpr int CGV = DV / 4;         // float4 column groups of C, G
     constexpr int NS = D * D / 4;       // float4 elements of S
@@ -77,7 +79,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     const size_t u = blockIdx.x;
     const bool decay = (a.flags & HLA_DECAY) != 0;
     const bool norm = (a.flags & HLA_NORMALIZE) != 0;
-    const bool unm = (a.flags & HLA_UNMASKED) != 0;
+    constexpr bool unm = UNM;
     const float g = decay ? a.gamma[u % a.H] : 1.f;
     const float g2 = g * g;
     const size_t kvu = (u / a.H) * a.Hkv + (u % a.H) / (a.H / a.Hkv);  // key/value row
@@ -182,12 +184,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
 #pragma unroll
     for (int i = 0; i < ITC; ++i) {
         const int e = tid + i * kThreads;
-        if (e < NC && !unm) cv[i] = G[e];
+        if constexpr (!UNM) {
+            if (e < NC) cv[i] = G[e];
+        }
     }
 #pragma unroll
     for (int i = 0; i < ITC; ++i) {
         const int e = tid + i * kThreads;
-        if (e < NC && !unm) {
+        if (!UNM && e < NC) {
             const int row = e / CGV, cg = e % CGV;
             const float qr = qs[row], gk = g * ks[row];
             float4 x = cv[i];
@@ -249,7 +253,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
 
 template <typename T, int D, int DV>
 cudaError_t launch_t(const DecodeArgs &a, cudaStream_t st) {
-    decode_kernel<T, D, DV><<<a.N, kThreads, 0, st>>>(a);
+    if (a.flags & HLA_UNMASKED) decode_kernel<T, D, DV, true><<<a.N, kThreads, 0, st>>>(a);
+    else decode_kernel<T, D, DV, false><<<a.N, kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 template <typename T, int D>
