@@ -20,7 +20,12 @@ reading in hla_oracle.c).  The unmasked variant (o_t = q_t^T S_t C_t, skill card
 "Higher-order linear attention", bullet "Streaming Computation") is pinned by an
 all-pairs brute force, the dense form [L o ((L o QK^T)(QK^T)^T)]V, its relation to the
 masked output through G, chunk invariance, resume and decode continuation; shared
-key/value heads (bullet "Multi-Head Support") by equality with repeated heads.
+key/value heads (bullet "Multi-Head Support") by equality with repeated heads.  The
+asymmetric variant AHLA (section 2, o_t = sum_{a<=b<=t} (q_t.k_b)(q_b.k_a) v_a) is pinned
+by its brute-force triple sum, the dense form (L o A)(L o A)V, brute-force definitions of
+its five summaries, a closed form for constant inputs, chunk invariance, associativity
+of its concatenation rule, concatenation equal to the joined sequence, resume and
+decode continuation.
 """
 from __future__ import annotations
 
@@ -60,7 +65,7 @@ def _load():
         _lib.hla_oracle_forward.argtypes = [i] * 7 + [dp, dp, dp, dp, i, d] + [dp] * 5 + [dp] + [dp] * 5 + [i]
         _lib.hla_oracle_forward_chunked.argtypes = [i] * 8 + [dp, dp, dp, dp, i, d] + [dp] * 5 + [dp] + [dp] * 5 + [i]
         _lib.hla_oracle_decode_step.argtypes = [i] * 6 + [dp, i, d] + [dp] * 5 + [dp, dp, dp, dp, i]
-        _lib.hla_oracle_combine.argtypes = [i, i, i] + [dp] * 10 + [dp] + [dp] * 5
+        _lib.hla_oracle_combine.argtypes = [i, i, i, i] + [dp] * 10 + [dp] + [dp] * 5
         for f in (_lib.hla_oracle_forward, _lib.hla_oracle_forward_chunked,
                   _lib.hla_oracle_decode_step, _lib.hla_oracle_combine):
             f.restype = ctypes.c_int
@@ -120,9 +125,18 @@ def default_threads() -> int:
         return os.cpu_count() or 1
 
 
+VARIANTS = {"masked": 0, "unmasked": 1, "asymmetric": 2}
+
+
+def _variant(unmasked=False, asymmetric=False) -> int:
+    assert not (unmasked and asymmetric)
+    return 1 if unmasked else (2 if asymmetric else 0)
+
+
 def forward(q, k, v, gamma=None, normalize=False, eps=0.0, state_in=None,
-            want_state=True, chunk=None, nthreads=None, unmasked=False):
-    """2nd-order HLA forward in fp64, masked (default) or unmasked.
+            want_state=True, chunk=None, nthreads=None, unmasked=False, asymmetric=False):
+    """2nd-order HLA forward in fp64: masked (default), unmasked, or the asymmetric
+    variant AHLA (its state R, P, m^K, E, n in the S, C, m, G, h arrays).
 
     q: [B,H,n,d]; k: [B,Hkv,n,d]; v: [B,Hkv,n,dv] with H a multiple of Hkv (query
     head h reads key/value head h // (H // Hkv)); gamma: [H] or None.  chunk=None
@@ -145,7 +159,7 @@ def forward(q, k, v, gamma=None, normalize=False, eps=0.0, state_in=None,
     nt = nthreads or default_threads()
     args_tail = [_p(q), _p(k), _p(v), _p(g), int(bool(normalize)), float(eps)] + _state_ptrs(sin) + \
         [_p(o)] + _state_ptrs(sout) + [nt]
-    um = int(bool(unmasked))
+    um = _variant(unmasked, asymmetric)
     if chunk is None:
         rc = lib.hla_oracle_forward(B, H, Hkv, n, d, dv, um, *args_tail)
     else:
@@ -156,7 +170,7 @@ def forward(q, k, v, gamma=None, normalize=False, eps=0.0, state_in=None,
 
 
 def decode_step(state: State, q, k, v, H, gamma=None, normalize=False, eps=0.0, nthreads=None,
-                unmasked=False):
+                unmasked=False, asymmetric=False):
     """One decode step for N (sequence, head) pairs, in place on ``state``.
     q: [N,d]; k: [N/H*Hkv,d]; v: [N/H*Hkv,dv]; pair u uses gamma[u % H] and key/value
     row (u // H) * Hkv + (u % H) // (H // Hkv).  Returns o [N,dv]."""
@@ -168,7 +182,7 @@ def decode_step(state: State, q, k, v, H, gamma=None, normalize=False, eps=0.0, 
     for x in state.astuple():
         assert x.dtype == np.float64 and x.flags.c_contiguous
     o = np.zeros((N, dv))
-    rc = _load().hla_oracle_decode_step(N, H, Hkv, d, dv, int(bool(unmasked)), _p(g), int(bool(normalize)),
+    rc = _load().hla_oracle_decode_step(N, H, Hkv, d, dv, _variant(unmasked, asymmetric), _p(g), int(bool(normalize)),
                                         float(eps),
                                         *_state_ptrs(state), _p(q), _p(k), _p(v), _p(o),
                                         nthreads or default_threads())
@@ -177,14 +191,15 @@ def decode_step(state: State, q, k, v, H, gamma=None, normalize=False, eps=0.0, 
     return o
 
 
-def combine(A: State, Bst: State, decay_pow=None) -> State:
-    """Segment concatenation out = A (+) B for every item (A earlier than B)."""
+def combine(A: State, Bst: State, decay_pow=None, asymmetric=False) -> State:
+    """Segment concatenation out = A (+) B for every item (A earlier than B), by the
+    masked rule or the asymmetric variant's rule."""
     A = State(*(_f64(x) for x in A.astuple()))
     Bst = State(*(_f64(x) for x in Bst.astuple()))
     count, d, dv = A.C.shape
     out = State.zeros(count, d, dv)
     f = _f64(decay_pow)
-    rc = _load().hla_oracle_combine(count, d, dv, *_state_ptrs(A), *_state_ptrs(Bst), _p(f),
+    rc = _load().hla_oracle_combine(count, d, dv, 2 if asymmetric else 0, *_state_ptrs(A), *_state_ptrs(Bst), _p(f),
                                     *_state_ptrs(out))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")

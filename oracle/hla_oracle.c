@@ -45,6 +45,21 @@
  * part of this variant and are left at zero.  Its concatenation is the linear
  * part of the rule above (S, C, m).
  *
+ * Asymmetric variant AHLA (gist.science summary, section 2 "Asymmetrische
+ * Hogere-orde Lineaire Aandacht"): the operator Q (K^T Q)(K^T V) = A A V with
+ * A = Q K^T, masked to o_t = sum_{a<=b<=t} (q_t.k_b)(q_b.k_a) v_a: the value index a
+ * is routed through the intermediate key index b.  Its streaming summaries (the
+ * section names P^KV, m^K, E, n):
+ *   P_t = g P_{t-1} + k_t v_t^T,   m_t = g m_{t-1} + k_t,
+ *   E_t = g E_{t-1} + k_t (q_t^T P_t),   n_t = g n_{t-1} + k_t (q_t . m_t),
+ *   o_t = q_t^T E_t,   ratio form o_t = q_t^T E_t / (q_t^T n_t + eps),
+ * so the pair weight is g^{(t-b)+(b-a)} = g^{t-a}.  Composing segment A before B
+ * (f = g^{len B}) needs one more summary, R = sum_b k_b q_b^T without decay:
+ *   P = f P_A + P_B,  m = f m_A + m_B,  R = R_A + R_B,
+ *   E = f E_A + E_B + f R_B P_A,   n = f n_A + n_B + f R_B m_A.
+ * In the five state arrays the variant keeps R in S, P in C, m^K in m, E in G
+ * and n in h.
+ *
  * Multi-query heads (skill card, section "Architecture Overview", bullet
  * "Multi-Head Support"): k and v may have Hkv heads with H a multiple of Hkv;
  * query head h reads key/value head h / (H / Hkv).  The summaries stay per query
@@ -70,7 +85,7 @@ typedef struct {
 /* one (b,h) stream: the five summaries of one head, plus its decay factor */
 typedef struct {
     int d, dv;
-    int unmasked; /* 1: o = q^T S C, G and h not carried */
+    int variant; /* 0 masked, 1 unmasked (o = q^T S C; G, h not carried), 2 asymmetric */
     double g;
     double *S, *C, *m, *G, *h; /* views into caller state for this (b,h) */
     double *kc;                /* scratch: k^T C_{t-1}, length dv        */
@@ -87,7 +102,39 @@ static void step_token(stream_t *st, const double *q, const double *k,
     const double g = st->g, g2 = g * g;
     double *S = st->S, *C = st->C, *m = st->m, *G = st->G, *h = st->h;
 
-    if (!st->unmasked) {
+    if (st->variant == 2) { /* asymmetric: R in S, P in C, m^K in m, E in G, n in h */
+        for (int i = 0; i < d; ++i) /* R_t = R_{t-1} + k q^T */
+            for (int j = 0; j < d; ++j) S[i * d + j] += k[i] * q[j];
+        for (int i = 0; i < d; ++i) { /* P_t = g P_{t-1} + k v^T, m_t = g m_{t-1} + k */
+            for (int j = 0; j < dv; ++j) C[i * dv + j] = g * C[i * dv + j] + k[i] * v[j];
+            m[i] = g * m[i] + k[i];
+        }
+        double zeta = 0.0; /* z = q^T P_t, zeta = q . m_t */
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i) acc += q[i] * C[i * dv + j];
+            st->kc[j] = acc;
+        }
+        for (int i = 0; i < d; ++i) zeta += q[i] * m[i];
+        for (int i = 0; i < d; ++i) { /* E_t = g E_{t-1} + k z^T, n_t = g n_{t-1} + k zeta */
+            for (int j = 0; j < dv; ++j) G[i * dv + j] = g * G[i * dv + j] + k[i] * st->kc[j];
+            h[i] = g * h[i] + k[i] * zeta;
+        }
+        if (!o) return;
+        double den = 0.0; /* o = q^T E_t [/ (q^T n_t + eps)] */
+        if (normalize) {
+            for (int i = 0; i < d; ++i) den += q[i] * h[i];
+            den += eps;
+        }
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i) acc += q[i] * G[i * dv + j];
+            o[j] = normalize ? acc / den : acc;
+        }
+        return;
+    }
+
+    if (st->variant == 0) {
         /* k^T C_{t-1} and k^T m_{t-1} */
         for (int j = 0; j < dv; ++j) {
             double acc = 0.0;
@@ -140,7 +187,7 @@ static void step_token(stream_t *st, const double *q, const double *k,
 
 /* R7: out = A (+) B, A earlier in time than B, f = g^{len(B)}.
  * out may alias A or B: every output is formed in a private buffer first. */
-static void combine_one(int d, int dv, double f,
+static void combine_one(int d, int dv, double f, int variant,
                         const double *SA, const double *CA, const double *mA,
                         const double *GA, const double *hA,
                         const double *SB, const double *CB, const double *mB,
@@ -150,6 +197,28 @@ static void combine_one(int d, int dv, double f,
     const double f2 = f * f;
     double *tG = (double *)malloc(sizeof(double) * (size_t)d * dv);
     double *th = (double *)malloc(sizeof(double) * (size_t)d);
+    if (variant == 2) {
+        /* asymmetric: E = f E_A + E_B + f R_B P_A, n = f n_A + n_B + f R_B m_A,
+         * P = f P_A + P_B, m = f m_A + m_B, R = R_A + R_B (R in S, P in C, E in G, n in h) */
+        for (int i = 0; i < d; ++i) {
+            for (int j = 0; j < dv; ++j) {
+                double cross = 0.0; /* (R_B P_A)[i][j] */
+                for (int l = 0; l < d; ++l) cross += SB[i * d + l] * CA[l * dv + j];
+                tG[i * dv + j] = f * GA[i * dv + j] + GB[i * dv + j] + f * cross;
+            }
+            double crossm = 0.0; /* (R_B m_A)[i] */
+            for (int l = 0; l < d; ++l) crossm += SB[i * d + l] * mA[l];
+            th[i] = f * hA[i] + hB[i] + f * crossm;
+        }
+        for (int i = 0; i < d * d; ++i) S[i] = SA[i] + SB[i];
+        for (int i = 0; i < d * dv; ++i) C[i] = f * CA[i] + CB[i];
+        for (int i = 0; i < d; ++i) m[i] = f * mA[i] + mB[i];
+        memcpy(G, tG, sizeof(double) * (size_t)d * dv);
+        memcpy(h, th, sizeof(double) * (size_t)d);
+        free(tG);
+        free(th);
+        return;
+    }
     for (int i = 0; i < d; ++i) {
         for (int j = 0; j < dv; ++j) {
             double cross = 0.0; /* (S_B C_A)[i][j] */
@@ -175,7 +244,7 @@ static void combine_one(int d, int dv, double f,
 typedef struct {
     int B, H, n, d, dv, chunk;
     int Hkv;      /* key/value heads; query head h reads head h / (H / Hkv) */
-    int unmasked; /* variant: 0 masked, 1 unmasked */
+    int variant;  /* 0 masked, 1 unmasked, 2 asymmetric */
     const double *q, *k, *v, *gamma;
     int normalize;
     double eps;
@@ -201,7 +270,7 @@ static void load_state(stream_t *st, const ostate *in, size_t u)
         memcpy(st->S, in->S + u * d * d, sizeof(double) * d * d);
         memcpy(st->C, in->C + u * d * dv, sizeof(double) * d * dv);
         memcpy(st->m, in->m + u * d, sizeof(double) * d);
-        if (st->unmasked) { /* not part of the unmasked state */
+        if (st->variant == 1) { /* not part of the unmasked state */
             memset(st->G, 0, sizeof(double) * d * dv);
             memset(st->h, 0, sizeof(double) * d);
         } else {
@@ -233,7 +302,7 @@ static stream_t stream_new(int d, int dv)
     stream_t st;
     st.d = d;
     st.dv = dv;
-    st.unmasked = 0;
+    st.variant = 0;
     st.g = 1.0;
     st.S = (double *)calloc((size_t)d * d, sizeof(double));
     st.C = (double *)calloc((size_t)d * dv, sizeof(double));
@@ -284,7 +353,7 @@ static void run_chunked(job_t *J, stream_t *st, int u)
     const size_t ko = kv_unit(J, u) * n * d, vo = kv_unit(J, u) * n * dv;
     stream_t loc = stream_new(d, dv);
     loc.g = st->g;
-    loc.unmasked = st->unmasked;
+    loc.variant = st->variant;
     /* prefix state lives in st */
     load_state(st, &J->in, u);
     for (int t0 = 0; t0 < n; t0 += c) {
@@ -297,7 +366,7 @@ static void run_chunked(job_t *J, stream_t *st, int u)
         /* outputs of this chunk: continue from the prefix in a copy */
         stream_t run = stream_new(d, dv);
         run.g = st->g;
-        run.unmasked = st->unmasked;
+        run.variant = st->variant;
         memcpy(run.S, st->S, sizeof(double) * d * d);
         memcpy(run.C, st->C, sizeof(double) * d * dv);
         memcpy(run.m, st->m, sizeof(double) * d);
@@ -309,11 +378,11 @@ static void run_chunked(job_t *J, stream_t *st, int u)
                        J->o ? J->o + oo + (size_t)t * dv : NULL);
         stream_free(&run);
         /* prefix <- prefix (+) local; the unmasked variant keeps G, h at zero */
-        combine_one(d, dv, pow(st->g, (double)len),
+        combine_one(d, dv, pow(st->g, (double)len), st->variant,
                     st->S, st->C, st->m, st->G, st->h,
                     loc.S, loc.C, loc.m, loc.G, loc.h,
                     st->S, st->C, st->m, st->G, st->h);
-        if (st->unmasked) {
+        if (st->variant == 1) {
             memset(st->G, 0, sizeof(double) * d * dv);
             memset(st->h, 0, sizeof(double) * d);
         }
@@ -341,7 +410,7 @@ static void *worker(void *arg)
         int u = take_unit(J, total);
         if (u < 0) break;
         st.g = J->gamma ? J->gamma[u % J->H] : 1.0;
-        st.unmasked = J->unmasked;
+        st.variant = J->variant;
         if (J->mode == 0) run_serial(J, &st, u);
         else if (J->mode == 1) run_chunked(J, &st, u);
         else run_decode(J, &st, u);
@@ -373,9 +442,9 @@ static int check_dims(int B, int H, int n, int d, int dv)
     return (B < 0 || H < 1 || n < 0 || d < 1 || dv < 1) ? -1 : 0;
 }
 
-static int check_heads(int H, int Hkv, int unmasked)
+static int check_heads(int H, int Hkv, int variant)
 {
-    return (Hkv < 1 || H % Hkv || (unmasked != 0 && unmasked != 1)) ? -1 : 0;
+    return (Hkv < 1 || H % Hkv || variant < 0 || variant > 2) ? -1 : 0;
 }
 
 /* ------------------------------------------------------------------------- */
@@ -383,8 +452,9 @@ static int check_heads(int H, int Hkv, int unmasked)
 
 /* Serial recurrence over n tokens for every (b,h).  gamma: [H] or NULL (no
  * decay).  state_in / state_out: pointers may be NULL (zeros / skip).  Hkv:
- * key/value heads (H for ordinary multi-head); unmasked: 0 or 1 (variant). */
-int hla_oracle_forward(int B, int H, int Hkv, int n, int d, int dv, int unmasked,
+ * key/value heads (H for ordinary multi-head); variant: 0 masked, 1 unmasked,
+ * 2 asymmetric. */
+int hla_oracle_forward(int B, int H, int Hkv, int n, int d, int dv, int variant,
                        const double *q, const double *k, const double *v,
                        const double *gamma, int normalize, double eps,
                        double *Si, double *Ci, double *mi, double *Gi, double *hi,
@@ -392,11 +462,11 @@ int hla_oracle_forward(int B, int H, int Hkv, int n, int d, int dv, int unmasked
                        double *So, double *Co, double *mo, double *Go, double *ho,
                        int nthreads)
 {
-    if (check_dims(B, H, n, d, dv) || check_heads(H, Hkv, unmasked)) return -1;
+    if (check_dims(B, H, n, d, dv) || check_heads(H, Hkv, variant)) return -1;
     job_t J;
     memset(&J, 0, sizeof J);
     J.B = B; J.H = H; J.n = n; J.d = d; J.dv = dv; J.chunk = 0;
-    J.Hkv = Hkv; J.unmasked = unmasked;
+    J.Hkv = Hkv; J.variant = variant;
     J.q = q; J.k = k; J.v = v; J.gamma = gamma;
     J.normalize = normalize; J.eps = eps;
     J.in = (ostate){Si, Ci, mi, Gi, hi};
@@ -407,7 +477,7 @@ int hla_oracle_forward(int B, int H, int Hkv, int n, int d, int dv, int unmasked
 }
 
 /* Chunked-scan forward (chunk >= 1): see run_chunked. */
-int hla_oracle_forward_chunked(int B, int H, int Hkv, int n, int d, int dv, int unmasked, int chunk,
+int hla_oracle_forward_chunked(int B, int H, int Hkv, int n, int d, int dv, int variant, int chunk,
                                const double *q, const double *k, const double *v,
                                const double *gamma, int normalize, double eps,
                                double *Si, double *Ci, double *mi, double *Gi, double *hi,
@@ -415,11 +485,11 @@ int hla_oracle_forward_chunked(int B, int H, int Hkv, int n, int d, int dv, int 
                                double *So, double *Co, double *mo, double *Go, double *ho,
                                int nthreads)
 {
-    if (check_dims(B, H, n, d, dv) || check_heads(H, Hkv, unmasked) || chunk < 1) return -1;
+    if (check_dims(B, H, n, d, dv) || check_heads(H, Hkv, variant) || chunk < 1) return -1;
     job_t J;
     memset(&J, 0, sizeof J);
     J.B = B; J.H = H; J.n = n; J.d = d; J.dv = dv; J.chunk = chunk;
-    J.Hkv = Hkv; J.unmasked = unmasked;
+    J.Hkv = Hkv; J.variant = variant;
     J.q = q; J.k = k; J.v = v; J.gamma = gamma;
     J.normalize = normalize; J.eps = eps;
     J.in = (ostate){Si, Ci, mi, Gi, hi};
@@ -432,18 +502,18 @@ int hla_oracle_forward_chunked(int B, int H, int Hkv, int n, int d, int dv, int 
 /* One decode step for N independent (sequence, head) pairs, pair u using
  * gamma[u % H].  The state arrays are read and written in place.
  * q: [N][d], o: [N][dv]; k: [N/H*Hkv][d], v: [N/H*Hkv][dv]. */
-int hla_oracle_decode_step(int N, int H, int Hkv, int d, int dv, int unmasked,
+int hla_oracle_decode_step(int N, int H, int Hkv, int d, int dv, int variant,
                            const double *gamma, int normalize, double eps,
                            double *S, double *C, double *m, double *G, double *h,
                            const double *q, const double *k, const double *v,
                            double *o, int nthreads)
 {
-    if (check_dims(1, H, 1, d, dv) || check_heads(H, Hkv, unmasked) || N < 0) return -1;
+    if (check_dims(1, H, 1, d, dv) || check_heads(H, Hkv, variant) || N < 0) return -1;
     if (N % H) return -1;
     job_t J;
     memset(&J, 0, sizeof J);
     J.B = N / H; J.H = H; J.n = 1; J.d = d; J.dv = dv;
-    J.Hkv = Hkv; J.unmasked = unmasked;
+    J.Hkv = Hkv; J.variant = variant;
     J.q = q; J.k = k; J.v = v; J.gamma = gamma;
     J.normalize = normalize; J.eps = eps;
     J.in = (ostate){S, C, m, G, h};
@@ -454,8 +524,10 @@ int hla_oracle_decode_step(int N, int H, int Hkv, int d, int dv, int unmasked,
 }
 
 /* Segment concatenation for `count` independent items: out_i = A_i (+) B_i
- * with f_i = decay_pow[i] (NULL: f = 1).  out may alias A or B. */
-int hla_oracle_combine(int count, int d, int dv,
+ * with f_i = decay_pow[i] (NULL: f = 1), by the rule of `variant` (0 masked,
+ * 2 asymmetric; the unmasked state uses the masked rule's S, C, m).  out may
+ * alias A or B. */
+int hla_oracle_combine(int count, int d, int dv, int variant,
                        const double *SA, const double *CA, const double *mA,
                        const double *GA, const double *hA,
                        const double *SB, const double *CB, const double *mB,
@@ -463,10 +535,10 @@ int hla_oracle_combine(int count, int d, int dv,
                        const double *decay_pow,
                        double *S, double *C, double *m, double *G, double *h)
 {
-    if (count < 0 || d < 1 || dv < 1) return -1;
+    if (count < 0 || d < 1 || dv < 1 || variant < 0 || variant > 2) return -1;
     for (int i = 0; i < count; ++i) {
         const size_t a = (size_t)i * d * d, b = (size_t)i * d * dv, c = (size_t)i * d;
-        combine_one(d, dv, decay_pow ? decay_pow[i] : 1.0,
+        combine_one(d, dv, decay_pow ? decay_pow[i] : 1.0, variant,
                     SA + a, CA + b, mA + c, GA + b, hA + c,
                     SB + a, CB + b, mB + c, GB + b, hB + c,
                     S + a, C + b, m + c, G + b, h + c);

@@ -66,8 +66,11 @@ def test_pin_rejects_planted_mistake(tmp_path, name):
 # its own pin (all-pairs brute force; repeated-head equivalence)
 MUTATIONS_VARIANTS = {
     # the unmasked variant still subtracts the cross summary
-    "unmasked_keeps_cross": ("    if (!st->unmasked) {\n        /* k^T C_{t-1} and k^T m_{t-1} */",
-                             "    if (1) {\n        /* k^T C_{t-1} and k^T m_{t-1} */"),
+    "unmasked_keeps_cross": ("    if (st->variant == 0) {\n        /* k^T C_{t-1} and k^T m_{t-1} */",
+                             "    if (st->variant != 2) {\n        /* k^T C_{t-1} and k^T m_{t-1} */"),
+    # asymmetric variant: z from P before the current token (drops the pairs a = b)
+    "asym_stale_p": ("            for (int i = 0; i < d; ++i) acc += q[i] * C[i * dv + j];\n            st->kc[j] = acc;\n        }\n        for (int i = 0; i < d; ++i) zeta",
+                     "            for (int i = 0; i < d; ++i) acc += q[i] * (C[i * dv + j] - k[i] * v[j]);\n            st->kc[j] = acc;\n        }\n        for (int i = 0; i < d; ++i) zeta"),
     # query heads mapped to key/value heads round-robin instead of in groups
     "kv_round_robin": ("return (size_t)b * J->Hkv + hh / (J->H / J->Hkv);",
                        "return (size_t)b * J->Hkv + hh % J->Hkv;"),
@@ -92,7 +95,14 @@ def test_variant_pins_reject_planted_mistake(tmp_path, name):
     none = [None] * 5
     rng = np.random.default_rng(2)
     n, dd, dv = 8, 3, 2
-    if name == "unmasked_keeps_cross":
+    if name == "asym_stale_p":
+        from test_oracle_pins import brute_force_asym
+        q, k, v = rand_inputs(rng, 1, 1, n, dd, dv)
+        o = np.zeros((1, 1, n, dv))
+        assert L.hla_oracle_forward(1, 1, 1, n, dd, dv, 2, P(q), P(k), P(v), None, 0, 0.0, *none, P(o), *none,
+                                    1) == 0
+        assert rel(o[0, 0], brute_force_asym(q[0, 0], k[0, 0], v[0, 0])) > 1e-6, f"mutation {name} not caught"
+    elif name == "unmasked_keeps_cross":
         q, k, v = rand_inputs(rng, 1, 1, n, dd, dv)
         o = np.zeros((1, 1, n, dv))
         assert L.hla_oracle_forward(1, 1, 1, n, dd, dv, 1, P(q), P(k), P(v), None, 0, 0.0, *none, P(o), *none,

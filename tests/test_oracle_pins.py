@@ -427,3 +427,110 @@ def test_shared_kv_heads_equal_repeated_heads(unmasked, H, Hkv):
     assert np.array_equal(od, od_ref)
     for a, b in zip(st.astuple(), st_ref.astuple()):
         assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------- asymmetric variant (AHLA)
+# gist.science summary, section 2 "Asymmetrische Hogere-orde Lineaire Aandacht": the
+# operator Q (K^T Q)(K^T V) = A A V, A = Q K^T, routed through an intermediate key
+# index; masked: o_t = sum_{a<=b<=t} (q_t.k_b)(q_b.k_a) v_a; summaries P^KV, m^K, E, n.
+def brute_force_asym(q, k, v, g=1.0, normalize=False, eps=0.0):
+    n, dv = q.shape[0], v.shape[1]
+    o = np.zeros((n, dv))
+    for t in range(n):
+        num, den = np.zeros(dv), 0.0
+        for b in range(t + 1):
+            for a in range(b + 1):
+                w = (g ** (t - a)) * (q[t] @ k[b]) * (q[b] @ k[a])
+                num += w * v[a]
+                den += w
+        o[t] = num / (den + eps) if normalize else num
+    return o
+
+
+def brute_state_asym(q, k, v, g=1.0):
+    """R, P, m^K, E, n after the last token, each from its definition."""
+    n = q.shape[0]
+    T = n - 1
+    R = sum(np.outer(k[b], q[b]) for b in range(n))
+    P = sum(g ** (T - a) * np.outer(k[a], v[a]) for a in range(n))
+    m = sum(g ** (T - a) * k[a] for a in range(n))
+    E = sum(g ** (T - a) * (q[b] @ k[a]) * np.outer(k[b], v[a]) for b in range(n) for a in range(b + 1))
+    nn = sum(g ** (T - a) * (q[b] @ k[a]) * k[b] for b in range(n) for a in range(b + 1))
+    return R, P, m, E, nn
+
+
+@pytest.mark.parametrize("decay", [False, True])
+@pytest.mark.parametrize("normalize", [False, True])
+@pytest.mark.parametrize("n,d,dv", [(1, 1, 1), (8, 3, 2), (15, 4, 3)])
+def test_asym_brute_force_and_state(decay, normalize, n, d, dv):
+    rng = np.random.default_rng(500 + n + d)
+    B, H = 2, 2
+    q, k, v = rand_inputs(rng, B, H, n, d, dv, positive=normalize)
+    gamma = np.array([0.8, 0.55]) if decay else None
+    o, st = oracle.forward(q, k, v, gamma=gamma, normalize=normalize, eps=1e-3, asymmetric=True)
+    for b in range(B):
+        for h in range(H):
+            g = gamma[h] if decay else 1.0
+            assert rel(o[b, h], brute_force_asym(q[b, h], k[b, h], v[b, h], g, normalize, 1e-3)) < 1e-12
+            u = b * H + h
+            for got, ref in zip(st.astuple(), brute_state_asym(q[b, h], k[b, h], v[b, h], g)):
+                assert rel(got[u], ref) < 1e-12
+
+
+def test_asym_dense_form_and_constant_inputs():
+    rng = np.random.default_rng(51)
+    n, d, dv = 13, 3, 2
+    q, k, v = rand_inputs(rng, 1, 1, n, d, dv)
+    o, _ = oracle.forward(q, k, v, asymmetric=True)
+    L = np.tril(np.ones((n, n)))
+    A = q[0, 0] @ k[0, 0].T
+    assert rel(o[0, 0], (L * A) @ (L * A) @ v[0, 0]) < 1e-12
+    # constant q = k = x, v = y: (x.x)^2 times the number of pairs a <= b <= t
+    x, y = np.array([0.5, -1.0, 2.0]), np.array([1.5, -0.25])
+    qc = np.tile(x, (1, 1, n, 1)); vc = np.tile(y, (1, 1, n, 1))
+    oc, _ = oracle.forward(qc, qc, vc, asymmetric=True)
+    for t in range(n):
+        assert rel(oc[0, 0, t], (x @ x) ** 2 * (t + 1) * (t + 2) / 2 * y) < 1e-13
+
+
+@pytest.mark.parametrize("decay", [False, True])
+def test_asym_chunked_combine_resume_decode(decay):
+    rng = np.random.default_rng(52)
+    B, H, n, d, dv = 2, 2, 22, 3, 4
+    q, k, v = rand_inputs(rng, B, H, n, d, dv, positive=True)
+    gamma = np.array([0.9, 0.7]) if decay else None
+    kw = dict(gamma=gamma, normalize=True, eps=1e-3, asymmetric=True)
+    o, s = oracle.forward(q, k, v, **kw)
+    for c in (1, 3, 8, 22, 30):
+        oc, sc = oracle.forward(q, k, v, chunk=c, **kw)
+        assert rel(oc, o) < 1e-12
+        for a, b in zip(sc.astuple(), s.astuple()):
+            assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
+    # the concatenation of two halves' states equals the state of the whole sequence
+    n1 = 9
+    _, s1 = oracle.forward(q[:, :, :n1], k[:, :, :n1], v[:, :, :n1], **kw)
+    _, s2 = oracle.forward(q[:, :, n1:], k[:, :, n1:], v[:, :, n1:], **kw)
+    f = np.tile(gamma ** (n - n1), B) if decay else None
+    sj = oracle.combine(s1, s2, f, asymmetric=True)
+    for a, b in zip(sj.astuple(), s.astuple()):
+        assert np.allclose(a, b, rtol=1e-11, atol=1e-11)
+    # associativity with a third piece
+    n2 = 15
+    _, sa = oracle.forward(q[:, :, :n1], k[:, :, :n1], v[:, :, :n1], **kw)
+    _, sb = oracle.forward(q[:, :, n1:n2], k[:, :, n1:n2], v[:, :, n1:n2], **kw)
+    _, sc3 = oracle.forward(q[:, :, n2:], k[:, :, n2:], v[:, :, n2:], **kw)
+    fb = np.tile(gamma ** (n2 - n1), B) if decay else None
+    fc = np.tile(gamma ** (n - n2), B) if decay else None
+    fbc = np.tile(gamma ** (n - n1), B) if decay else None
+    left = oracle.combine(oracle.combine(sa, sb, fb, asymmetric=True), sc3, fc, asymmetric=True)
+    right = oracle.combine(sa, oracle.combine(sb, sc3, fc, asymmetric=True), fbc, asymmetric=True)
+    for a, b in zip(left.astuple(), right.astuple()):
+        assert np.allclose(a, b, rtol=1e-11, atol=1e-11)
+    # resume and decode continuation
+    o2, _ = oracle.forward(q[:, :, n1:], k[:, :, n1:], v[:, :, n1:], state_in=s1, **kw)
+    assert rel(o2, o[:, :, n1:]) < 1e-12
+    st = s1.copy()
+    for t in range(n1, n):
+        od = oracle.decode_step(st, q[:, :, t].reshape(B * H, d), k[:, :, t].reshape(B * H, d),
+                                v[:, :, t].reshape(B * H, dv), H, **kw)
+        assert rel(od.reshape(B, H, dv), o[:, :, t]) < 1e-12
