@@ -1,4 +1,5 @@
-"""GB300-native second-order Higher-order Linear Attention (HLA): masked and unmasked.
+"""GB300-native second-order Higher-order Linear Attention (HLA): masked, unmasked and
+the asymmetric variant AHLA.
 
 Thin ctypes binding over the C ABI in ``include/hla.h`` (library
 ``_lib/libhla_gb300.so``, built for sm_103a by ``_build.build()``).  Functions named
@@ -19,11 +20,11 @@ from ._build import LIB_PATH
 
 HLA_OK, HLA_ERR_ARG, HLA_ERR_UNSUPPORTED, HLA_ERR_CUDA, HLA_ERR_TIMEOUT = 0, 1, 2, 3, 4
 HLA_F32, HLA_BF16 = 0, 1
-HLA_NORMALIZE, HLA_DECAY, HLA_UNMASKED = 1, 2, 4
+HLA_NORMALIZE, HLA_DECAY, HLA_UNMASKED, HLA_ASYMMETRIC = 1, 2, 4, 8
 
 __all__ = [
     "HLA_OK", "HLA_ERR_ARG", "HLA_ERR_UNSUPPORTED", "HLA_ERR_CUDA", "HLA_ERR_TIMEOUT",
-    "HLA_F32", "HLA_BF16", "HLA_NORMALIZE", "HLA_DECAY", "HLA_UNMASKED",
+    "HLA_F32", "HLA_BF16", "HLA_NORMALIZE", "HLA_DECAY", "HLA_UNMASKED", "HLA_ASYMMETRIC",
     "HlaError", "hla_params", "hla_state", "library", "EXPORTS",
     "hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combine", "hla_decode_step",
     "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
@@ -72,7 +73,7 @@ def library(path: str | None = None):
     lib.hla_forward_chunked.argtypes = [P, vp, vp, vp, vp, S, S, vp, sz, vp]
     lib.hla_forward_chunked_noalloc.argtypes = [P, vp, vp, vp, vp, S, S, vp]
     lib.hla_forward_chunked_noalloc.restype = ctypes.c_int
-    lib.hla_state_combine.argtypes = [i, i, i, S, S, S, vp, vp]
+    lib.hla_state_combine.argtypes = [i, i, i, u, S, S, S, vp, vp]
     lib.hla_decode_step.argtypes = [i, i, i, i, i, i, u, f, vp, S, vp, vp, vp, vp, vp]
     lib.hla_sync_status.argtypes = [vp]
     for fn in (lib.hla_forward_chunked, lib.hla_state_combine, lib.hla_decode_step, lib.hla_sync_status):
@@ -145,8 +146,8 @@ def hla_forward_chunked_noalloc(params: hla_params, q, k, v, o, state_in=None, s
                                                  _stream(stream)))
 
 
-def hla_state_combine(count: int, d: int, dv: int, A, B, out, decay_pow=None, stream=None) -> None:
-    _check(library().hla_state_combine(count, d, dv, _state_struct(A), _state_struct(B), _state_struct(out),
+def hla_state_combine(count: int, d: int, dv: int, flags: int, A, B, out, decay_pow=None, stream=None) -> None:
+    _check(library().hla_state_combine(count, d, dv, flags, _state_struct(A), _state_struct(B), _state_struct(out),
                                        _ptr(decay_pow), _stream(stream)))
 
 
@@ -195,13 +196,17 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
+def _variant_flags(unmasked: bool, asymmetric: bool) -> int:
+    return (HLA_UNMASKED if unmasked else 0) | (HLA_ASYMMETRIC if asymmetric else 0)
+
+
 def make_params(q, v, chunk: int, gamma=None, normalize: bool = False, eps: float = 0.0,
-                unmasked: bool = False) -> hla_params:
+                unmasked: bool = False, asymmetric: bool = False) -> hla_params:
     """Parameters for q [B,H,n,d] and v [B,Hkv,n,dv] (Hkv = H, or a divisor of H when
     key/value heads are shared)."""
     B, H, n, d = q.shape
     flags = (HLA_NORMALIZE if normalize else 0) | (HLA_DECAY if gamma is not None else 0) | \
-        (HLA_UNMASKED if unmasked else 0)
+        _variant_flags(unmasked, asymmetric)
     return hla_params(B, H, n, d, v.shape[-1], chunk, _dtype_code(q), flags, float(eps), _ptr(gamma),
                       v.shape[1])
 
@@ -213,12 +218,14 @@ def new_workspace(nbytes: int, device="cuda"):
 
 
 def forward(q, k, v, chunk: int, gamma=None, normalize: bool = False, eps: float = 0.0, state_in=None,
-            return_state: bool = False, out=None, workspace=None, stream=None, unmasked: bool = False):
-    """2nd-order HLA forward (masked; unmasked with ``unmasked=True``).  q [B,H,n,d],
+            return_state: bool = False, out=None, workspace=None, stream=None, unmasked: bool = False,
+            asymmetric: bool = False):
+    """2nd-order HLA forward (masked; unmasked with ``unmasked=True``; the asymmetric
+    variant AHLA with ``asymmetric=True``, state R, P, m^K, E, n).  q [B,H,n,d],
     k [B,Hkv,n,d], v [B,Hkv,n,dv] contiguous CUDA tensors (bf16 or fp32; Hkv divides H);
     gamma [H] fp32 or None.  Returns o (and the final State)."""
     import torch
-    p = make_params(q, v, chunk, gamma, normalize, eps, unmasked)
+    p = make_params(q, v, chunk, gamma, normalize, eps, unmasked, asymmetric)
     o = out if out is not None else torch.empty(q.shape[:3] + (v.shape[-1],), dtype=q.dtype, device=q.device)
     need = hla_forward_workspace_size(p)
     if workspace is None and need:
@@ -228,15 +235,16 @@ def forward(q, k, v, chunk: int, gamma=None, normalize: bool = False, eps: float
     return (o, st) if return_state else o
 
 
-def state_combine(A: State, B: State, decay_pow=None, out: State | None = None, stream=None) -> State:
+def state_combine(A: State, B: State, decay_pow=None, out: State | None = None, stream=None,
+                  unmasked: bool = False, asymmetric: bool = False) -> State:
     count, d, dv = A.C.shape
     out = out if out is not None else State.empty(count, d, dv, device=A.S.device)
-    hla_state_combine(count, d, dv, A, B, out, decay_pow, stream)
+    hla_state_combine(count, d, dv, _variant_flags(unmasked, asymmetric), A, B, out, decay_pow, stream)
     return out
 
 
 def decode_step(state: State, q, k, v, H: int, gamma=None, normalize: bool = False, eps: float = 0.0,
-                out=None, stream=None, unmasked: bool = False):
+                out=None, stream=None, unmasked: bool = False, asymmetric: bool = False):
     """One decode step for N pairs (q [N,d]; k [N/H*Hkv,d], v [N/H*Hkv,dv]); state
     updated in place."""
     import torch
@@ -245,6 +253,6 @@ def decode_step(state: State, q, k, v, H: int, gamma=None, normalize: bool = Fal
     Hkv = k.shape[0] * H // N if N else H
     o = out if out is not None else torch.empty((N, dv), dtype=q.dtype, device=q.device)
     flags = (HLA_NORMALIZE if normalize else 0) | (HLA_DECAY if gamma is not None else 0) | \
-        (HLA_UNMASKED if unmasked else 0)
+        _variant_flags(unmasked, asymmetric)
     hla_decode_step(N, H, Hkv, d, dv, _dtype_code(q), flags, float(eps), gamma, state, q, k, v, o, stream)
     return o

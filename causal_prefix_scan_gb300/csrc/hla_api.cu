@@ -59,8 +59,10 @@ hla_status check_params(const hla_params *p) {
     if (p->B < 1 || p->H < 1 || p->n < 0) return fail(HLA_ERR_ARG, "need B >= 1, H >= 1, n >= 0");
     if (p->d < 1 || p->dv < 1 || p->chunk < 1) return fail(HLA_ERR_ARG, "need d, dv, chunk >= 1");
     if (p->in_dtype != HLA_F32 && p->in_dtype != HLA_BF16) return fail(HLA_ERR_ARG, "unknown in_dtype");
-    if (p->flags & ~(unsigned)(HLA_NORMALIZE | HLA_DECAY | HLA_UNMASKED))
+    if (p->flags & ~(unsigned)(HLA_NORMALIZE | HLA_DECAY | HLA_UNMASKED | HLA_ASYMMETRIC))
         return fail(HLA_ERR_ARG, "unknown flag bits");
+    if ((p->flags & HLA_UNMASKED) && (p->flags & HLA_ASYMMETRIC))
+        return fail(HLA_ERR_ARG, "HLA_UNMASKED and HLA_ASYMMETRIC exclude each other");
     if ((p->flags & HLA_DECAY) && !p->gamma) return fail(HLA_ERR_ARG, "HLA_DECAY needs gamma");
     if (p->Hkv < 0 || (p->Hkv > 0 && p->H % p->Hkv != 0))
         return fail(HLA_ERR_ARG, "Hkv must divide H (0 means Hkv = H)");
@@ -163,9 +165,11 @@ hla_status hla_forward_chunked(const hla_params *p, const void *q, const void *k
     return HLA_OK;
 }
 
-hla_status hla_state_combine(int count, int d, int dv, const hla_state *A, const hla_state *B,
+hla_status hla_state_combine(int count, int d, int dv, unsigned flags, const hla_state *A, const hla_state *B,
                              const hla_state *out, const float *decay_pow, void *stream) {
     if (count < 0) return fail(HLA_ERR_ARG, "count must be >= 0");
+    if ((flags & HLA_UNMASKED) && (flags & HLA_ASYMMETRIC))
+        return fail(HLA_ERR_ARG, "HLA_UNMASKED and HLA_ASYMMETRIC exclude each other");
     if (!width_ok(d) || !width_ok(dv)) return fail(HLA_ERR_UNSUPPORTED, "d, dv must be in {16,32,64,128}");
     if (!A || !B || !out) return fail(HLA_ERR_ARG, "A, B, out must be set");
     hla_status s;
@@ -173,7 +177,7 @@ hla_status hla_state_combine(int count, int d, int dv, const hla_state *A, const
         (s = check_state(out, "out")) != HLA_OK)
         return s;
     hla::CombineArgs a;
-    a.count = count; a.d = d; a.dv = dv;
+    a.count = count; a.d = d; a.dv = dv; a.flags = flags;
     a.A = hla::to_ptrs(A); a.B = hla::to_ptrs(B); a.out = hla::to_ptrs(out);
     a.decay_pow = decay_pow;
     cudaError_t e = hla::combine_launch(a, static_cast<cudaStream_t>(stream));
@@ -188,8 +192,10 @@ hla_status hla_decode_step(int N, int H, int Hkv, int d, int dv, hla_dtype dtype
     if (Hkv < 0 || (Hkv > 0 && H % Hkv != 0)) return fail(HLA_ERR_ARG, "Hkv must divide H (0 means Hkv = H)");
     if (!width_ok(d) || !width_ok(dv)) return fail(HLA_ERR_UNSUPPORTED, "d, dv must be in {16,32,64,128}");
     if (dtype != HLA_F32 && dtype != HLA_BF16) return fail(HLA_ERR_ARG, "unknown dtype");
-    if (flags & ~(unsigned)(HLA_NORMALIZE | HLA_DECAY | HLA_UNMASKED))
+    if (flags & ~(unsigned)(HLA_NORMALIZE | HLA_DECAY | HLA_UNMASKED | HLA_ASYMMETRIC))
         return fail(HLA_ERR_ARG, "unknown flag bits");
+    if ((flags & HLA_UNMASKED) && (flags & HLA_ASYMMETRIC))
+        return fail(HLA_ERR_ARG, "HLA_UNMASKED and HLA_ASYMMETRIC exclude each other");
     if ((flags & HLA_DECAY) && !gamma) return fail(HLA_ERR_ARG, "HLA_DECAY needs gamma");
     if (!state) return fail(HLA_ERR_ARG, "state must be set");
     hla_status s;

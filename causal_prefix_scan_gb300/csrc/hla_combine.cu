@@ -3,6 +3,11 @@
 // f = g^{len(B)}:
 //   S = f S_A + S_B,  C = f C_A + C_B,  m = f m_A + m_B,
 //   G = f^2 G_A + G_B + f S_B C_A,   h = f^2 h_A + h_B + f S_B m_A.
+// The unmasked state (S, C, m) uses the linear terms and writes G, h as zeros.
+// The asymmetric variant AHLA (R, P, m^K, E, n in the same arrays) combines by
+//   S = S_A + S_B,  C = f C_A + C_B,  m = f m_A + m_B,
+//   G = f G_A + G_B + f S_B C_A,   h = f h_A + h_B + f S_B m_A
+// (the same cross product, E decays like P).
 // Two launches on one stream: the cross terms (G, h), which read S_B, C_A and
 // m_A, run first; the linear terms (S, C, m) second.  Each output element is
 // read and written by one thread only, so out may be A or B.
@@ -26,7 +31,9 @@ __global__ void __launch_bounds__(kThreads) cross_kernel(CombineArgs a) {
     const int lr = tid / 16, lc = tid % 16;  // row in slab, column lane
     constexpr int NCOL = DV / 16 > 0 ? DV / 16 : 1;
     const float f = a.decay_pow ? a.decay_pow[item] : 1.f;
-    const float f2 = f * f;
+    const bool asym = (a.flags & HLA_ASYMMETRIC) != 0, unm = (a.flags & HLA_UNMASKED) != 0;
+    const float f2 = asym ? f : f * f;  // decay of G (E for the asymmetric variant)
+    const float fx = unm ? 0.f : 1.f;   // the unmasked state has no G, h
     const float *SB = a.B.S + (size_t)item * D * D;
     const float *CA = a.A.C + (size_t)item * D * DV;
     for (int e = tid; e < kRows * D; e += kThreads) {
@@ -59,13 +66,13 @@ __global__ void __launch_bounds__(kThreads) cross_kernel(CombineArgs a) {
 #pragma unroll
         for (int j = 0; j < NCOL; ++j) {
             const int c = lc + 16 * j;
-            if (c < DV) a.out.G[gb + c] = f2 * a.A.G[gb + c] + a.B.G[gb + c] + f * acc[j];
+            if (c < DV) a.out.G[gb + c] = fx * (f2 * a.A.G[gb + c] + a.B.G[gb + c] + f * acc[j]);
         }
         if (lc == 0) {
             float s = 0.f;
             for (int l = 0; l < D; ++l) s += sb[lr][l] * ma[l];
             const size_t hb = (size_t)item * D + row;
-            a.out.h[hb] = f2 * a.A.h[hb] + a.B.h[hb] + f * s;
+            a.out.h[hb] = fx * (f2 * a.A.h[hb] + a.B.h[hb] + f * s);
         }
     }
 }
@@ -77,9 +84,9 @@ __global__ void linear_kernel(CombineArgs a) {
     for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
         const size_t item = e / per, r = e % per;
         const float f = a.decay_pow ? a.decay_pow[item] : 1.f;
-        if (r < nS) {
+        if (r < nS) {  // S (R of the asymmetric variant, which does not decay)
             const size_t i = item * nS + r;
-            a.out.S[i] = f * a.A.S[i] + a.B.S[i];
+            a.out.S[i] = ((a.flags & HLA_ASYMMETRIC) ? 1.f : f) * a.A.S[i] + a.B.S[i];
         } else if (r < nS + nC) {
             const size_t i = item * nC + (r - nS);
             a.out.C[i] = f * a.A.C[i] + a.B.C[i];

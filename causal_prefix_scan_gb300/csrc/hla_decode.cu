@@ -251,9 +251,150 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeArgs a) {
     }
 }
 
+// Asymmetric variant AHLA (gist.science summary, section 2), state (R, P, m^K,
+// E, n) in the (S, C, m, G, h) arrays:
+//   R += k q^T;  z = g P_{t-1}^T q + (q.k) v (= P_t^T q);  P = g P + k v^T;
+//   zeta = g (q.m) + q.k (= q.m^K_t);  m^K = g m^K + k;
+//   o = g E_{t-1}^T q + (q.k) z (= E_t^T q);  E = g E + k z^T;  n = g n + k zeta;
+//   den = g (q.n_{t-1}) + (q.k) zeta.
+// Each array is streamed once from HBM and written once.
+template <typename T, int D, int DV>
+__global__ void __launch_bounds__(kThreads, 3) decode_asym_kernel(DecodeArgs a) {
+    constexpr int CG = D / 4, CGV = DV / 4;
+    constexpr int NS = D * D / 4, NC = D * DV / 4;
+    constexpr int ITS = (NS + kThreads - 1) / kThreads;
+    constexpr int ITC = (NC + kThreads - 1) / kThreads;
+    __shared__ float qs[D], ks[D], vs[DV], zs[DV];
+    __shared__ float4 redv[kThreads];
+    __shared__ float4 ysum[CGV];
+    __shared__ float red[kThreads / 32];
+
+    const int tid = threadIdx.x;
+    const size_t u = blockIdx.x;
+    const bool decay = (a.flags & HLA_DECAY) != 0;
+    const bool norm = (a.flags & HLA_NORMALIZE) != 0;
+    const float g = decay ? a.gamma[u % a.H] : 1.f;
+    const size_t kvu = (u / a.H) * a.Hkv + (u % a.H) / (a.H / a.Hkv);
+    const T *q = static_cast<const T *>(a.q) + u * D;
+    const T *k = static_cast<const T *>(a.k) + kvu * D;
+    const T *v = static_cast<const T *>(a.v) + kvu * DV;
+    for (int i = tid; i < D; i += kThreads) { qs[i] = ldf(q, i); ks[i] = ldf(k, i); }
+    for (int j = tid; j < DV; j += kThreads) vs[j] = ldf(v, j);
+    __syncthreads();
+    float4 *R = reinterpret_cast<float4 *>(a.st.S + u * D * D);
+    float4 *P = reinterpret_cast<float4 *>(a.st.C + u * D * DV);
+    float4 *E = reinterpret_cast<float4 *>(a.st.G + u * D * DV);
+    float *m = a.st.m + u * D;
+    float *n = a.st.h + u * D;
+
+    // ---- R += k q^T
+    float4 rv[ITS];
+#pragma unroll
+    for (int i = 0; i < ITS; ++i) {
+        const int e = tid + i * kThreads;
+        if (e < NS) rv[i] = R[e];
+    }
+#pragma unroll
+    for (int i = 0; i < ITS; ++i) {
+        const int e = tid + i * kThreads;
+        if (e < NS) {
+            const int row = e / CG, c0 = (e % CG) * 4;
+            const float kr = ks[row];
+            float4 x = rv[i];
+            x.x += kr * qs[c0]; x.y += kr * qs[c0 + 1]; x.z += kr * qs[c0 + 2]; x.w += kr * qs[c0 + 3];
+            R[e] = x;
+        }
+    }
+    // column reduction of x over the threads sharing a column group -> dst
+    auto colsum = [&](float4 x, float4 *dst) {
+        redv[tid] = x;
+        __syncthreads();
+        if (tid < CGV) {
+            float4 s = make_float4(0, 0, 0, 0);
+            for (int t = tid; t < kThreads; t += CGV) {
+                const float4 y = redv[t];
+                s.x += y.x; s.y += y.y; s.z += y.z; s.w += y.w;
+            }
+            dst[tid] = s;
+        }
+        __syncthreads();
+    };
+    // ---- P: y1 = P_{t-1}^T q; P = g P + k v^T
+    float4 cv[ITC];
+#pragma unroll
+    for (int i = 0; i < ITC; ++i) {
+        const int e = tid + i * kThreads;
+        if (e < NC) cv[i] = P[e];
+    }
+    float4 yp = make_float4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < ITC; ++i) {
+        const int e = tid + i * kThreads;
+        if (e < NC) {
+            const int row = e / CGV, c0 = (e % CGV) * 4;
+            const float qr = qs[row], kr = ks[row];
+            float4 x = cv[i];
+            yp.x += qr * x.x; yp.y += qr * x.y; yp.z += qr * x.z; yp.w += qr * x.w;
+            x.x = g * x.x + kr * vs[c0]; x.y = g * x.y + kr * vs[c0 + 1];
+            x.z = g * x.z + kr * vs[c0 + 2]; x.w = g * x.w + kr * vs[c0 + 3];
+            P[e] = x;
+        }
+    }
+    colsum(yp, ysum);
+    // scalars q.k, q.m_{t-1}, q.n_{t-1}
+    float pqk = 0.f, pqm = 0.f, pqn = 0.f;
+    for (int i = tid; i < D; i += kThreads) {
+        pqk += qs[i] * ks[i];
+        pqm += qs[i] * m[i];
+        pqn += qs[i] * n[i];
+    }
+    const float qk = block_sum(pqk, red);
+    const float qm = block_sum(pqm, red);
+    const float qn = norm ? block_sum(pqn, red) : 0.f;
+    const float zeta = g * qm + qk;
+    for (int j = tid; j < DV; j += kThreads) {
+        const float *y1 = reinterpret_cast<const float *>(&ysum[j >> 2]);
+        zs[j] = g * y1[j & 3] + qk * vs[j];
+    }
+    __syncthreads();
+    // ---- E: y2 = E_{t-1}^T q; E = g E + k z^T
+#pragma unroll
+    for (int i = 0; i < ITC; ++i) {
+        const int e = tid + i * kThreads;
+        if (e < NC) cv[i] = E[e];
+    }
+    yp = make_float4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < ITC; ++i) {
+        const int e = tid + i * kThreads;
+        if (e < NC) {
+            const int row = e / CGV, c0 = (e % CGV) * 4;
+            const float qr = qs[row], kr = ks[row];
+            float4 x = cv[i];
+            yp.x += qr * x.x; yp.y += qr * x.y; yp.z += qr * x.z; yp.w += qr * x.w;
+            x.x = g * x.x + kr * zs[c0]; x.y = g * x.y + kr * zs[c0 + 1];
+            x.z = g * x.z + kr * zs[c0 + 2]; x.w = g * x.w + kr * zs[c0 + 3];
+            E[e] = x;
+        }
+    }
+    colsum(yp, ysum);
+    for (int i = tid; i < D; i += kThreads) {
+        m[i] = g * m[i] + ks[i];
+        n[i] = g * n[i] + ks[i] * zeta;
+    }
+    const float den = norm ? g * qn + qk * zeta + a.eps : 1.f;
+    T *o = static_cast<T *>(a.o) + u * DV;
+    for (int j = tid; j < DV; j += kThreads) {
+        const float *y2 = reinterpret_cast<const float *>(&ysum[j >> 2]);
+        const float num = g * y2[j & 3] + qk * zs[j];
+        stf(o, j, norm ? num / den : num);
+    }
+}
+
 template <typename T, int D, int DV>
 cudaError_t launch_t(const DecodeArgs &a, cudaStream_t st) {
-    if (a.flags & HLA_UNMASKED) decode_kernel<T, D, DV, true><<<a.N, kThreads, 0, st>>>(a);
+    if (a.flags & HLA_ASYMMETRIC) decode_asym_kernel<T, D, DV><<<a.N, kThreads, 0, st>>>(a);
+    else if (a.flags & HLA_UNMASKED) decode_kernel<T, D, DV, true><<<a.N, kThreads, 0, st>>>(a);
     else decode_kernel<T, D, DV, false><<<a.N, kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }

@@ -18,8 +18,14 @@
 // linear attention", bullet "Streaming Computation"): with the same u,
 //   M[t,b] = g^{t-b} u_t.q_b            (b <= t)
 //   o_t    = sum_b M[t,b] v_b + g^{tau_t} u_t^T C_p,  den_t = sum_b M[t,b] + g^{tau_t} u_t.m_p
-// and only S, C, m are carried.  Key/value heads may be shared: query head h
-// reads key/value head h / (H / Hkv).
+// and only S, C, m are carried.  Asymmetric variant AHLA (gist.science summary,
+// section 2; state R, P, m^K, E, n kept in the S, C, m, X, Y buffers): with the
+// same A,
+//   z_b    = g^{tau_b} P_p^T q_b + sum_{a<=b} A[b,a] v_a       (= P_b^T q_b)
+//   zeta_b = g^{tau_b} q_b.m_p + sum_{a<=b} A[b,a]              (= q_b . m^K_b)
+//   o_t    = g^{tau_t} q_t^T E_p + sum_{b<=t} A[t,b] z_b,  den_t = g^{tau_t} q_t.n_p + sum_b A[t,b] zeta_b
+// and P, m^K, E, n move to the chunk end with w_b, R = R + sum_b k_b q_b^T (no decay).
+// Key/value heads may be shared: query head h reads key/value head h / (H / Hkv).
 #include "hla_internal.h"
 
 namespace hla {
@@ -57,9 +63,11 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
     float *Q = Y + D;               // c*D
     float *K = Q + kMaxChunk * D;   // c*D
     float *V = K + kMaxChunk * D;   // c*DV
-    float *U = V + kMaxChunk * DV;  // c*D
-    float *A = U + kMaxChunk * D;   // c*c (A, then M)
-    float *gp = A + kMaxChunk * kMaxChunk;  // g^x, x = 0..2c+1
+    constexpr int DU = D > DV ? D : DV;
+    float *U = V + kMaxChunk * DV;  // c*D (u-vectors), or c*DV (z-vectors of the asymmetric variant)
+    float *A = U + kMaxChunk * DU;  // c*c (A, then M)
+    float *Z = A + kMaxChunk * kMaxChunk;  // c: zeta of the asymmetric variant
+    float *gp = Z + kMaxChunk;      // g^x, x = 0..2c+1
 
     const int tid = threadIdx.x;
     const int u = blockIdx.x;  // pair index b*H + h
@@ -67,6 +75,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
     const bool decay = (a.flags & HLA_DECAY) != 0;
     const bool norm = (a.flags & HLA_NORMALIZE) != 0;
     const bool unm = (a.flags & HLA_UNMASKED) != 0;
+    const bool asym = (a.flags & HLA_ASYMMETRIC) != 0;
     const float g = decay ? a.gamma[hh] : 1.f;
     const float lg = log2f(g);
     const size_t kvu = (size_t)(u / a.H) * a.Hkv + hh / (a.H / a.Hkv);  // key/value head
@@ -78,7 +87,13 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
     for (int x = tid; x <= 2 * c + 1; x += kThreads) gp[x] = decay ? gpow(lg, (float)x) : 1.f;
 
     // ---- prefix state
-    if (a.sin.S) {
+    if (a.sin.S && asym) {  // R, P, m^K, E, n as stored
+        const float *Si = a.sin.S + (size_t)u * D * D, *Ci = a.sin.C + (size_t)u * D * DV;
+        const float *mi = a.sin.m + (size_t)u * D, *Gi = a.sin.G + (size_t)u * D * DV, *hi = a.sin.h + (size_t)u * D;
+        for (int e = tid; e < D * D; e += kThreads) S[e] = Si[e];
+        for (int e = tid; e < D * DV; e += kThreads) { Cs[e] = Ci[e]; X[e] = Gi[e]; }
+        for (int e = tid; e < D; e += kThreads) { m[e] = mi[e]; Y[e] = hi[e]; }
+    } else if (a.sin.S) {
         const float *Si = a.sin.S + (size_t)u * D * D, *Ci = a.sin.C + (size_t)u * D * DV;
         const float *mi = a.sin.m + (size_t)u * D, *Gi = a.sin.G + (size_t)u * D * DV, *hi = a.sin.h + (size_t)u * D;
         for (int e = tid; e < D * D; e += kThreads) S[e] = Si[e];
@@ -126,6 +141,75 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
             A[e] = acc;
         }
         __syncthreads();
+        if (asym) {
+            // z_b = g^{b+1} (P_p^T q_b) + sum_{a<=b} A[b,a] v_a; zeta_b likewise with m_p and 1
+            for (int e = tid; e < c * DV; e += kThreads) {
+                const int b = e / DV, j = e % DV;
+                float pz = 0.f;
+                for (int i = 0; i < D; ++i) pz += Q[b * D + i] * Cs[i * DV + j];
+                float acc = gp[b + 1] * pz;
+                for (int s2 = 0; s2 <= b; ++s2) acc += A[b * c + s2] * V[s2 * DV + j];
+                U[e] = acc;
+            }
+            for (int b = tid; b < c; b += kThreads) {
+                float qm = 0.f;
+                for (int i = 0; i < D; ++i) qm += Q[b * D + i] * m[i];
+                float acc = gp[b + 1] * qm;
+                for (int s2 = 0; s2 <= b; ++s2) acc += A[b * c + s2];
+                Z[b] = acc;
+            }
+            __syncthreads();
+            // o_t = g^{t+1} q_t^T E_p + sum_{b<=t} A[t,b] z_b  [/ (g^{t+1} q_t.n_p + sum_b A[t,b] zeta_b + eps)]
+            for (int e = tid; e < L * DV; e += kThreads) {
+                const int t = e / DV, j = e % DV;
+                float num = 0.f;
+                for (int b = 0; b <= t; ++b) num += A[t * c + b] * U[b * DV + j];
+                float pe = 0.f;
+                for (int i = 0; i < D; ++i) pe += Q[t * D + i] * X[i * DV + j];
+                num += gp[t + 1] * pe;
+                if (norm) {
+                    float den = 0.f;
+                    for (int b = 0; b <= t; ++b) den += A[t * c + b] * Z[b];
+                    float pn = 0.f;
+                    for (int i = 0; i < D; ++i) pn += Q[t * D + i] * Y[i];
+                    den += gp[t + 1] * pn;
+                    num = num / (den + a.eps);
+                }
+                st_out(o, (size_t)t0 * DV + e, num);
+            }
+            __syncthreads();
+            // state to the chunk end: R += K^T Q, P, m^K, E, n with w_b = g^{L-1-b}
+            const float gL = gp[L];
+            for (int e = tid; e < D * D; e += kThreads) {
+                const int i = e / D, j = e % D;
+                float acc = 0.f;
+                for (int s2 = 0; s2 < L; ++s2) acc += K[s2 * D + i] * Q[s2 * D + j];
+                S[e] += acc;
+            }
+            for (int e = tid; e < D * DV; e += kThreads) {
+                const int i = e / DV, j = e % DV;
+                float ap = 0.f, ae = 0.f;
+                for (int b = 0; b < L; ++b) {
+                    const float wk = gp[L - 1 - b] * K[b * D + i];
+                    ap += wk * V[b * DV + j];
+                    ae += wk * U[b * DV + j];
+                }
+                Cs[e] = gL * Cs[e] + ap;
+                X[e] = gL * X[e] + ae;
+            }
+            for (int i = tid; i < D; i += kThreads) {
+                float am = 0.f, an = 0.f;
+                for (int b = 0; b < L; ++b) {
+                    const float wk = gp[L - 1 - b] * K[b * D + i];
+                    am += wk;
+                    an += wk * Z[b];
+                }
+                m[i] = gL * m[i] + am;
+                Y[i] = gL * Y[i] + an;
+            }
+            __syncthreads();
+            continue;
+        }
         // u_b = g^{b+1} (S_p q_b) + sum_{a<=b} A[b,a] k_a   (S symmetric)
         for (int e = tid; e < c * D; e += kThreads) {
             const int b = e / D, i = e % D;
@@ -205,7 +289,13 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
         // re-tabulate is unnecessary: gp depends only on g
     }
 
-    if (a.sout.S) {
+    if (a.sout.S && asym) {  // R, P, m^K, E, n as stored
+        float *So = a.sout.S + (size_t)u * D * D, *Co = a.sout.C + (size_t)u * D * DV;
+        float *mo = a.sout.m + (size_t)u * D, *Go = a.sout.G + (size_t)u * D * DV, *ho = a.sout.h + (size_t)u * D;
+        for (int e = tid; e < D * D; e += kThreads) So[e] = S[e];
+        for (int e = tid; e < D * DV; e += kThreads) { Co[e] = Cs[e]; Go[e] = X[e]; }
+        for (int i = tid; i < D; i += kThreads) { mo[i] = m[i]; ho[i] = Y[i]; }
+    } else if (a.sout.S) {
         float *So = a.sout.S + (size_t)u * D * D, *Co = a.sout.C + (size_t)u * D * DV;
         float *mo = a.sout.m + (size_t)u * D, *Go = a.sout.G + (size_t)u * D * DV, *ho = a.sout.h + (size_t)u * D;
         for (int e = tid; e < D * D; e += kThreads) So[e] = S[e];
@@ -227,8 +317,9 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
 
 template <typename T, int D, int DV>
 cudaError_t launch_t(const FwdArgs &a, cudaStream_t st) {
-    const size_t floats = (size_t)D * D + 2 * (size_t)D * DV + 2 * D + (size_t)kMaxChunk * (3 * D + DV) +
-                          (size_t)kMaxChunk * kMaxChunk + 2 * kMaxChunk + 2;
+    constexpr int DU = D > DV ? D : DV;
+    const size_t floats = (size_t)D * D + 2 * (size_t)D * DV + 2 * D + (size_t)kMaxChunk * (2 * D + DV + DU) +
+                          (size_t)kMaxChunk * kMaxChunk + kMaxChunk + 2 * kMaxChunk + 2;
     const size_t bytes = floats * sizeof(float);
     auto kern = fwd_simt_kernel<T, D, DV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);

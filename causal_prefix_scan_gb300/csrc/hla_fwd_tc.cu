@@ -17,6 +17,7 @@ extern template cudaError_t launch_flags<true, true, true>(const FwdArgs &, cuda
 
 bool fwd_tc_supported(const hla_params &p) {
     auto ok = [](int x) { return x == 64 || x == 128; };
+    if (p.flags & HLA_ASYMMETRIC) return false;  // the asymmetric variant runs on the CUDA-core path
     return p.in_dtype == HLA_BF16 && ok(p.d) && ok(p.dv) && ok(p.chunk);
 }
 

@@ -39,13 +39,14 @@ struct FwdArgs {
 bool fwd_simt_supported(const hla_params &p);
 cudaError_t fwd_simt_launch(const FwdArgs &a, cudaStream_t st);
 
-// Tensor-core path (bf16 inputs; d, dv, chunk in {64,128}).
+// Tensor-core path (bf16 inputs; d, dv, chunk in {64,128}; asymmetric: dv <= d).
 bool fwd_tc_supported(const hla_params &p);
 size_t fwd_tc_workspace(const hla_params &p, int num_sms);
 cudaError_t fwd_tc_launch(const FwdArgs &a, cudaStream_t st, int num_sms);
 
 struct CombineArgs {
     int count, d, dv;
+    unsigned flags;  // 0, HLA_UNMASKED or HLA_ASYMMETRIC: which concatenation rule
     StatePtrs A, B, out;
     const float *decay_pow;
 };

@@ -26,6 +26,14 @@
  * "Linear-Time Higher-Order Interactions", bullet "Streaming Computation"):
  *       o_t = q_t^T S_t C_t, ratio form o_t = q_t^T S_t C_t / (q_t^T S_t m_t + eps),
  *   with the same decayed S, C, m; G and h are not part of this variant.
+ * Asymmetric variant AHLA (gist.science summary, section 2): the operator
+ *   Q (K^T Q)(K^T V), masked to o_t = sum_{a<=b<=t} (q_t.k_b)(q_b.k_a) v_a, with
+ *   summaries P_t = g P_{t-1} + k v^T, m^K_t = g m^K_{t-1} + k,
+ *   E_t = g E_{t-1} + k (q^T P_t), n_t = g n_{t-1} + k (q . m^K_t), o_t = q_t^T E_t
+ *   (ratio form: / (q_t^T n_t + eps)), and R_t = R_{t-1} + k q^T (no decay), which
+ *   composes segments: E = f E_A + E_B + f R_B P_A, n = f n_A + n_B + f R_B m_A,
+ *   R = R_A + R_B, P = f P_A + P_B, m^K = f m^K_A + m^K_B.  The state arrays hold
+ *   R in S, P in C, m^K in m, E in G and n in h.
  * Shared key/value heads (same card, section "Architecture Overview", bullet
  *   "Multi-Head Support"): k and v may carry Hkv heads, H a multiple of Hkv;
  *   query head h reads key/value head h / (H / Hkv).  The summaries stay per
@@ -78,8 +86,10 @@ typedef enum { HLA_F32 = 0, HLA_BF16 = 1 } hla_dtype;
 enum {
     HLA_NORMALIZE = 1u,  /* ratio-normalised output (section 1, "Normalisatie")          */
     HLA_DECAY = 2u,      /* per-head exponential decay ("Belangrijkste bijdragen", item 2) */
-    HLA_UNMASKED = 4u    /* unmasked output o = q^T S C (skill card, "Streaming Computation");
+    HLA_UNMASKED = 4u,   /* unmasked output o = q^T S C (skill card, "Streaming Computation");
                             state carries S, C, m; G and h are written as zeros          */
+    HLA_ASYMMETRIC = 8u  /* asymmetric variant AHLA (section 2): o = q^T E, see below;
+                            not combined with HLA_UNMASKED                               */
 };
 
 typedef struct {
@@ -103,7 +113,8 @@ typedef struct {
 /*
  * Supported shapes of hla_forward_chunked
  *   in_dtype HLA_BF16, d in {64,128}, dv in {64,128}, chunk in {64,128}:
- *       tensor-core path (tcgen05 MMA, TMEM accumulators, TMA tile loads).
+ *       tensor-core path (tcgen05 MMA, TMEM accumulators, TMA tile loads);
+ *       with HLA_ASYMMETRIC only dv <= d.
  *   in_dtype HLA_F32 or HLA_BF16 with d, dv in {16,32,64} and chunk in
  *       {16,32,64}: CUDA-core fp32 path (fp32 inputs keep full precision).
  *   Anything else: HLA_ERR_UNSUPPORTED.  Any n >= 0; a final partial chunk is
@@ -146,12 +157,15 @@ HLA_API hla_status hla_forward_chunked(const hla_params *p, const void *q, const
  *   S = f S_A + S_B,  C = f C_A + C_B,  m = f m_A + m_B,
  *   G = f^2 G_A + G_B + f S_B C_A,  h = f^2 h_A + h_B + f S_B m_A,
  * with f = decay_pow[i] (= g^{len(B)}), or f = 1 when decay_pow is NULL.
+ * flags: 0 (masked), HLA_UNMASKED (S, C, m as above; G, h written as zeros) or
+ * HLA_ASYMMETRIC (the AHLA rule above: S = S_A + S_B, G = f G_A + G_B + f S_B C_A,
+ * h = f h_A + h_B + f S_B m_A; other flag bits are ignored).
  * A, B, out: states of `count` items with widths d, dv (any d, dv in
  * {16,32,64,128}).  out may be A or B (all five pointers equal); partial
  * aliasing between different arrays is not allowed.  The product S_B C_A is
  * formed in fp32.
  */
-HLA_API hla_status hla_state_combine(int count, int d, int dv, const hla_state *A,
+HLA_API hla_status hla_state_combine(int count, int d, int dv, unsigned flags, const hla_state *A,
                              const hla_state *B, const hla_state *out,
                              const float *decay_pow, void *stream);
 
@@ -163,6 +177,7 @@ HLA_API hla_status hla_state_combine(int count, int d, int dv, const hla_state *
  * o = q^T (S_t C_t - G_t) (divided by q^T (S_t m_t - h_t) + eps with
  * HLA_NORMALIZE).  With HLA_UNMASKED the output is o = q^T S_t C_t (divided by
  * q^T S_t m_t + eps), and G, h are neither read nor written (they may be NULL).
+ * With HLA_ASYMMETRIC the state is (R, P, m^K, E, n) and the output q^T E_t.
  *   q: [N][d], o: [N][dv]; k: [N/H*Hkv][d], v: [N/H*Hkv][dv] (row s*Hkv + h/(H/Hkv)
  *   for pair u); element type `dtype` (HLA_F32 or HLA_BF16);
  *   Hkv: key/value heads per sequence, H % Hkv == 0 (0 means H);

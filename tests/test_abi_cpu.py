@@ -61,7 +61,9 @@ def _call(p, q=16, k=16, v=16, o=16, sin=None, sout=None, ws=None, ws_bytes=0):
     (dict(H=0), hla.HLA_ERR_ARG),
     (dict(n=-1), hla.HLA_ERR_ARG),
     (dict(in_dtype=7), hla.HLA_ERR_ARG),
-    (dict(flags=8), hla.HLA_ERR_ARG),
+    (dict(flags=16), hla.HLA_ERR_ARG),
+    (dict(flags=hla.HLA_UNMASKED | hla.HLA_ASYMMETRIC), hla.HLA_ERR_ARG),
+    (dict(flags=hla.HLA_ASYMMETRIC, d=128, dv=128), hla.HLA_ERR_UNSUPPORTED),  # not on the CUDA-core path
     (dict(H=6, Hkv=4), hla.HLA_ERR_ARG),                    # key/value heads must divide H
     (dict(Hkv=-1), hla.HLA_ERR_ARG),
     (dict(flags=hla.HLA_DECAY), hla.HLA_ERR_ARG),          # decay without gamma
@@ -90,18 +92,22 @@ def test_combine_and_decode_reject_bad_args(lib):
     L = hla.library()
     st = hla.hla_state(16, 16, 16, 16, 16)
     sp = ctypes.pointer(st)
-    assert L.hla_state_combine(-1, 64, 64, sp, sp, sp, None, None) == hla.HLA_ERR_ARG
-    assert L.hla_state_combine(1, 48, 64, sp, sp, sp, None, None) == hla.HLA_ERR_UNSUPPORTED
-    assert L.hla_state_combine(1, 64, 64, None, sp, sp, None, None) == hla.HLA_ERR_ARG
+    assert L.hla_state_combine(-1, 64, 64, 0, sp, sp, sp, None, None) == hla.HLA_ERR_ARG
+    assert L.hla_state_combine(1, 48, 64, 0, sp, sp, sp, None, None) == hla.HLA_ERR_UNSUPPORTED
+    assert L.hla_state_combine(1, 64, 64, 0, None, sp, sp, None, None) == hla.HLA_ERR_ARG
+    assert L.hla_state_combine(1, 64, 64, hla.HLA_UNMASKED | hla.HLA_ASYMMETRIC, sp, sp, sp, None,
+                               None) == hla.HLA_ERR_ARG
     assert L.hla_decode_step(5, 2, 0, 64, 64, hla.HLA_BF16, 0, 0.0, None, sp, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
     assert L.hla_decode_step(4, 2, 0, 64, 64, hla.HLA_BF16, hla.HLA_DECAY, 0.0, None, sp, 16, 16, 16, 16,
                              None) == hla.HLA_ERR_ARG
     assert L.hla_decode_step(4, 2, 0, 64, 64, 9, 0, 0.0, None, sp, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
     assert L.hla_decode_step(4, 2, 0, 64, 64, hla.HLA_BF16, 0, 0.0, None, None, 16, 16, 16, 16,
                              None) == hla.HLA_ERR_ARG
-    # key/value heads must divide the query heads; flag bits above HLA_UNMASKED are unknown
+    # key/value heads must divide the query heads; flag bits above HLA_ASYMMETRIC are unknown
     assert L.hla_decode_step(6, 3, 2, 64, 64, hla.HLA_BF16, 0, 0.0, None, sp, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
-    assert L.hla_decode_step(4, 2, 0, 64, 64, hla.HLA_BF16, 8, 0.0, None, sp, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
+    assert L.hla_decode_step(4, 2, 0, 64, 64, hla.HLA_BF16, 16, 0.0, None, sp, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
+    assert L.hla_decode_step(4, 2, 0, 64, 64, hla.HLA_BF16, hla.HLA_UNMASKED | hla.HLA_ASYMMETRIC, 0.0, None, sp,
+                             16, 16, 16, 16, None) == hla.HLA_ERR_ARG
     # the unmasked state needs S, C, m only
     um = hla.hla_state(16, 16, None, None, None)
     assert L.hla_decode_step(4, 2, 0, 64, 64, hla.HLA_BF16, hla.HLA_UNMASKED, 0.0, None, ctypes.pointer(um),

@@ -200,6 +200,33 @@ def test_shared_kv_heads(unmasked, chunk, d, dv, dtype):
                   what=f"shared kv unmasked={unmasked} c{chunk} d{d} dv{dv}")
 
 
+# ------------------------------------------------------- asymmetric variant (AHLA)
+@pytest.mark.parametrize("d,dv,chunk,n", [(16, 32, 16, 100), (64, 64, 64, 130), (32, 16, 32, 45), (64, 32, 64, 200)])
+@pytest.mark.parametrize("decay,normalize", [(False, False), (True, False), (True, True)])
+def test_asym_forward(d, dv, chunk, n, decay, normalize):
+    for dtype in ("f32", "bf16"):
+        w = small("asym", d=d, dv=dv, chunk=chunk, n=n, dtype=dtype, decay=decay,
+                  qk="elu1" if normalize else "l2", seed=27)
+        x = W.make_inputs(w)
+        o, st = run_forward(x, dtype, chunk, normalize=normalize, eps=1e-6, asymmetric=True)
+        o_ref, st_ref = run_oracle(x, normalize=normalize, eps=1e-6, asymmetric=True)
+        assert_parity(o, o_ref, st, st_ref, tol=TOL_F32 if dtype == "f32" else TOL_BF16,
+                      what=f"asym {dtype} d{d} dv{dv}", asymmetric=True)
+
+
+def test_asym_resume_and_shared_kv():
+    w = small("asym_kv", B=2, H=4, Hkv=2, n=300, d=64, dv=64, chunk=64, dtype="f32", decay=True, qk="elu1",
+              seed=28)
+    x = W.make_inputs(w)
+    n1 = 117
+    x1 = {kk: (vv[:, :, :n1] if kk != "gamma" else vv) for kk, vv in x.items()}
+    x2 = {kk: (vv[:, :, n1:] if kk != "gamma" else vv) for kk, vv in x.items()}
+    _, st1 = run_oracle(x1, normalize=True, eps=1e-6, asymmetric=True)
+    o2, st2 = run_forward(x2, "f32", 64, normalize=True, eps=1e-6, state_in=st1, asymmetric=True)
+    o2_ref, st2_ref = run_oracle(x2, normalize=True, eps=1e-6, state_in=st1, asymmetric=True)
+    assert_parity(o2, o2_ref, st2, st2_ref, tol=TOL_F32, what="asym resume, shared kv", asymmetric=True)
+
+
 # ------------------------------------------------------------------ combine
 @pytest.mark.parametrize("d,dv", [(64, 64), (128, 128), (16, 32), (64, 128)])
 def test_state_combine(d, dv):
@@ -282,6 +309,57 @@ def test_decode_unmasked_and_shared_heads(unmasked, Hkv):
         got.G[...] = ref.G
         got.h[...] = ref.h
     state_errors(got, ref, 1e-5, "decode state")
+
+
+@pytest.mark.parametrize("d,dv,Hkv", [(128, 128, 4), (64, 64, 2), (32, 16, 1)])
+def test_decode_asym(d, dv, Hkv):
+    seqs, H, steps = 6, 4, 3
+    N = seqs * H
+    rng = np.random.default_rng(21)
+    gamma = np.exp(rng.uniform(np.log(0.9), np.log(0.999), H))
+    pre = W.make_inputs(W.Workload("pre", seqs, H, 40, d, dv, 64, "bf16", "elu1", seed=35, Hkv=Hkv))
+    _, st = oracle.forward(pre["q"], pre["k"], pre["v"], gamma=gamma, asymmetric=True)
+    st32 = oracle.State(*(np.asarray(a, np.float32).astype(np.float64) for a in st.astuple()))
+    dst = state_to_dev(st32)
+    g = torch.from_numpy(gamma.astype(np.float32)).cuda()
+    g64 = gamma.astype(np.float32).astype(np.float64)
+    ref = st32.copy()
+    for s in range(steps):
+        toks = W.make_decode_tokens(seqs, H, d, dv, 1, seed=50 + s)
+        qn = np.abs(toks["q"][0])
+        kn = np.ascontiguousarray(np.abs(toks["k"][0]).reshape(seqs, H, d)[:, :Hkv].reshape(seqs * Hkv, d))
+        vn = np.ascontiguousarray(toks["v"][0].reshape(seqs, H, dv)[:, :Hkv].reshape(seqs * Hkv, dv))
+        q, k, v = to_dev(qn, "bf16"), to_dev(kn, "bf16"), to_dev(vn, "bf16")
+        o = hla.decode_step(dst, q, k, v, H, gamma=g, normalize=True, eps=1e-6, asymmetric=True)
+        o_ref = oracle.decode_step(ref, qn, kn, vn, H, gamma=g64, normalize=True, eps=1e-6, asymmetric=True)
+        hla.hla_sync_status()
+        og = o.float().cpu().numpy()
+        assert max(rel_l2(og[u], o_ref[u]) for u in range(N)) <= TOL_BF16, f"step {s}"
+    state_errors(state_to_np(dst, N, d, dv), ref, 1e-5, "asym decode state", asymmetric=True)
+
+
+@pytest.mark.parametrize("variant", ["unmasked", "asymmetric"])
+def test_state_combine_variants(variant):
+    d, dv, cnt = 64, 32, 6
+    rng = np.random.default_rng(22)
+    kw = {variant: True}
+    wa = W.Workload("ca", 1, cnt, 30, d, dv, 64, "f32", "l2", seed=36)
+    wb = W.Workload("cb", 1, cnt, 23, d, dv, 64, "f32", "l2", seed=37)
+    xa, xb = W.make_inputs(wa), W.make_inputs(wb)
+    gamma = rng.uniform(0.9, 0.99, cnt)
+    _, A = oracle.forward(xa["q"], xa["k"], xa["v"], gamma=gamma, **kw)
+    _, B = oracle.forward(xb["q"], xb["k"], xb["v"], gamma=gamma, **kw)
+    f = gamma ** 23
+    ref = oracle.combine(A, B, f, asymmetric=(variant == "asymmetric"))
+    if variant == "unmasked":
+        ref.G[...] = 0.0
+        ref.h[...] = 0.0
+    f32 = lambda st: oracle.State(*(np.asarray(a, np.float32).astype(np.float64) for a in st.astuple()))
+    dA, dB = state_to_dev(f32(A)), state_to_dev(f32(B))
+    df = torch.from_numpy(f.astype(np.float32)).cuda()
+    out = hla.state_combine(dA, dB, df, **kw)
+    hla.hla_sync_status()
+    state_errors(state_to_np(out, cnt, d, dv), ref, 1e-5, f"combine {variant}", asymmetric=True)
 
 
 # ---------------------------------------------------- full-size workloads
