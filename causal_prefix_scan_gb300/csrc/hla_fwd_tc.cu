@@ -1,23 +1,27 @@
 // hla_fwd_tc.cu -- host entry of the tensor-core forward: support check,
-// workspace size, and dispatch to the (decay, normalise, unmasked) launchers
-// compiled in hla_fwd_tc_f0..f7.cu.
+// workspace size, and dispatch to the (decay, normalise, variant) launchers
+// compiled in hla_fwd_tc_f0..f11.cu.
 #include "hla_fwd_tc.cuh"
 
 namespace hla {
 namespace tc {
-extern template cudaError_t launch_flags<false, false, false>(const FwdArgs &, cudaStream_t, int);
-extern template cudaError_t launch_flags<false, false, true>(const FwdArgs &, cudaStream_t, int);
-extern template cudaError_t launch_flags<false, true, false>(const FwdArgs &, cudaStream_t, int);
-extern template cudaError_t launch_flags<false, true, true>(const FwdArgs &, cudaStream_t, int);
-extern template cudaError_t launch_flags<true, false, false>(const FwdArgs &, cudaStream_t, int);
-extern template cudaError_t launch_flags<true, false, true>(const FwdArgs &, cudaStream_t, int);
-extern template cudaError_t launch_flags<true, true, false>(const FwdArgs &, cudaStream_t, int);
-extern template cudaError_t launch_flags<true, true, true>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t launch_flags<false, false, 0>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t launch_flags<false, false, 1>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t launch_flags<false, false, 2>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t launch_flags<false, true, 0>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t launch_flags<false, true, 1>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t launch_flags<false, true, 2>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t launch_flags<true, false, 0>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t launch_flags<true, false, 1>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t launch_flags<true, false, 2>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t launch_flags<true, true, 0>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t launch_flags<true, true, 1>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t launch_flags<true, true, 2>(const FwdArgs &, cudaStream_t, int);
 }  // namespace tc
 
 bool fwd_tc_supported(const hla_params &p) {
     auto ok = [](int x) { return x == 64 || x == 128; };
-    if (p.flags & HLA_ASYMMETRIC) return false;  // the asymmetric variant runs on the CUDA-core path
+    if ((p.flags & HLA_ASYMMETRIC) && p.dv > p.d) return false;  // its spare accumulator is d wide
     return p.in_dtype == HLA_BF16 && ok(p.d) && ok(p.dv) && ok(p.chunk);
 }
 
@@ -27,17 +31,21 @@ size_t fwd_tc_workspace(const hla_params &p, int num_sms) {
 }
 
 cudaError_t fwd_tc_launch(const FwdArgs &a, cudaStream_t st, int num_sms) {
-    const int key = ((a.flags & HLA_DECAY) ? 4 : 0) | ((a.flags & HLA_NORMALIZE) ? 2 : 0) |
-                    ((a.flags & HLA_UNMASKED) ? 1 : 0);
+    const int var = (a.flags & HLA_UNMASKED) ? 1 : ((a.flags & HLA_ASYMMETRIC) ? 2 : 0);
+    const int key = ((a.flags & HLA_DECAY) ? 6 : 0) + ((a.flags & HLA_NORMALIZE) ? 3 : 0) + var;
     switch (key) {
-        case 0: return tc::launch_flags<false, false, false>(a, st, num_sms);
-        case 1: return tc::launch_flags<false, false, true>(a, st, num_sms);
-        case 2: return tc::launch_flags<false, true, false>(a, st, num_sms);
-        case 3: return tc::launch_flags<false, true, true>(a, st, num_sms);
-        case 4: return tc::launch_flags<true, false, false>(a, st, num_sms);
-        case 5: return tc::launch_flags<true, false, true>(a, st, num_sms);
-        case 6: return tc::launch_flags<true, true, false>(a, st, num_sms);
-        default: return tc::launch_flags<true, true, true>(a, st, num_sms);
+        case 0: return tc::launch_flags<false, false, 0>(a, st, num_sms);
+        case 1: return tc::launch_flags<false, false, 1>(a, st, num_sms);
+        case 2: return tc::launch_flags<false, false, 2>(a, st, num_sms);
+        case 3: return tc::launch_flags<false, true, 0>(a, st, num_sms);
+        case 4: return tc::launch_flags<false, true, 1>(a, st, num_sms);
+        case 5: return tc::launch_flags<false, true, 2>(a, st, num_sms);
+        case 6: return tc::launch_flags<true, false, 0>(a, st, num_sms);
+        case 7: return tc::launch_flags<true, false, 1>(a, st, num_sms);
+        case 8: return tc::launch_flags<true, false, 2>(a, st, num_sms);
+        case 9: return tc::launch_flags<true, true, 0>(a, st, num_sms);
+        case 10: return tc::launch_flags<true, true, 1>(a, st, num_sms);
+        default: return tc::launch_flags<true, true, 2>(a, st, num_sms);
     }
 }
 

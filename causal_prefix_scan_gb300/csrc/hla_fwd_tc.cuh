@@ -167,9 +167,11 @@ __device__ __forceinline__ int row_of(int q, int l) {
     else return 16 * q + (l & 15);
 }
 
-template <int C, int D, int DV, bool DECAY, bool NORM, bool UNM>
+template <int C, int D, int DV, bool DECAY, bool NORM, int VAR>
 struct Kern {
     using K_ = Cfg<C, D, DV>;
+    // variant: 0 masked, 1 unmasked (o = q^T S C), 2 asymmetric (AHLA)
+    static constexpr bool UNM = VAR == 1, ASYM = VAR == 2;
     static constexpr uint32_t TW = K_::TW, TS = K_::TS, TX = K_::TX, T4 = K_::T4;
     const TcParams &P;
     uint8_t *base;
@@ -581,7 +583,10 @@ struct Kern {
     }
 
     // den[t] = q_t . Y for every row t of the Q tile (all threads; partials in rsum).
-    __device__ void row_dot_Y(const uint8_t *Q) {
+    __device__ void row_dot_Y(const uint8_t *Q) { row_dot(Q, Yrun(), den()); }
+    // out[r] = q_r . vec for the rows of a [C x D] tile (all threads; rsum() is
+    // scratch; out is written by threads < C after an internal barrier).
+    __device__ void row_dot(const uint8_t *Q, const float *vec, float *out) {
         constexpr int NPR = kThreads / C, CPT = D / NPR;
         const int r = tid % C, part = tid / C;
         float acc = 0.f;
@@ -590,7 +595,7 @@ struct Kern {
             float q8[8];
             tile_load_row8(Q, C, r, part * CPT + c0, q8);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc += q8[j] * Yrun()[part * CPT + c0 + j];
+            for (int j = 0; j < 8; ++j) acc += q8[j] * vec[part * CPT + c0 + j];
         }
         rsum()[part * C + r] = acc;
         __syncthreads();
@@ -598,19 +603,60 @@ struct Kern {
             float sacc = 0.f;
 #pragma unroll
             for (int pp = 0; pp < NPR; ++pp) sacc += rsum()[pp * C + tid];
-            den()[tid] = sacc;
+            out[tid] = sacc;
         }
     }
+    // Column sums with per-row weights: dm[i] = sm * dm[i] + sum_{r < L} rw[r] t[r][i]
+    // for a [C x D] tile (all threads; scr: 8 x D floats; rw in shared memory).
+    __device__ void tile_colsums_rw(const uint8_t *t, int L, const float *rw, float *scr, float *dm, float sm) {
+        constexpr int NB = D / 8, NG = kThreads / NB;
+        const int cb = tid % NB, rg = tid / NB;
+        float am[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) am[j] = 0.f;
+        for (int r = rg; r < L; r += NG) {
+            float a[8];
+            tile_load_row8(t, C, r, cb * 8, a);
+            const float w = rw[r];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) am[j] += w * a[j];
+        }
+#pragma unroll
+        for (int off = NB; off < 32; off <<= 1) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) am[j] += __shfl_xor_sync(0xffffffffu, am[j], off);
+        }
+        if (lane < NB) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) scr[warp * D + cb * 8 + j] = am[j];
+        }
+        __syncthreads();
+        if (tid < D) {
+            float a = 0.f;
+#pragma unroll
+            for (int w8 = 0; w8 < kThreads / 32; ++w8) a += scr[w8 * D + tid];
+            dm[tid] = sm * dm[tid] + a;
+        }
+        __syncthreads();
+    }
 
-    // A-tilde = tril(Gamma1 o A) from TMEM W -> tA()
+    // A-tilde = tril(Gamma1 o A) from TMEM W -> tA(); with ROWSUM its row partial
+    // sums go to rsum() (one slot per column part).
+    template <bool ROWSUM = false>
     __device__ void epi_atilde() {
         float gt[3];
         load_g16<1>(gt);
+        float rs = 0.f;
         for_row<C, C>(TW, [&](int c0, float (&v)[16]) {
             if (rowC < 0) return;
             mask_row<1>(rowC, c0, v, gt);
+            if constexpr (ROWSUM) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) rs += v[i];
+            }
             tile_store_row16(tA(), C, rowC, c0, v);
         });
+        if constexpr (ROWSUM) put_partial<C>(rsum(), rowC, rs);
     }
 
     // ======================================================================== pass 1
@@ -740,6 +786,35 @@ struct Kern {
 
     // ======================================================================== scan
     __device__ bool prefix_init() {
+        if constexpr (ASYM) {  // R -> TS, P -> T4, E -> TX, m^K -> mrun(), n -> Yrun(), as stored
+            if (!P.sin.S) {
+                zero_slot<D, D>(TS);
+                zero_slot<D, DV>(TX);
+                zero_slot<D, DV>(T4);
+                for (int i = tid; i < D; i += kThreads) mrun()[i] = Yrun()[i] = 0.f;
+            } else {
+                const float *Si = P.sin.S + (size_t)bh * D * D, *Ci = P.sin.C + (size_t)bh * D * DV;
+                const float *Gi = P.sin.G + (size_t)bh * D * DV;
+                auto load = [&](const float *src, int ld) {
+                    return [=](int c0, float (&v)[16]) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4) {
+                            const float4 a = *reinterpret_cast<const float4 *>(src + rowD * ld + c0 + i);
+                            v[i] = a.x; v[i + 1] = a.y; v[i + 2] = a.z; v[i + 3] = a.w;
+                        }
+                    };
+                };
+                rmw_row<D, D>(TS, load(Si, D));
+                rmw_row<D, DV>(T4, load(Ci, DV));
+                rmw_row<D, DV>(TX, load(Gi, DV));
+                for (int i = tid; i < D; i += kThreads) {
+                    mrun()[i] = P.sin.m[(size_t)bh * D + i];
+                    Yrun()[i] = P.sin.h[(size_t)bh * D + i];
+                }
+            }
+            publish();
+            return true;
+        }
         if constexpr (UNM) {  // S -> TS, C -> TX, m -> mrun(); G, h are not part of the state
             if (!P.sin.S) {
                 zero_slot<D, D>(TS);
@@ -1479,6 +1554,368 @@ struct Kern {
         __syncthreads();
         return true;
     }
+
+    // ======================================================================== asymmetric variant
+    // AHLA (gist.science summary, section 2): o_t = sum_{a<=b<=t} (q_t.k_b)(q_b.k_a) v_a
+    // = q_t^T E_t.  Per chunk, with A-tilde as in the masked path and the state
+    // (P_p, E_p, m_p, n_p) at the chunk start:
+    //   Z    = A-tilde V + diag(g^tau) Q P_p          (rows z_b = P_b^T q_b)
+    //   zeta = rowsum(A-tilde) + diag(g^tau) Q m_p    (zeta_b = q_b . m^K_b)
+    //   O    = A-tilde Z + diag(g^tau) Q E_p,  den = A-tilde zeta + diag(g^tau) Q n_p
+    //   P <- g^L P + K^T W V,  E <- g^L E + K^T W Z,  m^K <- g^L m^K + K^T w,
+    //   n <- g^L n + K^T W zeta,  R <- R + K^T Q  (W = diag(g^{L - tau})).
+    // TMEM: work W (A, Z, O), R in the S slot (spare in pass 2), E in the X slot,
+    // P in the fourth slot; m^K in mrun(), n in Yrun().  Requires dv <= d.
+    //   zeta, and n, are formed only when the normaliser or the state is wanted.
+
+    // Pass 1: the piece's R, P, E, m^K, n from zero.  P and m^K are rescaled per
+    // chunk (their values at the chunk start feed the next chunk); E and n take
+    // weights relative to the piece end; R has no decay.
+    __device__ bool pass1_asym(int jb, int je) {
+        for (int i = tid; i < D; i += kThreads) mrun()[i] = Yrun()[i] = 0.f;
+        const int LB = min(P.n, je * C) - jb * C;
+        int stage = 0;
+        tma_chunk(jb, 0);
+        for (int jj = jb; jj < je; ++jj) {
+            const bool first = (jj == jb);
+            const int L = min(C, P.n - jj * C);
+            const int rest = LB - (jj - jb) * C - L;
+            if (K_::NSTAGE == 1 && !first) tma_chunk(jj, 0);
+            uint8_t *Q = sQ(stage), *Kt = sK(stage), *V = sV(stage);
+            if (!wait_tma(stage)) return false;
+            if (K_::NSTAGE == 2 && jj + 1 < je) tma_chunk(jj + 1, stage ^ 1);
+            if (tid == 0) mma_kk<C, D>(TW, Q, Kt, false);  // A = Q K^T
+            commit();
+            if (!first) {  // P_p -> bf16 operand, P decayed to the chunk end; diag(g^tau) Q
+                extract_state<DV>(T4, tQ(), gp(L));
+                if constexpr (DECAY) scaled_tile_copy<D>(Q, tS(), [&](int r) { return gp(r + 1); });
+            }
+            if (need_mY) row_dot(Q, mrun(), den());  // q_b . m_p (m local to the piece)
+            if (!wait_mma()) return false;
+            epi_atilde<true>();
+            publish();
+            if (tid == 0) {
+                mma_km<DV, C>(TW, tA(), V, false);                                    // A-tilde V
+                if (!first) mma_km<DV, D>(TW, DECAY ? tS() : Q, tQ(), true);         // + diag(g^tau) Q P_p
+            }
+            commit();
+            if (need_mY && tid < C) {  // zeta_b (in den()), then the weight of k_b in n
+                const float zeta = sum_partials<C>(rsum(), tid) + (first ? 0.f : gp(tid + 1) * den()[tid]);
+                den()[tid] = tid < L ? gp(rest + L - 1 - tid) * zeta : 0.f;
+            }
+            if (!wait_mma()) return false;
+            // Z -> tU() with the piece-end factor g^rest (E's weights are g^{rest} W)
+            {
+                const float zs = DECAY ? gp(rest) : 1.f;
+                for_row<C, DV>(TW, [&](int c0, float (&v)[16]) {
+                    if (rowC < 0) return;
+                    if constexpr (DECAY) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= zs;
+                    }
+                    tile_store_row16(tU(), C, rowC, c0, v);
+                });
+            }
+            if constexpr (DECAY)  // K_w = diag(g^{L-1-tau}) K
+                scaled_tile_copy<D>(Kt, tA(), [&](int r) { return r < L ? gp(L - 1 - r) : 0.f; });
+            publish();
+            if (tid == 0) {
+                mma_mm<DV>(T4, DECAY ? tA() : Kt, V, !first);    // P += K^T W V
+                mma_mm<DV>(TX, DECAY ? tA() : Kt, tU(), !first); // E += g^rest K^T W Z
+                mma_mm<D>(TS, Kt, Q, !first);                    // R += K^T Q
+            }
+            commit();
+            if (need_mY) {  // n += sum_b g^{rest+L-1-b} zeta_b k_b; m^K <- g^L m^K + sum_b g^{L-1-b} k_b
+                tile_colsums_rw(Kt, L, den(), reinterpret_cast<float *>(tQ()), Yrun(), 1.f);
+                tile_colsums<false>(Kt, nullptr, L, 1.f, reinterpret_cast<float *>(tQ()), mrun(), gp(L), nullptr,
+                                    1.f);
+            }
+            if (!wait_mma()) return false;
+            stage ^= (K_::NSTAGE - 1);
+        }
+        return true;
+    }
+
+    // prefix <- prefix (+) L_0 (+) ... (+) L_{cnt-1} by the asymmetric rule
+    //   R <- R + R_L,  P <- f P + P_L,  m^K <- f m^K + m_L,
+    //   E <- f E + E_L + f R_L P,   n <- f n + n_L + f R_L m^K   (P, m^K before the step).
+    // Unrolled, the product of step r reaches the result with weight
+    // g^{start(cnt) - start(r)}; it accumulates, weighted, in the spare accumulator
+    // (R_L from the summary as the A operand, the old P from TMEM as B), as in the
+    // masked fold; step r+1 runs while the MMAs of step r do.
+    template <typename Start>
+    __device__ bool fold_asym(const float *Lsum, int cnt, Start &&start, bool zero_prefix) {
+        constexpr int NS = share<D>(), NV = share<DV>();
+        const int cs = share_col<D>(), cv = share_col<DV>();
+        const int t_end = start(cnt);
+        unsigned pend = 0u;
+        bool cross = false;
+        for (int r = 0; r < cnt; ++r) {
+            const float *RL = Lsum + (size_t)r * K_::SUM, *EL = RL + D * D, *PL = EL + D * DV, *mL = PL + D * DV,
+                        *nL = mL + D;
+            const int b = K_::FBUF == 2 ? (r & 1) : 0;
+            const bool z = zero_prefix && r == 0;
+            const float f = gp(start(r + 1) - start(r));
+            const float coef = DECAY ? gp(t_end - start(r)) : 1.f;
+            uint8_t *shi = fShi(b), *slo = fSlo(b), *chi = fChi(b), *clo = fClo(b);
+            const float mLi = tid < D ? __ldcg(mL + tid) : 0.f, nLi = tid < D ? __ldcg(nL + tid) : 0.f;
+            if (pend >> b & 1u) {
+                if (!wait_buf(b)) return false;
+                pend &= ~(1u << b);
+            } else if (r > 0) {
+                __syncthreads();  // every thread's m^K update of the last step precedes the reads below
+            }
+            float rm = 0.f;  // row partial of R_L m_old
+#pragma unroll
+            for (int c = 0; c < NS; c += 16) {  // R: R_L -> operand (hi + lo), R += R_L
+                float rl[16], v[16];
+                ld_sum16(RL, rowD, cs + c, rl);
+                if (!z) {
+                    ld_share<D>(TS, c, v);
+                    tmem_wait_ld();
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    rm += rl[i] * (z ? 0.f : mrun()[cs + c + i]);
+                    v[i] = z ? rl[i] : v[i] + rl[i];
+                }
+                if (!z) store_hilo(shi, slo, D, rowD, cs + c, rl);
+                st_share<D>(TS, c, v);
+            }
+#pragma unroll
+            for (int c = 0; c < NV; c += 16) {  // P: weighted old P -> operand, update; E without the product
+                float pl[16], el[16], v[16], w[16];
+                ld_sum16(PL, rowD, cv + c, pl);
+                ld_sum16(EL, rowD, cv + c, el);
+                if (!z) {
+                    ld_share<DV>(T4, c, v);
+                    ld_share<DV>(TX, c, w);
+                    tmem_wait_ld();
+                }
+                float o[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    o[i] = z ? 0.f : coef * v[i];
+                    v[i] = z ? pl[i] : f * v[i] + pl[i];
+                    w[i] = z ? el[i] : f * w[i] + el[i];
+                }
+                if (!z) store_hilo(chi, clo, D, rowD, cv + c, o);
+                st_share<DV>(T4, c, v);
+                st_share<DV>(TX, c, w);
+            }
+            tmem_wait_st();
+            put_partial<D>(part(b), rowD, rm);
+            publish();
+            if (!z) {
+                if (tid == 0) {
+                    mma_ss(TW, shi, chi, cross);
+                    mma_ss(TW, shi, clo, true);
+                    mma_ss(TW, slo, chi, true);
+                }
+                commit_buf(b);
+                pend |= 1u << b;
+                cross = true;
+            }
+            if (tid < D) {
+                if (z) {
+                    Yrun()[tid] = nLi;
+                    mrun()[tid] = mLi;
+                } else {
+                    Yrun()[tid] = f * Yrun()[tid] + nLi + f * sum_partials<D>(part(b), tid);
+                    mrun()[tid] = f * mrun()[tid] + mLi;
+                }
+            }
+        }
+        if ((pend & 1u) && !wait_mma()) return false;
+        if ((pend & 2u) && !wait_mma2()) return false;
+        if (cross) {  // E += sum of the products
+            constexpr int N = share<DV>();
+#pragma unroll
+            for (int c = 0; c < N; c += 16) {
+                float v[16], w[16];
+                ld_share<DV>(TW, c, v);
+                ld_share<DV>(TX, c, w);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[i] += v[i];
+                st_share<DV>(TX, c, w);
+            }
+            tmem_wait_st();
+        }
+        tc_sync();
+        return true;
+    }
+
+    // State export, part 1 (asymmetric): R = R_prefix + R_L to state_out now (pass 2
+    // uses its slot); without the normaliser also m^K = f m_p + m_L and
+    // n = f n_p + n_L + f R_L m_p (pass 2 carries P, E, and m^K, n when normalising).
+    __device__ void export_pre_asym(const float *Lown, float f) {
+        const float *RL = Lown, *mL = Lown + D * D + 2 * D * DV, *nL = mL + D;
+        float *Ro = P.sout.S + (size_t)bh * D * D;
+        constexpr int NS = share<D>();
+        const int cs = share_col<D>();
+        float rm = 0.f;
+#pragma unroll
+        for (int c = 0; c < NS; c += 16) {
+            float rl[16], v[16];
+            ld_sum16(RL, rowD, cs + c, rl);
+            ld_share<D>(TS, c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                rm += rl[i] * mrun()[cs + c + i];
+                v[i] += rl[i];
+            }
+            st_row16(Ro + rowD * D + cs + c, v);
+        }
+        if constexpr (!NORM) put_partial<D>(part(), rowD, rm);
+        tc_sync();
+        if constexpr (!NORM) {
+            if (tid < D) {
+                const float mp = mrun()[tid];
+                Yrun()[tid] = f * Yrun()[tid] + __ldcg(nL + tid) + f * sum_partials<D>(part(), tid);
+                mrun()[tid] = f * mp + __ldcg(mL + tid);
+            }
+            __syncthreads();
+        }
+    }
+
+    // State export, part 2 (asymmetric): P, E, m^K, n at the sequence end.
+    __device__ void export_post_asym() {
+        float *Co = P.sout.C + (size_t)bh * D * DV, *Go = P.sout.G + (size_t)bh * D * DV;
+        constexpr int NV = share<DV>();
+        const int cv = share_col<DV>();
+#pragma unroll
+        for (int c = 0; c < NV; c += 16) {
+            float v[16], w[16];
+            ld_share<DV>(T4, c, v);
+            ld_share<DV>(TX, c, w);
+            tmem_wait_ld();
+            st_row16(Co + rowD * DV + cv + c, v);
+            st_row16(Go + rowD * DV + cv + c, w);
+        }
+        for (int i = tid; i < D; i += kThreads) {
+            P.sout.m[(size_t)bh * D + i] = mrun()[i];
+            P.sout.h[(size_t)bh * D + i] = Yrun()[i];
+        }
+    }
+
+    // Pass 2 (asymmetric): outputs from the exact prefix (P in the fourth slot, E in
+    // the X slot, m^K, n).  The S slot is the spare accumulator here.  With the
+    // normaliser: den() holds q_b . m_p, then zeta_b, then the weight of k_b in the
+    // n update; rsum() holds row partials, then den_t in its first C entries.
+    __device__ bool pass2_asym(int jb, int je) {
+        int stage = 0;
+        tma_chunk(jb, 0);
+        for (int jj = jb; jj < je; ++jj) {
+            const int t0 = jj * C;
+            const int L = min(C, P.n - t0);
+            uint8_t *Q = sQ(stage), *Kt = sK(stage), *V = sV(stage);
+            if (tid == 0) bulk_wait_read();  // the previous chunk's O store has left tS()
+            if (!wait_tma(stage)) return false;
+            if (K_::NSTAGE == 2 && jj + 1 < je) tma_chunk(jj + 1, stage ^ 1);
+            if (tid == 0) mma_kk<C, D>(TW, Q, Kt, false);  // A = Q K^T
+            commit();
+            extract_state<DV>(T4, tQ(), gp(L));  // P_p -> bf16, P decayed to the chunk end
+            publish();
+            if (tid == 0) mma_km<DV, D>(TS, Q, tQ(), false);  // spare = Q P_p
+            commit2();
+            extract_state<DV>(TX, tS(), gp(L));  // E_p -> bf16, E decayed to the chunk end
+            if constexpr (NORM) row_dot(Q, mrun(), den());  // q_b . m_p
+            if (!wait_mma()) return false;  // A
+            epi_atilde<NORM>();
+            publish();
+            if (tid == 0) mma_km<DV, C>(TW, tA(), V, false);  // A-tilde V
+            commit();
+            if constexpr (NORM) {  // zeta_b = rowsum(A-tilde)_b + g^tau q_b . m_p
+                if (tid < C) den()[tid] = sum_partials<C>(rsum(), tid) + gp(tid + 1) * den()[tid];
+            }
+            if (!wait_mma2()) return false;  // Q P_p
+            if (!wait_mma()) return false;   // A-tilde V
+            // Z = A-tilde V + g^tau Q P_p -> tU()
+            {
+                const float gt = (DECAY && rowC >= 0) ? gp(rowC + 1) : 1.f;
+                for_row2<C, DV>(TW, TS, [&](int c0, float (&v)[16], float (&sp)[16]) {
+                    if (rowC < 0) return;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] += gt * sp[i];
+                    tile_store_row16(tU(), C, rowC, c0, v);
+                });
+            }
+            if constexpr (DECAY)  // K_w = diag(g^{L-1-tau}) K -> tQ (P_p has been read)
+                scaled_tile_copy<D>(Kt, tQ(), [&](int r) { return r < L ? gp(L - 1 - r) : 0.f; });
+            publish();
+            if (tid == 0) mma_km<DV, C>(TW, tA(), tU(), false);  // O = A-tilde Z
+            commit();
+            if (tid == 0) {
+                mma_km<DV, D>(TS, Q, tS(), false);               // spare = Q E_p
+                mma_mm<DV>(T4, DECAY ? tQ() : Kt, V, true);      // P += K^T W V
+                mma_mm<DV>(TX, DECAY ? tQ() : Kt, tU(), true);   // E += K^T W Z
+            }
+            commit2();
+            if constexpr (NORM) {
+                // den_t = sum_b A-tilde[t,b] zeta_b + g^tau q_t . n_p: one partial per
+                // (row, part) over C / NPR columns of A-tilde and D / NPR of q (tA read only)
+                constexpr int NPR = kThreads / C, CA = C / NPR, CQ = D / NPR;
+                const int r = tid % C, pp = tid / C;
+                float acc = 0.f, accq = 0.f;
+#pragma unroll
+                for (int c0 = 0; c0 < CA; c0 += 8) {
+                    float a8[8];
+                    tile_load_row8(tA(), C, r, pp * CA + c0, a8);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc += a8[j] * den()[pp * CA + c0 + j];
+                }
+#pragma unroll
+                for (int c0 = 0; c0 < CQ; c0 += 8) {
+                    float q8[8];
+                    tile_load_row8(Q, C, r, pp * CQ + c0, q8);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) accq += q8[j] * Yrun()[pp * CQ + c0 + j];
+                }
+                rsum()[pp * C + r] = acc + (DECAY ? gp(r + 1) : 1.f) * accq;
+                __syncthreads();
+                if (tid < C) {
+                    float sacc = 0.f;
+#pragma unroll
+                    for (int q2 = 0; q2 < NPR; ++q2) sacc += rsum()[q2 * C + tid];
+                    rsum()[tid] = sacc;
+                    den()[tid] = tid < L ? gp(L - 1 - tid) * den()[tid] : 0.f;  // weight of k_b in n
+                }
+            }
+            if (!wait_mma()) return false;   // O = A-tilde Z
+            if (!wait_mma2()) return false;  // Q E_p, P and E updates
+            if constexpr (NORM) {  // n, m^K to the chunk end (scratch: tA, whose readers have finished)
+                tile_colsums_rw(Kt, L, den(), reinterpret_cast<float *>(tA()), Yrun(), gp(L));
+                tile_colsums<false>(Kt, nullptr, L, 1.f, reinterpret_cast<float *>(tA()), mrun(), gp(L), nullptr,
+                                    1.f);
+            }
+            if (K_::NSTAGE == 1 && jj + 1 < je) tma_chunk(jj + 1, 0);
+            {
+                const float g1t = (DECAY && rowC >= 0) ? gp(rowC + 1) : 1.f;
+                float inv = 1.f;
+                if constexpr (NORM) {
+                    if (rowC >= 0) inv = 1.f / (rsum()[rowC] + P.eps);
+                }
+                for_row2<C, DV>(TW, TS, [&](int c0, float (&v)[16], float (&sp)[16]) {
+                    if (rowC < 0) return;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = (v[i] + g1t * sp[i]) * inv;
+                    tile_store_row16(tS(), C, rowC, c0, v);
+                });
+            }
+            publish();
+            if (tid == 0) {
+#pragma unroll
+                for (int kb = 0; kb < DV / 64; ++kb) tma_store_3d(tS() + kb * C * 128, &P.tmO, kb * 64, t0, bh);
+                bulk_commit();
+            }
+            stage ^= (K_::NSTAGE - 1);
+        }
+        if (tid == 0) bulk_wait_read();
+        __syncthreads();
+        return true;
+    }
 };
 
 // The last CTA to finish returns the workspace header and flags to zero, so the
@@ -1495,7 +1932,7 @@ __device__ __forceinline__ void finish_cta(const TcParams &P) {
     }
 }
 
-template <int C, int D, int DV, bool DECAY, bool NORM, bool UNM>
+template <int C, int D, int DV, bool DECAY, bool NORM, int VAR>
 __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(const __grid_constant__ TcParams P) {
     using K_ = Cfg<C, D, DV>;
     // No static shared memory: the dynamic block starts at the (1024-byte
@@ -1507,7 +1944,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
     int *ticket_p = reinterpret_cast<int *>(base + K_::OFF_BAR + 36);
     int *misalign_p = reinterpret_cast<int *>(base + K_::OFF_BAR + 40);
 
-    Kern<C, D, DV, DECAY, NORM, UNM> x(P, base);
+    Kern<C, D, DV, DECAY, NORM, VAR> x(P, base);
     x.tid = threadIdx.x;
     x.warp = threadIdx.x >> 5;
     x.lane = threadIdx.x & 31;
@@ -1598,7 +2035,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
             const Piece pc = piece(bh);
             if (pc.last && !want_out) continue;
             select(bh);
-            if constexpr (UNM) ok = x.pass1_unm(pc.jb, pc.je);
+            if constexpr (VAR == 1) ok = x.pass1_unm(pc.jb, pc.je);
+            else if constexpr (VAR == 2) ok = x.pass1_asym(pc.jb, pc.je);
             else ok = x.pass1(pc.jb, pc.je);
             if (!ok) break;
             x.store_summary(P.summ + ((size_t)bh * P.kmax + pc.k) * K_::SUM);
@@ -1626,7 +2064,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
             if (pc.k > 0) {  // with a zero state_in the first fold step sets the prefix
                 if (!(ok = x.wait_flags(0, pc.k))) break;
                 const float *Ls = P.summ + (size_t)bh * P.kmax * K_::SUM;
-                if constexpr (UNM) ok = x.fold_unm(Ls, pc.k, start, !P.sin.S);
+                if constexpr (VAR == 1) ok = x.fold_unm(Ls, pc.k, start, !P.sin.S);
+                else if constexpr (VAR == 2) ok = x.fold_asym(Ls, pc.k, start, !P.sin.S);
                 else ok = x.fold_all(Ls, pc.k, start, !P.sin.S);
                 if (!ok) break;
             }
@@ -1634,15 +2073,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
             if (pc.last && want_out) {
                 const float *Lown = P.summ + ((size_t)bh * P.kmax + pc.k) * K_::SUM;
                 const float fown = DECAY ? gpow(x.lg, (float)(P.n - start(pc.k))) : 1.f;
-                if constexpr (UNM) x.export_pre_unm(Lown, fown);
+                if constexpr (VAR == 1) x.export_pre_unm(Lown, fown);
+                else if constexpr (VAR == 2) x.export_pre_asym(Lown, fown);
                 else x.export_pre(Lown, fown);
             }
-            if constexpr (UNM) ok = x.pass2_unm(pc.jb, pc.je);
+            if constexpr (VAR == 1) ok = x.pass2_unm(pc.jb, pc.je);
+            else if constexpr (VAR == 2) ok = x.pass2_asym(pc.jb, pc.je);
             else ok = x.pass2(pc.jb, pc.je);
             if (!ok) break;
             // ---- state export, part 2: the final state at the sequence end
             if (pc.last && want_out) {
-                if constexpr (UNM) x.export_post_unm();
+                if constexpr (VAR == 1) x.export_post_unm();
+                else if constexpr (VAR == 2) x.export_post_asym();
                 else ok = x.export_post();
                 if (!ok) break;
             }
@@ -1722,7 +2164,7 @@ inline WsLayout ws_layout(const hla_params &p, const Plan &pl) {
     return w;
 }
 
-template <int C, int D, int DV, bool DECAY, bool NORM, bool UNM>
+template <int C, int D, int DV, bool DECAY, bool NORM, int VAR>
 cudaError_t launch_cfg(const FwdArgs &a, cudaStream_t st, int num_sms) {
     using K_ = Cfg<C, D, DV>;
     hla_params p{a.B, a.H, a.n, a.d, a.dv, a.chunk, a.in_dtype, a.flags, a.eps, a.gamma};
@@ -1744,7 +2186,7 @@ cudaError_t launch_cfg(const FwdArgs &a, cudaStream_t st, int num_sms) {
     P.flagsw = reinterpret_cast<unsigned *>(ws + wl.off_flags);
     P.summ = reinterpret_cast<float *>(ws + wl.off_summ);
     P.err = a.err;
-    auto kern = fwd_tc_kernel<C, D, DV, DECAY, NORM, UNM>;
+    auto kern = fwd_tc_kernel<C, D, DV, DECAY, NORM, VAR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K_::SMEM_LAUNCH);
     if (e != cudaSuccess) return e;
     kern<<<pl.ncta, kThreads, K_::SMEM_LAUNCH, st>>>(P);
@@ -1753,18 +2195,20 @@ cudaError_t launch_cfg(const FwdArgs &a, cudaStream_t st, int num_sms) {
 
 // Launcher for one (decay, normalise) combination over all supported shapes;
 // explicitly instantiated in hla_fwd_tc_f<flags>.cu.
-template <bool DECAY, bool NORM, bool UNM>
+template <bool DECAY, bool NORM, int VAR>
 cudaError_t launch_flags(const FwdArgs &a, cudaStream_t st, int ns) {
     const int key = (a.chunk == 128 ? 4 : 0) | (a.d == 128 ? 2 : 0) | (a.dv == 128 ? 1 : 0);
     switch (key) {
-        case 0: return launch_cfg<64, 64, 64, DECAY, NORM, UNM>(a, st, ns);
-        case 1: return launch_cfg<64, 64, 128, DECAY, NORM, UNM>(a, st, ns);
-        case 2: return launch_cfg<64, 128, 64, DECAY, NORM, UNM>(a, st, ns);
-        case 3: return launch_cfg<64, 128, 128, DECAY, NORM, UNM>(a, st, ns);
-        case 4: return launch_cfg<128, 64, 64, DECAY, NORM, UNM>(a, st, ns);
-        case 5: return launch_cfg<128, 64, 128, DECAY, NORM, UNM>(a, st, ns);
-        case 6: return launch_cfg<128, 128, 64, DECAY, NORM, UNM>(a, st, ns);
-        default: return launch_cfg<128, 128, 128, DECAY, NORM, UNM>(a, st, ns);
+        case 0: return launch_cfg<64, 64, 64, DECAY, NORM, VAR>(a, st, ns);
+        case 2: return launch_cfg<64, 128, 64, DECAY, NORM, VAR>(a, st, ns);
+        case 3: return launch_cfg<64, 128, 128, DECAY, NORM, VAR>(a, st, ns);
+        case 4: return launch_cfg<128, 64, 64, DECAY, NORM, VAR>(a, st, ns);
+        case 6: return launch_cfg<128, 128, 64, DECAY, NORM, VAR>(a, st, ns);
+        case 7: return launch_cfg<128, 128, 128, DECAY, NORM, VAR>(a, st, ns);
+        default:  // dv > d: not for the asymmetric variant, whose spare accumulator is d wide
+            if constexpr (VAR == 2) return cudaErrorInvalidValue;
+            else return key == 1 ? launch_cfg<64, 64, 128, DECAY, NORM, VAR>(a, st, ns)
+                                 : launch_cfg<128, 64, 128, DECAY, NORM, VAR>(a, st, ns);
     }
 }
 

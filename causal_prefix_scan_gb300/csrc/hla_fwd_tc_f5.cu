@@ -1,4 +1,4 @@
-// Tensor-core forward kernels with decay=true, normalise=false, unmasked output (all supported shapes).
+// Tensor-core forward kernels with decay=false, normalise=true, asymmetric (AHLA) output (all supported shapes).
 #include "hla_fwd_tc.cuh"
 
-template cudaError_t hla::tc::launch_flags<true, false, true>(const hla::FwdArgs &, cudaStream_t, int);
+template cudaError_t hla::tc::launch_flags<false, true, 2>(const hla::FwdArgs &, cudaStream_t, int);

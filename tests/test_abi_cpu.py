@@ -63,7 +63,7 @@ def _call(p, q=16, k=16, v=16, o=16, sin=None, sout=None, ws=None, ws_bytes=0):
     (dict(in_dtype=7), hla.HLA_ERR_ARG),
     (dict(flags=16), hla.HLA_ERR_ARG),
     (dict(flags=hla.HLA_UNMASKED | hla.HLA_ASYMMETRIC), hla.HLA_ERR_ARG),
-    (dict(flags=hla.HLA_ASYMMETRIC, d=128, dv=128), hla.HLA_ERR_UNSUPPORTED),  # not on the CUDA-core path
+    (dict(flags=hla.HLA_ASYMMETRIC, d=64, dv=128), hla.HLA_ERR_UNSUPPORTED),  # needs dv <= d on tensor cores
     (dict(H=6, Hkv=4), hla.HLA_ERR_ARG),                    # key/value heads must divide H
     (dict(Hkv=-1), hla.HLA_ERR_ARG),
     (dict(flags=hla.HLA_DECAY), hla.HLA_ERR_ARG),          # decay without gamma

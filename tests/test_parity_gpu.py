@@ -214,6 +214,39 @@ def test_asym_forward(d, dv, chunk, n, decay, normalize):
                       what=f"asym {dtype} d{d} dv{dv}", asymmetric=True)
 
 
+TC_SHAPES_ASYM = [sh for sh in TC_SHAPES if sh[2] <= sh[1]]  # (chunk, d, dv) with dv <= d
+
+
+@pytest.mark.parametrize("chunk,d,dv", TC_SHAPES_ASYM)
+@pytest.mark.parametrize("decay,normalize", [(False, False), (False, True), (True, False), (True, True)])
+def test_tc_asym_variants(chunk, d, dv, decay, normalize):
+    n = 5 * chunk + 17
+    w = small("asym_tc", d=d, dv=dv, chunk=chunk, n=n, decay=decay, qk="elu1" if normalize else "l2",
+              gamma_lo=0.9, gamma_hi=0.999, seed=29)
+    x = W.make_inputs(w)
+    o, st = run_forward(x, "bf16", chunk, normalize=normalize, eps=1e-6, asymmetric=True)
+    o_ref, st_ref = run_oracle(x, normalize=normalize, eps=1e-6, asymmetric=True)
+    assert_parity(o, o_ref, st, st_ref, what=f"asym tc c{chunk} d{d} dv{dv} decay={decay} norm={normalize}",
+                  asymmetric=True)
+
+
+@pytest.mark.parametrize("B,H,Hkv,n,chunk,d,dv", [(1, 3, 3, 8192, 64, 64, 64), (1, 400, 400, 40, 64, 64, 64),
+                                                  (1, 8, 2, 4990, 128, 128, 128)])
+def test_tc_asym_runs_resume_shared_kv(B, H, Hkv, n, chunk, d, dv):
+    w = small("asym_runs", B=B, H=H, Hkv=Hkv, n=n, chunk=chunk, d=d, dv=dv, decay=True, qk="elu1", seed=30)
+    x = W.make_inputs(w)
+    o, st = run_forward(x, "bf16", chunk, normalize=True, eps=1e-6, asymmetric=True)
+    o_ref, st_ref = run_oracle(x, normalize=True, eps=1e-6, asymmetric=True)
+    assert_parity(o, o_ref, st, st_ref, what=f"asym runs B{B}H{H}n{n}", asymmetric=True)
+    n1 = n // 3 + 5
+    x1 = {kk: (vv[:, :, :n1] if kk != "gamma" else vv) for kk, vv in x.items()}
+    x2 = {kk: (vv[:, :, n1:] if kk != "gamma" else vv) for kk, vv in x.items()}
+    _, st1 = run_oracle(x1, normalize=True, eps=1e-6, asymmetric=True)
+    o2, st2 = run_forward(x2, "bf16", chunk, normalize=True, eps=1e-6, state_in=st1, asymmetric=True)
+    o2_ref, st2_ref = run_oracle(x2, normalize=True, eps=1e-6, state_in=st1, asymmetric=True)
+    assert_parity(o2, o2_ref, st2, st2_ref, what="asym resume", asymmetric=True)
+
+
 def test_asym_resume_and_shared_kv():
     w = small("asym_kv", B=2, H=4, Hkv=2, n=300, d=64, dv=64, chunk=64, dtype="f32", decay=True, qk="elu1",
               seed=28)
