@@ -37,7 +37,11 @@ METRIC = "masked 2nd-order HLA forward tokens/s and % roofline on 1 GB300"
 
 
 def metric_for(w) -> str:
-    return METRIC.replace("masked", "unmasked", 1) if getattr(w, "unmasked", False) else METRIC
+    if getattr(w, "unmasked", False):
+        return METRIC.replace("masked", "unmasked", 1)
+    if getattr(w, "asymmetric", False):
+        return METRIC.replace("masked 2nd-order HLA", "masked asymmetric 2nd-order HLA (AHLA)", 1)
+    return METRIC
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 FWD_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd_tc.cuh")
@@ -51,6 +55,8 @@ def alg_flops_per_token_head(w: W.Workload) -> float:
     c, d, dv = w.chunk, w.d, w.dv
     if w.unmasked:
         return c * (3 * d + dv) + 4 * d * d + 4 * d * dv
+    if w.asymmetric:  # A, A-tilde V, A-tilde Z at half; Q P_p, Q E_p, P, E updates; R update
+        return c * (d + 2 * dv) + 8 * d * dv + 2 * d * d
     return c * (3 * d + dv) + 4 * d * d + 6 * d * dv + 2 * d * d * dv / c
 
 
@@ -200,7 +206,7 @@ def oracle_rate(w: W.Workload, x, batch_rows: int, n_tokens: int, nthreads: int)
     oracle.build()
     t0 = time.perf_counter()
     oracle.forward(q, k, v, gamma=g, normalize=w.normalize, eps=w.eps, want_state=True, nthreads=nthreads,
-                   unmasked=w.unmasked)
+                   unmasked=w.unmasked, asymmetric=w.asymmetric)
     return time.perf_counter() - t0, batch_rows * n_tokens
 
 
@@ -243,7 +249,7 @@ def workload_by_name(name: str):
 
 def config_dict(w: W.Workload, nsets: int, set_bytes: int, world: int):
     variant = "normalised" if w.normalize else ("decay" if w.decay else "unnormalised")
-    variant = ("unmasked " if w.unmasked else "masked ") + variant
+    variant = ("unmasked " if w.unmasked else ("asymmetric " if w.asymmetric else "masked ")) + variant
     return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.kv_heads, "n": w.n, "d": w.d, "dv": w.dv,
             "chunk": w.chunk,
             "variant": variant, "inputs": f"q,k {w.qk}, v N(0,1), seed {w.seed}",
@@ -270,7 +276,7 @@ def bench_forward(args, w: W.Workload, rank, world, local, dist):
         q, k, v = (host[n].to(dev, non_blocking=True) for n in ("q", "k", "v"))
         o = torch.empty(q.shape[:3] + (w.dv,), dtype=tdt, device=dev)
         sets.append((q, k, v, o))
-    params = hla.make_params(sets[0][0], sets[0][2], w.chunk, gamma, w.normalize, w.eps, w.unmasked)
+    params = hla.make_params(sets[0][0], sets[0][2], w.chunk, gamma, w.normalize, w.eps, w.unmasked, w.asymmetric)
     ws_bytes = hla.hla_forward_workspace_size(params)
     ws = hla.new_workspace(ws_bytes, dev)
     st = hla.State.empty(w.B * w.H, w.d, w.dv, device=dev)
@@ -532,7 +538,7 @@ def bench_reference(args, w, rank, world):
     def one(i):
         t0 = offs[i % len(offs)]
         oracle.forward(sl(x["q"], t0), sl(x["k"], t0), sl(x["v"], t0), gamma=g, normalize=w.normalize,
-                       eps=w.eps, nthreads=cores, unmasked=w.unmasked)
+                       eps=w.eps, nthreads=cores, unmasked=w.unmasked, asymmetric=w.asymmetric)
 
     for i in range(args.warmup):
         one(i)

@@ -38,6 +38,7 @@ class Workload:
     seed: int = 0
     note: str = field(default="", compare=False)
     unmasked: bool = False    # unmasked variant o = q^T S C
+    asymmetric: bool = False  # asymmetric variant AHLA, o = q^T E
     Hkv: int = 0              # key/value heads (0: H); query head h reads head h // (H // Hkv)
 
     @property
@@ -65,12 +66,14 @@ FWD_NORM = Workload("fwd_bf16_norm_B2H16n8192d64dv128", 2, 16, 8192, 64, 128, 64
                     normalize=True, eps=1e-6, seed=3)
 FWD_DECAY = Workload("fwd_bf16_decay_B1H32n32768d128", 1, 32, 32768, 128, 128, 128, "bf16", "l2",
                      decay=True, seed=4)
-# Widening beyond the masked forward: the unmasked variant, and keys/values shared
-# by groups of query heads, on the shape of the B4H8n2048d64 workload.
+# Widening beyond the masked forward: the unmasked variant, keys/values shared by
+# groups of query heads, and the asymmetric variant, on the shape of the
+# B4H8n2048d64 workload.
 FWD_UNMASKED = Workload("fwd_bf16_unmasked_B4H8n2048d64", 4, 8, 2048, 64, 64, 64, "bf16", "l2", seed=6,
                         unmasked=True)
 FWD_SHARED_KV = Workload("fwd_bf16_kv2_B4H8n2048d64", 4, 8, 2048, 64, 64, 64, "bf16", "l2", seed=7, Hkv=2)
-WORKLOADS = {w.name: w for w in (SMALL_F32, FWD_BF16, FWD_NORM, FWD_DECAY, FWD_UNMASKED, FWD_SHARED_KV)}
+FWD_ASYM = Workload("fwd_bf16_asym_B4H8n2048d64", 4, 8, 2048, 64, 64, 64, "bf16", "l2", seed=8, asymmetric=True)
+WORKLOADS = {w.name: w for w in (SMALL_F32, FWD_BF16, FWD_NORM, FWD_DECAY, FWD_UNMASKED, FWD_SHARED_KV, FWD_ASYM)}
 
 
 @dataclass(frozen=True)

@@ -396,11 +396,12 @@ def test_state_combine_variants(variant):
 
 
 # ---------------------------------------------------- full-size workloads
-@pytest.mark.parametrize("w", [W.FWD_BF16, W.FWD_NORM, W.FWD_DECAY, W.FWD_UNMASKED, W.FWD_SHARED_KV],
+@pytest.mark.parametrize("w", [W.FWD_BF16, W.FWD_NORM, W.FWD_DECAY, W.FWD_UNMASKED, W.FWD_SHARED_KV, W.FWD_ASYM],
                          ids=lambda w: w.name)
 def test_full_workload(w):
     x = W.make_inputs(w)
-    o, st = run_forward(x, w.dtype, w.chunk, normalize=w.normalize, eps=w.eps, unmasked=w.unmasked)
-    o_ref, st_ref = run_oracle(x, normalize=w.normalize, eps=w.eps, unmasked=w.unmasked)
-    err = assert_parity(o, o_ref, st, st_ref, what=w.name)
+    kw = dict(normalize=w.normalize, eps=w.eps, unmasked=w.unmasked, asymmetric=w.asymmetric)
+    o, st = run_forward(x, w.dtype, w.chunk, **kw)
+    o_ref, st_ref = run_oracle(x, **kw)
+    err = assert_parity(o, o_ref, st, st_ref, what=w.name, asymmetric=w.asymmetric)
     print(f"{w.name}: max per-(b,h) rel L2 {err:.3e}")
