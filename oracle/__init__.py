@@ -25,7 +25,9 @@ asymmetric variant AHLA (section 2, o_t = sum_{a<=b<=t} (q_t.k_b)(q_b.k_a) v_a) 
 by its brute-force triple sum, the dense form (L o A)(L o A)V, brute-force definitions of
 its five summaries, a closed form for constant inputs, chunk invariance, associativity
 of its concatenation rule, concatenation equal to the joined sequence, resume and
-decode continuation.
+decode continuation.  The backward pass (reverse mode of the masked recurrence; the
+pages give no gradient formulas) is pinned by central finite differences of the
+forward and by the gradient of the dense masked-matrix form.
 """
 from __future__ import annotations
 
@@ -66,8 +68,9 @@ def _load():
         _lib.hla_oracle_forward_chunked.argtypes = [i] * 8 + [dp, dp, dp, dp, i, d] + [dp] * 5 + [dp] + [dp] * 5 + [i]
         _lib.hla_oracle_decode_step.argtypes = [i] * 6 + [dp, i, d] + [dp] * 5 + [dp, dp, dp, dp, i]
         _lib.hla_oracle_combine.argtypes = [i, i, i, i] + [dp] * 10 + [dp] + [dp] * 5
+        _lib.hla_oracle_backward.argtypes = [i] * 5 + [dp] * 8 + [i]
         for f in (_lib.hla_oracle_forward, _lib.hla_oracle_forward_chunked,
-                  _lib.hla_oracle_decode_step, _lib.hla_oracle_combine):
+                  _lib.hla_oracle_decode_step, _lib.hla_oracle_combine, _lib.hla_oracle_backward):
             f.restype = ctypes.c_int
     return _lib
 
@@ -204,3 +207,20 @@ def combine(A: State, Bst: State, decay_pow=None, asymmetric=False) -> State:
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return out
+
+
+def backward(q, k, v, go, gamma=None, nthreads=None):
+    """Gradients (dq, dk, dv) of sum_t go_t . o_t for the masked forward from a zero
+    state, without normalisation (reverse mode of the recurrence in hla_oracle.c).
+    q, k: [B,H,n,d]; v, go: [B,H,n,dv]; gamma: [H] or None."""
+    q, k, v, go = _f64(q), _f64(k), _f64(v), _f64(go)
+    B, H, n, d = q.shape
+    dv = v.shape[-1]
+    assert k.shape == q.shape and v.shape == (B, H, n, dv) and go.shape == v.shape
+    g = _f64(gamma)
+    dq, dk, dvv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    rc = _load().hla_oracle_backward(B, H, n, d, dv, _p(q), _p(k), _p(v), _p(g), _p(go), _p(dq), _p(dk),
+                                     _p(dvv), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return dq, dk, dvv

@@ -523,6 +523,128 @@ int hla_oracle_decode_step(int N, int H, int Hkv, int d, int dv, int variant,
     return run_job(&J, nthreads);
 }
 
+/* ------------------------------------------------------------------------- */
+/* backward pass of the masked forward (zero initial state, no normalisation) */
+/*
+ * Forward, in the form X = S C - G (gist.science summary, section 1, expanded):
+ *   S_t = g S_{t-1} + k_t k_t^T,  u_t = S_t q_t,  X_t = g^2 X_{t-1} + u_t v_t^T,
+ *   o_t = X_t^T q_t.
+ * Reverse mode with upstream gradients go_t = dL/do_t, accumulators
+ * Lam_t = dL/dX_t = q_t go_t^T + g^2 Lam_{t+1} and Om_t = dL/dS_t = du_t q_t^T + g Om_{t+1}:
+ *   du_t = Lam_t v_t,  dv_t = Lam_t^T u_t,  dq_t = X_t go_t + S_t du_t,
+ *   dk_t = (Om_t + Om_t^T) k_t.
+ * The pages give no gradient formulas; this is the chain rule applied to the
+ * recurrence above, token by token, from the last token to the first.
+ */
+static void backward_unit(int n, int d, int dv, double g, const double *q, const double *k,
+                          const double *v, const double *go, double *dq, double *dk, double *dvo)
+{
+    double *S = (double *)calloc((size_t)(n + 1) * d * d, sizeof(double));  /* S_t after token t */
+    double *X = (double *)calloc((size_t)(n + 1) * d * dv, sizeof(double)); /* X_t after token t */
+    double *U = (double *)calloc((size_t)n * d, sizeof(double));            /* u_t */
+    double *Lam = (double *)calloc((size_t)d * dv, sizeof(double));
+    double *Om = (double *)calloc((size_t)d * d, sizeof(double));
+    double *du = (double *)calloc((size_t)d, sizeof(double));
+    for (int t = 0; t < n; ++t) { /* forward, keeping every state */
+        const double *qt = q + (size_t)t * d, *kt = k + (size_t)t * d, *vt = v + (size_t)t * dv;
+        const double *Sp = S + (size_t)t * d * d, *Xp = X + (size_t)t * d * dv;
+        double *St = S + (size_t)(t + 1) * d * d, *Xt = X + (size_t)(t + 1) * d * dv, *ut = U + (size_t)t * d;
+        for (int i = 0; i < d; ++i)
+            for (int j = 0; j < d; ++j) St[i * d + j] = g * Sp[i * d + j] + kt[i] * kt[j];
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < d; ++j) acc += St[i * d + j] * qt[j];
+            ut[i] = acc;
+        }
+        for (int i = 0; i < d; ++i)
+            for (int j = 0; j < dv; ++j) Xt[i * dv + j] = g * g * Xp[i * dv + j] + ut[i] * vt[j];
+    }
+    for (int t = n - 1; t >= 0; --t) { /* reverse */
+        const double *qt = q + (size_t)t * d, *kt = k + (size_t)t * d, *vt = v + (size_t)t * dv;
+        const double *gt = go + (size_t)t * dv, *ut = U + (size_t)t * d;
+        const double *St = S + (size_t)(t + 1) * d * d, *Xt = X + (size_t)(t + 1) * d * dv;
+        /* Lam_t = q_t go_t^T + g^2 Lam_{t+1} */
+        for (int i = 0; i < d; ++i)
+            for (int j = 0; j < dv; ++j) Lam[i * dv + j] = g * g * Lam[i * dv + j] + qt[i] * gt[j];
+        /* du_t = Lam_t v_t;  dv_t = Lam_t^T u_t */
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) acc += Lam[i * dv + j] * vt[j];
+            du[i] = acc;
+        }
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i) acc += Lam[i * dv + j] * ut[i];
+            dvo[(size_t)t * dv + j] = acc;
+        }
+        /* dq_t = X_t go_t + S_t du_t */
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) acc += Xt[i * dv + j] * gt[j];
+            for (int j = 0; j < d; ++j) acc += St[i * d + j] * du[j];
+            dq[(size_t)t * d + i] = acc;
+        }
+        /* Om_t = du_t q_t^T + g Om_{t+1};  dk_t = (Om_t + Om_t^T) k_t */
+        for (int i = 0; i < d; ++i)
+            for (int j = 0; j < d; ++j) Om[i * d + j] = g * Om[i * d + j] + du[i] * qt[j];
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < d; ++j) acc += (Om[i * d + j] + Om[j * d + i]) * kt[j];
+            dk[(size_t)t * d + i] = acc;
+        }
+    }
+    free(S); free(X); free(U); free(Lam); free(Om); free(du);
+}
+
+typedef struct {
+    int B, H, n, d, dv, next;
+    const double *q, *k, *v, *go, *gamma;
+    double *dq, *dk, *dv_out;
+    pthread_mutex_t lock;
+} bjob_t;
+
+static void *bworker(void *arg)
+{
+    bjob_t *J = (bjob_t *)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        const int u = J->next < J->B * J->H ? J->next++ : -1;
+        pthread_mutex_unlock(&J->lock);
+        if (u < 0) break;
+        const size_t qo = (size_t)u * J->n * J->d, vo = (size_t)u * J->n * J->dv;
+        backward_unit(J->n, J->d, J->dv, J->gamma ? J->gamma[u % J->H] : 1.0, J->q + qo, J->k + qo, J->v + vo,
+                      J->go + vo, J->dq + qo, J->dk + qo, J->dv_out + vo);
+    }
+    return NULL;
+}
+
+/* Gradients of sum_t go_t . o_t with respect to q, k, v for the masked forward
+ * from a zero state, without normalisation.  Layout as the forward (Hkv = H). */
+int hla_oracle_backward(int B, int H, int n, int d, int dv, const double *q, const double *k,
+                        const double *v, const double *gamma, const double *go, double *dq, double *dk,
+                        double *dvo, int nthreads)
+{
+    if (check_dims(B, H, n, d, dv)) return -1;
+    bjob_t J;
+    memset(&J, 0, sizeof J);
+    J.B = B; J.H = H; J.n = n; J.d = d; J.dv = dv;
+    J.q = q; J.k = k; J.v = v; J.go = go; J.gamma = gamma;
+    J.dq = dq; J.dk = dk; J.dv_out = dvo;
+    pthread_mutex_init(&J.lock, NULL);
+    const int total = B * H;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > total) nthreads = total > 0 ? total : 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * nthreads);
+    int started = 0;
+    for (int i = 1; i < nthreads; ++i)
+        if (pthread_create(&th[started], NULL, bworker, &J) == 0) ++started;
+    bworker(&J);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&J.lock);
+    return 0;
+}
+
 /* Segment concatenation for `count` independent items: out_i = A_i (+) B_i
  * with f_i = decay_pow[i] (NULL: f = 1), by the rule of `variant` (0 masked,
  * 2 asymmetric; the unmasked state uses the masked rule's S, C, m).  out may

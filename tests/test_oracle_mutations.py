@@ -120,3 +120,41 @@ def test_variant_pins_reject_planted_mistake(tmp_path, name):
         kr, vr = np.repeat(k, H // Hkv, axis=1), np.repeat(v, H // Hkv, axis=1)
         ref = np.stack([brute_force(q[0, h], kr[0, h], vr[0, h]) for h in range(H)])
         assert rel(o[0], ref) > 1e-6, f"mutation {name} not caught"
+
+
+def test_backward_pin_rejects_planted_mistake(tmp_path):
+    # dk from Om + Om (dropping the transpose) must fail the finite-difference pin
+    text = open(SRC).read()
+    old = "acc += (Om[i * d + j] + Om[j * d + i]) * kt[j];"
+    assert text.count(old) == 1
+    src = tmp_path / "mut_bwd.c"
+    src.write_text(text.replace(old, "acc += (Om[i * d + j] + Om[i * d + j]) * kt[j];"))
+    lib = tmp_path / "libmut_bwd.so"
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", str(lib), str(src), "-lm"])
+    L = ctypes.CDLL(str(lib))
+    dp = ctypes.POINTER(ctypes.c_double)
+    L.hla_oracle_backward.argtypes = [ctypes.c_int] * 5 + [dp] * 8 + [ctypes.c_int]
+    L.hla_oracle_forward.argtypes = [ctypes.c_int] * 7 + [dp, dp, dp, dp, ctypes.c_int, ctypes.c_double] + \
+        [dp] * 5 + [dp] + [dp] * 5 + [ctypes.c_int]
+    P = lambda a: a.ctypes.data_as(dp)
+    rng = np.random.default_rng(3)
+    n, d, dv = 5, 3, 2
+    q, k, v = rand_inputs(rng, 1, 1, n, d, dv)
+    go = rng.standard_normal((1, 1, n, dv))
+    dq, dk, dvv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    assert L.hla_oracle_backward(1, 1, n, d, dv, P(q), P(k), P(v), None, P(go), P(dq), P(dk), P(dvv), 1) == 0
+    none = [None] * 5
+
+    def loss(kk):
+        o = np.zeros((1, 1, n, dv))
+        assert L.hla_oracle_forward(1, 1, 1, n, d, dv, 0, P(q), P(kk), P(v), None, 0, 0.0, *none, P(o), *none,
+                                    1) == 0
+        return float(np.sum(go * o))
+
+    num = np.zeros_like(k)
+    for idx in np.ndindex(*k.shape):
+        kp, km = k.copy(), k.copy()
+        kp[idx] += 1e-6
+        km[idx] -= 1e-6
+        num[idx] = (loss(kp) - loss(km)) / 2e-6
+    assert rel(dk, num) > 1e-4, "mutation in the backward not caught by the finite-difference pin"

@@ -534,3 +534,49 @@ def test_asym_chunked_combine_resume_decode(decay):
         od = oracle.decode_step(st, q[:, :, t].reshape(B * H, d), k[:, :, t].reshape(B * H, d),
                                 v[:, :, t].reshape(B * H, dv), H, **kw)
         assert rel(od.reshape(B, H, dv), o[:, :, t]) < 1e-12
+
+
+# ------------------------------------------------------------------ backward
+# The pages give no gradient formulas.  The oracle's reverse-mode recurrence is
+# pinned by central finite differences of the forward oracle and by the gradient
+# of the dense masked-matrix form O = [L o (Q U^T)] V, U = (L o QK^T) K.
+@pytest.mark.parametrize("decay", [False, True])
+def test_backward_finite_differences(decay):
+    rng = np.random.default_rng(61)
+    B, H, n, d, dv = 1, 2, 6, 3, 2
+    q, k, v = rand_inputs(rng, B, H, n, d, dv)
+    go = rng.standard_normal((B, H, n, dv))
+    gamma = np.array([0.8, 0.6]) if decay else None
+    dq, dk, dvv = oracle.backward(q, k, v, go, gamma)
+    loss = lambda q_, k_, v_: float(np.sum(go * oracle.forward(q_, k_, v_, gamma=gamma, want_state=False)[0]))
+    eps = 1e-6
+    for x, grad, which in ((q, dq, 0), (k, dk, 1), (v, dvv, 2)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = [q, k, v]; args_m = [q, k, v]
+            args_p[which] = xp; args_m[which] = xm
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        assert rel(grad, num) < 1e-7, which
+
+
+def test_backward_dense_form():
+    rng = np.random.default_rng(62)
+    n, d, dv = 11, 4, 3
+    q, k, v = rand_inputs(rng, 1, 1, n, d, dv)
+    go = rng.standard_normal((1, 1, n, dv))
+    dq, dk, dvv = oracle.backward(q, k, v, go)
+    Q, K, V, G = q[0, 0], k[0, 0], v[0, 0], go[0, 0]
+    L = np.tril(np.ones((n, n)))
+    At = L * (Q @ K.T)            # A-tilde
+    U = At @ K
+    M = L * (Q @ U.T)
+    dV = M.T @ G
+    dM = L * (G @ V.T)
+    dU = dM.T @ Q
+    dAt = L * (dU @ K.T)
+    dQ = dM @ U + dAt @ K
+    dK = At.T @ dU + dAt.T @ Q
+    assert rel(dq[0, 0], dQ) < 1e-12 and rel(dk[0, 0], dK) < 1e-12 and rel(dvv[0, 0], dV) < 1e-12
