@@ -1,5 +1,5 @@
 """GB300-native second-order Higher-order Linear Attention (HLA): masked, unmasked and
-the asymmetric variant AHLA.
+the asymmetric variant AHLA, and the backward pass of the masked forward.
 
 Thin ctypes binding over the C ABI in ``include/hla.h`` (library
 ``_lib/libhla_gb300.so``, built for sm_103a by ``_build.build()``).  Functions named
@@ -28,12 +28,14 @@ __all__ = [
     "HlaError", "hla_params", "hla_state", "library", "EXPORTS",
     "hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combine", "hla_decode_step",
     "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
-    "State", "new_workspace", "forward", "state_combine", "decode_step",
+    "hla_backward_workspace_size", "hla_backward_chunked",
+    "State", "new_workspace", "forward", "state_combine", "decode_step", "backward",
 ]
 
 # Every symbol include/hla.h declares.
 EXPORTS = ("hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combine", "hla_decode_step",
-           "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc")
+           "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
+           "hla_backward_workspace_size", "hla_backward_chunked")
 
 
 class HlaError(RuntimeError):
@@ -75,8 +77,12 @@ def library(path: str | None = None):
     lib.hla_forward_chunked_noalloc.restype = ctypes.c_int
     lib.hla_state_combine.argtypes = [i, i, i, u, S, S, S, vp, vp]
     lib.hla_decode_step.argtypes = [i, i, i, i, i, i, u, f, vp, S, vp, vp, vp, vp, vp]
+    lib.hla_backward_workspace_size.argtypes = [P]
+    lib.hla_backward_workspace_size.restype = sz
+    lib.hla_backward_chunked.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.hla_sync_status.argtypes = [vp]
-    for fn in (lib.hla_forward_chunked, lib.hla_state_combine, lib.hla_decode_step, lib.hla_sync_status):
+    for fn in (lib.hla_forward_chunked, lib.hla_state_combine, lib.hla_decode_step, lib.hla_sync_status,
+               lib.hla_backward_chunked):
         fn.restype = ctypes.c_int
     lib.hla_status_string.argtypes = [ctypes.c_int]
     lib.hla_status_string.restype = ctypes.c_char_p
@@ -155,6 +161,16 @@ def hla_decode_step(N: int, H: int, Hkv: int, d: int, dv: int, dtype: int, flags
                     state, q, k, v, o, stream=None) -> None:
     _check(library().hla_decode_step(N, H, Hkv, d, dv, dtype, flags, eps, _ptr(gamma), _state_struct(state),
                                      _ptr(q), _ptr(k), _ptr(v), _ptr(o), _stream(stream)))
+
+
+def hla_backward_workspace_size(params: hla_params) -> int:
+    return library().hla_backward_workspace_size(ctypes.byref(params))
+
+
+def hla_backward_chunked(params: hla_params, q, k, v, dout, dq, dk, dv, workspace, workspace_bytes: int,
+                         stream=None) -> None:
+    _check(library().hla_backward_chunked(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq),
+                                          _ptr(dk), _ptr(dv), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def hla_sync_status(stream=None) -> None:
@@ -256,3 +272,18 @@ def decode_step(state: State, q, k, v, H: int, gamma=None, normalize: bool = Fal
         _variant_flags(unmasked, asymmetric)
     hla_decode_step(N, H, Hkv, d, dv, _dtype_code(q), flags, float(eps), gamma, state, q, k, v, o, stream)
     return o
+
+
+def backward(q, k, v, dout, chunk: int, gamma=None, workspace=None, out=None, stream=None):
+    """Gradients (dq, dk, dv) of sum(dout * o) for the masked forward o of q, k, v from a
+    zero state, without normalisation.  q, k [B,H,n,d]; v, dout [B,H,n,dv] contiguous CUDA
+    tensors of one dtype (bf16 or fp32); gamma [H] fp32 or None.  ``out`` may hold three
+    preallocated result tensors."""
+    import torch
+    p = make_params(q, v, chunk, gamma)
+    need = hla_backward_workspace_size(p)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = out if out is not None else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    hla_backward_chunked(p, q, k, v, dout, dq, dk, dv, workspace, need if workspace is not None else 0, stream)
+    return dq, dk, dv

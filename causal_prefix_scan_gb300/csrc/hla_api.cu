@@ -165,6 +165,58 @@ hla_status hla_forward_chunked(const hla_params *p, const void *q, const void *k
     return HLA_OK;
 }
 
+namespace {
+hla_status check_bwd_params(const hla_params *p) {
+    if (!p) return fail(HLA_ERR_ARG, "params is NULL");
+    if (p->B < 1 || p->H < 1 || p->n < 0) return fail(HLA_ERR_ARG, "need B >= 1, H >= 1, n >= 0");
+    if (p->in_dtype != HLA_F32 && p->in_dtype != HLA_BF16) return fail(HLA_ERR_ARG, "unknown in_dtype");
+    if (p->flags & ~(unsigned)(HLA_NORMALIZE | HLA_DECAY | HLA_UNMASKED | HLA_ASYMMETRIC))
+        return fail(HLA_ERR_ARG, "unknown flag bits");
+    if ((p->flags & HLA_DECAY) && !p->gamma) return fail(HLA_ERR_ARG, "HLA_DECAY needs gamma");
+    if (p->Hkv < 0 || (p->Hkv > 0 && p->H % p->Hkv != 0))
+        return fail(HLA_ERR_ARG, "Hkv must divide H (0 means Hkv = H)");
+    if ((long long)p->B * p->H * (long long)p->n * (p->d > p->dv ? p->d : p->dv) > (1LL << 40))
+        return fail(HLA_ERR_ARG, "problem too large");
+    if (!hla::bwd_simt_supported(*p))
+        return fail(HLA_ERR_UNSUPPORTED,
+                    "backward supports flags 0 or HLA_DECAY, Hkv = H, d, dv, chunk in {16,32,64} "
+                    "(got flags=%u Hkv=%d d=%d dv=%d chunk=%d)",
+                    p->flags, p->Hkv, p->d, p->dv, p->chunk);
+    return HLA_OK;
+}
+}  // namespace
+
+size_t hla_backward_workspace_size(const hla_params *p) {
+    if (check_bwd_params(p) != HLA_OK) return 0;
+    return hla::bwd_simt_workspace(*p);
+}
+
+hla_status hla_backward_chunked(const hla_params *p, const void *q, const void *k, const void *v, const void *dout,
+                                void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    hla_status s = check_bwd_params(p);
+    if (s != HLA_OK) return s;
+    if (p->n == 0) return HLA_OK;
+    if (!q || !k || !v || !dout || !dq || !dk || !dv)
+        return fail(HLA_ERR_ARG, "q, k, v, dout, dq, dk, dv must be set when n > 0");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv))
+        return fail(HLA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    const size_t need = hla::bwd_simt_workspace(*p);
+    if (!workspace || workspace_bytes < need)
+        return fail(HLA_ERR_ARG, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
+    if (!aligned16(workspace)) return fail(HLA_ERR_ARG, "workspace must be 16-byte aligned");
+    hla::BwdArgs a;
+    a.B = p->B; a.H = p->H; a.n = p->n; a.d = p->d; a.dv = p->dv; a.chunk = p->chunk;
+    a.in_dtype = p->in_dtype; a.flags = p->flags & HLA_DECAY; a.gamma = p->gamma;
+    a.q = q; a.k = k; a.v = v; a.go = dout;
+    a.grad_q = dq; a.grad_k = dk; a.grad_v = dv;
+    a.workspace = static_cast<float *>(workspace);
+    cudaError_t e = hla::bwd_simt_launch(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return HLA_OK;
+}
+
 hla_status hla_state_combine(int count, int d, int dv, unsigned flags, const hla_state *A, const hla_state *B,
                              const hla_state *out, const float *decay_pow, void *stream) {
     if (count < 0) return fail(HLA_ERR_ARG, "count must be >= 0");

@@ -1,0 +1,8 @@
+// Backward kernels for f32 inputs and chunk length 16.
+#include "hla_bwd_simt.cuh"
+
+namespace hla {
+namespace bwd {
+template cudaError_t launch_d<float, 16>(const BwdArgs &, cudaStream_t);
+}  // namespace bwd
+}  // namespace hla

@@ -1,0 +1,503 @@
+// hla_bwd_simt.cuh -- chunk-parallel backward pass of the masked second-order HLA
+// forward on CUDA cores (fp32 arithmetic), for d, dv, chunk in {16,32,64}, zero
+// initial state, no normalisation, one key/value head per query head.
+//
+// The pages motivate chunk-parallel training ("Higher-order Linear Attention",
+// gist.science summary, section 4) but print no gradient.  Forward in the working
+// form of the forward kernels (section 1, with X = S C - G):
+//   S_t = g S_{t-1} + k_t k_t^T,  u_t = S_t q_t,  X_t = g^2 X_{t-1} + u_t v_t^T,
+//   o_t = X_t^T q_t.
+// Reverse mode with the upstream gradient g_t = dL/do_t and the accumulators
+//   Lam_t = dL/dX_t = q_t g_t^T + g^2 Lam_{t+1},  Om_t = dL/dS_t = du_t q_t^T + g Om_{t+1}
+// gives  du_t = Lam_t v_t,  dv_t = Lam_t^T u_t,  dq_t = X_t g_t + S_t du_t,
+// dk_t = (Om_t + Om_t^T) k_t.
+//
+// Chunk form (tau = 0..L-1 inside a chunk; S_p, X_p the states before it; Lam, Om
+// the accumulators of everything after it):
+//   A~[t,s] = g^{t-s} q_t.k_s,  P[s,b] = g^{2(s-b)} g_s.v_b  (lower triangles)
+//   U  = diag(g^{tau+1}) Q S_p + A~ K
+//   dU = P^T Q + diag(g^{2(L-tau)}) V Lam^T
+//   B[t,a] = g^{t-a} du_t.k_a,  M[s,t] = g^{2(s-t)} q_s.u_t  (lower triangles)
+//   dQ = P U + diag(g^{2(tau+1)}) G X_p^T + diag(g^{tau+1}) dU S_p + B K
+//   dK = A~^T dU + B^T Q + diag(g^{L-tau}) K (Om + Om^T)
+//   dV = M^T G + diag(g^{2(L-tau)}) U Lam
+// and the chunk-to-chunk maps
+//   S <- g^L S + Sloc,           X <- g^{2L} X + S_p Cq + Xloc,
+//   Lam <- g^{2L} Lam + Lloc,    Om <- g^L Om + Oloc + Lam_next W,
+// with the chunk-local sums (weights zero past the chunk's last token)
+//   Sloc = sum_s g^{L-1-s} k_s k_s^T,  Cq = sum_s g^{2L-1-s} q_s v_s^T,
+//   Xloc = sum_s g^{2(L-1-s)} (A~K)_s v_s^T,  Lloc = sum_s g^{2s} q_s g_s^T,
+//   W = sum_s g^{2L-s} v_s q_s^T,  Oloc = sum_s g^s (P^T Q)_s q_s^T.
+//
+// Three launches: (1) one CTA per chunk writes the six local sums; (2) the scan,
+// one CTA per (b,h, column block, direction), walks the chunks forward for S, X
+// and backward for Lam, Om and writes the states every chunk needs; (3) one CTA
+// per chunk forms dq, dk, dv.
+#pragma once
+#include "hla_internal.h"
+
+namespace hla {
+namespace bwd {
+
+constexpr int kThreads = 256;
+constexpr int kSplit = 4;  // column blocks per (b,h) and direction in the scan
+
+template <typename T>
+__device__ __forceinline__ float ld_t(const T *p, size_t i);
+template <>
+__device__ __forceinline__ float ld_t<float>(const float *p, size_t i) { return p[i]; }
+template <>
+__device__ __forceinline__ float ld_t<__nv_bfloat16>(const __nv_bfloat16 *p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+template <typename T>
+__device__ __forceinline__ void st_t(T *p, size_t i, float x);
+template <>
+__device__ __forceinline__ void st_t<float>(float *p, size_t i, float x) { p[i] = x; }
+template <>
+__device__ __forceinline__ void st_t<__nv_bfloat16>(__nv_bfloat16 *p, size_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+// ---- small shared-memory products on a 4x4 register tile per thread --------------
+// acc[i][j] += sum_k w_k A(m0+i, k) B(k, n0 + j*ns).  A(m,k) = TA ? A[k*lda+m] : A[m*lda+k];
+// B(k,n) = TB ? B[n*ldb+k] : B[k*ldb+n].  K a multiple of 4, leading dimensions multiples
+// of 4 floats, bases 16-byte aligned.  ns == 1: four adjacent columns; else strided.
+template <bool TA, bool TB>
+__device__ __forceinline__ void mac(float (&acc)[4][4], const float *A, int lda, const float *B, int ldb, int m0,
+                                    int n0, int ns, int K, const float *kw = nullptr) {
+#pragma unroll 2
+    for (int k = 0; k < K; k += 4) {
+        float a[4][4], b[4][4];  // [kk][i], [kk][j]
+        if (TA) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float4 x = *reinterpret_cast<const float4 *>(A + (size_t)(k + kk) * lda + m0);
+                a[kk][0] = x.x; a[kk][1] = x.y; a[kk][2] = x.z; a[kk][3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 x = *reinterpret_cast<const float4 *>(A + (size_t)(m0 + i) * lda + k);
+                a[0][i] = x.x; a[1][i] = x.y; a[2][i] = x.z; a[3][i] = x.w;
+            }
+        }
+        if (kw) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float w = kw[k + kk];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) a[kk][i] *= w;
+            }
+        }
+        if (TB) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 x = *reinterpret_cast<const float4 *>(B + (size_t)(n0 + j * ns) * ldb + k);
+                b[0][j] = x.x; b[1][j] = x.y; b[2][j] = x.z; b[3][j] = x.w;
+            }
+        } else if (ns == 1) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float4 x = *reinterpret_cast<const float4 *>(B + (size_t)(k + kk) * ldb + n0);
+                b[kk][0] = x.x; b[kk][1] = x.y; b[kk][2] = x.z; b[kk][3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) b[kk][j] = B[(size_t)(k + kk) * ldb + n0 + j * ns];
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[kk][i], b[kk][j], acc[i][j]);
+    }
+}
+
+// The same term scaled by rs[row] before it is added.
+template <bool TA, bool TB>
+__device__ __forceinline__ void mac_rs(float (&acc)[4][4], const float *rs, const float *A, int lda, const float *B,
+                                       int ldb, int m0, int n0, int ns, int K) {
+    float t[4][4] = {};
+    mac<TA, TB>(t, A, lda, B, ldb, m0, n0, ns, K);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(rs[m0 + i], t[i][j], acc[i][j]);
+}
+
+// Every 4x4 tile of an M x N result, one per thread per round.  STRIDED spreads a
+// thread's four columns N/4 apart (conflict-free rows when B is read transposed).
+template <bool STRIDED, class Body>
+__device__ __forceinline__ void tiles(int M, int N, Body body) {
+    const int tn = N / 4, count = (M / 4) * tn;
+    for (int t = threadIdx.x; t < count; t += kThreads) {
+        const int m0 = (t / tn) * 4;
+        const int n0 = STRIDED ? t % tn : (t % tn) * 4, ns = STRIDED ? tn : 1;
+        float acc[4][4] = {};
+        body(acc, m0, n0, ns);
+    }
+}
+
+template <class F>
+__device__ __forceinline__ void each(const float (&acc)[4][4], int m0, int n0, int ns, F f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f(m0 + i, n0 + j * ns, acc[i][j]);
+}
+
+template <typename T>
+__device__ __forceinline__ void load_rows(const T *src, float *dst, int ld, int rows, int L, int W) {
+    for (int e = threadIdx.x; e < rows * W; e += kThreads) {
+        const int r = e / W, x = e % W;
+        dst[r * ld + x] = r < L ? ld_t(src, (size_t)r * W + x) : 0.f;
+    }
+}
+
+__device__ __forceinline__ void load_mat(const float *src, float *dst, int ld, int rows, int W) {
+    for (int e = threadIdx.x; e < rows * W; e += kThreads) dst[(e / W) * ld + e % W] = src[e];
+}
+
+// Workspace: the six local sums of every (b,h, chunk), then the four states of
+// every (b,h, chunk).
+struct BwdWs {
+    int d, dv;
+    __host__ __device__ size_t loc_floats() const { return 2 * (size_t)d * d + 4 * (size_t)d * dv; }
+    __host__ __device__ size_t st_floats() const { return 2 * (size_t)d * d + 2 * (size_t)d * dv; }
+    // local sums: Sloc d*d, Cq d*dv, Xloc d*dv, Lloc d*dv, W dv*d, Oloc d*d
+    __host__ __device__ size_t o_sloc() const { return 0; }
+    __host__ __device__ size_t o_cq() const { return (size_t)d * d; }
+    __host__ __device__ size_t o_xloc() const { return o_cq() + (size_t)d * dv; }
+    __host__ __device__ size_t o_lloc() const { return o_xloc() + (size_t)d * dv; }
+    __host__ __device__ size_t o_w() const { return o_lloc() + (size_t)d * dv; }
+    __host__ __device__ size_t o_oloc() const { return o_w() + (size_t)d * dv; }
+    // states: S_p d*d, X_p d*dv, Lam_next d*dv, Om_next d*d
+    __host__ __device__ size_t o_sp() const { return 0; }
+    __host__ __device__ size_t o_xp() const { return (size_t)d * d; }
+    __host__ __device__ size_t o_lam() const { return o_xp() + (size_t)d * dv; }
+    __host__ __device__ size_t o_om() const { return o_lam() + (size_t)d * dv; }
+};
+
+__device__ __forceinline__ void fill_gp(float *gp, int c, float lg, bool decay) {
+    for (int x = threadIdx.x; x <= 2 * c; x += kThreads) gp[x] = decay ? gpow(lg, (float)x) : 1.f;
+}
+
+// ---- (1) chunk-local sums --------------------------------------------------------
+template <int C, int D, int DV>
+struct LocSmem {
+    static constexpr int LQ = D + 4, LV = DV + 4, LT = C + 4;
+    static constexpr int Q = 0, K = Q + C * LQ, V = K + C * LQ, G = V + C * LV, A = G + C * LV, P = A + C * LT,
+                         U = P + C * LT, DU = U + C * LQ, GP = DU + C * LQ, WS = GP + 2 * C + 4,
+                         TOTAL = WS + 6 * C;
+};
+
+template <typename T, int C, int D, int DV>
+__global__ void __launch_bounds__(kThreads) bwd_local_kernel(BwdArgs a) {
+    using Sm = LocSmem<C, D, DV>;
+    extern __shared__ __align__(16) float sm[];
+    float *Q = sm + Sm::Q, *K = sm + Sm::K, *V = sm + Sm::V, *G = sm + Sm::G, *A = sm + Sm::A, *P = sm + Sm::P;
+    float *U = sm + Sm::U, *dU = sm + Sm::DU, *gp = sm + Sm::GP, *w = sm + Sm::WS;
+    const int nch = (a.n + C - 1) / C, u = blockIdx.x / nch, ch = blockIdx.x % nch;
+    const int t0 = ch * C, L = min(C, a.n - t0);
+    const bool decay = (a.flags & HLA_DECAY) != 0;
+    const float lg = log2f(decay ? a.gamma[u % a.H] : 1.f);
+    const size_t rq = ((size_t)u * a.n + t0) * D, rv = ((size_t)u * a.n + t0) * DV;
+    load_rows(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L, D);
+    load_rows(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L, D);
+    load_rows(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L, DV);
+    load_rows(static_cast<const T *>(a.go) + rv, G, Sm::LV, C, L, DV);
+    fill_gp(gp, C, lg, decay);
+    __syncthreads();
+    for (int s = threadIdx.x; s < C; s += kThreads) {
+        const bool in = s < L;
+        w[0 * C + s] = in ? gp[L - 1 - s] : 0.f;        // Sloc
+        w[1 * C + s] = in ? gp[2 * L - 1 - s] : 0.f;    // Cq
+        w[2 * C + s] = in ? gp[2 * (L - 1 - s)] : 0.f;  // Xloc
+        w[3 * C + s] = in ? gp[2 * s] : 0.f;            // Lloc
+        w[4 * C + s] = in ? gp[2 * L - s] : 0.f;        // W
+        w[5 * C + s] = in ? gp[s] : 0.f;                // Oloc
+    }
+    // A~ = tril(g^{t-s} Q K^T), P = tril(g^{2(s-b)} G V^T)
+    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, true>(acc, Q, Sm::LQ, K, Sm::LQ, m0, n0, ns, D);
+        each(acc, m0, n0, ns, [&](int t, int s, float x) { A[t * Sm::LT + s] = s <= t ? gp[t - s] * x : 0.f; });
+    });
+    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, true>(acc, G, Sm::LV, V, Sm::LV, m0, n0, ns, DV);
+        each(acc, m0, n0, ns, [&](int s, int b, float x) { P[s * Sm::LT + b] = b <= s ? gp[2 * (s - b)] * x : 0.f; });
+    });
+    __syncthreads();
+    // U = A~ K (the part of u without the earlier state), dU = P^T Q
+    tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, false>(acc, A, Sm::LT, K, Sm::LQ, m0, n0, ns, C);
+        each(acc, m0, n0, ns, [&](int t, int i, float x) { U[t * Sm::LQ + i] = x; });
+    });
+    tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, P, Sm::LT, Q, Sm::LQ, m0, n0, ns, C);
+        each(acc, m0, n0, ns, [&](int t, int i, float x) { dU[t * Sm::LQ + i] = x; });
+    });
+    __syncthreads();
+    const BwdWs ws{D, DV};
+    float *out = a.workspace + ((size_t)u * nch + ch) * ws.loc_floats();
+    auto put = [&](size_t off, int ld) {
+        return [=](int i, int j, float x) { out[off + (size_t)i * ld + j] = x; };
+    };
+    tiles<false>(D, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, K, Sm::LQ, K, Sm::LQ, m0, n0, ns, C, w + 0 * C);
+        each(acc, m0, n0, ns, put(ws.o_sloc(), D));
+    });
+    tiles<false>(D, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, Q, Sm::LQ, V, Sm::LV, m0, n0, ns, C, w + 1 * C);
+        each(acc, m0, n0, ns, put(ws.o_cq(), DV));
+    });
+    tiles<false>(D, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, U, Sm::LQ, V, Sm::LV, m0, n0, ns, C, w + 2 * C);
+        each(acc, m0, n0, ns, put(ws.o_xloc(), DV));
+    });
+    tiles<false>(D, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, Q, Sm::LQ, G, Sm::LV, m0, n0, ns, C, w + 3 * C);
+        each(acc, m0, n0, ns, put(ws.o_lloc(), DV));
+    });
+    tiles<false>(DV, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, V, Sm::LV, Q, Sm::LQ, m0, n0, ns, C, w + 4 * C);
+        each(acc, m0, n0, ns, put(ws.o_w(), D));
+    });
+    tiles<false>(D, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, dU, Sm::LQ, Q, Sm::LQ, m0, n0, ns, C, w + 5 * C);
+        each(acc, m0, n0, ns, put(ws.o_oloc(), D));
+    });
+}
+
+// ---- (2) scan over chunks ---------------------------------------------------------
+// blockIdx.x = (u * kSplit + part) * 2 + dir.  dir 0: S (whole) and the columns
+// [part*dv/kSplit, ...) of X, forward in time.  dir 1: Lam (whole) and the columns
+// [part*d/kSplit, ...) of Om, backward in time.  Each CTA stores its column block
+// of X_p / Om_next and the row block `part` of S_p / Lam_next.
+template <int C, int D, int DV>
+struct ScanSmem {
+    static constexpr int WMAX = DV > D ? DV : D;
+    static constexpr int NB = WMAX / kSplit;  // widest column block
+    static constexpr int FW = WMAX + 4, LB = NB + 4;
+    // F: S or Lam (D x <= WMAX); FL its increment; BK: the column block of X or Om;
+    // R: the product operand block (Cq or W, <= WMAX rows); BL: the block increment
+    static constexpr int F = 0, FL = F + D * FW, BK = FL + D * FW, R = BK + D * LB, BL = R + WMAX * LB,
+                         TOTAL = BL + D * LB;
+};
+
+template <int C, int D, int DV>
+__global__ void __launch_bounds__(kThreads) bwd_scan_kernel(BwdArgs a) {
+    using Sm = ScanSmem<C, D, DV>;
+    extern __shared__ __align__(16) float sm[];
+    float *F = sm + Sm::F, *Fl = sm + Sm::FL, *Bk = sm + Sm::BK, *R = sm + Sm::R, *Bl = sm + Sm::BL;
+    const int dir = blockIdx.x & 1, part = (blockIdx.x >> 1) % kSplit, u = (blockIdx.x >> 1) / kSplit;
+    const int nch = (a.n + C - 1) / C;
+    const bool decay = (a.flags & HLA_DECAY) != 0;
+    const float lg = log2f(decay ? a.gamma[u % a.H] : 1.f);
+    const BwdWs ws{D, DV};
+    const float *loc = a.workspace + (size_t)u * nch * ws.loc_floats();
+    float *st = a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + (size_t)u * nch * ws.st_floats();
+    // dir 0: F = S (D x D), block of X (D x DV), R = block of Cq (D x DV)
+    // dir 1: F = Lam (D x DV), block of Om (D x D), R = block of W (DV x D)
+    const int fw = dir == 0 ? D : DV, bw = dir == 0 ? DV : D, nb = bw / kSplit, c0 = part * nb;
+    const int rk = dir == 0 ? D : DV;  // inner dimension of F R
+    const int rows = D / kSplit, rows0 = part * rows;
+    for (int e = threadIdx.x; e < D * Sm::FW; e += kThreads) F[e] = 0.f;
+    for (int e = threadIdx.x; e < D * Sm::LB; e += kThreads) Bk[e] = 0.f;
+    __syncthreads();
+    for (int it = 0; it < nch; ++it) {
+        const int ch = dir == 0 ? it : nch - 1 - it;
+        const int L = min(C, a.n - ch * C);
+        const float f1 = decay ? gpow(lg, (float)L) : 1.f, f2 = decay ? gpow(lg, (float)(2 * L)) : 1.f;
+        const float *lc = loc + (size_t)ch * ws.loc_floats();
+        float *so = st + (size_t)ch * ws.st_floats();
+        // the states this chunk starts from (S_p, X_p) or ends into (Lam_next, Om_next)
+        float *fo = so + (dir == 0 ? ws.o_sp() : ws.o_lam()), *bo = so + (dir == 0 ? ws.o_xp() : ws.o_om());
+        for (int e = threadIdx.x; e < rows * fw; e += kThreads) {
+            const int r = rows0 + e / fw, x = e % fw;
+            fo[(size_t)r * fw + x] = F[r * Sm::FW + x];
+        }
+        for (int e = threadIdx.x; e < D * nb; e += kThreads) {
+            const int r = e / nb, x = e % nb;
+            bo[(size_t)r * bw + c0 + x] = Bk[r * Sm::LB + x];
+        }
+        // this chunk's local sums
+        const float *fl = lc + (dir == 0 ? ws.o_sloc() : ws.o_lloc());
+        const float *rr = lc + (dir == 0 ? ws.o_cq() : ws.o_w());
+        const float *bl = lc + (dir == 0 ? ws.o_xloc() : ws.o_oloc());
+        load_mat(fl, Fl, Sm::FW, D, fw);
+        for (int e = threadIdx.x; e < rk * nb; e += kThreads)
+            R[(e / nb) * Sm::LB + e % nb] = rr[(size_t)(e / nb) * bw + c0 + e % nb];
+        for (int e = threadIdx.x; e < D * nb; e += kThreads)
+            Bl[(e / nb) * Sm::LB + e % nb] = bl[(size_t)(e / nb) * bw + c0 + e % nb];
+        __syncthreads();
+        // block <- f_b block + Bl + F R  (F the state before this chunk's update)
+        const float fb = dir == 0 ? f2 : f1, ff = dir == 0 ? f1 : f2;
+        tiles<false>(D, nb, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+            mac<false, false>(acc, F, Sm::FW, R, Sm::LB, m0, n0, ns, rk);
+            each(acc, m0, n0, ns, [&](int i, int j, float x) {
+                Bk[i * Sm::LB + j] = fb * Bk[i * Sm::LB + j] + Bl[i * Sm::LB + j] + x;
+            });
+        });
+        __syncthreads();
+        for (int e = threadIdx.x; e < D * fw; e += kThreads) {
+            const int r = e / fw, x = e % fw;
+            F[r * Sm::FW + x] = ff * F[r * Sm::FW + x] + Fl[r * Sm::FW + x];
+        }
+        __syncthreads();
+    }
+}
+
+// ---- (3) gradients of one chunk ---------------------------------------------------
+template <int C, int D, int DV>
+struct GradSmem {
+    static constexpr int LQ = D + 4, LV = DV + 4, LT = C + 4;
+    static constexpr int Q = 0, K = Q + C * LQ, V = K + C * LQ, G = V + C * LV, SP = G + C * LV, XP = SP + D * LQ,
+                         LAM = XP + D * LV, OM = LAM + D * LV, A = OM + D * LQ, P = A + C * LT, BM = P + C * LT,
+                         U = BM + C * LT, DU = U + C * LQ, GP = DU + C * LQ, RS = GP + 2 * C + 4,
+                         TOTAL = RS + 4 * C;
+};
+
+template <typename T, int C, int D, int DV>
+__global__ void __launch_bounds__(kThreads) bwd_grad_kernel(BwdArgs a) {
+    using Sm = GradSmem<C, D, DV>;
+    extern __shared__ __align__(16) float sm[];
+    float *Q = sm + Sm::Q, *K = sm + Sm::K, *V = sm + Sm::V, *G = sm + Sm::G, *Sp = sm + Sm::SP, *Xp = sm + Sm::XP;
+    float *Lam = sm + Sm::LAM, *Om = sm + Sm::OM, *A = sm + Sm::A, *P = sm + Sm::P, *Bm = sm + Sm::BM;
+    float *U = sm + Sm::U, *dU = sm + Sm::DU, *gp = sm + Sm::GP, *rs = sm + Sm::RS;
+    const int nch = (a.n + C - 1) / C, u = blockIdx.x / nch, ch = blockIdx.x % nch;
+    const int t0 = ch * C, L = min(C, a.n - t0);
+    const bool decay = (a.flags & HLA_DECAY) != 0;
+    const float lg = log2f(decay ? a.gamma[u % a.H] : 1.f);
+    const size_t rq = ((size_t)u * a.n + t0) * D, rv = ((size_t)u * a.n + t0) * DV;
+    const BwdWs ws{D, DV};
+    const float *so =
+        a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
+    load_rows(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L, D);
+    load_rows(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L, D);
+    load_rows(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L, DV);
+    load_rows(static_cast<const T *>(a.go) + rv, G, Sm::LV, C, L, DV);
+    load_mat(so + ws.o_sp(), Sp, Sm::LQ, D, D);
+    load_mat(so + ws.o_xp(), Xp, Sm::LV, D, DV);
+    load_mat(so + ws.o_lam(), Lam, Sm::LV, D, DV);
+    load_mat(so + ws.o_om(), Om, Sm::LQ, D, D);
+    fill_gp(gp, C, lg, decay);
+    __syncthreads();
+    float *r_u = rs, *r_x = rs + C, *r_l2 = rs + 2 * C, *r_l1 = rs + 3 * C;
+    for (int t = threadIdx.x; t < C; t += kThreads) {
+        const bool in = t < L;
+        r_u[t] = gp[t + 1];                    // g^{tau+1}
+        r_x[t] = gp[2 * (t + 1)];              // g^{2(tau+1)}
+        r_l2[t] = in ? gp[2 * (L - t)] : 0.f;  // g^{2(L-tau)}
+        r_l1[t] = in ? gp[L - t] : 0.f;        // g^{L-tau}
+    }
+    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, true>(acc, Q, Sm::LQ, K, Sm::LQ, m0, n0, ns, D);
+        each(acc, m0, n0, ns, [&](int t, int s, float x) { A[t * Sm::LT + s] = s <= t ? gp[t - s] * x : 0.f; });
+    });
+    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, true>(acc, G, Sm::LV, V, Sm::LV, m0, n0, ns, DV);
+        each(acc, m0, n0, ns, [&](int s, int b, float x) { P[s * Sm::LT + b] = b <= s ? gp[2 * (s - b)] * x : 0.f; });
+    });
+    __syncthreads();
+    // U = diag(g^{tau+1}) Q S_p + A~ K;  dU = P^T Q + diag(g^{2(L-tau)}) V Lam^T
+    tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac_rs<false, false>(acc, r_u, Q, Sm::LQ, Sp, Sm::LQ, m0, n0, ns, D);
+        mac<false, false>(acc, A, Sm::LT, K, Sm::LQ, m0, n0, ns, C);
+        each(acc, m0, n0, ns, [&](int t, int i, float x) { U[t * Sm::LQ + i] = x; });
+    });
+    tiles<true>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, P, Sm::LT, Q, Sm::LQ, m0, n0, ns, C);
+        mac_rs<false, true>(acc, r_l2, V, Sm::LV, Lam, Sm::LV, m0, n0, ns, DV);
+        each(acc, m0, n0, ns, [&](int t, int i, float x) { dU[t * Sm::LQ + i] = x; });
+    });
+    __syncthreads();
+    // B = tril(g^{t-a} dU K^T)
+    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, true>(acc, dU, Sm::LQ, K, Sm::LQ, m0, n0, ns, D);
+        each(acc, m0, n0, ns, [&](int t, int s, float x) { Bm[t * Sm::LT + s] = s <= t ? gp[t - s] * x : 0.f; });
+    });
+    __syncthreads();
+    T *gq = static_cast<T *>(a.grad_q) + rq;
+    T *gk = static_cast<T *>(a.grad_k) + rq;
+    T *gv = static_cast<T *>(a.grad_v) + rv;
+    // dQ = P U + diag(g^{2(tau+1)}) G X_p^T + diag(g^{tau+1}) dU S_p + B K   (S_p symmetric)
+    tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, false>(acc, P, Sm::LT, U, Sm::LQ, m0, n0, ns, C);
+        mac_rs<false, true>(acc, r_x, G, Sm::LV, Xp, Sm::LV, m0, n0, ns, DV);
+        mac_rs<false, false>(acc, r_u, dU, Sm::LQ, Sp, Sm::LQ, m0, n0, ns, D);
+        mac<false, false>(acc, Bm, Sm::LT, K, Sm::LQ, m0, n0, ns, C);
+        each(acc, m0, n0, ns, [&](int t, int i, float x) {
+            if (t < L) st_t(gq, (size_t)t * D + i, x);
+        });
+    });
+    // dK = A~^T dU + B^T Q + diag(g^{L-tau}) K (Om + Om^T)
+    tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, A, Sm::LT, dU, Sm::LQ, m0, n0, ns, C);
+        mac<true, false>(acc, Bm, Sm::LT, Q, Sm::LQ, m0, n0, ns, C);
+        mac_rs<false, false>(acc, r_l1, K, Sm::LQ, Om, Sm::LQ, m0, n0, ns, D);
+        mac_rs<false, true>(acc, r_l1, K, Sm::LQ, Om, Sm::LQ, m0, n0, ns, D);
+        each(acc, m0, n0, ns, [&](int t, int i, float x) {
+            if (t < L) st_t(gk, (size_t)t * D + i, x);
+        });
+    });
+    __syncthreads();
+    // M = tril(g^{2(s-t)} Q U^T) into the slot of P
+    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, true>(acc, Q, Sm::LQ, U, Sm::LQ, m0, n0, ns, D);
+        each(acc, m0, n0, ns, [&](int s, int t, float x) { P[s * Sm::LT + t] = t <= s ? gp[2 * (s - t)] * x : 0.f; });
+    });
+    __syncthreads();
+    // dV = M^T G + diag(g^{2(L-tau)}) U Lam
+    tiles<false>(C, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, P, Sm::LT, G, Sm::LV, m0, n0, ns, C);
+        mac_rs<false, false>(acc, r_l2, U, Sm::LQ, Lam, Sm::LV, m0, n0, ns, D);
+        each(acc, m0, n0, ns, [&](int t, int j, float x) {
+            if (t < L) st_t(gv, (size_t)t * DV + j, x);
+        });
+    });
+}
+
+template <typename Kern>
+cudaError_t smem_attr(Kern kern, size_t bytes) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <typename T, int C, int D, int DV>
+cudaError_t launch_t(const BwdArgs &a, cudaStream_t st) {
+    const int nch = (a.n + C - 1) / C, units = a.B * a.H;
+    const size_t b1 = LocSmem<C, D, DV>::TOTAL * sizeof(float), b2 = ScanSmem<C, D, DV>::TOTAL * sizeof(float),
+                 b3 = GradSmem<C, D, DV>::TOTAL * sizeof(float);
+    cudaError_t e;
+    if ((e = smem_attr(bwd_local_kernel<T, C, D, DV>, b1)) != cudaSuccess) return e;
+    if ((e = smem_attr(bwd_scan_kernel<C, D, DV>, b2)) != cudaSuccess) return e;
+    if ((e = smem_attr(bwd_grad_kernel<T, C, D, DV>, b3)) != cudaSuccess) return e;
+    bwd_local_kernel<T, C, D, DV><<<units * nch, kThreads, b1, st>>>(a);
+    bwd_scan_kernel<C, D, DV><<<units * kSplit * 2, kThreads, b2, st>>>(a);
+    bwd_grad_kernel<T, C, D, DV><<<units * nch, kThreads, b3, st>>>(a);
+    return cudaGetLastError();
+}
+template <typename T, int C, int D>
+cudaError_t launch_dv(const BwdArgs &a, cudaStream_t st) {
+    switch (a.dv) {
+        case 16: return launch_t<T, C, D, 16>(a, st);
+        case 32: return launch_t<T, C, D, 32>(a, st);
+        case 64: return launch_t<T, C, D, 64>(a, st);
+    }
+    return cudaErrorInvalidValue;
+}
+template <typename T, int C>
+cudaError_t launch_d(const BwdArgs &a, cudaStream_t st) {
+    switch (a.d) {
+        case 16: return launch_dv<T, C, 16>(a, st);
+        case 32: return launch_dv<T, C, 32>(a, st);
+        case 64: return launch_dv<T, C, 64>(a, st);
+    }
+    return cudaErrorInvalidValue;
+}
+// One translation unit per (element type, chunk) instantiates launch_d.
+}  // namespace bwd
+}  // namespace hla

@@ -65,6 +65,21 @@ struct DecodeArgs {
 };
 cudaError_t decode_launch(const DecodeArgs &a, cudaStream_t st);
 
+struct BwdArgs {
+    int B, H, n, d, dv, chunk;
+    hla_dtype in_dtype;
+    unsigned flags;  // 0 or HLA_DECAY
+    const float *gamma;
+    const void *q, *k, *v, *go;    // inputs and the gradient of the output
+    void *grad_q, *grad_k, *grad_v;  // outputs
+    float *workspace;
+};
+
+// Backward of the masked forward on CUDA cores (d, dv, chunk in {16,32,64}).
+bool bwd_simt_supported(const hla_params &p);
+size_t bwd_simt_workspace(const hla_params &p);
+cudaError_t bwd_simt_launch(const BwdArgs &a, cudaStream_t st);
+
 // Set this thread's last-error message and return `s`.
 hla_status report(hla_status s, const char *msg);
 

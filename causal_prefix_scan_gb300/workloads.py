@@ -73,7 +73,11 @@ FWD_UNMASKED = Workload("fwd_bf16_unmasked_B4H8n2048d64", 4, 8, 2048, 64, 64, 64
                         unmasked=True)
 FWD_SHARED_KV = Workload("fwd_bf16_kv2_B4H8n2048d64", 4, 8, 2048, 64, 64, 64, "bf16", "l2", seed=7, Hkv=2)
 FWD_ASYM = Workload("fwd_bf16_asym_B4H8n2048d64", 4, 8, 2048, 64, 64, 64, "bf16", "l2", seed=8, asymmetric=True)
-WORKLOADS = {w.name: w for w in (SMALL_F32, FWD_BF16, FWD_NORM, FWD_DECAY, FWD_UNMASKED, FWD_SHARED_KV, FWD_ASYM)}
+# The backward pass (training) on the same shape: q, k, v as above plus the
+# gradient of the output from make_dout.
+BWD_BF16 = Workload("bwd_bf16_B4H8n2048d64", 4, 8, 2048, 64, 64, 64, "bf16", "l2", seed=9)
+WORKLOADS = {w.name: w for w in (SMALL_F32, FWD_BF16, FWD_NORM, FWD_DECAY, FWD_UNMASKED, FWD_SHARED_KV, FWD_ASYM,
+                                 BWD_BF16)}
 
 
 @dataclass(frozen=True)
@@ -135,6 +139,14 @@ def make_inputs(w: Workload):
     if w.dtype == "bf16":
         q, k, v = round_bf16(q), round_bf16(k), round_bf16(v)
     return {"q": q, "k": k, "v": v, "gamma": gamma}
+
+
+def make_dout(w: Workload) -> np.ndarray:
+    """The gradient of the output for a backward workload: float32 standard normals
+    of shape [B,H,n,dv] from default_rng(seed + 1000), rounded like the inputs."""
+    rng = np.random.default_rng(w.seed + 1000)
+    g = rng.standard_normal((w.B, w.H, w.n, w.dv), dtype=np.float32)
+    return round_bf16(g) if w.dtype == "bf16" else g
 
 
 def make_decode_tokens(seqs: int, H: int, d: int, dv: int, steps: int, seed: int):

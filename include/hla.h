@@ -189,6 +189,29 @@ HLA_API hla_status hla_decode_step(int N, int H, int Hkv, int d, int dv, hla_dty
                            const void *q, const void *k, const void *v, void *o,
                            void *stream);
 
+/*
+ * Backward pass (training) of the masked forward with zero initial state and no
+ * normalisation.  The pages motivate chunk-parallel training (section 4) but give
+ * no gradient; this call is reverse-mode differentiation of the section 1
+ * recurrence, evaluated chunk-parallel: per-chunk local sums, a scan over chunks
+ * (the states S, X = S C - G forward in time and the adjoints dL/dX, dL/dS
+ * backward in time), then per-chunk gradients.  Its result equals the gradient
+ * of sum_t dout_t . o_t up to floating-point rounding.
+ *
+ *   p      as for hla_forward_chunked; supported: flags 0 or HLA_DECAY only
+ *          (others HLA_ERR_UNSUPPORTED), Hkv 0 or H, d, dv, chunk in {16,32,64},
+ *          in_dtype HLA_F32 or HLA_BF16 (fp32 arithmetic either way);
+ *   q, k   [B][H][n][d], v and dout [B][H][n][dv], in_dtype, read only;
+ *   dq, dk [B][H][n][d], dv [B][H][n][dv], in_dtype, written (not accumulated);
+ *   workspace device scratch of at least hla_backward_workspace_size(p) bytes,
+ *          16-byte aligned, no initial contents needed.
+ * All tensor pointers 16-byte aligned.  Three kernel launches on `stream`.
+ */
+HLA_API size_t hla_backward_workspace_size(const hla_params *p);
+HLA_API hla_status hla_backward_chunked(const hla_params *p, const void *q, const void *k, const void *v,
+                                        const void *dout, void *dq, void *dk, void *dv, void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
 /* Synchronise `stream`, then report and clear the sticky device flag: HLA_OK,
  * HLA_ERR_TIMEOUT if a bounded device wait expired since the last call, or
  * HLA_ERR_CUDA if the stream reported an error. */

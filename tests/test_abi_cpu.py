@@ -123,3 +123,52 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(hla, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         hla.library(str(tmp_path / "nope.so"))
+
+
+def _bcall(p, ptrs=(16,) * 7, ws=16, ws_bytes=1 << 40):
+    q, k, v, do, dq, dk, dv = ptrs
+    return hla.library().hla_backward_chunked(ctypes.byref(p) if p is not None else None, q, k, v, do, dq, dk, dv,
+                                              ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), hla.HLA_ERR_ARG),
+    (dict(n=-1), hla.HLA_ERR_ARG),
+    (dict(flags=16), hla.HLA_ERR_ARG),
+    (dict(flags=hla.HLA_DECAY), hla.HLA_ERR_ARG),            # decay without gamma
+    (dict(flags=hla.HLA_NORMALIZE), hla.HLA_ERR_UNSUPPORTED),
+    (dict(flags=hla.HLA_UNMASKED), hla.HLA_ERR_UNSUPPORTED),
+    (dict(flags=hla.HLA_ASYMMETRIC), hla.HLA_ERR_UNSUPPORTED),
+    (dict(H=4, Hkv=2), hla.HLA_ERR_UNSUPPORTED),             # shared key/value heads
+    (dict(H=6, Hkv=4), hla.HLA_ERR_ARG),
+    (dict(d=128), hla.HLA_ERR_UNSUPPORTED),
+    (dict(dv=128), hla.HLA_ERR_UNSUPPORTED),
+    (dict(chunk=128), hla.HLA_ERR_UNSUPPORTED),
+    (dict(d=48), hla.HLA_ERR_UNSUPPORTED),
+])
+def test_backward_rejects_bad_params(lib, kw, status):
+    assert _bcall(_params(**kw)) == status
+    assert hla.hla_last_error()
+    assert hla.hla_backward_workspace_size(_params(**kw)) == 0
+
+
+def test_backward_rejects_null_misaligned_and_short_workspace(lib):
+    assert _bcall(None) == hla.HLA_ERR_ARG
+    assert _bcall(_params(), ptrs=(16, 16, 16, None, 16, 16, 16)) == hla.HLA_ERR_ARG
+    assert _bcall(_params(), ptrs=(16, 16, 16, 16, 16, 8, 16)) == hla.HLA_ERR_ARG
+    need = hla.hla_backward_workspace_size(_params())
+    assert _bcall(_params(), ws_bytes=need - 1) == hla.HLA_ERR_ARG
+    assert "workspace" in hla.hla_last_error()
+    assert _bcall(_params(), ws=None) == hla.HLA_ERR_ARG
+    assert _bcall(_params(), ws=8) == hla.HLA_ERR_ARG
+
+
+def test_backward_workspace_size_and_empty_sequence(lib):
+    # per (b,h, chunk): six local sums and four states, fp32
+    for B, H, n, d, dv, c in [(1, 2, 128, 64, 64, 64), (2, 3, 100, 32, 16, 32), (1, 1, 1, 16, 64, 16)]:
+        nch = -(-n // c)
+        want = B * H * nch * (4 * d * d + 6 * d * dv) * 4
+        got = hla.hla_backward_workspace_size(_params(B=B, H=H, n=n, d=d, dv=dv, chunk=c, in_dtype=hla.HLA_F32))
+        assert got == want
+    # no tokens: nothing to compute, no pointer needed
+    assert _bcall(_params(n=0), ptrs=(None,) * 7, ws=None, ws_bytes=0) == hla.HLA_OK

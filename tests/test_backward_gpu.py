@@ -1,0 +1,120 @@
+"""GPU parity of the backward pass: dq, dk, dv from the CUDA kernels (through the C
+ABI) against the fp64 oracle's reverse-mode gradient on the same seeded inputs, plus
+a directional-derivative check against the library's own forward.  Tolerance per
+(b,h) relative L2: 1e-4 for fp32 inputs, 2e-2 for bf16 inputs and outputs."""
+import numpy as np
+import pytest
+import torch
+
+import causal_prefix_scan_gb300 as hla
+import oracle
+from causal_prefix_scan_gb300 import workloads as W
+from gpu_helpers import TOL_BF16, TOL_F32, per_pair_errors, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def small(**kw):
+    base = dict(B=1, H=2, n=256, d=64, dv=64, chunk=64, dtype="bf16", qk="l2", seed=31, gamma_lo=0.85,
+                gamma_hi=0.999)
+    base.update(kw)
+    return W.Workload("bwd", **base)
+
+
+def run_backward(x, g, dtype, chunk):
+    q, k, v = (to_dev(x[n], dtype) for n in ("q", "k", "v"))
+    dout = to_dev(g, dtype)
+    gam = None if x.get("gamma") is None else torch.from_numpy(np.asarray(x["gamma"], np.float32)).cuda()
+    dq, dk, dv = hla.backward(q, k, v, dout, chunk=chunk, gamma=gam)
+    hla.hla_sync_status()
+    return tuple(t.float().cpu().numpy() for t in (dq, dk, dv))
+
+
+def run_oracle(x, g):
+    gam = None if x.get("gamma") is None else np.asarray(x["gamma"], np.float64)
+    return oracle.backward(x["q"], x["k"], x["v"], g, gam)
+
+
+def check(got, ref, tol, what):
+    worst = 0.0
+    for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+        assert np.all(np.isfinite(a)), f"{what}: non-finite {name}"
+        e = per_pair_errors(a, b).max()
+        assert e <= tol, f"{what}: {name} max per-(b,h) rel L2 {e:.3e} > {tol}"
+        worst = max(worst, float(e))
+    return worst
+
+
+@pytest.mark.parametrize("d,dv,chunk,n", [(16, 32, 16, 100), (32, 32, 32, 33), (64, 64, 64, 130),
+                                          (64, 16, 16, 7), (16, 64, 64, 200), (32, 16, 32, 1), (64, 32, 32, 96)])
+@pytest.mark.parametrize("decay", [False, True])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_backward_shapes(d, dv, chunk, n, decay, dtype):
+    w = small(d=d, dv=dv, chunk=chunk, n=n, decay=decay, dtype=dtype)
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    got = run_backward(x, g, dtype, chunk)
+    check(got, run_oracle(x, g), TOL_F32 if dtype == "f32" else TOL_BF16,
+          f"bwd {dtype} d{d} dv{dv} c{chunk} n{n} decay={decay}")
+
+
+def test_backward_many_pairs_and_chunks():
+    # several (b,h) pairs with distinct decay rates, many chunks, ragged tail
+    w = small(B=2, H=3, n=16 * 21 + 5, d=32, dv=64, chunk=16, decay=True, dtype="f32")
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    check(run_backward(x, g, "f32", 16), run_oracle(x, g), TOL_F32, "bwd B2H3 many chunks")
+
+
+def test_backward_chunk_lengths_agree():
+    w = small(n=192, d=32, dv=32, dtype="f32", decay=True)
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    res = [run_backward(x, g, "f32", c) for c in (16, 32, 64)]
+    for other in res[1:]:
+        for a, b in zip(res[0], other):
+            assert per_pair_errors(a, b).max() <= 1e-5
+
+
+def test_backward_is_gradient_of_forward():
+    """<dq, e_q> + <dk, e_k> + <dv, e_v> equals the derivative in s of
+    f(s) = sum(dout * forward(q + s e_q, k + s e_k, v + s e_v)), with the library's
+    fp32 forward.  Along a line the output is a polynomial of degree 5 in s (q enters
+    twice, k twice, v once), so the seven-point central difference, exact for degree
+    <= 6, leaves only rounding error."""
+    w = small(n=80, d=16, dv=16, chunk=16, dtype="f32", decay=True, qk="scaled")
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    rng = np.random.default_rng(5)
+    dirs = [rng.standard_normal(x[n].shape).astype(np.float32) for n in ("q", "k", "v")]
+    dq, dk, dv = run_backward(x, g, "f32", 16)
+    want = sum(float(np.sum(a.astype(np.float64) * e)) for a, e in zip((dq, dk, dv), dirs))
+    gam = torch.from_numpy(x["gamma"]).cuda()
+    gd = to_dev(g, "f32").double()
+
+    def f(s):
+        q, k, v = (to_dev(x[n] + s * e, "f32") for n, e in zip(("q", "k", "v"), dirs))
+        o = hla.forward(q, k, v, chunk=16, gamma=gam)
+        hla.hla_sync_status()
+        return float((o.double() * gd).sum())
+
+    s = 0.1
+    F = {j: f(j * s) for j in (-3, -2, -1, 1, 2, 3)}
+    fd = (45 * (F[1] - F[-1]) - 9 * (F[2] - F[-2]) + (F[3] - F[-3])) / (60 * s)
+    assert abs(fd - want) <= 1e-3 * abs(want), (fd, want)
+
+
+def test_backward_empty_sequence():
+    q = torch.empty((1, 2, 0, 32), device="cuda")
+    v = torch.empty((1, 2, 0, 32), device="cuda")
+    dq, dk, dv = hla.backward(q, q, v, v, chunk=32)
+    hla.hla_sync_status()
+    assert dq.shape == q.shape and dv.shape == v.shape
+
+
+def test_backward_full_workload():
+    w = W.BWD_BF16
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    err = check(run_backward(x, g, w.dtype, w.chunk), run_oracle(x, g), TOL_BF16, w.name)
+    print(f"{w.name}: max per-(b,h) rel L2 {err:.3e}")
