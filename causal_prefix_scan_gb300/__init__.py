@@ -28,14 +28,14 @@ __all__ = [
     "HlaError", "hla_params", "hla_state", "library", "EXPORTS",
     "hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combine", "hla_decode_step",
     "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
-    "hla_backward_workspace_size", "hla_backward_chunked",
+    "hla_backward_workspace_size", "hla_backward_chunked", "hla_backward_chunked_traced",
     "State", "new_workspace", "forward", "state_combine", "decode_step", "backward",
 ]
 
 # Every symbol include/hla.h declares.
 EXPORTS = ("hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combine", "hla_decode_step",
            "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
-           "hla_backward_workspace_size", "hla_backward_chunked")
+           "hla_backward_workspace_size", "hla_backward_chunked", "hla_backward_chunked_traced")
 
 
 class HlaError(RuntimeError):
@@ -80,9 +80,11 @@ def library(path: str | None = None):
     lib.hla_backward_workspace_size.argtypes = [P]
     lib.hla_backward_workspace_size.restype = sz
     lib.hla_backward_chunked.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.hla_backward_chunked_traced.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp,
+                                                ctypes.POINTER(ctypes.c_void_p)]
     lib.hla_sync_status.argtypes = [vp]
     for fn in (lib.hla_forward_chunked, lib.hla_state_combine, lib.hla_decode_step, lib.hla_sync_status,
-               lib.hla_backward_chunked):
+               lib.hla_backward_chunked, lib.hla_backward_chunked_traced):
         fn.restype = ctypes.c_int
     lib.hla_status_string.argtypes = [ctypes.c_int]
     lib.hla_status_string.restype = ctypes.c_char_p
@@ -171,6 +173,20 @@ def hla_backward_chunked(params: hla_params, q, k, v, dout, dq, dk, dv, workspac
                          stream=None) -> None:
     _check(library().hla_backward_chunked(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq),
                                           _ptr(dk), _ptr(dv), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def hla_backward_chunked_traced(params: hla_params, q, k, v, dout, dq, dk, dv, workspace, workspace_bytes: int,
+                                stream=None, events=None) -> None:
+    """hla_backward_chunked recording four events (torch.cuda.Event that have been
+    recorded once, or raw cudaEvent_t ints) at its phase boundaries."""
+    arr = None
+    if events is not None:
+        hs = [e if isinstance(e, int) else e.cuda_event for e in events]
+        assert len(hs) == 4 and all(hs), "four created events are needed"
+        arr = (ctypes.c_void_p * 4)(*hs)
+    _check(library().hla_backward_chunked_traced(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace_bytes,
+                                                 _stream(stream), arr))
 
 
 def hla_sync_status(stream=None) -> None:

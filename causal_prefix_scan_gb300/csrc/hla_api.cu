@@ -194,6 +194,12 @@ size_t hla_backward_workspace_size(const hla_params *p) {
 hla_status hla_backward_chunked(const hla_params *p, const void *q, const void *k, const void *v, const void *dout,
                                 void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
                                 void *stream) {
+    return hla_backward_chunked_traced(p, q, k, v, dout, dq, dk, dv, workspace, workspace_bytes, stream, nullptr);
+}
+
+hla_status hla_backward_chunked_traced(const hla_params *p, const void *q, const void *k, const void *v,
+                                       const void *dout, void *dq, void *dk, void *dv, void *workspace,
+                                       size_t workspace_bytes, void *stream, void *const *phase_events) {
     hla_status s = check_bwd_params(p);
     if (s != HLA_OK) return s;
     if (p->n == 0) return HLA_OK;
@@ -212,6 +218,11 @@ hla_status hla_backward_chunked(const hla_params *p, const void *q, const void *
     a.q = q; a.k = k; a.v = v; a.go = dout;
     a.grad_q = dq; a.grad_k = dk; a.grad_v = dv;
     a.workspace = static_cast<float *>(workspace);
+    if (phase_events) {
+        for (int i = 0; i < 4; ++i)
+            if (!phase_events[i]) return fail(HLA_ERR_ARG, "phase_events must hold four events");
+    }
+    a.events = reinterpret_cast<cudaEvent_t const *>(phase_events);
     cudaError_t e = hla::bwd_simt_launch(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return HLA_OK;

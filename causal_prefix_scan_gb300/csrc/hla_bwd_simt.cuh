@@ -475,9 +475,14 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t st) {
     if ((e = smem_attr(bwd_local_kernel<T, C, D, DV>, b1)) != cudaSuccess) return e;
     if ((e = smem_attr(bwd_scan_kernel<C, D, DV>, b2)) != cudaSuccess) return e;
     if ((e = smem_attr(bwd_grad_kernel<T, C, D, DV>, b3)) != cudaSuccess) return e;
+    auto mark = [&](int i) { return a.events ? cudaEventRecord(a.events[i], st) : cudaSuccess; };
+    if ((e = mark(0)) != cudaSuccess) return e;
     bwd_local_kernel<T, C, D, DV><<<units * nch, kThreads, b1, st>>>(a);
+    if ((e = mark(1)) != cudaSuccess) return e;
     bwd_scan_kernel<C, D, DV><<<units * kSplit * 2, kThreads, b2, st>>>(a);
+    if ((e = mark(2)) != cudaSuccess) return e;
     bwd_grad_kernel<T, C, D, DV><<<units * nch, kThreads, b3, st>>>(a);
+    if ((e = mark(3)) != cudaSuccess) return e;
     return cudaGetLastError();
 }
 template <typename T, int C, int D>

@@ -73,6 +73,7 @@ struct BwdArgs {
     const void *q, *k, *v, *go;    // inputs and the gradient of the output
     void *grad_q, *grad_k, *grad_v;  // outputs
     float *workspace;
+    cudaEvent_t const *events;  // NULL or four events recorded at the phase boundaries
 };
 
 // Backward of the masked forward on CUDA cores (d, dv, chunk in {16,32,64}).

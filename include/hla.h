@@ -212,6 +212,15 @@ HLA_API hla_status hla_backward_chunked(const hla_params *p, const void *q, cons
                                         const void *dout, void *dq, void *dk, void *dv, void *workspace,
                                         size_t workspace_bytes, void *stream);
 
+/* hla_backward_chunked with per-phase tracing: phase_events is NULL (then this is
+ * hla_backward_chunked) or four cudaEvent_t handles of the current device, recorded
+ * on `stream` before the local-sums kernel, after it, after the scan kernel and
+ * after the gradient kernel.  The caller owns the events (created with timing
+ * enabled to read elapsed times).  With n == 0 no event is recorded. */
+HLA_API hla_status hla_backward_chunked_traced(const hla_params *p, const void *q, const void *k, const void *v,
+                                               const void *dout, void *dq, void *dk, void *dv, void *workspace,
+                                               size_t workspace_bytes, void *stream, void *const *phase_events);
+
 /* Synchronise `stream`, then report and clear the sticky device flag: HLA_OK,
  * HLA_ERR_TIMEOUT if a bounded device wait expired since the last call, or
  * HLA_ERR_CUDA if the stream reported an error. */

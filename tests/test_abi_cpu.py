@@ -172,3 +172,11 @@ def test_backward_workspace_size_and_empty_sequence(lib):
         assert got == want
     # no tokens: nothing to compute, no pointer needed
     assert _bcall(_params(n=0), ptrs=(None,) * 7, ws=None, ws_bytes=0) == hla.HLA_OK
+
+
+def test_backward_traced_rejects_missing_events(lib):
+    p = _params()
+    ev = (ctypes.c_void_p * 4)(16, 16, None, 16)
+    assert hla.library().hla_backward_chunked_traced(ctypes.byref(p), 16, 16, 16, 16, 16, 16, 16, 16, 1 << 40, None,
+                                                     ev) == hla.HLA_ERR_ARG
+    assert "event" in hla.hla_last_error()
