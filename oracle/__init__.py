@@ -27,7 +27,12 @@ its five summaries, a closed form for constant inputs, chunk invariance, associa
 of its concatenation rule, concatenation equal to the joined sequence, resume and
 decode continuation.  The backward pass (reverse mode of the masked recurrence; the
 pages give no gradient formulas) is pinned by central finite differences of the
-forward and by the gradient of the dense masked-matrix form.
+forward and by the gradient of the dense masked-matrix form.  The masked third-order
+output (``forward3``, section 3 "Derde-orde HLA"; the pages print no formula) is
+pinned by its brute-force quadruple-index sum, the dense form
+[(L o ((L o A)(L o A)^T))(L o A)]V, brute-force definitions of its cross summaries
+and segment maps, a closed form for constant inputs, chunk invariance of the
+segment-map scan, associativity of its concatenation and resume.
 """
 from __future__ import annotations
 
@@ -40,6 +45,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "hla_oracle.c")
+_SRC3 = os.path.join(_HERE, "hla_oracle3.c")
 _LIB_DIR = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_LIB_DIR, "libhla_oracle.so")
 
@@ -47,12 +53,14 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile hla_oracle.c into a shared library (gcc, -O2, no fast-math)."""
+    """Compile hla_oracle.c and hla_oracle3.c into one shared library (gcc, -O2, no
+    fast-math)."""
     os.makedirs(_LIB_DIR, exist_ok=True)
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC3))
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(
-            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"])
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, _SRC3, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -69,8 +77,11 @@ def _load():
         _lib.hla_oracle_decode_step.argtypes = [i] * 6 + [dp, i, d] + [dp] * 5 + [dp, dp, dp, dp, i]
         _lib.hla_oracle_combine.argtypes = [i, i, i, i] + [dp] * 10 + [dp] + [dp] * 5
         _lib.hla_oracle_backward.argtypes = [i] * 5 + [dp] * 8 + [i]
+        _lib.hla_oracle3_forward.argtypes = [i] * 6 + [dp] * 6 + [i]
+        _lib.hla_oracle3_combine.argtypes = [i, i, i, dp, dp, dp]
         for f in (_lib.hla_oracle_forward, _lib.hla_oracle_forward_chunked,
-                  _lib.hla_oracle_decode_step, _lib.hla_oracle_combine, _lib.hla_oracle_backward):
+                  _lib.hla_oracle_decode_step, _lib.hla_oracle_combine, _lib.hla_oracle_backward,
+                  _lib.hla_oracle3_forward, _lib.hla_oracle3_combine):
             f.restype = ctypes.c_int
     return _lib
 
@@ -224,3 +235,62 @@ def backward(q, k, v, go, gamma=None, nthreads=None):
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return dq, dk, dvv
+
+
+# ------------------------------------------------------------------ third order
+STATE3_FIELDS = ("SK", "SQ", "Z1", "MKQ", "P", "Z2", "G1", "G2", "G3", "T", "MQP")
+
+
+def _state3_shapes(units, d, dv):
+    return {n: (units, d, d) if n in ("SK", "SQ", "Z1", "MKQ") else (units, d, dv) for n in STATE3_FIELDS}
+
+
+def state3_pack(st: dict, units, d, dv) -> np.ndarray:
+    """dict of the eleven third-order arrays -> [units][4d^2 + 7 d dv] in the C layout."""
+    shp = _state3_shapes(units, d, dv)
+    parts = [np.asarray(st[n], np.float64).reshape(shp[n]).reshape(units, -1) for n in STATE3_FIELDS]
+    return np.ascontiguousarray(np.concatenate(parts, axis=1))
+
+
+def state3_unpack(buf: np.ndarray, units, d, dv) -> dict:
+    shp = _state3_shapes(units, d, dv)
+    out, off = {}, 0
+    for n in STATE3_FIELDS:
+        w = int(np.prod(shp[n][1:]))
+        out[n] = buf[:, off:off + w].reshape(shp[n]).copy()
+        off += w
+    return out
+
+
+def forward3(q, k, v, state_in=None, chunk=None, want_state=True, nthreads=None):
+    """Masked third-order HLA forward in fp64 (hla_oracle3.c): o_t = q_t^T T_t with
+    T_t = S^K S^Q P - G1 - G2 + G3.  q, k: [B,H,n,d]; v: [B,H,n,dv].  chunk=None runs
+    the serial recurrence in the moments and cross summaries; chunk=c the chunked scan
+    over segment summaries (S^K, S^Q, P, T, M^QP, M^KQ; the other fields come back NaN).
+    state_in / the returned state: dict with the fields of STATE3_FIELDS, each
+    [B*H, d, d] or [B*H, d, dv] (T is derived and ignored on input).
+    Returns (o [B,H,n,dv], state or None)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, n, d = q.shape
+    dv = v.shape[-1]
+    assert k.shape == q.shape and v.shape == (B, H, n, dv)
+    units = B * H
+    sin = state3_pack(state_in, units, d, dv) if state_in is not None else None
+    sout = np.zeros((units, 4 * d * d + 7 * d * dv)) if want_state else None
+    o = np.zeros((B, H, n, dv))
+    rc = _load().hla_oracle3_forward(B, H, n, d, dv, int(chunk or 0), _p(q), _p(k), _p(v), _p(sin), _p(o), _p(sout),
+                                     nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return o, (state3_unpack(sout, units, d, dv) if want_state else None)
+
+
+def combine3(A: dict, Bst: dict) -> dict:
+    """Concatenation of third-order segment summaries (A before B) for every item."""
+    units, d, dv = np.asarray(A["P"]).shape
+    a, b = state3_pack(A, units, d, dv), state3_pack(Bst, units, d, dv)
+    out = np.zeros_like(a)
+    rc = _load().hla_oracle3_combine(units, d, dv, _p(a), _p(b), _p(out))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return state3_unpack(out, units, d, dv)
