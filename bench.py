@@ -49,6 +49,8 @@ FWD_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd
 DECODE_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_decode.cu")
 BWD_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_bwd_simt.cuh")
 BWD_METRIC = "masked 2nd-order HLA backward (dq, dk, dv) tokens/s and % roofline on 1 GB300"
+FWD3_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd3_simt.cuh")
+FWD3_METRIC = "masked 3rd-order HLA forward tokens/s and % roofline on 1 GB300"
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz (maximum SM clock)
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2070e6 / 1e12
 
@@ -286,6 +288,30 @@ def cpu_baseline_backward(w: W.Workload, x, g):
                       f"tokens of the same inputs, threads over (b,h); mean of {reps} run(s)", "seconds": secs}
 
 
+def oracle3_rate(x, batch_rows: int, n_tokens: int, nthreads: int):
+    import oracle
+    sl = lambda a: np.ascontiguousarray(a[:batch_rows, :, :n_tokens], dtype=np.float64)
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.forward3(sl(x["q"]), sl(x["k"]), sl(x["v"]), nthreads=nthreads)
+    return time.perf_counter() - t0, batch_rows * n_tokens
+
+
+def cpu_baseline_third(w: W.Workload, x):
+    """The third-order oracle (serial recurrence) on the first batch rows, all heads and
+    tokens, repeated to about 10 s."""
+    cores = cpu_threads()
+    rows = max(1, min(w.B, -(-cores // w.H)))
+    used = min(cores, rows * w.H)
+    secs, toks = oracle3_rate(x, rows, w.n, used)
+    reps = max(1, min(500, int(10.0 / max(secs, 1e-9))))
+    if reps > 1:
+        secs = (secs + sum(oracle3_rate(x, rows, w.n, used)[0] for _ in range(reps - 1))) / reps
+    return {"value": toks / secs, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"fp64 serial third-order recurrence over {rows} of {w.B} batch row(s) x {w.H} heads x {w.n} "
+                      f"tokens of the same inputs, threads over (b,h); mean of {reps} run(s)", "seconds": secs}
+
+
 # ----------------------------------------------------------------- forward bench
 def workload_by_name(name: str):
     if name in W.WORKLOADS:
@@ -460,45 +486,83 @@ def bench_forward(args, w: W.Workload, rank, world, local, dist):
     return line
 
 
-# ----------------------------------------------------------------- backward bench
-def bench_backward(args, w: W.Workload, rank, world, local, dist):
-    """A step is one hla_backward_chunked call (three kernels: local sums, scan,
-    gradients) over the whole batch.  The steps are launched eagerly with events at
-    the phase boundaries (hla_backward_chunked_traced), so every kernel's duration is
-    measured inside the timed region."""
+# ----------------------------------------------------------------- multi-kernel benches
+def fwd3_flops_per_token_head(w: W.Workload) -> dict:
+    """Algorithmic fp32 flops per token-head of each third-order kernel (an FMA is 2
+    flops; triangular chunk products at half).  Local sums: A~, A~K, A~V at half and
+    K^T K, Q^T Q, U^T Q, K^T V, U^T W, Q^T W; scan: S^Q P, S^K X, M^KQ P per chunk;
+    outputs: A~, A~K, A~V, Q U^T, M W at half and Q S^K, Q P, Q T in full."""
+    c, d, dv = w.chunk, w.d, w.dv
+    return {"fwd3_local_kernel": c * (2 * d + dv) + 6 * d * d + 6 * d * dv,
+            "fwd3_scan_kernel": 6 * d * d * dv / c,
+            "fwd3_out_kernel": c * (3 * d + 2 * dv) + 2 * d * d + 4 * d * dv}
+
+
+def is_backward(w) -> bool:
+    return isinstance(w, W.Workload) and w.name.startswith("bwd_")
+
+
+def is_third(w) -> bool:
+    return isinstance(w, W.Workload) and w.name.startswith("fwd3_")
+
+
+def bench_phased(args, w: W.Workload, rank, world, local, dist):
+    """The backward pass or the third-order forward: a step is one library call
+    (three kernels: local sums, scan over chunks, per-chunk results) over the whole
+    batch.  Steps are launched eagerly with events at the phase boundaries (the
+    *_traced entry points), so every kernel's duration is measured inside the timed
+    region."""
     import torch
     import causal_prefix_scan_gb300 as hla
     from causal_prefix_scan_gb300 import _build
     _build.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    bwd = is_backward(w)
     x = W.make_inputs(w)
-    gout = W.make_dout(w)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    in_names = ("q", "k", "v", "dout") if bwd else ("q", "k", "v")
     host = {k: torch.from_numpy(x[k]).to(tdt).pin_memory() for k in ("q", "k", "v")}
-    host["dout"] = torch.from_numpy(gout).to(tdt).pin_memory()
+    gout = None
+    if bwd:
+        gout = W.make_dout(w)
+        host["dout"] = torch.from_numpy(gout).to(tdt).pin_memory()
     gamma = torch.from_numpy(x["gamma"]).to(dev) if x["gamma"] is not None else None
     esz = 2 if w.dtype == "bf16" else 4
-    set_bytes = w.token_heads * (3 * w.d + 3 * w.dv) * esz
+    set_bytes = w.token_heads * ((3 * w.d + 3 * w.dv) if bwd else (2 * w.d + 2 * w.dv)) * esz
     nsets = max(2, min(16, -(-2 * L2_BYTES // set_bytes)))
     sets = []
     for _ in range(nsets):
-        ins = tuple(host[n].to(dev, non_blocking=True) for n in ("q", "k", "v", "dout"))
-        outs = (torch.empty_like(ins[0]), torch.empty_like(ins[1]), torch.empty_like(ins[2]))
-        sets.append(ins + outs)
-    params = hla.make_params(sets[0][0], sets[0][2], w.chunk, gamma)
-    ws_bytes = hla.hla_backward_workspace_size(params)
+        ins = tuple(host[n].to(dev, non_blocking=True) for n in in_names)
+        outs = (torch.empty_like(ins[0]), torch.empty_like(ins[1]), torch.empty_like(ins[2])) if bwd else \
+            (torch.empty(ins[0].shape[:3] + (w.dv,), dtype=tdt, device=dev),)
+        sets.append((ins, outs))
+    if bwd:
+        params = hla.make_params(sets[0][0][0], sets[0][0][2], w.chunk, gamma)
+        ws_bytes = hla.hla_backward_workspace_size(params)
+        names = ("bwd_local_kernel", "bwd_scan_kernel", "bwd_grad_kernel")
+        fl = bwd_flops_per_token_head(w)
+        src, metric = BWD_KERNEL_SRC, BWD_METRIC
+    else:
+        params = hla.make_params(sets[0][0][0], sets[0][0][2], w.chunk)
+        ws_bytes = hla.hla_forward3_workspace_size(params)
+        names = ("fwd3_local_kernel", "fwd3_scan_kernel", "fwd3_out_kernel")
+        fl = fwd3_flops_per_token_head(w)
+        src, metric = FWD3_KERNEL_SRC, FWD3_METRIC
+        st3 = hla.State3.empty(w.B * w.H, w.d, w.dv, device=dev)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def step(i, events=None):
-        q, k, v, do, dq, dk, dv = sets[i % nsets]
-        hla.hla_backward_chunked_traced(params, q, k, v, do, dq, dk, dv, ws, ws_bytes, stream, events)
+    def call(ins, outs, s, events=None):
+        if bwd:
+            hla.hla_backward_chunked_traced(params, *ins, *outs, ws, ws_bytes, s, events)
+        else:
+            hla.hla_forward3_chunked_traced(params, *ins, outs[0], None, st3, ws, ws_bytes, s, events)
 
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            step(i)
+            call(*sets[i % nsets], stream)
     hla.hla_sync_status(stream)
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
@@ -512,7 +576,7 @@ def bench_backward(args, w: W.Workload, rank, world, local, dist):
     with ClockSampler(gpu_selector(local)) as clk, torch.cuda.stream(stream):
         ev0.record(stream)
         for i in range(K):
-            step(i, evs[i])
+            call(*sets[i % nsets], stream, evs[i])
         ev1.record(stream)
         stream.synchronize()
     torch.cuda.synchronize()
@@ -521,35 +585,34 @@ def bench_backward(args, w: W.Workload, rank, world, local, dist):
     t_max = max_over_ranks(dist, ev0.elapsed_time(ev1))
     ms_per_step = t_max / K
     value = world * w.tokens * K / (t_max / 1e3)
-    names = ("bwd_local_kernel", "bwd_scan_kernel", "bwd_grad_kernel")
     phase_ms = {nm: sum(e4[j].elapsed_time(e4[j + 1]) for e4 in evs) / K for j, nm in enumerate(names)}
 
-    # ---- end to end: q, k, v, dout uploaded and dq, dk, dv read back every step;
+    # ---- end to end: the inputs uploaded and the results read back every step;
     # step i+1's upload and step i-1's download overlap step i (two buffer sets)
     Ke = min(K, 100)
-    outs_host = [[torch.empty(t.shape, dtype=tdt).pin_memory() for t in sets[0][4:]] for _ in range(2)]
+    outs_host = [[torch.empty(t.shape, dtype=tdt).pin_memory() for t in sets[0][1]] for _ in range(2)]
     s_up, s_down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev = {kk: [torch.cuda.Event() for _ in range(2)] for kk in ("up", "bwd", "down")}
+    ev = {kk: [torch.cuda.Event() for _ in range(2)] for kk in ("up", "run", "down")}
 
     def e2e_steps(n):
         for i in range(n):
             b = i % 2
-            q, k, v, do, dq, dk, dv = sets[b]
+            ins, outs = sets[b]
             if i >= 2:
-                s_up.wait_event(ev["bwd"][b])
+                s_up.wait_event(ev["run"][b])
             with torch.cuda.stream(s_up):
-                for dst, n_ in zip((q, k, v, do), ("q", "k", "v", "dout")):
+                for dst, n_ in zip(ins, in_names):
                     dst.copy_(host[n_], non_blocking=True)
             ev["up"][b].record(s_up)
             stream.wait_event(ev["up"][b])
             if i >= 2:
                 stream.wait_event(ev["down"][b])
-            hla.hla_backward_chunked(params, q, k, v, do, dq, dk, dv, ws, ws_bytes, stream)
-            ev["bwd"][b].record(stream)
-            s_down.wait_event(ev["bwd"][b])
+            call(ins, outs, stream)
+            ev["run"][b].record(stream)
+            s_down.wait_event(ev["run"][b])
             with torch.cuda.stream(s_down):
-                for dst, src in zip(outs_host[b], (dq, dk, dv)):
-                    dst.copy_(src, non_blocking=True)
+                for dst, src_ in zip(outs_host[b], outs):
+                    dst.copy_(src_, non_blocking=True)
             ev["down"][b].record(s_down)
         stream.wait_stream(s_up)
         stream.wait_stream(s_down)
@@ -574,29 +637,31 @@ def bench_backward(args, w: W.Workload, rank, world, local, dist):
            "overlap": "upload of step i+1 and download of step i-1 on their own streams during step i"}
 
     # ---- roofline of the dominant kernel: fp32 FMA work on the CUDA cores
-    fl = bwd_flops_per_token_head(w)
     top = max(phase_ms, key=phase_ms.get)
     flops_launch = fl[top] * w.token_heads
     ach = flops_launch / (phase_ms[top] / 1e3) / 1e12
     roofline = {"bound": "alu", "achieved": ach, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
                 "frac": ach / FP32_ALU_TFLOPS,
                 "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz (fp32 FMA, CUDA cores)",
-                "traffic": traffic_for(top, w.name, BWD_KERNEL_SRC), "kernel": top,
+                "traffic": traffic_for(top, w.name, src), "kernel": top,
                 "alg_flops_per_launch": flops_launch,
                 "phases": {nm: {"ms": phase_ms[nm], "alg_flops": fl[nm] * w.token_heads,
                                 "tflops": fl[nm] * w.token_heads / (phase_ms[nm] / 1e3) / 1e12 if phase_ms[nm] else None}
                            for nm in names},
-                "alg_bytes_per_step": bwd_bytes_per_step(w)}
+                "alg_bytes_per_step": set_bytes}
     cfg = config_dict(w, nsets, set_bytes, world)
-    cfg["variant"] = "backward of the masked forward" + (" with decay" if w.decay else "")
-    cfg["inputs"] += f", dout N(0,1) seed {w.seed + 1000}"
-    line = {"metric": BWD_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+    if bwd:
+        cfg["variant"] = "backward of the masked forward" + (" with decay" if w.decay else "")
+        cfg["inputs"] += f", dout N(0,1) seed {w.seed + 1000}"
+    else:
+        cfg["variant"] = "masked third order"
+    line = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": cfg, "roofline": roofline, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clk.summary(),
             "token_heads_per_s": world * w.token_heads * K / (t_max / 1e3)}
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_backward(w, x, gout)
+        line["cpu_baseline"] = cpu_baseline_backward(w, x, gout) if bwd else cpu_baseline_third(w, x)
     return line
 
 
@@ -717,6 +782,8 @@ def bench_reference(args, w, rank, world):
     cores = min(cpu_threads(), w.H)
     if is_backward(w):
         return bench_reference_backward(args, w, x, cores, world)
+    if is_third(w):
+        return bench_reference_third(args, w, x, cores, world)
     secs, _ = oracle_rate(w, x, 1, min(w.n, 128), cores)
     budget = 90.0 / max(1, args.steps + args.warmup)
     n_s = int(max(16, min(w.n, 128 * budget / max(secs, 1e-9))))
@@ -746,8 +813,34 @@ def bench_reference(args, w, rank, world):
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def is_backward(w) -> bool:
-    return isinstance(w, W.Workload) and w.name.startswith("bwd_")
+def bench_reference_third(args, w, x, cores, world):
+    """The third-order oracle on the host cores: each step 1 batch row x H heads x a
+    window of tokens (from a zero state)."""
+    import oracle
+    secs, _ = oracle3_rate(x, 1, min(w.n, 128), cores)
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    n_s = int(max(16, min(w.n, 128 * budget / max(secs, 1e-9))))
+    sl = lambda a, t0: np.ascontiguousarray(a[:1, :, t0:t0 + n_s], dtype=np.float64)
+    offs = list(range(0, max(1, w.n - n_s + 1), max(1, n_s)))
+
+    def one(i):
+        t0 = offs[i % len(offs)]
+        oracle.forward3(sl(x["q"], t0), sl(x["k"], t0), sl(x["v"], t0), nthreads=cores)
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(i)
+    dt = time.perf_counter() - t0
+    value = n_s * args.steps / dt
+    sample = f"fp64 serial third-order recurrence on 1 batch row x {w.H} heads x {n_s}-token windows per step"
+    return {"impl": "reference", "metric": FWD3_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(w, 1, 0, world),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def bench_reference_backward(args, w, x, cores, world):
@@ -803,8 +896,8 @@ def main():
     dist = dist_init(world)
     if isinstance(w, W.DecodeWorkload):
         line = bench_decode(args, w, rank, world, local, dist)
-    elif is_backward(w):
-        line = bench_backward(args, w, rank, world, local, dist)
+    elif is_backward(w) or is_third(w):
+        line = bench_phased(args, w, rank, world, local, dist)
     else:
         line = bench_forward(args, w, rank, world, local, dist)
     if rank == 0:

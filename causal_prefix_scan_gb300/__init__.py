@@ -1,5 +1,6 @@
 """GB300-native second-order Higher-order Linear Attention (HLA): masked, unmasked and
-the asymmetric variant AHLA, and the backward pass of the masked forward.
+the asymmetric variant AHLA, the backward pass of the masked forward, and masked
+third-order HLA (forward and decode).
 
 Thin ctypes binding over the C ABI in ``include/hla.h`` (library
 ``_lib/libhla_gb300.so``, built for sm_103a by ``_build.build()``).  Functions named
@@ -29,13 +30,16 @@ __all__ = [
     "hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combine", "hla_decode_step",
     "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
     "hla_backward_workspace_size", "hla_backward_chunked", "hla_backward_chunked_traced",
+    "hla_state3", "hla_forward3_workspace_size", "hla_forward3_chunked", "hla_forward3_chunked_traced",
+    "hla_decode3_step", "State3", "forward3", "decode3_step",
     "State", "new_workspace", "forward", "state_combine", "decode_step", "backward",
 ]
 
 # Every symbol include/hla.h declares.
 EXPORTS = ("hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combine", "hla_decode_step",
            "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
-           "hla_backward_workspace_size", "hla_backward_chunked", "hla_backward_chunked_traced")
+           "hla_backward_workspace_size", "hla_backward_chunked", "hla_backward_chunked_traced",
+           "hla_forward3_workspace_size", "hla_forward3_chunked", "hla_forward3_chunked_traced", "hla_decode3_step")
 
 
 class HlaError(RuntimeError):
@@ -54,6 +58,10 @@ class hla_params(ctypes.Structure):
 class hla_state(ctypes.Structure):
     _fields_ = [("S", ctypes.c_void_p), ("C", ctypes.c_void_p), ("m", ctypes.c_void_p),
                 ("G", ctypes.c_void_p), ("h", ctypes.c_void_p)]
+
+
+class hla_state3(ctypes.Structure):
+    _fields_ = [("S", ctypes.c_void_p), ("P", ctypes.c_void_p), ("T", ctypes.c_void_p)]
 
 
 _lib = None
@@ -82,9 +90,17 @@ def library(path: str | None = None):
     lib.hla_backward_chunked.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.hla_backward_chunked_traced.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp,
                                                 ctypes.POINTER(ctypes.c_void_p)]
+    S3 = ctypes.POINTER(hla_state3)
+    lib.hla_forward3_workspace_size.argtypes = [P]
+    lib.hla_forward3_workspace_size.restype = sz
+    lib.hla_forward3_chunked.argtypes = [P, vp, vp, vp, vp, S3, S3, vp, sz, vp]
+    lib.hla_forward3_chunked_traced.argtypes = [P, vp, vp, vp, vp, S3, S3, vp, sz, vp,
+                                                ctypes.POINTER(ctypes.c_void_p)]
+    lib.hla_decode3_step.argtypes = [i, i, i, i, S3, vp, vp, vp, vp, vp]
     lib.hla_sync_status.argtypes = [vp]
     for fn in (lib.hla_forward_chunked, lib.hla_state_combine, lib.hla_decode_step, lib.hla_sync_status,
-               lib.hla_backward_chunked, lib.hla_backward_chunked_traced):
+               lib.hla_backward_chunked, lib.hla_backward_chunked_traced, lib.hla_forward3_chunked,
+               lib.hla_forward3_chunked_traced, lib.hla_decode3_step):
         fn.restype = ctypes.c_int
     lib.hla_status_string.argtypes = [ctypes.c_int]
     lib.hla_status_string.restype = ctypes.c_char_p
@@ -189,6 +205,44 @@ def hla_backward_chunked_traced(params: hla_params, q, k, v, dout, dq, dk, dv, w
                                                  _stream(stream), arr))
 
 
+def _state3_struct(st):
+    if st is None:
+        return None
+    return ctypes.byref(hla_state3(*(_ptr(x) for x in (st.S, st.P, st.T))))
+
+
+def _events(events):
+    if events is None:
+        return None
+    hs = [e if isinstance(e, int) else e.cuda_event for e in events]
+    assert len(hs) == 4 and all(hs), "four created events are needed"
+    return (ctypes.c_void_p * 4)(*hs)
+
+
+def hla_forward3_workspace_size(params: hla_params) -> int:
+    return library().hla_forward3_workspace_size(ctypes.byref(params))
+
+
+def hla_forward3_chunked(params: hla_params, q, k, v, o, state_in=None, state_out=None, workspace=None,
+                         workspace_bytes: int = 0, stream=None) -> None:
+    _check(library().hla_forward3_chunked(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                          _state3_struct(state_in), _state3_struct(state_out), _ptr(workspace),
+                                          workspace_bytes, _stream(stream)))
+
+
+def hla_forward3_chunked_traced(params: hla_params, q, k, v, o, state_in=None, state_out=None, workspace=None,
+                                workspace_bytes: int = 0, stream=None, events=None) -> None:
+    _check(library().hla_forward3_chunked_traced(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                                 _state3_struct(state_in), _state3_struct(state_out),
+                                                 _ptr(workspace), workspace_bytes, _stream(stream),
+                                                 _events(events)))
+
+
+def hla_decode3_step(N: int, d: int, dv: int, dtype: int, state, q, k, v, o, stream=None) -> None:
+    _check(library().hla_decode3_step(N, d, dv, dtype, _state3_struct(state), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                      _stream(stream)))
+
+
 def hla_sync_status(stream=None) -> None:
     _check(library().hla_sync_status(_stream(stream)))
 
@@ -217,6 +271,27 @@ class State:
 
     def astuple(self):
         return (self.S, self.C, self.m, self.G, self.h)
+
+
+@dataclass
+class State3:
+    """Third-order streaming state of `units` pairs, fp32: S [U,d,d] (key moment S^K),
+    P [U,d,dv] (key-value moment), T [U,d,dv] (masked third-order accumulator)."""
+    S: object
+    P: object
+    T: object
+
+    @staticmethod
+    def empty(units: int, d: int, dv: int, device="cuda") -> "State3":
+        import torch
+        z = lambda *s: torch.empty(*s, dtype=torch.float32, device=device)
+        return State3(z(units, d, d), z(units, d, dv), z(units, d, dv))
+
+    @staticmethod
+    def zeros(units: int, d: int, dv: int, device="cuda") -> "State3":
+        import torch
+        z = lambda *s: torch.zeros(*s, dtype=torch.float32, device=device)
+        return State3(z(units, d, d), z(units, d, dv), z(units, d, dv))
 
 
 def _dtype_code(t) -> int:
@@ -303,3 +378,28 @@ def backward(q, k, v, dout, chunk: int, gamma=None, workspace=None, out=None, st
     dq, dk, dv = out if out is not None else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     hla_backward_chunked(p, q, k, v, dout, dq, dk, dv, workspace, need if workspace is not None else 0, stream)
     return dq, dk, dv
+
+
+def forward3(q, k, v, chunk: int, state_in: State3 | None = None, return_state: bool = False, out=None,
+             workspace=None, stream=None):
+    """Masked third-order HLA forward.  q, k [B,H,n,d], v [B,H,n,dv] contiguous CUDA
+    tensors (bf16 or fp32).  Returns o (and the final State3)."""
+    import torch
+    p = make_params(q, v, chunk)
+    o = out if out is not None else torch.empty(q.shape[:3] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    need = hla_forward3_workspace_size(p)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = State3.empty(p.B * p.H, p.d, p.dv, device=q.device) if return_state else None
+    hla_forward3_chunked(p, q, k, v, o, state_in, st, workspace, need if workspace is not None else 0, stream)
+    return (o, st) if return_state else o
+
+
+def decode3_step(state: State3, q, k, v, out=None, stream=None):
+    """One third-order decode step for N pairs (q, k [N,d], v [N,dv]); state updated in place."""
+    import torch
+    N, d = q.shape
+    dv = v.shape[-1]
+    o = out if out is not None else torch.empty((N, dv), dtype=q.dtype, device=q.device)
+    hla_decode3_step(N, d, dv, _dtype_code(q), state, q, k, v, o, stream)
+    return o

@@ -228,6 +228,119 @@ hla_status hla_backward_chunked_traced(const hla_params *p, const void *q, const
     return HLA_OK;
 }
 
+namespace {
+hla_status check_fwd3_params(const hla_params *p) {
+    if (!p) return fail(HLA_ERR_ARG, "params is NULL");
+    if (p->B < 1 || p->H < 1 || p->n < 0) return fail(HLA_ERR_ARG, "need B >= 1, H >= 1, n >= 0");
+    if (p->in_dtype != HLA_F32 && p->in_dtype != HLA_BF16) return fail(HLA_ERR_ARG, "unknown in_dtype");
+    if (p->flags & ~(unsigned)(HLA_NORMALIZE | HLA_DECAY | HLA_UNMASKED | HLA_ASYMMETRIC))
+        return fail(HLA_ERR_ARG, "unknown flag bits");
+    if (p->Hkv < 0 || (p->Hkv > 0 && p->H % p->Hkv != 0))
+        return fail(HLA_ERR_ARG, "Hkv must divide H (0 means Hkv = H)");
+    if ((long long)p->B * p->H * (long long)p->n * (p->d > p->dv ? p->d : p->dv) > (1LL << 40))
+        return fail(HLA_ERR_ARG, "problem too large");
+    if (!hla::fwd3_supported(*p))
+        return fail(HLA_ERR_UNSUPPORTED,
+                    "third order supports flags 0, Hkv = H, d, dv, chunk in {16,32,64} "
+                    "(got flags=%u Hkv=%d d=%d dv=%d chunk=%d)",
+                    p->flags, p->Hkv, p->d, p->dv, p->chunk);
+    return HLA_OK;
+}
+
+hla_status check_state3(const hla_state3 *s, const char *name) {
+    if (!s) return HLA_OK;
+    if (!s->S || !s->P || !s->T) return fail(HLA_ERR_ARG, "%s: all three pointers must be set", name);
+    if (!aligned16(s->S) || !aligned16(s->P) || !aligned16(s->T))
+        return fail(HLA_ERR_ARG, "%s: pointers must be 16-byte aligned", name);
+    return HLA_OK;
+}
+}  // namespace
+
+size_t hla_forward3_workspace_size(const hla_params *p) {
+    if (check_fwd3_params(p) != HLA_OK) return 0;
+    return hla::fwd3_workspace(*p);
+}
+
+hla_status hla_forward3_chunked(const hla_params *p, const void *q, const void *k, const void *v, void *o,
+                                const hla_state3 *state_in, const hla_state3 *state_out, void *workspace,
+                                size_t workspace_bytes, void *stream) {
+    return hla_forward3_chunked_traced(p, q, k, v, o, state_in, state_out, workspace, workspace_bytes, stream,
+                                       nullptr);
+}
+
+hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const void *k, const void *v, void *o,
+                                       const hla_state3 *state_in, const hla_state3 *state_out, void *workspace,
+                                       size_t workspace_bytes, void *stream, void *const *phase_events) {
+    hla_status s = check_fwd3_params(p);
+    if (s != HLA_OK) return s;
+    if ((s = check_state3(state_in, "state_in")) != HLA_OK) return s;
+    if ((s = check_state3(state_out, "state_out")) != HLA_OK) return s;
+    if (state_in && state_out && (state_in->S == state_out->S || state_in->P == state_out->P || state_in->T == state_out->T))
+        return fail(HLA_ERR_ARG, "state_out may not alias state_in");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (p->n == 0) {  // no tokens: state_out = state_in (or zeros)
+        if (!state_out) return HLA_OK;
+        const size_t BH = (size_t)p->B * p->H, D = p->d, DV = p->dv;
+        const size_t sz[3] = {BH * D * D * 4, BH * D * DV * 4, BH * D * DV * 4};
+        float *dst[3] = {state_out->S, state_out->P, state_out->T};
+        for (int i = 0; i < 3; ++i) {
+            cudaError_t e;
+            if (state_in) {
+                const float *src[3] = {state_in->S, state_in->P, state_in->T};
+                e = cudaMemcpyAsync(dst[i], src[i], sz[i], cudaMemcpyDeviceToDevice, st);
+            } else {
+                e = cudaMemsetAsync(dst[i], 0, sz[i], st);
+            }
+            if (e != cudaSuccess) return cuda_fail(e, "state copy");
+        }
+        return HLA_OK;
+    }
+    if (!q || !k || !v || !o) return fail(HLA_ERR_ARG, "q, k, v, o must be set when n > 0");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return fail(HLA_ERR_ARG, "q, k, v, o must be 16-byte aligned");
+    const size_t need = hla::fwd3_workspace(*p);
+    if (!workspace || workspace_bytes < need)
+        return fail(HLA_ERR_ARG, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
+    if (!aligned16(workspace)) return fail(HLA_ERR_ARG, "workspace must be 16-byte aligned");
+    if (phase_events) {
+        for (int i = 0; i < 4; ++i)
+            if (!phase_events[i]) return fail(HLA_ERR_ARG, "phase_events must hold four events");
+    }
+    hla::Fwd3Args a;
+    a.B = p->B; a.H = p->H; a.n = p->n; a.d = p->d; a.dv = p->dv; a.chunk = p->chunk;
+    a.in_dtype = p->in_dtype;
+    a.q = q; a.k = k; a.v = v; a.o = o;
+    a.sin_S = state_in ? state_in->S : nullptr;
+    a.sin_P = state_in ? state_in->P : nullptr;
+    a.sin_T = state_in ? state_in->T : nullptr;
+    a.sout_S = state_out ? state_out->S : nullptr;
+    a.sout_P = state_out ? state_out->P : nullptr;
+    a.sout_T = state_out ? state_out->T : nullptr;
+    a.workspace = static_cast<float *>(workspace);
+    a.events = reinterpret_cast<cudaEvent_t const *>(phase_events);
+    cudaError_t e = hla::fwd3_launch(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "third-order forward launch");
+    return HLA_OK;
+}
+
+hla_status hla_decode3_step(int N, int d, int dv, hla_dtype dtype, const hla_state3 *state, const void *q,
+                            const void *k, const void *v, void *o, void *stream) {
+    if (N < 0) return fail(HLA_ERR_ARG, "need N >= 0");
+    if (!width_ok(d) || !width_ok(dv)) return fail(HLA_ERR_UNSUPPORTED, "d, dv must be in {16,32,64,128}");
+    if (dtype != HLA_F32 && dtype != HLA_BF16) return fail(HLA_ERR_ARG, "unknown dtype");
+    if (!state) return fail(HLA_ERR_ARG, "state must be set");
+    hla_status s = check_state3(state, "state");
+    if (s != HLA_OK) return s;
+    if (N > 0 && (!q || !k || !v || !o)) return fail(HLA_ERR_ARG, "q, k, v, o must be set");
+    hla::Decode3Args a;
+    a.N = N; a.d = d; a.dv = dv; a.dtype = dtype;
+    a.S = state->S; a.P = state->P; a.T = state->T;
+    a.q = q; a.k = k; a.v = v; a.o = o;
+    cudaError_t e = hla::decode3_launch(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "third-order decode launch");
+    return HLA_OK;
+}
+
 hla_status hla_state_combine(int count, int d, int dv, unsigned flags, const hla_state *A, const hla_state *B,
                              const hla_state *out, const float *decay_pow, void *stream) {
     if (count < 0) return fail(HLA_ERR_ARG, "count must be >= 0");

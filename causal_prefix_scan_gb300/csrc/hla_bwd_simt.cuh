@@ -34,133 +34,13 @@
 // and backward for Lam, Om and writes the states every chunk needs; (3) one CTA
 // per chunk forms dq, dk, dv.
 #pragma once
-#include "hla_internal.h"
+#include "hla_smem_tile.cuh"
 
 namespace hla {
 namespace bwd {
 
-constexpr int kThreads = 256;
+using namespace tile;
 constexpr int kSplit = 4;  // column blocks per (b,h) and direction in the scan
-
-template <typename T>
-__device__ __forceinline__ float ld_t(const T *p, size_t i);
-template <>
-__device__ __forceinline__ float ld_t<float>(const float *p, size_t i) { return p[i]; }
-template <>
-__device__ __forceinline__ float ld_t<__nv_bfloat16>(const __nv_bfloat16 *p, size_t i) {
-    return __bfloat162float(p[i]);
-}
-template <typename T>
-__device__ __forceinline__ void st_t(T *p, size_t i, float x);
-template <>
-__device__ __forceinline__ void st_t<float>(float *p, size_t i, float x) { p[i] = x; }
-template <>
-__device__ __forceinline__ void st_t<__nv_bfloat16>(__nv_bfloat16 *p, size_t i, float x) {
-    p[i] = __float2bfloat16_rn(x);
-}
-
-// ---- small shared-memory products on a 4x4 register tile per thread --------------
-// acc[i][j] += sum_k w_k A(m0+i, k) B(k, n0 + j*ns).  A(m,k) = TA ? A[k*lda+m] : A[m*lda+k];
-// B(k,n) = TB ? B[n*ldb+k] : B[k*ldb+n].  K a multiple of 4, leading dimensions multiples
-// of 4 floats, bases 16-byte aligned.  ns == 1: four adjacent columns; else strided.
-template <bool TA, bool TB>
-__device__ __forceinline__ void mac(float (&acc)[4][4], const float *A, int lda, const float *B, int ldb, int m0,
-                                    int n0, int ns, int K, const float *kw = nullptr) {
-#pragma unroll 2
-    for (int k = 0; k < K; k += 4) {
-        float a[4][4], b[4][4];  // [kk][i], [kk][j]
-        if (TA) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const float4 x = *reinterpret_cast<const float4 *>(A + (size_t)(k + kk) * lda + m0);
-                a[kk][0] = x.x; a[kk][1] = x.y; a[kk][2] = x.z; a[kk][3] = x.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float4 x = *reinterpret_cast<const float4 *>(A + (size_t)(m0 + i) * lda + k);
-                a[0][i] = x.x; a[1][i] = x.y; a[2][i] = x.z; a[3][i] = x.w;
-            }
-        }
-        if (kw) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const float w = kw[k + kk];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) a[kk][i] *= w;
-            }
-        }
-        if (TB) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 x = *reinterpret_cast<const float4 *>(B + (size_t)(n0 + j * ns) * ldb + k);
-                b[0][j] = x.x; b[1][j] = x.y; b[2][j] = x.z; b[3][j] = x.w;
-            }
-        } else if (ns == 1) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const float4 x = *reinterpret_cast<const float4 *>(B + (size_t)(k + kk) * ldb + n0);
-                b[kk][0] = x.x; b[kk][1] = x.y; b[kk][2] = x.z; b[kk][3] = x.w;
-            }
-        } else {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) b[kk][j] = B[(size_t)(k + kk) * ldb + n0 + j * ns];
-        }
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[kk][i], b[kk][j], acc[i][j]);
-    }
-}
-
-// The same term scaled by rs[row] before it is added.
-template <bool TA, bool TB>
-__device__ __forceinline__ void mac_rs(float (&acc)[4][4], const float *rs, const float *A, int lda, const float *B,
-                                       int ldb, int m0, int n0, int ns, int K) {
-    float t[4][4] = {};
-    mac<TA, TB>(t, A, lda, B, ldb, m0, n0, ns, K);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(rs[m0 + i], t[i][j], acc[i][j]);
-}
-
-// Every 4x4 tile of an M x N result, one per thread per round.  STRIDED spreads a
-// thread's four columns N/4 apart (conflict-free rows when B is read transposed).
-template <bool STRIDED, class Body>
-__device__ __forceinline__ void tiles(int M, int N, Body body) {
-    const int tn = N / 4, count = (M / 4) * tn;
-    for (int t = threadIdx.x; t < count; t += kThreads) {
-        const int m0 = (t / tn) * 4;
-        const int n0 = STRIDED ? t % tn : (t % tn) * 4, ns = STRIDED ? tn : 1;
-        float acc[4][4] = {};
-        body(acc, m0, n0, ns);
-    }
-}
-
-template <class F>
-__device__ __forceinline__ void each(const float (&acc)[4][4], int m0, int n0, int ns, F f) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) f(m0 + i, n0 + j * ns, acc[i][j]);
-}
-
-template <typename T>
-__device__ __forceinline__ void load_rows(const T *src, float *dst, int ld, int rows, int L, int W) {
-    for (int e = threadIdx.x; e < rows * W; e += kThreads) {
-        const int r = e / W, x = e % W;
-        dst[r * ld + x] = r < L ? ld_t(src, (size_t)r * W + x) : 0.f;
-    }
-}
-
-__device__ __forceinline__ void load_mat(const float *src, float *dst, int ld, int rows, int W) {
-    for (int e = threadIdx.x; e < rows * W; e += kThreads) dst[(e / W) * ld + e % W] = src[e];
-}
 
 // Workspace: the six local sums of every (b,h, chunk), then the four states of
 // every (b,h, chunk).

@@ -1,0 +1,322 @@
+// hla_fwd3_simt.cuh -- chunk-parallel forward of masked third-order HLA on CUDA
+// cores (fp32 arithmetic), for d, dv, chunk in {16,32,64}.
+//
+// "Higher-order Linear Attention", gist.science summary, section 3 "Derde-orde HLA":
+// the operator A A^T A (A = Q K^T) with every factor causal,
+//   o_t = sum_{b<=t} sum_{a<=b} sum_{c<=b} (q_t.k_a)(k_a.q_b)(q_b.k_c) v_c
+//       = q_t^T T_t,   T_t = sum_{b<=t} S^K_b q_b q_b^T P_b,
+// with the prefix moments S^K_b = sum_{a<=b} k_a k_a^T and P_b = sum_{c<=b} k_c v_c^T.
+// T equals S^K S^Q P minus the cross summaries of the pages (G1 + G2 - G3).
+//
+// Chunk form (prefix state S^K_p, P_p, T_p before the chunk):
+//   A~ = tril(Q K^T),  U = Q S^K_p + A~ K  (rows u_b = S^K_b q_b),
+//   W = Q P_p + A~ V  (rows w_b = P_b^T q_b),  M = tril(Q U^T),  O = Q T_p + M W.
+// Segment summaries and their concatenation (section 4, bullet "Derde-orde scans":
+// segment-level linear maps compose third-order states exactly), A before B:
+//   T = T_A + T_B + S^K_A M^QP_B + M^KQ_B P_A + S^K_A S^Q_B P_A,  S^K, P add,
+// with the chunk-local sums (from a zero prefix, U and W without their first terms)
+//   S^K = K^T K,  S^Q = Q^T Q,  P = K^T V,  T = U^T W,  M^QP = Q^T W,  M^KQ = U^T Q.
+//
+// Three launches: (1) one CTA per chunk writes the local sums; (2) the scan, one CTA
+// per (b,h) and column block of dv, walks the chunks and writes each chunk's prefix
+// state (and the final state); (3) one CTA per chunk forms the outputs.
+#pragma once
+#include "hla_smem_tile.cuh"
+
+namespace hla {
+namespace fwd3 {
+using namespace tile;
+constexpr int kSplit = 4;  // column blocks of dv per (b,h) in the scan
+
+// Workspace: the local sums of every (b,h, chunk), then the prefix states.
+struct Ws3 {
+    int d, dv;
+    // local sums: S^K d*d, S^Q d*d, M^KQ d*d, P d*dv, T d*dv, M^QP d*dv
+    __host__ __device__ size_t loc_floats() const { return 3 * (size_t)d * d + 3 * (size_t)d * dv; }
+    __host__ __device__ size_t o_sk() const { return 0; }
+    __host__ __device__ size_t o_sq() const { return (size_t)d * d; }
+    __host__ __device__ size_t o_mkq() const { return 2 * (size_t)d * d; }
+    __host__ __device__ size_t o_p() const { return 3 * (size_t)d * d; }
+    __host__ __device__ size_t o_t() const { return o_p() + (size_t)d * dv; }
+    __host__ __device__ size_t o_mqp() const { return o_t() + (size_t)d * dv; }
+    // prefix state: S^K d*d, P d*dv, T d*dv
+    __host__ __device__ size_t st_floats() const { return (size_t)d * d + 2 * (size_t)d * dv; }
+    __host__ __device__ size_t s_sk() const { return 0; }
+    __host__ __device__ size_t s_p() const { return (size_t)d * d; }
+    __host__ __device__ size_t s_t() const { return (size_t)d * d + (size_t)d * dv; }
+};
+
+// ---- (1) chunk-local sums --------------------------------------------------------
+template <int C, int D, int DV>
+struct LocSmem3 {
+    static constexpr int LQ = D + 4, LV = DV + 4, LT = C + 4;
+    static constexpr int Q = 0, K = Q + C * LQ, V = K + C * LQ, A = V + C * LV, U = A + C * LT, W = U + C * LQ,
+                         TOTAL = W + C * LV;
+};
+
+template <typename T, int C, int D, int DV>
+__global__ void __launch_bounds__(kThreads) fwd3_local_kernel(Fwd3Args a) {
+    using Sm = LocSmem3<C, D, DV>;
+    extern __shared__ __align__(16) float sm[];
+    float *Q = sm + Sm::Q, *K = sm + Sm::K, *V = sm + Sm::V, *A = sm + Sm::A, *U = sm + Sm::U, *W = sm + Sm::W;
+    const int nch = (a.n + C - 1) / C, u = blockIdx.x / nch, ch = blockIdx.x % nch;
+    const int t0 = ch * C, L = min(C, a.n - t0);
+    const size_t rq = ((size_t)u * a.n + t0) * D, rv = ((size_t)u * a.n + t0) * DV;
+    load_rows(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L, D);
+    load_rows(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L, D);
+    load_rows(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L, DV);
+    __syncthreads();
+    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, true>(acc, Q, Sm::LQ, K, Sm::LQ, m0, n0, ns, D);
+        each(acc, m0, n0, ns, [&](int t, int s, float x) { A[t * Sm::LT + s] = s <= t ? x : 0.f; });
+    });
+    __syncthreads();
+    // U = A~ K, W = A~ V (no earlier state)
+    tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, false>(acc, A, Sm::LT, K, Sm::LQ, m0, n0, ns, C);
+        each(acc, m0, n0, ns, [&](int t, int i, float x) { U[t * Sm::LQ + i] = x; });
+    });
+    tiles<false>(C, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, false>(acc, A, Sm::LT, V, Sm::LV, m0, n0, ns, C);
+        each(acc, m0, n0, ns, [&](int t, int j, float x) { W[t * Sm::LV + j] = x; });
+    });
+    __syncthreads();
+    const Ws3 ws{D, DV};
+    float *out = a.workspace + ((size_t)u * nch + ch) * ws.loc_floats();
+    auto put = [&](size_t off, int ld) {
+        return [=](int i, int j, float x) { out[off + (size_t)i * ld + j] = x; };
+    };
+    // rows past the chunk's last token are zero in Q, K, V, U, W
+    tiles<false>(D, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, K, Sm::LQ, K, Sm::LQ, m0, n0, ns, C);
+        each(acc, m0, n0, ns, put(ws.o_sk(), D));
+    });
+    tiles<false>(D, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, Q, Sm::LQ, Q, Sm::LQ, m0, n0, ns, C);
+        each(acc, m0, n0, ns, put(ws.o_sq(), D));
+    });
+    tiles<false>(D, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, U, Sm::LQ, Q, Sm::LQ, m0, n0, ns, C);
+        each(acc, m0, n0, ns, put(ws.o_mkq(), D));
+    });
+    tiles<false>(D, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, K, Sm::LQ, V, Sm::LV, m0, n0, ns, C);
+        each(acc, m0, n0, ns, put(ws.o_p(), DV));
+    });
+    tiles<false>(D, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, U, Sm::LQ, W, Sm::LV, m0, n0, ns, C);
+        each(acc, m0, n0, ns, put(ws.o_t(), DV));
+    });
+    tiles<false>(D, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, Q, Sm::LQ, W, Sm::LV, m0, n0, ns, C);
+        each(acc, m0, n0, ns, put(ws.o_mqp(), DV));
+    });
+}
+
+// ---- (2) scan over chunks ---------------------------------------------------------
+// blockIdx.x = u * kSplit + part.  The CTA keeps S^K whole and the columns
+// [part*dv/kSplit, ...) of P and T; it stores the row block `part` of S^K and its
+// column blocks of P, T as each chunk's prefix state, and the same of the final state.
+template <int C, int D, int DV>
+struct ScanSmem3 {
+    static constexpr int NB = DV / kSplit, LF = D + 4, LB = NB + 4;
+    static constexpr int SK = 0, SKL = SK + D * LF, SQL = SKL + D * LF, MKQL = SQL + D * LF, PB = MKQL + D * LF,
+                         TB = PB + D * LB, PL = TB + D * LB, TL = PL + D * LB, MQPL = TL + D * LB, X = MQPL + D * LB,
+                         TOTAL = X + D * LB;
+};
+
+template <int C, int D, int DV>
+__global__ void __launch_bounds__(kThreads) fwd3_scan_kernel(Fwd3Args a) {
+    using Sm = ScanSmem3<C, D, DV>;
+    constexpr int NB = Sm::NB, LF = Sm::LF, LB = Sm::LB;
+    extern __shared__ __align__(16) float sm[];
+    float *SK = sm + Sm::SK, *SKl = sm + Sm::SKL, *SQl = sm + Sm::SQL, *MKQl = sm + Sm::MKQL;
+    float *Pb = sm + Sm::PB, *Tb = sm + Sm::TB, *Pl = sm + Sm::PL, *Tl = sm + Sm::TL, *MQPl = sm + Sm::MQPL;
+    float *X = sm + Sm::X;
+    const int part = blockIdx.x % kSplit, u = blockIdx.x / kSplit;
+    const int nch = (a.n + C - 1) / C, c0 = part * NB;
+    constexpr int ROWS = D / kSplit;
+    const int r0 = part * ROWS;
+    const Ws3 ws{D, DV};
+    const float *loc = a.workspace + (size_t)u * nch * ws.loc_floats();
+    float *st = a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + (size_t)u * nch * ws.st_floats();
+    // initial state: state_in or zeros
+    for (int e = threadIdx.x; e < D * D; e += kThreads)
+        SK[(e / D) * LF + e % D] = a.sin_S ? a.sin_S[(size_t)u * D * D + e] : 0.f;
+    for (int e = threadIdx.x; e < D * NB; e += kThreads) {
+        const int r = e / NB, x = e % NB;
+        const size_t g = (size_t)u * D * DV + (size_t)r * DV + c0 + x;
+        Pb[r * LB + x] = a.sin_P ? a.sin_P[g] : 0.f;
+        Tb[r * LB + x] = a.sin_T ? a.sin_T[g] : 0.f;
+    }
+    __syncthreads();
+    for (int ch = 0; ch < nch; ++ch) {
+        const float *lc = loc + (size_t)ch * ws.loc_floats();
+        float *so = st + (size_t)ch * ws.st_floats();
+        // this chunk's prefix state
+        for (int e = threadIdx.x; e < ROWS * D; e += kThreads) {
+            const int r = r0 + e / D, x = e % D;
+            so[ws.s_sk() + (size_t)r * D + x] = SK[r * LF + x];
+        }
+        for (int e = threadIdx.x; e < D * NB; e += kThreads) {
+            const int r = e / NB, x = e % NB;
+            so[ws.s_p() + (size_t)r * DV + c0 + x] = Pb[r * LB + x];
+            so[ws.s_t() + (size_t)r * DV + c0 + x] = Tb[r * LB + x];
+        }
+        // its local sums
+        load_mat(lc + ws.o_sk(), SKl, LF, D, D);
+        load_mat(lc + ws.o_sq(), SQl, LF, D, D);
+        load_mat(lc + ws.o_mkq(), MKQl, LF, D, D);
+        for (int e = threadIdx.x; e < D * NB; e += kThreads) {
+            const int r = e / NB, x = e % NB;
+            const size_t g = (size_t)r * DV + c0 + x;
+            Pl[r * LB + x] = lc[ws.o_p() + g];
+            Tl[r * LB + x] = lc[ws.o_t() + g];
+            MQPl[r * LB + x] = lc[ws.o_mqp() + g];
+        }
+        __syncthreads();
+        // X = M^QP_B + S^Q_B P_A  (block columns)
+        tiles<false>(D, NB, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+            mac<false, false>(acc, SQl, LF, Pb, LB, m0, n0, ns, D);
+            each(acc, m0, n0, ns, [&](int i, int j, float x) { X[i * LB + j] = MQPl[i * LB + j] + x; });
+        });
+        __syncthreads();
+        // T <- T + T_B + S^K_A X + M^KQ_B P_A
+        tiles<false>(D, NB, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+            mac<false, false>(acc, SK, LF, X, LB, m0, n0, ns, D);
+            mac<false, false>(acc, MKQl, LF, Pb, LB, m0, n0, ns, D);
+            each(acc, m0, n0, ns, [&](int i, int j, float x) { Tb[i * LB + j] += Tl[i * LB + j] + x; });
+        });
+        __syncthreads();
+        // P <- P + P_B, S^K <- S^K + S^K_B
+        for (int e = threadIdx.x; e < D * NB; e += kThreads) {
+            const int r = e / NB, x = e % NB;
+            Pb[r * LB + x] += Pl[r * LB + x];
+        }
+        for (int e = threadIdx.x; e < D * D; e += kThreads) {
+            const int r = e / D, x = e % D;
+            SK[r * LF + x] += SKl[r * LF + x];
+        }
+        __syncthreads();
+    }
+    // final state
+    if (a.sout_S) {
+        for (int e = threadIdx.x; e < ROWS * D; e += kThreads) {
+            const int r = r0 + e / D, x = e % D;
+            a.sout_S[(size_t)u * D * D + (size_t)r * D + x] = SK[r * LF + x];
+        }
+        for (int e = threadIdx.x; e < D * NB; e += kThreads) {
+            const int r = e / NB, x = e % NB;
+            const size_t g = (size_t)u * D * DV + (size_t)r * DV + c0 + x;
+            a.sout_P[g] = Pb[r * LB + x];
+            a.sout_T[g] = Tb[r * LB + x];
+        }
+    }
+}
+
+// ---- (3) outputs of one chunk -----------------------------------------------------
+template <int C, int D, int DV>
+struct OutSmem3 {
+    static constexpr int LQ = D + 4, LV = DV + 4, LT = C + 4;
+    static constexpr int Q = 0, K = Q + C * LQ, V = K + C * LQ, SK = V + C * LV, P = SK + D * LQ, TP = P + D * LV,
+                         A = TP + D * LV, M = A + C * LT, U = M + C * LT, W = U + C * LQ, TOTAL = W + C * LV;
+};
+
+template <typename T, int C, int D, int DV>
+__global__ void __launch_bounds__(kThreads) fwd3_out_kernel(Fwd3Args a) {
+    using Sm = OutSmem3<C, D, DV>;
+    extern __shared__ __align__(16) float sm[];
+    float *Q = sm + Sm::Q, *K = sm + Sm::K, *V = sm + Sm::V, *SK = sm + Sm::SK, *P = sm + Sm::P, *Tp = sm + Sm::TP;
+    float *A = sm + Sm::A, *M = sm + Sm::M, *U = sm + Sm::U, *W = sm + Sm::W;
+    const int nch = (a.n + C - 1) / C, u = blockIdx.x / nch, ch = blockIdx.x % nch;
+    const int t0 = ch * C, L = min(C, a.n - t0);
+    const size_t rq = ((size_t)u * a.n + t0) * D, rv = ((size_t)u * a.n + t0) * DV;
+    const Ws3 ws{D, DV};
+    const float *so =
+        a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
+    load_rows(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L, D);
+    load_rows(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L, D);
+    load_rows(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L, DV);
+    load_mat(so + ws.s_sk(), SK, Sm::LQ, D, D);
+    load_mat(so + ws.s_p(), P, Sm::LV, D, DV);
+    load_mat(so + ws.s_t(), Tp, Sm::LV, D, DV);
+    __syncthreads();
+    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, true>(acc, Q, Sm::LQ, K, Sm::LQ, m0, n0, ns, D);
+        each(acc, m0, n0, ns, [&](int t, int s, float x) { A[t * Sm::LT + s] = s <= t ? x : 0.f; });
+    });
+    __syncthreads();
+    // U = Q S^K_p + A~ K;  W = Q P_p + A~ V
+    tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, false>(acc, Q, Sm::LQ, SK, Sm::LQ, m0, n0, ns, D);
+        mac<false, false>(acc, A, Sm::LT, K, Sm::LQ, m0, n0, ns, C);
+        each(acc, m0, n0, ns, [&](int t, int i, float x) { U[t * Sm::LQ + i] = x; });
+    });
+    tiles<false>(C, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, false>(acc, Q, Sm::LQ, P, Sm::LV, m0, n0, ns, D);
+        mac<false, false>(acc, A, Sm::LT, V, Sm::LV, m0, n0, ns, C);
+        each(acc, m0, n0, ns, [&](int t, int j, float x) { W[t * Sm::LV + j] = x; });
+    });
+    __syncthreads();
+    // M = tril(Q U^T)
+    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, true>(acc, Q, Sm::LQ, U, Sm::LQ, m0, n0, ns, D);
+        each(acc, m0, n0, ns, [&](int t, int b, float x) { M[t * Sm::LT + b] = b <= t ? x : 0.f; });
+    });
+    __syncthreads();
+    // O = Q T_p + M W
+    T *o = static_cast<T *>(a.o) + rv;
+    tiles<false>(C, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, false>(acc, Q, Sm::LQ, Tp, Sm::LV, m0, n0, ns, D);
+        mac<false, false>(acc, M, Sm::LT, W, Sm::LV, m0, n0, ns, C);
+        each(acc, m0, n0, ns, [&](int t, int j, float x) {
+            if (t < L) st_t(o, (size_t)t * DV + j, x);
+        });
+    });
+}
+
+template <typename Kern>
+cudaError_t smem_attr(Kern kern, size_t bytes) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <typename T, int C, int D, int DV>
+cudaError_t launch_t(const Fwd3Args &a, cudaStream_t st) {
+    const int nch = (a.n + C - 1) / C, units = a.B * a.H;
+    const size_t b1 = LocSmem3<C, D, DV>::TOTAL * sizeof(float), b2 = ScanSmem3<C, D, DV>::TOTAL * sizeof(float),
+                 b3 = OutSmem3<C, D, DV>::TOTAL * sizeof(float);
+    cudaError_t e;
+    if ((e = smem_attr(fwd3_local_kernel<T, C, D, DV>, b1)) != cudaSuccess) return e;
+    if ((e = smem_attr(fwd3_scan_kernel<C, D, DV>, b2)) != cudaSuccess) return e;
+    if ((e = smem_attr(fwd3_out_kernel<T, C, D, DV>, b3)) != cudaSuccess) return e;
+    auto mark = [&](int i) { return a.events ? cudaEventRecord(a.events[i], st) : cudaSuccess; };
+    if ((e = mark(0)) != cudaSuccess) return e;
+    fwd3_local_kernel<T, C, D, DV><<<units * nch, kThreads, b1, st>>>(a);
+    if ((e = mark(1)) != cudaSuccess) return e;
+    fwd3_scan_kernel<C, D, DV><<<units * kSplit, kThreads, b2, st>>>(a);
+    if ((e = mark(2)) != cudaSuccess) return e;
+    fwd3_out_kernel<T, C, D, DV><<<units * nch, kThreads, b3, st>>>(a);
+    if ((e = mark(3)) != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+template <typename T, int C, int D>
+cudaError_t launch_dv(const Fwd3Args &a, cudaStream_t st) {
+    switch (a.dv) {
+        case 16: return launch_t<T, C, D, 16>(a, st);
+        case 32: return launch_t<T, C, D, 32>(a, st);
+        case 64: return launch_t<T, C, D, 64>(a, st);
+    }
+    return cudaErrorInvalidValue;
+}
+template <typename T, int C>
+cudaError_t launch_d(const Fwd3Args &a, cudaStream_t st) {
+    switch (a.d) {
+        case 16: return launch_dv<T, C, 16>(a, st);
+        case 32: return launch_dv<T, C, 32>(a, st);
+        case 64: return launch_dv<T, C, 64>(a, st);
+    }
+    return cudaErrorInvalidValue;
+}
+// One translation unit per (element type, chunk) instantiates launch_d.
+}  // namespace fwd3
+}  // namespace hla

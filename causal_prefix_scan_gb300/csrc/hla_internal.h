@@ -81,6 +81,31 @@ bool bwd_simt_supported(const hla_params &p);
 size_t bwd_simt_workspace(const hla_params &p);
 cudaError_t bwd_simt_launch(const BwdArgs &a, cudaStream_t st);
 
+struct Fwd3Args {
+    int B, H, n, d, dv, chunk;
+    hla_dtype in_dtype;
+    const void *q, *k, *v;
+    void *o;
+    const float *sin_S, *sin_P, *sin_T;  // state before the first token (all NULL: zeros)
+    float *sout_S, *sout_P, *sout_T;     // state after the last token (all NULL: skip)
+    float *workspace;
+    cudaEvent_t const *events;  // NULL or four events recorded at the phase boundaries
+};
+
+struct Decode3Args {
+    int N, d, dv;
+    hla_dtype dtype;
+    float *S, *P, *T;
+    const void *q, *k, *v;
+    void *o;
+};
+
+// Masked third-order forward and decode on CUDA cores.
+bool fwd3_supported(const hla_params &p);
+size_t fwd3_workspace(const hla_params &p);
+cudaError_t fwd3_launch(const Fwd3Args &a, cudaStream_t st);
+cudaError_t decode3_launch(const Decode3Args &a, cudaStream_t st);
+
 // Set this thread's last-error message and return `s`.
 hla_status report(hla_status s, const char *msg);
 

@@ -221,6 +221,53 @@ HLA_API hla_status hla_backward_chunked_traced(const hla_params *p, const void *
                                                const void *dout, void *dq, void *dk, void *dv, void *workspace,
                                                size_t workspace_bytes, void *stream, void *const *phase_events);
 
+/*
+ * Masked third-order HLA (section 3 "Derde-orde HLA": the operator A A^T A with
+ * A = Q K^T, every factor causal):
+ *   o_t = sum_{b<=t} sum_{a<=b} sum_{c<=b} (q_t.k_a)(k_a.q_b)(q_b.k_c) v_c = q_t^T T_t,
+ *   T_t = sum_{b<=t} S^K_b q_b q_b^T P_b   (= S^K S^Q P^KV minus the cross summaries
+ *   G1 + G2 - G3 that remove a key after its query),
+ * with S^K_t = sum k k^T and P_t = sum k v^T.  The streaming state of a pair is
+ * (S [d][d] = S^K, P [d][dv], T [d][dv]), fp32; no decay, no normalisation.
+ */
+typedef struct {
+    float *S, *P, *T;
+} hla_state3;
+
+/* Bytes of device workspace hla_forward3_chunked needs (0 for invalid parameters). */
+HLA_API size_t hla_forward3_workspace_size(const hla_params *p);
+
+/*
+ * Masked third-order forward over n tokens for every (b,h) pair, chunk-parallel
+ * (section 4, "Derde-orde scans"): chunk-local sums, a scan over chunks that composes
+ * states with the segment-level linear maps M^KQ and M^QP, then per-chunk outputs.
+ *   p         flags must be 0, Hkv 0 or H, d, dv, chunk in {16,32,64}; in_dtype
+ *             HLA_F32 or HLA_BF16 (fp32 arithmetic);
+ *   q, k      [B][H][n][d]; v, o [B][H][n][dv]; in_dtype;
+ *   state_in  (S, P, T) before the first token, or NULL for zeros;
+ *   state_out (S, P, T) after the last token, or NULL; may not alias state_in;
+ *   workspace at least hla_forward3_workspace_size(p) bytes, 16-byte aligned.
+ * Three kernel launches on `stream`.
+ */
+HLA_API hla_status hla_forward3_chunked(const hla_params *p, const void *q, const void *k, const void *v, void *o,
+                                        const hla_state3 *state_in, const hla_state3 *state_out, void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
+/* hla_forward3_chunked recording four caller-owned events on `stream` (NULL: none):
+ * before the local-sums kernel, after it, after the scan and after the output kernel. */
+HLA_API hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const void *k, const void *v,
+                                               void *o, const hla_state3 *state_in, const hla_state3 *state_out,
+                                               void *workspace, size_t workspace_bytes, void *stream,
+                                               void *const *phase_events);
+
+/*
+ * One third-order decode step for N independent pairs, state updated in place:
+ *   S += k k^T;  P += k v^T;  T += (S q)(P^T q)^T;  o = T^T q.
+ * q, k: [N][d], v, o: [N][dv], element type `dtype`; d, dv in {16,32,64,128}.
+ */
+HLA_API hla_status hla_decode3_step(int N, int d, int dv, hla_dtype dtype, const hla_state3 *state, const void *q,
+                                    const void *k, const void *v, void *o, void *stream);
+
 /* Synchronise `stream`, then report and clear the sticky device flag: HLA_OK,
  * HLA_ERR_TIMEOUT if a bounded device wait expired since the last call, or
  * HLA_ERR_CUDA if the stream reported an error. */

@@ -180,3 +180,60 @@ def test_backward_traced_rejects_missing_events(lib):
     assert hla.library().hla_backward_chunked_traced(ctypes.byref(p), 16, 16, 16, 16, 16, 16, 16, 16, 1 << 40, None,
                                                      ev) == hla.HLA_ERR_ARG
     assert "event" in hla.hla_last_error()
+
+
+def _f3call(p, ptrs=(16,) * 4, sin=None, sout=None, ws=16, ws_bytes=1 << 40):
+    q, k, v, o = ptrs
+    return hla.library().hla_forward3_chunked(ctypes.byref(p) if p is not None else None, q, k, v, o, sin, sout, ws,
+                                              ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), hla.HLA_ERR_ARG),
+    (dict(n=-1), hla.HLA_ERR_ARG),
+    (dict(flags=16), hla.HLA_ERR_ARG),
+    (dict(flags=hla.HLA_NORMALIZE), hla.HLA_ERR_UNSUPPORTED),
+    (dict(flags=hla.HLA_DECAY, gamma=16), hla.HLA_ERR_UNSUPPORTED),
+    (dict(flags=hla.HLA_UNMASKED), hla.HLA_ERR_UNSUPPORTED),
+    (dict(H=4, Hkv=2), hla.HLA_ERR_UNSUPPORTED),
+    (dict(d=128), hla.HLA_ERR_UNSUPPORTED),
+    (dict(chunk=128), hla.HLA_ERR_UNSUPPORTED),
+    (dict(dv=48), hla.HLA_ERR_UNSUPPORTED),
+])
+def test_forward3_rejects_bad_params(lib, kw, status):
+    assert _f3call(_params(**kw)) == status
+    assert hla.hla_last_error()
+    assert hla.hla_forward3_workspace_size(_params(**kw)) == 0
+
+
+def test_forward3_rejects_null_misaligned_short_workspace_and_aliasing(lib):
+    assert _f3call(None) == hla.HLA_ERR_ARG
+    assert _f3call(_params(), ptrs=(16, None, 16, 16)) == hla.HLA_ERR_ARG
+    assert _f3call(_params(), ptrs=(16, 16, 8, 16)) == hla.HLA_ERR_ARG
+    need = hla.hla_forward3_workspace_size(_params())
+    assert _f3call(_params(), ws_bytes=need - 1) == hla.HLA_ERR_ARG
+    s3 = hla.hla_state3(16, 16, 16)
+    assert _f3call(_params(), sin=ctypes.pointer(s3), sout=ctypes.pointer(s3)) == hla.HLA_ERR_ARG
+    bad = hla.hla_state3(16, None, 16)
+    assert _f3call(_params(), sout=ctypes.pointer(bad)) == hla.HLA_ERR_ARG
+    # no tokens and no state: nothing to do
+    assert _f3call(_params(n=0), ptrs=(None,) * 4, ws=None, ws_bytes=0) == hla.HLA_OK
+
+
+def test_forward3_workspace_size(lib):
+    # per (b,h, chunk): local sums 3d^2 + 3 d dv and prefix state d^2 + 2 d dv, fp32
+    for B, H, n, d, dv, c in [(1, 2, 128, 64, 64, 64), (2, 3, 100, 32, 16, 32)]:
+        nch = -(-n // c)
+        want = B * H * nch * (4 * d * d + 5 * d * dv) * 4
+        assert hla.hla_forward3_workspace_size(_params(B=B, H=H, n=n, d=d, dv=dv, chunk=c)) == want
+
+
+def test_decode3_rejects_bad_args(lib):
+    L = hla.library()
+    s3 = ctypes.pointer(hla.hla_state3(16, 16, 16))
+    assert L.hla_decode3_step(-1, 64, 64, hla.HLA_BF16, s3, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
+    assert L.hla_decode3_step(4, 48, 64, hla.HLA_BF16, s3, 16, 16, 16, 16, None) == hla.HLA_ERR_UNSUPPORTED
+    assert L.hla_decode3_step(4, 64, 64, 9, s3, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
+    assert L.hla_decode3_step(4, 64, 64, hla.HLA_BF16, None, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
+    assert L.hla_decode3_step(4, 64, 64, hla.HLA_BF16, ctypes.pointer(hla.hla_state3(16, 8, 16)), 16, 16, 16, 16,
+                              None) == hla.HLA_ERR_ARG
