@@ -51,6 +51,7 @@ BWD_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_bwd
 BWD_METRIC = "masked 2nd-order HLA backward (dq, dk, dv) tokens/s and % roofline on 1 GB300"
 FWD3_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd3_simt.cuh")
 FWD3_METRIC = "masked 3rd-order HLA forward tokens/s and % roofline on 1 GB300"
+FWD3_DISPATCH_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd3_simt.cu")
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz (maximum SM clock)
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2070e6 / 1e12
 
@@ -318,7 +319,9 @@ def workload_by_name(name: str):
         return W.WORKLOADS[name]
     if name == W.DECODE.name:
         return W.DECODE
-    raise SystemExit(f"unknown workload {name}; choose from {list(W.WORKLOADS) + [W.DECODE.name]}")
+    if name == W.DECODE3.name:
+        return W.DECODE3
+    raise SystemExit(f"unknown workload {name}; choose from {list(W.WORKLOADS) + [W.DECODE.name, W.DECODE3.name]}")
 
 
 def config_dict(w: W.Workload, nsets: int, set_bytes: int, world: int):
@@ -674,11 +677,21 @@ def bench_decode(args, dw: W.DecodeWorkload, rank, world, local, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     N, d, dv = dw.seqs * dw.H, dw.d, dw.dv
+    third = dw.order == 3
+    if third:  # a drawn third-order state (S^K symmetric)
+        gs = torch.Generator(device=dev)
+        gs.manual_seed(dw.seed)
+        a_ = torch.randn((N, d, d), generator=gs, device=dev) * 0.05
+        st = hla.State3((a_ + a_.transpose(1, 2)).contiguous(),
+                        torch.randn((N, d, dv), generator=gs, device=dev) * 0.05,
+                        torch.randn((N, d, dv), generator=gs, device=dev) * 0.05)
+        del a_
     # prefill the state with the forward over a seeded prefix (drawn on the device)
-    pw = W.Workload("decode_prefix", dw.seqs, dw.H, dw.prefix, d, dv, dw.chunk, "bf16", "l2", seed=dw.seed)
-    st = hla.State.empty(N, d, dv, device=dev)
+    pw = W.Workload("decode_prefix", dw.seqs, dw.H, dw.prefix, d, dv, max(dw.chunk, 64), "bf16", "l2", seed=dw.seed)
+    if not third:
+        st = hla.State.empty(N, d, dv, device=dev)
     rows = 32
-    for b0 in range(0, dw.seqs, rows):
+    for b0 in range(0, dw.seqs if not third else 0, rows):
         px = W.make_inputs_device(pw.with_(B=min(rows, dw.seqs - b0), seed=dw.seed * 1000 + b0), device=dev)
         sub = hla.State(*(a[b0 * dw.H:(b0 + px["q"].shape[0]) * dw.H] for a in st.astuple()))
         p = hla.make_params(px["q"], px["v"], dw.chunk)
@@ -703,7 +716,10 @@ def bench_decode(args, dw: W.DecodeWorkload, rank, world, local, dist):
 
     def step(i, s):
         q, k, v = toks[i % T]
-        hla.hla_decode_step(N, dw.H, 0, d, dv, hla.HLA_BF16, 0, 0.0, None, st, q, k, v, o, s)
+        if third:
+            hla.hla_decode3_step(N, d, dv, hla.HLA_BF16, st, q, k, v, o, s)
+        else:
+            hla.hla_decode_step(N, dw.H, 0, d, dv, hla.HLA_BF16, 0, 0.0, None, st, q, k, v, o, s)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -736,7 +752,7 @@ def bench_decode(args, dw: W.DecodeWorkload, rank, world, local, dist):
     t_max = max_over_ranks(dist, ev0.elapsed_time(ev1))
     ms = t_max / steps
     value = world * dw.seqs * steps / (t_max / 1e3)
-    state_bytes = (d * d + 2 * d * dv + 2 * d) * 4
+    state_bytes = (d * d + 2 * d * dv + (0 if third else 2 * d)) * 4
     bytes_step = N * (2 * state_bytes + (2 * d + 2 * dv) * 2)
     peaks, peak_kind = load_peaks()
     ach = bytes_step / (ms / 1e3) / 1e9
@@ -750,21 +766,27 @@ def bench_decode(args, dw: W.DecodeWorkload, rank, world, local, dist):
         e0.record(stream)
         for _ in range(Ke):
             q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True); v.copy_(hv, non_blocking=True)
-            hla.hla_decode_step(N, dw.H, 0, d, dv, hla.HLA_BF16, 0, 0.0, None, st, q, k, v, o, stream)
+            if third:
+                hla.hla_decode3_step(N, d, dv, hla.HLA_BF16, st, q, k, v, o, stream)
+            else:
+                hla.hla_decode_step(N, dw.H, 0, d, dv, hla.HLA_BF16, 0, 0.0, None, st, q, k, v, o, stream)
             ho.copy_(o, non_blocking=True)
         e1.record(stream)
     stream.synchronize()
     te = max_over_ranks(dist, e0.elapsed_time(e1))
-    line = {"metric": "HLA decode step tokens/s and % HBM roofline on 1 GB300", "value": value,
+    line = {"metric": ("third-order " if third else "") + "HLA decode step tokens/s and % HBM roofline on 1 GB300",
+            "value": value,
             "unit": "tokens/s", "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": dw.name, "seqs": dw.seqs, "H": dw.H, "d": d, "dv": dv, "prefix": dw.prefix,
-                       "l2": f"state {N * state_bytes / 2**30:.2f} GiB >> L2"},
+                       "l2": f"state {N * state_bytes / 2**30:.2f} GiB >> L2",
+                       "state": "drawn N(0, 0.05^2), S^K symmetric" if third else "prefilled by the forward"},
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": ach / peaks["hbm_gbs"], "traffic": traffic_for("decode_kernel", dw.name,
-                                                                                   DECODE_KERNEL_SRC),
-                         "kernel": "decode_kernel", "alg_bytes_per_launch": bytes_step,
+                         "frac": ach / peaks["hbm_gbs"],
+                         "traffic": traffic_for("decode3_kernel" if third else "decode_kernel", dw.name,
+                                                FWD3_DISPATCH_SRC if third else DECODE_KERNEL_SRC),
+                         "kernel": "decode3_kernel" if third else "decode_kernel", "alg_bytes_per_launch": bytes_step,
                          "peak_source": peak_kind},
             "e2e": {"value": world * dw.seqs * Ke / (te / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": 3 * N * d * 2, "d2h_bytes_per_step": N * dv * 2, "steps": Ke},

@@ -156,23 +156,27 @@ __global__ void __launch_bounds__(kThreads) bwd_local_kernel(BwdArgs a) {
 // blockIdx.x = (u * kSplit + part) * 2 + dir.  dir 0: S (whole) and the columns
 // [part*dv/kSplit, ...) of X, forward in time.  dir 1: Lam (whole) and the columns
 // [part*d/kSplit, ...) of Om, backward in time.  Each CTA stores its column block
-// of X_p / Om_next and the row block `part` of S_p / Lam_next.
+// of X_p / Om_next and the row block `part` of S_p / Lam_next.  The next chunk's local
+// sums are copied into the other of two shared buffers (cp.async) while the current
+// chunk is applied.
 template <int C, int D, int DV>
 struct ScanSmem {
     static constexpr int WMAX = DV > D ? DV : D;
     static constexpr int NB = WMAX / kSplit;  // widest column block
     static constexpr int FW = WMAX + 4, LB = NB + 4;
-    // F: S or Lam (D x <= WMAX); FL its increment; BK: the column block of X or Om;
-    // R: the product operand block (Cq or W, <= WMAX rows); BL: the block increment
-    static constexpr int F = 0, FL = F + D * FW, BK = FL + D * FW, R = BK + D * LB, BL = R + WMAX * LB,
-                         TOTAL = BL + D * LB;
+    // F: S or Lam (D x <= WMAX); BK: the column block of X or Om; then two buffers of
+    // FL (the increment of F), R (the product operand block, Cq or W, <= WMAX rows)
+    // and BL (the block increment)
+    static constexpr int F = 0, BK = F + D * FW, BUF = BK + D * LB;
+    static constexpr int B_FL = 0, B_R = D * FW, B_BL = B_R + WMAX * LB, BUFSZ = B_BL + D * LB;
+    static constexpr int TOTAL = BUF + 2 * BUFSZ;
 };
 
 template <int C, int D, int DV>
 __global__ void __launch_bounds__(kThreads) bwd_scan_kernel(BwdArgs a) {
     using Sm = ScanSmem<C, D, DV>;
     extern __shared__ __align__(16) float sm[];
-    float *F = sm + Sm::F, *Fl = sm + Sm::FL, *Bk = sm + Sm::BK, *R = sm + Sm::R, *Bl = sm + Sm::BL;
+    float *F = sm + Sm::F, *Bk = sm + Sm::BK;
     const int dir = blockIdx.x & 1, part = (blockIdx.x >> 1) % kSplit, u = (blockIdx.x >> 1) / kSplit;
     const int nch = (a.n + C - 1) / C;
     const bool decay = (a.flags & HLA_DECAY) != 0;
@@ -185,14 +189,25 @@ __global__ void __launch_bounds__(kThreads) bwd_scan_kernel(BwdArgs a) {
     const int fw = dir == 0 ? D : DV, bw = dir == 0 ? DV : D, nb = bw / kSplit, c0 = part * nb;
     const int rk = dir == 0 ? D : DV;  // inner dimension of F R
     const int rows = D / kSplit, rows0 = part * rows;
+    auto chunk_at = [&](int it) { return dir == 0 ? it : nch - 1 - it; };
+    auto issue = [&](int it) {  // the local sums of step it into buffer it & 1
+        const float *lc = loc + (size_t)chunk_at(it) * ws.loc_floats();
+        float *b = sm + Sm::BUF + (it & 1) * Sm::BUFSZ;
+        copy_mat_async(lc + (dir == 0 ? ws.o_sloc() : ws.o_lloc()), fw, b + Sm::B_FL, Sm::FW, D, fw);
+        copy_mat_async(lc + (dir == 0 ? ws.o_cq() : ws.o_w()) + c0, bw, b + Sm::B_R, Sm::LB, rk, nb);
+        copy_mat_async(lc + (dir == 0 ? ws.o_xloc() : ws.o_oloc()) + c0, bw, b + Sm::B_BL, Sm::LB, D, nb);
+    };
+    if (nch > 0) issue(0);
+    cp_async_commit();
     for (int e = threadIdx.x; e < D * Sm::FW; e += kThreads) F[e] = 0.f;
     for (int e = threadIdx.x; e < D * Sm::LB; e += kThreads) Bk[e] = 0.f;
     __syncthreads();
     for (int it = 0; it < nch; ++it) {
-        const int ch = dir == 0 ? it : nch - 1 - it;
+        if (it + 1 < nch) issue(it + 1);
+        cp_async_commit();
+        const int ch = chunk_at(it);
         const int L = min(C, a.n - ch * C);
         const float f1 = decay ? gpow(lg, (float)L) : 1.f, f2 = decay ? gpow(lg, (float)(2 * L)) : 1.f;
-        const float *lc = loc + (size_t)ch * ws.loc_floats();
         float *so = st + (size_t)ch * ws.st_floats();
         // the states this chunk starts from (S_p, X_p) or ends into (Lam_next, Om_next)
         float *fo = so + (dir == 0 ? ws.o_sp() : ws.o_lam()), *bo = so + (dir == 0 ? ws.o_xp() : ws.o_om());
@@ -204,23 +219,21 @@ __global__ void __launch_bounds__(kThreads) bwd_scan_kernel(BwdArgs a) {
             const int r = e / nb, x = e % nb;
             bo[(size_t)r * bw + c0 + x] = Bk[r * Sm::LB + x];
         }
-        // this chunk's local sums
-        const float *fl = lc + (dir == 0 ? ws.o_sloc() : ws.o_lloc());
-        const float *rr = lc + (dir == 0 ? ws.o_cq() : ws.o_w());
-        const float *bl = lc + (dir == 0 ? ws.o_xloc() : ws.o_oloc());
-        load_mat(fl, Fl, Sm::FW, D, fw);
-        for (int e = threadIdx.x; e < rk * nb; e += kThreads)
-            R[(e / nb) * Sm::LB + e % nb] = rr[(size_t)(e / nb) * bw + c0 + e % nb];
-        for (int e = threadIdx.x; e < D * nb; e += kThreads)
-            Bl[(e / nb) * Sm::LB + e % nb] = bl[(size_t)(e / nb) * bw + c0 + e % nb];
+        cp_async_wait<1>();  // step it's copies (the group before the one just committed)
         __syncthreads();
+        const float *b = sm + Sm::BUF + (it & 1) * Sm::BUFSZ;
+        const float *Fl = b + Sm::B_FL, *R = b + Sm::B_R, *Bl = b + Sm::B_BL;
         // block <- f_b block + Bl + F R  (F the state before this chunk's update)
         const float fb = dir == 0 ? f2 : f1, ff = dir == 0 ? f1 : f2;
-        tiles<false>(D, nb, [&](float (&acc)[4][4], int m0, int n0, int ns) {
-            mac<false, false>(acc, F, Sm::FW, R, Sm::LB, m0, n0, ns, rk);
-            each(acc, m0, n0, ns, [&](int i, int j, float x) {
-                Bk[i * Sm::LB + j] = fb * Bk[i * Sm::LB + j] + Bl[i * Sm::LB + j] + x;
-            });
+        tiles22(D, nb, [&](float (&acc)[2][2], int m0, int n0) {
+            mac22(acc, F, Sm::FW, R, Sm::LB, m0, n0, rk);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int o = (m0 + i) * Sm::LB + n0 + j;
+                    Bk[o] = fb * Bk[o] + Bl[o] + acc[i][j];
+                }
         });
         __syncthreads();
         for (int e = threadIdx.x; e < D * fw; e += kThreads) {
@@ -229,6 +242,7 @@ __global__ void __launch_bounds__(kThreads) bwd_scan_kernel(BwdArgs a) {
         }
         __syncthreads();
     }
+    cp_async_wait<0>();
 }
 
 // ---- (3) gradients of one chunk ---------------------------------------------------
@@ -256,14 +270,16 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(BwdArgs a) {
     const BwdWs ws{D, DV};
     const float *so =
         a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
+    // the chunk's states arrive asynchronously while A~ and P are formed
+    copy_mat_async(so + ws.o_sp(), D, Sp, Sm::LQ, D, D);
+    copy_mat_async(so + ws.o_xp(), DV, Xp, Sm::LV, D, DV);
+    copy_mat_async(so + ws.o_lam(), DV, Lam, Sm::LV, D, DV);
+    copy_mat_async(so + ws.o_om(), D, Om, Sm::LQ, D, D);
+    cp_async_commit();
     load_rows(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L, D);
     load_rows(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L, D);
     load_rows(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L, DV);
     load_rows(static_cast<const T *>(a.go) + rv, G, Sm::LV, C, L, DV);
-    load_mat(so + ws.o_sp(), Sp, Sm::LQ, D, D);
-    load_mat(so + ws.o_xp(), Xp, Sm::LV, D, DV);
-    load_mat(so + ws.o_lam(), Lam, Sm::LV, D, DV);
-    load_mat(so + ws.o_om(), Om, Sm::LQ, D, D);
     fill_gp(gp, C, lg, decay);
     __syncthreads();
     float *r_u = rs, *r_x = rs + C, *r_l2 = rs + 2 * C, *r_l1 = rs + 3 * C;
@@ -282,6 +298,7 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(BwdArgs a) {
         mac<false, true>(acc, G, Sm::LV, V, Sm::LV, m0, n0, ns, DV);
         each(acc, m0, n0, ns, [&](int s, int b, float x) { P[s * Sm::LT + b] = b <= s ? gp[2 * (s - b)] * x : 0.f; });
     });
+    cp_async_wait<0>();
     __syncthreads();
     // U = diag(g^{tau+1}) Q S_p + A~ K;  dU = P^T Q + diag(g^{2(L-tau)}) V Lam^T
     tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {

@@ -117,12 +117,16 @@ __global__ void __launch_bounds__(kThreads) fwd3_local_kernel(Fwd3Args a) {
 // blockIdx.x = u * kSplit + part.  The CTA keeps S^K whole and the columns
 // [part*dv/kSplit, ...) of P and T; it stores the row block `part` of S^K and its
 // column blocks of P, T as each chunk's prefix state, and the same of the final state.
+// The next chunk's local sums are copied into the other of two shared buffers
+// (cp.async) while the current chunk is applied.
 template <int C, int D, int DV>
 struct ScanSmem3 {
     static constexpr int NB = DV / kSplit, LF = D + 4, LB = NB + 4;
-    static constexpr int SK = 0, SKL = SK + D * LF, SQL = SKL + D * LF, MKQL = SQL + D * LF, PB = MKQL + D * LF,
-                         TB = PB + D * LB, PL = TB + D * LB, TL = PL + D * LB, MQPL = TL + D * LB, X = MQPL + D * LB,
-                         TOTAL = X + D * LB;
+    static constexpr int SK = 0, PB = SK + D * LF, TB = PB + D * LB, X = TB + D * LB, BUF = X + D * LB;
+    // one buffer: S^K_B, S^Q_B, M^KQ_B (D x LF each), then the column blocks of P_B, T_B, M^QP_B
+    static constexpr int B_SK = 0, B_SQ = D * LF, B_MKQ = 2 * D * LF, B_P = 3 * D * LF, B_T = B_P + D * LB,
+                         B_MQP = B_T + D * LB, BUFSZ = B_MQP + D * LB;
+    static constexpr int TOTAL = BUF + 2 * BUFSZ;
 };
 
 template <int C, int D, int DV>
@@ -130,9 +134,7 @@ __global__ void __launch_bounds__(kThreads) fwd3_scan_kernel(Fwd3Args a) {
     using Sm = ScanSmem3<C, D, DV>;
     constexpr int NB = Sm::NB, LF = Sm::LF, LB = Sm::LB;
     extern __shared__ __align__(16) float sm[];
-    float *SK = sm + Sm::SK, *SKl = sm + Sm::SKL, *SQl = sm + Sm::SQL, *MKQl = sm + Sm::MKQL;
-    float *Pb = sm + Sm::PB, *Tb = sm + Sm::TB, *Pl = sm + Sm::PL, *Tl = sm + Sm::TL, *MQPl = sm + Sm::MQPL;
-    float *X = sm + Sm::X;
+    float *SK = sm + Sm::SK, *Pb = sm + Sm::PB, *Tb = sm + Sm::TB, *X = sm + Sm::X;
     const int part = blockIdx.x % kSplit, u = blockIdx.x / kSplit;
     const int nch = (a.n + C - 1) / C, c0 = part * NB;
     constexpr int ROWS = D / kSplit;
@@ -140,6 +142,18 @@ __global__ void __launch_bounds__(kThreads) fwd3_scan_kernel(Fwd3Args a) {
     const Ws3 ws{D, DV};
     const float *loc = a.workspace + (size_t)u * nch * ws.loc_floats();
     float *st = a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + (size_t)u * nch * ws.st_floats();
+    auto issue = [&](int ch) {  // the local sums of chunk ch into buffer ch & 1
+        const float *lc = loc + (size_t)ch * ws.loc_floats();
+        float *b = sm + Sm::BUF + (ch & 1) * Sm::BUFSZ;
+        copy_mat_async(lc + ws.o_sk(), D, b + Sm::B_SK, LF, D, D);
+        copy_mat_async(lc + ws.o_sq(), D, b + Sm::B_SQ, LF, D, D);
+        copy_mat_async(lc + ws.o_mkq(), D, b + Sm::B_MKQ, LF, D, D);
+        copy_mat_async(lc + ws.o_p() + c0, DV, b + Sm::B_P, LB, D, NB);
+        copy_mat_async(lc + ws.o_t() + c0, DV, b + Sm::B_T, LB, D, NB);
+        copy_mat_async(lc + ws.o_mqp() + c0, DV, b + Sm::B_MQP, LB, D, NB);
+    };
+    if (nch > 0) issue(0);
+    cp_async_commit();
     // initial state: state_in or zeros
     for (int e = threadIdx.x; e < D * D; e += kThreads)
         SK[(e / D) * LF + e % D] = a.sin_S ? a.sin_S[(size_t)u * D * D + e] : 0.f;
@@ -151,9 +165,10 @@ __global__ void __launch_bounds__(kThreads) fwd3_scan_kernel(Fwd3Args a) {
     }
     __syncthreads();
     for (int ch = 0; ch < nch; ++ch) {
-        const float *lc = loc + (size_t)ch * ws.loc_floats();
-        float *so = st + (size_t)ch * ws.st_floats();
+        if (ch + 1 < nch) issue(ch + 1);
+        cp_async_commit();
         // this chunk's prefix state
+        float *so = st + (size_t)ch * ws.st_floats();
         for (int e = threadIdx.x; e < ROWS * D; e += kThreads) {
             const int r = r0 + e / D, x = e % D;
             so[ws.s_sk() + (size_t)r * D + x] = SK[r * LF + x];
@@ -163,29 +178,30 @@ __global__ void __launch_bounds__(kThreads) fwd3_scan_kernel(Fwd3Args a) {
             so[ws.s_p() + (size_t)r * DV + c0 + x] = Pb[r * LB + x];
             so[ws.s_t() + (size_t)r * DV + c0 + x] = Tb[r * LB + x];
         }
-        // its local sums
-        load_mat(lc + ws.o_sk(), SKl, LF, D, D);
-        load_mat(lc + ws.o_sq(), SQl, LF, D, D);
-        load_mat(lc + ws.o_mkq(), MKQl, LF, D, D);
-        for (int e = threadIdx.x; e < D * NB; e += kThreads) {
-            const int r = e / NB, x = e % NB;
-            const size_t g = (size_t)r * DV + c0 + x;
-            Pl[r * LB + x] = lc[ws.o_p() + g];
-            Tl[r * LB + x] = lc[ws.o_t() + g];
-            MQPl[r * LB + x] = lc[ws.o_mqp() + g];
-        }
+        cp_async_wait<1>();  // chunk ch's copies (the group before the one just committed)
         __syncthreads();
+        const float *b = sm + Sm::BUF + (ch & 1) * Sm::BUFSZ;
+        const float *SKl = b + Sm::B_SK, *SQl = b + Sm::B_SQ, *MKQl = b + Sm::B_MKQ;
+        const float *Pl = b + Sm::B_P, *Tl = b + Sm::B_T, *MQPl = b + Sm::B_MQP;
         // X = M^QP_B + S^Q_B P_A  (block columns)
-        tiles<false>(D, NB, [&](float (&acc)[4][4], int m0, int n0, int ns) {
-            mac<false, false>(acc, SQl, LF, Pb, LB, m0, n0, ns, D);
-            each(acc, m0, n0, ns, [&](int i, int j, float x) { X[i * LB + j] = MQPl[i * LB + j] + x; });
+        tiles22(D, NB, [&](float (&acc)[2][2], int m0, int n0) {
+            mac22(acc, SQl, LF, Pb, LB, m0, n0, D);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    X[(m0 + i) * LB + n0 + j] = MQPl[(m0 + i) * LB + n0 + j] + acc[i][j];
         });
         __syncthreads();
         // T <- T + T_B + S^K_A X + M^KQ_B P_A
-        tiles<false>(D, NB, [&](float (&acc)[4][4], int m0, int n0, int ns) {
-            mac<false, false>(acc, SK, LF, X, LB, m0, n0, ns, D);
-            mac<false, false>(acc, MKQl, LF, Pb, LB, m0, n0, ns, D);
-            each(acc, m0, n0, ns, [&](int i, int j, float x) { Tb[i * LB + j] += Tl[i * LB + j] + x; });
+        tiles22(D, NB, [&](float (&acc)[2][2], int m0, int n0) {
+            mac22(acc, SK, LF, X, LB, m0, n0, D);
+            mac22(acc, MKQl, LF, Pb, LB, m0, n0, D);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    Tb[(m0 + i) * LB + n0 + j] += Tl[(m0 + i) * LB + n0 + j] + acc[i][j];
         });
         __syncthreads();
         // P <- P + P_B, S^K <- S^K + S^K_B
@@ -199,6 +215,7 @@ __global__ void __launch_bounds__(kThreads) fwd3_scan_kernel(Fwd3Args a) {
         }
         __syncthreads();
     }
+    cp_async_wait<0>();
     // final state
     if (a.sout_S) {
         for (int e = threadIdx.x; e < ROWS * D; e += kThreads) {
@@ -234,17 +251,20 @@ __global__ void __launch_bounds__(kThreads) fwd3_out_kernel(Fwd3Args a) {
     const Ws3 ws{D, DV};
     const float *so =
         a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
+    // the prefix state arrives asynchronously while A~ is formed
+    copy_mat_async(so + ws.s_sk(), D, SK, Sm::LQ, D, D);
+    copy_mat_async(so + ws.s_p(), DV, P, Sm::LV, D, DV);
+    copy_mat_async(so + ws.s_t(), DV, Tp, Sm::LV, D, DV);
+    cp_async_commit();
     load_rows(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L, D);
     load_rows(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L, D);
     load_rows(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L, DV);
-    load_mat(so + ws.s_sk(), SK, Sm::LQ, D, D);
-    load_mat(so + ws.s_p(), P, Sm::LV, D, DV);
-    load_mat(so + ws.s_t(), Tp, Sm::LV, D, DV);
     __syncthreads();
     tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, true>(acc, Q, Sm::LQ, K, Sm::LQ, m0, n0, ns, D);
         each(acc, m0, n0, ns, [&](int t, int s, float x) { A[t * Sm::LT + s] = s <= t ? x : 0.f; });
     });
+    cp_async_wait<0>();
     __syncthreads();
     // U = Q S^K_p + A~ K;  W = Q P_p + A~ V
     tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {

@@ -125,8 +125,54 @@ __device__ __forceinline__ void load_rows(const T *src, float *dst, int ld, int 
     }
 }
 
-__device__ __forceinline__ void load_mat(const float *src, float *dst, int ld, int rows, int W) {
-    for (int e = threadIdx.x; e < rows * W; e += kThreads) dst[(e / W) * ld + e % W] = src[e];
+// ---- asynchronous global -> shared copies (16-byte cp.async, L2 only) -------------
+__device__ __forceinline__ void cp_async16(float *dst, const float *src) {
+    const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// rows x cols floats (cols a multiple of 4; both leading dimensions multiples of 4,
+// both bases 16-byte aligned) from global (ld src_ld) to shared (ld dst_ld).
+__device__ __forceinline__ void copy_mat_async(const float *src, int src_ld, float *dst, int dst_ld, int rows,
+                                               int cols) {
+    const int q = cols / 4;
+    for (int e = threadIdx.x; e < rows * q; e += kThreads) {
+        const int r = e / q, c = (e % q) * 4;
+        cp_async16(dst + (size_t)r * dst_ld + c, src + (size_t)r * src_ld + c);
+    }
+}
+
+// acc[i][j] += sum_k A[(m0+i)*lda + k] B[k*ldb + n0+j] for a 2x2 tile (K a multiple of
+// 4; lda a multiple of 4; n0 even, ldb even).
+__device__ __forceinline__ void mac22(float (&acc)[2][2], const float *A, int lda, const float *B, int ldb, int m0,
+                                      int n0, int K) {
+#pragma unroll 4
+    for (int k = 0; k < K; k += 4) {
+        const float4 a0 = *reinterpret_cast<const float4 *>(A + (size_t)m0 * lda + k);
+        const float4 a1 = *reinterpret_cast<const float4 *>(A + (size_t)(m0 + 1) * lda + k);
+        const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float2 b = *reinterpret_cast<const float2 *>(B + (size_t)(k + kk) * ldb + n0);
+            acc[0][0] = fmaf(av0[kk], b.x, acc[0][0]);
+            acc[0][1] = fmaf(av0[kk], b.y, acc[0][1]);
+            acc[1][0] = fmaf(av1[kk], b.x, acc[1][0]);
+            acc[1][1] = fmaf(av1[kk], b.y, acc[1][1]);
+        }
+    }
+}
+
+// Every 2x2 tile of an M x N result (M, N even), one per thread per round.
+template <class Body>
+__device__ __forceinline__ void tiles22(int M, int N, Body body) {
+    const int tn = N / 2, count = (M / 2) * tn;
+    for (int t = threadIdx.x; t < count; t += kThreads) {
+        float acc[2][2] = {};
+        body(acc, (t / tn) * 2, (t % tn) * 2);
+    }
 }
 
 }  // namespace tile

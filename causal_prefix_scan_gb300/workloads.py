@@ -93,9 +93,14 @@ class DecodeWorkload:
     steps: int
     chunk: int
     seed: int
+    order: int = 2            # 3: third-order decode on the state (S^K, P, T)
 
 
 DECODE = DecodeWorkload("decode_256x32_d128_prefix4096_steps1024", 256, 32, 128, 128, 4096, 1024, 128, seed=5)
+# Third-order decode on the same pairs and widths.  Its state is drawn (seeded, on the
+# device) instead of prefilled: the forward covers widths up to 64, and the cost of a
+# step does not depend on the state's values.
+DECODE3 = DecodeWorkload("decode3_256x32_d128_steps1024", 256, 32, 128, 128, 0, 1024, 0, seed=12, order=3)
 
 
 def round_bf16(x: np.ndarray) -> np.ndarray:
