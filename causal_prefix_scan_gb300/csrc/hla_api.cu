@@ -318,7 +318,9 @@ hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const
     a.sout_T = state_out ? state_out->T : nullptr;
     a.workspace = static_cast<float *>(workspace);
     a.events = reinterpret_cast<cudaEvent_t const *>(phase_events);
-    cudaError_t e = hla::fwd3_launch(a, st);
+    cudaError_t e = status_ptr(&a.err);
+    if (e != cudaSuccess) return cuda_fail(e, "status word");
+    e = hla::fwd3_launch(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "third-order forward launch");
     return HLA_OK;
 }

@@ -19,11 +19,20 @@
 //
 // Three launches: (1) one CTA per chunk writes the local sums; (2) the scan, one CTA
 // per (b,h) and column block of dv, walks the chunks and writes each chunk's prefix
-// state (and the final state); (3) one CTA per chunk forms the outputs.
+// state (and the final state); (3) one CTA per chunk forms the outputs.  For bf16
+// inputs with d = dv = chunk = 64, (1) and (3) run on the tensor cores
+// (hla_fwd3_tc.cu); the kernels here are the CUDA-core versions for every shape.
 #pragma once
+#include <type_traits>
+
 #include "hla_smem_tile.cuh"
 
 namespace hla {
+namespace fwd3tc {
+cudaError_t local_tc(const Fwd3Args &a, cudaStream_t st);
+cudaError_t out_tc(const Fwd3Args &a, cudaStream_t st);
+}  // namespace fwd3tc
+
 namespace fwd3 {
 using namespace tile;
 constexpr int kSplit = 4;  // column blocks of dv per (b,h) in the scan
@@ -309,13 +318,22 @@ cudaError_t launch_t(const Fwd3Args &a, cudaStream_t st) {
     if ((e = smem_attr(fwd3_local_kernel<T, C, D, DV>, b1)) != cudaSuccess) return e;
     if ((e = smem_attr(fwd3_scan_kernel<C, D, DV>, b2)) != cudaSuccess) return e;
     if ((e = smem_attr(fwd3_out_kernel<T, C, D, DV>, b3)) != cudaSuccess) return e;
+    constexpr bool TC = std::is_same<T, __nv_bfloat16>::value && C == 64 && D == 64 && DV == 64;
     auto mark = [&](int i) { return a.events ? cudaEventRecord(a.events[i], st) : cudaSuccess; };
     if ((e = mark(0)) != cudaSuccess) return e;
-    fwd3_local_kernel<T, C, D, DV><<<units * nch, kThreads, b1, st>>>(a);
+    if constexpr (TC) {
+        if ((e = fwd3tc::local_tc(a, st)) != cudaSuccess) return e;
+    } else {
+        fwd3_local_kernel<T, C, D, DV><<<units * nch, kThreads, b1, st>>>(a);
+    }
     if ((e = mark(1)) != cudaSuccess) return e;
     fwd3_scan_kernel<C, D, DV><<<units * kSplit, kThreads, b2, st>>>(a);
     if ((e = mark(2)) != cudaSuccess) return e;
-    fwd3_out_kernel<T, C, D, DV><<<units * nch, kThreads, b3, st>>>(a);
+    if constexpr (TC) {
+        if ((e = fwd3tc::out_tc(a, st)) != cudaSuccess) return e;
+    } else {
+        fwd3_out_kernel<T, C, D, DV><<<units * nch, kThreads, b3, st>>>(a);
+    }
     if ((e = mark(3)) != cudaSuccess) return e;
     return cudaGetLastError();
 }

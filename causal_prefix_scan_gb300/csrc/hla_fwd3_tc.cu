@@ -1,0 +1,344 @@
+// hla_fwd3_tc.cu -- tensor-core (tcgen05 MMA, TMEM accumulators) kernels for the
+// chunk-local sums and the outputs of masked third-order HLA, bf16 inputs,
+// d = dv = chunk = 64.  The chunk algebra is that of hla_fwd3_simt.cuh
+// ("Higher-order Linear Attention", gist.science summary, sections 3 and 4):
+//   A~ = tril(Q K^T),  U = Q S^K_p + A~ K,  W = Q P_p + A~ V,  M = tril(Q U^T),
+//   O = Q T_p + M W;
+//   local sums (zero prefix): S^K = K^T K, S^Q = Q^T Q, M^KQ = U^T Q, P = K^T V,
+//   T = U^T W, M^QP = Q^T W.
+// One CTA (8 warps, two per TMEM lane quadrant) per chunk; every product is a
+// 64-row tcgen05.mma group issued by thread 0 from 128-byte-swizzled bf16 tiles.
+// The fp32 prefix states enter as bf16 hi + lo pairs (two MMAs each), so their
+// rounding is that of fp32; A~, U, W and M are rounded to bf16 between products.
+// The scan between the two kernels stays on the CUDA cores (hla_fwd3_simt.cuh).
+#include "hla_fwd3_simt.cuh"
+
+namespace hla {
+namespace fwd3tc {
+using fwd3::Ws3;
+namespace {
+
+constexpr int kTc = 256;
+constexpr int N64 = 64;
+constexpr int TILE = 64 * 64 * 2;  // one bf16 64 x 64 swizzled tile
+constexpr uint32_t kCols = 256;    // TMEM columns: four 64-column accumulators
+
+struct Ctx {
+    uint8_t *base;
+    uint64_t *bar;
+    uint32_t tb, ph;
+    int tid, warp, lane, quad, half;
+    int row, c0;  // the accumulator row this thread reads and its first of 16 columns
+    unsigned *err;
+
+    __device__ uint8_t *tile(int i) const { return base + i * TILE; }
+    __device__ uint32_t taddr(uint32_t slot, int col) const {
+        return tb + slot + ((uint32_t)(32 * quad) << 16) + (uint32_t)col;
+    }
+    // 16 columns [c0, c0 + 16) of row `row` of the 64-row accumulator at `slot`
+    __device__ void ld_row(uint32_t slot, float (&v)[16]) const {
+        tmem_ld16x2<16>(taddr(slot, half * 32), v);
+        tmem_wait_ld();
+    }
+    // shared-memory and TMEM writes of all threads visible to the MMAs issued next
+    __device__ void publish() const {
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    __device__ void commit() const {
+        if (tid == 0) umma_commit(bar);
+    }
+    // false: the bounded wait expired (status flag raised); uniform across the CTA
+    __device__ bool wait() {
+        const bool ok = mbar_wait(bar, ph, err);
+        ph ^= 1u;
+        tc_fence_after();
+        return !__syncthreads_or(!ok);
+    }
+};
+
+// ---- MMA groups (thread 0).  Every operand is one 64 x 64 tile.
+// A K-major [64 x 64] (rows = M), B K-major [N x 64]
+__device__ __forceinline__ void mma_kk(uint32_t d, const uint8_t *a, const uint8_t *b, bool acc) {
+    constexpr uint32_t id = make_idesc(64, N64, false, false);
+    const uint64_t da = make_sdesc(smem_u32(a), 16u, 1024u), db = make_sdesc(smem_u32(b), 16u, 1024u);
+#pragma unroll
+    for (int k = 0; k < 64; k += 16) {
+        const uint32_t kk = ((uint32_t)k * 2u) >> 4;
+        umma_f16(d, da + kk, db + kk, id, (acc || k > 0) ? 1u : 0u);
+    }
+}
+// A K-major [64 x 64], B MN-major [64 (contraction) x N]
+__device__ __forceinline__ void mma_km(uint32_t d, const uint8_t *a, const uint8_t *b, bool acc) {
+    constexpr uint32_t id = make_idesc(64, N64, false, true);
+    const uint64_t da = make_sdesc(smem_u32(a), 16u, 1024u), db = make_sdesc(smem_u32(b), 64u * 128u, 1024u);
+#pragma unroll
+    for (int k = 0; k < 64; k += 16)
+        umma_f16(d, da + (((uint32_t)k * 2u) >> 4), db + (uint32_t)(k * 8), id, (acc || k > 0) ? 1u : 0u);
+}
+// A MN-major [64 (contraction) x 64] read as 64 x 64, B MN-major [64 (contraction) x N]
+__device__ __forceinline__ void mma_mm(uint32_t d, const uint8_t *a, const uint8_t *b) {
+    constexpr uint32_t id = make_idesc(64, N64, true, true);
+    const uint64_t da = make_sdesc(smem_u32(a), 64u * 128u, 1024u), db = make_sdesc(smem_u32(b), 64u * 128u, 1024u);
+#pragma unroll
+    for (int k = 0; k < 64; k += 16) umma_f16(d, da + (uint32_t)(k * 8), db + (uint32_t)(k * 8), id, k > 0 ? 1u : 0u);
+}
+
+// L rows of 64 bf16 (row-major) into a swizzled tile; rows >= L are zero.
+__device__ __forceinline__ void load_tile_bf16(const __nv_bfloat16 *src, int L, uint8_t *tile) {
+    for (int e = threadIdx.x; e < 64 * 8; e += kTc) {
+        const int r = e >> 3, c = (e & 7) * 8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < L) v = *reinterpret_cast<const uint4 *>(src + (size_t)r * 64 + c);
+        *reinterpret_cast<uint4 *>(tile + tile_off(64, r, c)) = v;
+    }
+}
+// A 64 x 64 fp32 matrix (row-major) into bf16 hi and lo tiles (hi + lo = the value to
+// about 2^-17 relative).
+__device__ __forceinline__ void load_tile_hilo(const float *src, uint8_t *hi, uint8_t *lo) {
+    for (int e = threadIdx.x; e < 64 * 4; e += kTc) {
+        const int r = e >> 2, c = (e & 3) * 16;
+        float v[16], h[16], l[16];
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(src + (size_t)r * 64 + c + i);
+            v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            h[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+            l[i] = v[i] - h[i];
+        }
+        tile_store_row16(hi, 64, r, c, h);
+        tile_store_row16(lo, 64, r, c, l);
+    }
+}
+
+// Block setup shared by both kernels: barrier, TMEM allocation.  Returns false if
+// the shared window is not 1024-byte aligned (then nothing was allocated).
+__device__ bool setup(Ctx &x, uint8_t *smem, int ntiles, unsigned *err) {
+    x.base = smem;
+    x.bar = reinterpret_cast<uint64_t *>(smem + ntiles * TILE);
+    uint32_t *tptr = reinterpret_cast<uint32_t *>(smem + ntiles * TILE + 8);
+    int *bad = reinterpret_cast<int *>(smem + ntiles * TILE + 12);
+    x.tid = threadIdx.x;
+    x.warp = x.tid >> 5;
+    x.lane = x.tid & 31;
+    x.quad = x.warp & 3;
+    x.half = x.warp >> 2;
+    x.row = 16 * x.quad + (x.lane & 15);
+    x.c0 = x.half * 32 + (x.lane >> 4) * 16;
+    x.ph = 0;
+    x.err = err;
+    if (x.tid == 0) {
+        *bad = (smem_u32(smem) & 1023u) != 0;
+        mbar_init(x.bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (*bad) {
+        if (x.tid == 0) atomicOr(err, DEV_TIMEOUT);
+        return false;
+    }
+    if (x.warp == 0) {
+        tmem_alloc(tptr, kCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    x.tb = *tptr;
+    return true;
+}
+
+__device__ void teardown(const Ctx &x) {
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (x.warp == 0) tmem_dealloc(x.tb, kCols);
+}
+
+// 16 accumulator values of this thread's row into a tile, lower triangle kept
+__device__ __forceinline__ void store_tril(const Ctx &x, uint8_t *tile, float (&v)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        if (x.c0 + i > x.row) v[i] = 0.f;
+    tile_store_row16(tile, 64, x.row, x.c0, v);
+}
+
+__device__ __forceinline__ void st_row16(float *dst, const float (&v)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+}
+
+// tiles of the local-sums kernel
+enum { L_Q, L_K, L_V, L_A, L_U, L_W, L_N };
+// tiles of the output kernel
+enum { O_Q, O_K, O_V, O_SH, O_SL, O_PH, O_PL, O_TH, O_TL, O_A, O_U, O_W, O_N };
+
+__global__ void __launch_bounds__(kTc, 2) fwd3_local_tc_kernel(const __grid_constant__ Fwd3Args a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    Ctx x;
+    if (!setup(x, smem_raw, L_N, a.err)) return;
+    const int nch = (a.n + 63) / 64, u = blockIdx.x / nch, ch = blockIdx.x % nch;
+    const int t0 = ch * 64, L = min(64, a.n - t0);
+    const size_t r0 = ((size_t)u * a.n + t0) * 64;
+    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.q) + r0, L, x.tile(L_Q));
+    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.k) + r0, L, x.tile(L_K));
+    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.v) + r0, L, x.tile(L_V));
+    x.publish();
+    float v[16];
+    do {
+        // A~ = tril(Q K^T)
+        if (x.tid == 0) mma_kk(x.tb, x.tile(L_Q), x.tile(L_K), false);
+        x.commit();
+        if (!x.wait()) break;
+        x.ld_row(0, v);
+        store_tril(x, x.tile(L_A), v);
+        x.publish();
+        // U = A~ K, W = A~ V (no earlier state)
+        if (x.tid == 0) {
+            mma_km(x.tb + 64, x.tile(L_A), x.tile(L_K), false);
+            mma_km(x.tb + 128, x.tile(L_A), x.tile(L_V), false);
+        }
+        x.commit();
+        if (!x.wait()) break;
+        x.ld_row(64, v);
+        tile_store_row16(x.tile(L_U), 64, x.row, x.c0, v);
+        x.ld_row(128, v);
+        tile_store_row16(x.tile(L_W), 64, x.row, x.c0, v);
+        x.publish();
+        // S^K = K^T K, S^Q = Q^T Q, M^KQ = U^T Q, P = K^T V (rows = feature index)
+        if (x.tid == 0) {
+            mma_mm(x.tb + 0, x.tile(L_K), x.tile(L_K));
+            mma_mm(x.tb + 64, x.tile(L_Q), x.tile(L_Q));
+            mma_mm(x.tb + 128, x.tile(L_U), x.tile(L_Q));
+            mma_mm(x.tb + 192, x.tile(L_K), x.tile(L_V));
+        }
+        x.commit();
+        if (!x.wait()) break;
+        const Ws3 ws{64, 64};
+        float *out = a.workspace + ((size_t)u * nch + ch) * ws.loc_floats();
+        const size_t ro = (size_t)x.row * 64 + x.c0;
+        x.ld_row(0, v);
+        st_row16(out + ws.o_sk() + ro, v);
+        x.ld_row(64, v);
+        st_row16(out + ws.o_sq() + ro, v);
+        x.ld_row(128, v);
+        st_row16(out + ws.o_mkq() + ro, v);
+        x.ld_row(192, v);
+        st_row16(out + ws.o_p() + ro, v);
+        x.publish();  // the reads of columns 0-127 precede their reuse
+        // T = U^T W, M^QP = Q^T W
+        if (x.tid == 0) {
+            mma_mm(x.tb + 0, x.tile(L_U), x.tile(L_W));
+            mma_mm(x.tb + 64, x.tile(L_Q), x.tile(L_W));
+        }
+        x.commit();
+        if (!x.wait()) break;
+        x.ld_row(0, v);
+        st_row16(out + ws.o_t() + ro, v);
+        x.ld_row(64, v);
+        st_row16(out + ws.o_mqp() + ro, v);
+    } while (false);
+    teardown(x);
+}
+
+__global__ void __launch_bounds__(kTc, 2) fwd3_out_tc_kernel(const __grid_constant__ Fwd3Args a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    Ctx x;
+    if (!setup(x, smem_raw, O_N, a.err)) return;
+    const int nch = (a.n + 63) / 64, u = blockIdx.x / nch, ch = blockIdx.x % nch;
+    const int t0 = ch * 64, L = min(64, a.n - t0);
+    const size_t r0 = ((size_t)u * a.n + t0) * 64;
+    const Ws3 ws{64, 64};
+    const float *so = a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
+    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.q) + r0, L, x.tile(O_Q));
+    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.k) + r0, L, x.tile(O_K));
+    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.v) + r0, L, x.tile(O_V));
+    load_tile_hilo(so + ws.s_sk(), x.tile(O_SH), x.tile(O_SL));
+    load_tile_hilo(so + ws.s_p(), x.tile(O_PH), x.tile(O_PL));
+    load_tile_hilo(so + ws.s_t(), x.tile(O_TH), x.tile(O_TL));
+    x.publish();
+    constexpr uint32_t SA = 0, SU = 64, SW = 128, SO = 192;
+    float v[16];
+    do {
+        // A~ = Q K^T, and the prefix-state terms Q S^K_p, Q P_p, Q T_p
+        if (x.tid == 0) {
+            mma_kk(x.tb + SA, x.tile(O_Q), x.tile(O_K), false);
+            mma_km(x.tb + SU, x.tile(O_Q), x.tile(O_SH), false);
+            mma_km(x.tb + SU, x.tile(O_Q), x.tile(O_SL), true);
+            mma_km(x.tb + SW, x.tile(O_Q), x.tile(O_PH), false);
+            mma_km(x.tb + SW, x.tile(O_Q), x.tile(O_PL), true);
+            mma_km(x.tb + SO, x.tile(O_Q), x.tile(O_TH), false);
+            mma_km(x.tb + SO, x.tile(O_Q), x.tile(O_TL), true);
+        }
+        x.commit();
+        if (!x.wait()) break;
+        x.ld_row(SA, v);
+        store_tril(x, x.tile(O_A), v);
+        x.publish();
+        // U += A~ K, W += A~ V
+        if (x.tid == 0) {
+            mma_km(x.tb + SU, x.tile(O_A), x.tile(O_K), true);
+            mma_km(x.tb + SW, x.tile(O_A), x.tile(O_V), true);
+        }
+        x.commit();
+        if (!x.wait()) break;
+        x.ld_row(SU, v);
+        tile_store_row16(x.tile(O_U), 64, x.row, x.c0, v);
+        x.ld_row(SW, v);
+        tile_store_row16(x.tile(O_W), 64, x.row, x.c0, v);
+        x.publish();
+        // M = tril(Q U^T)
+        if (x.tid == 0) mma_kk(x.tb + SA, x.tile(O_Q), x.tile(O_U), false);
+        x.commit();
+        if (!x.wait()) break;
+        x.ld_row(SA, v);
+        store_tril(x, x.tile(O_A), v);
+        x.publish();
+        // O += M W
+        if (x.tid == 0) mma_km(x.tb + SO, x.tile(O_A), x.tile(O_W), true);
+        x.commit();
+        if (!x.wait()) break;
+        x.ld_row(SO, v);
+        if (x.row < L) {
+            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o) + r0 + (size_t)x.row * 64 + x.c0;
+            uint4 p0, p1;
+            p0.x = pack_bf16(v[0], v[1]);   p0.y = pack_bf16(v[2], v[3]);
+            p0.z = pack_bf16(v[4], v[5]);   p0.w = pack_bf16(v[6], v[7]);
+            p1.x = pack_bf16(v[8], v[9]);   p1.y = pack_bf16(v[10], v[11]);
+            p1.z = pack_bf16(v[12], v[13]); p1.w = pack_bf16(v[14], v[15]);
+            reinterpret_cast<uint4 *>(o)[0] = p0;
+            reinterpret_cast<uint4 *>(o)[1] = p1;
+        }
+    } while (false);
+    teardown(x);
+}
+
+constexpr size_t kLocalSmem = L_N * TILE + 64, kOutSmem = O_N * TILE + 64;
+
+}  // namespace
+
+cudaError_t local_tc(const Fwd3Args &a, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(fwd3_local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kLocalSmem);
+    if (e != cudaSuccess) return e;
+    const int nch = (a.n + 63) / 64;
+    fwd3_local_tc_kernel<<<a.B * a.H * nch, kTc, kLocalSmem, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t out_tc(const Fwd3Args &a, cudaStream_t st) {
+    cudaError_t e =
+        cudaFuncSetAttribute(fwd3_out_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
+    if (e != cudaSuccess) return e;
+    const int nch = (a.n + 63) / 64;
+    fwd3_out_tc_kernel<<<a.B * a.H * nch, kTc, kOutSmem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace fwd3tc
+}  // namespace hla

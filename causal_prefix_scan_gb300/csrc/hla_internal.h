@@ -90,6 +90,7 @@ struct Fwd3Args {
     float *sout_S, *sout_P, *sout_T;     // state after the last token (all NULL: skip)
     float *workspace;
     cudaEvent_t const *events;  // NULL or four events recorded at the phase boundaries
+    unsigned *err;              // sticky device status word (bounded waits of the tensor-core kernels)
 };
 
 struct Decode3Args {
