@@ -52,6 +52,7 @@ BWD_METRIC = "masked 2nd-order HLA backward (dq, dk, dv) tokens/s and % roofline
 FWD3_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd3_simt.cuh")
 FWD3_METRIC = "masked 3rd-order HLA forward tokens/s and % roofline on 1 GB300"
 FWD3_DISPATCH_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd3_simt.cu")
+FWD3_TC_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd3_tc.cu")
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz (maximum SM clock)
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2070e6 / 1e12
 
@@ -549,8 +550,10 @@ def bench_phased(args, w: W.Workload, rank, world, local, dist):
     else:
         params = hla.make_params(sets[0][0][0], sets[0][0][2], w.chunk)
         ws_bytes = hla.hla_forward3_workspace_size(params)
-        names = ("fwd3_local_kernel", "fwd3_scan_kernel", "fwd3_out_kernel")
-        fl = fwd3_flops_per_token_head(w)
+        tc = w.dtype == "bf16" and w.d == w.dv == w.chunk == 64  # local sums and outputs on the tensor cores
+        names = ("fwd3_local_tc_kernel" if tc else "fwd3_local_kernel", "fwd3_scan_kernel",
+                 "fwd3_out_tc_kernel" if tc else "fwd3_out_kernel")
+        fl = dict(zip(names, fwd3_flops_per_token_head(w).values()))
         src, metric = FWD3_KERNEL_SRC, FWD3_METRIC
         st3 = hla.State3.empty(w.B * w.H, w.d, w.dv, device=dev)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -639,17 +642,28 @@ def bench_phased(args, w: W.Workload, rank, world, local, dist):
            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in outs_host[0])), "steps": Ke,
            "overlap": "upload of step i+1 and download of step i-1 on their own streams during step i"}
 
-    # ---- roofline of the dominant kernel: fp32 FMA work on the CUDA cores
+    # ---- roofline of the dominant kernel: fp32 FMA work on the CUDA cores, or bf16
+    # MMAs for the tensor-core kernels
+    peaks, peak_kind = load_peaks()
+    alu_src = "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz (fp32 FMA, CUDA cores)"
+    tc_src = (f"{peak_kind} bf16 dense (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback bf16 dense")
+
+    def bound_of(nm):
+        return ("tensor", peaks["bf16_tflops"], tc_src) if "_tc_" in nm else ("alu", FP32_ALU_TFLOPS, alu_src)
+
     top = max(phase_ms, key=phase_ms.get)
     flops_launch = fl[top] * w.token_heads
     ach = flops_launch / (phase_ms[top] / 1e3) / 1e12
-    roofline = {"bound": "alu", "achieved": ach, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
-                "frac": ach / FP32_ALU_TFLOPS,
-                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz (fp32 FMA, CUDA cores)",
-                "traffic": traffic_for(top, w.name, src), "kernel": top,
+    bnd, peak, psrc = bound_of(top)
+    src_top = FWD3_TC_KERNEL_SRC if "_tc_" in top else src
+    roofline = {"bound": bnd, "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                "peak_source": psrc, "traffic": traffic_for(top, w.name, src_top), "kernel": top,
                 "alg_flops_per_launch": flops_launch,
                 "phases": {nm: {"ms": phase_ms[nm], "alg_flops": fl[nm] * w.token_heads,
-                                "tflops": fl[nm] * w.token_heads / (phase_ms[nm] / 1e3) / 1e12 if phase_ms[nm] else None}
+                                "tflops": fl[nm] * w.token_heads / (phase_ms[nm] / 1e3) / 1e12 if phase_ms[nm] else None,
+                                "bound": bound_of(nm)[0],
+                                "frac": (fl[nm] * w.token_heads / (phase_ms[nm] / 1e3) / 1e12) / bound_of(nm)[1]
+                                if phase_ms[nm] else None}
                            for nm in names},
                 "alg_bytes_per_step": set_bytes}
     cfg = config_dict(w, nsets, set_bytes, world)

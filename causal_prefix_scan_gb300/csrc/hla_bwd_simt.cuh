@@ -86,10 +86,10 @@ __global__ void __launch_bounds__(kThreads) bwd_local_kernel(BwdArgs a) {
     const bool decay = (a.flags & HLA_DECAY) != 0;
     const float lg = log2f(decay ? a.gamma[u % a.H] : 1.f);
     const size_t rq = ((size_t)u * a.n + t0) * D, rv = ((size_t)u * a.n + t0) * DV;
-    load_rows(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L, D);
-    load_rows(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L, D);
-    load_rows(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L, DV);
-    load_rows(static_cast<const T *>(a.go) + rv, G, Sm::LV, C, L, DV);
+    load_rows<D>(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L);
+    load_rows<D>(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L);
+    load_rows<DV>(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L);
+    load_rows<DV>(static_cast<const T *>(a.go) + rv, G, Sm::LV, C, L);
     fill_gp(gp, C, lg, decay);
     __syncthreads();
     for (int s = threadIdx.x; s < C; s += kThreads) {
@@ -102,21 +102,21 @@ __global__ void __launch_bounds__(kThreads) bwd_local_kernel(BwdArgs a) {
         w[5 * C + s] = in ? gp[s] : 0.f;                // Oloc
     }
     // A~ = tril(g^{t-s} Q K^T), P = tril(g^{2(s-b)} G V^T)
-    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<true, C, C>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, true>(acc, Q, Sm::LQ, K, Sm::LQ, m0, n0, ns, D);
         each(acc, m0, n0, ns, [&](int t, int s, float x) { A[t * Sm::LT + s] = s <= t ? gp[t - s] * x : 0.f; });
     });
-    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<true, C, C>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, true>(acc, G, Sm::LV, V, Sm::LV, m0, n0, ns, DV);
         each(acc, m0, n0, ns, [&](int s, int b, float x) { P[s * Sm::LT + b] = b <= s ? gp[2 * (s - b)] * x : 0.f; });
     });
     __syncthreads();
     // U = A~ K (the part of u without the earlier state), dU = P^T Q
-    tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, C, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, false>(acc, A, Sm::LT, K, Sm::LQ, m0, n0, ns, C);
         each(acc, m0, n0, ns, [&](int t, int i, float x) { U[t * Sm::LQ + i] = x; });
     });
-    tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, C, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, P, Sm::LT, Q, Sm::LQ, m0, n0, ns, C);
         each(acc, m0, n0, ns, [&](int t, int i, float x) { dU[t * Sm::LQ + i] = x; });
     });
@@ -126,27 +126,27 @@ __global__ void __launch_bounds__(kThreads) bwd_local_kernel(BwdArgs a) {
     auto put = [&](size_t off, int ld) {
         return [=](int i, int j, float x) { out[off + (size_t)i * ld + j] = x; };
     };
-    tiles<false>(D, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, D, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, K, Sm::LQ, K, Sm::LQ, m0, n0, ns, C, w + 0 * C);
         each(acc, m0, n0, ns, put(ws.o_sloc(), D));
     });
-    tiles<false>(D, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, D, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, Q, Sm::LQ, V, Sm::LV, m0, n0, ns, C, w + 1 * C);
         each(acc, m0, n0, ns, put(ws.o_cq(), DV));
     });
-    tiles<false>(D, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, D, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, U, Sm::LQ, V, Sm::LV, m0, n0, ns, C, w + 2 * C);
         each(acc, m0, n0, ns, put(ws.o_xloc(), DV));
     });
-    tiles<false>(D, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, D, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, Q, Sm::LQ, G, Sm::LV, m0, n0, ns, C, w + 3 * C);
         each(acc, m0, n0, ns, put(ws.o_lloc(), DV));
     });
-    tiles<false>(DV, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, DV, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, V, Sm::LV, Q, Sm::LQ, m0, n0, ns, C, w + 4 * C);
         each(acc, m0, n0, ns, put(ws.o_w(), D));
     });
-    tiles<false>(D, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, D, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, dU, Sm::LQ, Q, Sm::LQ, m0, n0, ns, C, w + 5 * C);
         each(acc, m0, n0, ns, put(ws.o_oloc(), D));
     });
@@ -167,35 +167,34 @@ struct ScanSmem {
     // F: S or Lam (D x <= WMAX); BK: the column block of X or Om; then two buffers of
     // FL (the increment of F), R (the product operand block, Cq or W, <= WMAX rows)
     // and BL (the block increment)
-    static constexpr int F = 0, BK = F + D * FW, BUF = BK + D * LB;
+    static constexpr int F = 0, BK = F + D * FW, RED = BK + D * LB, BUF = RED + kThreads * 16;
     static constexpr int B_FL = 0, B_R = D * FW, B_BL = B_R + WMAX * LB, BUFSZ = B_BL + D * LB;
     static constexpr int TOTAL = BUF + 2 * BUFSZ;
 };
 
-template <int C, int D, int DV>
-__global__ void __launch_bounds__(kThreads) bwd_scan_kernel(BwdArgs a) {
+// One direction of the scan (DIR 0: S and X forward; DIR 1: Lam and Om backward).
+template <int C, int D, int DV, int DIR>
+__device__ __forceinline__ void scan_dir(const BwdArgs &a, float *sm, int part, int u) {
     using Sm = ScanSmem<C, D, DV>;
-    extern __shared__ __align__(16) float sm[];
-    float *F = sm + Sm::F, *Bk = sm + Sm::BK;
-    const int dir = blockIdx.x & 1, part = (blockIdx.x >> 1) % kSplit, u = (blockIdx.x >> 1) / kSplit;
-    const int nch = (a.n + C - 1) / C;
+    // DIR 0: F = S (D x D), block of X (D x DV), R = block of Cq (D x DV)
+    // DIR 1: F = Lam (D x DV), block of Om (D x D), R = block of W (DV x D)
+    constexpr int FWD = DIR == 0 ? D : DV, BW = DIR == 0 ? DV : D, NBD = BW / kSplit;
+    constexpr int RK = DIR == 0 ? D : DV;  // inner dimension of F R
+    constexpr int ROWS = D / kSplit;
+    float *F = sm + Sm::F, *Bk = sm + Sm::BK, *red = sm + Sm::RED;
+    const int nch = (a.n + C - 1) / C, c0 = part * NBD, rows0 = part * ROWS;
     const bool decay = (a.flags & HLA_DECAY) != 0;
     const float lg = log2f(decay ? a.gamma[u % a.H] : 1.f);
     const BwdWs ws{D, DV};
     const float *loc = a.workspace + (size_t)u * nch * ws.loc_floats();
     float *st = a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + (size_t)u * nch * ws.st_floats();
-    // dir 0: F = S (D x D), block of X (D x DV), R = block of Cq (D x DV)
-    // dir 1: F = Lam (D x DV), block of Om (D x D), R = block of W (DV x D)
-    const int fw = dir == 0 ? D : DV, bw = dir == 0 ? DV : D, nb = bw / kSplit, c0 = part * nb;
-    const int rk = dir == 0 ? D : DV;  // inner dimension of F R
-    const int rows = D / kSplit, rows0 = part * rows;
-    auto chunk_at = [&](int it) { return dir == 0 ? it : nch - 1 - it; };
+    auto chunk_at = [&](int it) { return DIR == 0 ? it : nch - 1 - it; };
     auto issue = [&](int it) {  // the local sums of step it into buffer it & 1
         const float *lc = loc + (size_t)chunk_at(it) * ws.loc_floats();
         float *b = sm + Sm::BUF + (it & 1) * Sm::BUFSZ;
-        copy_mat_async(lc + (dir == 0 ? ws.o_sloc() : ws.o_lloc()), fw, b + Sm::B_FL, Sm::FW, D, fw);
-        copy_mat_async(lc + (dir == 0 ? ws.o_cq() : ws.o_w()) + c0, bw, b + Sm::B_R, Sm::LB, rk, nb);
-        copy_mat_async(lc + (dir == 0 ? ws.o_xloc() : ws.o_oloc()) + c0, bw, b + Sm::B_BL, Sm::LB, D, nb);
+        copy_mat_async<FWD>(lc + (DIR == 0 ? ws.o_sloc() : ws.o_lloc()), FWD, b + Sm::B_FL, Sm::FW, D);
+        copy_mat_async<NBD>(lc + (DIR == 0 ? ws.o_cq() : ws.o_w()) + c0, BW, b + Sm::B_R, Sm::LB, RK);
+        copy_mat_async<NBD>(lc + (DIR == 0 ? ws.o_xloc() : ws.o_oloc()) + c0, BW, b + Sm::B_BL, Sm::LB, D);
     };
     if (nch > 0) issue(0);
     cp_async_commit();
@@ -210,39 +209,43 @@ __global__ void __launch_bounds__(kThreads) bwd_scan_kernel(BwdArgs a) {
         const float f1 = decay ? gpow(lg, (float)L) : 1.f, f2 = decay ? gpow(lg, (float)(2 * L)) : 1.f;
         float *so = st + (size_t)ch * ws.st_floats();
         // the states this chunk starts from (S_p, X_p) or ends into (Lam_next, Om_next)
-        float *fo = so + (dir == 0 ? ws.o_sp() : ws.o_lam()), *bo = so + (dir == 0 ? ws.o_xp() : ws.o_om());
-        for (int e = threadIdx.x; e < rows * fw; e += kThreads) {
-            const int r = rows0 + e / fw, x = e % fw;
-            fo[(size_t)r * fw + x] = F[r * Sm::FW + x];
+        float *fo = so + (DIR == 0 ? ws.o_sp() : ws.o_lam()), *bo = so + (DIR == 0 ? ws.o_xp() : ws.o_om());
+        for (int e = threadIdx.x; e < ROWS * FWD; e += kThreads) {
+            const int r = rows0 + e / FWD, x = e % FWD;
+            fo[(size_t)r * FWD + x] = F[r * Sm::FW + x];
         }
-        for (int e = threadIdx.x; e < D * nb; e += kThreads) {
-            const int r = e / nb, x = e % nb;
-            bo[(size_t)r * bw + c0 + x] = Bk[r * Sm::LB + x];
+        for (int e = threadIdx.x; e < D * NBD; e += kThreads) {
+            const int r = e / NBD, x = e % NBD;
+            bo[(size_t)r * BW + c0 + x] = Bk[r * Sm::LB + x];
         }
         cp_async_wait<1>();  // step it's copies (the group before the one just committed)
         __syncthreads();
         const float *b = sm + Sm::BUF + (it & 1) * Sm::BUFSZ;
         const float *Fl = b + Sm::B_FL, *R = b + Sm::B_R, *Bl = b + Sm::B_BL;
-        // block <- f_b block + Bl + F R  (F the state before this chunk's update)
-        const float fb = dir == 0 ? f2 : f1, ff = dir == 0 ? f1 : f2;
-        tiles22(D, nb, [&](float (&acc)[2][2], int m0, int n0) {
-            mac22(acc, F, Sm::FW, R, Sm::LB, m0, n0, rk);
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int o = (m0 + i) * Sm::LB + n0 + j;
-                    Bk[o] = fb * Bk[o] + Bl[o] + acc[i][j];
-                }
-        });
+        // block <- f_b block + Bl + F R  (F the state before this chunk's update), F R over all threads
+        const float fb = DIR == 0 ? f2 : f1, ff = DIR == 0 ? f1 : f2;
+        mac_ksplit<D, NBD, RK>(F, Sm::FW, R, Sm::LB, red);
         __syncthreads();
-        for (int e = threadIdx.x; e < D * fw; e += kThreads) {
-            const int r = e / fw, x = e % fw;
+        for (int e = threadIdx.x; e < D * NBD; e += kThreads) {
+            const int o = (e / NBD) * Sm::LB + e % NBD;
+            Bk[o] = fb * Bk[o] + Bl[o] + ksplit_sum<D, NBD, RK>(red, e);
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < D * FWD; e += kThreads) {
+            const int r = e / FWD, x = e % FWD;
             F[r * Sm::FW + x] = ff * F[r * Sm::FW + x] + Fl[r * Sm::FW + x];
         }
         __syncthreads();
     }
     cp_async_wait<0>();
+}
+
+template <int C, int D, int DV>
+__global__ void __launch_bounds__(kThreads) bwd_scan_kernel(BwdArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    const int dir = blockIdx.x & 1, part = (blockIdx.x >> 1) % kSplit, u = (blockIdx.x >> 1) / kSplit;
+    if (dir == 0) scan_dir<C, D, DV, 0>(a, sm, part, u);
+    else scan_dir<C, D, DV, 1>(a, sm, part, u);
 }
 
 // ---- (3) gradients of one chunk ---------------------------------------------------
@@ -271,15 +274,15 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(BwdArgs a) {
     const float *so =
         a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
     // the chunk's states arrive asynchronously while A~ and P are formed
-    copy_mat_async(so + ws.o_sp(), D, Sp, Sm::LQ, D, D);
-    copy_mat_async(so + ws.o_xp(), DV, Xp, Sm::LV, D, DV);
-    copy_mat_async(so + ws.o_lam(), DV, Lam, Sm::LV, D, DV);
-    copy_mat_async(so + ws.o_om(), D, Om, Sm::LQ, D, D);
+    copy_mat_async<D>(so + ws.o_sp(), D, Sp, Sm::LQ, D);
+    copy_mat_async<DV>(so + ws.o_xp(), DV, Xp, Sm::LV, D);
+    copy_mat_async<DV>(so + ws.o_lam(), DV, Lam, Sm::LV, D);
+    copy_mat_async<D>(so + ws.o_om(), D, Om, Sm::LQ, D);
     cp_async_commit();
-    load_rows(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L, D);
-    load_rows(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L, D);
-    load_rows(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L, DV);
-    load_rows(static_cast<const T *>(a.go) + rv, G, Sm::LV, C, L, DV);
+    load_rows<D>(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L);
+    load_rows<D>(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L);
+    load_rows<DV>(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L);
+    load_rows<DV>(static_cast<const T *>(a.go) + rv, G, Sm::LV, C, L);
     fill_gp(gp, C, lg, decay);
     __syncthreads();
     float *r_u = rs, *r_x = rs + C, *r_l2 = rs + 2 * C, *r_l1 = rs + 3 * C;
@@ -290,30 +293,30 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(BwdArgs a) {
         r_l2[t] = in ? gp[2 * (L - t)] : 0.f;  // g^{2(L-tau)}
         r_l1[t] = in ? gp[L - t] : 0.f;        // g^{L-tau}
     }
-    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<true, C, C>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, true>(acc, Q, Sm::LQ, K, Sm::LQ, m0, n0, ns, D);
         each(acc, m0, n0, ns, [&](int t, int s, float x) { A[t * Sm::LT + s] = s <= t ? gp[t - s] * x : 0.f; });
     });
-    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<true, C, C>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, true>(acc, G, Sm::LV, V, Sm::LV, m0, n0, ns, DV);
         each(acc, m0, n0, ns, [&](int s, int b, float x) { P[s * Sm::LT + b] = b <= s ? gp[2 * (s - b)] * x : 0.f; });
     });
     cp_async_wait<0>();
     __syncthreads();
     // U = diag(g^{tau+1}) Q S_p + A~ K;  dU = P^T Q + diag(g^{2(L-tau)}) V Lam^T
-    tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, C, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac_rs<false, false>(acc, r_u, Q, Sm::LQ, Sp, Sm::LQ, m0, n0, ns, D);
         mac<false, false>(acc, A, Sm::LT, K, Sm::LQ, m0, n0, ns, C);
         each(acc, m0, n0, ns, [&](int t, int i, float x) { U[t * Sm::LQ + i] = x; });
     });
-    tiles<true>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<true, C, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, P, Sm::LT, Q, Sm::LQ, m0, n0, ns, C);
         mac_rs<false, true>(acc, r_l2, V, Sm::LV, Lam, Sm::LV, m0, n0, ns, DV);
         each(acc, m0, n0, ns, [&](int t, int i, float x) { dU[t * Sm::LQ + i] = x; });
     });
     __syncthreads();
     // B = tril(g^{t-a} dU K^T)
-    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<true, C, C>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, true>(acc, dU, Sm::LQ, K, Sm::LQ, m0, n0, ns, D);
         each(acc, m0, n0, ns, [&](int t, int s, float x) { Bm[t * Sm::LT + s] = s <= t ? gp[t - s] * x : 0.f; });
     });
@@ -322,7 +325,7 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(BwdArgs a) {
     T *gk = static_cast<T *>(a.grad_k) + rq;
     T *gv = static_cast<T *>(a.grad_v) + rv;
     // dQ = P U + diag(g^{2(tau+1)}) G X_p^T + diag(g^{tau+1}) dU S_p + B K   (S_p symmetric)
-    tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, C, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, false>(acc, P, Sm::LT, U, Sm::LQ, m0, n0, ns, C);
         mac_rs<false, true>(acc, r_x, G, Sm::LV, Xp, Sm::LV, m0, n0, ns, DV);
         mac_rs<false, false>(acc, r_u, dU, Sm::LQ, Sp, Sm::LQ, m0, n0, ns, D);
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(BwdArgs a) {
         });
     });
     // dK = A~^T dU + B^T Q + diag(g^{L-tau}) K (Om + Om^T)
-    tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, C, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, A, Sm::LT, dU, Sm::LQ, m0, n0, ns, C);
         mac<true, false>(acc, Bm, Sm::LT, Q, Sm::LQ, m0, n0, ns, C);
         mac_rs<false, false>(acc, r_l1, K, Sm::LQ, Om, Sm::LQ, m0, n0, ns, D);
@@ -343,13 +346,13 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(BwdArgs a) {
     });
     __syncthreads();
     // M = tril(g^{2(s-t)} Q U^T) into the slot of P
-    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<true, C, C>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, true>(acc, Q, Sm::LQ, U, Sm::LQ, m0, n0, ns, D);
         each(acc, m0, n0, ns, [&](int s, int t, float x) { P[s * Sm::LT + t] = t <= s ? gp[2 * (s - t)] * x : 0.f; });
     });
     __syncthreads();
     // dV = M^T G + diag(g^{2(L-tau)}) U Lam
-    tiles<false>(C, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, C, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, P, Sm::LT, G, Sm::LV, m0, n0, ns, C);
         mac_rs<false, false>(acc, r_l2, U, Sm::LQ, Lam, Sm::LV, m0, n0, ns, D);
         each(acc, m0, n0, ns, [&](int t, int j, float x) {

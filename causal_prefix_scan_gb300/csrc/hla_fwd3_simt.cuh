@@ -71,21 +71,21 @@ __global__ void __launch_bounds__(kThreads) fwd3_local_kernel(Fwd3Args a) {
     const int nch = (a.n + C - 1) / C, u = blockIdx.x / nch, ch = blockIdx.x % nch;
     const int t0 = ch * C, L = min(C, a.n - t0);
     const size_t rq = ((size_t)u * a.n + t0) * D, rv = ((size_t)u * a.n + t0) * DV;
-    load_rows(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L, D);
-    load_rows(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L, D);
-    load_rows(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L, DV);
+    load_rows<D>(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L);
+    load_rows<D>(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L);
+    load_rows<DV>(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L);
     __syncthreads();
-    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<true, C, C>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, true>(acc, Q, Sm::LQ, K, Sm::LQ, m0, n0, ns, D);
         each(acc, m0, n0, ns, [&](int t, int s, float x) { A[t * Sm::LT + s] = s <= t ? x : 0.f; });
     });
     __syncthreads();
     // U = A~ K, W = A~ V (no earlier state)
-    tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, C, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, false>(acc, A, Sm::LT, K, Sm::LQ, m0, n0, ns, C);
         each(acc, m0, n0, ns, [&](int t, int i, float x) { U[t * Sm::LQ + i] = x; });
     });
-    tiles<false>(C, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, C, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, false>(acc, A, Sm::LT, V, Sm::LV, m0, n0, ns, C);
         each(acc, m0, n0, ns, [&](int t, int j, float x) { W[t * Sm::LV + j] = x; });
     });
@@ -96,27 +96,27 @@ __global__ void __launch_bounds__(kThreads) fwd3_local_kernel(Fwd3Args a) {
         return [=](int i, int j, float x) { out[off + (size_t)i * ld + j] = x; };
     };
     // rows past the chunk's last token are zero in Q, K, V, U, W
-    tiles<false>(D, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, D, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, K, Sm::LQ, K, Sm::LQ, m0, n0, ns, C);
         each(acc, m0, n0, ns, put(ws.o_sk(), D));
     });
-    tiles<false>(D, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, D, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, Q, Sm::LQ, Q, Sm::LQ, m0, n0, ns, C);
         each(acc, m0, n0, ns, put(ws.o_sq(), D));
     });
-    tiles<false>(D, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, D, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, U, Sm::LQ, Q, Sm::LQ, m0, n0, ns, C);
         each(acc, m0, n0, ns, put(ws.o_mkq(), D));
     });
-    tiles<false>(D, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, D, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, K, Sm::LQ, V, Sm::LV, m0, n0, ns, C);
         each(acc, m0, n0, ns, put(ws.o_p(), DV));
     });
-    tiles<false>(D, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, D, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, U, Sm::LQ, W, Sm::LV, m0, n0, ns, C);
         each(acc, m0, n0, ns, put(ws.o_t(), DV));
     });
-    tiles<false>(D, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, D, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<true, false>(acc, Q, Sm::LQ, W, Sm::LV, m0, n0, ns, C);
         each(acc, m0, n0, ns, put(ws.o_mqp(), DV));
     });
@@ -131,7 +131,8 @@ __global__ void __launch_bounds__(kThreads) fwd3_local_kernel(Fwd3Args a) {
 template <int C, int D, int DV>
 struct ScanSmem3 {
     static constexpr int NB = DV / kSplit, LF = D + 4, LB = NB + 4;
-    static constexpr int SK = 0, PB = SK + D * LF, TB = PB + D * LB, X = TB + D * LB, BUF = X + D * LB;
+    static constexpr int SK = 0, PB = SK + D * LF, TB = PB + D * LB, X = TB + D * LB, Y = X + D * LB,
+                         RED = Y + D * LB, RSZ = kThreads * 16, BUF = RED + 2 * RSZ;
     // one buffer: S^K_B, S^Q_B, M^KQ_B (D x LF each), then the column blocks of P_B, T_B, M^QP_B
     static constexpr int B_SK = 0, B_SQ = D * LF, B_MKQ = 2 * D * LF, B_P = 3 * D * LF, B_T = B_P + D * LB,
                          B_MQP = B_T + D * LB, BUFSZ = B_MQP + D * LB;
@@ -143,7 +144,8 @@ __global__ void __launch_bounds__(kThreads) fwd3_scan_kernel(Fwd3Args a) {
     using Sm = ScanSmem3<C, D, DV>;
     constexpr int NB = Sm::NB, LF = Sm::LF, LB = Sm::LB;
     extern __shared__ __align__(16) float sm[];
-    float *SK = sm + Sm::SK, *Pb = sm + Sm::PB, *Tb = sm + Sm::TB, *X = sm + Sm::X;
+    float *SK = sm + Sm::SK, *Pb = sm + Sm::PB, *Tb = sm + Sm::TB, *X = sm + Sm::X, *Y = sm + Sm::Y;
+    float *red1 = sm + Sm::RED, *red2 = red1 + Sm::RSZ;
     const int part = blockIdx.x % kSplit, u = blockIdx.x / kSplit;
     const int nch = (a.n + C - 1) / C, c0 = part * NB;
     constexpr int ROWS = D / kSplit;
@@ -154,12 +156,12 @@ __global__ void __launch_bounds__(kThreads) fwd3_scan_kernel(Fwd3Args a) {
     auto issue = [&](int ch) {  // the local sums of chunk ch into buffer ch & 1
         const float *lc = loc + (size_t)ch * ws.loc_floats();
         float *b = sm + Sm::BUF + (ch & 1) * Sm::BUFSZ;
-        copy_mat_async(lc + ws.o_sk(), D, b + Sm::B_SK, LF, D, D);
-        copy_mat_async(lc + ws.o_sq(), D, b + Sm::B_SQ, LF, D, D);
-        copy_mat_async(lc + ws.o_mkq(), D, b + Sm::B_MKQ, LF, D, D);
-        copy_mat_async(lc + ws.o_p() + c0, DV, b + Sm::B_P, LB, D, NB);
-        copy_mat_async(lc + ws.o_t() + c0, DV, b + Sm::B_T, LB, D, NB);
-        copy_mat_async(lc + ws.o_mqp() + c0, DV, b + Sm::B_MQP, LB, D, NB);
+        copy_mat_async<D>(lc + ws.o_sk(), D, b + Sm::B_SK, LF, D);
+        copy_mat_async<D>(lc + ws.o_sq(), D, b + Sm::B_SQ, LF, D);
+        copy_mat_async<D>(lc + ws.o_mkq(), D, b + Sm::B_MKQ, LF, D);
+        copy_mat_async<NB>(lc + ws.o_p() + c0, DV, b + Sm::B_P, LB, D);
+        copy_mat_async<NB>(lc + ws.o_t() + c0, DV, b + Sm::B_T, LB, D);
+        copy_mat_async<NB>(lc + ws.o_mqp() + c0, DV, b + Sm::B_MQP, LB, D);
     };
     if (nch > 0) issue(0);
     cp_async_commit();
@@ -192,32 +194,26 @@ __global__ void __launch_bounds__(kThreads) fwd3_scan_kernel(Fwd3Args a) {
         const float *b = sm + Sm::BUF + (ch & 1) * Sm::BUFSZ;
         const float *SKl = b + Sm::B_SK, *SQl = b + Sm::B_SQ, *MKQl = b + Sm::B_MKQ;
         const float *Pl = b + Sm::B_P, *Tl = b + Sm::B_T, *MQPl = b + Sm::B_MQP;
-        // X = M^QP_B + S^Q_B P_A  (block columns)
-        tiles22(D, NB, [&](float (&acc)[2][2], int m0, int n0) {
-            mac22(acc, SQl, LF, Pb, LB, m0, n0, D);
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    X[(m0 + i) * LB + n0 + j] = MQPl[(m0 + i) * LB + n0 + j] + acc[i][j];
-        });
+        // S^Q_B P_A and M^KQ_B P_A (block columns), each over all threads
+        mac_ksplit<D, NB, D>(SQl, LF, Pb, LB, red1);
+        mac_ksplit<D, NB, D>(MKQl, LF, Pb, LB, red2);
         __syncthreads();
-        // T <- T + T_B + S^K_A X + M^KQ_B P_A
-        tiles22(D, NB, [&](float (&acc)[2][2], int m0, int n0) {
-            mac22(acc, SK, LF, X, LB, m0, n0, D);
-            mac22(acc, MKQl, LF, Pb, LB, m0, n0, D);
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    Tb[(m0 + i) * LB + n0 + j] += Tl[(m0 + i) * LB + n0 + j] + acc[i][j];
-        });
-        __syncthreads();
-        // P <- P + P_B, S^K <- S^K + S^K_B
+        // X = M^QP_B + S^Q_B P_A,  Y = M^KQ_B P_A
         for (int e = threadIdx.x; e < D * NB; e += kThreads) {
-            const int r = e / NB, x = e % NB;
-            Pb[r * LB + x] += Pl[r * LB + x];
+            const int o = (e / NB) * LB + e % NB;
+            X[o] = MQPl[o] + ksplit_sum<D, NB, D>(red1, e);
+            Y[o] = ksplit_sum<D, NB, D>(red2, e);
         }
+        __syncthreads();
+        // T <- T + T_B + S^K_A X + Y
+        mac_ksplit<D, NB, D>(SK, LF, X, LB, red1);
+        __syncthreads();
+        for (int e = threadIdx.x; e < D * NB; e += kThreads) {
+            const int o = (e / NB) * LB + e % NB;
+            Tb[o] += Tl[o] + Y[o] + ksplit_sum<D, NB, D>(red1, e);
+            Pb[o] += Pl[o];  // P <- P + P_B (read above only, before this barrier)
+        }
+        // S^K <- S^K + S^K_B
         for (int e = threadIdx.x; e < D * D; e += kThreads) {
             const int r = e / D, x = e % D;
             SK[r * LF + x] += SKl[r * LF + x];
@@ -261,41 +257,41 @@ __global__ void __launch_bounds__(kThreads) fwd3_out_kernel(Fwd3Args a) {
     const float *so =
         a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
     // the prefix state arrives asynchronously while A~ is formed
-    copy_mat_async(so + ws.s_sk(), D, SK, Sm::LQ, D, D);
-    copy_mat_async(so + ws.s_p(), DV, P, Sm::LV, D, DV);
-    copy_mat_async(so + ws.s_t(), DV, Tp, Sm::LV, D, DV);
+    copy_mat_async<D>(so + ws.s_sk(), D, SK, Sm::LQ, D);
+    copy_mat_async<DV>(so + ws.s_p(), DV, P, Sm::LV, D);
+    copy_mat_async<DV>(so + ws.s_t(), DV, Tp, Sm::LV, D);
     cp_async_commit();
-    load_rows(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L, D);
-    load_rows(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L, D);
-    load_rows(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L, DV);
+    load_rows<D>(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L);
+    load_rows<D>(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L);
+    load_rows<DV>(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L);
     __syncthreads();
-    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<true, C, C>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, true>(acc, Q, Sm::LQ, K, Sm::LQ, m0, n0, ns, D);
         each(acc, m0, n0, ns, [&](int t, int s, float x) { A[t * Sm::LT + s] = s <= t ? x : 0.f; });
     });
     cp_async_wait<0>();
     __syncthreads();
     // U = Q S^K_p + A~ K;  W = Q P_p + A~ V
-    tiles<false>(C, D, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, C, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, false>(acc, Q, Sm::LQ, SK, Sm::LQ, m0, n0, ns, D);
         mac<false, false>(acc, A, Sm::LT, K, Sm::LQ, m0, n0, ns, C);
         each(acc, m0, n0, ns, [&](int t, int i, float x) { U[t * Sm::LQ + i] = x; });
     });
-    tiles<false>(C, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, C, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, false>(acc, Q, Sm::LQ, P, Sm::LV, m0, n0, ns, D);
         mac<false, false>(acc, A, Sm::LT, V, Sm::LV, m0, n0, ns, C);
         each(acc, m0, n0, ns, [&](int t, int j, float x) { W[t * Sm::LV + j] = x; });
     });
     __syncthreads();
     // M = tril(Q U^T)
-    tiles<true>(C, C, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<true, C, C>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, true>(acc, Q, Sm::LQ, U, Sm::LQ, m0, n0, ns, D);
         each(acc, m0, n0, ns, [&](int t, int b, float x) { M[t * Sm::LT + b] = b <= t ? x : 0.f; });
     });
     __syncthreads();
     // O = Q T_p + M W
     T *o = static_cast<T *>(a.o) + rv;
-    tiles<false>(C, DV, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+    tiles<false, C, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, false>(acc, Q, Sm::LQ, Tp, Sm::LV, m0, n0, ns, D);
         mac<false, false>(acc, M, Sm::LT, W, Sm::LV, m0, n0, ns, C);
         each(acc, m0, n0, ns, [&](int t, int j, float x) {

@@ -98,9 +98,9 @@ __device__ __forceinline__ void mac_rs(float (&acc)[4][4], const float *rs, cons
 
 // Every 4x4 tile of an M x N result, one per thread per round.  STRIDED spreads a
 // thread's four columns N/4 apart (conflict-free rows when B is read transposed).
-template <bool STRIDED, class Body>
-__device__ __forceinline__ void tiles(int M, int N, Body body) {
-    const int tn = N / 4, count = (M / 4) * tn;
+template <bool STRIDED, int M, int N, class Body>
+__device__ __forceinline__ void tiles(Body body) {
+    constexpr int tn = N / 4, count = (M / 4) * tn;
     for (int t = threadIdx.x; t < count; t += kThreads) {
         const int m0 = (t / tn) * 4;
         const int n0 = STRIDED ? t % tn : (t % tn) * 4, ns = STRIDED ? tn : 1;
@@ -117,8 +117,9 @@ __device__ __forceinline__ void each(const float (&acc)[4][4], int m0, int n0, i
         for (int j = 0; j < 4; ++j) f(m0 + i, n0 + j * ns, acc[i][j]);
 }
 
-template <typename T>
-__device__ __forceinline__ void load_rows(const T *src, float *dst, int ld, int rows, int L, int W) {
+// `rows` rows of W values (row-major, ld W) into shared rows of ld `ld`; rows >= L zero.
+template <int W, typename T>
+__device__ __forceinline__ void load_rows(const T *src, float *dst, int ld, int rows, int L) {
     for (int e = threadIdx.x; e < rows * W; e += kThreads) {
         const int r = e / W, x = e % W;
         dst[r * ld + x] = r < L ? ld_t(src, (size_t)r * W + x) : 0.f;
@@ -134,35 +135,45 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
-// rows x cols floats (cols a multiple of 4; both leading dimensions multiples of 4,
+// rows x COLS floats (COLS a multiple of 4; both leading dimensions multiples of 4,
 // both bases 16-byte aligned) from global (ld src_ld) to shared (ld dst_ld).
-__device__ __forceinline__ void copy_mat_async(const float *src, int src_ld, float *dst, int dst_ld, int rows,
-                                               int cols) {
-    const int q = cols / 4;
+template <int COLS>
+__device__ __forceinline__ void copy_mat_async(const float *src, int src_ld, float *dst, int dst_ld, int rows) {
+    constexpr int q = COLS / 4;
     for (int e = threadIdx.x; e < rows * q; e += kThreads) {
         const int r = e / q, c = (e % q) * 4;
         cp_async16(dst + (size_t)r * dst_ld + c, src + (size_t)r * src_ld + c);
     }
 }
 
-// acc[i][j] += sum_k A[(m0+i)*lda + k] B[k*ldb + n0+j] for a 2x2 tile (K a multiple of
-// 4; lda a multiple of 4; n0 even, ldb even).
-__device__ __forceinline__ void mac22(float (&acc)[2][2], const float *A, int lda, const float *B, int ldb, int m0,
-                                      int n0, int K) {
-#pragma unroll 4
-    for (int k = 0; k < K; k += 4) {
-        const float4 a0 = *reinterpret_cast<const float4 *>(A + (size_t)m0 * lda + k);
-        const float4 a1 = *reinterpret_cast<const float4 *>(A + (size_t)(m0 + 1) * lda + k);
-        const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+// Partial products of an M x N result (M a multiple of 4, N in {4, 8, 16}; K a power
+// of two >= 4) over all threads: the (M/4)(N/4) 4x4 tiles times G contraction slices
+// of K / G, G = min(kThreads / tiles, K / 4).  Thread t < tiles * G takes tile
+// t % tiles and slice t / tiles and stores its 16 partial sums to
+// red[slice][M][N]; ksplit_sum adds the G slices of one element.
+__host__ __device__ constexpr int ksplit_slices(int M, int N, int K) {
+    return (kThreads / ((M / 4) * (N / 4))) < K / 4 ? kThreads / ((M / 4) * (N / 4)) : K / 4;
+}
+template <int M, int N, int K>
+__device__ __forceinline__ void mac_ksplit(const float *A, int lda, const float *B, int ldb, float *red) {
+    constexpr int tn = N / 4, T = (M / 4) * tn, G = ksplit_slices(M, N, K), kr = K / G;
+    if (threadIdx.x >= T * G) return;
+    const int t = threadIdx.x % T, g = threadIdx.x / T;
+    const int m0 = (t / tn) * 4, n0 = (t % tn) * 4;
+    float acc[4][4] = {};
+    mac<false, false>(acc, A + g * kr, lda, B + (size_t)g * kr * ldb, ldb, m0, n0, 1, kr);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const float2 b = *reinterpret_cast<const float2 *>(B + (size_t)(k + kk) * ldb + n0);
-            acc[0][0] = fmaf(av0[kk], b.x, acc[0][0]);
-            acc[0][1] = fmaf(av0[kk], b.y, acc[0][1]);
-            acc[1][0] = fmaf(av1[kk], b.x, acc[1][0]);
-            acc[1][1] = fmaf(av1[kk], b.y, acc[1][1]);
-        }
-    }
+    for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4 *>(red + ((size_t)g * M + m0 + i) * N + n0) =
+            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+}
+template <int M, int N, int K>
+__device__ __forceinline__ float ksplit_sum(const float *red, int e) {
+    constexpr int G = ksplit_slices(M, N, K);
+    float s = 0.f;
+#pragma unroll
+    for (int g = 0; g < G; ++g) s += red[(size_t)g * M * N + e];
+    return s;
 }
 
 // Every 2x2 tile of an M x N result (M, N even), one per thread per round.
