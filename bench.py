@@ -53,6 +53,7 @@ FWD3_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fw
 FWD3_METRIC = "masked 3rd-order HLA forward tokens/s and % roofline on 1 GB300"
 FWD3_DISPATCH_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd3_simt.cu")
 FWD3_TC_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd3_tc.cu")
+BWD_TC_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_bwd_tc.cu")
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz (maximum SM clock)
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2070e6 / 1e12
 
@@ -544,8 +545,10 @@ def bench_phased(args, w: W.Workload, rank, world, local, dist):
     if bwd:
         params = hla.make_params(sets[0][0][0], sets[0][0][2], w.chunk, gamma)
         ws_bytes = hla.hla_backward_workspace_size(params)
-        names = ("bwd_local_kernel", "bwd_scan_kernel", "bwd_grad_kernel")
-        fl = bwd_flops_per_token_head(w)
+        tc = w.dtype == "bf16" and w.d == w.dv == w.chunk == 64  # local sums and gradients on the tensor cores
+        names = ("bwd_local_tc_kernel" if tc else "bwd_local_kernel", "bwd_scan_kernel",
+                 "bwd_grad_tc_kernel" if tc else "bwd_grad_kernel")
+        fl = dict(zip(names, bwd_flops_per_token_head(w).values()))
         src, metric = BWD_KERNEL_SRC, BWD_METRIC
     else:
         params = hla.make_params(sets[0][0][0], sets[0][0][2], w.chunk)
@@ -655,7 +658,7 @@ def bench_phased(args, w: W.Workload, rank, world, local, dist):
     flops_launch = fl[top] * w.token_heads
     ach = flops_launch / (phase_ms[top] / 1e3) / 1e12
     bnd, peak, psrc = bound_of(top)
-    src_top = FWD3_TC_KERNEL_SRC if "_tc_" in top else src
+    src_top = (BWD_TC_KERNEL_SRC if bwd else FWD3_TC_KERNEL_SRC) if "_tc_" in top else src
     roofline = {"bound": bnd, "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
                 "peak_source": psrc, "traffic": traffic_for(top, w.name, src_top), "kernel": top,
                 "alg_flops_per_launch": flops_launch,

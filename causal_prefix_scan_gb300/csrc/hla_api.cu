@@ -223,7 +223,9 @@ hla_status hla_backward_chunked_traced(const hla_params *p, const void *q, const
             if (!phase_events[i]) return fail(HLA_ERR_ARG, "phase_events must hold four events");
     }
     a.events = reinterpret_cast<cudaEvent_t const *>(phase_events);
-    cudaError_t e = hla::bwd_simt_launch(a, static_cast<cudaStream_t>(stream));
+    cudaError_t e = status_ptr(&a.err);
+    if (e != cudaSuccess) return cuda_fail(e, "status word");
+    e = hla::bwd_simt_launch(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return HLA_OK;
 }

@@ -32,11 +32,20 @@
 // Three launches: (1) one CTA per chunk writes the six local sums; (2) the scan,
 // one CTA per (b,h, column block, direction), walks the chunks forward for S, X
 // and backward for Lam, Om and writes the states every chunk needs; (3) one CTA
-// per chunk forms dq, dk, dv.
+// per chunk forms dq, dk, dv.  For bf16 inputs with d = dv = chunk = 64, (1) and (3)
+// run on the tensor cores (hla_bwd_tc.cu); the kernels here are the CUDA-core
+// versions for every shape.
 #pragma once
+#include <type_traits>
+
 #include "hla_smem_tile.cuh"
 
 namespace hla {
+namespace bwdtc {
+// tensor-core versions of the local-sums and gradient kernels (bf16, d = dv = chunk = 64)
+cudaError_t local_tc(const BwdArgs &a, cudaStream_t st);
+cudaError_t grad_tc(const BwdArgs &a, cudaStream_t st);
+}  // namespace bwdtc
 namespace bwd {
 
 using namespace tile;
@@ -375,13 +384,22 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t st) {
     if ((e = smem_attr(bwd_local_kernel<T, C, D, DV>, b1)) != cudaSuccess) return e;
     if ((e = smem_attr(bwd_scan_kernel<C, D, DV>, b2)) != cudaSuccess) return e;
     if ((e = smem_attr(bwd_grad_kernel<T, C, D, DV>, b3)) != cudaSuccess) return e;
+    constexpr bool TC = std::is_same<T, __nv_bfloat16>::value && C == 64 && D == 64 && DV == 64;
     auto mark = [&](int i) { return a.events ? cudaEventRecord(a.events[i], st) : cudaSuccess; };
     if ((e = mark(0)) != cudaSuccess) return e;
-    bwd_local_kernel<T, C, D, DV><<<units * nch, kThreads, b1, st>>>(a);
+    if constexpr (TC) {
+        if ((e = bwdtc::local_tc(a, st)) != cudaSuccess) return e;
+    } else {
+        bwd_local_kernel<T, C, D, DV><<<units * nch, kThreads, b1, st>>>(a);
+    }
     if ((e = mark(1)) != cudaSuccess) return e;
     bwd_scan_kernel<C, D, DV><<<units * kSplit * 2, kThreads, b2, st>>>(a);
     if ((e = mark(2)) != cudaSuccess) return e;
-    bwd_grad_kernel<T, C, D, DV><<<units * nch, kThreads, b3, st>>>(a);
+    if constexpr (TC) {
+        if ((e = bwdtc::grad_tc(a, st)) != cudaSuccess) return e;
+    } else {
+        bwd_grad_kernel<T, C, D, DV><<<units * nch, kThreads, b3, st>>>(a);
+    }
     if ((e = mark(3)) != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -74,6 +74,7 @@ struct BwdArgs {
     void *grad_q, *grad_k, *grad_v;  // outputs
     float *workspace;
     cudaEvent_t const *events;  // NULL or four events recorded at the phase boundaries
+    unsigned *err;              // sticky device status word (bounded waits of the tensor-core kernels)
 };
 
 // Backward of the masked forward on CUDA cores (d, dv, chunk in {16,32,64}).
