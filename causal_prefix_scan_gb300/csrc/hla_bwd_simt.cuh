@@ -33,8 +33,9 @@
 // one CTA per (b,h, column block, direction), walks the chunks forward for S, X
 // and backward for Lam, Om and writes the states every chunk needs; (3) one CTA
 // per chunk forms dq, dk, dv.  For bf16 inputs with d = dv = chunk = 64, (1) and (3)
-// run on the tensor cores (hla_bwd_tc.cu); the kernels here are the CUDA-core
-// versions for every shape.
+// run on the tensor cores (hla_bwd_tc.cu) and the scan as elementwise prefix sums
+// around one tensor-core product stage per chunk (hla_scan_tc.cu); the kernels here
+// are the CUDA-core versions for every shape.
 #pragma once
 #include <type_traits>
 
@@ -46,6 +47,10 @@ namespace bwdtc {
 cudaError_t local_tc(const BwdArgs &a, cudaStream_t st);
 cudaError_t grad_tc(const BwdArgs &a, cudaStream_t st);
 }  // namespace bwdtc
+namespace scantc {
+// the scan as elementwise prefix sums around one tensor-core product stage per chunk
+cudaError_t bwd_scan(const BwdArgs &a, cudaStream_t st);
+}  // namespace scantc
 namespace bwd {
 
 using namespace tile;
@@ -393,7 +398,11 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t st) {
         bwd_local_kernel<T, C, D, DV><<<units * nch, kThreads, b1, st>>>(a);
     }
     if ((e = mark(1)) != cudaSuccess) return e;
-    bwd_scan_kernel<C, D, DV><<<units * kSplit * 2, kThreads, b2, st>>>(a);
+    if constexpr (TC) {
+        if ((e = scantc::bwd_scan(a, st)) != cudaSuccess) return e;
+    } else {
+        bwd_scan_kernel<C, D, DV><<<units * kSplit * 2, kThreads, b2, st>>>(a);
+    }
     if ((e = mark(2)) != cudaSuccess) return e;
     if constexpr (TC) {
         if ((e = bwdtc::grad_tc(a, st)) != cudaSuccess) return e;

@@ -21,7 +21,9 @@
 // per (b,h) and column block of dv, walks the chunks and writes each chunk's prefix
 // state (and the final state); (3) one CTA per chunk forms the outputs.  For bf16
 // inputs with d = dv = chunk = 64, (1) and (3) run on the tensor cores
-// (hla_fwd3_tc.cu); the kernels here are the CUDA-core versions for every shape.
+// (hla_fwd3_tc.cu) and (2) as elementwise prefix sums around one tensor-core product
+// stage per chunk (hla_scan_tc.cu); the kernels here are the CUDA-core versions for
+// every shape.
 #pragma once
 #include <type_traits>
 
@@ -32,6 +34,10 @@ namespace fwd3tc {
 cudaError_t local_tc(const Fwd3Args &a, cudaStream_t st);
 cudaError_t out_tc(const Fwd3Args &a, cudaStream_t st);
 }  // namespace fwd3tc
+namespace scantc {
+// the scan as elementwise prefix sums around one tensor-core product stage per chunk
+cudaError_t fwd3_scan(const Fwd3Args &a, cudaStream_t st);
+}  // namespace scantc
 
 namespace fwd3 {
 using namespace tile;
@@ -323,7 +329,11 @@ cudaError_t launch_t(const Fwd3Args &a, cudaStream_t st) {
         fwd3_local_kernel<T, C, D, DV><<<units * nch, kThreads, b1, st>>>(a);
     }
     if ((e = mark(1)) != cudaSuccess) return e;
-    fwd3_scan_kernel<C, D, DV><<<units * kSplit, kThreads, b2, st>>>(a);
+    if constexpr (TC) {
+        if ((e = scantc::fwd3_scan(a, st)) != cudaSuccess) return e;
+    } else {
+        fwd3_scan_kernel<C, D, DV><<<units * kSplit, kThreads, b2, st>>>(a);
+    }
     if ((e = mark(2)) != cudaSuccess) return e;
     if constexpr (TC) {
         if ((e = fwd3tc::out_tc(a, st)) != cudaSuccess) return e;
