@@ -50,10 +50,11 @@ __global__ void __launch_bounds__(kTc, 2) bwd_local_tc_kernel(const __grid_const
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v) + r0;
     const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(a.go) + r0;
     fill_gp(gp, a, u);
-    load_tile_bf16(q, L, x.tile(L_Q));
-    load_tile_bf16(k, L, x.tile(L_K));
-    load_tile_bf16(v, L, x.tile(L_V));
-    load_tile_bf16(g, L, x.tile(L_G));
+    {
+        const __nv_bfloat16 *src[4] = {q, k, v, g};
+        uint8_t *dst[4] = {x.tile(L_Q), x.tile(L_K), x.tile(L_V), x.tile(L_G)};
+        load_tiles_bf16<4>(src, L, dst);
+    }
     __syncthreads();
     const uint8_t *kw1 = x.tile(L_K), *qw2 = x.tile(L_Q), *qw4 = x.tile(L_Q), *vw5 = x.tile(L_V);
     if (decay) {  // weighted copies: g^{L-1-s} K, g^{2L-1-s} Q, g^{2s} Q, g^{2L-s} V
@@ -170,13 +171,17 @@ __global__ void __launch_bounds__(kTc, 1) bwd_grad_tc_kernel(const __grid_consta
     const float *so =
         a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
     fill_gp(gp, a, u);
-    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.q) + r0, L, x.tile(G_Q));
-    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.k) + r0, L, x.tile(G_K));
-    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.v) + r0, L, x.tile(G_V));
-    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.go) + r0, L, x.tile(G_G));
-    load_tile_hilo(so + ws.o_sp(), x.tile(G_SH), x.tile(G_SL));
-    load_tile_hilo(so + ws.o_xp(), x.tile(G_XH), x.tile(G_XL));
-    load_tile_hilo(so + ws.o_lam(), x.tile(G_LH), x.tile(G_LL));
+    {
+        const __nv_bfloat16 *src[4] = {static_cast<const __nv_bfloat16 *>(a.q) + r0,
+                                       static_cast<const __nv_bfloat16 *>(a.k) + r0,
+                                       static_cast<const __nv_bfloat16 *>(a.v) + r0,
+                                       static_cast<const __nv_bfloat16 *>(a.go) + r0};
+        uint8_t *dst[4] = {x.tile(G_Q), x.tile(G_K), x.tile(G_V), x.tile(G_G)};
+        load_tiles_bf16<4>(src, L, dst);
+        const float *ss[3] = {so + ws.o_sp(), so + ws.o_xp(), so + ws.o_lam()};
+        uint8_t *hi[3] = {x.tile(G_SH), x.tile(G_XH), x.tile(G_LH)}, *lo[3] = {x.tile(G_SL), x.tile(G_XL), x.tile(G_LL)};
+        load_tiles_hilo<3>(ss, hi, lo);
+    }
     load_sym_hilo(so + ws.o_om(), x.tile(G_OH), x.tile(G_OL));
     x.publish();
     // row scales of this thread's token row t

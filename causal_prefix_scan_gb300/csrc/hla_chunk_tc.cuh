@@ -161,6 +161,53 @@ __device__ __forceinline__ void store_tril(const Ctx &x, uint8_t *tile, float (&
     tile_store_row16(tile, 64, x.row, x.c0, v);
 }
 
+// N tiles of L rows of 64 bf16 each (row-major) into swizzled tiles, rows >= L zero;
+// every global load of the batch is issued before the first shared store.
+template <int N>
+__device__ __forceinline__ void load_tiles_bf16(const __nv_bfloat16 *const (&src)[N], int L, uint8_t *const (&tile)[N]) {
+    uint4 v[N][2];
+#pragma unroll
+    for (int t = 0; t < N; ++t)
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const int e = threadIdx.x + p * kTc, r = e >> 3, c = (e & 7) * 8;
+            v[t][p] = r < L ? *reinterpret_cast<const uint4 *>(src[t] + (size_t)r * 64 + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+    for (int t = 0; t < N; ++t)
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const int e = threadIdx.x + p * kTc, r = e >> 3, c = (e & 7) * 8;
+            *reinterpret_cast<uint4 *>(tile[t] + tile_off(64, r, c)) = v[t][p];
+        }
+}
+// N fp32 64 x 64 matrices (row-major) into bf16 hi and lo tiles; all loads first.
+template <int N>
+__device__ __forceinline__ void load_tiles_hilo(const float *const (&src)[N], uint8_t *const (&hi)[N],
+                                                uint8_t *const (&lo)[N]) {
+    const int r = threadIdx.x >> 2, c = (threadIdx.x & 3) * 16;  // kTc == 256: one row segment each
+    float4 v[N][4];
+#pragma unroll
+    for (int t = 0; t < N; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[t][i] = *reinterpret_cast<const float4 *>(src[t] + (size_t)r * 64 + c + 4 * i);
+#pragma unroll
+    for (int t = 0; t < N; ++t) {
+        float h[16], l[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float x[4] = {v[t][i].x, v[t][i].y, v[t][i].z, v[t][i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                h[4 * i + k] = __bfloat162float(__float2bfloat16_rn(x[k]));
+                l[4 * i + k] = x[k] - h[4 * i + k];
+            }
+        }
+        tile_store_row16(hi[t], 64, r, c, h);
+        tile_store_row16(lo[t], 64, r, c, l);
+    }
+}
+
 // L rows of 64 bf16 scaled by w[r] into a swizzled tile (bf16 after scaling); rows >= L zero.
 __device__ __forceinline__ void load_tile_scaled(const __nv_bfloat16 *src, int L, const float *w, uint8_t *tile) {
     for (int e = threadIdx.x; e < 64 * 4; e += kTc) {
@@ -190,6 +237,14 @@ __device__ __forceinline__ void store_tril_decay(const Ctx &x, uint8_t *tile, fl
         v[i] = dlt >= 0 ? gp[step * dlt] * v[i] : 0.f;
     }
     tile_store_row16(tile, 64, x.row, x.c0, v);
+}
+// 16 consecutive fp32 values from global memory
+__device__ __forceinline__ void ld_row16(const float *src, float (&v)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(src + i);
+        v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
+    }
 }
 // 16 fp32 values as bf16 to global memory (two 16-byte stores)
 __device__ __forceinline__ void st_row16_bf16(__nv_bfloat16 *dst, const float (&v)[16]) {

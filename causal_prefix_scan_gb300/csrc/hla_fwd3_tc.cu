@@ -32,9 +32,13 @@ __global__ void __launch_bounds__(kTc, 2) fwd3_local_tc_kernel(const __grid_cons
     const int nch = (a.n + 63) / 64, u = blockIdx.x / nch, ch = blockIdx.x % nch;
     const int t0 = ch * 64, L = min(64, a.n - t0);
     const size_t r0 = ((size_t)u * a.n + t0) * 64;
-    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.q) + r0, L, x.tile(L_Q));
-    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.k) + r0, L, x.tile(L_K));
-    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.v) + r0, L, x.tile(L_V));
+    {
+        const __nv_bfloat16 *src[3] = {static_cast<const __nv_bfloat16 *>(a.q) + r0,
+                                       static_cast<const __nv_bfloat16 *>(a.k) + r0,
+                                       static_cast<const __nv_bfloat16 *>(a.v) + r0};
+        uint8_t *dst[3] = {x.tile(L_Q), x.tile(L_K), x.tile(L_V)};
+        load_tiles_bf16<3>(src, L, dst);
+    }
     x.publish();
     float v[16];
     do {
@@ -102,12 +106,16 @@ __global__ void __launch_bounds__(kTc, 2) fwd3_out_tc_kernel(const __grid_consta
     const size_t r0 = ((size_t)u * a.n + t0) * 64;
     const Ws3 ws{64, 64};
     const float *so = a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
-    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.q) + r0, L, x.tile(O_Q));
-    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.k) + r0, L, x.tile(O_K));
-    load_tile_bf16(static_cast<const __nv_bfloat16 *>(a.v) + r0, L, x.tile(O_V));
-    load_tile_hilo(so + ws.s_sk(), x.tile(O_SH), x.tile(O_SL));
-    load_tile_hilo(so + ws.s_p(), x.tile(O_PH), x.tile(O_PL));
-    load_tile_hilo(so + ws.s_t(), x.tile(O_TH), x.tile(O_TL));
+    {
+        const __nv_bfloat16 *src[3] = {static_cast<const __nv_bfloat16 *>(a.q) + r0,
+                                       static_cast<const __nv_bfloat16 *>(a.k) + r0,
+                                       static_cast<const __nv_bfloat16 *>(a.v) + r0};
+        uint8_t *dst[3] = {x.tile(O_Q), x.tile(O_K), x.tile(O_V)};
+        load_tiles_bf16<3>(src, L, dst);
+        const float *ss[3] = {so + ws.s_sk(), so + ws.s_p(), so + ws.s_t()};
+        uint8_t *hi[3] = {x.tile(O_SH), x.tile(O_PH), x.tile(O_TH)}, *lo[3] = {x.tile(O_SL), x.tile(O_PL), x.tile(O_TL)};
+        load_tiles_hilo<3>(ss, hi, lo);
+    }
     x.publish();
     constexpr uint32_t SA = 0, SU = 64, SW = 128, SO = 192;
     float v[16];

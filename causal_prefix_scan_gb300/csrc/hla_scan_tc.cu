@@ -104,11 +104,18 @@ __global__ void __launch_bounds__(kTc, 2) bwd_incr_tc_kernel(const __grid_consta
     float *lc = a.workspace + ((size_t)u * nch + ch) * ws.loc_floats();
     const float *so =
         a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
-    load_tile_hilo(so + ws.o_sp(), x.tile(B_SH), x.tile(B_SL));
-    load_tile_hilo(lc + ws.o_cq(), x.tile(B_CH), x.tile(B_CL));
-    load_tile_hilo(so + ws.o_lam(), x.tile(B_LH), x.tile(B_LL));
-    load_tile_hilo(lc + ws.o_w(), x.tile(B_WH), x.tile(B_WL));
+    {
+        const float *ss[4] = {so + ws.o_sp(), lc + ws.o_cq(), so + ws.o_lam(), lc + ws.o_w()};
+        uint8_t *hi[4] = {x.tile(B_SH), x.tile(B_CH), x.tile(B_LH), x.tile(B_WH)};
+        uint8_t *lo[4] = {x.tile(B_SL), x.tile(B_CL), x.tile(B_LL), x.tile(B_WL)};
+        load_tiles_hilo<4>(ss, hi, lo);
+    }
     x.publish();
+    // the addends of the epilogue, fetched while the products run
+    const size_t ro = (size_t)x.row * 64 + x.c0;
+    float xa[16], oa[16];
+    ld_row16(lc + ws.o_xloc() + ro, xa);
+    ld_row16(lc + ws.o_oloc() + ro, oa);
     do {
         // S_p C_q (rows = key feature), Lam_n W (rows = key feature)
         if (x.tid == 0) {
@@ -117,15 +124,14 @@ __global__ void __launch_bounds__(kTc, 2) bwd_incr_tc_kernel(const __grid_consta
         }
         x.commit();
         if (!x.wait()) break;
-        const size_t ro = (size_t)x.row * 64 + x.c0;
         float r[16];
         x.ld_row(0, r);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] += lc[ws.o_xloc() + ro + i];
+        for (int i = 0; i < 16; ++i) r[i] += xa[i];
         st_row16(lc + ws.o_xloc() + ro, r);
         x.ld_row(64, r);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] += lc[ws.o_oloc() + ro + i];
+        for (int i = 0; i < 16; ++i) r[i] += oa[i];
         st_row16(lc + ws.o_oloc() + ro, r);
     } while (false);
     teardown(x);
@@ -143,13 +149,17 @@ __global__ void __launch_bounds__(kTc, 2) fwd3_incr_tc_kernel(const __grid_const
     float *lc = a.workspace + ((size_t)u * nch + ch) * ws.loc_floats();
     const float *so =
         a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
-    load_tile_hilo(lc + ws.o_sq(), x.tile(T_QH), x.tile(T_QL));
-    load_tile_hilo(lc + ws.o_mkq(), x.tile(T_MH), x.tile(T_ML));
-    load_tile_hilo(so + ws.s_sk(), x.tile(T_KH), x.tile(T_KL));
-    load_tile_hilo(so + ws.s_p(), x.tile(T_PH), x.tile(T_PL));
+    {
+        const float *ss[4] = {lc + ws.o_sq(), lc + ws.o_mkq(), so + ws.s_sk(), so + ws.s_p()};
+        uint8_t *hi[4] = {x.tile(T_QH), x.tile(T_MH), x.tile(T_KH), x.tile(T_PH)};
+        uint8_t *lo[4] = {x.tile(T_QL), x.tile(T_ML), x.tile(T_KL), x.tile(T_PL)};
+        load_tiles_hilo<4>(ss, hi, lo);
+    }
     x.publish();
     const size_t ro = (size_t)x.row * 64 + x.c0;
-    float r[16];
+    float r[16], qa[16], ta[16];  // epilogue addends M^QP_B and T_B, fetched while the products run
+    ld_row16(lc + ws.o_mqp() + ro, qa);
+    ld_row16(lc + ws.o_t() + ro, ta);
     do {
         // S^Q_B P_p, M^KQ_B P_p
         if (x.tid == 0) {
@@ -164,7 +174,7 @@ __global__ void __launch_bounds__(kTc, 2) fwd3_incr_tc_kernel(const __grid_const
             float h[16], l[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const float s = r[i] + lc[ws.o_mqp() + ro + i];
+                const float s = r[i] + qa[i];
                 h[i] = __bfloat162float(__float2bfloat16_rn(s));
                 l[i] = s - h[i];
             }
@@ -178,7 +188,7 @@ __global__ void __launch_bounds__(kTc, 2) fwd3_incr_tc_kernel(const __grid_const
         if (!x.wait()) break;
         x.ld_row(64, r);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] += lc[ws.o_t() + ro + i];
+        for (int i = 0; i < 16; ++i) r[i] += ta[i];
         st_row16(lc + ws.o_t() + ro, r);
     } while (false);
     teardown(x);
