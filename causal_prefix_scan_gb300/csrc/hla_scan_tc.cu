@@ -44,41 +44,52 @@ struct PrefixArgs {
 
 constexpr int kPrefixThreads = 256;
 
+// Each thread scans four consecutive elements (count a multiple of 4, 16-byte aligned).
 __global__ void __launch_bounds__(kPrefixThreads) chunk_prefix_kernel(const __grid_constant__ PrefixArgs a) {
     const PrefixJob &j = a.job[blockIdx.y];
-    const int blocks = (j.count + kPrefixThreads - 1) / kPrefixThreads;
-    const int u = blockIdx.x / blocks, e = (blockIdx.x % blocks) * kPrefixThreads + threadIdx.x;
+    const int per_unit = (j.count / 4 + kPrefixThreads - 1) / kPrefixThreads;
+    const int u = blockIdx.x / per_unit, e = ((blockIdx.x % per_unit) * kPrefixThreads + threadIdx.x) * 4;
     if (u >= a.units || e >= j.count) return;
     const float lg = a.gamma ? log2f(a.gamma[u % a.H]) : 0.f;
-    float R = j.init ? j.init[(size_t)u * j.count + e] : 0.f;
+    float4 R = j.init ? *reinterpret_cast<const float4 *>(j.init + (size_t)u * j.count + e) : make_float4(0, 0, 0, 0);
     const float *in = j.in + (size_t)u * a.nch * j.in_stride + j.in_off + e;
     float *out = j.out + (size_t)u * a.nch * j.out_stride + j.out_off + e;
+    // walk the chunks with pointer steps: forward +stride, reverse -stride from the last chunk
+    const long long sin = j.reverse ? -(long long)j.in_stride : (long long)j.in_stride;
+    const long long sout = j.reverse ? -(long long)j.out_stride : (long long)j.out_stride;
+    if (j.reverse) {
+        in += (size_t)(a.nch - 1) * j.in_stride;
+        out += (size_t)(a.nch - 1) * j.out_stride;
+    }
     constexpr int U = 8;  // loads of U chunks issued before their dependent updates
     for (int i0 = 0; i0 < a.nch; i0 += U) {
-        float v[U];
+        float4 v[U];
 #pragma unroll
-        for (int k = 0; k < U; ++k) {
-            const int it = i0 + k, ch = j.reverse ? a.nch - 1 - it : it;
-            v[k] = it < a.nch ? __ldcg(in + (size_t)ch * j.in_stride) : 0.f;
-        }
+        for (int k = 0; k < U; ++k)
+            v[k] = i0 + k < a.nch ? __ldcg(reinterpret_cast<const float4 *>(in + (long long)k * sin))
+                                  : make_float4(0, 0, 0, 0);
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const int it = i0 + k;
             if (it < a.nch) {
-                const int ch = j.reverse ? a.nch - 1 - it : it;
-                out[(size_t)ch * j.out_stride] = R;
-                const int L = min(a.chunk, a.n - ch * a.chunk);
-                const float f = a.gamma ? gpow(lg, (float)(j.power * L)) : 1.f;
-                R = f * R + v[k];
+                *reinterpret_cast<float4 *>(out + (long long)k * sout) = R;
+                float f = 1.f;
+                if (a.gamma) {
+                    const int ch = j.reverse ? a.nch - 1 - it : it;
+                    f = gpow(lg, (float)(j.power * min(a.chunk, a.n - ch * a.chunk)));
+                }
+                R.x = f * R.x + v[k].x; R.y = f * R.y + v[k].y; R.z = f * R.z + v[k].z; R.w = f * R.w + v[k].w;
             }
         }
+        in += U * sin;
+        out += U * sout;
     }
-    if (j.fin) j.fin[(size_t)u * j.count + e] = R;
+    if (j.fin) *reinterpret_cast<float4 *>(j.fin + (size_t)u * j.count + e) = R;
 }
 
 cudaError_t prefix(const PrefixArgs &a, cudaStream_t st) {
     int mx = 0;
-    for (int i = 0; i < a.njobs; ++i) mx = max(mx, (a.job[i].count + kPrefixThreads - 1) / kPrefixThreads);
+    for (int i = 0; i < a.njobs; ++i) mx = max(mx, (a.job[i].count / 4 + kPrefixThreads - 1) / kPrefixThreads);
     dim3 grid((unsigned)(a.units * mx), (unsigned)a.njobs);
     chunk_prefix_kernel<<<grid, kPrefixThreads, 0, st>>>(a);
     return cudaGetLastError();
