@@ -54,6 +54,7 @@ FWD3_METRIC = "masked 3rd-order HLA forward tokens/s and % roofline on 1 GB300"
 FWD3_DISPATCH_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd3_simt.cu")
 FWD3_TC_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd3_tc.cu")
 BWD_TC_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_bwd_tc.cu")
+SCAN_TC_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_scan_tc.cu")
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz (maximum SM clock)
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2070e6 / 1e12
 
@@ -546,7 +547,7 @@ def bench_phased(args, w: W.Workload, rank, world, local, dist):
         params = hla.make_params(sets[0][0][0], sets[0][0][2], w.chunk, gamma)
         ws_bytes = hla.hla_backward_workspace_size(params)
         tc = w.dtype == "bf16" and w.d == w.dv == w.chunk == 64  # local sums and gradients on the tensor cores
-        names = ("bwd_local_tc_kernel" if tc else "bwd_local_kernel", "bwd_scan_kernel",
+        names = ("bwd_local_tc_kernel" if tc else "bwd_local_kernel", "bwd_scan_tc_kernels" if tc else "bwd_scan_kernel",
                  "bwd_grad_tc_kernel" if tc else "bwd_grad_kernel")
         fl = dict(zip(names, bwd_flops_per_token_head(w).values()))
         src, metric = BWD_KERNEL_SRC, BWD_METRIC
@@ -554,7 +555,8 @@ def bench_phased(args, w: W.Workload, rank, world, local, dist):
         params = hla.make_params(sets[0][0][0], sets[0][0][2], w.chunk)
         ws_bytes = hla.hla_forward3_workspace_size(params)
         tc = w.dtype == "bf16" and w.d == w.dv == w.chunk == 64  # local sums and outputs on the tensor cores
-        names = ("fwd3_local_tc_kernel" if tc else "fwd3_local_kernel", "fwd3_scan_kernel",
+        names = ("fwd3_local_tc_kernel" if tc else "fwd3_local_kernel",
+                 "fwd3_scan_tc_kernels" if tc else "fwd3_scan_kernel",
                  "fwd3_out_tc_kernel" if tc else "fwd3_out_kernel")
         fl = dict(zip(names, fwd3_flops_per_token_head(w).values()))
         src, metric = FWD3_KERNEL_SRC, FWD3_METRIC
@@ -654,17 +656,24 @@ def bench_phased(args, w: W.Workload, rank, world, local, dist):
     def bound_of(nm):
         return ("tensor", peaks["bf16_tflops"], tc_src) if "_tc_" in nm else ("alu", FP32_ALU_TFLOPS, alu_src)
 
+    def source_of(nm):  # the file whose hash keys the committed DRAM traffic of this phase
+        if "_scan_tc_" in nm:
+            return SCAN_TC_SRC
+        if "_tc_" in nm:
+            return BWD_TC_KERNEL_SRC if bwd else FWD3_TC_KERNEL_SRC
+        return src
+
     top = max(phase_ms, key=phase_ms.get)
     flops_launch = fl[top] * w.token_heads
     ach = flops_launch / (phase_ms[top] / 1e3) / 1e12
     bnd, peak, psrc = bound_of(top)
-    src_top = (BWD_TC_KERNEL_SRC if bwd else FWD3_TC_KERNEL_SRC) if "_tc_" in top else src
+    src_top = source_of(top)
     roofline = {"bound": bnd, "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
                 "peak_source": psrc, "traffic": traffic_for(top, w.name, src_top), "kernel": top,
                 "alg_flops_per_launch": flops_launch,
                 "phases": {nm: {"ms": phase_ms[nm], "alg_flops": fl[nm] * w.token_heads,
                                 "tflops": fl[nm] * w.token_heads / (phase_ms[nm] / 1e3) / 1e12 if phase_ms[nm] else None,
-                                "bound": bound_of(nm)[0],
+                                "bound": bound_of(nm)[0], "traffic": traffic_for(nm, w.name, source_of(nm)),
                                 "frac": (fl[nm] * w.token_heads / (phase_ms[nm] / 1e3) / 1e12) / bound_of(nm)[1]
                                 if phase_ms[nm] else None}
                            for nm in names},
