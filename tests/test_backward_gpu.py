@@ -118,3 +118,12 @@ def test_backward_full_workload():
     g = W.make_dout(w)
     err = check(run_backward(x, g, w.dtype, w.chunk), run_oracle(x, g), TOL_BF16, w.name)
     print(f"{w.name}: max per-(b,h) rel L2 {err:.3e}")
+
+
+def test_backward_tensor_core_pairs_with_decay():
+    """The tensor-core pipeline (bf16, d = dv = chunk = 64) over several pairs with
+    distinct per-head decay rates and a ragged final chunk."""
+    w = small(B=2, H=3, n=64 * 5 + 21, d=64, dv=64, chunk=64, decay=True, dtype="bf16", seed=37)
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    check(run_backward(x, g, "bf16", 64), run_oracle(x, g), TOL_BF16, "bwd tc B2H3 decay")

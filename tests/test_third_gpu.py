@@ -134,3 +134,20 @@ def test_forward3_full_workload():
     o_ref, st_ref = oracle.forward3(x["q"], x["k"], x["v"])
     err = check(o, st, o_ref, st_ref, TOL_BF16, w.name)
     print(f"{w.name}: max per-(b,h) rel L2 {err:.3e}")
+
+
+def test_forward3_tensor_core_resume_and_pairs():
+    """The tensor-core pipeline (bf16, d = dv = chunk = 64): several pairs, a split in the
+    middle of a chunk, state_out of the first part fed back as state_in."""
+    w = small(B=2, H=3, n=300, d=64, dv=64, chunk=64, dtype="bf16", seed=43)
+    x = W.make_inputs(w)
+    cut = 157
+    first = {n: x[n][:, :, :cut] for n in ("q", "k", "v")}
+    second = {n: x[n][:, :, cut:] for n in ("q", "k", "v")}
+    o1, st1 = run3(first, "bf16", 64)
+    sin = hla.State3(*(torch.from_numpy(st1[n].astype(np.float32)).cuda() for n in ("S", "P", "T")))
+    o2, st2 = run3(second, "bf16", 64, state_in=sin)
+    o_ref, st_ref = oracle.forward3(x["q"], x["k"], x["v"])
+    _, st1_ref = oracle.forward3(first["q"], first["k"], first["v"])
+    check(o1, st1, o_ref[:, :, :cut], st1_ref, TOL_BF16, "fwd3 tc first part")
+    check(o2, st2, o_ref[:, :, cut:], st_ref, TOL_BF16, "fwd3 tc resumed")
