@@ -127,3 +127,11 @@ def test_backward_tensor_core_pairs_with_decay():
     x = W.make_inputs(w)
     g = W.make_dout(w)
     check(run_backward(x, g, "bf16", 64), run_oracle(x, g), TOL_BF16, "bwd tc B2H3 decay")
+
+
+@pytest.mark.parametrize("n", [1, 5, 64, 65])
+def test_backward_tensor_core_short_sequences(n):
+    w = small(n=n, d=64, dv=64, chunk=64, decay=True, dtype="bf16", seed=38)
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    check(run_backward(x, g, "bf16", 64), run_oracle(x, g), TOL_BF16, f"bwd tc n{n}")

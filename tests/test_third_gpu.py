@@ -151,3 +151,12 @@ def test_forward3_tensor_core_resume_and_pairs():
     _, st1_ref = oracle.forward3(first["q"], first["k"], first["v"])
     check(o1, st1, o_ref[:, :, :cut], st1_ref, TOL_BF16, "fwd3 tc first part")
     check(o2, st2, o_ref[:, :, cut:], st_ref, TOL_BF16, "fwd3 tc resumed")
+
+
+@pytest.mark.parametrize("n", [1, 5, 64, 65])
+def test_forward3_tensor_core_short_sequences(n):
+    w = small(n=n, d=64, dv=64, chunk=64, dtype="bf16", seed=44)
+    x = W.make_inputs(w)
+    o, st = run3(x, "bf16", 64)
+    o_ref, st_ref = oracle.forward3(x["q"], x["k"], x["v"])
+    check(o, st, o_ref, st_ref, TOL_BF16, f"fwd3 tc n{n}")
