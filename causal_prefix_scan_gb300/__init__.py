@@ -31,7 +31,7 @@ __all__ = [
     "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
     "hla_backward_workspace_size", "hla_backward_chunked", "hla_backward_chunked_traced",
     "hla_state3", "hla_forward3_workspace_size", "hla_forward3_chunked", "hla_forward3_chunked_traced",
-    "hla_decode3_step", "State3", "forward3", "decode3_step",
+    "hla_decode3_step", "State3", "forward3", "decode3_step", "hla_selftest_expired_wait",
     "State", "new_workspace", "forward", "state_combine", "decode_step", "backward",
 ]
 
@@ -39,7 +39,8 @@ __all__ = [
 EXPORTS = ("hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combine", "hla_decode_step",
            "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
            "hla_backward_workspace_size", "hla_backward_chunked", "hla_backward_chunked_traced",
-           "hla_forward3_workspace_size", "hla_forward3_chunked", "hla_forward3_chunked_traced", "hla_decode3_step")
+           "hla_forward3_workspace_size", "hla_forward3_chunked", "hla_forward3_chunked_traced", "hla_decode3_step",
+           "hla_selftest_expired_wait")
 
 
 class HlaError(RuntimeError):
@@ -98,9 +99,10 @@ def library(path: str | None = None):
                                                 ctypes.POINTER(ctypes.c_void_p)]
     lib.hla_decode3_step.argtypes = [i, i, i, i, S3, vp, vp, vp, vp, vp]
     lib.hla_sync_status.argtypes = [vp]
+    lib.hla_selftest_expired_wait.argtypes = [vp]
     for fn in (lib.hla_forward_chunked, lib.hla_state_combine, lib.hla_decode_step, lib.hla_sync_status,
                lib.hla_backward_chunked, lib.hla_backward_chunked_traced, lib.hla_forward3_chunked,
-               lib.hla_forward3_chunked_traced, lib.hla_decode3_step):
+               lib.hla_forward3_chunked_traced, lib.hla_decode3_step, lib.hla_selftest_expired_wait):
         fn.restype = ctypes.c_int
     lib.hla_status_string.argtypes = [ctypes.c_int]
     lib.hla_status_string.restype = ctypes.c_char_p
@@ -241,6 +243,12 @@ def hla_forward3_chunked_traced(params: hla_params, q, k, v, o, state_in=None, s
 def hla_decode3_step(N: int, d: int, dv: int, dtype: int, state, q, k, v, o, stream=None) -> None:
     _check(library().hla_decode3_step(N, d, dv, dtype, _state3_struct(state), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                                       _stream(stream)))
+
+
+def hla_selftest_expired_wait(stream=None) -> None:
+    """Launch the failure-path self-test (a bounded wait that expires); the next
+    hla_sync_status reports HLA_ERR_TIMEOUT."""
+    _check(library().hla_selftest_expired_wait(_stream(stream)))
 
 
 def hla_sync_status(stream=None) -> None:

@@ -77,6 +77,18 @@ hla_status check_params(const hla_params *p) {
     return HLA_OK;
 }
 
+// One CTA waits, with the bounded barrier wait of the kernels (short poll limit), on a
+// barrier whose phase nothing completes: the wait expires and raises the status word.
+__global__ void expired_wait_kernel(unsigned *err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        hla::mbar_init(&bar, 1);
+        hla::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) hla::mbar_wait(&bar, 0u, err, 1u << 14);
+}
+
 }  // namespace
 
 namespace hla {
@@ -394,6 +406,16 @@ hla_status hla_decode_step(int N, int H, int Hkv, int d, int dv, hla_dtype dtype
     a.q = q; a.k = k; a.v = v; a.o = o;
     cudaError_t e = hla::decode_launch(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return HLA_OK;
+}
+
+hla_status hla_selftest_expired_wait(void *stream) {
+    unsigned *err = nullptr;
+    cudaError_t e = status_ptr(&err);
+    if (e != cudaSuccess) return cuda_fail(e, "status word");
+    expired_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
     return HLA_OK;
 }
 

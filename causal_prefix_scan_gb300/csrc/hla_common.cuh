@@ -53,8 +53,8 @@ HLA_DEVICE bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 // Bounded wait for the phase with the given parity to complete.  Returns false
 // (and raises the sticky flag) if it never does.
-HLA_DEVICE bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+HLA_DEVICE bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err, uint32_t limit = kWaitLimit) {
+    for (uint32_t i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;  // try_wait itself suspends briefly
         if (i > 4096) __nanosleep(64);
     }

@@ -268,6 +268,13 @@ HLA_API hla_status hla_forward3_chunked_traced(const hla_params *p, const void *
 HLA_API hla_status hla_decode3_step(int N, int d, int dv, hla_dtype dtype, const hla_state3 *state, const void *q,
                                     const void *k, const void *v, void *o, void *stream);
 
+/* Self-test of the failure path: launches one CTA that waits, with the library's
+ * bounded barrier wait (a short poll limit), on a barrier that nothing completes.  The
+ * wait expires, raises the sticky device flag and the kernel returns; nothing traps or
+ * hangs.  The next hla_sync_status on `stream` reports HLA_ERR_TIMEOUT (once) and the
+ * context stays usable. */
+HLA_API hla_status hla_selftest_expired_wait(void *stream);
+
 /* Synchronise `stream`, then report and clear the sticky device flag: HLA_OK,
  * HLA_ERR_TIMEOUT if a bounded device wait expired since the last call, or
  * HLA_ERR_CUDA if the stream reported an error. */
