@@ -386,10 +386,12 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t st) {
     const size_t b1 = LocSmem<C, D, DV>::TOTAL * sizeof(float), b2 = ScanSmem<C, D, DV>::TOTAL * sizeof(float),
                  b3 = GradSmem<C, D, DV>::TOTAL * sizeof(float);
     cudaError_t e;
-    if ((e = smem_attr(bwd_local_kernel<T, C, D, DV>, b1)) != cudaSuccess) return e;
-    if ((e = smem_attr(bwd_scan_kernel<C, D, DV>, b2)) != cudaSuccess) return e;
-    if ((e = smem_attr(bwd_grad_kernel<T, C, D, DV>, b3)) != cudaSuccess) return e;
     constexpr bool TC = std::is_same<T, __nv_bfloat16>::value && C == 64 && D == 64 && DV == 64;
+    if constexpr (!TC) {  // the CUDA-core kernels (the tensor-core ones set their own attributes)
+        if ((e = smem_attr(bwd_local_kernel<T, C, D, DV>, b1)) != cudaSuccess) return e;
+        if ((e = smem_attr(bwd_scan_kernel<C, D, DV>, b2)) != cudaSuccess) return e;
+        if ((e = smem_attr(bwd_grad_kernel<T, C, D, DV>, b3)) != cudaSuccess) return e;
+    }
     auto mark = [&](int i) { return a.events ? cudaEventRecord(a.events[i], st) : cudaSuccess; };
     if ((e = mark(0)) != cudaSuccess) return e;
     if constexpr (TC) {
