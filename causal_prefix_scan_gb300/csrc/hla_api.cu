@@ -191,7 +191,7 @@ hla_status check_bwd_params(const hla_params *p) {
         return fail(HLA_ERR_ARG, "problem too large");
     if (!hla::bwd_simt_supported(*p))
         return fail(HLA_ERR_UNSUPPORTED,
-                    "backward supports flags 0 or HLA_DECAY, Hkv = H, d, dv, chunk in {16,32,64} "
+                    "backward supports flags 0 or HLA_DECAY, d, dv, chunk in {16,32,64} "
                     "(got flags=%u Hkv=%d d=%d dv=%d chunk=%d)",
                     p->flags, p->Hkv, p->d, p->dv, p->chunk);
     return HLA_OK;
@@ -226,10 +226,13 @@ hla_status hla_backward_chunked_traced(const hla_params *p, const void *q, const
     if (!aligned16(workspace)) return fail(HLA_ERR_ARG, "workspace must be 16-byte aligned");
     hla::BwdArgs a;
     a.B = p->B; a.H = p->H; a.n = p->n; a.d = p->d; a.dv = p->dv; a.chunk = p->chunk;
+    a.Hkv = p->Hkv > 0 ? p->Hkv : p->H;
     a.in_dtype = p->in_dtype; a.flags = p->flags & HLA_DECAY; a.gamma = p->gamma;
     a.q = q; a.k = k; a.v = v; a.go = dout;
     a.grad_q = dq; a.grad_k = dk; a.grad_v = dv;
     a.workspace = static_cast<float *>(workspace);
+    a.dk_pair = a.Hkv < a.H ? a.workspace + hla::bwd_pair_offset(*p) : nullptr;
+    a.dv_pair = a.Hkv < a.H ? a.dk_pair + (size_t)p->B * p->H * p->n * p->d : nullptr;
     if (phase_events) {
         for (int i = 0; i < 4; ++i)
             if (!phase_events[i]) return fail(HLA_ERR_ARG, "phase_events must hold four events");

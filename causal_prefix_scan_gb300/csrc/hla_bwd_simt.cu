@@ -30,14 +30,22 @@ cudaError_t launch_c(const BwdArgs &a, cudaStream_t st) {
 bool bwd_simt_supported(const hla_params &p) {
     auto ok = [](int x) { return x == 16 || x == 32 || x == 64; };
     const int hkv = p.Hkv > 0 ? p.Hkv : p.H;
-    return ok(p.d) && ok(p.dv) && ok(p.chunk) && hkv == p.H &&
+    return ok(p.d) && ok(p.dv) && ok(p.chunk) && p.H % hkv == 0 &&
            !(p.flags & (HLA_NORMALIZE | HLA_UNMASKED | HLA_ASYMMETRIC));
 }
 
-size_t bwd_simt_workspace(const hla_params &p) {
+// Local sums and chunk states, then (shared key/value heads only) the per-query-head
+// dk, dv before their group sum.
+size_t bwd_pair_offset(const hla_params &p) {
     const size_t nch = ((size_t)p.n + p.chunk - 1) / p.chunk;
     const bwd::BwdWs w{p.d, p.dv};
-    return (size_t)p.B * p.H * nch * (w.loc_floats() + w.st_floats()) * sizeof(float);
+    return (size_t)p.B * p.H * nch * (w.loc_floats() + w.st_floats());
+}
+
+size_t bwd_simt_workspace(const hla_params &p) {
+    const int hkv = p.Hkv > 0 ? p.Hkv : p.H;
+    const size_t pair = hkv < p.H ? (size_t)p.B * p.H * p.n * ((size_t)p.d + p.dv) : 0;
+    return (bwd_pair_offset(p) + pair) * sizeof(float);
 }
 
 cudaError_t bwd_simt_launch(const BwdArgs &a, cudaStream_t st) {

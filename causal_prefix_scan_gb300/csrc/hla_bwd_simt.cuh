@@ -56,6 +56,28 @@ namespace bwd {
 using namespace tile;
 constexpr int kSplit = 4;  // column blocks per (b,h) and direction in the scan
 
+// Key/value head read by query pair u = b*H + h: b*Hkv + h / (H / Hkv).
+__device__ __forceinline__ size_t kv_unit(const BwdArgs &a, int u) {
+    return (size_t)(u / a.H) * a.Hkv + (u % a.H) / (a.H / a.Hkv);
+}
+
+// Shared key/value heads: dk, dv of a key/value head = the sum of the per-query-head
+// fp32 gradients of its group (in head order), converted to the output type.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) bwd_group_sum_kernel(const float *pair, T *out, int B, int H, int Hkv,
+                                                                  size_t per_head) {
+    const size_t total = (size_t)B * Hkv * per_head;
+    const int grp = H / Hkv;
+    for (size_t e = (size_t)blockIdx.x * kThreads + threadIdx.x; e < total; e += (size_t)gridDim.x * kThreads) {
+        const size_t j = e / per_head, x = e % per_head;  // key/value unit b*Hkv + h', element
+        const size_t b = j / Hkv, hk = j % Hkv;
+        const float *src = pair + ((b * H + hk * grp) * per_head + x);
+        float s = 0.f;
+        for (int g = 0; g < grp; ++g) s += src[(size_t)g * per_head];
+        st_t(out, e, s);
+    }
+}
+
 // Workspace: the six local sums of every (b,h, chunk), then the four states of
 // every (b,h, chunk).
 struct BwdWs {
@@ -100,9 +122,10 @@ __global__ void __launch_bounds__(kThreads) bwd_local_kernel(BwdArgs a) {
     const bool decay = (a.flags & HLA_DECAY) != 0;
     const float lg = log2f(decay ? a.gamma[u % a.H] : 1.f);
     const size_t rq = ((size_t)u * a.n + t0) * D, rv = ((size_t)u * a.n + t0) * DV;
+    const size_t kvu = kv_unit(a, u), rk = (kvu * a.n + t0) * D, rkv = (kvu * a.n + t0) * DV;
     load_rows<D>(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L);
-    load_rows<D>(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L);
-    load_rows<DV>(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L);
+    load_rows<D>(static_cast<const T *>(a.k) + rk, K, Sm::LQ, C, L);
+    load_rows<DV>(static_cast<const T *>(a.v) + rkv, V, Sm::LV, C, L);
     load_rows<DV>(static_cast<const T *>(a.go) + rv, G, Sm::LV, C, L);
     fill_gp(gp, C, lg, decay);
     __syncthreads();
@@ -293,9 +316,10 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(BwdArgs a) {
     copy_mat_async<DV>(so + ws.o_lam(), DV, Lam, Sm::LV, D);
     copy_mat_async<D>(so + ws.o_om(), D, Om, Sm::LQ, D);
     cp_async_commit();
+    const size_t kvu = kv_unit(a, u), rk = (kvu * a.n + t0) * D, rkv = (kvu * a.n + t0) * DV;
     load_rows<D>(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L);
-    load_rows<D>(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L);
-    load_rows<DV>(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L);
+    load_rows<D>(static_cast<const T *>(a.k) + rk, K, Sm::LQ, C, L);
+    load_rows<DV>(static_cast<const T *>(a.v) + rkv, V, Sm::LV, C, L);
     load_rows<DV>(static_cast<const T *>(a.go) + rv, G, Sm::LV, C, L);
     fill_gp(gp, C, lg, decay);
     __syncthreads();
@@ -336,8 +360,11 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(BwdArgs a) {
     });
     __syncthreads();
     T *gq = static_cast<T *>(a.grad_q) + rq;
-    T *gk = static_cast<T *>(a.grad_k) + rq;
-    T *gv = static_cast<T *>(a.grad_v) + rv;
+    // dk, dv: straight to the output with one query head per key/value head, else to
+    // the per-query-head fp32 staging that the group sum reads
+    T *gk = a.dk_pair ? nullptr : static_cast<T *>(a.grad_k) + rq;
+    T *gv = a.dv_pair ? nullptr : static_cast<T *>(a.grad_v) + rv;
+    float *pk = a.dk_pair ? a.dk_pair + rq : nullptr, *pv = a.dv_pair ? a.dv_pair + rv : nullptr;
     // dQ = P U + diag(g^{2(tau+1)}) G X_p^T + diag(g^{tau+1}) dU S_p + B K   (S_p symmetric)
     tiles<false, C, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, false>(acc, P, Sm::LT, U, Sm::LQ, m0, n0, ns, C);
@@ -355,7 +382,10 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(BwdArgs a) {
         mac_rs<false, false>(acc, r_l1, K, Sm::LQ, Om, Sm::LQ, m0, n0, ns, D);
         mac_rs<false, true>(acc, r_l1, K, Sm::LQ, Om, Sm::LQ, m0, n0, ns, D);
         each(acc, m0, n0, ns, [&](int t, int i, float x) {
-            if (t < L) st_t(gk, (size_t)t * D + i, x);
+            if (t < L) {
+                if (pk) pk[(size_t)t * D + i] = x;
+                else st_t(gk, (size_t)t * D + i, x);
+            }
         });
     });
     __syncthreads();
@@ -370,7 +400,10 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(BwdArgs a) {
         mac<true, false>(acc, P, Sm::LT, G, Sm::LV, m0, n0, ns, C);
         mac_rs<false, false>(acc, r_l2, U, Sm::LQ, Lam, Sm::LV, m0, n0, ns, D);
         each(acc, m0, n0, ns, [&](int t, int j, float x) {
-            if (t < L) st_t(gv, (size_t)t * DV + j, x);
+            if (t < L) {
+                if (pv) pv[(size_t)t * DV + j] = x;
+                else st_t(gv, (size_t)t * DV + j, x);
+            }
         });
     });
 }
@@ -410,6 +443,15 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t st) {
         if ((e = bwdtc::grad_tc(a, st)) != cudaSuccess) return e;
     } else {
         bwd_grad_kernel<T, C, D, DV><<<units * nch, kThreads, b3, st>>>(a);
+    }
+    if (a.dk_pair) {  // shared key/value heads: sum each group's gradients
+        const size_t elems = (size_t)a.B * a.Hkv * a.n * (D > DV ? D : DV);
+        const int blocks = (int)((elems + kThreads - 1) / kThreads < 8192 ? (elems + kThreads - 1) / kThreads : 8192);
+        bwd_group_sum_kernel<T><<<blocks, kThreads, 0, st>>>(a.dk_pair, static_cast<T *>(a.grad_k), a.B, a.H, a.Hkv,
+                                                            (size_t)a.n * D);
+        bwd_group_sum_kernel<T><<<blocks, kThreads, 0, st>>>(a.dv_pair, static_cast<T *>(a.grad_v), a.B, a.H, a.Hkv,
+                                                            (size_t)a.n * DV);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if ((e = mark(3)) != cudaSuccess) return e;
     return cudaGetLastError();

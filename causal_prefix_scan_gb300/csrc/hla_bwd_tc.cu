@@ -45,9 +45,10 @@ __global__ void __launch_bounds__(kTc, 2) bwd_local_tc_kernel(const __grid_const
     const int t0 = ch * 64, L = min(64, a.n - t0);
     const bool decay = (a.flags & HLA_DECAY) != 0;
     const size_t r0 = ((size_t)u * a.n + t0) * 64;
+    const size_t rk = (bwd::kv_unit(a, u) * a.n + t0) * 64;  // rows of the key/value head
     const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q) + r0;
-    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k) + r0;
-    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v) + r0;
+    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k) + rk;
+    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v) + rk;
     const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(a.go) + r0;
     fill_gp(gp, a, u);
     {
@@ -172,9 +173,10 @@ __global__ void __launch_bounds__(kTc, 1) bwd_grad_tc_kernel(const __grid_consta
         a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
     fill_gp(gp, a, u);
     {
+        const size_t rk = (bwd::kv_unit(a, u) * a.n + t0) * 64;  // rows of the key/value head
         const __nv_bfloat16 *src[4] = {static_cast<const __nv_bfloat16 *>(a.q) + r0,
-                                       static_cast<const __nv_bfloat16 *>(a.k) + r0,
-                                       static_cast<const __nv_bfloat16 *>(a.v) + r0,
+                                       static_cast<const __nv_bfloat16 *>(a.k) + rk,
+                                       static_cast<const __nv_bfloat16 *>(a.v) + rk,
                                        static_cast<const __nv_bfloat16 *>(a.go) + r0};
         uint8_t *dst[4] = {x.tile(G_Q), x.tile(G_K), x.tile(G_V), x.tile(G_G)};
         load_tiles_bf16<4>(src, L, dst);
@@ -277,12 +279,18 @@ __global__ void __launch_bounds__(kTc, 1) bwd_grad_tc_kernel(const __grid_consta
         x.ld_row(128, s);
 #pragma unroll
         for (int i = 0; i < 16; ++i) r[i] += r_l1 * s[i];
-        if (in) st_row16_bf16(static_cast<__nv_bfloat16 *>(a.grad_k) + ro, r);
+        if (in) {  // per-query-head fp32 staging with shared key/value heads
+            if (a.dk_pair) st_row16(a.dk_pair + ro, r);
+            else st_row16_bf16(static_cast<__nv_bfloat16 *>(a.grad_k) + ro, r);
+        }
         x.ld_row(0, r);
         x.ld_row(192, s);
 #pragma unroll
         for (int i = 0; i < 16; ++i) r[i] += r_l2 * s[i];
-        if (in) st_row16_bf16(static_cast<__nv_bfloat16 *>(a.grad_v) + ro, r);
+        if (in) {
+            if (a.dv_pair) st_row16(a.dv_pair + ro, r);
+            else st_row16_bf16(static_cast<__nv_bfloat16 *>(a.grad_v) + ro, r);
+        }
     } while (false);
     teardown(x);
 }

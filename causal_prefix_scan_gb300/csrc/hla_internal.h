@@ -67,12 +67,14 @@ cudaError_t decode_launch(const DecodeArgs &a, cudaStream_t st);
 
 struct BwdArgs {
     int B, H, n, d, dv, chunk;
+    int Hkv;  // key/value heads (H % Hkv == 0); below H, dk and dv are summed over each group
     hla_dtype in_dtype;
     unsigned flags;  // 0 or HLA_DECAY
     const float *gamma;
     const void *q, *k, *v, *go;    // inputs and the gradient of the output
     void *grad_q, *grad_k, *grad_v;  // outputs
     float *workspace;
+    float *dk_pair, *dv_pair;  // Hkv < H: fp32 dk, dv of every query head before the group sum
     cudaEvent_t const *events;  // NULL or four events recorded at the phase boundaries
     unsigned *err;              // sticky device status word (bounded waits of the tensor-core kernels)
 };
@@ -80,6 +82,7 @@ struct BwdArgs {
 // Backward of the masked forward on CUDA cores (d, dv, chunk in {16,32,64}).
 bool bwd_simt_supported(const hla_params &p);
 size_t bwd_simt_workspace(const hla_params &p);
+size_t bwd_pair_offset(const hla_params &p);  // floats before the per-query-head dk, dv
 cudaError_t bwd_simt_launch(const BwdArgs &a, cudaStream_t st);
 
 struct Fwd3Args {

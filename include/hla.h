@@ -199,10 +199,12 @@ HLA_API hla_status hla_decode_step(int N, int H, int Hkv, int d, int dv, hla_dty
  * of sum_t dout_t . o_t up to floating-point rounding.
  *
  *   p      as for hla_forward_chunked; supported: flags 0 or HLA_DECAY only
- *          (others HLA_ERR_UNSUPPORTED), Hkv 0 or H, d, dv, chunk in {16,32,64},
- *          in_dtype HLA_F32 or HLA_BF16 (fp32 arithmetic either way);
- *   q, k   [B][H][n][d], v and dout [B][H][n][dv], in_dtype, read only;
- *   dq, dk [B][H][n][d], dv [B][H][n][dv], in_dtype, written (not accumulated);
+ *          (others HLA_ERR_UNSUPPORTED), Hkv dividing H (0 means H), d, dv, chunk in
+ *          {16,32,64}, in_dtype HLA_F32 or HLA_BF16 (fp32 arithmetic either way);
+ *   q      [B][H][n][d], k [B][Hkv][n][d], v [B][Hkv][n][dv], dout [B][H][n][dv],
+ *          in_dtype, read only (query head h reads key/value head h / (H / Hkv));
+ *   dq     [B][H][n][d], dk [B][Hkv][n][d], dv [B][Hkv][n][dv], in_dtype, written (not
+ *          accumulated); with Hkv < H, dk and dv are the sums over each group;
  *   workspace device scratch of at least hla_backward_workspace_size(p) bytes,
  *          16-byte aligned, no initial contents needed.
  * All tensor pointers 16-byte aligned.  Three kernel launches on `stream`.

@@ -597,9 +597,9 @@ static void backward_unit(int n, int d, int dv, double g, const double *q, const
 }
 
 typedef struct {
-    int B, H, n, d, dv, next;
+    int B, H, Hkv, n, d, dv, next;
     const double *q, *k, *v, *go, *gamma;
-    double *dq, *dk, *dv_out;
+    double *dq, *dk_pair, *dv_pair;  /* dk, dv of every query head before the group sum */
     pthread_mutex_t lock;
 } bjob_t;
 
@@ -611,25 +611,34 @@ static void *bworker(void *arg)
         const int u = J->next < J->B * J->H ? J->next++ : -1;
         pthread_mutex_unlock(&J->lock);
         if (u < 0) break;
+        /* query head h of batch row b reads key/value head h / (H / Hkv) */
+        const size_t kvu = (size_t)(u / J->H) * J->Hkv + (u % J->H) / (J->H / J->Hkv);
         const size_t qo = (size_t)u * J->n * J->d, vo = (size_t)u * J->n * J->dv;
-        backward_unit(J->n, J->d, J->dv, J->gamma ? J->gamma[u % J->H] : 1.0, J->q + qo, J->k + qo, J->v + vo,
-                      J->go + vo, J->dq + qo, J->dk + qo, J->dv_out + vo);
+        const size_t ko = kvu * J->n * J->d, kvo = kvu * J->n * J->dv;
+        backward_unit(J->n, J->d, J->dv, J->gamma ? J->gamma[u % J->H] : 1.0, J->q + qo, J->k + ko, J->v + kvo,
+                      J->go + vo, J->dq + qo, J->dk_pair + qo, J->dv_pair + vo);
     }
     return NULL;
 }
 
 /* Gradients of sum_t go_t . o_t with respect to q, k, v for the masked forward
- * from a zero state, without normalisation.  Layout as the forward (Hkv = H). */
-int hla_oracle_backward(int B, int H, int n, int d, int dv, const double *q, const double *k,
+ * from a zero state, without normalisation.  q, go: [B][H][n][.]; k, v, dk, dv:
+ * [B][Hkv][n][.] (H a multiple of Hkv; query head h reads key/value head
+ * h / (H / Hkv)).  The gradient of a shared key or value is the sum of the
+ * gradients through every query head of its group (chain rule), added in head order. */
+int hla_oracle_backward(int B, int H, int Hkv, int n, int d, int dv, const double *q, const double *k,
                         const double *v, const double *gamma, const double *go, double *dq, double *dk,
                         double *dvo, int nthreads)
 {
-    if (check_dims(B, H, n, d, dv)) return -1;
+    if (check_dims(B, H, n, d, dv) || Hkv < 1 || H % Hkv) return -1;
+    const size_t nd = (size_t)n * d, ndv = (size_t)n * dv;
+    double *dkp = (double *)calloc((size_t)B * H * nd + 1, sizeof(double));
+    double *dvp = (double *)calloc((size_t)B * H * ndv + 1, sizeof(double));
     bjob_t J;
     memset(&J, 0, sizeof J);
-    J.B = B; J.H = H; J.n = n; J.d = d; J.dv = dv;
+    J.B = B; J.H = H; J.Hkv = Hkv; J.n = n; J.d = d; J.dv = dv;
     J.q = q; J.k = k; J.v = v; J.go = go; J.gamma = gamma;
-    J.dq = dq; J.dk = dk; J.dv_out = dvo;
+    J.dq = dq; J.dk_pair = dkp; J.dv_pair = dvp;
     pthread_mutex_init(&J.lock, NULL);
     const int total = B * H;
     if (nthreads < 1) nthreads = 1;
@@ -642,6 +651,21 @@ int hla_oracle_backward(int B, int H, int n, int d, int dv, const double *q, con
     for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
     free(th);
     pthread_mutex_destroy(&J.lock);
+    /* group sums */
+    const int grp = H / Hkv;
+    for (int b = 0; b < B; ++b)
+        for (int j = 0; j < Hkv; ++j) {
+            double *dko = dk + ((size_t)b * Hkv + j) * nd, *dvo_ = dvo + ((size_t)b * Hkv + j) * ndv;
+            memset(dko, 0, nd * sizeof(double));
+            memset(dvo_, 0, ndv * sizeof(double));
+            for (int g = 0; g < grp; ++g) {
+                const size_t u = (size_t)b * H + (size_t)j * grp + g;
+                for (size_t e = 0; e < nd; ++e) dko[e] += dkp[u * nd + e];
+                for (size_t e = 0; e < ndv; ++e) dvo_[e] += dvp[u * ndv + e];
+            }
+        }
+    free(dkp);
+    free(dvp);
     return 0;
 }
 

@@ -139,7 +139,6 @@ def _bcall(p, ptrs=(16,) * 7, ws=16, ws_bytes=1 << 40):
     (dict(flags=hla.HLA_NORMALIZE), hla.HLA_ERR_UNSUPPORTED),
     (dict(flags=hla.HLA_UNMASKED), hla.HLA_ERR_UNSUPPORTED),
     (dict(flags=hla.HLA_ASYMMETRIC), hla.HLA_ERR_UNSUPPORTED),
-    (dict(H=4, Hkv=2), hla.HLA_ERR_UNSUPPORTED),             # shared key/value heads
     (dict(H=6, Hkv=4), hla.HLA_ERR_ARG),
     (dict(d=128), hla.HLA_ERR_UNSUPPORTED),
     (dict(dv=128), hla.HLA_ERR_UNSUPPORTED),
@@ -170,6 +169,12 @@ def test_backward_workspace_size_and_empty_sequence(lib):
         want = B * H * nch * (4 * d * d + 6 * d * dv) * 4
         got = hla.hla_backward_workspace_size(_params(B=B, H=H, n=n, d=d, dv=dv, chunk=c, in_dtype=hla.HLA_F32))
         assert got == want
+    # shared key/value heads: plus the fp32 dk, dv of every query head before the group sum
+    B, H, n, d, dv, c = 2, 4, 100, 32, 16, 32
+    nch = -(-n // c)
+    base = B * H * nch * (4 * d * d + 6 * d * dv) * 4
+    assert hla.hla_backward_workspace_size(_params(B=B, H=H, Hkv=2, n=n, d=d, dv=dv, chunk=c,
+                                                   in_dtype=hla.HLA_F32)) == base + B * H * n * (d + dv) * 4
     # no tokens: nothing to compute, no pointer needed
     assert _bcall(_params(n=0), ptrs=(None,) * 7, ws=None, ws_bytes=0) == hla.HLA_OK
 

@@ -135,3 +135,14 @@ def test_backward_tensor_core_short_sequences(n):
     x = W.make_inputs(w)
     g = W.make_dout(w)
     check(run_backward(x, g, "bf16", 64), run_oracle(x, g), TOL_BF16, f"bwd tc n{n}")
+
+
+@pytest.mark.parametrize("d,dv,chunk,dtype", [(64, 64, 64, "bf16"), (32, 16, 32, "f32")])
+@pytest.mark.parametrize("Hkv", [1, 2])
+def test_backward_shared_kv_heads(d, dv, chunk, dtype, Hkv):
+    """Keys and values shared by groups of query heads: dk, dv summed over each group."""
+    w = small(B=2, H=4, Hkv=Hkv, n=2 * chunk + 9, d=d, dv=dv, chunk=chunk, decay=True, dtype=dtype, seed=39)
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    check(run_backward(x, g, dtype, chunk), run_oracle(x, g), TOL_F32 if dtype == "f32" else TOL_BF16,
+          f"bwd {dtype} H4 Hkv{Hkv}")

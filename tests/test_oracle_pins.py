@@ -580,3 +580,23 @@ def test_backward_dense_form():
     dQ = dM @ U + dAt @ K
     dK = At.T @ dU + dAt.T @ Q
     assert rel(dq[0, 0], dQ) < 1e-12 and rel(dk[0, 0], dK) < 1e-12 and rel(dvv[0, 0], dV) < 1e-12
+
+
+def test_backward_shared_kv_heads_is_group_sum_of_repeated_heads():
+    """Keys and values shared by groups of query heads: the gradient equals that of the
+    same computation with every key/value head repeated for its query heads, with dk
+    and dv summed over each group (chain rule through the repetition)."""
+    rng = np.random.default_rng(12)
+    B, H, Hkv, n, d, dv = 2, 6, 2, 9, 3, 2
+    q = rng.standard_normal((B, H, n, d))
+    k = rng.standard_normal((B, Hkv, n, d))
+    v = rng.standard_normal((B, Hkv, n, dv))
+    go = rng.standard_normal((B, H, n, dv))
+    g = rng.uniform(0.8, 1.0, H)
+    rep = H // Hkv
+    kr, vr = np.repeat(k, rep, axis=1), np.repeat(v, rep, axis=1)
+    dq_r, dk_r, dv_r = oracle.backward(q, kr, vr, go, g)
+    dq, dk, dvv = oracle.backward(q, k, v, go, g)
+    assert rel(dq, dq_r) < 1e-13
+    assert rel(dk, dk_r.reshape(B, Hkv, rep, n, d).sum(axis=2)) < 1e-13
+    assert rel(dvv, dv_r.reshape(B, Hkv, rep, n, dv).sum(axis=2)) < 1e-13
