@@ -76,7 +76,7 @@ def _load():
         _lib.hla_oracle_forward_chunked.argtypes = [i] * 8 + [dp, dp, dp, dp, i, d] + [dp] * 5 + [dp] + [dp] * 5 + [i]
         _lib.hla_oracle_decode_step.argtypes = [i] * 6 + [dp, i, d] + [dp] * 5 + [dp, dp, dp, dp, i]
         _lib.hla_oracle_combine.argtypes = [i, i, i, i] + [dp] * 10 + [dp] + [dp] * 5
-        _lib.hla_oracle_backward.argtypes = [i] * 6 + [dp] * 8 + [i]
+        _lib.hla_oracle_backward.argtypes = [i] * 7 + [d] + [dp] * 8 + [i]
         _lib.hla_oracle3_forward.argtypes = [i] * 6 + [dp] * 6 + [i]
         _lib.hla_oracle3_combine.argtypes = [i, i, i, dp, dp, dp]
         for f in (_lib.hla_oracle_forward, _lib.hla_oracle_forward_chunked,
@@ -220,9 +220,10 @@ def combine(A: State, Bst: State, decay_pow=None, asymmetric=False) -> State:
     return out
 
 
-def backward(q, k, v, go, gamma=None, nthreads=None):
+def backward(q, k, v, go, gamma=None, nthreads=None, normalize=False, eps=0.0):
     """Gradients (dq, dk, dv) of sum_t go_t . o_t for the masked forward from a zero
-    state, without normalisation (reverse mode of the recurrence in hla_oracle.c).
+    state (reverse mode of the recurrence in hla_oracle.c), through the ratio
+    normalisation o = num / (den + eps) when `normalize`.
     q, go: [B,H,n,d|dv]; k, v: [B,Hkv,n,d|dv] with H a multiple of Hkv (query head h
     reads key/value head h // (H // Hkv); dk, dv sum over the heads of a group);
     gamma: [H] or None."""
@@ -233,8 +234,8 @@ def backward(q, k, v, go, gamma=None, nthreads=None):
     assert k.shape == (B, Hkv, n, d) and v.shape == (B, Hkv, n, dv) and go.shape == (B, H, n, dv) and H % Hkv == 0
     g = _f64(gamma)
     dq, dk, dvv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
-    rc = _load().hla_oracle_backward(B, H, Hkv, n, d, dv, _p(q), _p(k), _p(v), _p(g), _p(go), _p(dq), _p(dk),
-                                     _p(dvv), nthreads or default_threads())
+    rc = _load().hla_oracle_backward(B, H, Hkv, n, d, dv, int(bool(normalize)), float(eps), _p(q), _p(k), _p(v),
+                                     _p(g), _p(go), _p(dq), _p(dk), _p(dvv), nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return dq, dk, dvv

@@ -524,31 +524,32 @@ int hla_oracle_decode_step(int N, int H, int Hkv, int d, int dv, int variant,
 }
 
 /* ------------------------------------------------------------------------- */
-/* backward pass of the masked forward (zero initial state, no normalisation) */
-/*
- * Forward, in the form X = S C - G (gist.science summary, section 1, expanded):
- *   S_t = g S_{t-1} + k_t k_t^T,  u_t = S_t q_t,  X_t = g^2 X_{t-1} + u_t v_t^T,
- *   o_t = X_t^T q_t.
- * Reverse mode with upstream gradients go_t = dL/do_t, accumulators
- * Lam_t = dL/dX_t = q_t go_t^T + g^2 Lam_{t+1} and Om_t = dL/dS_t = du_t q_t^T + g Om_{t+1}:
- *   du_t = Lam_t v_t,  dv_t = Lam_t^T u_t,  dq_t = X_t go_t + S_t du_t,
- *   dk_t = (Om_t + Om_t^T) k_t.
- * The pages give no gradient formulas; this is the chain rule applied to the
- * recurrence above, token by token, from the last token to the first.
- */
-static void backward_unit(int n, int d, int dv, double g, const double *q, const double *k,
-                          const double *v, const double *go, double *dq, double *dk, double *dvo)
+/* backward pass of the masked forward (zero initial state), optionally through the
+ * ratio normalisation o_t = n_t / (den_t + eps), n_t = X_t^T q_t, den_t = Y_t . q_t with
+ * Y_t = g^2 Y_{t-1} + u_t (the output with every value equal to one).  Reverse mode
+ * with r_t = 1 / (den_t + eps), gn_t = r_t go_t, gd_t = -r_t (go_t . o_t):
+ *   Lam_t = q_t gn_t^T + g^2 Lam_{t+1},  Lamy_t = gd_t q_t + g^2 Lamy_{t+1},
+ *   du_t = Lam_t v_t + Lamy_t,  dv_t = Lam_t^T u_t,  dq_t = X_t gn_t + gd_t Y_t + S_t du_t,
+ *   Om_t = du_t q_t^T + g Om_{t+1},  dk_t = (Om_t + Om_t^T) k_t.
+ * Without normalisation gn = go and gd = 0. */
+static void backward_unit(int n, int d, int dv, double g, int normalize, double eps, const double *q,
+                          const double *k, const double *v, const double *go, double *dq, double *dk, double *dvo)
 {
     double *S = (double *)calloc((size_t)(n + 1) * d * d, sizeof(double));  /* S_t after token t */
     double *X = (double *)calloc((size_t)(n + 1) * d * dv, sizeof(double)); /* X_t after token t */
+    double *Y = (double *)calloc((size_t)(n + 1) * d, sizeof(double));      /* Y_t after token t */
     double *U = (double *)calloc((size_t)n * d, sizeof(double));            /* u_t */
+    double *gn = (double *)calloc((size_t)n * dv + 1, sizeof(double));      /* dL/dn_t */
+    double *gd = (double *)calloc((size_t)n + 1, sizeof(double));           /* dL/dden_t */
     double *Lam = (double *)calloc((size_t)d * dv, sizeof(double));
+    double *Lamy = (double *)calloc((size_t)d, sizeof(double));
     double *Om = (double *)calloc((size_t)d * d, sizeof(double));
     double *du = (double *)calloc((size_t)d, sizeof(double));
     for (int t = 0; t < n; ++t) { /* forward, keeping every state */
         const double *qt = q + (size_t)t * d, *kt = k + (size_t)t * d, *vt = v + (size_t)t * dv;
-        const double *Sp = S + (size_t)t * d * d, *Xp = X + (size_t)t * d * dv;
-        double *St = S + (size_t)(t + 1) * d * d, *Xt = X + (size_t)(t + 1) * d * dv, *ut = U + (size_t)t * d;
+        const double *Sp = S + (size_t)t * d * d, *Xp = X + (size_t)t * d * dv, *Yp = Y + (size_t)t * d;
+        double *St = S + (size_t)(t + 1) * d * d, *Xt = X + (size_t)(t + 1) * d * dv, *Yt = Y + (size_t)(t + 1) * d;
+        double *ut = U + (size_t)t * d;
         for (int i = 0; i < d; ++i)
             for (int j = 0; j < d; ++j) St[i * d + j] = g * Sp[i * d + j] + kt[i] * kt[j];
         for (int i = 0; i < d; ++i) {
@@ -556,19 +557,40 @@ static void backward_unit(int n, int d, int dv, double g, const double *q, const
             for (int j = 0; j < d; ++j) acc += St[i * d + j] * qt[j];
             ut[i] = acc;
         }
-        for (int i = 0; i < d; ++i)
+        for (int i = 0; i < d; ++i) {
             for (int j = 0; j < dv; ++j) Xt[i * dv + j] = g * g * Xp[i * dv + j] + ut[i] * vt[j];
+            Yt[i] = g * g * Yp[i] + ut[i];
+        }
+        const double *gt = go + (size_t)t * dv;
+        if (normalize) { /* n_t, den_t, then gn_t and gd_t */
+            double den = eps, dot = 0.0;
+            for (int i = 0; i < d; ++i) den += qt[i] * Yt[i];
+            const double r = 1.0 / den;
+            for (int j = 0; j < dv; ++j) {
+                double nj = 0.0;
+                for (int i = 0; i < d; ++i) nj += Xt[i * dv + j] * qt[i];
+                gn[(size_t)t * dv + j] = r * gt[j];
+                dot += gt[j] * nj * r; /* go_t . o_t */
+            }
+            gd[t] = -r * dot;
+        } else {
+            for (int j = 0; j < dv; ++j) gn[(size_t)t * dv + j] = gt[j];
+            gd[t] = 0.0;
+        }
     }
     for (int t = n - 1; t >= 0; --t) { /* reverse */
         const double *qt = q + (size_t)t * d, *kt = k + (size_t)t * d, *vt = v + (size_t)t * dv;
-        const double *gt = go + (size_t)t * dv, *ut = U + (size_t)t * d;
+        const double *gt = gn + (size_t)t * dv, *ut = U + (size_t)t * d;
         const double *St = S + (size_t)(t + 1) * d * d, *Xt = X + (size_t)(t + 1) * d * dv;
-        /* Lam_t = q_t go_t^T + g^2 Lam_{t+1} */
-        for (int i = 0; i < d; ++i)
-            for (int j = 0; j < dv; ++j) Lam[i * dv + j] = g * g * Lam[i * dv + j] + qt[i] * gt[j];
-        /* du_t = Lam_t v_t;  dv_t = Lam_t^T u_t */
+        const double *Yt = Y + (size_t)(t + 1) * d;
+        /* Lam_t = q_t gn_t^T + g^2 Lam_{t+1};  Lamy_t = gd_t q_t + g^2 Lamy_{t+1} */
         for (int i = 0; i < d; ++i) {
-            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) Lam[i * dv + j] = g * g * Lam[i * dv + j] + qt[i] * gt[j];
+            Lamy[i] = g * g * Lamy[i] + gd[t] * qt[i];
+        }
+        /* du_t = Lam_t v_t + Lamy_t;  dv_t = Lam_t^T u_t */
+        for (int i = 0; i < d; ++i) {
+            double acc = Lamy[i];
             for (int j = 0; j < dv; ++j) acc += Lam[i * dv + j] * vt[j];
             du[i] = acc;
         }
@@ -577,9 +599,9 @@ static void backward_unit(int n, int d, int dv, double g, const double *q, const
             for (int i = 0; i < d; ++i) acc += Lam[i * dv + j] * ut[i];
             dvo[(size_t)t * dv + j] = acc;
         }
-        /* dq_t = X_t go_t + S_t du_t */
+        /* dq_t = X_t gn_t + gd_t Y_t + S_t du_t */
         for (int i = 0; i < d; ++i) {
-            double acc = 0.0;
+            double acc = gd[t] * Yt[i];
             for (int j = 0; j < dv; ++j) acc += Xt[i * dv + j] * gt[j];
             for (int j = 0; j < d; ++j) acc += St[i * d + j] * du[j];
             dq[(size_t)t * d + i] = acc;
@@ -593,11 +615,12 @@ static void backward_unit(int n, int d, int dv, double g, const double *q, const
             dk[(size_t)t * d + i] = acc;
         }
     }
-    free(S); free(X); free(U); free(Lam); free(Om); free(du);
+    free(S); free(X); free(Y); free(U); free(gn); free(gd); free(Lam); free(Lamy); free(Om); free(du);
 }
 
 typedef struct {
-    int B, H, Hkv, n, d, dv, next;
+    int B, H, Hkv, n, d, dv, next, normalize;
+    double eps;
     const double *q, *k, *v, *go, *gamma;
     double *dq, *dk_pair, *dv_pair;  /* dk, dv of every query head before the group sum */
     pthread_mutex_t lock;
@@ -615,20 +638,21 @@ static void *bworker(void *arg)
         const size_t kvu = (size_t)(u / J->H) * J->Hkv + (u % J->H) / (J->H / J->Hkv);
         const size_t qo = (size_t)u * J->n * J->d, vo = (size_t)u * J->n * J->dv;
         const size_t ko = kvu * J->n * J->d, kvo = kvu * J->n * J->dv;
-        backward_unit(J->n, J->d, J->dv, J->gamma ? J->gamma[u % J->H] : 1.0, J->q + qo, J->k + ko, J->v + kvo,
-                      J->go + vo, J->dq + qo, J->dk_pair + qo, J->dv_pair + vo);
+        backward_unit(J->n, J->d, J->dv, J->gamma ? J->gamma[u % J->H] : 1.0, J->normalize, J->eps, J->q + qo,
+                      J->k + ko, J->v + kvo, J->go + vo, J->dq + qo, J->dk_pair + qo, J->dv_pair + vo);
     }
     return NULL;
 }
 
 /* Gradients of sum_t go_t . o_t with respect to q, k, v for the masked forward
- * from a zero state, without normalisation.  q, go: [B][H][n][.]; k, v, dk, dv:
+ * from a zero state, ratio-normalised when `normalize` (o = num / (den + eps)).
+ * q, go: [B][H][n][.]; k, v, dk, dv:
  * [B][Hkv][n][.] (H a multiple of Hkv; query head h reads key/value head
  * h / (H / Hkv)).  The gradient of a shared key or value is the sum of the
  * gradients through every query head of its group (chain rule), added in head order. */
-int hla_oracle_backward(int B, int H, int Hkv, int n, int d, int dv, const double *q, const double *k,
-                        const double *v, const double *gamma, const double *go, double *dq, double *dk,
-                        double *dvo, int nthreads)
+int hla_oracle_backward(int B, int H, int Hkv, int n, int d, int dv, int normalize, double eps, const double *q,
+                        const double *k, const double *v, const double *gamma, const double *go, double *dq,
+                        double *dk, double *dvo, int nthreads)
 {
     if (check_dims(B, H, n, d, dv) || Hkv < 1 || H % Hkv) return -1;
     const size_t nd = (size_t)n * d, ndv = (size_t)n * dv;
@@ -636,7 +660,7 @@ int hla_oracle_backward(int B, int H, int Hkv, int n, int d, int dv, const doubl
     double *dvp = (double *)calloc((size_t)B * H * ndv + 1, sizeof(double));
     bjob_t J;
     memset(&J, 0, sizeof J);
-    J.B = B; J.H = H; J.Hkv = Hkv; J.n = n; J.d = d; J.dv = dv;
+    J.B = B; J.H = H; J.Hkv = Hkv; J.n = n; J.d = d; J.dv = dv; J.normalize = normalize; J.eps = eps;
     J.q = q; J.k = k; J.v = v; J.go = go; J.gamma = gamma;
     J.dq = dq; J.dk_pair = dkp; J.dv_pair = dvp;
     pthread_mutex_init(&J.lock, NULL);

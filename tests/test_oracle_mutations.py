@@ -133,7 +133,7 @@ def test_backward_pin_rejects_planted_mistake(tmp_path):
     subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", str(lib), str(src), "-lm"])
     L = ctypes.CDLL(str(lib))
     dp = ctypes.POINTER(ctypes.c_double)
-    L.hla_oracle_backward.argtypes = [ctypes.c_int] * 6 + [dp] * 8 + [ctypes.c_int]
+    L.hla_oracle_backward.argtypes = [ctypes.c_int] * 7 + [ctypes.c_double] + [dp] * 8 + [ctypes.c_int]
     L.hla_oracle_forward.argtypes = [ctypes.c_int] * 7 + [dp, dp, dp, dp, ctypes.c_int, ctypes.c_double] + \
         [dp] * 5 + [dp] + [dp] * 5 + [ctypes.c_int]
     P = lambda a: a.ctypes.data_as(dp)
@@ -142,7 +142,8 @@ def test_backward_pin_rejects_planted_mistake(tmp_path):
     q, k, v = rand_inputs(rng, 1, 1, n, d, dv)
     go = rng.standard_normal((1, 1, n, dv))
     dq, dk, dvv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
-    assert L.hla_oracle_backward(1, 1, 1, n, d, dv, P(q), P(k), P(v), None, P(go), P(dq), P(dk), P(dvv), 1) == 0
+    assert L.hla_oracle_backward(1, 1, 1, n, d, dv, 0, 0.0, P(q), P(k), P(v), None, P(go), P(dq), P(dk), P(dvv),
+                                 1) == 0
     none = [None] * 5
 
     def loss(kk):

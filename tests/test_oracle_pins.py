@@ -600,3 +600,53 @@ def test_backward_shared_kv_heads_is_group_sum_of_repeated_heads():
     assert rel(dq, dq_r) < 1e-13
     assert rel(dk, dk_r.reshape(B, Hkv, rep, n, d).sum(axis=2)) < 1e-13
     assert rel(dvv, dv_r.reshape(B, Hkv, rep, n, dv).sum(axis=2)) < 1e-13
+
+
+@pytest.mark.parametrize("decay", [False, True])
+def test_backward_normalised_finite_differences(decay):
+    """Ratio-normalised output o = num / (den + eps): the reverse mode through the
+    denominator against central differences of the normalised forward (positive
+    features keep the denominator away from zero)."""
+    rng = np.random.default_rng(63)
+    B, H, n, d, dv = 1, 2, 6, 3, 2
+    q, k, v = rand_inputs(rng, B, H, n, d, dv)
+    q, k = np.abs(q) + 0.2, np.abs(k) + 0.2
+    go = rng.standard_normal((B, H, n, dv))
+    gamma = np.array([0.8, 0.6]) if decay else None
+    e0 = 1e-3
+    dq, dk, dvv = oracle.backward(q, k, v, go, gamma, normalize=True, eps=e0)
+    loss = lambda q_, k_, v_: float(np.sum(go * oracle.forward(q_, k_, v_, gamma=gamma, normalize=True, eps=e0,
+                                                                want_state=False)[0]))
+    h = 1e-6
+    for x, grad, which in ((q, dq, 0), (k, dk, 1), (v, dvv, 2)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = [q, k, v]; args_m = [q, k, v]
+            args_p[which] = xp; args_m[which] = xm
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        assert rel(grad, num) < 1e-6, which
+
+
+def test_backward_normalised_equals_augmented_value():
+    """The normalised gradient is the unnormalised one of the augmented values [V | 1]
+    (the denominator is the output with every value one) with upstream
+    [go / (den + eps) | -(go . o) / (den + eps)]; dv is its first dv columns."""
+    rng = np.random.default_rng(64)
+    B, H, n, d, dv = 2, 2, 13, 4, 3
+    q, k, v = rand_inputs(rng, B, H, n, d, dv)
+    q, k = np.abs(q) + 0.1, np.abs(k) + 0.1
+    go = rng.standard_normal((B, H, n, dv))
+    gamma = np.array([0.9, 0.7])
+    e0 = 1e-4
+    dq, dk, dvv = oracle.backward(q, k, v, go, gamma, normalize=True, eps=e0)
+    num, _ = oracle.forward(q, k, v, gamma=gamma, want_state=False)
+    den, _ = oracle.forward(q, k, np.ones((B, H, n, 1)), gamma=gamma, want_state=False)
+    r = 1.0 / (den + e0)
+    o = num * r
+    ga = np.concatenate([go * r, -np.sum(go * o, axis=-1, keepdims=True) * r], axis=-1)
+    va = np.concatenate([v, np.ones((B, H, n, 1))], axis=-1)
+    dq_a, dk_a, dv_a = oracle.backward(q, k, va, ga, gamma)
+    assert rel(dq, dq_a) < 1e-11 and rel(dk, dk_a) < 1e-11 and rel(dvv, dv_a[..., :dv]) < 1e-11
