@@ -373,13 +373,14 @@ def decode_step(state: State, q, k, v, H: int, gamma=None, normalize: bool = Fal
     return o
 
 
-def backward(q, k, v, dout, chunk: int, gamma=None, workspace=None, out=None, stream=None):
+def backward(q, k, v, dout, chunk: int, gamma=None, workspace=None, out=None, stream=None,
+             normalize: bool = False, eps: float = 0.0):
     """Gradients (dq, dk, dv) of sum(dout * o) for the masked forward o of q, k, v from a
-    zero state, without normalisation.  q, k [B,H,n,d]; v, dout [B,H,n,dv] contiguous CUDA
-    tensors of one dtype (bf16 or fp32); gamma [H] fp32 or None.  ``out`` may hold three
-    preallocated result tensors."""
+    zero state (with ``normalize=True`` the ratio-normalised o).  q [B,H,n,d], k [B,Hkv,n,d],
+    v [B,Hkv,n,dv], dout [B,H,n,dv] contiguous CUDA tensors of one dtype (bf16 or fp32);
+    gamma [H] fp32 or None.  ``out`` may hold three preallocated result tensors."""
     import torch
-    p = make_params(q, v, chunk, gamma)
+    p = make_params(q, v, chunk, gamma, normalize, eps)
     need = hla_backward_workspace_size(p)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)

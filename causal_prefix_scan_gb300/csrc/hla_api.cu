@@ -185,13 +185,14 @@ hla_status check_bwd_params(const hla_params *p) {
     if (p->flags & ~(unsigned)(HLA_NORMALIZE | HLA_DECAY | HLA_UNMASKED | HLA_ASYMMETRIC))
         return fail(HLA_ERR_ARG, "unknown flag bits");
     if ((p->flags & HLA_DECAY) && !p->gamma) return fail(HLA_ERR_ARG, "HLA_DECAY needs gamma");
+    if ((p->flags & HLA_NORMALIZE) && !(p->eps >= 0.f)) return fail(HLA_ERR_ARG, "eps must be >= 0");
     if (p->Hkv < 0 || (p->Hkv > 0 && p->H % p->Hkv != 0))
         return fail(HLA_ERR_ARG, "Hkv must divide H (0 means Hkv = H)");
     if ((long long)p->B * p->H * (long long)p->n * (p->d > p->dv ? p->d : p->dv) > (1LL << 40))
         return fail(HLA_ERR_ARG, "problem too large");
     if (!hla::bwd_simt_supported(*p))
         return fail(HLA_ERR_UNSUPPORTED,
-                    "backward supports flags 0 or HLA_DECAY, d, dv, chunk in {16,32,64} "
+                    "backward supports flags 0, HLA_DECAY, HLA_NORMALIZE, d, dv, chunk in {16,32,64} "
                     "(got flags=%u Hkv=%d d=%d dv=%d chunk=%d)",
                     p->flags, p->Hkv, p->d, p->dv, p->chunk);
     return HLA_OK;
@@ -200,6 +201,7 @@ hla_status check_bwd_params(const hla_params *p) {
 
 size_t hla_backward_workspace_size(const hla_params *p) {
     if (check_bwd_params(p) != HLA_OK) return 0;
+    if (p->flags & HLA_NORMALIZE) return p->n > 0 ? hla::bwd_norm_layout(*p).total : 0;
     return hla::bwd_simt_workspace(*p);
 }
 
@@ -220,10 +222,13 @@ hla_status hla_backward_chunked_traced(const hla_params *p, const void *q, const
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
         !aligned16(dv))
         return fail(HLA_ERR_ARG, "tensor pointers must be 16-byte aligned");
-    const size_t need = hla::bwd_simt_workspace(*p);
+    const bool norm = (p->flags & HLA_NORMALIZE) != 0;
+    const size_t need = norm ? hla::bwd_norm_layout(*p).total : hla::bwd_simt_workspace(*p);
     if (!workspace || workspace_bytes < need)
         return fail(HLA_ERR_ARG, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
-    if (!aligned16(workspace)) return fail(HLA_ERR_ARG, "workspace must be 16-byte aligned");
+    if (norm ? (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 : !aligned16(workspace))
+        return fail(HLA_ERR_ARG, norm ? "workspace must be 256-byte aligned with HLA_NORMALIZE"
+                                      : "workspace must be 16-byte aligned");
     hla::BwdArgs a;
     a.B = p->B; a.H = p->H; a.n = p->n; a.d = p->d; a.dv = p->dv; a.chunk = p->chunk;
     a.Hkv = p->Hkv > 0 ? p->Hkv : p->H;
@@ -240,6 +245,7 @@ hla_status hla_backward_chunked_traced(const hla_params *p, const void *q, const
     a.events = reinterpret_cast<cudaEvent_t const *>(phase_events);
     cudaError_t e = status_ptr(&a.err);
     if (e != cudaSuccess) return cuda_fail(e, "status word");
+    if (norm) return hla::bwd_norm_launch(*p, a, workspace, static_cast<cudaStream_t>(stream));
     e = hla::bwd_simt_launch(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return HLA_OK;

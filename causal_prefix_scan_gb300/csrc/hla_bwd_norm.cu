@@ -1,0 +1,226 @@
+// hla_bwd_norm.cu -- backward pass through the ratio normalisation
+// o_t = n_t / (den_t + eps) ("Higher-order Linear Attention", gist.science summary,
+// section 1, bullet "Normalisatie"), composed from the unnormalised kernels.
+//
+// The denominator den_t = q_t^T (S_t m_t - h_t) is the masked output with every value
+// equal to one, so the normalised output is the unnormalised one of the augmented values
+// [V | 1] followed by a division.  With r_t = 1 / (den_t + eps), the gradient is that of
+// the unnormalised forward of [V | 1] with upstream [r_t g_t | -r_t (g_t . o_t)]:
+//   1. n = forward(q, k, V) and den = forward(q, k, E) (E: a one in column 0 of a
+//      16-wide value tile), both unnormalised;
+//   2. gn = r g, g1 = [-r (g . n r), 0, ...] (one elementwise kernel);
+//   3. (dq, dk, dv) = backward(q, k, V, gn), (dq1, dk1, -) = backward(q, k, E, g1);
+//   4. dq += dq1, dk += dk1.
+// The two parts of dq and dk cancel to a large degree (with positive features and
+// zero-mean values the parts of dk are several times the sum), so every intermediate
+// stays in fp32: bf16 inputs are widened once and the whole chain runs on the fp32
+// CUDA-core kernels; rounding n, den, the upstream gradients or the partial results to
+// bf16 costs several per cent of the result.
+#include <cstdint>
+#include <cstdio>
+
+#include "hla_internal.h"
+
+namespace hla {
+namespace {
+
+constexpr int kEwThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ float ldx(const T *p, size_t i);
+template <>
+__device__ __forceinline__ float ldx<float>(const float *p, size_t i) { return p[i]; }
+template <>
+__device__ __forceinline__ float ldx<__nv_bfloat16>(const __nv_bfloat16 *p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+template <typename T>
+__device__ __forceinline__ void stx(T *p, size_t i, float x);
+template <>
+__device__ __forceinline__ void stx<float>(float *p, size_t i, float x) { p[i] = x; }
+template <>
+__device__ __forceinline__ void stx<__nv_bfloat16>(__nv_bfloat16 *p, size_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+// E: [rows][w1] with a one in column 0.
+__global__ void __launch_bounds__(kEwThreads) unit_value_kernel(float *e, size_t rows, int w1) {
+    for (size_t i = (size_t)blockIdx.x * kEwThreads + threadIdx.x; i < rows * w1; i += (size_t)gridDim.x * kEwThreads)
+        e[i] = (i % w1) == 0 ? 1.f : 0.f;
+}
+
+// One token row per warp: gn = r g, g1[., 0] = -r (g . n) r, other columns 0.
+__global__ void __launch_bounds__(kEwThreads) norm_upstream_kernel(const float *num, const float *den1, const float *g,
+                                                                    float *gn, float *g1, size_t rows, int dv, int w1,
+                                                                    float eps) {
+    const int lane = threadIdx.x & 31;
+    for (size_t r = ((size_t)blockIdx.x * kEwThreads + threadIdx.x) / 32; r < rows;
+         r += (size_t)gridDim.x * kEwThreads / 32) {
+        const float rr = 1.f / (den1[r * w1] + eps);
+        float dot = 0.f;
+        for (int j = lane; j < dv; j += 32) {
+            const float gj = g[r * dv + j];
+            dot = fmaf(gj, num[r * dv + j], dot);
+            gn[r * dv + j] = rr * gj;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        for (int j = lane; j < w1; j += 32) g1[r * w1 + j] = j == 0 ? -rr * rr * dot : 0.f;
+    }
+}
+
+template <typename Ti>
+__global__ void __launch_bounds__(kEwThreads) widen_kernel(float *dst, const Ti *src, size_t count) {
+    for (size_t i = (size_t)blockIdx.x * kEwThreads + threadIdx.x; i < count; i += (size_t)gridDim.x * kEwThreads)
+        dst[i] = ldx(src, i);
+}
+
+// dst = a + b (b NULL: dst = a), rounded once to the output type; dst may alias a.
+template <typename To>
+__global__ void __launch_bounds__(kEwThreads) sum_kernel(To *dst, const float *a, const float *b, size_t count) {
+    for (size_t i = (size_t)blockIdx.x * kEwThreads + threadIdx.x; i < count; i += (size_t)gridDim.x * kEwThreads)
+        stx(dst, i, b ? a[i] + b[i] : a[i]);
+}
+
+int grid_for(size_t work) {
+    const size_t b = (work + kEwThreads - 1) / kEwThreads;
+    return (int)(b < 8192 ? (b > 0 ? b : 1) : 8192);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+hla_status cuda_err(cudaError_t e, const char *where) {
+    char msg[192];
+    snprintf(msg, sizeof msg, "normalised backward, %s: %s", where, cudaGetErrorString(e));
+    return report(HLA_ERR_CUDA, msg);
+}
+
+constexpr int kUnitWidth = 16;
+
+// The unnormalised fp32 problem of width dv.
+hla_params unnormalised(const hla_params &p, int dv) {
+    hla_params q = p;
+    q.flags &= ~(unsigned)HLA_NORMALIZE;
+    q.in_dtype = HLA_F32;
+    q.dv = dv;
+    q.eps = 0.f;
+    return q;
+}
+
+}  // namespace
+
+NormLayout bwd_norm_layout(const hla_params &p) {
+    NormLayout L;
+    const int hkv = p.Hkv > 0 ? p.Hkv : p.H;
+    const size_t rq = (size_t)p.B * p.H * p.n, rkv = (size_t)p.B * hkv * p.n;
+    const int w1 = kUnitWidth;
+    const hla_params pv = unnormalised(p, p.dv), pe = unnormalised(p, w1);
+    const size_t fws = hla_forward_workspace_size(&pv), fws1 = hla_forward_workspace_size(&pe);
+    const size_t bws = bwd_simt_workspace(pv), bws1 = bwd_simt_workspace(pe);
+    const bool wide = p.in_dtype != HLA_F32;
+    size_t o = 0;
+    auto take = [&](size_t floats) { const size_t at = o; o = align256(o + floats * 4); return at; };
+    L.w1 = w1;
+    L.fwd_ws_bytes = fws > fws1 ? fws : fws1;
+    L.fwd_ws = take((L.fwd_ws_bytes + 3) / 4);
+    L.num = take(rq * p.dv);
+    L.den1 = take(rq * w1);
+    L.unit = take(rkv * w1);
+    L.gn = take(rq * p.dv);
+    L.g1 = take(rq * w1);
+    L.dq1 = take(rq * p.d);
+    L.dk1 = take(rkv * p.d);
+    L.dv1 = take(rkv * w1);
+    L.bwd_ws = take(((bws > bws1 ? bws : bws1) + 3) / 4);
+    // bf16 inputs: fp32 copies of q, k, v, g and fp32 results before the final rounding
+    L.q32 = wide ? take(rq * p.d) : 0;
+    L.k32 = wide ? take(rkv * p.d) : 0;
+    L.v32 = wide ? take(rkv * p.dv) : 0;
+    L.g32 = wide ? take(rq * p.dv) : 0;
+    L.dq32 = wide ? take(rq * p.d) : 0;
+    L.dk32 = wide ? take(rkv * p.d) : 0;
+    L.dv32 = wide ? take(rkv * p.dv) : 0;
+    L.total = o;
+    return L;
+}
+
+hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a0, void *workspace, cudaStream_t st) {
+    const NormLayout L = bwd_norm_layout(p);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    auto f = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
+    const int hkv = p.Hkv > 0 ? p.Hkv : p.H;
+    const size_t rq = (size_t)p.B * p.H * p.n, rkv = (size_t)p.B * hkv * p.n;
+    const bool wide = p.in_dtype != HLA_F32;
+    auto mark = [&](int i) { return a0.events ? cudaEventRecord(a0.events[i], st) : cudaSuccess; };
+    cudaError_t e;
+    if ((e = mark(0)) != cudaSuccess) return cuda_err(e, "event");
+    // fp32 operands
+    const float *q = static_cast<const float *>(a0.q), *k = static_cast<const float *>(a0.k);
+    const float *v = static_cast<const float *>(a0.v), *g = static_cast<const float *>(a0.go);
+    float *dq = static_cast<float *>(a0.grad_q), *dk = static_cast<float *>(a0.grad_k);
+    float *dv = static_cast<float *>(a0.grad_v);
+    if (wide) {
+        const __nv_bfloat16 *src[4] = {static_cast<const __nv_bfloat16 *>(a0.q), static_cast<const __nv_bfloat16 *>(a0.k),
+                                       static_cast<const __nv_bfloat16 *>(a0.v),
+                                       static_cast<const __nv_bfloat16 *>(a0.go)};
+        float *dst[4] = {f(L.q32), f(L.k32), f(L.v32), f(L.g32)};
+        const size_t cnt[4] = {rq * p.d, rkv * p.d, rkv * p.dv, rq * p.dv};
+        for (int i = 0; i < 4; ++i)
+            widen_kernel<__nv_bfloat16><<<grid_for(cnt[i]), kEwThreads, 0, st>>>(dst[i], src[i], cnt[i]);
+        q = dst[0]; k = dst[1]; v = dst[2]; g = dst[3];
+        dq = f(L.dq32); dk = f(L.dk32); dv = f(L.dv32);
+    }
+    // 1. numerator and denominator (unnormalised forwards)
+    if (L.fwd_ws_bytes && (e = cudaMemsetAsync(ws + L.fwd_ws, 0, L.fwd_ws_bytes, st)) != cudaSuccess)
+        return cuda_err(e, "workspace clear");
+    unit_value_kernel<<<grid_for(rkv * L.w1), kEwThreads, 0, st>>>(f(L.unit), rkv, L.w1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_err(e, "operands");
+    const hla_params pv = unnormalised(p, p.dv), pe = unnormalised(p, L.w1);
+    hla_status s = hla_forward_chunked(&pv, q, k, v, f(L.num), nullptr, nullptr, ws + L.fwd_ws, L.fwd_ws_bytes, st);
+    if (s != HLA_OK) return s;
+    s = hla_forward_chunked(&pe, q, k, f(L.unit), f(L.den1), nullptr, nullptr, ws + L.fwd_ws, L.fwd_ws_bytes, st);
+    if (s != HLA_OK) return s;
+    // 2. upstream gradients of the augmented problem
+    norm_upstream_kernel<<<grid_for(rq * 32), kEwThreads, 0, st>>>(f(L.num), f(L.den1), g, f(L.gn), f(L.g1), rq,
+                                                                    p.dv, L.w1, p.eps);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_err(e, "upstream gradients");
+    if ((e = mark(1)) != cudaSuccess) return cuda_err(e, "event");
+    // 3. the two unnormalised backward passes
+    BwdArgs a = a0;
+    a.in_dtype = HLA_F32;
+    a.events = nullptr;
+    a.q = q; a.k = k; a.v = v; a.go = f(L.gn);
+    a.grad_q = dq; a.grad_k = dk; a.grad_v = dv;
+    a.workspace = f(L.bwd_ws);
+    a.dk_pair = a.Hkv < a.H ? a.workspace + bwd_pair_offset(pv) : nullptr;
+    a.dv_pair = a.dk_pair ? a.dk_pair + rq * p.d : nullptr;
+    if ((e = bwd_simt_launch(a, st)) != cudaSuccess) return cuda_err(e, "backward of the numerator");
+    if ((e = mark(2)) != cudaSuccess) return cuda_err(e, "event");
+    BwdArgs b = a;
+    b.dv = L.w1;
+    b.v = f(L.unit);
+    b.go = f(L.g1);
+    b.grad_q = f(L.dq1);
+    b.grad_k = f(L.dk1);
+    b.grad_v = f(L.dv1);
+    b.dk_pair = b.Hkv < b.H ? b.workspace + bwd_pair_offset(pe) : nullptr;
+    b.dv_pair = b.dk_pair ? b.dk_pair + rq * p.d : nullptr;
+    if ((e = bwd_simt_launch(b, st)) != cudaSuccess) return cuda_err(e, "backward of the denominator");
+    // 4. dq = dq + dq1, dk = dk + dk1 (and dv), each rounded once to the output type
+    if (wide) {
+        sum_kernel<__nv_bfloat16><<<grid_for(rq * p.d), kEwThreads, 0, st>>>(
+            static_cast<__nv_bfloat16 *>(a0.grad_q), dq, f(L.dq1), rq * p.d);
+        sum_kernel<__nv_bfloat16><<<grid_for(rkv * p.d), kEwThreads, 0, st>>>(
+            static_cast<__nv_bfloat16 *>(a0.grad_k), dk, f(L.dk1), rkv * p.d);
+        sum_kernel<__nv_bfloat16><<<grid_for(rkv * p.dv), kEwThreads, 0, st>>>(
+            static_cast<__nv_bfloat16 *>(a0.grad_v), dv, nullptr, rkv * p.dv);
+    } else {
+        sum_kernel<float><<<grid_for(rq * p.d), kEwThreads, 0, st>>>(dq, dq, f(L.dq1), rq * p.d);
+        sum_kernel<float><<<grid_for(rkv * p.d), kEwThreads, 0, st>>>(dk, dk, f(L.dk1), rkv * p.d);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_err(e, "gradient sums");
+    if ((e = mark(3)) != cudaSuccess) return cuda_err(e, "event");
+    return HLA_OK;
+}
+
+}  // namespace hla

@@ -85,6 +85,18 @@ size_t bwd_simt_workspace(const hla_params &p);
 size_t bwd_pair_offset(const hla_params &p);  // floats before the per-query-head dk, dv
 cudaError_t bwd_simt_launch(const BwdArgs &a, cudaStream_t st);
 
+// Backward through the ratio normalisation: two unnormalised fp32 forwards (values and
+// a unit-value tile), the augmented upstream gradients, two unnormalised fp32 backwards
+// and a sum of their dq, dk.  Byte offsets into the caller's workspace (256-byte
+// aligned); the *32 buffers exist for bf16 inputs only.
+struct NormLayout {
+    int w1;  // width of the unit-value tile
+    size_t fwd_ws, fwd_ws_bytes, num, den1, unit, gn, g1, dq1, dk1, dv1, bwd_ws;
+    size_t q32, k32, v32, g32, dq32, dk32, dv32, total;
+};
+NormLayout bwd_norm_layout(const hla_params &p);
+hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a, void *workspace, cudaStream_t st);
+
 struct Fwd3Args {
     int B, H, n, d, dv, chunk;
     hla_dtype in_dtype;

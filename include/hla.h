@@ -190,24 +190,35 @@ HLA_API hla_status hla_decode_step(int N, int H, int Hkv, int d, int dv, hla_dty
                            void *stream);
 
 /*
- * Backward pass (training) of the masked forward with zero initial state and no
- * normalisation.  The pages motivate chunk-parallel training (section 4) but give
- * no gradient; this call is reverse-mode differentiation of the section 1
- * recurrence, evaluated chunk-parallel: per-chunk local sums, a scan over chunks
- * (the states S, X = S C - G forward in time and the adjoints dL/dX, dL/dS
- * backward in time), then per-chunk gradients.  Its result equals the gradient
- * of sum_t dout_t . o_t up to floating-point rounding.
+ * Backward pass (training) of the masked forward with zero initial state.  The
+ * pages motivate chunk-parallel training (section 4) but give no gradient; this
+ * call is reverse-mode differentiation of the section 1 recurrence, evaluated
+ * chunk-parallel: per-chunk local sums, a scan over chunks (the states S,
+ * X = S C - G forward in time and the adjoints dL/dX, dL/dS backward in time),
+ * then per-chunk gradients.  Its result equals the gradient of sum_t dout_t . o_t
+ * up to floating-point rounding.
  *
- *   p      as for hla_forward_chunked; supported: flags 0 or HLA_DECAY only
- *          (others HLA_ERR_UNSUPPORTED), Hkv dividing H (0 means H), d, dv, chunk in
- *          {16,32,64}, in_dtype HLA_F32 or HLA_BF16 (fp32 arithmetic either way);
+ * With HLA_NORMALIZE the output is o_t = n_t / (den_t + eps), den_t = q_t^T
+ * (S_t m_t - h_t) (section 1, "Normalisatie").  den is the unnormalised output of
+ * unit values, so the gradient is that of the unnormalised output of the values
+ * [V | 1] with upstream [r dout | -r (dout . o)], r = 1 / (den + eps): two
+ * unnormalised forwards, an elementwise kernel, two unnormalised backwards and a
+ * sum.  The two parts of dq and dk cancel to a large degree, so this chain runs in
+ * fp32 throughout (bf16 inputs are widened first) on the CUDA-core kernels.
+ *
+ *   p      as for hla_forward_chunked; supported: flags 0, HLA_DECAY, HLA_NORMALIZE
+ *          (eps >= 0) or both (HLA_UNMASKED, HLA_ASYMMETRIC: HLA_ERR_UNSUPPORTED),
+ *          Hkv dividing H (0 means H), d, dv, chunk in {16,32,64}, in_dtype
+ *          HLA_F32 or HLA_BF16 (fp32 arithmetic either way);
  *   q      [B][H][n][d], k [B][Hkv][n][d], v [B][Hkv][n][dv], dout [B][H][n][dv],
  *          in_dtype, read only (query head h reads key/value head h / (H / Hkv));
  *   dq     [B][H][n][d], dk [B][Hkv][n][d], dv [B][Hkv][n][dv], in_dtype, written (not
  *          accumulated); with Hkv < H, dk and dv are the sums over each group;
  *   workspace device scratch of at least hla_backward_workspace_size(p) bytes,
- *          16-byte aligned, no initial contents needed.
- * All tensor pointers 16-byte aligned.  Three kernel launches on `stream`.
+ *          16-byte aligned (256-byte aligned with HLA_NORMALIZE), no initial
+ *          contents needed.
+ * All tensor pointers 16-byte aligned.  Without HLA_NORMALIZE three kernel phases
+ * on `stream` (plus the group sums when Hkv < H); with it, the chain above.
  */
 HLA_API size_t hla_backward_workspace_size(const hla_params *p);
 HLA_API hla_status hla_backward_chunked(const hla_params *p, const void *q, const void *k, const void *v,
@@ -217,8 +228,10 @@ HLA_API hla_status hla_backward_chunked(const hla_params *p, const void *q, cons
 /* hla_backward_chunked with per-phase tracing: phase_events is NULL (then this is
  * hla_backward_chunked) or four cudaEvent_t handles of the current device, recorded
  * on `stream` before the local-sums kernel, after it, after the scan kernel and
- * after the gradient kernel.  The caller owns the events (created with timing
- * enabled to read elapsed times).  With n == 0 no event is recorded. */
+ * after the gradient kernel.  With HLA_NORMALIZE: at the start, after the two
+ * forwards and the upstream-gradient kernel, after the first backward and at the
+ * end.  The caller owns the events (created with timing enabled to read elapsed
+ * times).  With n == 0 no event is recorded. */
 HLA_API hla_status hla_backward_chunked_traced(const hla_params *p, const void *q, const void *k, const void *v,
                                                const void *dout, void *dq, void *dk, void *dv, void *workspace,
                                                size_t workspace_bytes, void *stream, void *const *phase_events);

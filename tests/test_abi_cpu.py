@@ -136,7 +136,8 @@ def _bcall(p, ptrs=(16,) * 7, ws=16, ws_bytes=1 << 40):
     (dict(n=-1), hla.HLA_ERR_ARG),
     (dict(flags=16), hla.HLA_ERR_ARG),
     (dict(flags=hla.HLA_DECAY), hla.HLA_ERR_ARG),            # decay without gamma
-    (dict(flags=hla.HLA_NORMALIZE), hla.HLA_ERR_UNSUPPORTED),
+    (dict(flags=hla.HLA_NORMALIZE, eps=-1.0), hla.HLA_ERR_ARG),
+    (dict(flags=hla.HLA_NORMALIZE, d=128), hla.HLA_ERR_UNSUPPORTED),
     (dict(flags=hla.HLA_UNMASKED), hla.HLA_ERR_UNSUPPORTED),
     (dict(flags=hla.HLA_ASYMMETRIC), hla.HLA_ERR_UNSUPPORTED),
     (dict(H=6, Hkv=4), hla.HLA_ERR_ARG),
@@ -177,6 +178,25 @@ def test_backward_workspace_size_and_empty_sequence(lib):
                                                    in_dtype=hla.HLA_F32)) == base + B * H * n * (d + dv) * 4
     # no tokens: nothing to compute, no pointer needed
     assert _bcall(_params(n=0), ptrs=(None,) * 7, ws=None, ws_bytes=0) == hla.HLA_OK
+    assert _bcall(_params(n=0, flags=hla.HLA_NORMALIZE), ptrs=(None,) * 7, ws=None, ws_bytes=0) == hla.HLA_OK
+
+
+def test_backward_normalised_workspace(lib):
+    # two unnormalised fp32 backwards and forwards share the scratch: at least the
+    # backward workspace plus the fp32 outputs of both forwards and the upstream gradients
+    for dt in (hla.HLA_F32, hla.HLA_BF16):
+        B, H, n, d, dv, c = 2, 3, 100, 32, 16, 32
+        plain = hla.hla_backward_workspace_size(_params(B=B, H=H, n=n, d=d, dv=dv, chunk=c, in_dtype=dt))
+        norm = hla.hla_backward_workspace_size(_params(B=B, H=H, n=n, d=d, dv=dv, chunk=c, in_dtype=dt,
+                                                       flags=hla.HLA_NORMALIZE, eps=1e-3))
+        rows = B * H * n
+        assert norm >= plain + rows * 4 * (2 * dv + 3 * 16 + 2 * d)
+        assert norm % 256 == 0
+    assert hla.hla_backward_workspace_size(_params(n=0, flags=hla.HLA_NORMALIZE)) == 0
+    # the scratch must be 256-byte aligned with HLA_NORMALIZE
+    p = _params(flags=hla.HLA_NORMALIZE, eps=1e-3)
+    assert _bcall(p, ws=16) == hla.HLA_ERR_ARG
+    assert "256" in hla.hla_last_error()
 
 
 def test_backward_traced_rejects_missing_events(lib):

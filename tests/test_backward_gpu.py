@@ -21,18 +21,21 @@ def small(**kw):
     return W.Workload("bwd", **base)
 
 
-def run_backward(x, g, dtype, chunk):
+def run_backward(x, g, dtype, chunk, eps=None):
     q, k, v = (to_dev(x[n], dtype) for n in ("q", "k", "v"))
     dout = to_dev(g, dtype)
     gam = None if x.get("gamma") is None else torch.from_numpy(np.asarray(x["gamma"], np.float32)).cuda()
-    dq, dk, dv = hla.backward(q, k, v, dout, chunk=chunk, gamma=gam)
+    dq, dk, dv = hla.backward(q, k, v, dout, chunk=chunk, gamma=gam, normalize=eps is not None,
+                              eps=0.0 if eps is None else eps)
     hla.hla_sync_status()
     return tuple(t.float().cpu().numpy() for t in (dq, dk, dv))
 
 
-def run_oracle(x, g):
+def run_oracle(x, g, eps=None):
     gam = None if x.get("gamma") is None else np.asarray(x["gamma"], np.float64)
-    return oracle.backward(x["q"], x["k"], x["v"], g, gam)
+    if eps is None:
+        return oracle.backward(x["q"], x["k"], x["v"], g, gam)
+    return oracle.backward(x["q"], x["k"], x["v"], g, gam, normalize=True, eps=eps)
 
 
 def check(got, ref, tol, what):
@@ -146,3 +149,53 @@ def test_backward_shared_kv_heads(d, dv, chunk, dtype, Hkv):
     g = W.make_dout(w)
     check(run_backward(x, g, dtype, chunk), run_oracle(x, g), TOL_F32 if dtype == "f32" else TOL_BF16,
           f"bwd {dtype} H4 Hkv{Hkv}")
+
+
+@pytest.mark.parametrize("d,dv,chunk,n,dtype", [(64, 64, 64, 64 * 3 + 17, "bf16"), (32, 16, 32, 100, "f32"),
+                                                (16, 32, 16, 45, "bf16"), (64, 32, 64, 70, "f32")])
+@pytest.mark.parametrize("decay", [False, True])
+def test_backward_normalised(d, dv, chunk, n, dtype, decay):
+    """Gradient through o = n / (den + eps) with positive features (den > 0)."""
+    w = small(B=2, H=2, n=n, d=d, dv=dv, chunk=chunk, decay=decay, dtype=dtype, qk="elu1", seed=41)
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    check(run_backward(x, g, dtype, chunk, eps=1e-3), run_oracle(x, g, eps=1e-3),
+          TOL_F32 if dtype == "f32" else TOL_BF16, f"bwd norm {dtype} d{d} dv{dv} c{chunk} n{n} decay={decay}")
+
+
+@pytest.mark.parametrize("d,dv,chunk,dtype", [(64, 64, 64, "bf16"), (32, 16, 32, "f32")])
+def test_backward_normalised_shared_kv_heads(d, dv, chunk, dtype):
+    w = small(B=1, H=4, Hkv=2, n=2 * chunk + 5, d=d, dv=dv, chunk=chunk, decay=True, dtype=dtype, qk="elu1",
+              seed=42)
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    check(run_backward(x, g, dtype, chunk, eps=0.5), run_oracle(x, g, eps=0.5),
+          TOL_F32 if dtype == "f32" else TOL_BF16, f"bwd norm {dtype} H4 Hkv2")
+
+
+def test_backward_normalised_is_gradient_of_forward():
+    """The normalised backward against central differences of the library's own
+    normalised fp32 forward along a random direction.  Along the line the output is a
+    rational function of s; with directions of scale 0.1 the seven-point stencil's
+    O(s^6) truncation error is below 1e-10 relative at s = 0.1 (fp64 check of the same
+    case), so the fp32 rounding of the forward sets the tolerance."""
+    w = small(n=70, d=16, dv=16, chunk=16, dtype="f32", decay=True, qk="elu1", seed=43)
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    rng = np.random.default_rng(6)
+    dirs = [0.1 * rng.standard_normal(x[n].shape).astype(np.float32) for n in ("q", "k", "v")]
+    dq, dk, dv = run_backward(x, g, "f32", 16, eps=1e-3)
+    want = sum(float(np.sum(a.astype(np.float64) * e)) for a, e in zip((dq, dk, dv), dirs))
+    gam = torch.from_numpy(x["gamma"]).cuda()
+    gd = to_dev(g, "f32").double()
+
+    def f(s):
+        q, k, v = (to_dev(x[n] + s * e, "f32") for n, e in zip(("q", "k", "v"), dirs))
+        o = hla.forward(q, k, v, chunk=16, gamma=gam, normalize=True, eps=1e-3)
+        hla.hla_sync_status()
+        return float((o.double() * gd).sum())
+
+    s = 0.1
+    F = {j: f(j * s) for j in (-3, -2, -1, 1, 2, 3)}
+    fd = (45 * (F[1] - F[-1]) - 9 * (F[2] - F[-2]) + (F[3] - F[-3])) / (60 * s)
+    assert abs(fd - want) <= 2e-3 * abs(want), (fd, want)
