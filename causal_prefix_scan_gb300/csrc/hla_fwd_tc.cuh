@@ -198,8 +198,8 @@ struct Kern {
     __device__ __forceinline__ float *rsum() const { return vec() + 2 * D; }      // pass 2: [NP_C x C]
     __device__ __forceinline__ float *den() const { return vec() + 2 * D + K_::NP_C * C; }  // pass 2: [C]
     __device__ __forceinline__ float *g16() const { return vec() + 2 * D + K_::R1; }  // g^j, g^{2j}
-    uint64_t *tma_bar, *mma_bar, *mma_bar2;
-    uint32_t tb, tph, mph, mph2;
+    uint64_t *tma_bar, *mma_bar, *mma_bar2, *mma_bar3;
+    uint32_t tb, tph, mph, mph2, mph3;
     int tid, warp, lane, quad, half;
     int rowC, rowD;  // rows this thread owns in token-row / state accumulators (-1: none)
     int bh;
@@ -239,6 +239,19 @@ struct Kern {
     }
     __device__ void commit2() {
         if (tid == 0) umma_commit(mma_bar2);
+    }
+    // Third barrier, three arrivals: independent products issued by the lane-0
+    // threads of warps 1-3 (or 0-2), each committing its own MMAs to it, so that
+    // their issue overlaps instead of queueing behind one thread.
+    static constexpr uint32_t kFan = 3;
+    __device__ bool wait_mma3() {
+        bool ok = mbar_wait(mma_bar3, mph3, P.err);
+        mph3 ^= 1u;
+        tc_fence_after();
+        return !__syncthreads_or(!ok);
+    }
+    __device__ void arrive3() {  // an arrival with no MMAs behind it
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(mma_bar3)) : "memory");
     }
     // Block barrier that also orders this thread's TMEM accesses around it.
     __device__ void tc_sync() {
@@ -714,13 +727,17 @@ struct Kern {
             publish();
             if (tid == 0) {
                 mma_mm<D>(TS, Kt, DECAY ? tA() : Kt, !first);  // S += K^T W K
-                mma_mm<DV>(TX, tU(), V, !first);               // X += (W^2 U)^T V
-                mma_mm<DV>(T4, Q, DECAY ? tS() : V, !first);   // C += Q^T W V
+                umma_commit(mma_bar3);
+            } else if (tid == 32) {
+                mma_mm<DV>(TX, tU(), V, !first);  // X += (W^2 U)^T V
+                umma_commit(mma_bar3);
+            } else if (tid == 64) {
+                mma_mm<DV>(T4, Q, DECAY ? tS() : V, !first);  // C += Q^T W V
+                umma_commit(mma_bar3);
             }
-            commit();
             if (need_mY)  // overlaps the MMAs; scratch: tQ is free once Q S_p has run
                 tile_colsums<true>(Q, tU(), L, gp(rest), reinterpret_cast<float *>(tQ()), mrun(), 1.f, Yrun(), 1.f);
-            if (!wait_mma()) return false;
+            if (!wait_mma3()) return false;
             stage ^= (K_::NSTAGE - 1);
         }
         return true;
@@ -1237,16 +1254,25 @@ struct Kern {
             if constexpr (DECAY)
                 scaled_tile_copy<D>(Kt, tA(), [&](int r) { return r < L ? gp(L - 1 - r) : 0.f; });
             publish();
+            // M = Q U^T and, with decay, S += K^T W K (it reads tA(), which the M
+            // epilogue rewrites) on the first barrier; the other products fan out
             if (tid == 0) {
-                mma_kk<C, D>(TW, Q, tU(), false);             // M = Q U^T
-                mma_mm<D>(TS, Kt, DECAY ? tA() : Kt, true);   // S += K^T W K (reads tA(): done before
-            }                                                // the M epilogue rewrites tA())
-            commit();
-            if (tid == 0) {
+                mma_kk<C, D>(TW, Q, tU(), false);                        // M = Q U^T
+                if constexpr (DECAY) mma_mm<D>(TS, Kt, tA(), true);       // S += K^T W K
+                umma_commit(mma_bar);
+            } else if (tid == 32) {
+                if constexpr (DECAY) arrive3();
+                else {
+                    mma_mm<D>(TS, Kt, Kt, true);  // S += K^T K
+                    umma_commit(mma_bar3);
+                }
+            } else if (tid == 64) {
                 mma_mm<DV>(TX, DECAY ? tS() : tU(), V, true);  // X += (W^2 U)^T V
-                mma_km<DV, D>(T4, Q, tQ(), false);            // spare = Q X_p
+                umma_commit(mma_bar3);
+            } else if (tid == 96) {
+                mma_km<DV, D>(T4, Q, tQ(), false);  // spare = Q X_p
+                umma_commit(mma_bar3);
             }
-            commit2();
             // Y <- g^{2L} Y + sum_b w_b^2 u_b (weights already on the tile)
             float ay = 0.f;
             float *ysc = rsum();  // rsum is free until the M epilogue
@@ -1261,7 +1287,7 @@ struct Kern {
                     for (int b = g; b < L; b += 2) ay += tile_load(tS(), C, b, i);
                 if (g == 1) ysc[i] = ay;
             }
-            if (!wait_mma()) return false;  // M and the S update
+            if (!wait_mma()) return false;  // M (and the S update with decay)
             if constexpr (NORM && DECAY) {
                 if (tid < D) Yrun()[tid] = gp(2 * L) * Yrun()[tid] + (ay + ysc[tid]);
                 __syncthreads();  // rsum is rewritten by the M epilogue
@@ -1285,7 +1311,7 @@ struct Kern {
             publish();
             if (tid == 0) mma_km<DV, C>(TW, tA(), V, false);  // O = M V
             commit();
-            if (!wait_mma2()) return false;  // X, S updates and Q X_p
+            if (!wait_mma3()) return false;  // X, S updates and Q X_p
             if (!wait_mma()) return false;   // M V
             // Q, K, V of this chunk are no longer read: with one input stage, start the
             // next chunk's load now so that it overlaps the output epilogue
@@ -1955,7 +1981,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
     x.tma_bar = &bars[0];  // [0], [1]: input stages
     x.mma_bar = &bars[2];
     x.mma_bar2 = &bars[3];
-    x.tph = x.mph = x.mph2 = 0;
+    x.mma_bar3 = reinterpret_cast<uint64_t *>(base + K_::OFF_BAR + 48);
+    x.tph = x.mph = x.mph2 = x.mph3 = 0;
 
     if (x.tid == 0) {
         *misalign_p = (smem_u32(base) & 1023u) != 0;
@@ -1963,6 +1990,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
         mbar_init(&bars[1], 1);
         mbar_init(&bars[2], 1);
         mbar_init(&bars[3], 1);
+        mbar_init(x.mma_bar3, decltype(x)::kFan);
         fence_mbar_init();
         tma_prefetch_desc(&P.tmQ);
         tma_prefetch_desc(&P.tmK);
