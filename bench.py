@@ -18,6 +18,7 @@ run N independent replicas ("replicas only"); value = tokens of all ranks / max 
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -53,6 +54,8 @@ FWD3_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fw
 FWD3_METRIC = "masked 3rd-order HLA forward tokens/s and % roofline on 1 GB300"
 FWD3_DISPATCH_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd3_simt.cu")
 FWD3_TC_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd3_tc.cu")
+BWD_NORM_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_bwd_norm.cu")
+NORM_UNIT_WIDTH = 16  # width of the unit-value tile of the normalised backward
 BWD_TC_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_bwd_tc.cu")
 SCAN_TC_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_scan_tc.cu")
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz (maximum SM clock)
@@ -267,13 +270,14 @@ def cpu_baseline_forward(w: W.Workload, x):
                       f"of the same inputs, threads over (b,h); mean of {reps} run(s)", "seconds": secs}
 
 
-def oracle_bwd_rate(x, g, batch_rows: int, n_tokens: int, nthreads: int):
+def oracle_bwd_rate(x, g, batch_rows: int, n_tokens: int, nthreads: int, w: W.Workload | None = None):
     import oracle
     sl = lambda a: np.ascontiguousarray(a[:batch_rows, :, :n_tokens], dtype=np.float64)
     gam = None if x["gamma"] is None else np.asarray(x["gamma"], np.float64)
+    norm = dict(normalize=True, eps=w.eps) if w is not None and w.normalize else {}
     oracle.build()
     t0 = time.perf_counter()
-    oracle.backward(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(g), gam, nthreads=nthreads)
+    oracle.backward(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(g), gam, nthreads=nthreads, **norm)
     return time.perf_counter() - t0, batch_rows * n_tokens
 
 
@@ -283,10 +287,10 @@ def cpu_baseline_backward(w: W.Workload, x, g):
     cores = cpu_threads()
     rows = max(1, min(w.B, -(-cores // w.H)))
     used = min(cores, rows * w.H)
-    secs, toks = oracle_bwd_rate(x, g, rows, w.n, used)
+    secs, toks = oracle_bwd_rate(x, g, rows, w.n, used, w)
     reps = max(1, min(500, int(10.0 / max(secs, 1e-9))))
     if reps > 1:
-        secs = (secs + sum(oracle_bwd_rate(x, g, rows, w.n, used)[0] for _ in range(reps - 1))) / reps
+        secs = (secs + sum(oracle_bwd_rate(x, g, rows, w.n, used, w)[0] for _ in range(reps - 1))) / reps
     return {"value": toks / secs, "unit": "tokens/s", "cores": used, "kind": "oracle",
             "sample": f"fp64 reverse-mode recurrence over {rows} of {w.B} batch row(s) x {w.H} heads x {w.n} "
                       f"tokens of the same inputs, threads over (b,h); mean of {reps} run(s)", "seconds": secs}
@@ -539,6 +543,31 @@ def is_third(w) -> bool:
     return isinstance(w, W.Workload) and w.name.startswith("fwd3_")
 
 
+def launches_per_step(w: W.Workload) -> int:
+    """Kernels of one library call: three for the backward or third order (four, the
+    tensor-core scans counted as their own launches, are reported per phase); the
+    normalised backward adds the input widening (bf16), the unit values, two forwards,
+    the upstream gradients, a second backward and the sums."""
+    if not (is_backward(w) and w.normalize):
+        return 3
+    bf = w.dtype == "bf16"
+    split = norm_segments(w) > 1  # two forwards and a segment scan per part instead of one forward
+    forwards = (4 + 2 + (1 if w.decay else 0)) if split else 2
+    return (4 if bf else 0) + 1 + forwards + 1 + 3 + 3 + (3 if bf else 2)
+
+
+def norm_segments(w: W.Workload) -> int:
+    """Segments per sequence of the normalised backward's fp32 forwards: the library's
+    rule (a power of two up to 16 dividing n into pieces of at least one chunk, with
+    B H P at most 608; 1 with shared key/value heads)."""
+    if w.kv_heads != w.H:
+        return 1
+    P = 1
+    while P < 16 and w.n % (2 * P) == 0 and w.n // (2 * P) >= w.chunk and w.B * w.H * 2 * P <= 4 * 152:
+        P *= 2
+    return P
+
+
 def bench_phased(args, w: W.Workload, rank, world, local, dist):
     """The backward pass or the third-order forward: a step is one library call
     (three kernels: local sums, scan over chunks, per-chunk results) over the whole
@@ -570,7 +599,19 @@ def bench_phased(args, w: W.Workload, rank, world, local, dist):
         outs = (torch.empty_like(ins[0]), torch.empty_like(ins[1]), torch.empty_like(ins[2])) if bwd else \
             (torch.empty(ins[0].shape[:3] + (w.dv,), dtype=tdt, device=dev),)
         sets.append((ins, outs))
-    if bwd:
+    if bwd and w.normalize:
+        # two fp32 forwards and the upstream-gradient kernel, the backward of the values,
+        # the backward of the unit column and the gradient sums (all fp32, CUDA cores)
+        params = hla.make_params(sets[0][0][0], sets[0][0][2], w.chunk, gamma, True, w.eps)
+        ws_bytes = hla.hla_backward_workspace_size(params)
+        names = ("norm_forwards_upstream", "norm_bwd_values", "norm_bwd_unit_sums")
+        w1 = dataclasses.replace(w, dv=NORM_UNIT_WIDTH)
+        fl = dict(zip(names, (alg_flops_per_token_head(w) + alg_flops_per_token_head(w1),
+                              sum(bwd_flops_per_token_head(w).values()),
+                              sum(bwd_flops_per_token_head(w1).values()))))
+        src, metric = BWD_NORM_SRC, BWD_METRIC
+        tc = False
+    elif bwd:
         params = hla.make_params(sets[0][0][0], sets[0][0][2], w.chunk, gamma)
         ws_bytes = hla.hla_backward_workspace_size(params)
         tc = w.dtype == "bf16" and w.d == w.dv == w.chunk == 64  # local sums and gradients on the tensor cores
@@ -697,14 +738,16 @@ def bench_phased(args, w: W.Workload, rank, world, local, dist):
                 "alg_bytes_per_step": set_bytes}
     cfg = config_dict(w, nsets, set_bytes, world)
     if bwd:
-        cfg["variant"] = "backward of the masked forward" + (" with decay" if w.decay else "")
+        cfg["variant"] = ("backward of the ratio-normalised masked forward" if w.normalize else
+                          "backward of the masked forward") + (" with decay" if w.decay else "")
         cfg["inputs"] += f", dout N(0,1) seed {w.seed + 1000}"
     else:
         cfg["variant"] = "masked third order"
     line = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": cfg, "roofline": roofline, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clk.summary(),
+            "config": cfg, "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step(w) * K,
+            "clocks": clk.summary(),
             "token_heads_per_s": world * w.token_heads * K / (t_max / 1e3)}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_backward(w, x, gout) if bwd else cpu_baseline_third(w, x)
@@ -913,7 +956,7 @@ def bench_reference_backward(args, w, x, cores, world):
     window of tokens (the gradient of a window from a zero state)."""
     import oracle
     gout = W.make_dout(w)
-    secs, _ = oracle_bwd_rate(x, gout, 1, min(w.n, 128), cores)
+    secs, _ = oracle_bwd_rate(x, gout, 1, min(w.n, 128), cores, w)
     budget = 90.0 / max(1, args.steps + args.warmup)
     n_s = int(max(16, min(w.n, 128 * budget / max(secs, 1e-9))))
     sl = lambda a, t0: np.ascontiguousarray(a[:1, :, t0:t0 + n_s], dtype=np.float64)
@@ -922,7 +965,8 @@ def bench_reference_backward(args, w, x, cores, world):
 
     def one(i):
         t0 = offs[i % len(offs)]
-        oracle.backward(sl(x["q"], t0), sl(x["k"], t0), sl(x["v"], t0), sl(gout, t0), gam, nthreads=cores)
+        oracle.backward(sl(x["q"], t0), sl(x["k"], t0), sl(x["v"], t0), sl(gout, t0), gam, nthreads=cores,
+                        **(dict(normalize=True, eps=w.eps) if w.normalize else {}))
 
     for i in range(args.warmup):
         one(i)

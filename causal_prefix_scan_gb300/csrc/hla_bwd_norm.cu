@@ -16,6 +16,12 @@
 // stays in fp32: bf16 inputs are widened once and the whole chain runs on the fp32
 // CUDA-core kernels; rounding n, den, the upstream gradients or the partial results to
 // bf16 costs several per cent of the result.
+//
+// The fp32 forward walks a sequence's chunks in one CTA, so step 1 splits every
+// sequence into P equal segments viewed as heads of their own: a forward from zero
+// gives each segment's state, an exclusive scan over the segments of a sequence (the
+// concatenation rule of section 4) gives each segment's initial state, and a second
+// forward from those states gives the outputs.
 #include <cstdint>
 #include <cstdio>
 
@@ -28,8 +34,6 @@ constexpr int kEwThreads = 256;
 
 template <typename T>
 __device__ __forceinline__ float ldx(const T *p, size_t i);
-template <>
-__device__ __forceinline__ float ldx<float>(const float *p, size_t i) { return p[i]; }
 template <>
 __device__ __forceinline__ float ldx<__nv_bfloat16>(const __nv_bfloat16 *p, size_t i) {
     return __bfloat162float(p[i]);
@@ -69,6 +73,52 @@ __global__ void __launch_bounds__(kEwThreads) norm_upstream_kernel(const float *
     }
 }
 
+// Exclusive scan over the P segments of each sequence (one CTA per sequence):
+// pre_0 = 0, pre_s = pre_{s-1} (+) seg_{s-1}, by the concatenation rule with A = pre_{s-1},
+// B = seg_{s-1}, f = g^{len}:  S = f S_A + S_B, C = f C_A + C_B, m = f m_A + m_B,
+// G = f^2 G_A + G_B + f S_B C_A, h = f^2 h_A + h_B + f S_B m_A.  Item i = sequence * P + s.
+constexpr int kScanMaxD = 64;
+__global__ void __launch_bounds__(kEwThreads) segment_scan_kernel(StatePtrs seg, StatePtrs pre, int P, int d, int dv,
+                                                                   int H, const float *gamma, int seg_len) {
+    __shared__ float sb[kScanMaxD * kScanMaxD], ca[kScanMaxD * kScanMaxD], ma[kScanMaxD];
+    const int seq = blockIdx.x, tid = threadIdx.x;
+    const size_t nS = (size_t)d * d, nC = (size_t)d * dv;
+    const float f = gamma ? exp2f(log2f(gamma[seq % H]) * (float)seg_len) : 1.f, f2 = f * f;
+    {
+        const size_t i0 = (size_t)seq * P;
+        for (size_t e = tid; e < nS; e += kEwThreads) pre.S[i0 * nS + e] = 0.f;
+        for (size_t e = tid; e < nC; e += kEwThreads) pre.C[i0 * nC + e] = pre.G[i0 * nC + e] = 0.f;
+        for (int e = tid; e < d; e += kEwThreads) pre.m[i0 * d + e] = pre.h[i0 * d + e] = 0.f;
+    }
+    __syncthreads();
+    for (int s = 1; s < P; ++s) {
+        const size_t a = (size_t)seq * P + s - 1, o = a + 1;  // pre_{s-1} and seg_{s-1} share index a
+        for (size_t e = tid; e < nS; e += kEwThreads) sb[e] = seg.S[a * nS + e];
+        for (size_t e = tid; e < nC; e += kEwThreads) ca[e] = pre.C[a * nC + e];
+        for (int e = tid; e < d; e += kEwThreads) ma[e] = pre.m[a * d + e];
+        __syncthreads();
+        for (size_t e = tid; e < nC; e += kEwThreads) {
+            const int r = (int)(e / dv), c = (int)(e % dv);
+            float acc = 0.f;
+            for (int k = 0; k < d; ++k) acc = fmaf(sb[r * d + k], ca[k * dv + c], acc);
+            pre.G[o * nC + e] = f2 * pre.G[a * nC + e] + seg.G[a * nC + e] + f * acc;
+            pre.C[o * nC + e] = f * ca[e] + seg.C[a * nC + e];
+        }
+        for (int r = tid; r < d; r += kEwThreads) {
+            float acc = 0.f;
+            for (int k = 0; k < d; ++k) acc = fmaf(sb[r * d + k], ma[k], acc);
+            pre.h[o * d + r] = f2 * pre.h[a * d + r] + seg.h[a * d + r] + f * acc;
+            pre.m[o * d + r] = f * ma[r] + seg.m[a * d + r];
+        }
+        for (size_t e = tid; e < nS; e += kEwThreads) pre.S[o * nS + e] = f * pre.S[a * nS + e] + sb[e];
+        __syncthreads();  // pre_s complete before it is read as pre_{s-1}
+    }
+}
+
+__global__ void __launch_bounds__(kEwThreads) repeat_kernel(float *dst, const float *src, int H, int P) {
+    for (int i = threadIdx.x; i < H * P; i += kEwThreads) dst[i] = src[i / P];
+}
+
 template <typename Ti>
 __global__ void __launch_bounds__(kEwThreads) widen_kernel(float *dst, const Ti *src, size_t count) {
     for (size_t i = (size_t)blockIdx.x * kEwThreads + threadIdx.x; i < count; i += (size_t)gridDim.x * kEwThreads)
@@ -96,6 +146,19 @@ hla_status cuda_err(cudaError_t e, const char *where) {
 }
 
 constexpr int kUnitWidth = 16;
+
+// Segments per sequence for the forwards: a power of two up to 16 that divides n into
+// pieces of at least one chunk, with B H P at most 4 x 152 CTAs; 1 (no split) with
+// shared key/value heads, whose head mapping the segment view does not keep.
+int segments(const hla_params &p) {
+    const int hkv = p.Hkv > 0 ? p.Hkv : p.H;
+    if (hkv != p.H) return 1;
+    int P = 1;
+    while (P < 16 && p.n % (2 * P) == 0 && p.n / (2 * P) >= p.chunk && (long long)p.B * p.H * 2 * P <= 4 * 152) P *= 2;
+    return P;
+}
+
+size_t state_floats(int d, int dv) { return (size_t)d * d + 2 * (size_t)d * dv + 2 * (size_t)d; }
 
 // The unnormalised fp32 problem of width dv.
 hla_params unnormalised(const hla_params &p, int dv) {
@@ -132,6 +195,12 @@ NormLayout bwd_norm_layout(const hla_params &p) {
     L.dk1 = take(rkv * p.d);
     L.dv1 = take(rkv * w1);
     L.bwd_ws = take(((bws > bws1 ? bws : bws1) + 3) / 4);
+    // segmented forwards: the repeated decay rates and two state sets (segments, prefixes)
+    L.P = segments(p);
+    const size_t items = (size_t)p.B * p.H * L.P, sf = state_floats(p.d, p.dv > w1 ? p.dv : w1);
+    L.grep = L.P > 1 ? take((size_t)p.H * L.P) : 0;
+    L.seg = L.P > 1 ? take(items * sf) : 0;
+    L.pre = L.P > 1 ? take(items * sf) : 0;
     // bf16 inputs: fp32 copies of q, k, v, g and fp32 results before the final rounding
     L.q32 = wide ? take(rq * p.d) : 0;
     L.k32 = wide ? take(rkv * p.d) : 0;
@@ -176,10 +245,45 @@ hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a0, void *workspa
     unit_value_kernel<<<grid_for(rkv * L.w1), kEwThreads, 0, st>>>(f(L.unit), rkv, L.w1);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_err(e, "operands");
     const hla_params pv = unnormalised(p, p.dv), pe = unnormalised(p, L.w1);
-    hla_status s = hla_forward_chunked(&pv, q, k, v, f(L.num), nullptr, nullptr, ws + L.fwd_ws, L.fwd_ws_bytes, st);
-    if (s != HLA_OK) return s;
-    s = hla_forward_chunked(&pe, q, k, f(L.unit), f(L.den1), nullptr, nullptr, ws + L.fwd_ws, L.fwd_ws_bytes, st);
-    if (s != HLA_OK) return s;
+    hla_status s;
+    if (L.P == 1) {
+        s = hla_forward_chunked(&pv, q, k, v, f(L.num), nullptr, nullptr, ws + L.fwd_ws, L.fwd_ws_bytes, st);
+        if (s != HLA_OK) return s;
+        s = hla_forward_chunked(&pe, q, k, f(L.unit), f(L.den1), nullptr, nullptr, ws + L.fwd_ws, L.fwd_ws_bytes, st);
+        if (s != HLA_OK) return s;
+    } else {
+        const int P = L.P;
+        if (p.flags & HLA_DECAY) repeat_kernel<<<1, kEwThreads, 0, st>>>(f(L.grep), p.gamma, p.H, P);
+        const size_t items = (size_t)p.B * p.H * P;
+        for (int part = 0; part < 2; ++part) {
+            hla_params ps = part == 0 ? pv : pe;
+            const int dvp = ps.dv;
+            ps.H = p.H * P;
+            ps.Hkv = p.H * P;
+            ps.n = p.n / P;
+            ps.gamma = (p.flags & HLA_DECAY) ? f(L.grep) : nullptr;
+            const size_t nS = (size_t)p.d * p.d, nC = (size_t)p.d * dvp;
+            auto states = [&](size_t off) {
+                hla_state t;
+                t.S = f(off);
+                t.C = t.S + items * nS;
+                t.m = t.C + items * nC;
+                t.G = t.m + items * p.d;
+                t.h = t.G + items * nC;
+                return t;
+            };
+            const hla_state sg = states(L.seg), pr = states(L.pre);
+            const void *vv = part == 0 ? static_cast<const void *>(v) : f(L.unit);
+            float *out = part == 0 ? f(L.num) : f(L.den1);
+            s = hla_forward_chunked(&ps, q, k, vv, out, nullptr, &sg, ws + L.fwd_ws, L.fwd_ws_bytes, st);
+            if (s != HLA_OK) return s;
+            segment_scan_kernel<<<p.B * p.H, kEwThreads, 0, st>>>(to_ptrs(&sg), to_ptrs(&pr), P, p.d, dvp, p.H,
+                                                                  (p.flags & HLA_DECAY) ? p.gamma : nullptr, p.n / P);
+            if ((e = cudaGetLastError()) != cudaSuccess) return cuda_err(e, "segment scan");
+            s = hla_forward_chunked(&ps, q, k, vv, out, &pr, nullptr, ws + L.fwd_ws, L.fwd_ws_bytes, st);
+            if (s != HLA_OK) return s;
+        }
+    }
     // 2. upstream gradients of the augmented problem
     norm_upstream_kernel<<<grid_for(rq * 32), kEwThreads, 0, st>>>(f(L.num), f(L.den1), g, f(L.gn), f(L.g1), rq,
                                                                     p.dv, L.w1, p.eps);

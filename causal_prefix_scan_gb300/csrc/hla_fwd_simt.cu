@@ -27,6 +27,7 @@
 // and P, m^K, E, n move to the chunk end with w_b, R = R + sum_b k_b q_b^T (no decay).
 // Key/value heads may be shared: query head h reads key/value head h / (H / Hkv).
 #include "hla_internal.h"
+#include "hla_smem_tile.cuh"
 
 namespace hla {
 namespace {
@@ -315,8 +316,199 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
     }
 }
 
+// ---- masked variant with register tiles ---------------------------------------
+// The same chunk algebra as above for the masked (optionally normalised, decayed)
+// forward, with every product on 4x4 register tiles over padded shared-memory rows
+// (leading dimensions = width + 4 floats, so that row-wise float4 reads of different
+// rows fall in different banks).  Products whose right operand is read transposed
+// (Q K^T, Q U^T) use column-strided tiles for the same reason.
+template <int D, int DV>
+struct TiledLayout {
+    static constexpr int LD = D + 4, LV = DV + 4, LC = kMaxChunk + 4;
+    static constexpr int S = 0, X = S + D * LD, Cs = X + D * LV, m = Cs + D * LV, Y = m + D;
+    static constexpr int Q = Y + D, K = Q + kMaxChunk * LD, U = K + kMaxChunk * LD, V = U + kMaxChunk * LD;
+    static constexpr int A = V + kMaxChunk * LV, gp = A + kMaxChunk * LC;
+    static constexpr int w1 = gp + 2 * kMaxChunk + 4, w2 = w1 + kMaxChunk, rden = w2 + kMaxChunk;
+    static constexpr int floats = rden + kMaxChunk;
+    static_assert(D % 4 == 0 && DV % 4 == 0 && X % 4 == 0 && Q % 4 == 0 && V % 4 == 0 && A % 4 == 0, "alignment");
+};
+
+template <class Body>
+__device__ __forceinline__ void tiles_rt(int M, int N, bool strided, Body body) {
+    const int tn = N / 4, count = (M / 4) * tn;
+    for (int t = threadIdx.x; t < count; t += kThreads) {
+        const int m0 = (t / tn) * 4;
+        const int n0 = strided ? t % tn : (t % tn) * 4, ns = strided ? tn : 1;
+        float acc[4][4] = {};
+        body(acc, m0, n0, ns);
+    }
+}
+
+template <typename T, int D, int DV>
+__global__ void __launch_bounds__(kThreads) fwd_simt_tiled_kernel(FwdArgs a) {
+    using Lt = TiledLayout<D, DV>;
+    constexpr int LD = Lt::LD, LV = Lt::LV, LC = Lt::LC;
+    extern __shared__ __align__(16) float sm[];
+    float *S = sm + Lt::S, *X = sm + Lt::X, *Cs = sm + Lt::Cs, *m = sm + Lt::m, *Y = sm + Lt::Y;
+    float *Q = sm + Lt::Q, *K = sm + Lt::K, *U = sm + Lt::U, *V = sm + Lt::V, *A = sm + Lt::A;
+    float *gp = sm + Lt::gp, *w1 = sm + Lt::w1, *w2 = sm + Lt::w2, *rden = sm + Lt::rden;
+    using tile::mac;
+    using tile::each;
+
+    const int c = a.chunk, tid = threadIdx.x;
+    const int u = blockIdx.x;  // pair index b*H + h
+    const int hh = u % a.H;
+    const bool decay = (a.flags & HLA_DECAY) != 0, norm = (a.flags & HLA_NORMALIZE) != 0;
+    const float lg = log2f(decay ? a.gamma[hh] : 1.f);
+    const size_t kvu = (size_t)(u / a.H) * a.Hkv + hh / (a.H / a.Hkv);
+    const T *q = static_cast<const T *>(a.q) + (size_t)u * a.n * D;
+    const T *k = static_cast<const T *>(a.k) + kvu * a.n * D;
+    const T *v = static_cast<const T *>(a.v) + kvu * a.n * DV;
+    T *o = static_cast<T *>(a.o) + (size_t)u * a.n * DV;
+    for (int x = tid; x <= 2 * c + 1; x += kThreads) gp[x] = decay ? gpow(lg, (float)x) : 1.f;
+
+    // ---- prefix state (X = S C - G, Y = S m - h)
+    if (a.sin.S) {
+        const float *Si = a.sin.S + (size_t)u * D * D, *Ci = a.sin.C + (size_t)u * D * DV;
+        const float *mi = a.sin.m + (size_t)u * D, *Gi = a.sin.G + (size_t)u * D * DV, *hi = a.sin.h + (size_t)u * D;
+        for (int e = tid; e < D * D; e += kThreads) S[(e / D) * LD + e % D] = Si[e];
+        for (int e = tid; e < D * DV; e += kThreads) Cs[(e / DV) * LV + e % DV] = Ci[e];
+        for (int e = tid; e < D; e += kThreads) m[e] = mi[e];
+        __syncthreads();
+        tiles_rt(D, DV, false, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+            mac<false, false>(acc, S, LD, Cs, LV, m0, n0, ns, D);
+            each(acc, m0, n0, ns, [&](int i, int j, float x) { X[i * LV + j] = x - Gi[(size_t)i * DV + j]; });
+        });
+        for (int i = tid; i < D; i += kThreads) {
+            float acc = 0.f;
+            for (int l = 0; l < D; ++l) acc = fmaf(S[i * LD + l], m[l], acc);
+            Y[i] = acc - hi[i];
+        }
+    } else {
+        for (int e = tid; e < D * D; e += kThreads) S[(e / D) * LD + e % D] = 0.f;
+        for (int e = tid; e < D * DV; e += kThreads) X[(e / DV) * LV + e % DV] = Cs[(e / DV) * LV + e % DV] = 0.f;
+        for (int e = tid; e < D; e += kThreads) m[e] = Y[e] = 0.f;
+    }
+    __syncthreads();
+
+    for (int t0 = 0; t0 < a.n; t0 += c) {
+        const int L = min(c, a.n - t0);
+        for (int e = tid; e < c * D; e += kThreads) {
+            const int t = e / D, i = e % D;
+            Q[t * LD + i] = t < L ? ld_in(q, (size_t)t0 * D + e) : 0.f;
+            K[t * LD + i] = t < L ? ld_in(k, (size_t)t0 * D + e) : 0.f;
+        }
+        for (int e = tid; e < c * DV; e += kThreads) {
+            const int t = e / DV;
+            V[t * LV + e % DV] = t < L ? ld_in(v, (size_t)t0 * DV + e) : 0.f;
+        }
+        for (int b = tid; b < c; b += kThreads) {
+            w1[b] = b < L ? gp[L - 1 - b] : 0.f;
+            w2[b] = b < L ? gp[2 * (L - 1 - b)] : 0.f;
+        }
+        __syncthreads();
+        // A[t,s] = g^{t-s} q_t.k_s, s <= t
+        tiles_rt(c, c, true, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+            mac<false, true>(acc, Q, LD, K, LD, m0, n0, ns, D);
+            each(acc, m0, n0, ns, [&](int t, int s2, float x) { A[t * LC + s2] = s2 <= t ? gp[t - s2] * x : 0.f; });
+        });
+        __syncthreads();
+        // U[b] = g^{b+1} S_p q_b + sum_{s<=b} A[b,s] k_s   (S symmetric)
+        tiles_rt(c, D, false, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+            mac<false, false>(acc, Q, LD, S, LD, m0, n0, ns, D);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] *= gp[m0 + i + 1];
+            mac<false, false>(acc, A, LC, K, LD, m0, n0, ns, c);
+            each(acc, m0, n0, ns, [&](int b, int i, float x) { U[b * LD + i] = x; });
+        });
+        __syncthreads();
+        // M[t,b] = g^{2(t-b)} q_t.u_b, b <= t (overwrites A)
+        tiles_rt(c, c, true, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+            mac<false, true>(acc, Q, LD, U, LD, m0, n0, ns, D);
+            each(acc, m0, n0, ns, [&](int t, int b, float x) { A[t * LC + b] = b <= t ? gp[2 * (t - b)] * x : 0.f; });
+        });
+        __syncthreads();
+        if (norm) {  // den_t = sum_b M[t,b] + g^{2 tau} q_t.Y_p
+            for (int t = tid; t < c; t += kThreads) {
+                float sm_ = 0.f, qy = 0.f;
+                for (int b = 0; b < c; ++b) sm_ += A[t * LC + b];
+                for (int i = 0; i < D; ++i) qy = fmaf(Q[t * LD + i], Y[i], qy);
+                rden[t] = 1.f / (sm_ + gp[2 * (t + 1)] * qy + a.eps);
+            }
+            __syncthreads();
+        }
+        // o_t = sum_b M[t,b] v_b + g^{2 tau} q_t^T X_p  (/ den_t)
+        tiles_rt(c, DV, false, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+            float px[4][4] = {};
+            mac<false, false>(acc, A, LC, V, LV, m0, n0, ns, c);
+            mac<false, false>(px, Q, LD, X, LV, m0, n0, ns, D);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = m0 + i;
+                if (t >= L) continue;
+                const float r = norm ? rden[t] : 1.f, gt = gp[2 * (t + 1)];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) st_out(o, (size_t)(t0 + t) * DV + n0 + j, (acc[i][j] + gt * px[i][j]) * r);
+            }
+        });
+        __syncthreads();
+        // state to the chunk end: weights w1 = g^{L-1-b} (S, C, m), w2 = w1^2 (X, Y)
+        const float gL = gp[L], g2L = gp[2 * L];
+        tiles_rt(D, D, false, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+            mac<true, false>(acc, K, LD, K, LD, m0, n0, ns, c, w1);
+            each(acc, m0, n0, ns, [&](int i, int j, float x) { S[i * LD + j] = gL * S[i * LD + j] + x; });
+        });
+        tiles_rt(D, DV, false, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+            float ax[4][4] = {};
+            mac<true, false>(acc, Q, LD, V, LV, m0, n0, ns, c, w1);
+            mac<true, false>(ax, U, LD, V, LV, m0, n0, ns, c, w2);
+            each(acc, m0, n0, ns, [&](int i, int j, float x) { Cs[i * LV + j] = gL * Cs[i * LV + j] + x; });
+            each(ax, m0, n0, ns, [&](int i, int j, float x) { X[i * LV + j] = g2L * X[i * LV + j] + x; });
+        });
+        for (int i = tid; i < D; i += kThreads) {
+            float am = 0.f, ay = 0.f;
+            for (int b = 0; b < L; ++b) {
+                am = fmaf(w1[b], Q[b * LD + i], am);
+                ay = fmaf(w2[b], U[b * LD + i], ay);
+            }
+            m[i] = gL * m[i] + am;
+            Y[i] = g2L * Y[i] + ay;
+        }
+        __syncthreads();
+    }
+
+    if (a.sout.S) {  // G = S C - X, h = S m - Y
+        float *So = a.sout.S + (size_t)u * D * D, *Co = a.sout.C + (size_t)u * D * DV;
+        float *mo = a.sout.m + (size_t)u * D, *Go = a.sout.G + (size_t)u * D * DV, *ho = a.sout.h + (size_t)u * D;
+        for (int e = tid; e < D * D; e += kThreads) So[e] = S[(e / D) * LD + e % D];
+        tiles_rt(D, DV, false, [&](float (&acc)[4][4], int m0, int n0, int ns) {
+            mac<false, false>(acc, S, LD, Cs, LV, m0, n0, ns, D);
+            each(acc, m0, n0, ns, [&](int i, int j, float x) {
+                Co[(size_t)i * DV + j] = Cs[i * LV + j];
+                Go[(size_t)i * DV + j] = x - X[i * LV + j];
+            });
+        });
+        for (int i = tid; i < D; i += kThreads) {
+            float acc = 0.f;
+            for (int l = 0; l < D; ++l) acc = fmaf(S[i * LD + l], m[l], acc);
+            mo[i] = m[i];
+            ho[i] = acc - Y[i];
+        }
+    }
+}
+
 template <typename T, int D, int DV>
 cudaError_t launch_t(const FwdArgs &a, cudaStream_t st) {
+    if (!(a.flags & (HLA_UNMASKED | HLA_ASYMMETRIC))) {
+        const size_t bytes = (size_t)TiledLayout<D, DV>::floats * sizeof(float);
+        auto kern = fwd_simt_tiled_kernel<T, D, DV>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e != cudaSuccess) return e;
+        kern<<<a.B * a.H, kThreads, bytes, st>>>(a);
+        return cudaGetLastError();
+    }
     constexpr int DU = D > DV ? D : DV;
     const size_t floats = (size_t)D * D + 2 * (size_t)D * DV + 2 * D + (size_t)kMaxChunk * (2 * D + DV + DU) +
                           (size_t)kMaxChunk * kMaxChunk + kMaxChunk + 2 * kMaxChunk + 2;

@@ -92,7 +92,10 @@ cudaError_t bwd_simt_launch(const BwdArgs &a, cudaStream_t st);
 struct NormLayout {
     int w1;  // width of the unit-value tile
     size_t fwd_ws, fwd_ws_bytes, num, den1, unit, gn, g1, dq1, dk1, dv1, bwd_ws;
-    size_t q32, k32, v32, g32, dq32, dk32, dv32, total;
+    size_t q32, k32, v32, g32, dq32, dk32, dv32;
+    int P;              // segments per sequence of the fp32 forwards (1: no split)
+    size_t grep, seg, pre;  // decay rates repeated per segment; segment states; their prefixes
+    size_t total;
 };
 NormLayout bwd_norm_layout(const hla_params &p);
 hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a, void *workspace, cudaStream_t st);

@@ -76,10 +76,14 @@ FWD_ASYM = Workload("fwd_bf16_asym_B4H8n2048d64", 4, 8, 2048, 64, 64, 64, "bf16"
 # The backward pass (training) on the same shape: q, k, v as above plus the
 # gradient of the output from make_dout.
 BWD_BF16 = Workload("bwd_bf16_B4H8n2048d64", 4, 8, 2048, 64, 64, 64, "bf16", "l2", seed=9)
+# Backward through the ratio normalisation: positive (elu+1) features as in the
+# normalised forward workload, on the backward workload's shape.
+BWD_NORM = Workload("bwd_bf16_norm_B4H8n2048d64", 4, 8, 2048, 64, 64, 64, "bf16", "elu1", normalize=True, eps=1e-6,
+                    seed=11)
 # Masked third-order HLA on the same shape.
 FWD3_BF16 = Workload("fwd3_bf16_B4H8n2048d64", 4, 8, 2048, 64, 64, 64, "bf16", "l2", seed=10)
 WORKLOADS = {w.name: w for w in (SMALL_F32, FWD_BF16, FWD_NORM, FWD_DECAY, FWD_UNMASKED, FWD_SHARED_KV, FWD_ASYM,
-                                 BWD_BF16, FWD3_BF16)}
+                                 BWD_BF16, BWD_NORM, FWD3_BF16)}
 
 
 @dataclass(frozen=True)

@@ -199,3 +199,15 @@ def test_backward_normalised_is_gradient_of_forward():
     F = {j: f(j * s) for j in (-3, -2, -1, 1, 2, 3)}
     fd = (45 * (F[1] - F[-1]) - 9 * (F[2] - F[-2]) + (F[3] - F[-3])) / (60 * s)
     assert abs(fd - want) <= 2e-3 * abs(want), (fd, want)
+
+
+@pytest.mark.parametrize("d,dv,chunk,n,dtype,decay", [(32, 16, 16, 256, "f32", True), (64, 64, 64, 1024, "bf16", True),
+                                                      (16, 32, 16, 96, "f32", False), (64, 32, 32, 512, "bf16", False)])
+def test_backward_normalised_segmented(d, dv, chunk, n, dtype, decay):
+    """Long enough sequences that the fp32 forwards run as 4-16 segments per sequence
+    (forward from zero, exclusive scan of the segment states, forward from the prefixes)."""
+    w = small(B=1, H=2, n=n, d=d, dv=dv, chunk=chunk, decay=decay, dtype=dtype, qk="elu1", seed=44)
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    check(run_backward(x, g, dtype, chunk, eps=1e-3), run_oracle(x, g, eps=1e-3),
+          TOL_F32 if dtype == "f32" else TOL_BF16, f"bwd norm segmented {dtype} d{d} dv{dv} c{chunk} n{n} decay={decay}")
