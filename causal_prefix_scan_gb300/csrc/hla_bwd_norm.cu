@@ -73,45 +73,57 @@ __global__ void __launch_bounds__(kEwThreads) norm_upstream_kernel(const float *
     }
 }
 
-// Exclusive scan over the P segments of each sequence (one CTA per sequence):
-// pre_0 = 0, pre_s = pre_{s-1} (+) seg_{s-1}, by the concatenation rule with A = pre_{s-1},
-// B = seg_{s-1}, f = g^{len}:  S = f S_A + S_B, C = f C_A + C_B, m = f m_A + m_B,
-// G = f^2 G_A + G_B + f S_B C_A, h = f^2 h_A + h_B + f S_B m_A.  Item i = sequence * P + s.
-constexpr int kScanMaxD = 64;
+// Exclusive scan over the P segments of each sequence: pre_0 = 0, pre_s = pre_{s-1} (+)
+// seg_{s-1} by the concatenation rule with A = pre_{s-1}, B = seg_{s-1}, f = g^{len}:
+//   S = f S_A + S_B, C = f C_A + C_B, m = f m_A + m_B,
+//   G = f^2 G_A + G_B + f S_B C_A, h = f^2 h_A + h_B + f S_B m_A.
+// Item i = sequence * P + s.  CTA (sequence, row block) writes rows [r0, r0 + kScanRows)
+// of every state; each keeps its own copy of the whole prefix C and m (the right
+// factor of the cross terms) in shared memory.
+constexpr int kScanMaxD = 64, kScanRows = 16;
 __global__ void __launch_bounds__(kEwThreads) segment_scan_kernel(StatePtrs seg, StatePtrs pre, int P, int d, int dv,
                                                                    int H, const float *gamma, int seg_len) {
-    __shared__ float sb[kScanMaxD * kScanMaxD], ca[kScanMaxD * kScanMaxD], ma[kScanMaxD];
-    const int seq = blockIdx.x, tid = threadIdx.x;
+    __shared__ float sb[kScanRows * kScanMaxD], ca[kScanMaxD * kScanMaxD], ma[kScanMaxD];
+    const int seq = blockIdx.x, r0 = blockIdx.y * kScanRows, tid = threadIdx.x;
     const size_t nS = (size_t)d * d, nC = (size_t)d * dv;
     const float f = gamma ? exp2f(log2f(gamma[seq % H]) * (float)seg_len) : 1.f, f2 = f * f;
     {
         const size_t i0 = (size_t)seq * P;
-        for (size_t e = tid; e < nS; e += kEwThreads) pre.S[i0 * nS + e] = 0.f;
-        for (size_t e = tid; e < nC; e += kEwThreads) pre.C[i0 * nC + e] = pre.G[i0 * nC + e] = 0.f;
-        for (int e = tid; e < d; e += kEwThreads) pre.m[i0 * d + e] = pre.h[i0 * d + e] = 0.f;
+        for (int e = tid; e < kScanRows * d; e += kEwThreads) pre.S[i0 * nS + (size_t)r0 * d + e] = 0.f;
+        for (int e = tid; e < kScanRows * dv; e += kEwThreads)
+            pre.C[i0 * nC + (size_t)r0 * dv + e] = pre.G[i0 * nC + (size_t)r0 * dv + e] = 0.f;
+        for (int e = tid; e < kScanRows; e += kEwThreads) pre.m[i0 * d + r0 + e] = pre.h[i0 * d + r0 + e] = 0.f;
+        for (size_t e = tid; e < nC; e += kEwThreads) ca[e] = 0.f;
+        for (int e = tid; e < d; e += kEwThreads) ma[e] = 0.f;
     }
     __syncthreads();
     for (int s = 1; s < P; ++s) {
-        const size_t a = (size_t)seq * P + s - 1, o = a + 1;  // pre_{s-1} and seg_{s-1} share index a
-        for (size_t e = tid; e < nS; e += kEwThreads) sb[e] = seg.S[a * nS + e];
-        for (size_t e = tid; e < nC; e += kEwThreads) ca[e] = pre.C[a * nC + e];
-        for (int e = tid; e < d; e += kEwThreads) ma[e] = pre.m[a * d + e];
+        const size_t a = (size_t)seq * P + s - 1;  // pre_{s-1} and seg_{s-1}; pre_s is item a + 1
+        for (int e = tid; e < kScanRows * d; e += kEwThreads) sb[e] = seg.S[a * nS + (size_t)r0 * d + e];
         __syncthreads();
-        for (size_t e = tid; e < nC; e += kEwThreads) {
-            const int r = (int)(e / dv), c = (int)(e % dv);
+        for (int e = tid; e < kScanRows * dv; e += kEwThreads) {
+            const int r = e / dv, c = e % dv;
+            const size_t gi = a * nC + (size_t)(r0 + r) * dv + c;
             float acc = 0.f;
             for (int k = 0; k < d; ++k) acc = fmaf(sb[r * d + k], ca[k * dv + c], acc);
-            pre.G[o * nC + e] = f2 * pre.G[a * nC + e] + seg.G[a * nC + e] + f * acc;
-            pre.C[o * nC + e] = f * ca[e] + seg.C[a * nC + e];
+            pre.G[gi + nC] = f2 * pre.G[gi] + seg.G[gi] + f * acc;
+            pre.C[gi + nC] = f * ca[(r0 + r) * dv + c] + seg.C[gi];
         }
-        for (int r = tid; r < d; r += kEwThreads) {
+        for (int r = tid; r < kScanRows; r += kEwThreads) {
             float acc = 0.f;
             for (int k = 0; k < d; ++k) acc = fmaf(sb[r * d + k], ma[k], acc);
-            pre.h[o * d + r] = f2 * pre.h[a * d + r] + seg.h[a * d + r] + f * acc;
-            pre.m[o * d + r] = f * ma[r] + seg.m[a * d + r];
+            const size_t hi = a * d + r0 + r;
+            pre.h[hi + d] = f2 * pre.h[hi] + seg.h[hi] + f * acc;
+            pre.m[hi + d] = f * ma[r0 + r] + seg.m[hi];
         }
-        for (size_t e = tid; e < nS; e += kEwThreads) pre.S[o * nS + e] = f * pre.S[a * nS + e] + sb[e];
-        __syncthreads();  // pre_s complete before it is read as pre_{s-1}
+        for (int e = tid; e < kScanRows * d; e += kEwThreads) {
+            const size_t si = a * nS + (size_t)r0 * d + e;
+            pre.S[si + nS] = f * pre.S[si] + sb[e];
+        }
+        __syncthreads();  // every read of ca, ma and sb for this step is done
+        for (size_t e = tid; e < nC; e += kEwThreads) ca[e] = f * ca[e] + seg.C[a * nC + e];
+        for (int e = tid; e < d; e += kEwThreads) ma[e] = f * ma[e] + seg.m[a * d + e];
+        __syncthreads();
     }
 }
 
@@ -277,8 +289,8 @@ hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a0, void *workspa
             float *out = part == 0 ? f(L.num) : f(L.den1);
             s = hla_forward_chunked(&ps, q, k, vv, out, nullptr, &sg, ws + L.fwd_ws, L.fwd_ws_bytes, st);
             if (s != HLA_OK) return s;
-            segment_scan_kernel<<<p.B * p.H, kEwThreads, 0, st>>>(to_ptrs(&sg), to_ptrs(&pr), P, p.d, dvp, p.H,
-                                                                  (p.flags & HLA_DECAY) ? p.gamma : nullptr, p.n / P);
+            segment_scan_kernel<<<dim3(p.B * p.H, p.d / kScanRows), kEwThreads, 0, st>>>(
+                to_ptrs(&sg), to_ptrs(&pr), P, p.d, dvp, p.H, (p.flags & HLA_DECAY) ? p.gamma : nullptr, p.n / P);
             if ((e = cudaGetLastError()) != cudaSuccess) return cuda_err(e, "segment scan");
             s = hla_forward_chunked(&ps, q, k, vv, out, &pr, nullptr, ws + L.fwd_ws, L.fwd_ws_bytes, st);
             if (s != HLA_OK) return s;
