@@ -1,6 +1,8 @@
 // hla_bwd_simt.cuh -- chunk-parallel backward pass of the masked second-order HLA
-// forward on CUDA cores (fp32 arithmetic), for d, dv, chunk in {16,32,64}, zero
-// initial state, no normalisation, one key/value head per query head.
+// forward on CUDA cores (fp32 arithmetic), for d, dv, chunk in {16,32,64} and a zero
+// initial state.  The kernels compute the unnormalised gradient; the ratio-normalised
+// one is composed from two such passes (hla_bwd_norm.cu).  Query heads may share key/
+// value heads: dk, dv are staged per query head and summed over each group.
 //
 // The pages motivate chunk-parallel training ("Higher-order Linear Attention",
 // gist.science summary, section 4) but print no gradient.  Forward in the working
