@@ -1208,7 +1208,11 @@ struct Kern {
     // Outputs from the exact prefix.  Q S_p and Q X_p go to the spare columns so
     // that they overlap the epilogues; two completion barriers let the block work
     // on one group of MMA results while the next group runs.
+    // With chunk >= d the next chunk's S_p fits in tU(), so S_p and X_p are extracted
+    // at the end of the previous chunk; otherwise at the start of each chunk (S_p in tS()).
+    static constexpr bool kTailState = C >= D;
     __device__ bool pass2(int jb, int je) {
+        uint8_t *const sp_tile = kTailState ? tU() : tS();
         int stage = 0;
         tma_chunk(jb, 0);
         for (int jj = jb; jj < je; ++jj) {
@@ -1220,14 +1224,20 @@ struct Kern {
             if (K_::NSTAGE == 2 && jj + 1 < je) tma_chunk(jj + 1, stage ^ 1);
             if (tid == 0) mma_kk<C, D>(TW, Q, Kt, false);  // A = Q K^T
             commit();
-            // meanwhile: S_p -> bf16 operand, then decay S to the chunk end
-            extract_state<D>(TS, tS(), gp(L));
-            publish();
-            if (tid == 0) mma_kk<D, D>(T4, Q, tS(), false);  // spare = Q S_p
-            commit2();
-            // meanwhile: X_p -> bf16 operand, then decay X; q . Y_p for the denominator
-            extract_state<DV>(TX, tQ(), gp(2 * L));
-            if constexpr (NORM) row_dot_Y(Q);
+            if (jj == jb || !kTailState) {
+                // S_p, X_p from TMEM -> bf16 operands, then S, X decay to the chunk end
+                extract_state<D>(TS, sp_tile, gp(L));
+                publish();
+                if (tid == 0) {
+                    mma_kk<D, D>(T4, Q, sp_tile, false);  // spare = Q S_p
+                    umma_commit(mma_bar2);
+                }
+                extract_state<DV>(TX, tQ(), gp(2 * L));
+            } else if (tid == 32) {  // S_p, X_p were extracted at the end of the previous chunk
+                mma_kk<D, D>(T4, Q, sp_tile, false);  // spare = Q S_p, beside thread 0's issue
+                umma_commit(mma_bar2);
+            }
+            if constexpr (NORM) row_dot_Y(Q);  // q . Y_p for the denominator
             if (!wait_mma()) return false;  // A
             epi_atilde();
             publish();
@@ -1277,7 +1287,7 @@ struct Kern {
             float ay = 0.f;
             float *ysc = rsum();  // rsum is free until the M epilogue
             if constexpr (NORM && !DECAY) {
-                // scratch: tS (S_p) is free once Q S_p has run
+                // scratch: tS() is free here (S_p, when it is there, has been read by Q S_p)
                 tile_colsums<false>(tU(), nullptr, L, 1.f, reinterpret_cast<float *>(tS()), Yrun(), gp(2 * L),
                                     nullptr, 1.f);
             } else if constexpr (NORM) {
@@ -1331,7 +1341,14 @@ struct Kern {
                     tile_store_row16(tS(), C, rowC, c0, v);
                 });
             }
-            publish();  // tile writes visible to the TMA; TMEM reads of W and the spare done
+            if (kTailState && jj + 1 < je) {
+                // the next chunk's S_p, X_p -> tU(), tQ() (their last readers, M, the X
+                // update and Q X_p, have completed), then S, X decay to its end
+                const int Ln = min(C, P.n - (jj + 1) * C);
+                extract_state<D>(TS, tU(), gp(Ln));
+                extract_state<DV>(TX, tQ(), gp(2 * Ln));
+            }
+            publish();  // tile writes visible to the TMA and the next MMAs; TMEM reads done
             if (tid == 0) {
 #pragma unroll
                 for (int kb = 0; kb < DV / 64; ++kb) tma_store_3d(tS() + kb * C * 128, &P.tmO, kb * 64, t0, bh);
