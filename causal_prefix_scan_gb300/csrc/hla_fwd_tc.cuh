@@ -1219,7 +1219,10 @@ struct Kern {
             const int t0 = jj * C;
             const int L = min(C, P.n - t0);
             uint8_t *Q = sQ(stage), *Kt = sK(stage), *V = sV(stage);
-            if (tid == 0) bulk_wait_read();  // the previous chunk's O store has left tS()
+            // the previous chunk's O store must have left tS() before tS() is rewritten:
+            // with S_p in tS() at once, otherwise before the U epilogue (which writes
+            // W^2 U there with decay), the scratch use with normalisation and the O tile
+            if (!kTailState && tid == 0) bulk_wait_read();
             if (!wait_tma(stage)) return false;
             if (K_::NSTAGE == 2 && jj + 1 < je) tma_chunk(jj + 1, stage ^ 1);
             if (tid == 0) mma_kk<C, D>(TW, Q, Kt, false);  // A = Q K^T
@@ -1243,6 +1246,7 @@ struct Kern {
             publish();
             if (tid == 0) mma_km<D, C>(TW, tA(), Kt, false);  // W = A-tilde K
             commit();
+            if (kTailState && tid == 0) bulk_wait_read();  // ordered by the barriers of the waits
             if (!wait_mma2()) return false;  // Q S_p
             if (!wait_mma()) return false;   // A-tilde K
             // U = g^tau Q S_p + A-tilde K -> tU(); W^2 U -> tS() (decay)
