@@ -211,3 +211,13 @@ def test_backward_normalised_segmented(d, dv, chunk, n, dtype, decay):
     g = W.make_dout(w)
     check(run_backward(x, g, dtype, chunk, eps=1e-3), run_oracle(x, g, eps=1e-3),
           TOL_F32 if dtype == "f32" else TOL_BF16, f"bwd norm segmented {dtype} d{d} dv{dv} c{chunk} n{n} decay={decay}")
+
+
+def test_backward_normalised_full_workload():
+    """The normalised backward at the size its bench leg times (B4 H8 n2048 d = dv = 64,
+    bf16, 16 segments per sequence in the forwards), against the oracle's gradient."""
+    w = W.BWD_NORM
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    err = check(run_backward(x, g, w.dtype, w.chunk, eps=w.eps), run_oracle(x, g, eps=w.eps), TOL_BF16, w.name)
+    print(f"{w.name}: max per-(b,h) rel L2 {err:.3e}")
