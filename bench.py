@@ -773,30 +773,29 @@ def bench_decode(args, dw: W.DecodeWorkload, rank, world, local, dist):
                         torch.randn((N, d, dv), generator=gs, device=dev) * 0.05)
         del a_
     # prefill the state with the forward over a seeded prefix (drawn on the device)
-    pw = W.Workload("decode_prefix", dw.seqs, dw.H, dw.prefix, d, dv, max(dw.chunk, 64), "bf16", "l2", seed=dw.seed)
     if not third:
         st = hla.State.empty(N, d, dv, device=dev)
-    rows = 32
-    for b0 in range(0, dw.seqs if not third else 0, rows):
-        px = W.make_inputs_device(pw.with_(B=min(rows, dw.seqs - b0), seed=dw.seed * 1000 + b0), device=dev)
-        sub = hla.State(*(a[b0 * dw.H:(b0 + px["q"].shape[0]) * dw.H] for a in st.astuple()))
-        p = hla.make_params(px["q"], px["v"], dw.chunk)
-        need = hla.hla_forward_workspace_size(p)
-        ws = hla.new_workspace(need, dev)
-        o = torch.empty_like(px["v"])
-        hla.hla_forward_chunked(p, px["q"], px["k"], px["v"], o, None, sub, ws, need)
-        del px, o, ws
+        for b0, pw in W.decode_prefix_blocks(dw):
+            px = W.make_inputs_device(pw, device=dev)
+            sub = hla.State(*(a[b0 * dw.H:(b0 + pw.B) * dw.H] for a in st.astuple()))
+            p = hla.make_params(px["q"], px["v"], dw.chunk)
+            need = hla.hla_forward_workspace_size(p)
+            ws = hla.new_workspace(need, dev)
+            o = torch.empty_like(px["v"])
+            hla.hla_forward_chunked(p, px["q"], px["k"], px["v"], o, None, sub, ws, need)
+            del px, o, ws
     torch.cuda.synchronize()
     hla.hla_sync_status()
     steps = args.steps
     T = min(steps, 64)  # distinct token sets cycled through
-    g = torch.Generator(device=dev)
-    g.manual_seed(dw.seed)
-    def draw(shape):
-        x = torch.randn(shape, generator=g, device=dev)
-        return (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
-    toks = [(draw((N, d)), draw((N, d)), torch.randn((N, dv), generator=g, device=dev).to(torch.bfloat16))
-            for _ in range(T)]
+    toks = W.decode_tokens_device(dw, T, device=dev)
+    # the oracle's continuation starts from the exact fp32 state of a seeded sample of pairs
+    cpu_sample = None
+    if rank == 0 and not third and not args.no_cpu_baseline:
+        idx = np.sort(np.random.default_rng(dw.seed + 500).choice(N, 64, replace=False))
+        ti = torch.from_numpy(idx).to(dev)
+        cpu_sample = (idx, [a.index_select(0, ti).double().cpu().numpy() for a in st.astuple()],
+                      [tuple(t.index_select(0, ti).float().cpu().numpy() for t in ts) for ts in toks])
     o = torch.empty((N, dv), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
@@ -877,7 +876,40 @@ def bench_decode(args, dw: W.DecodeWorkload, rank, world, local, dist):
             "e2e": {"value": world * dw.seqs * Ke / (te / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": 3 * N * d * 2, "d2h_bytes_per_step": N * dv * 2, "steps": Ke},
             "gpu_launches": steps, "clocks": clk.summary()}
+    if cpu_sample is not None:
+        line["cpu_baseline"] = cpu_baseline_decode(dw, *cpu_sample)
     return line
+
+
+def oracle_decode_rate(dw: W.DecodeWorkload, state, tok_sets, steps: int, nthreads: int):
+    """Continue the fp64 oracle's decode from `state` (the sampled pairs' fp32 state,
+    as oracle.State) for `steps` steps with the workload's token sets; returns seconds."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        q, k, v = tok_sets[i % len(tok_sets)]
+        oracle.decode_step(state, q, k, v, 1, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_decode(dw: W.DecodeWorkload, idx, state_arrays, tok_sets):
+    """The oracle's decode step continued from the prefilled fp32 state of a seeded
+    sample of (sequence, head) pairs for about 10 s; tokens/s counts sequence steps
+    (H pair steps each), the unit of the GPU line."""
+    import oracle
+    cores = cpu_threads()
+    used = min(cores, len(idx))
+    st = oracle.State(*(np.array(a, dtype=np.float64) for a in state_arrays))
+    secs = oracle_decode_rate(dw, st, tok_sets, 4, used)
+    steps = int(max(4, min(dw.steps, 10.0 * 4 / max(secs, 1e-9))))
+    st = oracle.State(*(np.array(a, dtype=np.float64) for a in state_arrays))
+    secs = oracle_decode_rate(dw, st, tok_sets, steps, used)
+    pair_steps = len(idx) * steps
+    return {"value": pair_steps / dw.H / secs, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"fp64 decode step continued from the prefilled fp32 state of {len(idx)} of {dw.seqs * dw.H} "
+                      f"(sequence, head) pairs for {steps} of {dw.steps} steps, threads over pairs; "
+                      f"tokens = pair steps / H", "seconds": secs}
 
 
 # ----------------------------------------------------------------- reference arm
@@ -885,7 +917,9 @@ def bench_reference(args, w, rank, world):
     """The oracle as it stands, on the host cores: each step one bounded sample of
     the workload (one batch row, all heads, a window of tokens)."""
     if isinstance(w, W.DecodeWorkload):
-        return {"impl": "reference", "unavailable": "the oracle arm is defined for the forward workloads"}
+        if w.order == 3:
+            return {"impl": "reference", "unavailable": "the oracle has no third-order decode step"}
+        return bench_reference_decode(args, w, world)
     x = W.make_inputs(w)
     cores = min(cpu_threads(), w.H)
     if is_backward(w):
@@ -917,6 +951,37 @@ def bench_reference(args, w, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_dict(w, 1, 0, world),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def bench_reference_decode(args, dw: W.DecodeWorkload, world):
+    """The oracle's decode step on the host cores: 64 (sequence, head) pairs whose
+    state the oracle prefills over a host-drawn 256-token prefix of the workload's
+    recipe (untimed; the cost of a step does not depend on the state's values), then
+    each step continues them for a window of steps sized so the run ends in about 90 s."""
+    import oracle
+    P = 64
+    cores = min(cpu_threads(), P)
+    pre = W.make_inputs(W.Workload("decode_ref_prefix", 1, P, 256, dw.d, dw.dv, 64, "bf16", "l2", seed=dw.seed))
+    _, st = oracle.forward(pre["q"], pre["k"], pre["v"], nthreads=cores)
+    toks = W.make_decode_tokens(1, P, dw.d, dw.dv, 16, seed=dw.seed)
+    sets = [(toks["q"][i], toks["k"][i], toks["v"][i]) for i in range(16)]
+    secs = oracle_decode_rate(dw, st.copy(), sets, 4, cores) / 4
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    s_per = int(max(1, min(dw.steps, budget / max(secs, 1e-9))))
+    for _ in range(args.warmup):
+        oracle_decode_rate(dw, st, sets, s_per, cores)
+    dt = sum(oracle_decode_rate(dw, st, sets, s_per, cores) for _ in range(args.steps))
+    value = P * s_per * args.steps / dw.H / dt
+    sample = (f"fp64 decode step on {P} of {dw.seqs * dw.H} (sequence, head) pairs x {s_per} steps per step, "
+              f"from an oracle-prefilled 256-token prefix; tokens = pair steps / H")
+    cfg = {"workload": dw.name, "seqs": dw.seqs, "H": dw.H, "d": dw.d, "dv": dw.dv, "prefix": dw.prefix,
+           "sample": sample}
+    return {"impl": "reference", "metric": "HLA decode step tokens/s and % HBM roofline on 1 GB300", "value": value,
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": cfg,
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 

@@ -30,6 +30,11 @@ size_t fwd_tc_workspace(const hla_params &p, int num_sms) {
     return tc::ws_layout(p, tc::make_plan(p, num_sms)).total;
 }
 
+size_t fwd_tc_sync_bytes(const hla_params &p, int num_sms) {
+    if (p.n == 0) return 0;
+    return tc::ws_layout(p, tc::make_plan(p, num_sms)).off_summ;
+}
+
 cudaError_t fwd_tc_launch(const FwdArgs &a, cudaStream_t st, int num_sms) {
     const int var = (a.flags & HLA_UNMASKED) ? 1 : ((a.flags & HLA_ASYMMETRIC) ? 2 : 0);
     const int key = ((a.flags & HLA_DECAY) ? 6 : 0) + ((a.flags & HLA_NORMALIZE) ? 3 : 0) + var;

@@ -169,6 +169,40 @@ def make_decode_tokens(seqs: int, H: int, d: int, dv: int, steps: int, seed: int
     return {"q": round_bf16(_rows_l2(q)), "k": round_bf16(_rows_l2(k)), "v": round_bf16(v)}
 
 
+# Sequences per prefill launch of a decode workload (bounds the device memory of
+# the drawn prefix: 32 sequences x 32 heads x 4096 tokens x 128 is 1 GiB per bf16 tensor).
+DECODE_PREFILL_ROWS = 32
+
+
+def decode_prefix_blocks(dw: DecodeWorkload):
+    """The prefill of a second-order decode workload as forward workloads over
+    blocks of at most DECODE_PREFILL_ROWS sequences.  Yields (b0, Workload): the
+    block's first sequence and its recipe, drawn on the device by
+    make_inputs_device (L2-normalised q, k, v ~ N(0,1), bf16, seed dw.seed * 1000 + b0)."""
+    base = Workload("decode_prefix", dw.seqs, dw.H, dw.prefix, dw.d, dw.dv, max(dw.chunk, 64), "bf16", "l2",
+                    seed=dw.seed)
+    for b0 in range(0, dw.seqs, DECODE_PREFILL_ROWS):
+        yield b0, base.with_(B=min(DECODE_PREFILL_ROWS, dw.seqs - b0), seed=dw.seed * 1000 + b0)
+
+
+def decode_tokens_device(dw: DecodeWorkload, count: int, device="cuda"):
+    """`count` token sets of a decode workload, drawn on the device with torch's
+    generator seeded by dw.seed: per set q [seqs*H, d], k [seqs*H, d] (N(0,1),
+    rows L2-normalised) and v [seqs*H, dv] (N(0,1)), in that order, as bf16.
+    Step i of the workload uses set i % count."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(dw.seed)
+    N = dw.seqs * dw.H
+
+    def draw(shape):
+        x = torch.randn(shape, generator=g, device=device)
+        return (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+
+    return [(draw((N, dw.d)), draw((N, dw.d)),
+             torch.randn((N, dw.dv), generator=g, device=device).to(torch.bfloat16)) for _ in range(count)]
+
+
 def make_inputs_device(w: Workload, device="cuda"):
     """Same recipe drawn on the device with torch's seeded generator, for
     workloads too large to draw on the host (the decode prefix).  Returns

@@ -316,6 +316,13 @@ HLA_API const char *hla_last_error(void);
  *
  *   - The first call on a device looks up the array's device address while
  *     that device is current; make that first call before any stream capture.
+ *     The address is kept per device together with the context it was taken
+ *     in: after cudaDeviceReset (or another teardown of the primary context)
+ *     the next call looks it up again, so make that call before any capture too.
+ *   - Each call clears the forward's ordering header and release flags at the
+ *     front of the array (one cudaMemsetAsync on `stream`) and then runs the
+ *     ordinary forward on the array; the rest of the array keeps whatever the
+ *     last call left there.
  *   - Every call shares the one array.  Calls that may overlap on the GPU
  *     (different streams, or different host threads on one device) race and
  *     corrupt each other's results: serialise them.
