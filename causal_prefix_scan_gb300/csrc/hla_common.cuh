@@ -23,12 +23,22 @@ namespace hla {
 // Sticky device-side status: set when a bounded wait expires.
 enum : unsigned { DEV_OK = 0u, DEV_TIMEOUT = 1u };
 
-// Upper bound on polls of a barrier or flag before a wait is declared failed.
-// With the sleep below this is several seconds, far beyond any legitimate wait.
+// Upper bound on polls of a flag (cross-CTA waits) before the wait is declared failed.
+// With the sleep in those loops this is several seconds, far beyond any legitimate wait.
 constexpr uint32_t kWaitLimit = 1u << 24;
+// Time limit of a barrier wait, in microseconds: far beyond any legitimate wait.
+constexpr uint32_t kWaitLimitUs = 2000000u;
+// Suspend hint of one barrier poll (ns): the polling thread sleeps in hardware until the
+// phase completes or this time passes, so waiting warps take no issue slots.
+constexpr uint32_t kSuspendNs = 1u << 20;
 
 HLA_DEVICE uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+HLA_DEVICE uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
 
 // ---------------------------------------------------------------- mbarrier
@@ -42,21 +52,25 @@ HLA_DEVICE void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
-HLA_DEVICE bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+// One poll: true once the phase with the given parity has completed; otherwise the
+// thread may sleep up to `hint_ns` (or until the phase completes) before it returns false.
+HLA_DEVICE bool mbar_try_wait(uint64_t *bar, uint32_t parity, uint32_t hint_ns = kSuspendNs) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase with the given parity to complete.  Returns false
-// (and raises the sticky flag) if it never does.
-HLA_DEVICE bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err, uint32_t limit = kWaitLimit) {
-    for (uint32_t i = 0; i < limit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;  // try_wait itself suspends briefly
-        if (i > 4096) __nanosleep(64);
+// Bounded wait for the phase with the given parity to complete.  Returns false (and
+// raises the sticky flag) if it does not within `limit_us` microseconds.
+HLA_DEVICE bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err, uint32_t limit_us = kWaitLimitUs) {
+    const uint32_t hint = limit_us * 1000u < kSuspendNs ? limit_us * 1000u : kSuspendNs;
+    if (mbar_try_wait(bar, parity, hint)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < (uint64_t)limit_us * 1000u) {
+        if (mbar_try_wait(bar, parity, hint)) return true;
     }
     atomicOr(err, DEV_TIMEOUT);
     return false;
@@ -112,6 +126,22 @@ HLA_DEVICE void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Warp-level forms: executed by all 32 lanes of a converged warp with warp-uniform
+// operands; elect.sync picks the one lane that issues.  Keeping the whole warp on the
+// issuing path lets the operands stay in uniform registers.
+HLA_DEVICE void umma_f16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+HLA_DEVICE void umma_commit_warp(uint64_t *bar) {
+    asm volatile(
+        "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar))
         : "memory");
 }
 // Arrive on `bar` once every previously issued tcgen05.mma of this thread completes.

@@ -1,7 +1,9 @@
 // hla_fwd_tc.cu -- host entry of the tensor-core forward: support check,
 // workspace size, and dispatch to the (decay, normalise, variant) launchers
-// compiled in hla_fwd_tc_f0..f11.cu.
-#include "hla_fwd_tc.cuh"
+// compiled in hla_fwd_tc_f0..f11.cu.  The masked variant at d = 64 runs the
+// warp-specialised kernel (hla_fwd_ws.cuh), every other shape and variant the
+// kernel of hla_fwd_tc.cuh.
+#include "hla_fwd_ws.cuh"
 
 namespace hla {
 namespace tc {
@@ -18,6 +20,12 @@ extern template cudaError_t launch_flags<true, true, 0>(const FwdArgs &, cudaStr
 extern template cudaError_t launch_flags<true, true, 1>(const FwdArgs &, cudaStream_t, int);
 extern template cudaError_t launch_flags<true, true, 2>(const FwdArgs &, cudaStream_t, int);
 }  // namespace tc
+namespace ws {
+extern template cudaError_t ws_launch_flags<false, false>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t ws_launch_flags<false, true>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t ws_launch_flags<true, false>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t ws_launch_flags<true, true>(const FwdArgs &, cudaStream_t, int);
+}  // namespace ws
 
 bool fwd_tc_supported(const hla_params &p) {
     auto ok = [](int x) { return x == 64 || x == 128; };
@@ -27,15 +35,27 @@ bool fwd_tc_supported(const hla_params &p) {
 
 size_t fwd_tc_workspace(const hla_params &p, int num_sms) {
     if (p.n == 0) return 0;
+    if (ws::ws_supported(p)) return ws::work_layout(p, ws::work_plan(p, num_sms)).total;
     return tc::ws_layout(p, tc::make_plan(p, num_sms)).total;
 }
 
 size_t fwd_tc_sync_bytes(const hla_params &p, int num_sms) {
     if (p.n == 0) return 0;
+    if (ws::ws_supported(p)) return ws::work_layout(p, ws::work_plan(p, num_sms)).off_summ;
     return tc::ws_layout(p, tc::make_plan(p, num_sms)).off_summ;
 }
 
 cudaError_t fwd_tc_launch(const FwdArgs &a, cudaStream_t st, int num_sms) {
+    const hla_params p{a.B, a.H, a.n, a.d, a.dv, a.chunk, a.in_dtype, a.flags, a.eps, a.gamma};
+    if (ws::ws_supported(p)) {
+        const int wkey = ((a.flags & HLA_DECAY) ? 2 : 0) + ((a.flags & HLA_NORMALIZE) ? 1 : 0);
+        switch (wkey) {
+            case 0: return ws::ws_launch_flags<false, false>(a, st, num_sms);
+            case 1: return ws::ws_launch_flags<false, true>(a, st, num_sms);
+            case 2: return ws::ws_launch_flags<true, false>(a, st, num_sms);
+            default: return ws::ws_launch_flags<true, true>(a, st, num_sms);
+        }
+    }
     const int var = (a.flags & HLA_UNMASKED) ? 1 : ((a.flags & HLA_ASYMMETRIC) ? 2 : 0);
     const int key = ((a.flags & HLA_DECAY) ? 6 : 0) + ((a.flags & HLA_NORMALIZE) ? 3 : 0) + var;
     switch (key) {
