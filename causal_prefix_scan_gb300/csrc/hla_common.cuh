@@ -307,4 +307,31 @@ HLA_DEVICE float ex2_approx(float y) {
 // g^x for x >= 0 with g in [0,1]; lg = log2(g) (may be -inf).  0^0 = 1.
 HLA_DEVICE float gpow(float lg, float x) { return x == 0.f ? 1.f : ex2_approx(lg * x); }
 
+// End of a kernel whose CTAs order themselves by a ticket and publish release flags:
+// the CTA that finishes last returns the two header counters (ticket, done) and the
+// flags to zero, so that the next call needs no clearing launch.  Every thread of the
+// CTA calls this once the CTA has read its last flag and its stores are complete; the
+// last CTA's threads share the clearing stores.  fb may be null.
+HLA_DEVICE void finish_grid(unsigned *ticket, unsigned *fa, unsigned *fb, int nflags, volatile unsigned *s_last) {
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned done = atomicAdd(ticket + 1, 1u);
+        __threadfence();
+        *s_last = (done == gridDim.x - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (*s_last) {
+        for (int i = threadIdx.x; i < nflags; i += blockDim.x) {
+            fa[i] = 0u;
+            if (fb) fb[i] = 0u;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            ticket[0] = 0u;
+            ticket[1] = 0u;
+            __threadfence();
+        }
+    }
+}
+
 }  // namespace hla

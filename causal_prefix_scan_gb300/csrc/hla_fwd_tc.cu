@@ -1,9 +1,10 @@
 // hla_fwd_tc.cu -- host entry of the tensor-core forward: support check,
 // workspace size, and dispatch to the (decay, normalise, variant) launchers
 // compiled in hla_fwd_tc_f0..f11.cu.  The masked variant at d = 64 runs the
-// warp-specialised kernel (hla_fwd_ws.cuh), every other shape and variant the
+// warp-specialised kernels: without decay on 128-token tiles (hla_fwd_ws2.cuh), with
+// decay on the caller's chunk (hla_fwd_ws.cuh); every other shape and variant runs the
 // kernel of hla_fwd_tc.cuh.
-#include "hla_fwd_ws.cuh"
+#include "hla_fwd_ws2.cuh"
 
 namespace hla {
 namespace tc {
@@ -26,6 +27,10 @@ extern template cudaError_t ws_launch_flags<false, true>(const FwdArgs &, cudaSt
 extern template cudaError_t ws_launch_flags<true, false>(const FwdArgs &, cudaStream_t, int);
 extern template cudaError_t ws_launch_flags<true, true>(const FwdArgs &, cudaStream_t, int);
 }  // namespace ws
+namespace ws2 {
+extern template cudaError_t launch_flags<false>(const FwdArgs &, cudaStream_t, int);
+extern template cudaError_t launch_flags<true>(const FwdArgs &, cudaStream_t, int);
+}  // namespace ws2
 
 bool fwd_tc_supported(const hla_params &p) {
     auto ok = [](int x) { return x == 64 || x == 128; };
@@ -35,18 +40,22 @@ bool fwd_tc_supported(const hla_params &p) {
 
 size_t fwd_tc_workspace(const hla_params &p, int num_sms) {
     if (p.n == 0) return 0;
+    if (ws2::ws2_supported(p)) return ws2::work_layout(p, ws2::work_plan(p, num_sms)).total;
     if (ws::ws_supported(p)) return ws::work_layout(p, ws::work_plan(p, num_sms)).total;
     return tc::ws_layout(p, tc::make_plan(p, num_sms)).total;
 }
 
 size_t fwd_tc_sync_bytes(const hla_params &p, int num_sms) {
     if (p.n == 0) return 0;
+    if (ws2::ws2_supported(p)) return ws2::work_layout(p, ws2::work_plan(p, num_sms)).off_summ;
     if (ws::ws_supported(p)) return ws::work_layout(p, ws::work_plan(p, num_sms)).off_summ;
     return tc::ws_layout(p, tc::make_plan(p, num_sms)).off_summ;
 }
 
 cudaError_t fwd_tc_launch(const FwdArgs &a, cudaStream_t st, int num_sms) {
     const hla_params p{a.B, a.H, a.n, a.d, a.dv, a.chunk, a.in_dtype, a.flags, a.eps, a.gamma};
+    if (ws2::ws2_supported(p))
+        return (a.flags & HLA_NORMALIZE) ? ws2::launch_flags<true>(a, st, num_sms) : ws2::launch_flags<false>(a, st, num_sms);
     if (ws::ws_supported(p)) {
         const int wkey = ((a.flags & HLA_DECAY) ? 2 : 0) + ((a.flags & HLA_NORMALIZE) ? 1 : 0);
         switch (wkey) {

@@ -1965,18 +1965,9 @@ struct Kern {
     }
 };
 
-// The last CTA to finish returns the workspace header and flags to zero, so the
-// next call needs no separate clearing launch.  Every CTA counts itself done
-// only after its last read of a flag.  Called by one thread per CTA.
-__device__ __forceinline__ void finish_cta(const TcParams &P) {
-    __threadfence();
-    const unsigned done = atomicAdd(P.ticket + 1, 1u);
-    if (done == gridDim.x - 1) {
-        for (int i = 0; i < P.BH * P.kmax; ++i) P.flagsw[i] = 0u;
-        P.ticket[0] = 0u;
-        P.ticket[1] = 0u;
-        __threadfence();
-    }
+// Every thread of the CTA, after its last read of a flag (finish_grid).
+__device__ __forceinline__ void finish_cta(const TcParams &P, volatile unsigned *s_last) {
+    finish_grid(P.ticket, P.flagsw, nullptr, P.BH * P.kmax, s_last);
 }
 
 template <int C, int D, int DV, bool DECAY, bool NORM, int VAR>
@@ -1990,6 +1981,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
     uint32_t *tmem_base_p = reinterpret_cast<uint32_t *>(base + K_::OFF_BAR + 32);
     int *ticket_p = reinterpret_cast<int *>(base + K_::OFF_BAR + 36);
     int *misalign_p = reinterpret_cast<int *>(base + K_::OFF_BAR + 40);
+    volatile unsigned *last_p = reinterpret_cast<volatile unsigned *>(base + K_::OFF_BAR + 44);
 
     Kern<C, D, DV, DECAY, NORM, VAR> x(P, base);
     x.tid = threadIdx.x;
@@ -2021,10 +2013,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
     }
     __syncthreads();
     if (*misalign_p) {  // cannot happen with no static shared memory; refuse rather than corrupt
-        if (x.tid == 0) {
-            atomicOr(P.err, DEV_TIMEOUT);
-            finish_cta(P);
-        }
+        if (x.tid == 0) atomicOr(P.err, DEV_TIMEOUT);
+        finish_cta(P, last_p);
         return;
     }
     if (x.warp == 0) {
@@ -2144,10 +2134,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
     __syncthreads();
     tc_fence_after();
     if (x.warp == 0) tmem_dealloc(x.tb, K_::TCOLS);
-    if (x.tid == 0) {
-        bulk_wait_all();  // the output stores are complete before the CTA counts itself done
-        finish_cta(P);
-    }
+    if (x.tid == 0) bulk_wait_all();  // the output stores are complete before the CTA counts itself done
+    finish_cta(P, last_p);
 }
 
 // ============================================================================ host side

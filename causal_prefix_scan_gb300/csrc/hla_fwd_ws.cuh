@@ -1267,18 +1267,9 @@ struct Fwd {
     }
 };
 
-__device__ __forceinline__ void finish_cta(const WsParams &P) {
-    __threadfence();
-    const unsigned done = atomicAdd(P.ticket + 1, 1u);
-    if (done == gridDim.x - 1) {
-        for (int i = 0; i < P.BH * P.kmax; ++i) {
-            P.flagA[i] = 0u;
-            P.flagB[i] = 0u;
-        }
-        P.ticket[0] = 0u;
-        P.ticket[1] = 0u;
-        __threadfence();
-    }
+// Every thread of the CTA, after its last read of a flag (finish_grid).
+__device__ __forceinline__ void finish_cta(const WsParams &P, volatile unsigned *s_last) {
+    finish_grid(P.ticket, P.flagA, P.flagB, P.BH * P.kmax, s_last);
 }
 
 template <int C, int D, int DV, bool DECAY, bool NORM>
@@ -1327,8 +1318,8 @@ __global__ void __launch_bounds__(kThreads, Lay<C, D, DV, DECAY, NORM>::CTAS)
         if (x.tid == 0) {
             atomicOr(P.err, DEV_TIMEOUT);
             atomicAdd(P.ticket, 1u);
-            finish_cta(P);
         }
+        finish_cta(P, misc + 4);
         return;
     }
     // TMEM first, then the ticket: a CTA that waits for TMEM holds no ticket that
@@ -1477,7 +1468,7 @@ __global__ void __launch_bounds__(kThreads, Lay<C, D, DV, DECAY, NORM>::CTAS)
     __syncthreads();
     tc_fence_after();
     if (x.warp == kWarpMma) tmem_dealloc(x.tb, L_::TCOLS);
-    if (x.tid == 0) finish_cta(P);
+    finish_cta(P, misc + 4);
 }
 
 // ============================================================================ host side
