@@ -46,7 +46,10 @@ def metric_for(w) -> str:
     return METRIC
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
-FWD_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd_tc.cuh")
+CSRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc")
+# source file of each forward kernel (its hash keys the committed DRAM traffic)
+FWD_KERNEL_SRCS = {"fwd_ws2_kernel": "hla_fwd_ws2.cuh", "fwd_ws_kernel": "hla_fwd_ws.cuh",
+                   "fwd_tc_kernel": "hla_fwd_tc.cuh", "fwd_simt_kernel": "hla_fwd_simt.cu"}
 DECODE_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_decode.cu")
 BWD_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_bwd_simt.cuh")
 BWD_METRIC = "masked 2nd-order HLA backward (dq, dk, dv) tokens/s and % roofline on 1 GB300"
@@ -494,7 +497,8 @@ def bench_forward(args, w: W.Workload, rank, world, local, dist):
            "replay": "CUDA graphs of up to 50 such steps (uploads, library calls, downloads and their "
                      "cross-stream order captured), replayed back to back"}
 
-    # ---- roofline of the (only) kernel of the step
+    # ---- roofline of the (only) kernel of the step, as the library names it
+    fwd_kernel = hla.hla_forward_kernel(params)
     peaks, peak_kind = load_peaks()
     bytes_launch = alg_bytes_per_launch(w)
     flops_launch = alg_flops_per_token_head(w) * w.token_heads
@@ -507,8 +511,8 @@ def bench_forward(args, w: W.Workload, rank, world, local, dist):
         ach, peak, unit, bound = flops_launch / t_launch / 1e12, peaks["bf16_tflops"], "TFLOP/s", "tensor"
     roofline = {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback",
-                "traffic": traffic_for("fwd_tc_kernel", w.name, FWD_KERNEL_SRC),
-                "kernel": "fwd_tc_kernel" if w.dtype == "bf16" else "fwd_simt_kernel",
+                "traffic": traffic_for(fwd_kernel, w.name, os.path.join(CSRC, FWD_KERNEL_SRCS[fwd_kernel])),
+                "kernel": fwd_kernel,
                 "alg_bytes_per_launch": bytes_launch, "alg_flops_per_launch": flops_launch,
                 "tensor_frac": (flops_launch / t_launch / 1e12) / peaks["bf16_tflops"],
                 "roofline_time_us": max(t_hbm, t_tc) * 1e6, "launch_time_us": t_launch * 1e6}

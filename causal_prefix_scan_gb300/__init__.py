@@ -27,8 +27,8 @@ __all__ = [
     "HLA_OK", "HLA_ERR_ARG", "HLA_ERR_UNSUPPORTED", "HLA_ERR_CUDA", "HLA_ERR_TIMEOUT",
     "HLA_F32", "HLA_BF16", "HLA_NORMALIZE", "HLA_DECAY", "HLA_UNMASKED", "HLA_ASYMMETRIC",
     "HlaError", "hla_params", "hla_state", "library", "EXPORTS",
-    "hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combine", "hla_decode_step",
-    "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
+    "hla_forward_workspace_size", "hla_forward_kernel", "hla_forward_chunked", "hla_state_combine",
+    "hla_decode_step", "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
     "hla_backward_workspace_size", "hla_backward_chunked", "hla_backward_chunked_traced",
     "hla_state3", "hla_forward3_workspace_size", "hla_forward3_chunked", "hla_forward3_chunked_traced",
     "hla_decode3_step", "State3", "forward3", "decode3_step", "hla_selftest_expired_wait",
@@ -40,7 +40,7 @@ EXPORTS = ("hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combi
            "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
            "hla_backward_workspace_size", "hla_backward_chunked", "hla_backward_chunked_traced",
            "hla_forward3_workspace_size", "hla_forward3_chunked", "hla_forward3_chunked_traced", "hla_decode3_step",
-           "hla_selftest_expired_wait")
+           "hla_selftest_expired_wait", "hla_forward_kernel")
 
 
 class HlaError(RuntimeError):
@@ -81,6 +81,8 @@ def library(path: str | None = None):
     i, u, f = ctypes.c_int, ctypes.c_uint, ctypes.c_float
     lib.hla_forward_workspace_size.argtypes = [P]
     lib.hla_forward_workspace_size.restype = sz
+    lib.hla_forward_kernel.argtypes = [P]
+    lib.hla_forward_kernel.restype = ctypes.c_char_p
     lib.hla_forward_chunked.argtypes = [P, vp, vp, vp, vp, S, S, vp, sz, vp]
     lib.hla_forward_chunked_noalloc.argtypes = [P, vp, vp, vp, vp, S, S, vp]
     lib.hla_forward_chunked_noalloc.restype = ctypes.c_int
@@ -154,6 +156,12 @@ def hla_last_error() -> str:
 
 def hla_forward_workspace_size(params: hla_params) -> int:
     return library().hla_forward_workspace_size(ctypes.byref(params))
+
+
+def hla_forward_kernel(params: hla_params):
+    """Name of the kernel the forward launches for these parameters (None: no launch)."""
+    r = library().hla_forward_kernel(ctypes.byref(params))
+    return r.decode() if r else None
 
 
 def hla_forward_chunked(params: hla_params, q, k, v, o, state_in=None, state_out=None, workspace=None,

@@ -118,6 +118,11 @@ size_t hla_forward_workspace_size(const hla_params *p) {
     return 0;
 }
 
+const char *hla_forward_kernel(const hla_params *p) {
+    if (check_params(p) != HLA_OK || p->n == 0) return nullptr;
+    return hla::fwd_tc_supported(*p) ? hla::fwd_tc_kernel_name(*p) : "fwd_simt_kernel";
+}
+
 hla_status hla_forward_chunked(const hla_params *p, const void *q, const void *k, const void *v, void *o,
                                const hla_state *state_in, const hla_state *state_out, void *workspace,
                                size_t workspace_bytes, void *stream) {

@@ -45,6 +45,12 @@ size_t fwd_tc_workspace(const hla_params &p, int num_sms) {
     return tc::ws_layout(p, tc::make_plan(p, num_sms)).total;
 }
 
+const char *fwd_tc_kernel_name(const hla_params &p) {
+    if (ws2::ws2_supported(p)) return "fwd_ws2_kernel";
+    if (ws::ws_supported(p)) return "fwd_ws_kernel";
+    return "fwd_tc_kernel";
+}
+
 size_t fwd_tc_sync_bytes(const hla_params &p, int num_sms) {
     if (p.n == 0) return 0;
     if (ws2::ws2_supported(p)) return ws2::work_layout(p, ws2::work_plan(p, num_sms)).off_summ;

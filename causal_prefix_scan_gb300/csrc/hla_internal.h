@@ -42,6 +42,7 @@ cudaError_t fwd_simt_launch(const FwdArgs &a, cudaStream_t st);
 // Tensor-core path (bf16 inputs; d, dv, chunk in {64,128}; asymmetric: dv <= d).
 bool fwd_tc_supported(const hla_params &p);
 size_t fwd_tc_workspace(const hla_params &p, int num_sms);
+const char *fwd_tc_kernel_name(const hla_params &p);
 // Bytes at the start of the tensor-core forward's workspace that must be zero when a
 // call starts (its ordering header and release flags); each call leaves them zero.
 size_t fwd_tc_sync_bytes(const hla_params &p, int num_sms);

@@ -127,6 +127,14 @@ typedef struct {
  * the exclusive scan and the flags that order it. */
 HLA_API size_t hla_forward_workspace_size(const hla_params *p);
 
+/* Name of the kernel hla_forward_chunked launches for these parameters on the
+ * current device: "fwd_ws2_kernel" (masked, no decay, bf16, d = dv = 64),
+ * "fwd_ws_kernel" (masked, bf16, d = 64, the other widths and decay),
+ * "fwd_tc_kernel" (other bf16 shapes) or "fwd_simt_kernel" (fp32 inputs).  NULL
+ * for invalid or unsupported parameters and for n = 0 (no launch).  The string is
+ * static; nothing is launched.  For tools that attribute measured time to a kernel. */
+HLA_API const char *hla_forward_kernel(const hla_params *p);
+
 /*
  * Masked second-order forward over n tokens for every (b,h) pair, by the
  * chunk-parallel scheme of section 4: per-segment summaries are combined with
