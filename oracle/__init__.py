@@ -79,9 +79,12 @@ def _load():
         _lib.hla_oracle_backward.argtypes = [i] * 7 + [d] + [dp] * 8 + [i]
         _lib.hla_oracle3_forward.argtypes = [i] * 6 + [dp] * 6 + [i]
         _lib.hla_oracle3_combine.argtypes = [i, i, i, dp, dp, dp]
+        _lib.hla_oracle3_forward_ex.argtypes = [i] * 6 + [dp, i, d] + [dp] * 6 + [i]
+        _lib.hla_oracle3_combine_ex.argtypes = [i, i, i, dp, dp, dp, dp]
         for f in (_lib.hla_oracle_forward, _lib.hla_oracle_forward_chunked,
                   _lib.hla_oracle_decode_step, _lib.hla_oracle_combine, _lib.hla_oracle_backward,
-                  _lib.hla_oracle3_forward, _lib.hla_oracle3_combine):
+                  _lib.hla_oracle3_forward, _lib.hla_oracle3_combine, _lib.hla_oracle3_forward_ex,
+                  _lib.hla_oracle3_combine_ex):
             f.restype = ctypes.c_int
     return _lib
 
@@ -266,35 +269,44 @@ def state3_unpack(buf: np.ndarray, units, d, dv) -> dict:
     return out
 
 
-def forward3(q, k, v, state_in=None, chunk=None, want_state=True, nthreads=None):
+def forward3(q, k, v, state_in=None, chunk=None, want_state=True, nthreads=None, gamma=None, normalize=False,
+             eps=1e-6):
     """Masked third-order HLA forward in fp64 (hla_oracle3.c): o_t = q_t^T T_t with
     T_t = S^K S^Q P - G1 - G2 + G3.  q, k: [B,H,n,d]; v: [B,H,n,dv].  chunk=None runs
     the serial recurrence in the moments and cross summaries; chunk=c the chunked scan
     over segment summaries (S^K, S^Q, P, T, M^QP, M^KQ; the other fields come back NaN).
+    gamma: [H] decay per head (every prefix moment decays by gamma per token; the
+    triple a, b, c <= t has weight gamma^(3t-a-b-c)) or None.  normalize: o = num /
+    (den + eps), den the output of unit values; the state then has dv + 1 value
+    columns, the unit column last (its P is the key mass m^K, its G1..G3 are h^(1..3)).
     state_in / the returned state: dict with the fields of STATE3_FIELDS, each
-    [B*H, d, d] or [B*H, d, dv] (T is derived and ignored on input).
+    [B*H, d, d] or [B*H, d, dve] (T is derived and ignored on input).
     Returns (o [B,H,n,dv], state or None)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, n, d = q.shape
     dv = v.shape[-1]
     assert k.shape == q.shape and v.shape == (B, H, n, dv)
+    dve = dv + (1 if normalize else 0)
     units = B * H
-    sin = state3_pack(state_in, units, d, dv) if state_in is not None else None
-    sout = np.zeros((units, 4 * d * d + 7 * d * dv)) if want_state else None
+    g = None if gamma is None else np.ascontiguousarray(np.asarray(gamma, np.float64).reshape(H))
+    sin = state3_pack(state_in, units, d, dve) if state_in is not None else None
+    sout = np.zeros((units, 4 * d * d + 7 * d * dve)) if want_state else None
     o = np.zeros((B, H, n, dv))
-    rc = _load().hla_oracle3_forward(B, H, n, d, dv, int(chunk or 0), _p(q), _p(k), _p(v), _p(sin), _p(o), _p(sout),
-                                     nthreads or default_threads())
+    rc = _load().hla_oracle3_forward_ex(B, H, n, d, dv, int(chunk or 0), _p(g), int(bool(normalize)), float(eps),
+                                        _p(q), _p(k), _p(v), _p(sin), _p(o), _p(sout), nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
-    return o, (state3_unpack(sout, units, d, dv) if want_state else None)
+    return o, (state3_unpack(sout, units, d, dve) if want_state else None)
 
 
-def combine3(A: dict, Bst: dict) -> dict:
-    """Concatenation of third-order segment summaries (A before B) for every item."""
+def combine3(A: dict, Bst: dict, decay_pow=None) -> dict:
+    """Concatenation of third-order segment summaries (A before B) for every item;
+    decay_pow: per item gamma^len(B), or None (no decay)."""
     units, d, dv = np.asarray(A["P"]).shape
     a, b = state3_pack(A, units, d, dv), state3_pack(Bst, units, d, dv)
     out = np.zeros_like(a)
-    rc = _load().hla_oracle3_combine(units, d, dv, _p(a), _p(b), _p(out))
+    f = None if decay_pow is None else np.ascontiguousarray(np.asarray(decay_pow, np.float64).reshape(units))
+    rc = _load().hla_oracle3_combine_ex(units, d, dv, _p(f), _p(a), _p(b), _p(out))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return state3_unpack(out, units, d, dv)

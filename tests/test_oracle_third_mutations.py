@@ -19,20 +19,19 @@ MUTATIONS = {
     "g3_sign": ("- q[i] * (s->G1[i * dv + j] + s->G2[i * dv + j] - s->G3[i * dv + j]);",
                 "- q[i] * (s->G1[i * dv + j] + s->G2[i * dv + j] + s->G3[i * dv + j]);"),
     # G2 without the term of the new key c = t against earlier queries
-    "g2_drops_term": ("s->G2[i * dv + j] += k[i] * kz2[j] + sksqk[i] * v[j];",
-                      "s->G2[i * dv + j] += k[i] * kz2[j];"),
+    "g2_drops_term": ("s->G2[i * dv + j] = g3 * s->G2[i * dv + j] + g2 * sksqk[i] * v[j] + k[i] * kz2[j];",
+                      "s->G2[i * dv + j] = g3 * s->G2[i * dv + j] + k[i] * kz2[j];"),
     # transposed auxiliary product in G1
     "z1_transposed": ("c += s->Z1[i * d + j] * k[j];", "c += s->Z1[j * d + i] * k[j];"),
     # G3 counts the triple a = c = t twice
-    "g3_double_count": ("+ z1tk[i] * v[j] - ksqk * k[i] * v[j];", "+ z1tk[i] * v[j];"),
+    "g3_double_count": ("+ z1tk[i] * v[j] - g * ksqk * k[i] * v[j];", "+ z1tk[i] * v[j];"),
 }
 
 MUTATIONS_SCAN = {
     # concatenation drops the S^K_A S^Q_B P_A cross term
-    "combine_drops_cross": ("B->MKQ[i * d + l] * A->P[l * dv + j] +\n                     SKSQ[i * d + l] * A->P[l * dv + j];",
-                            "B->MKQ[i * d + l] * A->P[l * dv + j];"),
+    "combine_drops_cross": ("+ f * t1 + f * t2 + f2 * t3;", "+ f * t1 + f * t2;"),
     # the cross term S^K_A M^QP_B taken with the later segment's key moment
-    "combine_wrong_segment": ("t += A->SK[i * d + l] * B->MQP[l * dv + j]", "t += B->SK[i * d + l] * B->MQP[l * dv + j]"),
+    "combine_wrong_segment": ("t1 += A->SK[i * d + l] * B->MQP[l * dv + j];", "t1 += B->SK[i * d + l] * B->MQP[l * dv + j];"),
     # M^QP composed with the wrong operand order (visible in the exported state)
     "mqp_order": ("acc += B->SQ[i * d + l] * A->P[l * dv + j];", "acc += A->SQ[i * d + l] * B->P[l * dv + j];"),
 }
