@@ -806,7 +806,7 @@ def bench_decode(args, dw: W.DecodeWorkload, rank, world, local, dist):
     def step(i, s):
         q, k, v = toks[i % T]
         if third:
-            hla.hla_decode3_step(N, d, dv, hla.HLA_BF16, st, q, k, v, o, s)
+            hla.hla_decode3_step(N, 1, d, dv, hla.HLA_BF16, 0, 0.0, None, st, q, k, v, o, s)
         else:
             hla.hla_decode_step(N, dw.H, 0, d, dv, hla.HLA_BF16, 0, 0.0, None, st, q, k, v, o, s)
 
@@ -856,7 +856,7 @@ def bench_decode(args, dw: W.DecodeWorkload, rank, world, local, dist):
         for _ in range(Ke):
             q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True); v.copy_(hv, non_blocking=True)
             if third:
-                hla.hla_decode3_step(N, d, dv, hla.HLA_BF16, st, q, k, v, o, stream)
+                hla.hla_decode3_step(N, 1, d, dv, hla.HLA_BF16, 0, 0.0, None, st, q, k, v, o, stream)
             else:
                 hla.hla_decode_step(N, dw.H, 0, d, dv, hla.HLA_BF16, 0, 0.0, None, st, q, k, v, o, stream)
             ho.copy_(o, non_blocking=True)

@@ -62,7 +62,8 @@ class hla_state(ctypes.Structure):
 
 
 class hla_state3(ctypes.Structure):
-    _fields_ = [("S", ctypes.c_void_p), ("P", ctypes.c_void_p), ("T", ctypes.c_void_p)]
+    _fields_ = [("S", ctypes.c_void_p), ("P", ctypes.c_void_p), ("T", ctypes.c_void_p),
+                ("m", ctypes.c_void_p), ("h", ctypes.c_void_p)]
 
 
 _lib = None
@@ -99,7 +100,7 @@ def library(path: str | None = None):
     lib.hla_forward3_chunked.argtypes = [P, vp, vp, vp, vp, S3, S3, vp, sz, vp]
     lib.hla_forward3_chunked_traced.argtypes = [P, vp, vp, vp, vp, S3, S3, vp, sz, vp,
                                                 ctypes.POINTER(ctypes.c_void_p)]
-    lib.hla_decode3_step.argtypes = [i, i, i, i, S3, vp, vp, vp, vp, vp]
+    lib.hla_decode3_step.argtypes = [i, i, i, i, i, u, f, vp, S3, vp, vp, vp, vp, vp]
     lib.hla_sync_status.argtypes = [vp]
     lib.hla_selftest_expired_wait.argtypes = [vp]
     for fn in (lib.hla_forward_chunked, lib.hla_state_combine, lib.hla_decode_step, lib.hla_sync_status,
@@ -218,7 +219,7 @@ def hla_backward_chunked_traced(params: hla_params, q, k, v, dout, dq, dk, dv, w
 def _state3_struct(st):
     if st is None:
         return None
-    return ctypes.byref(hla_state3(*(_ptr(x) for x in (st.S, st.P, st.T))))
+    return ctypes.byref(hla_state3(*(_ptr(x) for x in (st.S, st.P, st.T, st.m, st.h))))
 
 
 def _events(events):
@@ -248,9 +249,10 @@ def hla_forward3_chunked_traced(params: hla_params, q, k, v, o, state_in=None, s
                                                  _events(events)))
 
 
-def hla_decode3_step(N: int, d: int, dv: int, dtype: int, state, q, k, v, o, stream=None) -> None:
-    _check(library().hla_decode3_step(N, d, dv, dtype, _state3_struct(state), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
-                                      _stream(stream)))
+def hla_decode3_step(N: int, H: int, d: int, dv: int, dtype: int, flags: int, eps: float, gamma, state, q, k, v, o,
+                     stream=None) -> None:
+    _check(library().hla_decode3_step(N, H, d, dv, dtype, flags, eps, _ptr(gamma), _state3_struct(state), _ptr(q),
+                                      _ptr(k), _ptr(v), _ptr(o), _stream(stream)))
 
 
 def hla_selftest_expired_wait(stream=None) -> None:
@@ -292,22 +294,27 @@ class State:
 @dataclass
 class State3:
     """Third-order streaming state of `units` pairs, fp32: S [U,d,d] (key moment S^K),
-    P [U,d,dv] (key-value moment), T [U,d,dv] (masked third-order accumulator)."""
+    P [U,d,dv] (key-value moment), T [U,d,dv] (masked third-order accumulator); with
+    ratio normalisation also m [U,d] (key mass) and h [U,d] (T of a unit value)."""
     S: object
     P: object
     T: object
+    m: object = None
+    h: object = None
 
     @staticmethod
-    def empty(units: int, d: int, dv: int, device="cuda") -> "State3":
+    def empty(units: int, d: int, dv: int, device="cuda", normalize: bool = False) -> "State3":
         import torch
         z = lambda *s: torch.empty(*s, dtype=torch.float32, device=device)
-        return State3(z(units, d, d), z(units, d, dv), z(units, d, dv))
+        mh = (z(units, d), z(units, d)) if normalize else (None, None)
+        return State3(z(units, d, d), z(units, d, dv), z(units, d, dv), *mh)
 
     @staticmethod
-    def zeros(units: int, d: int, dv: int, device="cuda") -> "State3":
+    def zeros(units: int, d: int, dv: int, device="cuda", normalize: bool = False) -> "State3":
         import torch
         z = lambda *s: torch.zeros(*s, dtype=torch.float32, device=device)
-        return State3(z(units, d, d), z(units, d, dv), z(units, d, dv))
+        mh = (z(units, d), z(units, d)) if normalize else (None, None)
+        return State3(z(units, d, d), z(units, d, dv), z(units, d, dv), *mh)
 
 
 def _dtype_code(t) -> int:
@@ -398,25 +405,29 @@ def backward(q, k, v, dout, chunk: int, gamma=None, workspace=None, out=None, st
 
 
 def forward3(q, k, v, chunk: int, state_in: State3 | None = None, return_state: bool = False, out=None,
-             workspace=None, stream=None):
+             workspace=None, stream=None, gamma=None, normalize: bool = False, eps: float = 0.0):
     """Masked third-order HLA forward.  q, k [B,H,n,d], v [B,H,n,dv] contiguous CUDA
-    tensors (bf16 or fp32).  Returns o (and the final State3)."""
+    tensors (bf16 or fp32); gamma: [H] fp32 CUDA tensor of decay rates or None;
+    normalize: o = num / (den + eps).  Returns o (and the final State3)."""
     import torch
-    p = make_params(q, v, chunk)
+    p = make_params(q, v, chunk, gamma, normalize, eps)
     o = out if out is not None else torch.empty(q.shape[:3] + (v.shape[-1],), dtype=q.dtype, device=q.device)
     need = hla_forward3_workspace_size(p)
     if workspace is None and need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    st = State3.empty(p.B * p.H, p.d, p.dv, device=q.device) if return_state else None
+        workspace = new_workspace(need, device=q.device)
+    st = State3.empty(p.B * p.H, p.d, p.dv, device=q.device, normalize=normalize) if return_state else None
     hla_forward3_chunked(p, q, k, v, o, state_in, st, workspace, need if workspace is not None else 0, stream)
     return (o, st) if return_state else o
 
 
-def decode3_step(state: State3, q, k, v, out=None, stream=None):
-    """One third-order decode step for N pairs (q, k [N,d], v [N,dv]); state updated in place."""
+def decode3_step(state: State3, q, k, v, out=None, stream=None, H: int = 1, gamma=None, normalize: bool = False,
+                 eps: float = 0.0):
+    """One third-order decode step for N pairs (q, k [N,d], v [N,dv]); state updated in
+    place.  gamma: [H] decay rates (pair i uses gamma[i % H]) or None."""
     import torch
     N, d = q.shape
     dv = v.shape[-1]
     o = out if out is not None else torch.empty((N, dv), dtype=q.dtype, device=q.device)
-    hla_decode3_step(N, d, dv, _dtype_code(q), state, q, k, v, o, stream)
+    flags = (HLA_DECAY if gamma is not None else 0) | (HLA_NORMALIZE if normalize else 0)
+    hla_decode3_step(N, H, d, dv, _dtype_code(q), flags, float(eps), gamma, state, q, k, v, o, stream)
     return o

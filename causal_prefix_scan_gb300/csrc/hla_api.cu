@@ -269,17 +269,20 @@ hla_status check_fwd3_params(const hla_params *p) {
         return fail(HLA_ERR_ARG, "problem too large");
     if (!hla::fwd3_supported(*p))
         return fail(HLA_ERR_UNSUPPORTED,
-                    "third order supports flags 0, Hkv = H, d, dv, chunk in {16,32,64} "
+                    "third order supports flags HLA_DECAY, HLA_NORMALIZE, Hkv = H, d, dv, chunk in {16,32,64} "
                     "(got flags=%u Hkv=%d d=%d dv=%d chunk=%d)",
                     p->flags, p->Hkv, p->d, p->dv, p->chunk);
+    if ((p->flags & HLA_NORMALIZE) && !(p->eps >= 0.f)) return fail(HLA_ERR_ARG, "need eps >= 0");
+    if ((p->flags & HLA_DECAY) && !p->gamma) return fail(HLA_ERR_ARG, "HLA_DECAY needs gamma");
     return HLA_OK;
 }
 
-hla_status check_state3(const hla_state3 *s, const char *name) {
+hla_status check_state3(const hla_state3 *s, const char *name, bool normalize) {
     if (!s) return HLA_OK;
-    if (!s->S || !s->P || !s->T) return fail(HLA_ERR_ARG, "%s: all three pointers must be set", name);
+    if (!s->S || !s->P || !s->T) return fail(HLA_ERR_ARG, "%s: S, P, T must be set", name);
     if (!aligned16(s->S) || !aligned16(s->P) || !aligned16(s->T))
         return fail(HLA_ERR_ARG, "%s: pointers must be 16-byte aligned", name);
+    if (normalize && (!s->m || !s->h)) return fail(HLA_ERR_ARG, "%s: m and h must be set with HLA_NORMALIZE", name);
     return HLA_OK;
 }
 }  // namespace
@@ -301,20 +304,22 @@ hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const
                                        size_t workspace_bytes, void *stream, void *const *phase_events) {
     hla_status s = check_fwd3_params(p);
     if (s != HLA_OK) return s;
-    if ((s = check_state3(state_in, "state_in")) != HLA_OK) return s;
-    if ((s = check_state3(state_out, "state_out")) != HLA_OK) return s;
-    if (state_in && state_out && (state_in->S == state_out->S || state_in->P == state_out->P || state_in->T == state_out->T))
+    const bool norm = (p->flags & HLA_NORMALIZE) != 0;
+    if ((s = check_state3(state_in, "state_in", norm)) != HLA_OK) return s;
+    if ((s = check_state3(state_out, "state_out", norm)) != HLA_OK) return s;
+    if (state_in && state_out && (state_in->S == state_out->S || state_in->P == state_out->P || state_in->T == state_out->T ||
+                                  (norm && (state_in->m == state_out->m || state_in->h == state_out->h))))
         return fail(HLA_ERR_ARG, "state_out may not alias state_in");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (p->n == 0) {  // no tokens: state_out = state_in (or zeros)
         if (!state_out) return HLA_OK;
         const size_t BH = (size_t)p->B * p->H, D = p->d, DV = p->dv;
-        const size_t sz[3] = {BH * D * D * 4, BH * D * DV * 4, BH * D * DV * 4};
-        float *dst[3] = {state_out->S, state_out->P, state_out->T};
-        for (int i = 0; i < 3; ++i) {
+        const size_t sz[5] = {BH * D * D * 4, BH * D * DV * 4, BH * D * DV * 4, BH * D * 4, BH * D * 4};
+        float *dst[5] = {state_out->S, state_out->P, state_out->T, state_out->m, state_out->h};
+        for (int i = 0; i < (norm ? 5 : 3); ++i) {
             cudaError_t e;
             if (state_in) {
-                const float *src[3] = {state_in->S, state_in->P, state_in->T};
+                const float *src[5] = {state_in->S, state_in->P, state_in->T, state_in->m, state_in->h};
                 e = cudaMemcpyAsync(dst[i], src[i], sz[i], cudaMemcpyDeviceToDevice, st);
             } else {
                 e = cudaMemsetAsync(dst[i], 0, sz[i], st);
@@ -330,6 +335,8 @@ hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const
     if (!workspace || workspace_bytes < need)
         return fail(HLA_ERR_ARG, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
     if (!aligned16(workspace)) return fail(HLA_ERR_ARG, "workspace must be 16-byte aligned");
+    if (norm && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(HLA_ERR_ARG, "workspace must be 256-byte aligned with HLA_NORMALIZE");
     if (phase_events) {
         for (int i = 0; i < 4; ++i)
             if (!phase_events[i]) return fail(HLA_ERR_ARG, "phase_events must hold four events");
@@ -337,6 +344,7 @@ hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const
     hla::Fwd3Args a;
     a.B = p->B; a.H = p->H; a.n = p->n; a.d = p->d; a.dv = p->dv; a.chunk = p->chunk;
     a.in_dtype = p->in_dtype;
+    a.gamma = (p->flags & HLA_DECAY) ? p->gamma : nullptr;
     a.q = q; a.k = k; a.v = v; a.o = o;
     a.sin_S = state_in ? state_in->S : nullptr;
     a.sin_P = state_in ? state_in->P : nullptr;
@@ -348,22 +356,42 @@ hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const
     a.events = reinterpret_cast<cudaEvent_t const *>(phase_events);
     cudaError_t e = status_ptr(&a.err);
     if (e != cudaSuccess) return cuda_fail(e, "status word");
-    e = hla::fwd3_launch(a, st);
+    if (norm) {
+        hla::Norm3 nm;
+        nm.m_in = state_in ? state_in->m : nullptr;
+        nm.h_in = state_in ? state_in->h : nullptr;
+        nm.m_out = state_out ? state_out->m : nullptr;
+        nm.h_out = state_out ? state_out->h : nullptr;
+        nm.eps = p->eps;
+        e = hla::fwd3_norm_launch(a, nm, st);
+    } else {
+        e = hla::fwd3_launch(a, st);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "third-order forward launch");
     return HLA_OK;
 }
 
-hla_status hla_decode3_step(int N, int d, int dv, hla_dtype dtype, const hla_state3 *state, const void *q,
-                            const void *k, const void *v, void *o, void *stream) {
-    if (N < 0) return fail(HLA_ERR_ARG, "need N >= 0");
+hla_status hla_decode3_step(int N, int H, int d, int dv, hla_dtype dtype, unsigned flags, float eps,
+                            const float *gamma, const hla_state3 *state, const void *q, const void *k, const void *v,
+                            void *o, void *stream) {
+    if (N < 0 || H < 1) return fail(HLA_ERR_ARG, "need N >= 0, H >= 1");
     if (!width_ok(d) || !width_ok(dv)) return fail(HLA_ERR_UNSUPPORTED, "d, dv must be in {16,32,64,128}");
     if (dtype != HLA_F32 && dtype != HLA_BF16) return fail(HLA_ERR_ARG, "unknown dtype");
+    if (flags & ~(unsigned)(HLA_DECAY | HLA_NORMALIZE))
+        return fail(HLA_ERR_UNSUPPORTED, "third-order decode supports HLA_DECAY and HLA_NORMALIZE (got %u)", flags);
+    if ((flags & HLA_DECAY) && !gamma) return fail(HLA_ERR_ARG, "HLA_DECAY needs gamma");
+    const bool norm = (flags & HLA_NORMALIZE) != 0;
+    if (norm && !(eps >= 0.f)) return fail(HLA_ERR_ARG, "need eps >= 0");
     if (!state) return fail(HLA_ERR_ARG, "state must be set");
-    hla_status s = check_state3(state, "state");
+    hla_status s = check_state3(state, "state", norm);
     if (s != HLA_OK) return s;
     if (N > 0 && (!q || !k || !v || !o)) return fail(HLA_ERR_ARG, "q, k, v, o must be set");
     hla::Decode3Args a;
-    a.N = N; a.d = d; a.dv = dv; a.dtype = dtype;
+    a.N = N; a.H = H; a.d = d; a.dv = dv; a.dtype = dtype;
+    a.gamma = (flags & HLA_DECAY) ? gamma : nullptr;
+    a.eps = eps;
+    a.m = norm ? state->m : nullptr;
+    a.h = norm ? state->h : nullptr;
     a.S = state->S; a.P = state->P; a.T = state->T;
     a.q = q; a.k = k; a.v = v; a.o = o;
     cudaError_t e = hla::decode3_launch(a, static_cast<cudaStream_t>(stream));

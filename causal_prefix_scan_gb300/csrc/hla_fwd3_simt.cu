@@ -3,9 +3,12 @@
 // in hla_fwd3_<type>_c<chunk>.cu), and the third-order decode step.
 //
 // Decode step ("Higher-order Linear Attention", gist.science summary, section 3: the
-// online update of the third-order state), state (S^K, P, T) per pair:
-//   S^K_t = S^K + k k^T,  P_t = P + k v^T,  u = S^K_t q,  w = P_t^T q,
-//   T_t = T + u w^T,  o = T_t^T q = T^T q + (u.q) w.
+// online update of the third-order state), state (S^K, P, T) per pair, decay g per
+// token (1 without decay):
+//   S^K_t = g S^K + k k^T,  P_t = g P + k v^T,  u = S^K_t q,  w = P_t^T q,
+//   T_t = g^3 T + u w^T,  o = T_t^T q = g^3 T^T q + (u.q) w.
+// Ratio-normalised: the unit-value column of the state, the key mass m_t = g m + k and
+// h_t = g^3 h + u (m_t.q), gives den = h_t.q, and o = T_t^T q / (den + eps).
 // Each array is streamed once from HBM and written once.
 #include "hla_fwd3_simt.cuh"
 
@@ -48,9 +51,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode3_kernel(Decode3Args a) {
     __shared__ float qs[D], ks[D], us[D], vs[DV];
     __shared__ float4 redv[kThreads];
     __shared__ float4 wsum[CGV], ysum[CGV];
-    __shared__ float red[kThreads / 32];
+    __shared__ float red[kThreads / 32], red2[kThreads / 32];
     const int tid = threadIdx.x;
     const size_t u = blockIdx.x;
+    const float g = a.gamma ? a.gamma[u % a.H] : 1.f, g3 = g * g * g;
     const T *q = static_cast<const T *>(a.q) + u * D;
     const T *k = static_cast<const T *>(a.k) + u * D;
     const T *v = static_cast<const T *>(a.v) + u * DV;
@@ -90,7 +94,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode3_kernel(Decode3Args a) {
             const int c0 = (e % CG) * 4;
             const float kr = ks[row];
             float4 s = sv[i];
-            s.x += kr * ks[c0]; s.y += kr * ks[c0 + 1]; s.z += kr * ks[c0 + 2]; s.w += kr * ks[c0 + 3];
+            s.x = fmaf(g, s.x, kr * ks[c0]); s.y = fmaf(g, s.y, kr * ks[c0 + 1]);
+            s.z = fmaf(g, s.z, kr * ks[c0 + 2]); s.w = fmaf(g, s.w, kr * ks[c0 + 3]);
             S[e] = s;
             part = s.x * qs[c0] + s.y * qs[c0 + 1] + s.z * qs[c0 + 2] + s.w * qs[c0 + 3];
         }
@@ -114,12 +119,34 @@ __global__ void __launch_bounds__(kThreads, 3) decode3_kernel(Decode3Args a) {
             const int row = e / CGV, c0 = (e % CGV) * 4;
             const float kr = ks[row], qr = qs[row];
             float4 x = cv[i];
-            x.x += kr * vs[c0]; x.y += kr * vs[c0 + 1]; x.z += kr * vs[c0 + 2]; x.w += kr * vs[c0 + 3];
+            x.x = fmaf(g, x.x, kr * vs[c0]); x.y = fmaf(g, x.y, kr * vs[c0 + 1]);
+            x.z = fmaf(g, x.z, kr * vs[c0 + 2]); x.w = fmaf(g, x.w, kr * vs[c0 + 3]);
             P[e] = x;
             wp.x += qr * x.x; wp.y += qr * x.y; wp.z += qr * x.z; wp.w += qr * x.w;
         }
     }
     colsum(wp, wsum);  // also orders the writes of us[] before their reads
+    // ---- the unit-value column (ratio normalisation): m_t = g m + k, w1 = m_t.q,
+    // y1 = h.q, h_t = g^3 h + u w1
+    float w1 = 0.f, y1 = 0.f;
+    if (a.m) {
+        float pm = 0.f, ph = 0.f, hi = 0.f;
+        if (tid < D) {
+            const float mi = fmaf(g, a.m[u * D + tid], ks[tid]);
+            a.m[u * D + tid] = mi;
+            hi = a.h[u * D + tid];
+            pm = mi * qs[tid];
+            ph = hi * qs[tid];
+        }
+        pm = group_sum<32>(pm);
+        ph = group_sum<32>(ph);
+        if ((tid & 31) == 0) { red[tid >> 5] = pm; red2[tid >> 5] = ph; }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kThreads / 32; ++i) { w1 += red[i]; y1 += red2[i]; }
+        if (tid < D) a.h[u * D + tid] = fmaf(g3, hi, us[tid] * w1);
+        __syncthreads();  // red is reused below
+    }
     // ---- y = T^T q from T_{t-1};  T_t = T + u w^T
 #pragma unroll
     for (int i = 0; i < ITC; ++i) {
@@ -136,7 +163,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode3_kernel(Decode3Args a) {
             const float4 w = wsum[cg];
             float4 x = cv[i];
             yp.x += qr * x.x; yp.y += qr * x.y; yp.z += qr * x.z; yp.w += qr * x.w;
-            x.x += ur * w.x; x.y += ur * w.y; x.z += ur * w.z; x.w += ur * w.w;
+            x.x = fmaf(g3, x.x, ur * w.x); x.y = fmaf(g3, x.y, ur * w.y);
+            x.z = fmaf(g3, x.z, ur * w.z); x.w = fmaf(g3, x.w, ur * w.w);
             Tm[e] = x;
         }
     }
@@ -150,11 +178,12 @@ __global__ void __launch_bounds__(kThreads, 3) decode3_kernel(Decode3Args a) {
     float uq = 0.f;
 #pragma unroll
     for (int i = 0; i < kThreads / 32; ++i) uq += red[i];
+    const float inv = a.m ? 1.f / (fmaf(g3, y1, uq * w1) + a.eps) : 1.f;
     T *o = static_cast<T *>(a.o) + u * DV;
     for (int j = tid; j < DV; j += kThreads) {
         const float *w = reinterpret_cast<const float *>(&wsum[j >> 2]);
         const float *y = reinterpret_cast<const float *>(&ysum[j >> 2]);
-        st_t(o, j, y[j & 3] + uq * w[j & 3]);
+        st_t(o, j, fmaf(g3, y[j & 3], uq * w[j & 3]) * inv);
     }
 }
 
@@ -189,17 +218,130 @@ cudaError_t decode3_d(const Decode3Args &a, cudaStream_t st) {
 bool fwd3_supported(const hla_params &p) {
     auto ok = [](int x) { return x == 16 || x == 32 || x == 64; };
     const int hkv = p.Hkv > 0 ? p.Hkv : p.H;
-    return ok(p.d) && ok(p.dv) && ok(p.chunk) && hkv == p.H && p.flags == 0;
+    return ok(p.d) && ok(p.dv) && ok(p.chunk) && hkv == p.H && (p.flags & ~(unsigned)(HLA_DECAY | HLA_NORMALIZE)) == 0;
 }
 
-size_t fwd3_workspace(const hla_params &p) {
+namespace fwd3 {
+namespace {
+size_t pass_workspace(const hla_params &p, int dv) {
     const size_t nch = ((size_t)p.n + p.chunk - 1) / p.chunk;
-    const fwd3::Ws3 w{p.d, p.dv};
+    const Ws3 w{p.d, dv};
     return (size_t)p.B * p.H * nch * (w.loc_floats() + w.st_floats()) * sizeof(float);
+}
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr int kUnit = 16;  // width of the unit-value tile of the denominator pass
+
+// Workspace of the ratio-normalised forward: the passes' scratch (shared: the passes
+// run one after the other), the unit-value tile E and the denominator output (element
+// type of the inputs, [rows][16], a one in column 0 of E), and the denominator pass's
+// states (P and T of width 16 before and after, S after).
+struct NormWs {
+    size_t pass, e, den, pin, tin, pout, tout, sscr, total;
+};
+NormWs norm_ws(const hla_params &p) {
+    NormWs w;
+    const size_t rows = (size_t)p.B * p.H * p.n, units = (size_t)p.B * p.H, esz = p.in_dtype == HLA_F32 ? 4 : 2;
+    const size_t a = pass_workspace(p, p.dv), b = pass_workspace(p, kUnit);
+    size_t o = 0;
+    auto take = [&](size_t bytes) { const size_t at = o; o = align256(o + bytes); return at; };
+    w.pass = take(a > b ? a : b);
+    w.e = take(rows * kUnit * esz);
+    w.den = take(rows * kUnit * esz);
+    w.pin = take(units * p.d * kUnit * 4);
+    w.tin = take(units * p.d * kUnit * 4);
+    w.pout = take(units * p.d * kUnit * 4);
+    w.tout = take(units * p.d * kUnit * 4);
+    w.sscr = take(units * (size_t)p.d * p.d * 4);
+    w.total = o;
+    return w;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) unit_tile_kernel(T *e, size_t rows) {
+    for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < rows * kUnit; i += (size_t)gridDim.x * kThreads)
+        st_t(e, i, (i % kUnit) == 0 ? 1.f : 0.f);
+}
+// d-vectors per pair <-> column 0 of [d][16] tiles (the other columns zero)
+__global__ void __launch_bounds__(kThreads) to_column_kernel(float *dst, const float *src, size_t count) {
+    for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < count * kUnit; i += (size_t)gridDim.x * kThreads)
+        dst[i] = (i % kUnit) == 0 ? src[i / kUnit] : 0.f;
+}
+__global__ void __launch_bounds__(kThreads) from_column_kernel(float *dst, const float *src, size_t count) {
+    for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < count; i += (size_t)gridDim.x * kThreads)
+        dst[i] = src[i * kUnit];
+}
+// o = num / (den + eps), row by row (num is o itself)
+template <typename T>
+__global__ void __launch_bounds__(kThreads) ratio_kernel(T *o, const T *den, size_t rows, int dv, float eps) {
+    for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < rows * dv; i += (size_t)gridDim.x * kThreads) {
+        const size_t r = i / dv;
+        st_t(o, i, ld_t(o, i) / (ld_t(den, r * kUnit) + eps));
+    }
+}
+int grid_for(size_t work) {
+    const size_t b = (work + kThreads - 1) / kThreads;
+    return (int)(b < 4096 ? (b > 0 ? b : 1) : 4096);
+}
+
+template <typename T>
+cudaError_t norm_t(const Fwd3Args &a0, const Norm3 &nm, cudaStream_t st) {
+    hla_params p{};
+    p.B = a0.B; p.H = a0.H; p.n = a0.n; p.d = a0.d; p.dv = a0.dv; p.chunk = a0.chunk; p.in_dtype = a0.in_dtype;
+    const NormWs w = norm_ws(p);
+    uint8_t *base = reinterpret_cast<uint8_t *>(a0.workspace);
+    auto f = [&](size_t off) { return reinterpret_cast<float *>(base + off); };
+    const size_t rows = (size_t)a0.B * a0.H * a0.n, pd = (size_t)a0.B * a0.H * a0.d;
+    T *E = reinterpret_cast<T *>(base + w.e), *den = reinterpret_cast<T *>(base + w.den);
+    cudaError_t e;
+    auto mark = [&](int i) { return a0.events ? cudaEventRecord(a0.events[i], st) : cudaSuccess; };
+    if ((e = mark(0)) != cudaSuccess) return e;
+    unit_tile_kernel<T><<<grid_for(rows * kUnit), kThreads, 0, st>>>(E, rows);
+    if (nm.m_in) {
+        to_column_kernel<<<grid_for(pd * kUnit), kThreads, 0, st>>>(f(w.pin), nm.m_in, pd);
+        to_column_kernel<<<grid_for(pd * kUnit), kThreads, 0, st>>>(f(w.tin), nm.h_in, pd);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // numerator: the forward of the values, into o
+    Fwd3Args a = a0;
+    a.events = nullptr;
+    a.workspace = f(w.pass);
+    if ((e = launch_c<T>(a, st)) != cudaSuccess) return e;
+    if ((e = mark(1)) != cudaSuccess) return e;
+    // denominator: the forward of the unit values, same S
+    Fwd3Args b = a;
+    b.dv = kUnit;
+    b.v = E;
+    b.o = den;
+    b.sin_P = nm.m_in ? f(w.pin) : nullptr;
+    b.sin_T = nm.m_in ? f(w.tin) : nullptr;
+    if (!a0.sin_S) b.sin_P = b.sin_T = nullptr;
+    b.sout_S = nm.m_out ? f(w.sscr) : nullptr;
+    b.sout_P = nm.m_out ? f(w.pout) : nullptr;
+    b.sout_T = nm.m_out ? f(w.tout) : nullptr;
+    if ((e = launch_c<T>(b, st)) != cudaSuccess) return e;
+    if ((e = mark(2)) != cudaSuccess) return e;
+    ratio_kernel<T><<<grid_for(rows * a0.dv), kThreads, 0, st>>>(static_cast<T *>(a0.o), den, rows, a0.dv, nm.eps);
+    if (nm.m_out) {
+        from_column_kernel<<<grid_for(pd), kThreads, 0, st>>>(nm.m_out, f(w.pout), pd);
+        from_column_kernel<<<grid_for(pd), kThreads, 0, st>>>(nm.h_out, f(w.tout), pd);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return mark(3);
+}
+}  // namespace
+}  // namespace fwd3
+
+size_t fwd3_workspace(const hla_params &p) {
+    if (p.flags & HLA_NORMALIZE) return fwd3::norm_ws(p).total;
+    return fwd3::pass_workspace(p, p.dv);
 }
 
 cudaError_t fwd3_launch(const Fwd3Args &a, cudaStream_t st) {
     return a.in_dtype == HLA_F32 ? fwd3::launch_c<float>(a, st) : fwd3::launch_c<__nv_bfloat16>(a, st);
+}
+
+cudaError_t fwd3_norm_launch(const Fwd3Args &a, const Norm3 &nm, cudaStream_t st) {
+    return a.in_dtype == HLA_F32 ? fwd3::norm_t<float>(a, nm, st) : fwd3::norm_t<__nv_bfloat16>(a, nm, st);
 }
 
 cudaError_t decode3_launch(const Decode3Args &a, cudaStream_t st) {

@@ -17,6 +17,16 @@
 // with the chunk-local sums (from a zero prefix, U and W without their first terms)
 //   S^K = K^T K,  S^Q = Q^T Q,  P = K^T V,  T = U^T W,  M^QP = Q^T W,  M^KQ = U^T Q.
 //
+// Exponential decay (per head, g; every prefix moment decays by g per token, so the
+// triple a, b, c <= t weighs g^(3t-a-b-c)): with G[t][s] = g^(t-s) and tau the token's
+// index in its chunk,
+//   A~ = G o tril(Q K^T),  U = diag(g^(tau+1)) Q S^K_p + A~ K,  W = diag(g^(tau+1)) Q P_p + A~ V,
+//   M = G^3 o tril(Q U^T),  O = diag(g^(3(tau+1))) Q T_p + M W;
+// the local sums weight token b by g^(e-b) (S^K, S^Q, P), g^(3(e-b)) (T) and
+// g^(2(e-b)) (M^QP, M^KQ), e the chunk's last token; a chunk of L tokens composes with
+// f = g^L:  S^K = f S^K_A + S^K_B (P likewise),  X = M^QP_B + f S^Q_B P_A,
+//   T = f^3 T_A + T_B + f M^KQ_B P_A + f S^K_A X.
+//
 // Three launches: (1) one CTA per chunk writes the local sums; (2) the scan, one CTA
 // per (b,h) and column block of dv, walks the chunks and writes each chunk's prefix
 // state (and the final state); (3) one CTA per chunk forms the outputs.  For bf16
@@ -62,11 +72,19 @@ struct Ws3 {
 };
 
 // ---- (1) chunk-local sums --------------------------------------------------------
+// Powers g^x, x = 0 .. 3C (gp[x]); all ones without decay.
+constexpr int gp_count(int C) { return 3 * C + 4; }
+__device__ __forceinline__ void fill_powers(float *gp, int count, const Fwd3Args &a, int u) {
+    const bool decay = a.gamma != nullptr;
+    const float lg = decay ? log2f(a.gamma[u % a.H]) : 0.f;
+    for (int x = threadIdx.x; x < count; x += kThreads) gp[x] = decay ? gpow(lg, (float)x) : 1.f;
+}
+
 template <int C, int D, int DV>
 struct LocSmem3 {
     static constexpr int LQ = D + 4, LV = DV + 4, LT = C + 4;
     static constexpr int Q = 0, K = Q + C * LQ, V = K + C * LQ, A = V + C * LV, U = A + C * LT, W = U + C * LQ,
-                         TOTAL = W + C * LV;
+                         GP = W + C * LV, W1 = GP + gp_count(C), W2 = W1 + C, W3 = W2 + C, TOTAL = W3 + C;
 };
 
 template <typename T, int C, int D, int DV>
@@ -74,16 +92,25 @@ __global__ void __launch_bounds__(kThreads) fwd3_local_kernel(Fwd3Args a) {
     using Sm = LocSmem3<C, D, DV>;
     extern __shared__ __align__(16) float sm[];
     float *Q = sm + Sm::Q, *K = sm + Sm::K, *V = sm + Sm::V, *A = sm + Sm::A, *U = sm + Sm::U, *W = sm + Sm::W;
+    float *gp = sm + Sm::GP, *w1 = sm + Sm::W1, *w2 = sm + Sm::W2, *w3 = sm + Sm::W3;
     const int nch = (a.n + C - 1) / C, u = blockIdx.x / nch, ch = blockIdx.x % nch;
     const int t0 = ch * C, L = min(C, a.n - t0);
     const size_t rq = ((size_t)u * a.n + t0) * D, rv = ((size_t)u * a.n + t0) * DV;
+    fill_powers(gp, gp_count(C), a, u);
     load_rows<D>(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L);
     load_rows<D>(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L);
     load_rows<DV>(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L);
     __syncthreads();
+    // token weights of the local sums, relative to the chunk's last token e = L - 1
+    for (int b = threadIdx.x; b < C; b += kThreads) {
+        const int x = b < L ? L - 1 - b : 0;
+        w1[b] = gp[x];
+        w2[b] = gp[2 * x];
+        w3[b] = gp[3 * x];
+    }
     tiles<true, C, C>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, true>(acc, Q, Sm::LQ, K, Sm::LQ, m0, n0, ns, D);
-        each(acc, m0, n0, ns, [&](int t, int s, float x) { A[t * Sm::LT + s] = s <= t ? x : 0.f; });
+        each(acc, m0, n0, ns, [&](int t, int s, float x) { A[t * Sm::LT + s] = s <= t ? gp[t - s] * x : 0.f; });
     });
     __syncthreads();
     // U = A~ K, W = A~ V (no earlier state)
@@ -103,27 +130,27 @@ __global__ void __launch_bounds__(kThreads) fwd3_local_kernel(Fwd3Args a) {
     };
     // rows past the chunk's last token are zero in Q, K, V, U, W
     tiles<false, D, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
-        mac<true, false>(acc, K, Sm::LQ, K, Sm::LQ, m0, n0, ns, C);
+        mac<true, false>(acc, K, Sm::LQ, K, Sm::LQ, m0, n0, ns, C, w1);
         each(acc, m0, n0, ns, put(ws.o_sk(), D));
     });
     tiles<false, D, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
-        mac<true, false>(acc, Q, Sm::LQ, Q, Sm::LQ, m0, n0, ns, C);
+        mac<true, false>(acc, Q, Sm::LQ, Q, Sm::LQ, m0, n0, ns, C, w1);
         each(acc, m0, n0, ns, put(ws.o_sq(), D));
     });
     tiles<false, D, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
-        mac<true, false>(acc, U, Sm::LQ, Q, Sm::LQ, m0, n0, ns, C);
+        mac<true, false>(acc, U, Sm::LQ, Q, Sm::LQ, m0, n0, ns, C, w2);
         each(acc, m0, n0, ns, put(ws.o_mkq(), D));
     });
     tiles<false, D, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
-        mac<true, false>(acc, K, Sm::LQ, V, Sm::LV, m0, n0, ns, C);
+        mac<true, false>(acc, K, Sm::LQ, V, Sm::LV, m0, n0, ns, C, w1);
         each(acc, m0, n0, ns, put(ws.o_p(), DV));
     });
     tiles<false, D, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
-        mac<true, false>(acc, U, Sm::LQ, W, Sm::LV, m0, n0, ns, C);
+        mac<true, false>(acc, U, Sm::LQ, W, Sm::LV, m0, n0, ns, C, w3);
         each(acc, m0, n0, ns, put(ws.o_t(), DV));
     });
     tiles<false, D, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
-        mac<true, false>(acc, Q, Sm::LQ, W, Sm::LV, m0, n0, ns, C);
+        mac<true, false>(acc, Q, Sm::LQ, W, Sm::LV, m0, n0, ns, C, w2);
         each(acc, m0, n0, ns, put(ws.o_mqp(), DV));
     });
 }
@@ -157,6 +184,8 @@ __global__ void __launch_bounds__(kThreads) fwd3_scan_kernel(Fwd3Args a) {
     constexpr int ROWS = D / kSplit;
     const int r0 = part * ROWS;
     const Ws3 ws{D, DV};
+    const bool decay = a.gamma != nullptr;
+    const float lg = decay ? log2f(a.gamma[u % a.H]) : 0.f;
     const float *loc = a.workspace + (size_t)u * nch * ws.loc_floats();
     float *st = a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + (size_t)u * nch * ws.st_floats();
     auto issue = [&](int ch) {  // the local sums of chunk ch into buffer ch & 1
@@ -200,29 +229,31 @@ __global__ void __launch_bounds__(kThreads) fwd3_scan_kernel(Fwd3Args a) {
         const float *b = sm + Sm::BUF + (ch & 1) * Sm::BUFSZ;
         const float *SKl = b + Sm::B_SK, *SQl = b + Sm::B_SQ, *MKQl = b + Sm::B_MKQ;
         const float *Pl = b + Sm::B_P, *Tl = b + Sm::B_T, *MQPl = b + Sm::B_MQP;
+        const int L = min(C, a.n - ch * C);
+        const float f = decay ? gpow(lg, (float)L) : 1.f, f3 = f * f * f;
         // S^Q_B P_A and M^KQ_B P_A (block columns), each over all threads
         mac_ksplit<D, NB, D>(SQl, LF, Pb, LB, red1);
         mac_ksplit<D, NB, D>(MKQl, LF, Pb, LB, red2);
         __syncthreads();
-        // X = M^QP_B + S^Q_B P_A,  Y = M^KQ_B P_A
+        // X = M^QP_B + f S^Q_B P_A,  Y = M^KQ_B P_A
         for (int e = threadIdx.x; e < D * NB; e += kThreads) {
             const int o = (e / NB) * LB + e % NB;
-            X[o] = MQPl[o] + ksplit_sum<D, NB, D>(red1, e);
+            X[o] = MQPl[o] + f * ksplit_sum<D, NB, D>(red1, e);
             Y[o] = ksplit_sum<D, NB, D>(red2, e);
         }
         __syncthreads();
-        // T <- T + T_B + S^K_A X + Y
+        // T <- f^3 T + T_B + f Y + f S^K_A X
         mac_ksplit<D, NB, D>(SK, LF, X, LB, red1);
         __syncthreads();
         for (int e = threadIdx.x; e < D * NB; e += kThreads) {
             const int o = (e / NB) * LB + e % NB;
-            Tb[o] += Tl[o] + Y[o] + ksplit_sum<D, NB, D>(red1, e);
-            Pb[o] += Pl[o];  // P <- P + P_B (read above only, before this barrier)
+            Tb[o] = f3 * Tb[o] + Tl[o] + f * (Y[o] + ksplit_sum<D, NB, D>(red1, e));
+            Pb[o] = f * Pb[o] + Pl[o];  // P <- f P + P_B (read above only, before this barrier)
         }
-        // S^K <- S^K + S^K_B
+        // S^K <- f S^K + S^K_B
         for (int e = threadIdx.x; e < D * D; e += kThreads) {
             const int r = e / D, x = e % D;
-            SK[r * LF + x] += SKl[r * LF + x];
+            SK[r * LF + x] = f * SK[r * LF + x] + SKl[r * LF + x];
         }
         __syncthreads();
     }
@@ -247,7 +278,8 @@ template <int C, int D, int DV>
 struct OutSmem3 {
     static constexpr int LQ = D + 4, LV = DV + 4, LT = C + 4;
     static constexpr int Q = 0, K = Q + C * LQ, V = K + C * LQ, SK = V + C * LV, P = SK + D * LQ, TP = P + D * LV,
-                         A = TP + D * LV, M = A + C * LT, U = M + C * LT, W = U + C * LQ, TOTAL = W + C * LV;
+                         A = TP + D * LV, M = A + C * LT, U = M + C * LT, W = U + C * LQ, GP = W + C * LV,
+                         R1 = GP + gp_count(C), R3 = R1 + C, TOTAL = R3 + C;
 };
 
 template <typename T, int C, int D, int DV>
@@ -256,10 +288,12 @@ __global__ void __launch_bounds__(kThreads) fwd3_out_kernel(Fwd3Args a) {
     extern __shared__ __align__(16) float sm[];
     float *Q = sm + Sm::Q, *K = sm + Sm::K, *V = sm + Sm::V, *SK = sm + Sm::SK, *P = sm + Sm::P, *Tp = sm + Sm::TP;
     float *A = sm + Sm::A, *M = sm + Sm::M, *U = sm + Sm::U, *W = sm + Sm::W;
+    float *gp = sm + Sm::GP, *r1 = sm + Sm::R1, *r3 = sm + Sm::R3;
     const int nch = (a.n + C - 1) / C, u = blockIdx.x / nch, ch = blockIdx.x % nch;
     const int t0 = ch * C, L = min(C, a.n - t0);
     const size_t rq = ((size_t)u * a.n + t0) * D, rv = ((size_t)u * a.n + t0) * DV;
     const Ws3 ws{D, DV};
+    fill_powers(gp, gp_count(C), a, u);
     const float *so =
         a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
     // the prefix state arrives asynchronously while A~ is formed
@@ -271,34 +305,38 @@ __global__ void __launch_bounds__(kThreads) fwd3_out_kernel(Fwd3Args a) {
     load_rows<D>(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L);
     load_rows<DV>(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L);
     __syncthreads();
+    for (int t = threadIdx.x; t < C; t += kThreads) {  // row scales of the prefix-state terms
+        r1[t] = gp[t + 1];
+        r3[t] = gp[3 * (t + 1)];
+    }
     tiles<true, C, C>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, true>(acc, Q, Sm::LQ, K, Sm::LQ, m0, n0, ns, D);
-        each(acc, m0, n0, ns, [&](int t, int s, float x) { A[t * Sm::LT + s] = s <= t ? x : 0.f; });
+        each(acc, m0, n0, ns, [&](int t, int s, float x) { A[t * Sm::LT + s] = s <= t ? gp[t - s] * x : 0.f; });
     });
     cp_async_wait<0>();
     __syncthreads();
-    // U = Q S^K_p + A~ K;  W = Q P_p + A~ V
+    // U = diag(g^(tau+1)) Q S^K_p + A~ K;  W = diag(g^(tau+1)) Q P_p + A~ V
     tiles<false, C, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
-        mac<false, false>(acc, Q, Sm::LQ, SK, Sm::LQ, m0, n0, ns, D);
+        mac_rs<false, false>(acc, r1, Q, Sm::LQ, SK, Sm::LQ, m0, n0, ns, D);
         mac<false, false>(acc, A, Sm::LT, K, Sm::LQ, m0, n0, ns, C);
         each(acc, m0, n0, ns, [&](int t, int i, float x) { U[t * Sm::LQ + i] = x; });
     });
     tiles<false, C, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
-        mac<false, false>(acc, Q, Sm::LQ, P, Sm::LV, m0, n0, ns, D);
+        mac_rs<false, false>(acc, r1, Q, Sm::LQ, P, Sm::LV, m0, n0, ns, D);
         mac<false, false>(acc, A, Sm::LT, V, Sm::LV, m0, n0, ns, C);
         each(acc, m0, n0, ns, [&](int t, int j, float x) { W[t * Sm::LV + j] = x; });
     });
     __syncthreads();
-    // M = tril(Q U^T)
+    // M = G^3 o tril(Q U^T)
     tiles<true, C, C>([&](float (&acc)[4][4], int m0, int n0, int ns) {
         mac<false, true>(acc, Q, Sm::LQ, U, Sm::LQ, m0, n0, ns, D);
-        each(acc, m0, n0, ns, [&](int t, int b, float x) { M[t * Sm::LT + b] = b <= t ? x : 0.f; });
+        each(acc, m0, n0, ns, [&](int t, int b, float x) { M[t * Sm::LT + b] = b <= t ? gp[3 * (t - b)] * x : 0.f; });
     });
     __syncthreads();
-    // O = Q T_p + M W
+    // O = diag(g^(3(tau+1))) Q T_p + M W
     T *o = static_cast<T *>(a.o) + rv;
     tiles<false, C, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
-        mac<false, false>(acc, Q, Sm::LQ, Tp, Sm::LV, m0, n0, ns, D);
+        mac_rs<false, false>(acc, r3, Q, Sm::LQ, Tp, Sm::LV, m0, n0, ns, D);
         mac<false, false>(acc, M, Sm::LT, W, Sm::LV, m0, n0, ns, C);
         each(acc, m0, n0, ns, [&](int t, int j, float x) {
             if (t < L) st_t(o, (size_t)t * DV + j, x);
@@ -317,27 +355,29 @@ cudaError_t launch_t(const Fwd3Args &a, cudaStream_t st) {
     const size_t b1 = LocSmem3<C, D, DV>::TOTAL * sizeof(float), b2 = ScanSmem3<C, D, DV>::TOTAL * sizeof(float),
                  b3 = OutSmem3<C, D, DV>::TOTAL * sizeof(float);
     cudaError_t e;
-    constexpr bool TC = std::is_same<T, __nv_bfloat16>::value && C == 64 && D == 64 && DV == 64;
-    if constexpr (!TC) {  // the CUDA-core kernels (the tensor-core ones set their own attributes)
+    // the tensor-core kernels: bf16 at 64/64/64 without decay
+    constexpr bool TC_SHAPE = std::is_same<T, __nv_bfloat16>::value && C == 64 && D == 64 && DV == 64;
+    const bool tc = TC_SHAPE && a.gamma == nullptr;
+    if (!tc) {  // the CUDA-core kernels (the tensor-core ones set their own attributes)
         if ((e = smem_attr(fwd3_local_kernel<T, C, D, DV>, b1)) != cudaSuccess) return e;
         if ((e = smem_attr(fwd3_scan_kernel<C, D, DV>, b2)) != cudaSuccess) return e;
         if ((e = smem_attr(fwd3_out_kernel<T, C, D, DV>, b3)) != cudaSuccess) return e;
     }
     auto mark = [&](int i) { return a.events ? cudaEventRecord(a.events[i], st) : cudaSuccess; };
     if ((e = mark(0)) != cudaSuccess) return e;
-    if constexpr (TC) {
+    if (tc) {
         if ((e = fwd3tc::local_tc(a, st)) != cudaSuccess) return e;
     } else {
         fwd3_local_kernel<T, C, D, DV><<<units * nch, kThreads, b1, st>>>(a);
     }
     if ((e = mark(1)) != cudaSuccess) return e;
-    if constexpr (TC) {
+    if (tc) {
         if ((e = scantc::fwd3_scan(a, st)) != cudaSuccess) return e;
     } else {
         fwd3_scan_kernel<C, D, DV><<<units * kSplit, kThreads, b2, st>>>(a);
     }
     if ((e = mark(2)) != cudaSuccess) return e;
-    if constexpr (TC) {
+    if (tc) {
         if ((e = fwd3tc::out_tc(a, st)) != cudaSuccess) return e;
     } else {
         fwd3_out_kernel<T, C, D, DV><<<units * nch, kThreads, b3, st>>>(a);

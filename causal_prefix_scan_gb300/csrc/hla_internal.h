@@ -107,6 +107,7 @@ hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a, void *workspac
 struct Fwd3Args {
     int B, H, n, d, dv, chunk;
     hla_dtype in_dtype;
+    const float *gamma;  // [H] decay per head, or NULL (none)
     const void *q, *k, *v;
     void *o;
     const float *sin_S, *sin_P, *sin_T;  // state before the first token (all NULL: zeros)
@@ -117,9 +118,12 @@ struct Fwd3Args {
 };
 
 struct Decode3Args {
-    int N, d, dv;
+    int N, H, d, dv;
     hla_dtype dtype;
+    const float *gamma;  // [H] decay per head (pair u uses gamma[u % H]), or NULL
+    float eps;
     float *S, *P, *T;
+    float *m, *h;        // with ratio normalisation: key mass and the unit-value column of T; else NULL
     const void *q, *k, *v;
     void *o;
 };
@@ -128,6 +132,17 @@ struct Decode3Args {
 bool fwd3_supported(const hla_params &p);
 size_t fwd3_workspace(const hla_params &p);
 cudaError_t fwd3_launch(const Fwd3Args &a, cudaStream_t st);
+// Ratio-normalised third order: the forward of the values (into o), the forward of a
+// unit-value tile (the denominator) with the same S, then o /= den + eps.  m, h: the
+// key mass and the unit-value column of T per pair ([B*H][d]), before (in) and after
+// (out) the tokens; NULL for zeros / not wanted.  The workspace is fwd3_workspace(p)
+// with HLA_NORMALIZE.
+struct Norm3 {
+    const float *m_in, *h_in;
+    float *m_out, *h_out;
+    float eps;
+};
+cudaError_t fwd3_norm_launch(const Fwd3Args &a, const Norm3 &nm, cudaStream_t st);
 cudaError_t decode3_launch(const Decode3Args &a, cudaStream_t st);
 
 // Set this thread's last-error message and return `s`.

@@ -251,10 +251,21 @@ HLA_API hla_status hla_backward_chunked_traced(const hla_params *p, const void *
  *   T_t = sum_{b<=t} S^K_b q_b q_b^T P_b   (= S^K S^Q P^KV minus the cross summaries
  *   G1 + G2 - G3 that remove a key after its query),
  * with S^K_t = sum k k^T and P_t = sum k v^T.  The streaming state of a pair is
- * (S [d][d] = S^K, P [d][dv], T [d][dv]), fp32; no decay, no normalisation.
+ * (S [d][d] = S^K, P [d][dv], T [d][dv]), fp32.
+ *
+ * HLA_DECAY (gamma [H]): every prefix moment decays by gamma per token, so the triple
+ * a, b, c <= t weighs gamma^(3t-a-b-c); the updates become S^K_t = g S^K + k k^T,
+ * P_t = g P + k v^T, T_t = g^3 T + (S^K_t q)(P_t^T q)^T.  The section states no
+ * decayed third order; this is the second order's reading carried over.
+ * HLA_NORMALIZE (eps >= 0): o_t = num_t / (den_t + eps), den_t the masked output of
+ * unit values, q_t^T h_t with the key mass m_t = g m + k (P of a unit value) and
+ * h_t = g^3 h + (S^K_t q)(m_t . q) (T of a unit value; it combines the cross summaries
+ * h^(1..3) the section names as T combines G^(1..3)).  m [d] and h [d] are then part of
+ * the state; without HLA_NORMALIZE they are not used (may be NULL).
  */
 typedef struct {
     float *S, *P, *T;
+    float *m, *h;
 } hla_state3;
 
 /* Bytes of device workspace hla_forward3_chunked needs (0 for invalid parameters). */
@@ -264,13 +275,20 @@ HLA_API size_t hla_forward3_workspace_size(const hla_params *p);
  * Masked third-order forward over n tokens for every (b,h) pair, chunk-parallel
  * (section 4, "Derde-orde scans"): chunk-local sums, a scan over chunks that composes
  * states with the segment-level linear maps M^KQ and M^QP, then per-chunk outputs.
- *   p         flags must be 0, Hkv 0 or H, d, dv, chunk in {16,32,64}; in_dtype
+ *   p         flags 0, HLA_DECAY (gamma [H], values in [0, 1]), HLA_NORMALIZE
+ *             (eps >= 0) or both; Hkv 0 or H; d, dv, chunk in {16,32,64}; in_dtype
  *             HLA_F32 or HLA_BF16 (fp32 arithmetic);
  *   q, k      [B][H][n][d]; v, o [B][H][n][dv]; in_dtype;
- *   state_in  (S, P, T) before the first token, or NULL for zeros;
- *   state_out (S, P, T) after the last token, or NULL; may not alias state_in;
- *   workspace at least hla_forward3_workspace_size(p) bytes, 16-byte aligned.
- * Three kernel launches on `stream`.
+ *   state_in  (S, P, T; with HLA_NORMALIZE also m, h) before the first token, or NULL
+ *             for zeros;
+ *   state_out (S, P, T; with HLA_NORMALIZE also m, h) after the last token, or NULL;
+ *             may not alias state_in;
+ *   workspace at least hla_forward3_workspace_size(p) bytes, 16-byte aligned (256-byte
+ *             aligned with HLA_NORMALIZE).
+ * Three kernel launches on `stream` (tensor cores for bf16 at 64/64/64 without decay,
+ * CUDA cores otherwise).  With HLA_NORMALIZE the numerator and the denominator (a
+ * 16-wide unit-value tile with the same S) are two such forwards, followed by an
+ * elementwise division; the denominator passes through the input element type.
  */
 HLA_API hla_status hla_forward3_chunked(const hla_params *p, const void *q, const void *k, const void *v, void *o,
                                         const hla_state3 *state_in, const hla_state3 *state_out, void *workspace,
@@ -284,12 +302,16 @@ HLA_API hla_status hla_forward3_chunked_traced(const hla_params *p, const void *
                                                void *const *phase_events);
 
 /*
- * One third-order decode step for N independent pairs, state updated in place:
- *   S += k k^T;  P += k v^T;  T += (S q)(P^T q)^T;  o = T^T q.
- * q, k: [N][d], v, o: [N][dv], element type `dtype`; d, dv in {16,32,64,128}.
+ * One third-order decode step for N independent pairs, state updated in place
+ * (g = gamma[i % H] with HLA_DECAY, else 1):
+ *   S = g S + k k^T;  P = g P + k v^T;  T = g^3 T + (S q)(P^T q)^T;  o = T^T q;
+ * with HLA_NORMALIZE also m = g m + k, h = g^3 h + (S q)(m . q) and o /= (h . q + eps).
+ * q, k: [N][d], v, o: [N][dv], element type `dtype`; d, dv in {16,32,64,128}; flags
+ * 0, HLA_DECAY, HLA_NORMALIZE or both; H >= 1 (only the decay rate's index uses it).
  */
-HLA_API hla_status hla_decode3_step(int N, int d, int dv, hla_dtype dtype, const hla_state3 *state, const void *q,
-                                    const void *k, const void *v, void *o, void *stream);
+HLA_API hla_status hla_decode3_step(int N, int H, int d, int dv, hla_dtype dtype, unsigned flags, float eps,
+                                    const float *gamma, const hla_state3 *state, const void *q, const void *k,
+                                    const void *v, void *o, void *stream);
 
 /* Self-test of the failure path: launches one CTA that waits, with the library's
  * bounded barrier wait (a short poll limit), on a barrier that nothing completes.  The

@@ -217,9 +217,10 @@ def _f3call(p, ptrs=(16,) * 4, sin=None, sout=None, ws=16, ws_bytes=1 << 40):
     (dict(B=0), hla.HLA_ERR_ARG),
     (dict(n=-1), hla.HLA_ERR_ARG),
     (dict(flags=16), hla.HLA_ERR_ARG),
-    (dict(flags=hla.HLA_NORMALIZE), hla.HLA_ERR_UNSUPPORTED),
-    (dict(flags=hla.HLA_DECAY, gamma=16), hla.HLA_ERR_UNSUPPORTED),
+    (dict(flags=hla.HLA_NORMALIZE, eps=-1.0), hla.HLA_ERR_ARG),
+    (dict(flags=hla.HLA_DECAY), hla.HLA_ERR_ARG),  # decay without rates
     (dict(flags=hla.HLA_UNMASKED), hla.HLA_ERR_UNSUPPORTED),
+    (dict(flags=hla.HLA_ASYMMETRIC), hla.HLA_ERR_UNSUPPORTED),
     (dict(H=4, Hkv=2), hla.HLA_ERR_UNSUPPORTED),
     (dict(d=128), hla.HLA_ERR_UNSUPPORTED),
     (dict(chunk=128), hla.HLA_ERR_UNSUPPORTED),
@@ -241,6 +242,10 @@ def test_forward3_rejects_null_misaligned_short_workspace_and_aliasing(lib):
     assert _f3call(_params(), sin=ctypes.pointer(s3), sout=ctypes.pointer(s3)) == hla.HLA_ERR_ARG
     bad = hla.hla_state3(16, None, 16)
     assert _f3call(_params(), sout=ctypes.pointer(bad)) == hla.HLA_ERR_ARG
+    # ratio normalisation: the state needs m and h; the workspace 256-byte alignment
+    pn = _params(flags=hla.HLA_NORMALIZE)
+    assert _f3call(pn, sout=ctypes.pointer(hla.hla_state3(16, 16, 16))) == hla.HLA_ERR_ARG
+    assert _f3call(pn, ws=272) == hla.HLA_ERR_ARG
     # no tokens and no state: nothing to do
     assert _f3call(_params(n=0), ptrs=(None,) * 4, ws=None, ws_bytes=0) == hla.HLA_OK
 
@@ -256,9 +261,15 @@ def test_forward3_workspace_size(lib):
 def test_decode3_rejects_bad_args(lib):
     L = hla.library()
     s3 = ctypes.pointer(hla.hla_state3(16, 16, 16))
-    assert L.hla_decode3_step(-1, 64, 64, hla.HLA_BF16, s3, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
-    assert L.hla_decode3_step(4, 48, 64, hla.HLA_BF16, s3, 16, 16, 16, 16, None) == hla.HLA_ERR_UNSUPPORTED
-    assert L.hla_decode3_step(4, 64, 64, 9, s3, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
-    assert L.hla_decode3_step(4, 64, 64, hla.HLA_BF16, None, 16, 16, 16, 16, None) == hla.HLA_ERR_ARG
-    assert L.hla_decode3_step(4, 64, 64, hla.HLA_BF16, ctypes.pointer(hla.hla_state3(16, 8, 16)), 16, 16, 16, 16,
-                              None) == hla.HLA_ERR_ARG
+    call = lambda N=4, H=1, d=64, dv=64, dt=hla.HLA_BF16, fl=0, eps=0.0, g=None, st=s3: L.hla_decode3_step(
+        N, H, d, dv, dt, fl, eps, g, st, 16, 16, 16, 16, None)
+    assert call(N=-1) == hla.HLA_ERR_ARG
+    assert call(H=0) == hla.HLA_ERR_ARG
+    assert call(d=48) == hla.HLA_ERR_UNSUPPORTED
+    assert call(dt=9) == hla.HLA_ERR_ARG
+    assert call(st=None) == hla.HLA_ERR_ARG
+    assert call(st=ctypes.pointer(hla.hla_state3(16, 8, 16))) == hla.HLA_ERR_ARG
+    assert call(fl=hla.HLA_UNMASKED) == hla.HLA_ERR_UNSUPPORTED
+    assert call(fl=hla.HLA_DECAY) == hla.HLA_ERR_ARG  # no rates
+    assert call(fl=hla.HLA_NORMALIZE) == hla.HLA_ERR_ARG  # no m, h
+    assert call(fl=hla.HLA_NORMALIZE, eps=-1.0, st=ctypes.pointer(hla.hla_state3(16, 16, 16, 16, 16))) == hla.HLA_ERR_ARG
