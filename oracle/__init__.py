@@ -77,12 +77,14 @@ def _load():
         _lib.hla_oracle_decode_step.argtypes = [i] * 6 + [dp, i, d] + [dp] * 5 + [dp, dp, dp, dp, i]
         _lib.hla_oracle_combine.argtypes = [i, i, i, i] + [dp] * 10 + [dp] + [dp] * 5
         _lib.hla_oracle_backward.argtypes = [i] * 7 + [d] + [dp] * 8 + [i]
+        _lib.hla_oracle_backward_state.argtypes = [i] * 7 + [d] + [dp] * 5 + [dp] * 5 + [dp] * 3 + [dp] * 5 + [i]
         _lib.hla_oracle3_forward.argtypes = [i] * 6 + [dp] * 6 + [i]
         _lib.hla_oracle3_combine.argtypes = [i, i, i, dp, dp, dp]
         _lib.hla_oracle3_forward_ex.argtypes = [i] * 6 + [dp, i, d] + [dp] * 6 + [i]
         _lib.hla_oracle3_combine_ex.argtypes = [i, i, i, dp, dp, dp, dp]
         for f in (_lib.hla_oracle_forward, _lib.hla_oracle_forward_chunked,
                   _lib.hla_oracle_decode_step, _lib.hla_oracle_combine, _lib.hla_oracle_backward,
+                  _lib.hla_oracle_backward_state,
                   _lib.hla_oracle3_forward, _lib.hla_oracle3_combine, _lib.hla_oracle3_forward_ex,
                   _lib.hla_oracle3_combine_ex):
             f.restype = ctypes.c_int
@@ -223,13 +225,14 @@ def combine(A: State, Bst: State, decay_pow=None, asymmetric=False) -> State:
     return out
 
 
-def backward(q, k, v, go, gamma=None, nthreads=None, normalize=False, eps=0.0):
-    """Gradients (dq, dk, dv) of sum_t go_t . o_t for the masked forward from a zero
-    state (reverse mode of the recurrence in hla_oracle.c), through the ratio
-    normalisation o = num / (den + eps) when `normalize`.
+def backward(q, k, v, go, gamma=None, nthreads=None, normalize=False, eps=0.0, state_in=None, want_dstate=False):
+    """Gradients (dq, dk, dv) of sum_t go_t . o_t for the masked forward (reverse mode
+    of the recurrence in hla_oracle.c), through the ratio normalisation
+    o = num / (den + eps) when `normalize`.
     q, go: [B,H,n,d|dv]; k, v: [B,Hkv,n,d|dv] with H a multiple of Hkv (query head h
     reads key/value head h // (H // Hkv); dk, dv sum over the heads of a group);
-    gamma: [H] or None."""
+    gamma: [H] or None.  state_in: the State before the first token (None: zeros).
+    want_dstate: also return the gradient with respect to that state (a State)."""
     q, k, v, go = _f64(q), _f64(k), _f64(v), _f64(go)
     B, H, n, d = q.shape
     Hkv = k.shape[1]
@@ -237,11 +240,14 @@ def backward(q, k, v, go, gamma=None, nthreads=None, normalize=False, eps=0.0):
     assert k.shape == (B, Hkv, n, d) and v.shape == (B, Hkv, n, dv) and go.shape == (B, H, n, dv) and H % Hkv == 0
     g = _f64(gamma)
     dq, dk, dvv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
-    rc = _load().hla_oracle_backward(B, H, Hkv, n, d, dv, int(bool(normalize)), float(eps), _p(q), _p(k), _p(v),
-                                     _p(g), _p(go), _p(dq), _p(dk), _p(dvv), nthreads or default_threads())
+    sin = _as_state(state_in, B * H, d, dv)
+    dst = State.zeros(B * H, d, dv) if want_dstate else None
+    rc = _load().hla_oracle_backward_state(B, H, Hkv, n, d, dv, int(bool(normalize)), float(eps), _p(q), _p(k),
+                                           _p(v), _p(g), _p(go), *_state_ptrs(sin), _p(dq), _p(dk), _p(dvv),
+                                           *_state_ptrs(dst), nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
-    return dq, dk, dvv
+    return (dq, dk, dvv, dst) if want_dstate else (dq, dk, dvv)
 
 
 # ------------------------------------------------------------------ third order

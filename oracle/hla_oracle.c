@@ -532,12 +532,34 @@ int hla_oracle_decode_step(int N, int H, int Hkv, int d, int dv, int variant,
  *   du_t = Lam_t v_t + Lamy_t,  dv_t = Lam_t^T u_t,  dq_t = X_t gn_t + gd_t Y_t + S_t du_t,
  *   Om_t = du_t q_t^T + g Om_{t+1},  dk_t = (Om_t + Om_t^T) k_t.
  * Without normalisation gn = go and gd = 0. */
+/* The state before the first token (S, C, m, G, h of one pair, or NULLs: zeros) and the
+ * gradient with respect to it (NULLs: not wanted). */
+typedef struct {
+    const double *S, *C, *m, *G, *h;
+    double *dS, *dC, *dm, *dG, *dh;
+} bstate_t;
+
 static void backward_unit(int n, int d, int dv, double g, int normalize, double eps, const double *q,
-                          const double *k, const double *v, const double *go, double *dq, double *dk, double *dvo)
+                          const double *k, const double *v, const double *go, double *dq, double *dk, double *dvo,
+                          const bstate_t *st0)
 {
     double *S = (double *)calloc((size_t)(n + 1) * d * d, sizeof(double));  /* S_t after token t */
     double *X = (double *)calloc((size_t)(n + 1) * d * dv, sizeof(double)); /* X_t after token t */
     double *Y = (double *)calloc((size_t)(n + 1) * d, sizeof(double));      /* Y_t after token t */
+    /* the state before the first token: S_in, X_in = S_in C_in - G_in, Y_in = S_in m_in - h_in */
+    if (st0 && st0->S) {
+        for (int i = 0; i < d * d; ++i) S[i] = st0->S[i];
+        for (int i = 0; i < d; ++i) {
+            for (int j = 0; j < dv; ++j) {
+                double acc = -st0->G[i * dv + j];
+                for (int l = 0; l < d; ++l) acc += st0->S[i * d + l] * st0->C[l * dv + j];
+                X[i * dv + j] = acc;
+            }
+            double acc = -st0->h[i];
+            for (int l = 0; l < d; ++l) acc += st0->S[i * d + l] * st0->m[l];
+            Y[i] = acc;
+        }
+    }
     double *U = (double *)calloc((size_t)n * d, sizeof(double));            /* u_t */
     double *gn = (double *)calloc((size_t)n * dv + 1, sizeof(double));      /* dL/dn_t */
     double *gd = (double *)calloc((size_t)n + 1, sizeof(double));           /* dL/dden_t */
@@ -615,6 +637,40 @@ static void backward_unit(int n, int d, int dv, double g, int normalize, double 
             dk[(size_t)t * d + i] = acc;
         }
     }
+    /* the initial state: S_0 = g S_in + k k^T, X_0 = g^2 X_in + ..., Y_0 = g^2 Y_in + ...
+     * (n = 0: the adjoints are zero), then through X_in = S_in C_in - G_in and
+     * Y_in = S_in m_in - h_in */
+    if (st0 && st0->dS) {
+        const double g2 = n > 0 ? g * g : 0.0, g1 = n > 0 ? g : 0.0;
+        double *dX = (double *)calloc((size_t)d * dv, sizeof(double)), *dY = (double *)calloc((size_t)d, sizeof(double));
+        for (int i = 0; i < d * dv; ++i) dX[i] = g2 * Lam[i];
+        for (int i = 0; i < d; ++i) dY[i] = g2 * Lamy[i];
+        const int have = st0->S != NULL;
+        for (int i = 0; i < d; ++i)
+            for (int j = 0; j < d; ++j) {
+                double acc = g1 * Om[i * d + j];
+                if (have) {
+                    for (int c = 0; c < dv; ++c) acc += dX[i * dv + c] * st0->C[j * dv + c];
+                    acc += dY[i] * st0->m[j];
+                }
+                st0->dS[i * d + j] = acc;
+            }
+        for (int j = 0; j < d; ++j) {
+            for (int c = 0; c < dv; ++c) {
+                double acc = 0.0;
+                if (have)
+                    for (int i = 0; i < d; ++i) acc += st0->S[i * d + j] * dX[i * dv + c];
+                st0->dC[j * dv + c] = acc;
+            }
+            double acc = 0.0;
+            if (have)
+                for (int i = 0; i < d; ++i) acc += st0->S[i * d + j] * dY[i];
+            st0->dm[j] = acc;
+        }
+        for (int i = 0; i < d * dv; ++i) st0->dG[i] = -dX[i];
+        for (int i = 0; i < d; ++i) st0->dh[i] = -dY[i];
+        free(dX); free(dY);
+    }
     free(S); free(X); free(Y); free(U); free(gn); free(gd); free(Lam); free(Lamy); free(Om); free(du);
 }
 
@@ -623,6 +679,8 @@ typedef struct {
     double eps;
     const double *q, *k, *v, *go, *gamma;
     double *dq, *dk_pair, *dv_pair;  /* dk, dv of every query head before the group sum */
+    const double *sS, *sC, *sm, *sG, *sh;  /* state before the first token [B*H][...] or NULL */
+    double *dS, *dC, *dm, *dG, *dh;        /* its gradient, or NULL */
     pthread_mutex_t lock;
 } bjob_t;
 
@@ -638,8 +696,20 @@ static void *bworker(void *arg)
         const size_t kvu = (size_t)(u / J->H) * J->Hkv + (u % J->H) / (J->H / J->Hkv);
         const size_t qo = (size_t)u * J->n * J->d, vo = (size_t)u * J->n * J->dv;
         const size_t ko = kvu * J->n * J->d, kvo = kvu * J->n * J->dv;
+        const size_t dd = (size_t)J->d * J->d, ddv = (size_t)J->d * J->dv;
+        bstate_t st0;
+        st0.S = J->sS ? J->sS + u * dd : NULL;
+        st0.C = J->sS ? J->sC + u * ddv : NULL;
+        st0.m = J->sS ? J->sm + u * J->d : NULL;
+        st0.G = J->sS ? J->sG + u * ddv : NULL;
+        st0.h = J->sS ? J->sh + u * J->d : NULL;
+        st0.dS = J->dS ? J->dS + u * dd : NULL;
+        st0.dC = J->dS ? J->dC + u * ddv : NULL;
+        st0.dm = J->dS ? J->dm + u * J->d : NULL;
+        st0.dG = J->dS ? J->dG + u * ddv : NULL;
+        st0.dh = J->dS ? J->dh + u * J->d : NULL;
         backward_unit(J->n, J->d, J->dv, J->gamma ? J->gamma[u % J->H] : 1.0, J->normalize, J->eps, J->q + qo,
-                      J->k + ko, J->v + kvo, J->go + vo, J->dq + qo, J->dk_pair + qo, J->dv_pair + vo);
+                      J->k + ko, J->v + kvo, J->go + vo, J->dq + qo, J->dk_pair + qo, J->dv_pair + vo, &st0);
     }
     return NULL;
 }
@@ -650,11 +720,32 @@ static void *bworker(void *arg)
  * [B][Hkv][n][.] (H a multiple of Hkv; query head h reads key/value head
  * h / (H / Hkv)).  The gradient of a shared key or value is the sum of the
  * gradients through every query head of its group (chain rule), added in head order. */
+/* The same from the state (S, C, m, G, h) before the first token (sS NULL: zeros; all
+ * five [B*H][...] in the layout of the forward), also returning the gradient with
+ * respect to that state (dS NULL: not wanted; all five then set). */
+int hla_oracle_backward_state(int B, int H, int Hkv, int n, int d, int dv, int normalize, double eps,
+                              const double *q, const double *k, const double *v, const double *gamma,
+                              const double *go, const double *sS, const double *sC, const double *sm,
+                              const double *sG, const double *sh, double *dq, double *dk, double *dvo, double *dS,
+                              double *dC, double *dm, double *dG, double *dh, int nthreads);
+
 int hla_oracle_backward(int B, int H, int Hkv, int n, int d, int dv, int normalize, double eps, const double *q,
                         const double *k, const double *v, const double *gamma, const double *go, double *dq,
                         double *dk, double *dvo, int nthreads)
 {
+    return hla_oracle_backward_state(B, H, Hkv, n, d, dv, normalize, eps, q, k, v, gamma, go, NULL, NULL, NULL, NULL,
+                                     NULL, dq, dk, dvo, NULL, NULL, NULL, NULL, NULL, nthreads);
+}
+
+int hla_oracle_backward_state(int B, int H, int Hkv, int n, int d, int dv, int normalize, double eps,
+                              const double *q, const double *k, const double *v, const double *gamma,
+                              const double *go, const double *sS, const double *sC, const double *sm,
+                              const double *sG, const double *sh, double *dq, double *dk, double *dvo, double *dS,
+                              double *dC, double *dm, double *dG, double *dh, int nthreads)
+{
     if (check_dims(B, H, n, d, dv) || Hkv < 1 || H % Hkv) return -1;
+    if (sS && (!sC || !sm || !sG || !sh)) return -1;
+    if (dS && (!dC || !dm || !dG || !dh)) return -1;
     const size_t nd = (size_t)n * d, ndv = (size_t)n * dv;
     double *dkp = (double *)calloc((size_t)B * H * nd + 1, sizeof(double));
     double *dvp = (double *)calloc((size_t)B * H * ndv + 1, sizeof(double));
@@ -663,6 +754,8 @@ int hla_oracle_backward(int B, int H, int Hkv, int n, int d, int dv, int normali
     J.B = B; J.H = H; J.Hkv = Hkv; J.n = n; J.d = d; J.dv = dv; J.normalize = normalize; J.eps = eps;
     J.q = q; J.k = k; J.v = v; J.go = go; J.gamma = gamma;
     J.dq = dq; J.dk_pair = dkp; J.dv_pair = dvp;
+    J.sS = sS; J.sC = sC; J.sm = sm; J.sG = sG; J.sh = sh;
+    J.dS = dS; J.dC = dC; J.dm = dm; J.dG = dG; J.dh = dh;
     pthread_mutex_init(&J.lock, NULL);
     const int total = B * H;
     if (nthreads < 1) nthreads = 1;
