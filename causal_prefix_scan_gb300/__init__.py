@@ -30,7 +30,7 @@ __all__ = [
     "hla_forward_workspace_size", "hla_forward_kernel", "hla_forward_chunked", "hla_state_combine",
     "hla_decode_step", "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
     "hla_backward_workspace_size", "hla_backward_chunked", "hla_backward_chunked_traced",
-    "hla_state3", "hla_forward3_workspace_size", "hla_forward3_chunked", "hla_forward3_chunked_traced",
+    "hla_backward_chunked_state", "hla_state3", "hla_forward3_workspace_size", "hla_forward3_chunked", "hla_forward3_chunked_traced",
     "hla_decode3_step", "State3", "forward3", "decode3_step", "hla_selftest_expired_wait",
     "State", "new_workspace", "forward", "state_combine", "decode_step", "backward",
 ]
@@ -40,7 +40,7 @@ EXPORTS = ("hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combi
            "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
            "hla_backward_workspace_size", "hla_backward_chunked", "hla_backward_chunked_traced",
            "hla_forward3_workspace_size", "hla_forward3_chunked", "hla_forward3_chunked_traced", "hla_decode3_step",
-           "hla_selftest_expired_wait", "hla_forward_kernel")
+           "hla_selftest_expired_wait", "hla_forward_kernel", "hla_backward_chunked_state")
 
 
 class HlaError(RuntimeError):
@@ -94,6 +94,8 @@ def library(path: str | None = None):
     lib.hla_backward_chunked.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.hla_backward_chunked_traced.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp,
                                                 ctypes.POINTER(ctypes.c_void_p)]
+    lib.hla_backward_chunked_state.argtypes = [P, vp, vp, vp, vp, ctypes.POINTER(hla_state), vp, vp, vp,
+                                               ctypes.POINTER(hla_state), vp, sz, vp]
     S3 = ctypes.POINTER(hla_state3)
     lib.hla_forward3_workspace_size.argtypes = [P]
     lib.hla_forward3_workspace_size.restype = sz
@@ -200,6 +202,14 @@ def hla_backward_chunked(params: hla_params, q, k, v, dout, dq, dk, dv, workspac
                          stream=None) -> None:
     _check(library().hla_backward_chunked(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq),
                                           _ptr(dk), _ptr(dv), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def hla_backward_chunked_state(params: hla_params, q, k, v, dout, state_in, dq, dk, dv, d_state_in, workspace,
+                               workspace_bytes: int, stream=None) -> None:
+    _check(library().hla_backward_chunked_state(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                                _state_struct(state_in), _ptr(dq), _ptr(dk), _ptr(dv),
+                                                _state_struct(d_state_in), _ptr(workspace), workspace_bytes,
+                                                _stream(stream)))
 
 
 def hla_backward_chunked_traced(params: hla_params, q, k, v, dout, dq, dk, dv, workspace, workspace_bytes: int,
@@ -389,19 +399,26 @@ def decode_step(state: State, q, k, v, H: int, gamma=None, normalize: bool = Fal
 
 
 def backward(q, k, v, dout, chunk: int, gamma=None, workspace=None, out=None, stream=None,
-             normalize: bool = False, eps: float = 0.0):
+             normalize: bool = False, eps: float = 0.0, state_in: State | None = None, want_dstate: bool = False):
     """Gradients (dq, dk, dv) of sum(dout * o) for the masked forward o of q, k, v from a
-    zero state (with ``normalize=True`` the ratio-normalised o).  q [B,H,n,d], k [B,Hkv,n,d],
-    v [B,Hkv,n,dv], dout [B,H,n,dv] contiguous CUDA tensors of one dtype (bf16 or fp32);
-    gamma [H] fp32 or None.  ``out`` may hold three preallocated result tensors."""
+    zero state, or from ``state_in`` (with ``normalize=True`` the ratio-normalised o; not
+    with a state).  q [B,H,n,d], k [B,Hkv,n,d], v [B,Hkv,n,dv], dout [B,H,n,dv]
+    contiguous CUDA tensors of one dtype (bf16 or fp32); gamma [H] fp32 or None.
+    ``out`` may hold three preallocated result tensors.  ``want_dstate``: also return the
+    gradient with respect to the initial state (a State)."""
     import torch
     p = make_params(q, v, chunk, gamma, normalize, eps)
     need = hla_backward_workspace_size(p)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     dq, dk, dv = out if out is not None else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
-    hla_backward_chunked(p, q, k, v, dout, dq, dk, dv, workspace, need if workspace is not None else 0, stream)
-    return dq, dk, dv
+    if state_in is None and not want_dstate:
+        hla_backward_chunked(p, q, k, v, dout, dq, dk, dv, workspace, need if workspace is not None else 0, stream)
+        return dq, dk, dv
+    dst = State.empty(p.B * p.H, p.d, p.dv, device=q.device) if want_dstate else None
+    hla_backward_chunked_state(p, q, k, v, dout, state_in, dq, dk, dv, dst, workspace,
+                               need if workspace is not None else 0, stream)
+    return (dq, dk, dv, dst) if want_dstate else (dq, dk, dv)
 
 
 def forward3(q, k, v, chunk: int, state_in: State3 | None = None, return_state: bool = False, out=None,

@@ -210,24 +210,43 @@ size_t hla_backward_workspace_size(const hla_params *p) {
     return hla::bwd_simt_workspace(*p);
 }
 
-hla_status hla_backward_chunked(const hla_params *p, const void *q, const void *k, const void *v, const void *dout,
-                                void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
-                                void *stream) {
-    return hla_backward_chunked_traced(p, q, k, v, dout, dq, dk, dv, workspace, workspace_bytes, stream, nullptr);
-}
-
-hla_status hla_backward_chunked_traced(const hla_params *p, const void *q, const void *k, const void *v,
-                                       const void *dout, void *dq, void *dk, void *dv, void *workspace,
-                                       size_t workspace_bytes, void *stream, void *const *phase_events) {
+namespace {
+hla_status backward_impl(const hla_params *p, const void *q, const void *k, const void *v, const void *dout,
+                         const hla_state *state_in, void *dq, void *dk, void *dv, const hla_state *d_state_in,
+                         void *workspace, size_t workspace_bytes, void *stream, void *const *phase_events) {
     hla_status s = check_bwd_params(p);
     if (s != HLA_OK) return s;
-    if (p->n == 0) return HLA_OK;
+    const bool norm = (p->flags & HLA_NORMALIZE) != 0;
+    if ((state_in || d_state_in) && norm)
+        return fail(HLA_ERR_UNSUPPORTED, "a given initial state or its gradient: without HLA_NORMALIZE only");
+    if ((s = check_state(state_in, "state_in")) != HLA_OK) return s;
+    if ((s = check_state(d_state_in, "d_state_in")) != HLA_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t BH = (size_t)p->B * p->H, D = p->d, DV = p->dv;
+    if (d_state_in) {  // m and h enter only the denominator: their gradient is zero here
+        const size_t sz[2] = {BH * D * 4, BH * D * 4};
+        float *dst[2] = {d_state_in->m, d_state_in->h};
+        for (int i = 0; i < 2; ++i) {
+            cudaError_t e = cudaMemsetAsync(dst[i], 0, sz[i], st);
+            if (e != cudaSuccess) return cuda_fail(e, "state gradient clear");
+        }
+    }
+    if (p->n == 0) {  // no tokens: the state gradient is zero
+        if (d_state_in) {
+            const size_t sz[3] = {BH * D * D * 4, BH * D * DV * 4, BH * D * DV * 4};
+            float *dst[3] = {d_state_in->S, d_state_in->C, d_state_in->G};
+            for (int i = 0; i < 3; ++i) {
+                cudaError_t e = cudaMemsetAsync(dst[i], 0, sz[i], st);
+                if (e != cudaSuccess) return cuda_fail(e, "state gradient clear");
+            }
+        }
+        return HLA_OK;
+    }
     if (!q || !k || !v || !dout || !dq || !dk || !dv)
         return fail(HLA_ERR_ARG, "q, k, v, dout, dq, dk, dv must be set when n > 0");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
         !aligned16(dv))
         return fail(HLA_ERR_ARG, "tensor pointers must be 16-byte aligned");
-    const bool norm = (p->flags & HLA_NORMALIZE) != 0;
     const size_t need = norm ? hla::bwd_norm_layout(*p).total : hla::bwd_simt_workspace(*p);
     if (!workspace || workspace_bytes < need)
         return fail(HLA_ERR_ARG, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
@@ -243,6 +262,13 @@ hla_status hla_backward_chunked_traced(const hla_params *p, const void *q, const
     a.workspace = static_cast<float *>(workspace);
     a.dk_pair = a.Hkv < a.H ? a.workspace + hla::bwd_pair_offset(*p) : nullptr;
     a.dv_pair = a.Hkv < a.H ? a.dk_pair + (size_t)p->B * p->H * p->n * p->d : nullptr;
+    a.sin_S = state_in ? state_in->S : nullptr;
+    a.sin_C = state_in ? state_in->C : nullptr;
+    a.sin_G = state_in ? state_in->G : nullptr;
+    a.dS = d_state_in ? d_state_in->S : nullptr;
+    a.dC = d_state_in ? d_state_in->C : nullptr;
+    a.dG = d_state_in ? d_state_in->G : nullptr;
+    a.adj0 = d_state_in ? a.workspace + hla::bwd_adj0_offset(*p) : nullptr;
     if (phase_events) {
         for (int i = 0; i < 4; ++i)
             if (!phase_events[i]) return fail(HLA_ERR_ARG, "phase_events must hold four events");
@@ -250,10 +276,32 @@ hla_status hla_backward_chunked_traced(const hla_params *p, const void *q, const
     a.events = reinterpret_cast<cudaEvent_t const *>(phase_events);
     cudaError_t e = status_ptr(&a.err);
     if (e != cudaSuccess) return cuda_fail(e, "status word");
-    if (norm) return hla::bwd_norm_launch(*p, a, workspace, static_cast<cudaStream_t>(stream));
-    e = hla::bwd_simt_launch(a, static_cast<cudaStream_t>(stream));
+    if (norm) return hla::bwd_norm_launch(*p, a, workspace, st);
+    e = hla::bwd_simt_launch(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return HLA_OK;
+}
+}  // namespace
+
+hla_status hla_backward_chunked(const hla_params *p, const void *q, const void *k, const void *v, const void *dout,
+                                void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    return backward_impl(p, q, k, v, dout, nullptr, dq, dk, dv, nullptr, workspace, workspace_bytes, stream, nullptr);
+}
+
+hla_status hla_backward_chunked_traced(const hla_params *p, const void *q, const void *k, const void *v,
+                                       const void *dout, void *dq, void *dk, void *dv, void *workspace,
+                                       size_t workspace_bytes, void *stream, void *const *phase_events) {
+    return backward_impl(p, q, k, v, dout, nullptr, dq, dk, dv, nullptr, workspace, workspace_bytes, stream,
+                         phase_events);
+}
+
+hla_status hla_backward_chunked_state(const hla_params *p, const void *q, const void *k, const void *v,
+                                      const void *dout, const hla_state *state_in, void *dq, void *dk, void *dv,
+                                      const hla_state *d_state_in, void *workspace, size_t workspace_bytes,
+                                      void *stream) {
+    return backward_impl(p, q, k, v, dout, state_in, dq, dk, dv, d_state_in, workspace, workspace_bytes, stream,
+                         nullptr);
 }
 
 namespace {

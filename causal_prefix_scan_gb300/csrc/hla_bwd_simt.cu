@@ -41,10 +41,17 @@ size_t bwd_pair_offset(const hla_params &p) {
     return (size_t)p.B * p.H * nch * (w.loc_floats() + w.st_floats());
 }
 
-size_t bwd_simt_workspace(const hla_params &p) {
+// ... then the adjoints at the first token of every pair (Lam, Om), for the gradient of
+// a given initial state.
+size_t bwd_adj0_offset(const hla_params &p) {
     const int hkv = p.Hkv > 0 ? p.Hkv : p.H;
     const size_t pair = hkv < p.H ? (size_t)p.B * p.H * p.n * ((size_t)p.d + p.dv) : 0;
-    return (bwd_pair_offset(p) + pair) * sizeof(float);
+    return bwd_pair_offset(p) + pair;
+}
+
+size_t bwd_simt_workspace(const hla_params &p) {
+    const size_t adj = (size_t)p.B * p.H * ((size_t)p.d * p.dv + (size_t)p.d * p.d);
+    return (bwd_adj0_offset(p) + adj) * sizeof(float);
 }
 
 cudaError_t bwd_simt_launch(const BwdArgs &a, cudaStream_t st) {

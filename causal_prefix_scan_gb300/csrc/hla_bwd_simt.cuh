@@ -1,6 +1,8 @@
 // hla_bwd_simt.cuh -- chunk-parallel backward pass of the masked second-order HLA
-// forward on CUDA cores (fp32 arithmetic), for d, dv, chunk in {16,32,64} and a zero
-// initial state.  The kernels compute the unnormalised gradient; the ratio-normalised
+// forward on CUDA cores (fp32 arithmetic), for d, dv, chunk in {16,32,64}, from a zero
+// or a given initial state (S_in, X_in = S_in C_in - G_in; the gradient of that state
+// comes from the adjoints at the first token: dX_in = g^2 Lam, dS_in = g Om +
+// dX_in C_in^T, dC_in = S_in^T dX_in, dG_in = -dX_in).  The kernels compute the unnormalised gradient; the ratio-normalised
 // one is composed from two such passes (hla_bwd_norm.cu).  Query heads may share key/
 // value heads: dk, dv are staged per query head and summed over each group.
 //
@@ -240,6 +242,20 @@ __device__ __forceinline__ void scan_dir(const BwdArgs &a, float *sm, int part, 
     for (int e = threadIdx.x; e < D * Sm::FW; e += kThreads) F[e] = 0.f;
     for (int e = threadIdx.x; e < D * Sm::LB; e += kThreads) Bk[e] = 0.f;
     __syncthreads();
+    if (DIR == 0 && a.sin_S) {  // S = S_in; the column block of X_in = S_in C_in - G_in
+        float *R1 = sm + Sm::BUF + Sm::BUFSZ + Sm::B_R;  // buffer 1 is not in use yet
+        for (int e = threadIdx.x; e < D * D; e += kThreads)
+            F[(e / D) * Sm::FW + e % D] = a.sin_S[(size_t)u * D * D + e];
+        for (int e = threadIdx.x; e < D * NBD; e += kThreads)
+            R1[(e / NBD) * Sm::LB + e % NBD] = a.sin_C[(size_t)u * D * DV + (size_t)(e / NBD) * DV + c0 + e % NBD];
+        __syncthreads();
+        mac_ksplit<D, NBD, D>(F, Sm::FW, R1, Sm::LB, red);
+        __syncthreads();
+        for (int e = threadIdx.x; e < D * NBD; e += kThreads)
+            Bk[(e / NBD) * Sm::LB + e % NBD] = ksplit_sum<D, NBD, D>(red, e) -
+                                               a.sin_G[(size_t)u * D * DV + (size_t)(e / NBD) * DV + c0 + e % NBD];
+        __syncthreads();
+    }
     for (int it = 0; it < nch; ++it) {
         if (it + 1 < nch) issue(it + 1);
         cp_async_commit();
@@ -277,6 +293,55 @@ __device__ __forceinline__ void scan_dir(const BwdArgs &a, float *sm, int part, 
         __syncthreads();
     }
     cp_async_wait<0>();
+    if (DIR == 1 && a.adj0) {  // Lam and Om at the first token (rows of Lam, a column block of Om)
+        float *lam0 = a.adj0 + (size_t)u * (D * DV + D * D), *om0 = lam0 + D * DV;
+        for (int e = threadIdx.x; e < ROWS * FWD; e += kThreads) {
+            const int r = rows0 + e / FWD, x = e % FWD;
+            lam0[(size_t)r * FWD + x] = F[r * Sm::FW + x];
+        }
+        for (int e = threadIdx.x; e < D * NBD; e += kThreads) {
+            const int r = e / NBD, x = e % NBD;
+            om0[(size_t)r * BW + c0 + x] = Bk[r * Sm::LB + x];
+        }
+    }
+}
+
+// The gradient of the initial state from the adjoints at the first token, one CTA per
+// pair: dX_in = g^2 Lam, dG_in = -dX_in, dC_in = S_in^T dX_in, dS_in = g Om + dX_in C_in^T
+// (without a given state: dC_in = 0, dS_in = g Om).
+template <int D, int DV>
+struct StateGradSmem {
+    static constexpr int LS = D + 4, LX = DV + 4;
+    static constexpr int S = 0, C = S + D * LS, X = C + D * LX, TOTAL = X + D * LX;
+};
+template <int D, int DV>
+__global__ void __launch_bounds__(kThreads) bwd_state_grad_kernel(BwdArgs a) {
+    using Sm = StateGradSmem<D, DV>;
+    extern __shared__ __align__(16) float sm[];
+    float *S = sm + Sm::S, *Cm = sm + Sm::C, *dX = sm + Sm::X;
+    const int u = blockIdx.x;
+    const bool decay = (a.flags & HLA_DECAY) != 0;
+    const float g = decay ? a.gamma[u % a.H] : 1.f;
+    const float *lam0 = a.adj0 + (size_t)u * (D * DV + D * D), *om0 = lam0 + D * DV;
+    const size_t oS = (size_t)u * D * D, oC = (size_t)u * D * DV;
+    const bool have = a.sin_S != nullptr;
+    for (int e = threadIdx.x; e < D * DV; e += kThreads) {
+        const int r = e / DV, x = e % DV;
+        const float d = g * g * lam0[e];
+        dX[r * Sm::LX + x] = d;
+        a.dG[oC + e] = -d;
+        Cm[r * Sm::LX + x] = have ? a.sin_C[oC + e] : 0.f;
+    }
+    for (int e = threadIdx.x; e < D * D; e += kThreads) S[(e / D) * Sm::LS + e % D] = have ? a.sin_S[oS + e] : 0.f;
+    __syncthreads();
+    tiles<false, D, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<true, false>(acc, S, Sm::LS, dX, Sm::LX, m0, n0, ns, D);
+        each(acc, m0, n0, ns, [&](int j, int c, float x) { a.dC[oC + (size_t)j * DV + c] = x; });
+    });
+    tiles<false, D, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, true>(acc, dX, Sm::LX, Cm, Sm::LX, m0, n0, ns, DV);
+        each(acc, m0, n0, ns, [&](int i, int j, float x) { a.dS[oS + (size_t)i * D + j] = g * om0[(size_t)i * D + j] + x; });
+    });
 }
 
 template <int C, int D, int DV>
@@ -422,9 +487,14 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t st) {
                  b3 = GradSmem<C, D, DV>::TOTAL * sizeof(float);
     cudaError_t e;
     constexpr bool TC = std::is_same<T, __nv_bfloat16>::value && C == 64 && D == 64 && DV == 64;
+    // with a given initial state, or its gradient wanted, the scan is the CUDA-core one
+    const bool tc_scan = TC && !a.sin_S && !a.adj0;
+    if (!tc_scan && (e = smem_attr(bwd_scan_kernel<C, D, DV>, b2)) != cudaSuccess) return e;
+    if (a.adj0 &&
+        (e = smem_attr(bwd_state_grad_kernel<D, DV>, StateGradSmem<D, DV>::TOTAL * sizeof(float))) != cudaSuccess)
+        return e;
     if constexpr (!TC) {  // the CUDA-core kernels (the tensor-core ones set their own attributes)
         if ((e = smem_attr(bwd_local_kernel<T, C, D, DV>, b1)) != cudaSuccess) return e;
-        if ((e = smem_attr(bwd_scan_kernel<C, D, DV>, b2)) != cudaSuccess) return e;
         if ((e = smem_attr(bwd_grad_kernel<T, C, D, DV>, b3)) != cudaSuccess) return e;
     }
     auto mark = [&](int i) { return a.events ? cudaEventRecord(a.events[i], st) : cudaSuccess; };
@@ -435,11 +505,13 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t st) {
         bwd_local_kernel<T, C, D, DV><<<units * nch, kThreads, b1, st>>>(a);
     }
     if ((e = mark(1)) != cudaSuccess) return e;
-    if constexpr (TC) {
+    if (tc_scan) {
         if ((e = scantc::bwd_scan(a, st)) != cudaSuccess) return e;
     } else {
         bwd_scan_kernel<C, D, DV><<<units * kSplit * 2, kThreads, b2, st>>>(a);
     }
+    if (a.adj0)
+        bwd_state_grad_kernel<D, DV><<<units, kThreads, StateGradSmem<D, DV>::TOTAL * sizeof(float), st>>>(a);
     if ((e = mark(2)) != cudaSuccess) return e;
     if constexpr (TC) {
         if ((e = bwdtc::grad_tc(a, st)) != cudaSuccess) return e;

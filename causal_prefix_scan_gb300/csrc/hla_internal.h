@@ -79,6 +79,11 @@ struct BwdArgs {
     void *grad_q, *grad_k, *grad_v;  // outputs
     float *workspace;
     float *dk_pair, *dv_pair;  // Hkv < H: fp32 dk, dv of every query head before the group sum
+    // the state before the first token (NULL: zeros), fp32 [B*H][d][d], [B*H][d][dv] x 2
+    const float *sin_S, *sin_C, *sin_G;
+    // its gradient (dS NULL: not wanted), and the per-pair adjoints at the first token
+    // the scan leaves for it (Lam [d][dv], then Om [d][d])
+    float *dS, *dC, *dG, *adj0;
     cudaEvent_t const *events;  // NULL or four events recorded at the phase boundaries
     unsigned *err;              // sticky device status word (bounded waits of the tensor-core kernels)
 };
@@ -87,6 +92,7 @@ struct BwdArgs {
 bool bwd_simt_supported(const hla_params &p);
 size_t bwd_simt_workspace(const hla_params &p);
 size_t bwd_pair_offset(const hla_params &p);  // floats before the per-query-head dk, dv
+size_t bwd_adj0_offset(const hla_params &p);  // floats before the adjoints at the first token
 cudaError_t bwd_simt_launch(const BwdArgs &a, cudaStream_t st);
 
 // Backward through the ratio normalisation: two unnormalised fp32 forwards (values and

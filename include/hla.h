@@ -198,8 +198,8 @@ HLA_API hla_status hla_decode_step(int N, int H, int Hkv, int d, int dv, hla_dty
                            void *stream);
 
 /*
- * Backward pass (training) of the masked forward with zero initial state.  The
- * pages motivate chunk-parallel training (section 4) but give no gradient; this
+ * Backward pass (training) of the masked forward from a zero initial state (from a
+ * given one: hla_backward_chunked_state below).  The pages motivate chunk-parallel training (section 4) but give no gradient; this
  * call is reverse-mode differentiation of the section 1 recurrence, evaluated
  * chunk-parallel: per-chunk local sums, a scan over chunks (the states S,
  * X = S C - G forward in time and the adjoints dL/dX, dL/dS backward in time),
@@ -232,6 +232,27 @@ HLA_API size_t hla_backward_workspace_size(const hla_params *p);
 HLA_API hla_status hla_backward_chunked(const hla_params *p, const void *q, const void *k, const void *v,
                                         const void *dout, void *dq, void *dk, void *dv, void *workspace,
                                         size_t workspace_bytes, void *stream);
+
+/*
+ * hla_backward_chunked from a given initial state, with the gradient of that state:
+ * the forward it differentiates is hla_forward_chunked with state_in, so the outputs
+ * continue a stream whose state before the first token is (S, C, m, G, h); the state
+ * enters the recurrence as S_in and X_in = S_in C_in - G_in.  Reverse mode gives, from
+ * the adjoints at the first token (Lam = dL/dX, Om = dL/dS after it, decay g per token),
+ *   dX_in = g^2 Lam,  dG = -dX_in,  dC = S_in^T dX_in,  dS = g Om + dX_in C_in^T,
+ * and zero for m and h (they enter only the normalised denominator).
+ *   state_in    (S, C, m, G, h) fp32 [B*H][...] as for hla_forward_chunked, or NULL
+ *               (zeros; the call is then hla_backward_chunked plus the state gradient);
+ *   d_state_in  five fp32 arrays of the same shapes, written, or NULL (not wanted);
+ *   the rest as for hla_backward_chunked (same workspace size).
+ * HLA_NORMALIZE with a state or its gradient: HLA_ERR_UNSUPPORTED.  With a state or
+ * its gradient the scan between the local sums and the gradients runs on the CUDA
+ * cores (also on the tensor-core shape), plus one launch for the state gradient.
+ */
+HLA_API hla_status hla_backward_chunked_state(const hla_params *p, const void *q, const void *k, const void *v,
+                                              const void *dout, const hla_state *state_in, void *dq, void *dk,
+                                              void *dv, const hla_state *d_state_in, void *workspace,
+                                              size_t workspace_bytes, void *stream);
 
 /* hla_backward_chunked with per-phase tracing: phase_events is NULL (then this is
  * hla_backward_chunked) or four cudaEvent_t handles of the current device, recorded

@@ -164,16 +164,17 @@ def test_backward_rejects_null_misaligned_and_short_workspace(lib):
 
 
 def test_backward_workspace_size_and_empty_sequence(lib):
-    # per (b,h, chunk): six local sums and four states, fp32
+    # per (b,h, chunk): six local sums and four states; per (b,h) the adjoints at the
+    # first token (Lam d x dv, Om d x d) for the gradient of a given state; fp32
     for B, H, n, d, dv, c in [(1, 2, 128, 64, 64, 64), (2, 3, 100, 32, 16, 32), (1, 1, 1, 16, 64, 16)]:
         nch = -(-n // c)
-        want = B * H * nch * (4 * d * d + 6 * d * dv) * 4
+        want = (B * H * nch * (4 * d * d + 6 * d * dv) + B * H * (d * dv + d * d)) * 4
         got = hla.hla_backward_workspace_size(_params(B=B, H=H, n=n, d=d, dv=dv, chunk=c, in_dtype=hla.HLA_F32))
         assert got == want
     # shared key/value heads: plus the fp32 dk, dv of every query head before the group sum
     B, H, n, d, dv, c = 2, 4, 100, 32, 16, 32
     nch = -(-n // c)
-    base = B * H * nch * (4 * d * d + 6 * d * dv) * 4
+    base = (B * H * nch * (4 * d * d + 6 * d * dv) + B * H * (d * dv + d * d)) * 4
     assert hla.hla_backward_workspace_size(_params(B=B, H=H, Hkv=2, n=n, d=d, dv=dv, chunk=c,
                                                    in_dtype=hla.HLA_F32)) == base + B * H * n * (d + dv) * 4
     # no tokens: nothing to compute, no pointer needed
@@ -256,6 +257,17 @@ def test_forward3_workspace_size(lib):
         nch = -(-n // c)
         want = B * H * nch * (4 * d * d + 5 * d * dv) * 4
         assert hla.hla_forward3_workspace_size(_params(B=B, H=H, n=n, d=d, dv=dv, chunk=c)) == want
+
+
+def test_backward_state_rejects_bad_args(lib):
+    L = hla.library()
+    good = ctypes.pointer(hla.hla_state(16, 16, 16, 16, 16))
+    call = lambda p, sin=good, dst=good: L.hla_backward_chunked_state(ctypes.byref(p), 16, 16, 16, 16, sin, 16, 16,
+                                                                       16, dst, 16, 1 << 40, None)
+    assert call(_params(flags=hla.HLA_NORMALIZE)) == hla.HLA_ERR_UNSUPPORTED
+    assert call(_params(), sin=ctypes.pointer(hla.hla_state(16, None, 16, 16, 16))) == hla.HLA_ERR_ARG
+    assert call(_params(), dst=ctypes.pointer(hla.hla_state(16, 16, 8, 16, 16))) == hla.HLA_ERR_ARG
+    assert call(_params(d=48)) == hla.HLA_ERR_UNSUPPORTED
 
 
 def test_decode3_rejects_bad_args(lib):
