@@ -135,18 +135,27 @@ struct Lay {
     static_assert(DV == 64 || DV == 128, "dv");
 };
 
-// Named barrier over `count` threads.
+// Named barrier over `count` threads.  The ids (kBarE, kBarT, kBarAH) are immediates,
+// so that the kernels declare 4 of the 16 hardware barriers (0 is __syncthreads): a
+// register id makes the compiler reserve all 16 for the CTA.
 __device__ __forceinline__ void nbar(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+    if (id == kBarE) asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory");
+    else if (id == kBarT) asm volatile("bar.sync 2, %0;" ::"r"(count) : "memory");
+    else asm volatile("bar.sync 3, %0;" ::"r"(count) : "memory");
 }
 // Named barrier that also ORs a predicate over the participating threads.
 __device__ __forceinline__ bool nbar_or(int id, int count, bool v) {
     uint32_t r;
-    asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.u32 p, %2, 0;\n bar.red.or.pred q, %1, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(r)
-        : "r"(id), "r"((uint32_t)v), "r"(count)
-        : "memory");
+#define HLA_NBAR_OR(ID)                                                                                       \
+    asm volatile(                                                                                             \
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, " #ID ", %2, p;\n selp.u32 %0, 1, 0, q;\n}\n" \
+        : "=r"(r)                                                                                             \
+        : "r"((uint32_t)v), "r"(count)                                                                        \
+        : "memory")
+    if (id == kBarE) HLA_NBAR_OR(1);
+    else if (id == kBarT) HLA_NBAR_OR(2);
+    else HLA_NBAR_OR(3);
+#undef HLA_NBAR_OR
     return r != 0;
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
