@@ -401,8 +401,7 @@ def decode_step(state: State, q, k, v, H: int, gamma=None, normalize: bool = Fal
 def backward(q, k, v, dout, chunk: int, gamma=None, workspace=None, out=None, stream=None,
              normalize: bool = False, eps: float = 0.0, state_in: State | None = None, want_dstate: bool = False):
     """Gradients (dq, dk, dv) of sum(dout * o) for the masked forward o of q, k, v from a
-    zero state, or from ``state_in`` (with ``normalize=True`` the ratio-normalised o; not
-    with a state).  q [B,H,n,d], k [B,Hkv,n,d], v [B,Hkv,n,dv], dout [B,H,n,dv]
+    zero state, or from ``state_in`` (with ``normalize=True`` the ratio-normalised o).  q [B,H,n,d], k [B,Hkv,n,d], v [B,Hkv,n,dv], dout [B,H,n,dv]
     contiguous CUDA tensors of one dtype (bf16 or fp32); gamma [H] fp32 or None.
     ``out`` may hold three preallocated result tensors.  ``want_dstate``: also return the
     gradient with respect to the initial state (a State)."""

@@ -217,13 +217,11 @@ hla_status backward_impl(const hla_params *p, const void *q, const void *k, cons
     hla_status s = check_bwd_params(p);
     if (s != HLA_OK) return s;
     const bool norm = (p->flags & HLA_NORMALIZE) != 0;
-    if ((state_in || d_state_in) && norm)
-        return fail(HLA_ERR_UNSUPPORTED, "a given initial state or its gradient: without HLA_NORMALIZE only");
     if ((s = check_state(state_in, "state_in")) != HLA_OK) return s;
     if ((s = check_state(d_state_in, "d_state_in")) != HLA_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t BH = (size_t)p->B * p->H, D = p->d, DV = p->dv;
-    if (d_state_in) {  // m and h enter only the denominator: their gradient is zero here
+    if (d_state_in && !norm) {  // m and h enter only the denominator: their gradient is zero here
         const size_t sz[2] = {BH * D * 4, BH * D * 4};
         float *dst[2] = {d_state_in->m, d_state_in->h};
         for (int i = 0; i < 2; ++i) {
@@ -233,9 +231,9 @@ hla_status backward_impl(const hla_params *p, const void *q, const void *k, cons
     }
     if (p->n == 0) {  // no tokens: the state gradient is zero
         if (d_state_in) {
-            const size_t sz[3] = {BH * D * D * 4, BH * D * DV * 4, BH * D * DV * 4};
-            float *dst[3] = {d_state_in->S, d_state_in->C, d_state_in->G};
-            for (int i = 0; i < 3; ++i) {
+            const size_t sz[5] = {BH * D * D * 4, BH * D * DV * 4, BH * D * DV * 4, BH * D * 4, BH * D * 4};
+            float *dst[5] = {d_state_in->S, d_state_in->C, d_state_in->G, d_state_in->m, d_state_in->h};
+            for (int i = 0; i < 5; ++i) {
                 cudaError_t e = cudaMemsetAsync(dst[i], 0, sz[i], st);
                 if (e != cudaSuccess) return cuda_fail(e, "state gradient clear");
             }
@@ -265,9 +263,13 @@ hla_status backward_impl(const hla_params *p, const void *q, const void *k, cons
     a.sin_S = state_in ? state_in->S : nullptr;
     a.sin_C = state_in ? state_in->C : nullptr;
     a.sin_G = state_in ? state_in->G : nullptr;
+    a.sin_m = state_in ? state_in->m : nullptr;
+    a.sin_h = state_in ? state_in->h : nullptr;
     a.dS = d_state_in ? d_state_in->S : nullptr;
     a.dC = d_state_in ? d_state_in->C : nullptr;
     a.dG = d_state_in ? d_state_in->G : nullptr;
+    a.dm = d_state_in ? d_state_in->m : nullptr;
+    a.dh = d_state_in ? d_state_in->h : nullptr;
     a.adj0 = d_state_in ? a.workspace + hla::bwd_adj0_offset(*p) : nullptr;
     if (phase_events) {
         for (int i = 0; i < 4; ++i)

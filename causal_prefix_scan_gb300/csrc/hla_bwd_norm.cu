@@ -22,6 +22,12 @@
 // gives each segment's state, an exclusive scan over the segments of a sequence (the
 // concatenation rule of section 4) gives each segment's initial state, and a second
 // forward from those states gives the outputs.
+//
+// From a given initial state (S, C, m, G, h): both forwards start from it, the values'
+// pass from (S, C, G) and the unit values' pass from (S, C1, G1) with m and h in column
+// 0 of C1 and G1 (den is the output of unit values); both backward passes return their
+// state gradients, and dS = dS_1 + dS_2, dC, dG from the values' pass, dm and dh from
+// column 0 of the unit pass's dC1, dG1.
 #include <cstdint>
 #include <cstdio>
 
@@ -81,20 +87,30 @@ __global__ void __launch_bounds__(kEwThreads) norm_upstream_kernel(const float *
 // of every state; each keeps its own copy of the whole prefix C and m (the right
 // factor of the cross terms) in shared memory.
 constexpr int kScanMaxD = 64, kScanRows = 16;
-__global__ void __launch_bounds__(kEwThreads) segment_scan_kernel(StatePtrs seg, StatePtrs pre, int P, int d, int dv,
-                                                                   int H, const float *gamma, int seg_len) {
+// init: the state before the first segment of every sequence (init.S NULL: zeros).
+__global__ void __launch_bounds__(kEwThreads) segment_scan_kernel(StatePtrs seg, StatePtrs pre, StatePtrs init, int P,
+                                                                   int d, int dv, int H, const float *gamma,
+                                                                   int seg_len) {
     __shared__ float sb[kScanRows * kScanMaxD], ca[kScanMaxD * kScanMaxD], ma[kScanMaxD];
     const int seq = blockIdx.x, r0 = blockIdx.y * kScanRows, tid = threadIdx.x;
     const size_t nS = (size_t)d * d, nC = (size_t)d * dv;
     const float f = gamma ? exp2f(log2f(gamma[seq % H]) * (float)seg_len) : 1.f, f2 = f * f;
     {
         const size_t i0 = (size_t)seq * P;
-        for (int e = tid; e < kScanRows * d; e += kEwThreads) pre.S[i0 * nS + (size_t)r0 * d + e] = 0.f;
-        for (int e = tid; e < kScanRows * dv; e += kEwThreads)
-            pre.C[i0 * nC + (size_t)r0 * dv + e] = pre.G[i0 * nC + (size_t)r0 * dv + e] = 0.f;
-        for (int e = tid; e < kScanRows; e += kEwThreads) pre.m[i0 * d + r0 + e] = pre.h[i0 * d + r0 + e] = 0.f;
-        for (size_t e = tid; e < nC; e += kEwThreads) ca[e] = 0.f;
-        for (int e = tid; e < d; e += kEwThreads) ma[e] = 0.f;
+        const bool given = init.S != nullptr;
+        for (int e = tid; e < kScanRows * d; e += kEwThreads)
+            pre.S[i0 * nS + (size_t)r0 * d + e] = given ? init.S[(size_t)seq * nS + (size_t)r0 * d + e] : 0.f;
+        for (int e = tid; e < kScanRows * dv; e += kEwThreads) {
+            const size_t g = (size_t)seq * nC + (size_t)r0 * dv + e;
+            pre.C[i0 * nC + (size_t)r0 * dv + e] = given ? init.C[g] : 0.f;
+            pre.G[i0 * nC + (size_t)r0 * dv + e] = given ? init.G[g] : 0.f;
+        }
+        for (int e = tid; e < kScanRows; e += kEwThreads) {
+            pre.m[i0 * d + r0 + e] = given ? init.m[(size_t)seq * d + r0 + e] : 0.f;
+            pre.h[i0 * d + r0 + e] = given ? init.h[(size_t)seq * d + r0 + e] : 0.f;
+        }
+        for (size_t e = tid; e < nC; e += kEwThreads) ca[e] = given ? init.C[(size_t)seq * nC + e] : 0.f;
+        for (int e = tid; e < d; e += kEwThreads) ma[e] = given ? init.m[(size_t)seq * d + e] : 0.f;
     }
     __syncthreads();
     for (int s = 1; s < P; ++s) {
@@ -125,6 +141,16 @@ __global__ void __launch_bounds__(kEwThreads) segment_scan_kernel(StatePtrs seg,
         for (int e = tid; e < d; e += kEwThreads) ma[e] = f * ma[e] + seg.m[a * d + e];
         __syncthreads();
     }
+}
+
+// d-vectors per pair <-> column 0 of [d][w1] tiles (the other columns zero)
+__global__ void __launch_bounds__(kEwThreads) to_column_kernel(float *dst, const float *src, size_t count, int w1) {
+    for (size_t i = (size_t)blockIdx.x * kEwThreads + threadIdx.x; i < count * w1; i += (size_t)gridDim.x * kEwThreads)
+        dst[i] = (i % w1) == 0 ? src[i / w1] : 0.f;
+}
+__global__ void __launch_bounds__(kEwThreads) from_column_kernel(float *dst, const float *src, size_t count, int w1) {
+    for (size_t i = (size_t)blockIdx.x * kEwThreads + threadIdx.x; i < count; i += (size_t)gridDim.x * kEwThreads)
+        dst[i] = src[i * w1];
 }
 
 __global__ void __launch_bounds__(kEwThreads) repeat_kernel(float *dst, const float *src, int H, int P) {
@@ -213,6 +239,13 @@ NormLayout bwd_norm_layout(const hla_params &p) {
     L.grep = L.P > 1 ? take((size_t)p.H * L.P) : 0;
     L.seg = L.P > 1 ? take(items * sf) : 0;
     L.pre = L.P > 1 ? take(items * sf) : 0;
+    const size_t units = (size_t)p.B * p.H;
+    L.ce = take(units * p.d * w1);
+    L.ge = take(units * p.d * w1);
+    L.ds2 = take(units * p.d * p.d);
+    L.dce = take(units * p.d * w1);
+    L.dge = take(units * p.d * w1);
+    L.zvec = take(units * p.d);
     // bf16 inputs: fp32 copies of q, k, v, g and fp32 results before the final rounding
     L.q32 = wide ? take(rq * p.d) : 0;
     L.k32 = wide ? take(rkv * p.d) : 0;
@@ -257,11 +290,28 @@ hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a0, void *workspa
     unit_value_kernel<<<grid_for(rkv * L.w1), kEwThreads, 0, st>>>(f(L.unit), rkv, L.w1);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_err(e, "operands");
     const hla_params pv = unnormalised(p, p.dv), pe = unnormalised(p, L.w1);
+    // a given initial state: (S, C, G) for the values, (S, C1, G1) with m, h in column 0
+    // for the unit values; m and h of both are unused by the unnormalised passes
+    const bool given = a0.sin_S != nullptr, want = a0.dS != nullptr;
+    const size_t units = (size_t)p.B * p.H, pd = units * p.d;
+    hla_state sv{}, se{};
+    if (given || want) {
+        if ((e = cudaMemsetAsync(f(L.zvec), 0, pd * 4, st)) != cudaSuccess) return cuda_err(e, "state operands");
+    }
+    if (given) {
+        to_column_kernel<<<grid_for(pd * L.w1), kEwThreads, 0, st>>>(f(L.ce), a0.sin_m, pd, L.w1);
+        to_column_kernel<<<grid_for(pd * L.w1), kEwThreads, 0, st>>>(f(L.ge), a0.sin_h, pd, L.w1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_err(e, "state operands");
+        sv = hla_state{const_cast<float *>(a0.sin_S), const_cast<float *>(a0.sin_C), f(L.zvec),
+                       const_cast<float *>(a0.sin_G), f(L.zvec)};
+        se = hla_state{const_cast<float *>(a0.sin_S), f(L.ce), f(L.zvec), f(L.ge), f(L.zvec)};
+    }
+    const hla_state *sv_in = given ? &sv : nullptr, *se_in = given ? &se : nullptr;
     hla_status s;
     if (L.P == 1) {
-        s = hla_forward_chunked(&pv, q, k, v, f(L.num), nullptr, nullptr, ws + L.fwd_ws, L.fwd_ws_bytes, st);
+        s = hla_forward_chunked(&pv, q, k, v, f(L.num), sv_in, nullptr, ws + L.fwd_ws, L.fwd_ws_bytes, st);
         if (s != HLA_OK) return s;
-        s = hla_forward_chunked(&pe, q, k, f(L.unit), f(L.den1), nullptr, nullptr, ws + L.fwd_ws, L.fwd_ws_bytes, st);
+        s = hla_forward_chunked(&pe, q, k, f(L.unit), f(L.den1), se_in, nullptr, ws + L.fwd_ws, L.fwd_ws_bytes, st);
         if (s != HLA_OK) return s;
     } else {
         const int P = L.P;
@@ -289,8 +339,10 @@ hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a0, void *workspa
             float *out = part == 0 ? f(L.num) : f(L.den1);
             s = hla_forward_chunked(&ps, q, k, vv, out, nullptr, &sg, ws + L.fwd_ws, L.fwd_ws_bytes, st);
             if (s != HLA_OK) return s;
+            StatePtrs init{};
+            if (given) init = to_ptrs(part == 0 ? &sv : &se);
             segment_scan_kernel<<<dim3(p.B * p.H, p.d / kScanRows), kEwThreads, 0, st>>>(
-                to_ptrs(&sg), to_ptrs(&pr), P, p.d, dvp, p.H, (p.flags & HLA_DECAY) ? p.gamma : nullptr, p.n / P);
+                to_ptrs(&sg), to_ptrs(&pr), init, P, p.d, dvp, p.H, (p.flags & HLA_DECAY) ? p.gamma : nullptr, p.n / P);
             if ((e = cudaGetLastError()) != cudaSuccess) return cuda_err(e, "segment scan");
             s = hla_forward_chunked(&ps, q, k, vv, out, &pr, nullptr, ws + L.fwd_ws, L.fwd_ws_bytes, st);
             if (s != HLA_OK) return s;
@@ -310,6 +362,7 @@ hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a0, void *workspa
     a.workspace = f(L.bwd_ws);
     a.dk_pair = a.Hkv < a.H ? a.workspace + bwd_pair_offset(pv) : nullptr;
     a.dv_pair = a.dk_pair ? a.dk_pair + rq * p.d : nullptr;
+    a.adj0 = want ? a.workspace + bwd_adj0_offset(pv) : nullptr;  // dS, dC, dG of the values' pass: final
     if ((e = bwd_simt_launch(a, st)) != cudaSuccess) return cuda_err(e, "backward of the numerator");
     if ((e = mark(2)) != cudaSuccess) return cuda_err(e, "event");
     BwdArgs b = a;
@@ -321,7 +374,20 @@ hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a0, void *workspa
     b.grad_v = f(L.dv1);
     b.dk_pair = b.Hkv < b.H ? b.workspace + bwd_pair_offset(pe) : nullptr;
     b.dv_pair = b.dk_pair ? b.dk_pair + rq * p.d : nullptr;
+    b.sin_C = given ? f(L.ce) : nullptr;
+    b.sin_G = given ? f(L.ge) : nullptr;
+    b.dS = want ? f(L.ds2) : nullptr;
+    b.dC = want ? f(L.dce) : nullptr;
+    b.dG = want ? f(L.dge) : nullptr;
+    b.adj0 = want ? b.workspace + bwd_adj0_offset(pe) : nullptr;
     if ((e = bwd_simt_launch(b, st)) != cudaSuccess) return cuda_err(e, "backward of the denominator");
+    if (want) {  // dS += dS of the unit pass; dm, dh from column 0 of its dC, dG
+        sum_kernel<float><<<grid_for(units * p.d * p.d), kEwThreads, 0, st>>>(a0.dS, a0.dS, f(L.ds2),
+                                                                              units * p.d * p.d);
+        from_column_kernel<<<grid_for(pd), kEwThreads, 0, st>>>(a0.dm, f(L.dce), pd, L.w1);
+        from_column_kernel<<<grid_for(pd), kEwThreads, 0, st>>>(a0.dh, f(L.dge), pd, L.w1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_err(e, "state gradient");
+    }
     // 4. dq = dq + dq1, dk = dk + dk1 (and dv), each rounded once to the output type
     if (wide) {
         sum_kernel<__nv_bfloat16><<<grid_for(rq * p.d), kEwThreads, 0, st>>>(

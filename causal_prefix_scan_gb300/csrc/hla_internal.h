@@ -81,9 +81,11 @@ struct BwdArgs {
     float *dk_pair, *dv_pair;  // Hkv < H: fp32 dk, dv of every query head before the group sum
     // the state before the first token (NULL: zeros), fp32 [B*H][d][d], [B*H][d][dv] x 2
     const float *sin_S, *sin_C, *sin_G;
+    const float *sin_m, *sin_h;  // with ratio normalisation: the rest of the state
     // its gradient (dS NULL: not wanted), and the per-pair adjoints at the first token
     // the scan leaves for it (Lam [d][dv], then Om [d][d])
     float *dS, *dC, *dG, *adj0;
+    float *dm, *dh;  // with ratio normalisation
     cudaEvent_t const *events;  // NULL or four events recorded at the phase boundaries
     unsigned *err;              // sticky device status word (bounded waits of the tensor-core kernels)
 };
@@ -105,6 +107,9 @@ struct NormLayout {
     size_t q32, k32, v32, g32, dq32, dk32, dv32;
     int P;              // segments per sequence of the fp32 forwards (1: no split)
     size_t grep, seg, pre;  // decay rates repeated per segment; segment states; their prefixes
+    // a given initial state: the unit-value pass's C and G (m, h in column 0), its state
+    // gradient (S, C, G), and a zero d-vector per pair (the m, h the unnormalised passes ignore)
+    size_t ce, ge, ds2, dce, dge, zvec;
     size_t total;
 };
 NormLayout bwd_norm_layout(const hla_params &p);

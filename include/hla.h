@@ -240,14 +240,18 @@ HLA_API hla_status hla_backward_chunked(const hla_params *p, const void *q, cons
  * enters the recurrence as S_in and X_in = S_in C_in - G_in.  Reverse mode gives, from
  * the adjoints at the first token (Lam = dL/dX, Om = dL/dS after it, decay g per token),
  *   dX_in = g^2 Lam,  dG = -dX_in,  dC = S_in^T dX_in,  dS = g Om + dX_in C_in^T,
- * and zero for m and h (they enter only the normalised denominator).
+ * and zero for m and h without normalisation (they enter only the denominator).  With
+ * HLA_NORMALIZE the chain above runs from the state: the values' pass from (S, C, G),
+ * the unit values' pass from (S, C1, G1) with m, h in column 0 of C1, G1 (Y_in =
+ * S_in m_in - h_in is the unit values' X_in), and dS adds both passes' dS, while dm
+ * and dh are column 0 of the unit pass's dC1, dG1.
  *   state_in    (S, C, m, G, h) fp32 [B*H][...] as for hla_forward_chunked, or NULL
  *               (zeros; the call is then hla_backward_chunked plus the state gradient);
  *   d_state_in  five fp32 arrays of the same shapes, written, or NULL (not wanted);
  *   the rest as for hla_backward_chunked (same workspace size).
- * HLA_NORMALIZE with a state or its gradient: HLA_ERR_UNSUPPORTED.  With a state or
- * its gradient the scan between the local sums and the gradients runs on the CUDA
- * cores (also on the tensor-core shape), plus one launch for the state gradient.
+ * With a state or its gradient the scan between the local sums and the gradients runs
+ * on the CUDA cores (also on the tensor-core shape), plus one launch per pass for the
+ * state gradient.
  */
 HLA_API hla_status hla_backward_chunked_state(const hla_params *p, const void *q, const void *k, const void *v,
                                               const void *dout, const hla_state *state_in, void *dq, void *dk,

@@ -264,7 +264,7 @@ def test_backward_state_rejects_bad_args(lib):
     good = ctypes.pointer(hla.hla_state(16, 16, 16, 16, 16))
     call = lambda p, sin=good, dst=good: L.hla_backward_chunked_state(ctypes.byref(p), 16, 16, 16, 16, sin, 16, 16,
                                                                        16, dst, 16, 1 << 40, None)
-    assert call(_params(flags=hla.HLA_NORMALIZE)) == hla.HLA_ERR_UNSUPPORTED
+    assert call(_params(flags=hla.HLA_NORMALIZE, eps=-1.0)) == hla.HLA_ERR_ARG
     assert call(_params(), sin=ctypes.pointer(hla.hla_state(16, None, 16, 16, 16))) == hla.HLA_ERR_ARG
     assert call(_params(), dst=ctypes.pointer(hla.hla_state(16, 16, 8, 16, 16))) == hla.HLA_ERR_ARG
     assert call(_params(d=48)) == hla.HLA_ERR_UNSUPPORTED

@@ -120,3 +120,39 @@ def test_state_gradient_of_an_empty_sequence_is_zero():
     hla.hla_sync_status()
     for t in ds.astuple():
         assert not torch.any(t)
+
+
+@pytest.mark.parametrize("dtype,d,dv,chunk", [("f32", 32, 16, 16), ("f32", 16, 32, 32), ("bf16", 64, 64, 64)])
+@pytest.mark.parametrize("decay", [False, True])
+def test_normalised_backward_from_state(dtype, d, dv, chunk, decay):
+    """Ratio-normalised: the state a forward over a first part leaves (positive
+    denominators with elu+1 features), then the gradient of the second part and of that
+    state, all five arrays (m and h now carry the denominator's gradient)."""
+    cut, eps = 70, 1e-3
+    w = small(n=cut + 129, d=d, dv=dv, chunk=chunk, dtype=dtype, decay=decay, qk="elu1", seed=65)
+    x = W.make_inputs(w)
+    gam = None if x.get("gamma") is None else np.asarray(x["gamma"], np.float64)
+    _, st = oracle.forward(x["q"][:, :, :cut], x["k"][:, :, :cut], x["v"][:, :, :cut], gamma=gam, normalize=True,
+                           eps=eps)
+    second = {n: np.ascontiguousarray(x[n][:, :, cut:]) for n in ("q", "k", "v")}
+    second["gamma"] = x["gamma"]
+    w2 = small(n=129, d=d, dv=dv, chunk=chunk, dtype=dtype, decay=decay, qk="elu1", seed=66)
+    g = W.make_dout(w2)
+    dq, dk, dv_, ds = oracle.backward(second["q"], second["k"], second["v"], g, gam, normalize=True, eps=eps,
+                                      state_in=st, want_dstate=True)
+    q, k, v = (to_dev(second[n], dtype) for n in ("q", "k", "v"))
+    gd = None if gam is None else torch.from_numpy(np.asarray(gam, np.float32)).cuda()
+    gq, gk, gv, gs = hla.backward(q, k, v, to_dev(g, dtype), chunk=chunk, gamma=gd, normalize=True, eps=eps,
+                                  state_in=state_dev(st), want_dstate=True)
+    hla.hla_sync_status()
+    tol = TOL_F32 if dtype == "f32" else TOL_BF16
+    for name, a, b in (("dq", gq, dq), ("dk", gk, dk), ("dv", gv, dv_)):
+        e = per_pair_errors(a.float().cpu().numpy(), b).max()
+        assert e <= tol, f"{name}: {e:.3e}"
+    units = w.B * w.H
+    for name in ("S", "C", "m", "G", "h"):
+        a = getattr(gs, name).double().cpu().numpy().reshape(units, 1, -1)
+        b = getattr(ds, name).reshape(units, 1, -1)
+        e = per_pair_errors(a, b).max()
+        assert e <= tol, f"d{name}: {e:.3e}"
+
