@@ -30,7 +30,7 @@ __all__ = [
     "hla_forward_workspace_size", "hla_forward_kernel", "hla_forward_chunked", "hla_state_combine",
     "hla_decode_step", "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
     "hla_backward_workspace_size", "hla_backward_chunked", "hla_backward_chunked_traced",
-    "hla_backward_chunked_state", "hla_state3", "hla_forward3_workspace_size", "hla_forward3_chunked", "hla_forward3_chunked_traced",
+    "hla_backward_chunked_state", "hla_state3", "hla_state3_combine", "state3_combine", "hla_forward3_workspace_size", "hla_forward3_chunked", "hla_forward3_chunked_traced",
     "hla_decode3_step", "State3", "forward3", "decode3_step", "hla_selftest_expired_wait",
     "State", "new_workspace", "forward", "state_combine", "decode_step", "backward",
 ]
@@ -40,7 +40,7 @@ EXPORTS = ("hla_forward_workspace_size", "hla_forward_chunked", "hla_state_combi
            "hla_sync_status", "hla_status_string", "hla_last_error", "hla_forward_chunked_noalloc",
            "hla_backward_workspace_size", "hla_backward_chunked", "hla_backward_chunked_traced",
            "hla_forward3_workspace_size", "hla_forward3_chunked", "hla_forward3_chunked_traced", "hla_decode3_step",
-           "hla_selftest_expired_wait", "hla_forward_kernel", "hla_backward_chunked_state")
+           "hla_selftest_expired_wait", "hla_forward_kernel", "hla_backward_chunked_state", "hla_state3_combine")
 
 
 class HlaError(RuntimeError):
@@ -63,7 +63,8 @@ class hla_state(ctypes.Structure):
 
 class hla_state3(ctypes.Structure):
     _fields_ = [("S", ctypes.c_void_p), ("P", ctypes.c_void_p), ("T", ctypes.c_void_p),
-                ("m", ctypes.c_void_p), ("h", ctypes.c_void_p)]
+                ("m", ctypes.c_void_p), ("h", ctypes.c_void_p),
+                ("SQ", ctypes.c_void_p), ("MQP", ctypes.c_void_p), ("MKQ", ctypes.c_void_p), ("mqm", ctypes.c_void_p)]
 
 
 _lib = None
@@ -103,11 +104,13 @@ def library(path: str | None = None):
     lib.hla_forward3_chunked_traced.argtypes = [P, vp, vp, vp, vp, S3, S3, vp, sz, vp,
                                                 ctypes.POINTER(ctypes.c_void_p)]
     lib.hla_decode3_step.argtypes = [i, i, i, i, i, u, f, vp, S3, vp, vp, vp, vp, vp]
+    lib.hla_state3_combine.argtypes = [i, i, i, u, S3, S3, S3, vp, vp]
     lib.hla_sync_status.argtypes = [vp]
     lib.hla_selftest_expired_wait.argtypes = [vp]
     for fn in (lib.hla_forward_chunked, lib.hla_state_combine, lib.hla_decode_step, lib.hla_sync_status,
                lib.hla_backward_chunked, lib.hla_backward_chunked_traced, lib.hla_forward3_chunked,
-               lib.hla_forward3_chunked_traced, lib.hla_decode3_step, lib.hla_selftest_expired_wait):
+               lib.hla_forward3_chunked_traced, lib.hla_decode3_step, lib.hla_selftest_expired_wait,
+               lib.hla_state3_combine):
         fn.restype = ctypes.c_int
     lib.hla_status_string.argtypes = [ctypes.c_int]
     lib.hla_status_string.restype = ctypes.c_char_p
@@ -229,7 +232,8 @@ def hla_backward_chunked_traced(params: hla_params, q, k, v, dout, dq, dk, dv, w
 def _state3_struct(st):
     if st is None:
         return None
-    return ctypes.byref(hla_state3(*(_ptr(x) for x in (st.S, st.P, st.T, st.m, st.h))))
+    return ctypes.byref(hla_state3(*(_ptr(x) for x in (st.S, st.P, st.T, st.m, st.h, st.SQ, st.MQP, st.MKQ,
+                                                         st.mqm))))
 
 
 def _events(events):
@@ -263,6 +267,11 @@ def hla_decode3_step(N: int, H: int, d: int, dv: int, dtype: int, flags: int, ep
                      stream=None) -> None:
     _check(library().hla_decode3_step(N, H, d, dv, dtype, flags, eps, _ptr(gamma), _state3_struct(state), _ptr(q),
                                       _ptr(k), _ptr(v), _ptr(o), _stream(stream)))
+
+
+def hla_state3_combine(count: int, d: int, dv: int, flags: int, A, B, out, decay_pow=None, stream=None) -> None:
+    _check(library().hla_state3_combine(count, d, dv, flags, _state3_struct(A), _state3_struct(B),
+                                        _state3_struct(out), _ptr(decay_pow), _stream(stream)))
 
 
 def hla_selftest_expired_wait(stream=None) -> None:
@@ -305,26 +314,37 @@ class State:
 class State3:
     """Third-order streaming state of `units` pairs, fp32: S [U,d,d] (key moment S^K),
     P [U,d,dv] (key-value moment), T [U,d,dv] (masked third-order accumulator); with
-    ratio normalisation also m [U,d] (key mass) and h [U,d] (T of a unit value)."""
+    ratio normalisation also m [U,d] (key mass) and h [U,d] (T of a unit value); with
+    the segment maps (for state3_combine) SQ [U,d,d], MQP [U,d,dv], MKQ [U,d,d] and,
+    normalised, mqm [U,d]."""
     S: object
     P: object
     T: object
     m: object = None
     h: object = None
+    SQ: object = None
+    MQP: object = None
+    MKQ: object = None
+    mqm: object = None
 
     @staticmethod
-    def empty(units: int, d: int, dv: int, device="cuda", normalize: bool = False) -> "State3":
-        import torch
-        z = lambda *s: torch.empty(*s, dtype=torch.float32, device=device)
+    def _make(z, units, d, dv, normalize, maps):
         mh = (z(units, d), z(units, d)) if normalize else (None, None)
-        return State3(z(units, d, d), z(units, d, dv), z(units, d, dv), *mh)
+        mp = (z(units, d, d), z(units, d, dv), z(units, d, d), z(units, d) if normalize else None) if maps else \
+            (None,) * 4
+        return State3(z(units, d, d), z(units, d, dv), z(units, d, dv), *mh, *mp)
 
     @staticmethod
-    def zeros(units: int, d: int, dv: int, device="cuda", normalize: bool = False) -> "State3":
+    def empty(units: int, d: int, dv: int, device="cuda", normalize: bool = False, maps: bool = False) -> "State3":
         import torch
-        z = lambda *s: torch.zeros(*s, dtype=torch.float32, device=device)
-        mh = (z(units, d), z(units, d)) if normalize else (None, None)
-        return State3(z(units, d, d), z(units, d, dv), z(units, d, dv), *mh)
+        return State3._make(lambda *s: torch.empty(*s, dtype=torch.float32, device=device), units, d, dv, normalize,
+                            maps)
+
+    @staticmethod
+    def zeros(units: int, d: int, dv: int, device="cuda", normalize: bool = False, maps: bool = False) -> "State3":
+        import torch
+        return State3._make(lambda *s: torch.zeros(*s, dtype=torch.float32, device=device), units, d, dv, normalize,
+                            maps)
 
 
 def _dtype_code(t) -> int:
@@ -421,7 +441,7 @@ def backward(q, k, v, dout, chunk: int, gamma=None, workspace=None, out=None, st
 
 
 def forward3(q, k, v, chunk: int, state_in: State3 | None = None, return_state: bool = False, out=None,
-             workspace=None, stream=None, gamma=None, normalize: bool = False, eps: float = 0.0):
+             workspace=None, stream=None, gamma=None, normalize: bool = False, eps: float = 0.0, maps: bool = False):
     """Masked third-order HLA forward.  q, k [B,H,n,d], v [B,H,n,dv] contiguous CUDA
     tensors (bf16 or fp32); gamma: [H] fp32 CUDA tensor of decay rates or None;
     normalize: o = num / (den + eps).  Returns o (and the final State3)."""
@@ -431,9 +451,20 @@ def forward3(q, k, v, chunk: int, state_in: State3 | None = None, return_state: 
     need = hla_forward3_workspace_size(p)
     if workspace is None and need:
         workspace = new_workspace(need, device=q.device)
-    st = State3.empty(p.B * p.H, p.d, p.dv, device=q.device, normalize=normalize) if return_state else None
+    st = State3.empty(p.B * p.H, p.d, p.dv, device=q.device, normalize=normalize, maps=maps) if return_state else None
     hla_forward3_chunked(p, q, k, v, o, state_in, st, workspace, need if workspace is not None else 0, stream)
     return (o, st) if return_state else o
+
+
+def state3_combine(A: State3, B: State3, decay_pow=None, normalize: bool = False, out: State3 | None = None,
+                   stream=None) -> State3:
+    """Concatenation (A before B) of third-order states with their segment maps, item by
+    item; decay_pow [U] fp32 = gamma^(tokens of B) or None."""
+    units, d, dv = A.P.shape
+    if out is None:
+        out = State3.empty(units, d, dv, device=A.P.device, normalize=normalize, maps=True)
+    hla_state3_combine(units, d, dv, HLA_NORMALIZE if normalize else 0, A, B, out, decay_pow, stream)
+    return out
 
 
 def decode3_step(state: State3, q, k, v, out=None, stream=None, H: int = 1, gamma=None, normalize: bool = False,

@@ -327,12 +327,14 @@ hla_status check_fwd3_params(const hla_params *p) {
     return HLA_OK;
 }
 
-hla_status check_state3(const hla_state3 *s, const char *name, bool normalize) {
+hla_status check_state3(const hla_state3 *s, const char *name, bool normalize, bool maps = false) {
     if (!s) return HLA_OK;
     if (!s->S || !s->P || !s->T) return fail(HLA_ERR_ARG, "%s: S, P, T must be set", name);
     if (!aligned16(s->S) || !aligned16(s->P) || !aligned16(s->T))
         return fail(HLA_ERR_ARG, "%s: pointers must be 16-byte aligned", name);
     if (normalize && (!s->m || !s->h)) return fail(HLA_ERR_ARG, "%s: m and h must be set with HLA_NORMALIZE", name);
+    if (maps && (!s->SQ || !s->MQP || !s->MKQ || (normalize && !s->mqm)))
+        return fail(HLA_ERR_ARG, "%s: the segment maps SQ, MQP, MKQ (and mqm with HLA_NORMALIZE) must be set", name);
     return HLA_OK;
 }
 }  // namespace
@@ -355,8 +357,9 @@ hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const
     hla_status s = check_fwd3_params(p);
     if (s != HLA_OK) return s;
     const bool norm = (p->flags & HLA_NORMALIZE) != 0;
-    if ((s = check_state3(state_in, "state_in", norm)) != HLA_OK) return s;
-    if ((s = check_state3(state_out, "state_out", norm)) != HLA_OK) return s;
+    const bool maps = state_out && state_out->SQ;  // the segment maps are wanted
+    if ((s = check_state3(state_in, "state_in", norm, maps)) != HLA_OK) return s;
+    if ((s = check_state3(state_out, "state_out", norm, maps)) != HLA_OK) return s;
     if (state_in && state_out && (state_in->S == state_out->S || state_in->P == state_out->P || state_in->T == state_out->T ||
                                   (norm && (state_in->m == state_out->m || state_in->h == state_out->h))))
         return fail(HLA_ERR_ARG, "state_out may not alias state_in");
@@ -364,12 +367,17 @@ hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const
     if (p->n == 0) {  // no tokens: state_out = state_in (or zeros)
         if (!state_out) return HLA_OK;
         const size_t BH = (size_t)p->B * p->H, D = p->d, DV = p->dv;
-        const size_t sz[5] = {BH * D * D * 4, BH * D * DV * 4, BH * D * DV * 4, BH * D * 4, BH * D * 4};
-        float *dst[5] = {state_out->S, state_out->P, state_out->T, state_out->m, state_out->h};
-        for (int i = 0; i < (norm ? 5 : 3); ++i) {
+        const size_t sz[9] = {BH * D * D * 4, BH * D * DV * 4, BH * D * DV * 4, BH * D * 4, BH * D * 4,
+                              BH * D * D * 4, BH * D * DV * 4, BH * D * D * 4, BH * D * 4};
+        float *dst[9] = {state_out->S, state_out->P, state_out->T, state_out->m, state_out->h,
+                         state_out->SQ, state_out->MQP, state_out->MKQ, state_out->mqm};
+        const bool used[9] = {true, true, true, norm, norm, maps, maps, maps, maps && norm};
+        for (int i = 0; i < 9; ++i) {
+            if (!used[i]) continue;
             cudaError_t e;
             if (state_in) {
-                const float *src[5] = {state_in->S, state_in->P, state_in->T, state_in->m, state_in->h};
+                const float *src[9] = {state_in->S, state_in->P, state_in->T, state_in->m, state_in->h,
+                                       state_in->SQ, state_in->MQP, state_in->MKQ, state_in->mqm};
                 e = cudaMemcpyAsync(dst[i], src[i], sz[i], cudaMemcpyDeviceToDevice, st);
             } else {
                 e = cudaMemsetAsync(dst[i], 0, sz[i], st);
@@ -402,6 +410,12 @@ hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const
     a.sout_S = state_out ? state_out->S : nullptr;
     a.sout_P = state_out ? state_out->P : nullptr;
     a.sout_T = state_out ? state_out->T : nullptr;
+    a.sin_SQ = maps && state_in ? state_in->SQ : nullptr;
+    a.sin_MQP = maps && state_in ? state_in->MQP : nullptr;
+    a.sin_MKQ = maps && state_in ? state_in->MKQ : nullptr;
+    a.sout_SQ = maps ? state_out->SQ : nullptr;
+    a.sout_MQP = maps ? state_out->MQP : nullptr;
+    a.sout_MKQ = maps ? state_out->MKQ : nullptr;
     a.workspace = static_cast<float *>(workspace);
     a.events = reinterpret_cast<cudaEvent_t const *>(phase_events);
     cudaError_t e = status_ptr(&a.err);
@@ -412,12 +426,32 @@ hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const
         nm.h_in = state_in ? state_in->h : nullptr;
         nm.m_out = state_out ? state_out->m : nullptr;
         nm.h_out = state_out ? state_out->h : nullptr;
+        nm.mqm_in = maps && state_in ? state_in->mqm : nullptr;
+        nm.mqm_out = maps ? state_out->mqm : nullptr;
         nm.eps = p->eps;
         e = hla::fwd3_norm_launch(a, nm, st);
     } else {
         e = hla::fwd3_launch(a, st);
     }
     if (e != cudaSuccess) return cuda_fail(e, "third-order forward launch");
+    return HLA_OK;
+}
+
+hla_status hla_state3_combine(int count, int d, int dv, unsigned flags, const hla_state3 *A, const hla_state3 *B,
+                              const hla_state3 *out, const float *decay_pow, void *stream) {
+    if (count < 0) return fail(HLA_ERR_ARG, "need count >= 0");
+    auto ok = [](int x) { return x == 16 || x == 32 || x == 64; };
+    if (!ok(d) || !ok(dv)) return fail(HLA_ERR_UNSUPPORTED, "d, dv must be in {16,32,64} (got %d, %d)", d, dv);
+    if (flags & ~(unsigned)HLA_NORMALIZE) return fail(HLA_ERR_UNSUPPORTED, "flags must be 0 or HLA_NORMALIZE");
+    if (!A || !B || !out) return fail(HLA_ERR_ARG, "A, B, out must be set");
+    const bool norm = (flags & HLA_NORMALIZE) != 0;
+    hla_status s;
+    if ((s = check_state3(A, "A", norm, true)) != HLA_OK) return s;
+    if ((s = check_state3(B, "B", norm, true)) != HLA_OK) return s;
+    if ((s = check_state3(out, "out", norm, true)) != HLA_OK) return s;
+    cudaError_t e = hla::state3_combine_launch(count, d, dv, norm, *A, *B, *out, decay_pow,
+                                               static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "third-order combine launch");
     return HLA_OK;
 }
 

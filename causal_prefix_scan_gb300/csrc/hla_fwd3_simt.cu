@@ -236,7 +236,7 @@ constexpr int kUnit = 16;  // width of the unit-value tile of the denominator pa
 // type of the inputs, [rows][16], a one in column 0 of E), and the denominator pass's
 // states (P and T of width 16 before and after, S after).
 struct NormWs {
-    size_t pass, e, den, pin, tin, pout, tout, sscr, total;
+    size_t pass, e, den, pin, tin, pout, tout, sscr, mqpin, mqpout, sqs, mkqs, total;
 };
 NormWs norm_ws(const hla_params &p) {
     NormWs w;
@@ -252,6 +252,12 @@ NormWs norm_ws(const hla_params &p) {
     w.pout = take(units * p.d * kUnit * 4);
     w.tout = take(units * p.d * kUnit * 4);
     w.sscr = take(units * (size_t)p.d * p.d * 4);
+    // the unit values' segment maps: M^QP with mqm in column 0, before and after; S^Q and
+    // M^KQ of that pass (equal to the values' ones) land in scratch
+    w.mqpin = take(units * p.d * kUnit * 4);
+    w.mqpout = take(units * p.d * kUnit * 4);
+    w.sqs = take(units * (size_t)p.d * p.d * 4);
+    w.mkqs = take(units * (size_t)p.d * p.d * 4);
     w.total = o;
     return w;
 }
@@ -300,6 +306,7 @@ cudaError_t norm_t(const Fwd3Args &a0, const Norm3 &nm, cudaStream_t st) {
         to_column_kernel<<<grid_for(pd * kUnit), kThreads, 0, st>>>(f(w.pin), nm.m_in, pd);
         to_column_kernel<<<grid_for(pd * kUnit), kThreads, 0, st>>>(f(w.tin), nm.h_in, pd);
     }
+    if (nm.mqm_in) to_column_kernel<<<grid_for(pd * kUnit), kThreads, 0, st>>>(f(w.mqpin), nm.mqm_in, pd);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // numerator: the forward of the values, into o
     Fwd3Args a = a0;
@@ -318,6 +325,10 @@ cudaError_t norm_t(const Fwd3Args &a0, const Norm3 &nm, cudaStream_t st) {
     b.sout_S = nm.m_out ? f(w.sscr) : nullptr;
     b.sout_P = nm.m_out ? f(w.pout) : nullptr;
     b.sout_T = nm.m_out ? f(w.tout) : nullptr;
+    b.sin_MQP = nm.mqm_in ? f(w.mqpin) : nullptr;  // S^Q, M^KQ of state_in: those of the values
+    b.sout_SQ = a0.sout_SQ ? f(w.sqs) : nullptr;
+    b.sout_MQP = a0.sout_SQ ? f(w.mqpout) : nullptr;
+    b.sout_MKQ = a0.sout_SQ ? f(w.mkqs) : nullptr;
     if ((e = launch_c<T>(b, st)) != cudaSuccess) return e;
     if ((e = mark(2)) != cudaSuccess) return e;
     ratio_kernel<T><<<grid_for(rows * a0.dv), kThreads, 0, st>>>(static_cast<T *>(a0.o), den, rows, a0.dv, nm.eps);
@@ -325,6 +336,7 @@ cudaError_t norm_t(const Fwd3Args &a0, const Norm3 &nm, cudaStream_t st) {
         from_column_kernel<<<grid_for(pd), kThreads, 0, st>>>(nm.m_out, f(w.pout), pd);
         from_column_kernel<<<grid_for(pd), kThreads, 0, st>>>(nm.h_out, f(w.tout), pd);
     }
+    if (nm.mqm_out) from_column_kernel<<<grid_for(pd), kThreads, 0, st>>>(nm.mqm_out, f(w.mqpout), pd);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     return mark(3);
 }

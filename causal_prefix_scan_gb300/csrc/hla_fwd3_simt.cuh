@@ -382,6 +382,7 @@ cudaError_t launch_t(const Fwd3Args &a, cudaStream_t st) {
     } else {
         fwd3_out_kernel<T, C, D, DV><<<units * nch, kThreads, b3, st>>>(a);
     }
+    if (a.sout_SQ && (e = fwd3_maps_launch(a, st)) != cudaSuccess) return e;
     if ((e = mark(3)) != cudaSuccess) return e;
     return cudaGetLastError();
 }

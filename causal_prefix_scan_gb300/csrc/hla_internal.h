@@ -123,6 +123,10 @@ struct Fwd3Args {
     void *o;
     const float *sin_S, *sin_P, *sin_T;  // state before the first token (all NULL: zeros)
     float *sout_S, *sout_P, *sout_T;     // state after the last token (all NULL: skip)
+    // segment maps S^Q, M^QP, M^KQ: written with the state when sout_SQ is set, composed
+    // onto those of state_in (NULL: a state_in without maps, or none)
+    const float *sin_SQ, *sin_MQP, *sin_MKQ;
+    float *sout_SQ, *sout_MQP, *sout_MKQ;
     float *workspace;
     cudaEvent_t const *events;  // NULL or four events recorded at the phase boundaries
     unsigned *err;              // sticky device status word (bounded waits of the tensor-core kernels)
@@ -149,11 +153,17 @@ cudaError_t fwd3_launch(const Fwd3Args &a, cudaStream_t st);
 // (out) the tokens; NULL for zeros / not wanted.  The workspace is fwd3_workspace(p)
 // with HLA_NORMALIZE.
 struct Norm3 {
-    const float *m_in, *h_in;
-    float *m_out, *h_out;
+    const float *m_in, *h_in, *mqm_in;
+    float *m_out, *h_out, *mqm_out;  // mqm: the M^QP of a unit value (with the maps only)
     float eps;
 };
 cudaError_t fwd3_norm_launch(const Fwd3Args &a, const Norm3 &nm, cudaStream_t st);
+// The segment maps of a forward that has run (its local sums and prefix states are in
+// a.workspace) into a.sout_SQ, a.sout_MQP, a.sout_MKQ.
+cudaError_t fwd3_maps_launch(const Fwd3Args &a, cudaStream_t st);
+// hla_state3_combine on the device (d, dv in {16,32,64}).
+cudaError_t state3_combine_launch(int count, int d, int dv, bool norm, const hla_state3 &A, const hla_state3 &B,
+                                  const hla_state3 &out, const float *decay_pow, cudaStream_t st);
 cudaError_t decode3_launch(const Decode3Args &a, cudaStream_t st);
 
 // Set this thread's last-error message and return `s`.

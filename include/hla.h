@@ -287,10 +287,19 @@ HLA_API hla_status hla_backward_chunked_traced(const hla_params *p, const void *
  * h_t = g^3 h + (S^K_t q)(m_t . q) (T of a unit value; it combines the cross summaries
  * h^(1..3) the section names as T combines G^(1..3)).  m [d] and h [d] are then part of
  * the state; without HLA_NORMALIZE they are not used (may be NULL).
+ *
+ * Segment maps (section 4, "Derde-orde scans"): to concatenate two states with
+ * hla_state3_combine, each also carries the maps of its tokens, S^Q = sum q q^T [d][d],
+ * M^QP = sum_b q_b q_b^T P_b [d][dv] (the map P -> S^K_A M^QP_B), M^KQ = sum_b S^K_b q_b
+ * q_b^T [d][d] (the map P -> M^KQ_B P, named M^KQP), and with normalisation mqm [d],
+ * the M^QP of a unit value (so M^KQ m is the map M^KQm).  The maps are optional: the
+ * forward writes them when state_out->SQ is set (then state_in, if given, must carry
+ * them too), and the decode step neither reads nor writes them.
  */
 typedef struct {
     float *S, *P, *T;
     float *m, *h;
+    float *SQ, *MQP, *MKQ, *mqm;
 } hla_state3;
 
 /* Bytes of device workspace hla_forward3_chunked needs (0 for invalid parameters). */
@@ -337,6 +346,22 @@ HLA_API hla_status hla_forward3_chunked_traced(const hla_params *p, const void *
 HLA_API hla_status hla_decode3_step(int N, int H, int d, int dv, hla_dtype dtype, unsigned flags, float eps,
                                     const float *gamma, const hla_state3 *state, const void *q, const void *k,
                                     const void *v, void *o, void *stream);
+
+/*
+ * Concatenation of third-order states with their segment maps (section 4, "Derde-orde
+ * scans"), segment A before segment B, for `count` independent items; with decay
+ * f = decay_pow[i] = gamma^(tokens of B) (NULL: 1):
+ *   S^K = f S^K_A + S^K_B,  S^Q = f S^Q_A + S^Q_B,  P = f P_A + P_B,
+ *   T = f^3 T_A + T_B + f S^K_A M^QP_B + f M^KQ_B P_A + f^2 S^K_A S^Q_B P_A,
+ *   M^QP = f^2 M^QP_A + M^QP_B + f S^Q_B P_A,   M^KQ = f^2 M^KQ_A + M^KQ_B + f S^K_A S^Q_B,
+ * and with HLA_NORMALIZE the unit column likewise (m as P, h as T, mqm as M^QP).
+ * A, B, out: hla_state3 with S, P, T, SQ, MQP, MKQ (and m, h, mqm with HLA_NORMALIZE),
+ * fp32 [count][...]; out may alias A or B (each item is read whole before it is
+ * written).  flags: 0 or HLA_NORMALIZE; d, dv in {16, 32, 64}.  One launch on `stream`.
+ */
+HLA_API hla_status hla_state3_combine(int count, int d, int dv, unsigned flags, const hla_state3 *A,
+                                      const hla_state3 *B, const hla_state3 *out, const float *decay_pow,
+                                      void *stream);
 
 /* Self-test of the failure path: launches one CTA that waits, with the library's
  * bounded barrier wait (a short poll limit), on a barrier that nothing completes.  The

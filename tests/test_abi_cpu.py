@@ -270,6 +270,23 @@ def test_backward_state_rejects_bad_args(lib):
     assert call(_params(d=48)) == hla.HLA_ERR_UNSUPPORTED
 
 
+def test_state3_combine_rejects_bad_args(lib):
+    L = hla.library()
+    full = ctypes.pointer(hla.hla_state3(16, 16, 16, 16, 16, 16, 16, 16, 16))
+    nomaps = ctypes.pointer(hla.hla_state3(16, 16, 16, 16, 16))
+    call = lambda count=2, d=64, dv=64, fl=0, A=full, B=full, out=full: L.hla_state3_combine(count, d, dv, fl, A, B,
+                                                                                             out, None, None)
+    assert call(count=-1) == hla.HLA_ERR_ARG
+    assert call(d=128) == hla.HLA_ERR_UNSUPPORTED
+    assert call(fl=hla.HLA_DECAY) == hla.HLA_ERR_UNSUPPORTED
+    assert call(A=None) == hla.HLA_ERR_ARG
+    assert call(B=nomaps) == hla.HLA_ERR_ARG
+    assert call(count=0) == hla.HLA_OK  # nothing to do
+    # a forward that wants the maps needs them on a given state_in too
+    sout = ctypes.pointer(hla.hla_state3(16, 16, 16, 16, 16, 16, 16, 16, 16))
+    assert _f3call(_params(), sin=nomaps, sout=sout) == hla.HLA_ERR_ARG
+
+
 def test_decode3_rejects_bad_args(lib):
     L = hla.library()
     s3 = ctypes.pointer(hla.hla_state3(16, 16, 16))
