@@ -372,7 +372,7 @@ def make_params(q, v, chunk: int, gamma=None, normalize: bool = False, eps: floa
 
 
 def new_workspace(nbytes: int, device="cuda"):
-    """A zeroed device workspace of `nbytes` (the forward call keeps it zeroed between calls)."""
+    """A zeroed device workspace of `nbytes` (each forward call leaves it ready for the next)."""
     import torch
     return torch.zeros(max(int(nbytes), 1), dtype=torch.uint8, device=device)
 

@@ -8,6 +8,28 @@
 
 namespace hla {
 namespace chunktc {
+
+// One elementwise scan over the chunks of every pair: out[ch] = R, R = f_ch R + in[ch],
+// f_ch = g^{power * L_ch} (1 without decay), in chunk order (reverse: last chunk first).
+struct PrefixJob {
+    const float *in;
+    size_t in_stride, in_off;  // element e of chunk ch of pair u at in[(u * nch + ch) * in_stride + in_off + e]
+    float *out;
+    size_t out_stride, out_off;
+    const float *init;  // [units][count] or null (zeros)
+    float *fin;         // [units][count] or null
+    int count, reverse, power;
+};
+
+struct PrefixArgs {
+    PrefixJob job[2];
+    int njobs, units, nch, n, chunk, H;
+    const float *gamma;  // per head, or null (no decay)
+};
+
+// Launches the elementwise scans of `a` (hla_scan_tc.cu).
+cudaError_t chunk_prefix(const PrefixArgs &a, cudaStream_t st);
+
 namespace {
 
 constexpr int kTc = 256;

@@ -307,15 +307,42 @@ HLA_DEVICE float ex2_approx(float y) {
 // g^x for x >= 0 with g in [0,1]; lg = log2(g) (may be -inf).  0^0 = 1.
 HLA_DEVICE float gpow(float lg, float x) { return x == 0.f ? 1.f : ex2_approx(lg * x); }
 
-// End of a kernel whose CTAs order themselves by a ticket and publish release flags:
-// the CTA that finishes last returns the two header counters (ticket, done) and the
-// flags to zero, so that the next call needs no clearing launch.  Every thread of the
-// CTA calls this once the CTA has read its last flag and its stores are complete; the
-// last CTA's threads share the clearing stores.  fb may be null.
-HLA_DEVICE void finish_grid(unsigned *ticket, unsigned *fa, unsigned *fb, int nflags, volatile unsigned *s_last) {
+// Per-call ordering of the CTAs of a forward launch through its workspace header.
+// Header words 0-1 form one 64-bit word: the count of tickets taken (low half) and the
+// call generation g (high half); word 2 counts finished CTAs in the one call that
+// needs it.  Every CTA takes its ticket and g in one atomic, and the release flags of
+// this call carry the tag g + 1, which a zero (never written) flag and every flag of an
+// earlier call differ from.  The CTA that takes the last ticket starts generation g + 1
+// at once: every ticket of this call is out, and the next launch on the workspace
+// begins after this one ends, so no CTA clears anything when the call ends.  The tag
+// 0xFFFFFFFF is the exception: that call keeps the header, and its last CTA to finish
+// zeroes every flag and the header (generation 0), so a tag returns only after the
+// flags have been cleared.
+struct CallTicket {
+    unsigned ticket, tag;
+};
+constexpr unsigned kTagWrap = 0xFFFFFFFFu;
+
+// One thread per CTA.
+HLA_DEVICE CallTicket take_ticket(unsigned *hdr) {
+    unsigned long long *w = reinterpret_cast<unsigned long long *>(hdr);
+    const unsigned long long old = atomicAdd(w, 1ull);
+    CallTicket t;
+    t.ticket = (unsigned)old;
+    t.tag = (unsigned)(old >> 32) + 1u;
+    if (t.ticket == gridDim.x - 1 && t.tag != kTagWrap) atomicExch(w, (unsigned long long)t.tag << 32);
+    return t;
+}
+
+// End of the call with tag kTagWrap (a no-op for every other tag): the CTA that finishes
+// last zeroes the flags and the header.  Every thread of the CTA calls this once the CTA
+// has read its last flag; the last CTA's threads share the clearing stores.  fb may be null.
+HLA_DEVICE void finish_call(unsigned *hdr, unsigned tag, unsigned *fa, unsigned *fb, int nflags,
+                            volatile unsigned *s_last) {
+    if (tag != kTagWrap) return;
     if (threadIdx.x == 0) {
         __threadfence();
-        const unsigned done = atomicAdd(ticket + 1, 1u);
+        const unsigned done = atomicAdd(hdr + 2, 1u);
         __threadfence();
         *s_last = (done == gridDim.x - 1) ? 1u : 0u;
     }
@@ -327,8 +354,9 @@ HLA_DEVICE void finish_grid(unsigned *ticket, unsigned *fa, unsigned *fb, int nf
         }
         __syncthreads();
         if (threadIdx.x == 0) {
-            ticket[0] = 0u;
-            ticket[1] = 0u;
+            __threadfence();
+            *reinterpret_cast<unsigned long long *>(hdr) = 0ull;
+            hdr[2] = 0u;
             __threadfence();
         }
     }

@@ -86,7 +86,7 @@ struct TcParams {
     const float *gamma;
     void *o;
     StatePtrs sin, sout;
-    unsigned *ticket;   // workspace header: [0] ticket counter, [1] finished CTAs
+    unsigned *ticket;   // workspace header (take_ticket, finish_call)
     unsigned *flagsw;   // [BH][kmax] release flags
     float *summ;        // [BH][kmax][SUM] piece summaries
     unsigned *err;
@@ -201,6 +201,7 @@ struct Kern {
     uint64_t *tma_bar, *mma_bar, *mma_bar2, *mma_bar3;
     uint32_t tb, tph, mph, mph2, mph3;
     int tid, warp, lane, quad, half;
+    unsigned tag;  // the value this call's release flags carry
     int rowC, rowD;  // rows this thread owns in token-row / state accumulators (-1: none)
     int bh;
     int kvh;  // key/value head (b * Hkv + h / (H / Hkv)) of pair bh
@@ -926,7 +927,7 @@ struct Kern {
                 for (uint32_t it = 0; it < kWaitLimit; ++it) {
                     unsigned v;
                     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
-                    if (v) { ok = true; break; }
+                    if (v == tag) { ok = true; break; }
                     if (it > 256) __nanosleep(128);
                 }
             }
@@ -1965,9 +1966,9 @@ struct Kern {
     }
 };
 
-// Every thread of the CTA, after its last read of a flag (finish_grid).
-__device__ __forceinline__ void finish_cta(const TcParams &P, volatile unsigned *s_last) {
-    finish_grid(P.ticket, P.flagsw, nullptr, P.BH * P.kmax, s_last);
+// Every thread of the CTA, after its last read of a flag (finish_call).
+__device__ __forceinline__ void finish_cta(const TcParams &P, unsigned tag, volatile unsigned *s_last) {
+    finish_call(P.ticket, tag, P.flagsw, nullptr, P.BH * P.kmax, s_last);
 }
 
 template <int C, int D, int DV, bool DECAY, bool NORM, int VAR>
@@ -1982,6 +1983,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
     int *ticket_p = reinterpret_cast<int *>(base + K_::OFF_BAR + 36);
     int *misalign_p = reinterpret_cast<int *>(base + K_::OFF_BAR + 40);
     volatile unsigned *last_p = reinterpret_cast<volatile unsigned *>(base + K_::OFF_BAR + 44);
+    unsigned *tag_p = reinterpret_cast<unsigned *>(base + K_::OFF_BAR + 56);
 
     Kern<C, D, DV, DECAY, NORM, VAR> x(P, base);
     x.tid = threadIdx.x;
@@ -2009,12 +2011,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
         tma_prefetch_desc(&P.tmK);
         tma_prefetch_desc(&P.tmV);
         tma_prefetch_desc(&P.tmO);
-        *ticket_p = (int)atomicAdd(P.ticket, 1u);
+        const CallTicket t = take_ticket(P.ticket);
+        *ticket_p = (int)t.ticket;
+        *tag_p = t.tag;
     }
     __syncthreads();
+    x.tag = *tag_p;
     if (*misalign_p) {  // cannot happen with no static shared memory; refuse rather than corrupt
         if (x.tid == 0) atomicOr(P.err, DEV_TIMEOUT);
-        finish_cta(P, last_p);
+        finish_cta(P, x.tag, last_p);
         return;
     }
     if (x.warp == 0) {
@@ -2084,7 +2089,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
             __syncthreads();
             if (!pc.last && x.tid == 0) {
                 unsigned *f = P.flagsw + (size_t)bh * P.kmax + pc.k;
-                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
+                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(x.tag) : "memory");
             }
         }
         if (!ok) break;
@@ -2134,8 +2139,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
     __syncthreads();
     tc_fence_after();
     if (x.warp == 0) tmem_dealloc(x.tb, K_::TCOLS);
-    if (x.tid == 0) bulk_wait_all();  // the output stores are complete before the CTA counts itself done
-    finish_cta(P, last_p);
+    if (x.tid == 0) bulk_wait_all();  // the output stores are complete before the CTA ends
+    finish_cta(P, x.tag, last_p);
 }
 
 // ============================================================================ host side

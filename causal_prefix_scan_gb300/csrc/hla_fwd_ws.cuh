@@ -61,7 +61,7 @@ struct WsParams {
     float eps;
     const float *gamma;
     StatePtrs sin, sout;
-    unsigned *ticket;  // [0] ticket counter, [1] finished CTAs
+    unsigned *ticket;  // workspace header (take_ticket, finish_call)
     unsigned *flagA;   // [BH][kmax]: piece summary published
     unsigned *flagB;   // [BH][kmax]: piece X'', Y'' published
     float *summ;       // [BH][kmax][SUM]: S, X, C, m, Y of each piece from zero
@@ -173,6 +173,7 @@ struct Fwd {
     uint8_t *base;
     uint64_t *bars;
     volatile int *abort_p;  // CTA-wide: set once any wait of this CTA gave up
+    unsigned tag;           // the value this call's release flags carry
     uint32_t tb;            // TMEM base address
     int tid, warp, lane, quad;
     float lg;               // log2 of the current sequence's decay rate
@@ -252,7 +253,7 @@ struct Fwd {
             for (uint32_t it = 0; it < kWaitLimit; ++it) {
                 unsigned v;
                 asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
-                if (v) { ok = true; break; }
+                if (v == tag) { ok = true; break; }
                 if (*abort_p) break;
                 if (it > 256) __nanosleep(128);
             }
@@ -1044,7 +1045,7 @@ struct Fwd {
             ah_sync();
             if (ah == 0) {
                 unsigned *f = P.flagB + (size_t)bh * P.kmax;
-                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
+                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(tag) : "memory");
             }
             return;
         }
@@ -1105,7 +1106,7 @@ struct Fwd {
         ah_sync();  // every store of X'', Y'' precedes the release
         if (ah == 0) {
             unsigned *fl = P.flagB + (size_t)bh * P.kmax + k;
-            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(fl), "r"(1u) : "memory");
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(fl), "r"(tag) : "memory");
         }
     }
 
@@ -1276,9 +1277,9 @@ struct Fwd {
     }
 };
 
-// Every thread of the CTA, after its last read of a flag (finish_grid).
-__device__ __forceinline__ void finish_cta(const WsParams &P, volatile unsigned *s_last) {
-    finish_grid(P.ticket, P.flagA, P.flagB, P.BH * P.kmax, s_last);
+// Every thread of the CTA, after its last read of a flag (finish_call).
+__device__ __forceinline__ void finish_cta(const WsParams &P, unsigned tag, volatile unsigned *s_last) {
+    finish_call(P.ticket, tag, P.flagA, P.flagB, P.BH * P.kmax, s_last);
 }
 
 template <int C, int D, int DV, bool DECAY, bool NORM>
@@ -1290,7 +1291,7 @@ __global__ void __launch_bounds__(kThreads, Lay<C, D, DV, DECAY, NORM>::CTAS)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *base = smem_raw;
     Fwd<C, D, DV, DECAY, NORM> x(P, base);
-    uint32_t *misc = reinterpret_cast<uint32_t *>(base + L_::OFF_MISC);  // TMEM base, ticket, abort, misaligned
+    uint32_t *misc = reinterpret_cast<uint32_t *>(base + L_::OFF_MISC);  // TMEM base, ticket, abort, misaligned, last, tag
     x.bars = reinterpret_cast<uint64_t *>(base + L_::OFF_BAR);
     x.abort_p = reinterpret_cast<volatile int *>(misc + 2);
     x.tid = threadIdx.x;
@@ -1326,9 +1327,10 @@ __global__ void __launch_bounds__(kThreads, Lay<C, D, DV, DECAY, NORM>::CTAS)
     if (misc[3]) {  // cannot happen with no static shared memory; refuse rather than corrupt
         if (x.tid == 0) {
             atomicOr(P.err, DEV_TIMEOUT);
-            atomicAdd(P.ticket, 1u);
+            misc[5] = take_ticket(P.ticket).tag;
         }
-        finish_cta(P, misc + 4);
+        __syncthreads();
+        finish_cta(P, misc[5], misc + 4);
         return;
     }
     // TMEM first, then the ticket: a CTA that waits for TMEM holds no ticket that
@@ -1341,9 +1343,14 @@ __global__ void __launch_bounds__(kThreads, Lay<C, D, DV, DECAY, NORM>::CTAS)
     __syncthreads();
     tc_fence_after();
     x.tb = misc[0];
-    if (x.tid == 0) misc[1] = atomicAdd(P.ticket, 1u);
+    if (x.tid == 0) {
+        const CallTicket t = take_ticket(P.ticket);
+        misc[1] = t.ticket;
+        misc[5] = t.tag;
+    }
     __syncthreads();
     const int ticket = (int)misc[1];
+    x.tag = misc[5];
     const bool want_out = P.sout.S != nullptr;
     x.need_mY = NORM || want_out;
 
@@ -1439,7 +1446,7 @@ __global__ void __launch_bounds__(kThreads, Lay<C, D, DV, DECAY, NORM>::CTAS)
             x.ah_sync();
             if (x.ah == 0 && !pc.last) {
                 unsigned *f = P.flagA + (size_t)bh * P.kmax + pc.k;
-                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
+                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(x.tag) : "memory");
             }
         }
         // ---- scan, step 1: X'', Y'' of every piece that has a later piece
@@ -1477,7 +1484,7 @@ __global__ void __launch_bounds__(kThreads, Lay<C, D, DV, DECAY, NORM>::CTAS)
     __syncthreads();
     tc_fence_after();
     if (x.warp == kWarpMma) tmem_dealloc(x.tb, L_::TCOLS);
-    finish_cta(P, misc + 4);
+    finish_cta(P, x.tag, misc + 4);
 }
 
 // ============================================================================ host side

@@ -135,6 +135,7 @@ struct Fwd2 {
     uint8_t *base;
     uint64_t *bars;
     volatile int *abort_p;
+    unsigned tag;  // the value this call's release flags carry
     uint32_t tb;
     int tid, warp, lane, quad;
     int bh;
@@ -209,7 +210,7 @@ struct Fwd2 {
             for (uint32_t it = 0; it < kWaitLimit; ++it) {
                 unsigned v;
                 asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
-                if (v) { ok = true; break; }
+                if (v == tag) { ok = true; break; }
                 if (*abort_p) break;
                 if (it > 256) __nanosleep(128);
             }
@@ -864,7 +865,7 @@ struct Fwd2 {
             ah_sync();
             if (ah == 0) {
                 unsigned *f = P.flagB + (size_t)bh * P.kmax;
-                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
+                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(tag) : "memory");
             }
             return;
         }
@@ -925,7 +926,7 @@ struct Fwd2 {
         ah_sync();  // every store of X'', Y'' precedes the release
         if (ah == 0) {
             unsigned *fl = P.flagB + (size_t)bh * P.kmax + k;
-            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(fl), "r"(1u) : "memory");
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(fl), "r"(tag) : "memory");
         }
     }
 
@@ -1107,7 +1108,7 @@ __global__ void __launch_bounds__(kThreads, Lay<DV, NORM>::CTAS) fwd_ws2_kernel(
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *base = smem_raw;
     Fwd2<DV, NORM> x(P, base);
-    uint32_t *misc = reinterpret_cast<uint32_t *>(base + L_::OFF_MISC);  // TMEM base, ticket, abort, misaligned
+    uint32_t *misc = reinterpret_cast<uint32_t *>(base + L_::OFF_MISC);  // TMEM base, ticket, abort, misaligned, last, tag
     x.bars = reinterpret_cast<uint64_t *>(base + L_::OFF_BAR);
     x.abort_p = reinterpret_cast<volatile int *>(misc + 2);
     x.tid = threadIdx.x;
@@ -1150,9 +1151,10 @@ __global__ void __launch_bounds__(kThreads, Lay<DV, NORM>::CTAS) fwd_ws2_kernel(
     if (misc[3]) {  // cannot happen with no static shared memory; refuse rather than corrupt
         if (x.tid == 0) {
             atomicOr(P.err, DEV_TIMEOUT);
-            atomicAdd(P.ticket, 1u);
+            misc[5] = take_ticket(P.ticket).tag;
         }
-        ws::finish_cta(P, misc + 4);
+        __syncthreads();
+        ws::finish_cta(P, misc[5], misc + 4);
         return;
     }
     if (x.warp == ws::kWarpMma) {
@@ -1163,9 +1165,14 @@ __global__ void __launch_bounds__(kThreads, Lay<DV, NORM>::CTAS) fwd_ws2_kernel(
     __syncthreads();
     tc_fence_after();
     x.tb = misc[0];
-    if (x.tid == 0) misc[1] = atomicAdd(P.ticket, 1u);
+    if (x.tid == 0) {
+        const CallTicket t = take_ticket(P.ticket);
+        misc[1] = t.ticket;
+        misc[5] = t.tag;
+    }
     __syncthreads();
     const int ticket = (int)misc[1];
+    x.tag = misc[5];
     const bool want_out = P.sout.S != nullptr;
     x.need_mY = NORM || want_out;
 
@@ -1260,7 +1267,7 @@ __global__ void __launch_bounds__(kThreads, Lay<DV, NORM>::CTAS) fwd_ws2_kernel(
             x.ah_sync();
             if (x.ah == 0 && !pc.last) {
                 unsigned *f = P.flagA + (size_t)bh * P.kmax + pc.k;
-                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
+                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(x.tag) : "memory");
             }
             last_p1 = bh;
         }
@@ -1299,7 +1306,7 @@ __global__ void __launch_bounds__(kThreads, Lay<DV, NORM>::CTAS) fwd_ws2_kernel(
     __syncthreads();
     tc_fence_after();
     if (x.warp == ws::kWarpMma) tmem_dealloc(x.tb, L_::TCOLS);
-    ws::finish_cta(P, misc + 4);
+    ws::finish_cta(P, x.tag, misc + 4);
 }
 
 // ============================================================================ host side

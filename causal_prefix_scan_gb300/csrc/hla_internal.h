@@ -43,8 +43,9 @@ cudaError_t fwd_simt_launch(const FwdArgs &a, cudaStream_t st);
 bool fwd_tc_supported(const hla_params &p);
 size_t fwd_tc_workspace(const hla_params &p, int num_sms);
 const char *fwd_tc_kernel_name(const hla_params &p);
-// Bytes at the start of the tensor-core forward's workspace that must be zero when a
-// call starts (its ordering header and release flags); each call leaves them zero.
+// Bytes at the start of the tensor-core forward's workspace that hold its ordering
+// header and release flags: zero before the first call on a workspace; each call leaves
+// them ready for the next (its generation in the header, its tag on the flags).
 size_t fwd_tc_sync_bytes(const hla_params &p, int num_sms);
 cudaError_t fwd_tc_launch(const FwdArgs &a, cudaStream_t st, int num_sms);
 

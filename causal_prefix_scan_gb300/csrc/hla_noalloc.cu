@@ -21,7 +21,7 @@ constexpr int kMaxDevices = 64;
 
 // The scratch.  In host code this name is only a stand-in for the symbol, never
 // a usable device address: kernels get the address from cudaGetSymbolAddress.
-// Zero at module load; every forward call leaves its ordering header and flags zero.
+// Zero at module load; every forward call leaves its ordering header and flags ready for the next.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_mu;
@@ -99,9 +99,9 @@ extern "C" hla_status hla_forward_chunked_noalloc(const hla_params *p, const voi
     hla_status s = scratch_address(&scratch, &dev);
     if (s != HLA_OK) return s;
     // The forward's ordering header and release flags (one per sequence and piece)
-    // must start at zero.  Each call leaves them zero; they are cleared anyway in
-    // case an earlier call on this array did not finish.  Their size comes from the
-    // same work plan the forward uses.
+    // start each call at zero here: each call would leave them ready for the next,
+    // but they are cleared anyway in case an earlier call on this array did not
+    // finish.  Their size comes from the same work plan the forward uses.
     int nsm = 0;
     cudaError_t e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess || nsm < 1) return cuda_err(e, "SM count");

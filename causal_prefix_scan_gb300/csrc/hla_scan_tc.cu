@@ -24,24 +24,6 @@ namespace scantc {
 using namespace chunktc;
 namespace {
 
-// One elementwise scan over the chunks of every pair: out[ch] = R, R = f_ch R + in[ch],
-// f_ch = g^{power * L_ch} (1 without decay), in chunk order (reverse: last chunk first).
-struct PrefixJob {
-    const float *in;
-    size_t in_stride, in_off;  // element e of chunk ch of pair u at in[(u * nch + ch) * in_stride + in_off + e]
-    float *out;
-    size_t out_stride, out_off;
-    const float *init;  // [units][count] or null (zeros)
-    float *fin;         // [units][count] or null
-    int count, reverse, power;
-};
-
-struct PrefixArgs {
-    PrefixJob job[2];
-    int njobs, units, nch, n, chunk, H;
-    const float *gamma;  // per head, or null (no decay)
-};
-
 constexpr int kPrefixThreads = 256;
 
 // Each thread scans four consecutive elements (count a multiple of 4, 16-byte aligned).
@@ -87,13 +69,17 @@ __global__ void __launch_bounds__(kPrefixThreads) chunk_prefix_kernel(const __gr
     if (j.fin) *reinterpret_cast<float4 *>(j.fin + (size_t)u * j.count + e) = R;
 }
 
-cudaError_t prefix(const PrefixArgs &a, cudaStream_t st) {
+}  // namespace
+
+cudaError_t chunk_prefix(const PrefixArgs &a, cudaStream_t st) {
     int mx = 0;
     for (int i = 0; i < a.njobs; ++i) mx = max(mx, (a.job[i].count / 4 + kPrefixThreads - 1) / kPrefixThreads);
     dim3 grid((unsigned)(a.units * mx), (unsigned)a.njobs);
     chunk_prefix_kernel<<<grid, kPrefixThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
+
+namespace {
 
 // D (+)= A B with A, B fp32 given as hi + lo tiles: hi.hi + hi.lo + lo.hi
 __device__ __forceinline__ void mma3_km(uint32_t d, const uint8_t *ah, const uint8_t *al, const uint8_t *bh,
@@ -219,7 +205,7 @@ cudaError_t bwd_scan(const BwdArgs &a, cudaStream_t st) {
     p.njobs = 2; p.units = units; p.nch = nch; p.n = a.n; p.chunk = 64; p.H = a.H; p.gamma = gamma;
     p.job[0] = PrefixJob{loc, ws.loc_floats(), ws.o_sloc(), sta, ws.st_floats(), ws.o_sp(), nullptr, nullptr, 64 * 64, 0, 1};
     p.job[1] = PrefixJob{loc, ws.loc_floats(), ws.o_lloc(), sta, ws.st_floats(), ws.o_lam(), nullptr, nullptr, 64 * 64, 1, 2};
-    cudaError_t e = prefix(p, st);
+    cudaError_t e = chunk_prefix(p, st);
     if (e != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(bwd_incr_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kBwdIncrSmem)) != cudaSuccess)
@@ -228,7 +214,7 @@ cudaError_t bwd_scan(const BwdArgs &a, cudaStream_t st) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     p.job[0] = PrefixJob{loc, ws.loc_floats(), ws.o_xloc(), sta, ws.st_floats(), ws.o_xp(), nullptr, nullptr, 64 * 64, 0, 2};
     p.job[1] = PrefixJob{loc, ws.loc_floats(), ws.o_oloc(), sta, ws.st_floats(), ws.o_om(), nullptr, nullptr, 64 * 64, 1, 1};
-    return prefix(p, st);
+    return chunk_prefix(p, st);
 }
 
 // Third order: S^K_p and P_p (and the final S^K, P), the increments, then T_p (and the final T).
@@ -240,7 +226,7 @@ cudaError_t fwd3_scan(const Fwd3Args &a, cudaStream_t st) {
     p.njobs = 2; p.units = units; p.nch = nch; p.n = a.n; p.chunk = 64; p.H = a.H; p.gamma = nullptr;
     p.job[0] = PrefixJob{loc, ws.loc_floats(), ws.o_sk(), sta, ws.st_floats(), ws.s_sk(), a.sin_S, a.sout_S, 64 * 64, 0, 1};
     p.job[1] = PrefixJob{loc, ws.loc_floats(), ws.o_p(), sta, ws.st_floats(), ws.s_p(), a.sin_P, a.sout_P, 64 * 64, 0, 1};
-    cudaError_t e = prefix(p, st);
+    cudaError_t e = chunk_prefix(p, st);
     if (e != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(fwd3_incr_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kFwd3IncrSmem)) != cudaSuccess)
@@ -249,7 +235,7 @@ cudaError_t fwd3_scan(const Fwd3Args &a, cudaStream_t st) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     p.njobs = 1;
     p.job[0] = PrefixJob{loc, ws.loc_floats(), ws.o_t(), sta, ws.st_floats(), ws.s_t(), a.sin_T, a.sout_T, 64 * 64, 0, 1};
-    return prefix(p, st);
+    return chunk_prefix(p, st);
 }
 
 }  // namespace scantc

@@ -151,8 +151,10 @@ HLA_API const char *hla_forward_kernel(const hla_params *p);
  *   workspace device scratch of at least hla_forward_workspace_size(p) bytes,
  *             256-byte aligned, set to zero before its first use; every call
  *             (also one that ends in HLA_ERR_TIMEOUT) leaves its header and flags
- *             zero again, so it can be reused without clearing.  Calls sharing
- *             one workspace must not overlap in time.
+ *             ready for the next call (a call generation in the header, which
+ *             tags the flags), so it can be reused without clearing, also by a
+ *             call with other parameters.  Calls sharing one workspace must not
+ *             overlap in time.
  */
 HLA_API hla_status hla_forward_chunked(const hla_params *p, const void *q, const void *k,
                                const void *v, void *o, const hla_state *state_in,
