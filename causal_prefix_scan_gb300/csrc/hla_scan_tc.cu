@@ -70,8 +70,10 @@ __global__ void __launch_bounds__(kPrefixThreads) chunk_prefix_kernel(const __gr
 }
 
 }  // namespace
+}  // namespace scantc
 
-cudaError_t chunk_prefix(const PrefixArgs &a, cudaStream_t st) {
+cudaError_t chunktc::chunk_prefix(const PrefixArgs &a, cudaStream_t st) {
+    using namespace scantc;
     int mx = 0;
     for (int i = 0; i < a.njobs; ++i) mx = max(mx, (a.job[i].count / 4 + kPrefixThreads - 1) / kPrefixThreads);
     dim3 grid((unsigned)(a.units * mx), (unsigned)a.njobs);
@@ -79,6 +81,7 @@ cudaError_t chunk_prefix(const PrefixArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+namespace scantc {
 namespace {
 
 // D (+)= A B with A, B fp32 given as hi + lo tiles: hi.hi + hi.lo + lo.hi
