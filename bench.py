@@ -58,6 +58,7 @@ FWD3_METRIC = "masked 3rd-order HLA forward tokens/s and % roofline on 1 GB300"
 FWD3_DISPATCH_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd3_simt.cu")
 FWD3_TC_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_fwd3_tc.cu")
 BWD_NORM_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_bwd_norm.cu")
+BWD_NORM_TC_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_bwd_norm_tc.cu")
 NORM_UNIT_WIDTH = 16  # width of the unit-value tile of the normalised backward
 BWD_TC_KERNEL_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_bwd_tc.cu")
 SCAN_TC_SRC = os.path.join(ROOT, "causal_prefix_scan_gb300", "csrc", "hla_scan_tc.cu")
@@ -99,6 +100,25 @@ def bwd_flops_per_token_head(w: W.Workload) -> dict:
     return {"bwd_local_kernel": 3 * c * d + c * dv + 4 * d * d + 8 * d * dv,
             "bwd_scan_kernel": 4 * d * d * dv / c,
             "bwd_grad_kernel": 9 * c * d + 2 * c * dv + 6 * d * d + 6 * d * dv}
+
+
+def norm_tc(w: W.Workload) -> bool:
+    """The ratio-normalised backward runs on the tensor cores (bf16, d = dv = chunk = 64)."""
+    return w.normalize and w.dtype == "bf16" and w.d == w.dv == w.chunk == 64
+
+
+def bwd_norm_tc_flops_per_token_head(w: W.Workload) -> dict:
+    """Algorithmic flops per token-head of the three phases of the tensor-core
+    normalised backward (an FMA is 2 flops, triangular chunk products at half; the
+    unit column's d-vectors and the hi/lo split's extra products are not counted).
+    Forward and local sums: A~, A~K twice, M, P^T Q at half (c d each), M V and P at
+    half (c dv each), S_loc, Q S_p, O_loc (2 d^2 each), C_q, X_loc, Q X_p, L_loc, W
+    (2 d dv each), S_p C_q per chunk; scan: Lam W per chunk; gradients as for the
+    unnormalised backward."""
+    c, d, dv = w.chunk, w.d, w.dv
+    return {"bwd_norm_tc_forward_local": 6 * c * d + 2 * c * dv + 6 * d * d + 10 * d * dv + 2 * d * d * dv / c,
+            "bwd_norm_tc_scan": 2 * d * d * dv / c,
+            "bwd_norm_tc_grad_kernel": 9 * c * d + 2 * c * dv + 6 * d * d + 6 * d * dv}
 
 
 def bwd_bytes_per_step(w: W.Workload) -> float:
@@ -554,6 +574,8 @@ def launches_per_step(w: W.Workload) -> int:
     the upstream gradients, a second backward and the sums."""
     if not (is_backward(w) and w.normalize):
         return 3
+    if norm_tc(w):  # local sums, S prefix, increments, X/Y prefix, outputs, Lam suffix, increments, Om suffix, gradients
+        return 9 + (2 if w.kv_heads != w.H else 0)
     bf = w.dtype == "bf16"
     split = norm_segments(w) > 1  # two forwards and a segment scan per part instead of one forward
     forwards = (4 + 2 + (1 if w.decay else 0)) if split else 2
@@ -603,7 +625,14 @@ def bench_phased(args, w: W.Workload, rank, world, local, dist):
         outs = (torch.empty_like(ins[0]), torch.empty_like(ins[1]), torch.empty_like(ins[2])) if bwd else \
             (torch.empty(ins[0].shape[:3] + (w.dv,), dtype=tdt, device=dev),)
         sets.append((ins, outs))
-    if bwd and w.normalize:
+    if bwd and w.normalize and norm_tc(w):
+        params = hla.make_params(sets[0][0][0], sets[0][0][2], w.chunk, gamma, True, w.eps)
+        ws_bytes = hla.hla_backward_workspace_size(params)
+        fl = bwd_norm_tc_flops_per_token_head(w)
+        names = tuple(fl)
+        src, metric = BWD_NORM_TC_SRC, BWD_METRIC
+        tc = True
+    elif bwd and w.normalize:
         # two fp32 forwards and the upstream-gradient kernel, the backward of the values,
         # the backward of the unit column and the gradient sums (all fp32, CUDA cores)
         params = hla.make_params(sets[0][0][0], sets[0][0][2], w.chunk, gamma, True, w.eps)
@@ -719,6 +748,8 @@ def bench_phased(args, w: W.Workload, rank, world, local, dist):
         return ("tensor", peaks["bf16_tflops"], tc_src) if "_tc_" in nm else ("alu", FP32_ALU_TFLOPS, alu_src)
 
     def source_of(nm):  # the file whose hash keys the committed DRAM traffic of this phase
+        if nm.startswith("bwd_norm_tc_"):
+            return BWD_NORM_TC_SRC
         if "_scan_tc_" in nm:
             return SCAN_TC_SRC
         if "_tc_" in nm:
@@ -749,7 +780,7 @@ def bench_phased(args, w: W.Workload, rank, world, local, dist):
         cfg["variant"] = "masked third order"
     line = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if tc else "f32", "data": "synthetic",
             "config": cfg, "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step(w) * K,
             "clocks": clk.summary(),
             "token_heads_per_s": world * w.token_heads * K / (t_max / 1e3)}

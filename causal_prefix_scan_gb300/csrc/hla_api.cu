@@ -206,7 +206,11 @@ hla_status check_bwd_params(const hla_params *p) {
 
 size_t hla_backward_workspace_size(const hla_params *p) {
     if (check_bwd_params(p) != HLA_OK) return 0;
-    if (p->flags & HLA_NORMALIZE) return p->n > 0 ? hla::bwd_norm_layout(*p).total : 0;
+    if (p->flags & HLA_NORMALIZE) {
+        if (p->n == 0) return 0;
+        const size_t a = hla::bwd_norm_layout(*p).total, b = hla::bwd_norm_tc_workspace(*p);
+        return a > b ? a : b;
+    }
     return hla::bwd_simt_workspace(*p);
 }
 
@@ -245,7 +249,7 @@ hla_status backward_impl(const hla_params *p, const void *q, const void *k, cons
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
         !aligned16(dv))
         return fail(HLA_ERR_ARG, "tensor pointers must be 16-byte aligned");
-    const size_t need = norm ? hla::bwd_norm_layout(*p).total : hla::bwd_simt_workspace(*p);
+    const size_t need = hla_backward_workspace_size(p);
     if (!workspace || workspace_bytes < need)
         return fail(HLA_ERR_ARG, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
     if (norm ? (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 : !aligned16(workspace))
@@ -278,7 +282,10 @@ hla_status backward_impl(const hla_params *p, const void *q, const void *k, cons
     a.events = reinterpret_cast<cudaEvent_t const *>(phase_events);
     cudaError_t e = status_ptr(&a.err);
     if (e != cudaSuccess) return cuda_fail(e, "status word");
-    if (norm) return hla::bwd_norm_launch(*p, a, workspace, st);
+    if (norm) {
+        if (hla::bwd_norm_tc_supported(*p, a)) return hla::bwd_norm_tc_launch(*p, a, st);
+        return hla::bwd_norm_launch(*p, a, workspace, st);
+    }
     e = hla::bwd_simt_launch(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return HLA_OK;

@@ -115,6 +115,11 @@ struct NormLayout {
 };
 NormLayout bwd_norm_layout(const hla_params &p);
 hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a, void *workspace, cudaStream_t st);
+// The same on the tensor cores (hla_bwd_norm_tc.cu): bf16, d = dv = chunk = 64, no given
+// initial state and no state gradient.
+bool bwd_norm_tc_supported(const hla_params &p, const BwdArgs &a);
+size_t bwd_norm_tc_workspace(const hla_params &p);
+hla_status bwd_norm_tc_launch(const hla_params &p, const BwdArgs &a, cudaStream_t st);
 
 struct Fwd3Args {
     int B, H, n, d, dv, chunk;

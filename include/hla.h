@@ -211,10 +211,15 @@ HLA_API hla_status hla_decode_step(int N, int H, int Hkv, int d, int dv, hla_dty
  * With HLA_NORMALIZE the output is o_t = n_t / (den_t + eps), den_t = q_t^T
  * (S_t m_t - h_t) (section 1, "Normalisatie").  den is the unnormalised output of
  * unit values, so the gradient is that of the unnormalised output of the values
- * [V | 1] with upstream [r dout | -r (dout . o)], r = 1 / (den + eps): two
- * unnormalised forwards, an elementwise kernel, two unnormalised backwards and a
- * sum.  The two parts of dq and dk cancel to a large degree, so this chain runs in
- * fp32 throughout (bf16 inputs are widened first) on the CUDA-core kernels.
+ * [V | 1] with upstream [r dout | -r (dout . o)], r = 1 / (den + eps).  The two
+ * parts of dq and dk cancel to a large degree.  For bf16 inputs with d = dv =
+ * chunk = 64 (and no given state, below) it runs on the tensor cores in nine
+ * launches: the forward's local sums and scan, the outputs with r and the upstream,
+ * the backward's scan and the gradients; every product over the value index, where
+ * the two parts meet, is formed from bf16 hi + lo operands (about fp32 accuracy)
+ * and the unit column's terms in fp32.  Otherwise it is a chain of two unnormalised
+ * forwards, an elementwise kernel, two unnormalised backwards and a sum, in fp32
+ * throughout (bf16 inputs are widened first) on the CUDA-core kernels.
  *
  *   p      as for hla_forward_chunked; supported: flags 0, HLA_DECAY, HLA_NORMALIZE
  *          (eps >= 0) or both (HLA_UNMASKED, HLA_ASYMMETRIC: HLA_ERR_UNSUPPORTED),
@@ -228,7 +233,7 @@ HLA_API hla_status hla_decode_step(int N, int H, int Hkv, int d, int dv, hla_dty
  *          16-byte aligned (256-byte aligned with HLA_NORMALIZE), no initial
  *          contents needed.
  * All tensor pointers 16-byte aligned.  Without HLA_NORMALIZE three kernel phases
- * on `stream` (plus the group sums when Hkv < H); with it, the chain above.
+ * on `stream` (plus the group sums when Hkv < H); with it, the launches above.
  */
 HLA_API size_t hla_backward_workspace_size(const hla_params *p);
 HLA_API hla_status hla_backward_chunked(const hla_params *p, const void *q, const void *k, const void *v,
@@ -253,7 +258,7 @@ HLA_API hla_status hla_backward_chunked(const hla_params *p, const void *q, cons
  *   the rest as for hla_backward_chunked (same workspace size).
  * With a state or its gradient the scan between the local sums and the gradients runs
  * on the CUDA cores (also on the tensor-core shape), plus one launch per pass for the
- * state gradient.
+ * state gradient; with HLA_NORMALIZE it is the CUDA-core chain.
  */
 HLA_API hla_status hla_backward_chunked_state(const hla_params *p, const void *q, const void *k, const void *v,
                                               const void *dout, const hla_state *state_in, void *dq, void *dk,

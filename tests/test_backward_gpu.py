@@ -173,6 +173,23 @@ def test_backward_normalised_shared_kv_heads(d, dv, chunk, dtype):
           TOL_F32 if dtype == "f32" else TOL_BF16, f"bwd norm {dtype} H4 Hkv2")
 
 
+@pytest.mark.parametrize("decay", [False, True])
+@pytest.mark.parametrize("Hkv", [2, 1])
+def test_backward_normalised_values_with_a_common_offset(decay, Hkv):
+    """Values with a large common mean (3 + N(0,1)): every output is then close to every
+    value, and the two parts of the gradient (through the values and through the
+    denominator) are each 20-30 times their sum.  Rounding the upstream gradients or
+    the outputs to bf16 alone costs ~5% here (fp64 check of the same case), so this
+    holds the tensor-core path's mixed products to fp32-level accuracy."""
+    w = small(B=1, H=2, Hkv=Hkv, n=64 * 4 + 9, decay=decay, qk="elu1", seed=45)
+    x = W.make_inputs(w)
+    x["v"] = W.round_bf16(x["v"] + np.float32(3.0))
+    g = W.make_dout(w)
+    err = check(run_backward(x, g, "bf16", 64, eps=1e-3), run_oracle(x, g, eps=1e-3), TOL_BF16,
+                f"bwd norm offset values decay={decay} Hkv={Hkv}")
+    print(f"offset values decay={decay} Hkv={Hkv}: max per-(b,h) rel L2 {err:.3e}")
+
+
 def test_backward_normalised_is_gradient_of_forward():
     """The normalised backward against central differences of the library's own
     normalised fp32 forward along a random direction.  Along the line the output is a
