@@ -654,14 +654,17 @@ cudaError_t smem_attr(K kern, size_t bytes) {
 }  // namespace
 }  // namespace bwdn
 
-bool bwd_norm_tc_supported(const hla_params &p, const BwdArgs &a) {
+bool bwd_norm_tc_shape(const hla_params &p) {
     return p.in_dtype == HLA_BF16 && p.d == 64 && p.dv == 64 && p.chunk == 64 && (p.flags & HLA_NORMALIZE) &&
-           !(p.flags & (HLA_UNMASKED | HLA_ASYMMETRIC)) && !a.sin_S && !a.dS;
+           !(p.flags & (HLA_UNMASKED | HLA_ASYMMETRIC));
 }
 
+bool bwd_norm_tc_supported(const hla_params &p, const BwdArgs &a) { return bwd_norm_tc_shape(p) && !a.sin_S && !a.dS; }
+
 size_t bwd_norm_tc_workspace(const hla_params &p) {
+    if (!bwd_norm_tc_shape(p)) return 0;
     const int hkv = p.Hkv > 0 ? p.Hkv : p.H;
-    return bwdn::layout(p.B, p.H, hkv, p.n).total * sizeof(float);
+    return (bwdn::layout(p.B, p.H, hkv, p.n).total * sizeof(float) + 255) & ~size_t(255);
 }
 
 hla_status bwd_norm_tc_launch(const hla_params &p, const BwdArgs &a0, cudaStream_t st) {

@@ -115,8 +115,9 @@ struct NormLayout {
 };
 NormLayout bwd_norm_layout(const hla_params &p);
 hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a, void *workspace, cudaStream_t st);
-// The same on the tensor cores (hla_bwd_norm_tc.cu): bf16, d = dv = chunk = 64, no given
-// initial state and no state gradient.
+// The same on the tensor cores (hla_bwd_norm_tc.cu): bf16, d = dv = chunk = 64 (the shape),
+// no given initial state and no state gradient (supported); workspace bytes, 0 off the shape.
+bool bwd_norm_tc_shape(const hla_params &p);
 bool bwd_norm_tc_supported(const hla_params &p, const BwdArgs &a);
 size_t bwd_norm_tc_workspace(const hla_params &p);
 hla_status bwd_norm_tc_launch(const hla_params &p, const BwdArgs &a, cudaStream_t st);

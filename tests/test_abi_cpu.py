@@ -194,6 +194,17 @@ def test_backward_normalised_workspace(lib):
         assert norm >= plain + rows * 4 * (2 * dv + 3 * 16 + 2 * d)
         assert norm % 256 == 0
     assert hla.hla_backward_workspace_size(_params(n=0, flags=hla.HLA_NORMALIZE)) == 0
+    # the tensor-core shape (bf16, d = dv = chunk = 64) also covers that path's layout: per
+    # chunk six 64 x 64 local sums and four vectors, four states and two vectors; r and c
+    # per token; with shared key/value heads the per-query-head dk, dv
+    for Hkv in (3, 1):
+        B, H, n = 2, 3, 100
+        units, nch = B * H, -(-n // 64)
+        need = 4 * (units * nch * ((6 * 4096 + 4 * 64) + (4 * 4096 + 2 * 64)) + 2 * units * n
+                    + (2 * units * n * 64 if Hkv < H else 0))
+        got = hla.hla_backward_workspace_size(_params(B=B, H=H, Hkv=Hkv, n=n, d=64, dv=64, chunk=64,
+                                                      in_dtype=hla.HLA_BF16, flags=hla.HLA_NORMALIZE, eps=1e-3))
+        assert got >= need and got % 256 == 0
     # the scratch must be 256-byte aligned with HLA_NORMALIZE
     p = _params(flags=hla.HLA_NORMALIZE, eps=1e-3)
     assert _bcall(p, ws=16) == hla.HLA_ERR_ARG
