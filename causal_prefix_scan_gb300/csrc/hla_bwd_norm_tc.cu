@@ -253,6 +253,8 @@ __global__ void __launch_bounds__(kTc, 2) incr_kernel(const __grid_constant__ Bw
         uint8_t *hi[2] = {x.tile(I_AH), x.tile(I_BH)}, *lo[2] = {x.tile(I_AL), x.tile(I_BL)};
         load_tiles_hilo<2>(ss, hi, lo);
     }
+    float *mq = reinterpret_cast<float *>(smem_raw + I_N * TILE + 64);  // m_q [64]
+    if (MODE == 0 && x.tid < 64) mq[x.tid] = lc[NWs::L_MQ + x.tid];
     x.publish();
     const size_t ro = (size_t)x.row * 64 + x.c0;
     float *dst = lc + (MODE == 0 ? NWs::L_XLOC : NWs::L_OLOC) + ro;
@@ -268,11 +270,20 @@ __global__ void __launch_bounds__(kTc, 2) incr_kernel(const __grid_constant__ Bw
     do {
         if (x.tid == 0) mma3_km(x.tb + 0, x.tile(I_AH), x.tile(I_AL), x.tile(I_BH), x.tile(I_BL), false);
         x.commit();
-        if (MODE == 0 && x.tid < 64) {  // Y_loc += S_p m_q (fp32, while the product runs)
-            const float *sp = so + NWs::S_SP + (size_t)x.tid * 64, *mq = lc + NWs::L_MQ;
-            float acc = lc[NWs::L_YLOC + x.tid];
-            for (int j = 0; j < 64; ++j) acc = fmaf(sp[j], mq[j], acc);
-            lc[NWs::L_YLOC + x.tid] = acc;
+        if (MODE == 0) {  // Y_loc += S_p m_q while the product runs: S_p = hi + lo from the
+            // shared tiles, four threads per row, sixteen columns each
+            const int i = x.tid >> 2, j0 = (x.tid & 3) * 16;
+            float hv[8], lv[8], acc = 0.f;
+#pragma unroll
+            for (int h = 0; h < 16; h += 8) {
+                tile_load_row8(x.tile(I_AH), 64, i, j0 + h, hv);
+                tile_load_row8(x.tile(I_AL), 64, i, j0 + h, lv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc = fmaf(hv[e] + lv[e], mq[j0 + h + e], acc);
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            if ((x.tid & 3) == 0) lc[NWs::L_YLOC + i] += acc;
         }
         if (!x.wait()) break;
         float r[16];
@@ -642,7 +653,7 @@ __global__ void __launch_bounds__(kTc, 1) grad_kernel(const __grid_constant__ Bw
 }
 
 constexpr size_t kFwdLocalSmem = F_N * TILE + 64 + (kGp + 2 * 64) * 4;
-constexpr size_t kIncrSmem = I_N * TILE + 64;
+constexpr size_t kIncrSmem = I_N * TILE + 64 + 64 * 4;
 constexpr size_t kOutSmem = O_N * TILE + 64 + (kGp + 64 * 3 + 128 + 128) * 4;
 constexpr size_t kGradSmem = G_N * TILE + 64 + (kGp + 4 * 64) * 4;
 
