@@ -21,7 +21,7 @@ LIB_NAME = "libhla_gb300.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 
 SOURCES = ["hla_api.cu", "hla_fwd_tc.cu"] + [f"hla_fwd_tc_f{i}.cu" for i in range(12)] + \
-    ["hla_fwd_simt.cu", "hla_combine.cu", "hla_decode.cu", "hla_noalloc.cu", "hla_bwd_simt.cu", "hla_bwd_tc.cu", "hla_bwd_norm.cu", "hla_bwd_norm_tc.cu"] + \
+    ["hla_fwd_simt.cu", "hla_combine.cu", "hla_decode.cu", "hla_noalloc.cu", "hla_bwd_simt.cu", "hla_bwd_tc.cu", "hla_bwd_norm.cu", "hla_bwd_norm_tc.cu", "hla_bwd_split.cu"] + \
     [f"hla_bwd_{t}_c{c}.cu" for t in ("f32", "bf16") for c in (16, 32, 64)] + ["hla_fwd3_simt.cu", "hla_fwd3_tc.cu", "hla_scan_tc.cu", "hla_fwd3_maps.cu"] + \
     [f"hla_fwd3_{t}_c{c}.cu" for t in ("f32", "bf16") for c in (16, 32, 64)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -115,6 +115,13 @@ struct NormLayout {
 };
 NormLayout bwd_norm_layout(const hla_params &p);
 hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a, void *workspace, cudaStream_t st);
+// A backward pass split over value columns (hla_bwd_split.cu): columns [64 half, 64 half + 64)
+// of [rows][128] elements of type dt gathered into [rows][64] (or scattered back), and
+// the fp32 sum of the halves' dq, dk (first: overwrite) with its final rounding.
+cudaError_t cols_half_copy(const void *src, void *dst, size_t rows, hla_dtype dt, int half, bool gather,
+                           cudaStream_t st);
+cudaError_t acc_add(float *acc, const void *src, size_t count, hla_dtype dt, bool first, cudaStream_t st);
+cudaError_t acc_store(void *dst, const float *acc, size_t count, hla_dtype dt, cudaStream_t st);
 // The same on the tensor cores (hla_bwd_norm_tc.cu): bf16, d = dv = chunk = 64 (the shape),
 // no given initial state and no state gradient (supported); workspace bytes, 0 off the shape.
 bool bwd_norm_tc_shape(const hla_params &p);

@@ -142,8 +142,9 @@ def _bcall(p, ptrs=(16,) * 7, ws=16, ws_bytes=1 << 40):
     (dict(flags=hla.HLA_ASYMMETRIC), hla.HLA_ERR_UNSUPPORTED),
     (dict(H=6, Hkv=4), hla.HLA_ERR_ARG),
     (dict(d=128), hla.HLA_ERR_UNSUPPORTED),
-    (dict(dv=128), hla.HLA_ERR_UNSUPPORTED),
-    (dict(chunk=128), hla.HLA_ERR_UNSUPPORTED),
+    (dict(d=128, dv=128, chunk=128), hla.HLA_ERR_UNSUPPORTED),
+    (dict(dv=96), hla.HLA_ERR_UNSUPPORTED),
+    (dict(chunk=256), hla.HLA_ERR_UNSUPPORTED),
     (dict(d=48), hla.HLA_ERR_UNSUPPORTED),
 ])
 def test_backward_rejects_bad_params(lib, kw, status):
@@ -268,6 +269,31 @@ def test_forward3_workspace_size(lib):
         nch = -(-n // c)
         want = B * H * nch * (4 * d * d + 5 * d * dv) * 4
         assert hla.hla_forward3_workspace_size(_params(B=B, H=H, n=n, d=d, dv=dv, chunk=c)) == want
+
+
+def test_backward_value_halves_and_long_chunks(lib):
+    """dv = 128 runs as two 64-column halves: the half problem's workspace, then the two
+    gathered halves, the half's dq, dk, dv and the fp32 sums of dq, dk (256-byte aligned
+    regions).  A 128-token chunk runs as two 64-token ones: the same workspace as chunk 64."""
+    al = lambda x: -(-x // 256) * 256
+    for dt, el in ((hla.HLA_F32, 4), (hla.HLA_BF16, 2)):
+        for flags in (0, hla.HLA_NORMALIZE):
+            B, H, Hkv, n, d, c = 2, 4, 2, 100, 32, 32
+            kw = dict(B=B, H=H, Hkv=Hkv, n=n, d=d, chunk=c, in_dtype=dt, flags=flags, eps=1e-3)
+            inner = hla.hla_backward_workspace_size(_params(dv=64, **kw))
+            rq, rkv = B * H * n, B * Hkv * n
+            want = al(inner) + al(rkv * 64 * el) + al(rq * 64 * el) + al(rq * d * el) + al(rkv * d * el) \
+                + al(rkv * 64 * el) + al(rq * d * 4) + al(rkv * d * 4)
+            assert hla.hla_backward_workspace_size(_params(dv=128, **kw)) == want
+    for flags in (0, hla.HLA_NORMALIZE):
+        a = hla.hla_backward_workspace_size(_params(chunk=128, flags=flags, eps=1e-3))
+        assert a > 0 and a == hla.hla_backward_workspace_size(_params(chunk=64, flags=flags, eps=1e-3))
+    # the split needs a 256-byte aligned workspace, and supports no given state
+    assert _bcall(_params(dv=128), ws=16) == hla.HLA_ERR_ARG
+    good = ctypes.pointer(hla.hla_state(256, 256, 256, 256, 256))
+    assert hla.library().hla_backward_chunked_state(ctypes.byref(_params(dv=128)), 16, 16, 16, 16, good, 16, 16, 16,
+                                                    None, 256, 1 << 40, None) == hla.HLA_ERR_UNSUPPORTED
+    assert "dv = 128" in hla.hla_last_error()
 
 
 def test_backward_state_rejects_bad_args(lib):

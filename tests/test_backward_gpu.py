@@ -190,6 +190,45 @@ def test_backward_normalised_values_with_a_common_offset(decay, Hkv):
     print(f"offset values decay={decay} Hkv={Hkv}: max per-(b,h) rel L2 {err:.3e}")
 
 
+@pytest.mark.parametrize("d,chunk,dtype", [(64, 64, "bf16"), (32, 32, "f32"), (64, 128, "bf16"), (16, 16, "bf16")])
+@pytest.mark.parametrize("decay,normalize", [(False, False), (True, False), (False, True), (True, True)])
+def test_backward_value_width_128(d, chunk, dtype, decay, normalize):
+    """dv = 128 as two 64-column halves of the values (dq, dk summed in fp32, dv side by
+    side; normalised, each half keeps the whole denominator), and a 128-token chunk as two
+    of 64 tokens, against the oracle's gradient."""
+    w = small(B=1, H=2, n=2 * 64 + 37, d=d, dv=128, chunk=chunk, decay=decay, dtype=dtype,
+              qk="elu1" if normalize else "l2", seed=46)
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    eps = 1e-3 if normalize else None
+    check(run_backward(x, g, dtype, chunk, eps=eps), run_oracle(x, g, eps=eps), TOL_F32 if dtype == "f32" else TOL_BF16,
+          f"bwd dv128 {dtype} d{d} c{chunk} decay={decay} norm={normalize}")
+
+
+def test_backward_value_width_128_shared_heads_at_size():
+    """The backward shape of the d = 64, dv = 128 forward workload (ratio-normalised, bf16)
+    at 2048 tokens on four pairs, with two query heads per key/value head."""
+    w = small(B=1, H=4, Hkv=2, n=2048, d=64, dv=128, chunk=64, dtype="bf16", qk="elu1", seed=47)
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    err = check(run_backward(x, g, "bf16", 64, eps=1e-6), run_oracle(x, g, eps=1e-6), TOL_BF16, "bwd dv128 n2048")
+    print(f"bwd dv128 n2048 Hkv2: max per-(b,h) rel L2 {err:.3e}")
+
+
+@pytest.mark.parametrize("normalize", [False, True])
+def test_backward_chunk_128_is_chunk_64(normalize):
+    """The backward runs a 128-token chunk as two 64-token chunks: the same result, bit
+    for bit."""
+    w = small(B=1, H=2, n=300, qk="elu1" if normalize else "l2", decay=True, seed=48)
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    eps = 1e-3 if normalize else None
+    a = run_backward(x, g, "bf16", 128, eps=eps)
+    b = run_backward(x, g, "bf16", 64, eps=eps)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
 def test_backward_normalised_is_gradient_of_forward():
     """The normalised backward against central differences of the library's own
     normalised fp32 forward along a random direction.  Along the line the output is a
