@@ -395,6 +395,40 @@ hla_status hla_backward_chunked_state(const hla_params *p, const void *q, const 
 }
 
 namespace {
+// The shape the third-order kernels run: a 128-token chunk as two of 64 and dv = 128 as
+// two 64-column halves of the values (the output's column j and the state's P, T, M^QP
+// columns j depend on the values' column j only; S^K, S^Q, M^KQ and the unit column's
+// m, h, mqm on none), each half written into its columns (hla_bwd_split.cu copies).
+hla_params fwd3_inner(const hla_params &p) {
+    hla_params q = p;
+    if (q.chunk == 128) q.chunk = 64;
+    if (q.dv == 128) q.dv = 64;
+    return q;
+}
+
+// dv = 128: the half problem's workspace, the gathered value half, the output half, and
+// the value-column halves (P, T, M^QP, fp32) of state_in and of state_out (byte offsets).
+struct Split3 {
+    size_t vh, oh, sin, sout, total;
+};
+Split3 split3_layout(const hla_params &p) {
+    const hla_params q = fwd3_inner(p);
+    const size_t el = p.in_dtype == HLA_F32 ? 4 : 2, rows = (size_t)p.B * p.H * p.n;
+    const size_t half_state = (size_t)p.B * p.H * p.d * 64 * 4;
+    Split3 L;
+    size_t o = align256(hla::fwd3_workspace(q));
+    L.vh = o; o = align256(o + rows * 64 * el);
+    L.oh = o; o = align256(o + rows * 64 * el);
+    L.sin = o; o = align256(o + 3 * half_state);
+    L.sout = o; o = align256(o + 3 * half_state);
+    L.total = o;
+    return L;
+}
+
+hla_status forward3_impl(const hla_params *p, const void *q, const void *k, const void *v, void *o,
+                         const hla_state3 *state_in, const hla_state3 *state_out, void *workspace,
+                         size_t workspace_bytes, void *stream, void *const *phase_events);
+
 hla_status check_fwd3_params(const hla_params *p) {
     if (!p) return fail(HLA_ERR_ARG, "params is NULL");
     if (p->B < 1 || p->H < 1 || p->n < 0) return fail(HLA_ERR_ARG, "need B >= 1, H >= 1, n >= 0");
@@ -405,10 +439,12 @@ hla_status check_fwd3_params(const hla_params *p) {
         return fail(HLA_ERR_ARG, "Hkv must divide H (0 means Hkv = H)");
     if ((long long)p->B * p->H * (long long)p->n * (p->d > p->dv ? p->d : p->dv) > (1LL << 40))
         return fail(HLA_ERR_ARG, "problem too large");
-    if (!hla::fwd3_supported(*p))
+    const bool dv_ok = p->dv == 16 || p->dv == 32 || p->dv == 64 || p->dv == 128;
+    const bool c_ok = p->chunk == 16 || p->chunk == 32 || p->chunk == 64 || p->chunk == 128;
+    if (!dv_ok || !c_ok || !hla::fwd3_supported(fwd3_inner(*p)))
         return fail(HLA_ERR_UNSUPPORTED,
-                    "third order supports flags HLA_DECAY, HLA_NORMALIZE, Hkv = H, d, dv, chunk in {16,32,64} "
-                    "(got flags=%u Hkv=%d d=%d dv=%d chunk=%d)",
+                    "third order supports flags HLA_DECAY, HLA_NORMALIZE, Hkv = H, d in {16,32,64}, dv and chunk "
+                    "in {16,32,64,128} (got flags=%u Hkv=%d d=%d dv=%d chunk=%d)",
                     p->flags, p->Hkv, p->d, p->dv, p->chunk);
     if ((p->flags & HLA_NORMALIZE) && !(p->eps >= 0.f)) return fail(HLA_ERR_ARG, "need eps >= 0");
     if ((p->flags & HLA_DECAY) && !p->gamma) return fail(HLA_ERR_ARG, "HLA_DECAY needs gamma");
@@ -429,7 +465,8 @@ hla_status check_state3(const hla_state3 *s, const char *name, bool normalize, b
 
 size_t hla_forward3_workspace_size(const hla_params *p) {
     if (check_fwd3_params(p) != HLA_OK) return 0;
-    return hla::fwd3_workspace(*p);
+    if (p->dv == 128) return split3_layout(*p).total;
+    return hla::fwd3_workspace(fwd3_inner(*p));
 }
 
 hla_status hla_forward3_chunked(const hla_params *p, const void *q, const void *k, const void *v, void *o,
@@ -442,6 +479,13 @@ hla_status hla_forward3_chunked(const hla_params *p, const void *q, const void *
 hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const void *k, const void *v, void *o,
                                        const hla_state3 *state_in, const hla_state3 *state_out, void *workspace,
                                        size_t workspace_bytes, void *stream, void *const *phase_events) {
+    return forward3_impl(p, q, k, v, o, state_in, state_out, workspace, workspace_bytes, stream, phase_events);
+}
+
+namespace {
+hla_status forward3_impl(const hla_params *p, const void *q, const void *k, const void *v, void *o,
+                         const hla_state3 *state_in, const hla_state3 *state_out, void *workspace,
+                         size_t workspace_bytes, void *stream, void *const *phase_events) {
     hla_status s = check_fwd3_params(p);
     if (s != HLA_OK) return s;
     const bool norm = (p->flags & HLA_NORMALIZE) != 0;
@@ -477,16 +521,63 @@ hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const
     if (!q || !k || !v || !o) return fail(HLA_ERR_ARG, "q, k, v, o must be set when n > 0");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
         return fail(HLA_ERR_ARG, "q, k, v, o must be 16-byte aligned");
-    const size_t need = hla::fwd3_workspace(*p);
+    const size_t need = hla_forward3_workspace_size(p);
     if (!workspace || workspace_bytes < need)
         return fail(HLA_ERR_ARG, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
     if (!aligned16(workspace)) return fail(HLA_ERR_ARG, "workspace must be 16-byte aligned");
-    if (norm && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return fail(HLA_ERR_ARG, "workspace must be 256-byte aligned with HLA_NORMALIZE");
+    const bool split = p->dv == 128;
+    if ((norm || split) && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(HLA_ERR_ARG, "workspace must be 256-byte aligned with HLA_NORMALIZE or dv = 128");
     if (phase_events) {
         for (int i = 0; i < 4; ++i)
             if (!phase_events[i]) return fail(HLA_ERR_ARG, "phase_events must hold four events");
     }
+    if (split) {  // two 64-column halves of the values, each written into its columns
+        const hla_params in = fwd3_inner(*p);
+        const Split3 L = split3_layout(*p);
+        uint8_t *w = static_cast<uint8_t *>(workspace);
+        const size_t rows = (size_t)p->B * p->H * p->n, srows = (size_t)p->B * p->H * p->d;
+        const size_t hs = srows * 64;  // floats of one half array of the state
+        float *ti = reinterpret_cast<float *>(w + L.sin), *to = reinterpret_cast<float *>(w + L.sout);
+        auto ev = [&](int i) {
+            return phase_events ? cudaEventRecord(static_cast<cudaEvent_t>(phase_events[i]), st) : cudaSuccess;
+        };
+        cudaError_t e = ev(0);
+        for (int h = 0; h < 2 && e == cudaSuccess; ++h) {
+            if ((e = hla::cols_half_copy(v, w + L.vh, rows, p->in_dtype, h, true, st)) != cudaSuccess) break;
+            hla_state3 si{}, so{};
+            if (state_in) {
+                si = *state_in;
+                si.P = ti;
+                si.T = ti + hs;
+                si.MQP = maps ? ti + 2 * hs : nullptr;
+                const float *src[3] = {state_in->P, state_in->T, state_in->MQP};
+                for (int i = 0; i < (maps ? 3 : 2) && e == cudaSuccess; ++i)
+                    e = hla::cols_half_copy(src[i], ti + i * hs, srows, HLA_F32, h, true, st);
+                if (e != cudaSuccess) break;
+            }
+            if (state_out) {
+                so = *state_out;
+                so.P = to;
+                so.T = to + hs;
+                so.MQP = maps ? to + 2 * hs : nullptr;
+            }
+            s = forward3_impl(&in, q, k, w + L.vh, w + L.oh, state_in ? &si : nullptr, state_out ? &so : nullptr, w,
+                              L.vh, stream, nullptr);
+            if (s != HLA_OK) return s;
+            if ((e = hla::cols_half_copy(w + L.oh, o, rows, p->in_dtype, h, false, st)) != cudaSuccess) break;
+            if (state_out) {
+                float *dst[3] = {state_out->P, state_out->T, state_out->MQP};
+                for (int i = 0; i < (maps ? 3 : 2) && e == cudaSuccess; ++i)
+                    e = hla::cols_half_copy(to + i * hs, dst[i], srows, HLA_F32, h, false, st);
+            }
+        }
+        for (int i = 1; i < 4 && e == cudaSuccess; ++i) e = ev(i);
+        if (e != cudaSuccess) return cuda_fail(e, "third-order forward over value halves");
+        return HLA_OK;
+    }
+    const hla_params inner = fwd3_inner(*p);
+    p = &inner;
     hla::Fwd3Args a;
     a.B = p->B; a.H = p->H; a.n = p->n; a.d = p->d; a.dv = p->dv; a.chunk = p->chunk;
     a.in_dtype = p->in_dtype;
@@ -524,6 +615,7 @@ hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const
     if (e != cudaSuccess) return cuda_fail(e, "third-order forward launch");
     return HLA_OK;
 }
+}  // namespace
 
 hla_status hla_state3_combine(int count, int d, int dv, unsigned flags, const hla_state3 *A, const hla_state3 *B,
                               const hla_state3 *out, const float *decay_pow, void *stream) {

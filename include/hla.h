@@ -322,15 +322,21 @@ HLA_API size_t hla_forward3_workspace_size(const hla_params *p);
  * (section 4, "Derde-orde scans"): chunk-local sums, a scan over chunks that composes
  * states with the segment-level linear maps M^KQ and M^QP, then per-chunk outputs.
  *   p         flags 0, HLA_DECAY (gamma [H], values in [0, 1]), HLA_NORMALIZE
- *             (eps >= 0) or both; Hkv 0 or H; d, dv, chunk in {16,32,64}; in_dtype
- *             HLA_F32 or HLA_BF16 (fp32 arithmetic);
+ *             (eps >= 0) or both; Hkv 0 or H; d in {16,32,64}, dv and chunk in
+ *             {16,32,64,128}; in_dtype HLA_F32 or HLA_BF16 (fp32 arithmetic).
+ *             dv = 128 runs as two problems over the value columns [0,64) and
+ *             [64,128): the output's column j and the state's P, T, M^QP columns j
+ *             depend on column j of v only, while S, S^Q, M^KQ, m, h, mqm depend on
+ *             no value column; each half writes its columns of o and of state_out.
+ *             A 128-token chunk runs as two of 64 tokens (the same result up to
+ *             rounding);
  *   q, k      [B][H][n][d]; v, o [B][H][n][dv]; in_dtype;
  *   state_in  (S, P, T; with HLA_NORMALIZE also m, h) before the first token, or NULL
  *             for zeros;
  *   state_out (S, P, T; with HLA_NORMALIZE also m, h) after the last token, or NULL;
  *             may not alias state_in;
  *   workspace at least hla_forward3_workspace_size(p) bytes, 16-byte aligned (256-byte
- *             aligned with HLA_NORMALIZE).
+ *             aligned with HLA_NORMALIZE or dv = 128).
  * Three kernel launches on `stream` (tensor cores for bf16 at 64/64/64 without decay,
  * CUDA cores otherwise).  With HLA_NORMALIZE the numerator and the denominator (a
  * 16-wide unit-value tile with the same S) are two such forwards, followed by an
@@ -341,7 +347,8 @@ HLA_API hla_status hla_forward3_chunked(const hla_params *p, const void *q, cons
                                         size_t workspace_bytes, void *stream);
 
 /* hla_forward3_chunked recording four caller-owned events on `stream` (NULL: none):
- * before the local-sums kernel, after it, after the scan and after the output kernel. */
+ * before the local-sums kernel, after it, after the scan and after the output kernel
+ * (with dv = 128: the first before the call, the other three after it). */
 HLA_API hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const void *k, const void *v,
                                                void *o, const hla_state3 *state_in, const hla_state3 *state_out,
                                                void *workspace, size_t workspace_bytes, void *stream,

@@ -236,13 +236,33 @@ def _f3call(p, ptrs=(16,) * 4, sin=None, sout=None, ws=16, ws_bytes=1 << 40):
     (dict(flags=hla.HLA_ASYMMETRIC), hla.HLA_ERR_UNSUPPORTED),
     (dict(H=4, Hkv=2), hla.HLA_ERR_UNSUPPORTED),
     (dict(d=128), hla.HLA_ERR_UNSUPPORTED),
-    (dict(chunk=128), hla.HLA_ERR_UNSUPPORTED),
+    (dict(chunk=256), hla.HLA_ERR_UNSUPPORTED),
     (dict(dv=48), hla.HLA_ERR_UNSUPPORTED),
+    (dict(dv=96), hla.HLA_ERR_UNSUPPORTED),
 ])
 def test_forward3_rejects_bad_params(lib, kw, status):
     assert _f3call(_params(**kw)) == status
     assert hla.hla_last_error()
     assert hla.hla_forward3_workspace_size(_params(**kw)) == 0
+
+
+def test_forward3_value_halves_and_long_chunks(lib):
+    """dv = 128 runs as two 64-column halves: the half problem's workspace, the value and
+    output halves (input type) and the P, T, M^QP halves of state_in and state_out (fp32),
+    in 256-byte aligned regions; a 128-token chunk as two of 64 tokens (the same workspace)."""
+    al = lambda x: -(-x // 256) * 256
+    for dt, el in ((hla.HLA_F32, 4), (hla.HLA_BF16, 2)):
+        for flags in (0, hla.HLA_NORMALIZE):
+            B, H, n, d, c = 2, 3, 100, 32, 32
+            kw = dict(B=B, H=H, n=n, d=d, chunk=c, in_dtype=dt, flags=flags, eps=1e-3)
+            inner = hla.hla_forward3_workspace_size(_params(dv=64, **kw))
+            rows, half = B * H * n, B * H * d * 64 * 4
+            want = al(inner) + 2 * al(rows * 64 * el) + 2 * al(3 * half)
+            assert hla.hla_forward3_workspace_size(_params(dv=128, **kw)) == want
+        assert hla.hla_forward3_workspace_size(_params(chunk=128, in_dtype=dt)) == \
+            hla.hla_forward3_workspace_size(_params(chunk=64, in_dtype=dt))
+    assert _f3call(_params(dv=128), ws=16) == hla.HLA_ERR_ARG
+    assert "256" in hla.hla_last_error()
 
 
 def test_forward3_rejects_null_misaligned_short_workspace_and_aliasing(lib):
