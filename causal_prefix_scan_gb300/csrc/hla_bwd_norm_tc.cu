@@ -495,10 +495,14 @@ __global__ void __launch_bounds__(kTc, 2) out_local_kernel(const __grid_constant
 }
 
 // ======================================================================= 9. grad
-enum { G_Q, G_K, G_V, G_AH, G_AL, G_SH, G_SL, G_XH, G_XL, G_LH, G_LL, G_OH, G_OL, G_A, G_P, G_U, G_DU, G_B, G_M,
-       G_N };
+// A tile is reused once its last reader has completed: V (stage 1) then dU, Lam_n lo
+// (stage 1) then A-tilde, S_p hi (stages 1, 3) then M, S_p lo then (Om + Om^T) hi,
+// X_p hi (stage 3) then B, X_p lo then (Om + Om^T) lo -- 13 tiles, two CTAs per SM.
+// U Lam_n (for dv, where nothing cancels) takes Lam_n's hi part only.
+enum { G_Q, G_K, G_V, G_AH, G_AL, G_SH, G_SL, G_XH, G_XL, G_LH, G_LL, G_P, G_U, G_N };
+constexpr int G_DU = G_V, G_A = G_LL, G_M = G_SH, G_OH = G_SL, G_B = G_XH, G_OL = G_XL;
 
-__global__ void __launch_bounds__(kTc, 1) grad_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kTc, 2) grad_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Ctx x;
     if (!setup(x, smem_raw, G_N, a.err)) return;
@@ -529,7 +533,6 @@ __global__ void __launch_bounds__(kTc, 1) grad_kernel(const __grid_constant__ Bw
         uint8_t *hi[3] = {x.tile(G_SH), x.tile(G_XH), x.tile(G_LH)}, *lo[3] = {x.tile(G_SL), x.tile(G_XL), x.tile(G_LL)};
         load_tiles_hilo<3>(ss, hi, lo);
     }
-    load_sym_hilo(so + NWs::S_OM, x.tile(G_OH), x.tile(G_OL));
     __syncthreads();  // rr is read by the A tiles
     load_tile_rowscaled_hilo(static_cast<const __nv_bfloat16 *>(a.go) + r0, L, rr, x.tile(G_AH), x.tile(G_AL));
     x.publish();
@@ -598,7 +601,8 @@ __global__ void __launch_bounds__(kTc, 1) grad_kernel(const __grid_constant__ Bw
         x.ld_row(64, r);
         store_tril_decay(x, x.tile(G_M), r, gp, 2);
         x.publish();
-        // stage 4: P U + B K;  A~^T dU + B^T Q
+        // stage 4: P U + B K;  A~^T dU + B^T Q; meanwhile Om + Om^T into the tiles of S_p lo
+        // and X_p lo, whose readers (stage 3) are complete
         if (x.tid == 0) {
             mma_km(x.tb + 0, x.tile(G_P), x.tile(G_U), false);
             mma_km(x.tb + 0, x.tile(G_B), x.tile(G_K), true);
@@ -606,6 +610,7 @@ __global__ void __launch_bounds__(kTc, 1) grad_kernel(const __grid_constant__ Bw
             mma_mm(x.tb + 64, x.tile(G_B), x.tile(G_Q), true);
         }
         x.commit();
+        load_sym_hilo(so + NWs::S_OM, x.tile(G_OH), x.tile(G_OL));
         if (!x.wait()) break;
         // dQ = (P U + B K) + r_x (A X_p^T - c Y_p^T) + r_u (dU S_p)
         x.ld_row(0, r);
@@ -627,7 +632,6 @@ __global__ void __launch_bounds__(kTc, 1) grad_kernel(const __grid_constant__ Bw
             mma_mm(x.tb + 0, x.tile(G_M), x.tile(G_AH));
             mma_mm(x.tb + 0, x.tile(G_M), x.tile(G_AL), true);
             mma_km(x.tb + 192, x.tile(G_U), x.tile(G_LH), false);
-            mma_km(x.tb + 192, x.tile(G_U), x.tile(G_LL), true);
         }
         x.commit();
         if (!x.wait()) break;

@@ -32,8 +32,11 @@ __device__ __forceinline__ void fill_gp(float *gp, const BwdArgs &a, int u) {
 
 // tiles of the local-sums kernel (the last four: weighted copies, with decay only)
 enum { L_Q, L_K, L_V, L_G, L_A, L_P, L_UW, L_DUW, L_KW1, L_QW2, L_QW4, L_VW5, L_N };
-// tiles of the gradient kernel
-enum { G_Q, G_K, G_V, G_G, G_SH, G_SL, G_XH, G_XL, G_LH, G_LL, G_OH, G_OL, G_A, G_P, G_U, G_DU, G_B, G_M, G_N };
+// tiles of the gradient kernel; a tile is reused once its last reader has completed:
+// V (stage 1) then dU, S_p hi (stages 1, 3) then M, S_p lo then (Om + Om^T) hi,
+// X_p hi (stage 3) then B, X_p lo then (Om + Om^T) lo -- 13 tiles, two CTAs per SM
+enum { G_Q, G_K, G_V, G_G, G_SH, G_SL, G_XH, G_XL, G_LH, G_LL, G_A, G_P, G_U, G_N };
+constexpr int G_DU = G_V, G_M = G_SH, G_OH = G_SL, G_B = G_XH, G_OL = G_XL;
 
 __global__ void __launch_bounds__(kTc, 2) bwd_local_tc_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -160,7 +163,7 @@ __device__ __forceinline__ void load_sym_hilo(const float *src, uint8_t *hi, uin
     }
 }
 
-__global__ void __launch_bounds__(kTc, 1) bwd_grad_tc_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kTc, 2) bwd_grad_tc_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Ctx x;
     if (!setup(x, smem_raw, G_N, a.err)) return;
@@ -184,7 +187,6 @@ __global__ void __launch_bounds__(kTc, 1) bwd_grad_tc_kernel(const __grid_consta
         uint8_t *hi[3] = {x.tile(G_SH), x.tile(G_XH), x.tile(G_LH)}, *lo[3] = {x.tile(G_SL), x.tile(G_XL), x.tile(G_LL)};
         load_tiles_hilo<3>(ss, hi, lo);
     }
-    load_sym_hilo(so + ws.o_om(), x.tile(G_OH), x.tile(G_OL));
     x.publish();
     // row scales of this thread's token row t
     const int t = x.row;
@@ -245,7 +247,8 @@ __global__ void __launch_bounds__(kTc, 1) bwd_grad_tc_kernel(const __grid_consta
         x.ld_row(64, r);
         store_tril_decay(x, x.tile(G_M), r, gp, 2);
         x.publish();
-        // stage 4: P U + B K;  A~^T dU + B^T Q
+        // stage 4: P U + B K;  A~^T dU + B^T Q; meanwhile Om + Om^T into the tiles of S_p lo
+        // and X_p lo, whose readers (stage 3) are complete
         if (x.tid == 0) {
             mma_km(x.tb + 0, x.tile(G_P), x.tile(G_U), false);
             mma_km(x.tb + 0, x.tile(G_B), x.tile(G_K), true);
@@ -253,6 +256,7 @@ __global__ void __launch_bounds__(kTc, 1) bwd_grad_tc_kernel(const __grid_consta
             mma_mm(x.tb + 64, x.tile(G_B), x.tile(G_Q), true);
         }
         x.commit();
+        load_sym_hilo(so + ws.o_om(), x.tile(G_OH), x.tile(G_OL));
         if (!x.wait()) break;
         // dQ = (P U + B K) + r_x (G X_p^T) + r_u (dU S_p)
         x.ld_row(0, r);
