@@ -142,6 +142,7 @@ struct Fwd2 {
     int ah, part;
     int first_run;
     bool need_mY;
+    bool sp_early = false;  // the current piece's first pass-2 S_p tile was handed over in its setup
     int ts_bh = -1;  // the pair whose S_pre (with its hi / lo tiles) the scan left in TS
 
     __device__ Fwd2(const WsParams &p, uint8_t *b) : P(p), base(b) {}
@@ -658,6 +659,12 @@ struct Fwd2 {
         waitp(B_VF, vpar(it));
         if (tt == 0) arrive_empties(qs, ks);
     }
+    // S_p (TS) into the operand tile for Q S_p, then the MMA warp may go on (T warps)
+    __device__ void t_sp_tile() {
+        const int r = 16 * quad + (lane & 15);
+        rows64<D>(TS, [&](int c0, float (&v)[16]) { tile_store_row16(tSX(), D, r, c0, v); });
+        t_arrive(B_ST);
+    }
     __device__ void t_pass2(int it, bool first, uint32_t &ph, int tt) {
         const int qs = it & 1, ks = kslot(it);
         waitp(B_KF + ks, kpar(it));
@@ -666,8 +673,7 @@ struct Fwd2 {
             tc_fence_after();
         }
         const int r = 16 * quad + (lane & 15);
-        rows64<D>(TS, [&](int c0, float (&v)[16]) { tile_store_row16(tSX(), D, r, c0, v); });  // S_p
-        t_arrive(B_ST);
+        if (!(first && sp_early)) t_sp_tile();
         wait(B_UF, ph);  // Q S_p has read the S_p tile
         tc_fence_after();
         rows64<DV>(TX, [&](int c0, float (&v)[16]) { tile_store_row16(tSX(), D, r, c0, v); });  // X_p
@@ -987,6 +993,22 @@ struct Fwd2 {
         } else {
             st_tmem_zero<D>(TS);
         }
+        // TS = S_pre is final: the T warps hand the first pass-2 chunk its S_p operand now,
+        // so that U = Q S_p + A-tilde K runs while the X_pre rounds below are in flight.  The
+        // MMA warp then moves TS on (S += K^T K), so every later read of S_pre comes first:
+        // the last piece's S_pre m_k for Y_end.  (Folding state_in into piece 0 reads TS
+        // after its product; there the tile is handed over in pass 2 as for later chunks.)
+        sp_early = !(k == 0 && sin);
+        if (sp_early) {
+            if (last && want_out) {
+                const float *mk = summ_of(k) + D * D + 2 * D * DV;
+                for (int i = ah; i < D; i += 256) bvec[i] = __ldcg(mk + i);
+                ah_sync();
+                pscr[rpart() * D + row] = ah_rowdot_S(bvec);
+            }
+            ah_sync();
+            if (part == 1) t_sp_tile();
+        }
         if (last && want_out) {  // C_end = C_in + sum_{r<=k} C_r, m_end likewise -> state_out
             float *Co = P.sout.C + ((size_t)bh * D + row) * DV;
 #pragma unroll
@@ -1037,9 +1059,11 @@ struct Fwd2 {
         }
         if (last && want_out) {
             const float *mk = summ_of(k) + D * D + 2 * D * DV, *Yk = mk + D;
-            for (int i = ah; i < D; i += 256) bvec[i] = __ldcg(mk + i);
-            ah_sync();
-            pscr[rpart() * D + row] = ah_rowdot_S(bvec);
+            if (!sp_early) {
+                for (int i = ah; i < D; i += 256) bvec[i] = __ldcg(mk + i);
+                ah_sync();
+                pscr[rpart() * D + row] = ah_rowdot_S(bvec);
+            }
             ah_sync();
             for (int i = ah; i < D; i += 256) {
                 float sm = 0.f;
