@@ -58,6 +58,7 @@ struct WsParams {
     CUtensorMap tmQ, tmK, tmV, tmO;
     int B, H, n, BH, Hkv;
     int nchunks, cpc, kmax, runs_per_seq;
+    int tail_split;  // the last piece of each sequence split into two halves (runs_per_seq counts both)
     float eps;
     const float *gamma;
     StatePtrs sin, sout;

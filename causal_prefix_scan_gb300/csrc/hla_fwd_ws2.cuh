@@ -140,7 +140,6 @@ struct Fwd2 {
     int tid, warp, lane, quad;
     int bh;
     int ah, part;
-    int first_run;
     bool need_mY;
     bool sp_early = false;  // the current piece's first pass-2 S_p tile was handed over in its setup
     int ts_bh = -1;  // the pair whose S_pre (with its hi / lo tiles) the scan left in TS
@@ -733,9 +732,6 @@ struct Fwd2 {
         ws::nbar(kBarAH, 256);
         tc_fence_after();
     }
-    __device__ __forceinline__ int tstart(int r) const {
-        return r == 0 ? 0 : (int)(((long long)(first_run + r) * P.cpc - (long long)bh * P.nchunks) * CT);
-    }
     __device__ __forceinline__ const float *summ_of(int r) const {
         return P.summ + ((size_t)bh * P.kmax + r) * L_::SUM;
     }
@@ -1202,8 +1198,18 @@ __global__ void __launch_bounds__(kThreads, Lay<DV, NORM>::CTAS) fwd_ws2_kernel(
 
     const long long NCH = P.nchunks;
     const int run = P.runs_per_seq > 0 ? (ticket % P.BH) * P.runs_per_seq + ticket / P.BH : ticket;
-    const long long g0 = (long long)run * P.cpc;
-    const long long g1 = min((long long)P.BH * NCH, g0 + P.cpc);
+    long long g0 = (long long)run * P.cpc;
+    long long g1 = min((long long)P.BH * NCH, g0 + P.cpc);
+    int split_k = -1;
+    if (P.tail_split) {  // pieces 0 .. R-3 of cpc chunks, then two of cpc / 2 (R = runs_per_seq)
+        const int level = ticket / P.BH, seq = ticket % P.BH, whole = P.runs_per_seq - 2;
+        auto start = [&](int j) {
+            return j <= whole ? (long long)j * P.cpc : (long long)whole * P.cpc + (long long)(j - whole) * (P.cpc / 2);
+        };
+        g0 = (long long)seq * NCH + start(level);
+        g1 = (long long)seq * NCH + start(level + 1);
+        split_k = level;
+    }
     const int bh_lo = (int)(g0 / NCH), bh_hi = (int)((g1 - 1) / NCH);
     struct Piece {
         int jb, je, k;
@@ -1213,14 +1219,11 @@ __global__ void __launch_bounds__(kThreads, Lay<DV, NORM>::CTAS) fwd_ws2_kernel(
         Piece pc;
         pc.jb = (int)(max(g0, bh * NCH) - bh * NCH);
         pc.je = (int)(min(g1, (bh + 1) * NCH) - bh * NCH);
-        pc.k = (int)(run - (bh * NCH) / P.cpc);
+        pc.k = split_k >= 0 ? split_k : (int)(run - (bh * NCH) / P.cpc);
         pc.last = (pc.je == P.nchunks);
         return pc;
     };
-    auto select = [&](int bh) {
-        x.bh = bh;
-        x.first_run = (int)((bh * NCH) / P.cpc);
-    };
+    auto select = [&](int bh) { x.bh = bh; };
     int n_phase1 = 0;  // pieces that run pass 1, and their chunks
     x.n1 = 0;
     for (int bh = bh_lo; bh <= bh_hi; ++bh) {
@@ -1380,6 +1383,16 @@ cudaError_t launch_cfg(const FwdArgs &a, cudaStream_t st, int num_sms) {
     P.B = a.B; P.H = a.H; P.n = a.n; P.BH = BH; P.Hkv = a.Hkv;
     P.nchunks = pl.nchunks; P.cpc = pl.cpc; P.kmax = pl.kmax;
     P.runs_per_seq = pl.nchunks % pl.cpc == 0 ? pl.nchunks / pl.cpc : 0;
+    // The last piece of each sequence has the deepest scan and alone exports the state: split
+    // in two halves when the grid still fits on the device at once, so that its pass 2 and the
+    // export no longer end the launch (the piece count stays within kmax = runs + 1).
+    int ncta = pl.ncta;
+    if (P.runs_per_seq > 1 && pl.cpc % 2 == 0 && P.runs_per_seq + 1 <= pl.kmax &&
+        (long long)BH * (P.runs_per_seq + 1) <= (long long)num_sms * ws2_ctas_per_sm(p)) {
+        P.tail_split = 1;
+        P.runs_per_seq += 1;
+        ncta = BH * P.runs_per_seq;
+    }
     P.eps = a.eps; P.gamma = a.gamma;
     P.sin = a.sin; P.sout = a.sout;
     uint8_t *wsp = static_cast<uint8_t *>(a.workspace);
@@ -1392,7 +1405,7 @@ cudaError_t launch_cfg(const FwdArgs &a, cudaStream_t st, int num_sms) {
     auto kern = fwd_ws2_kernel<DV, NORM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L_::SMEM_LAUNCH);
     if (e != cudaSuccess) return e;
-    kern<<<pl.ncta, kThreads, L_::SMEM_LAUNCH, st>>>(P);
+    kern<<<ncta, kThreads, L_::SMEM_LAUNCH, st>>>(P);
     return cudaGetLastError();
 }
 template <bool NORM>

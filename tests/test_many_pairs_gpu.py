@@ -19,9 +19,10 @@ def wl(**kw):
     return W.Workload("pairs", **base)
 
 
-# (B, H, n): 8 pieces of 2 chunks; 7 pieces of one chunk with a ragged tail; 3 pieces of
-# 3 chunks; 2 pieces (one of 2 chunks, one of 1)
-SHAPES = [(4, 8, 2048), (2, 12, 777), (8, 12, 1100), (10, 14, 300)]
+# (B, H, n): 7 pieces of 2 chunks and the last piece split in two of 1; 7 pieces of one
+# chunk with a ragged tail; 3 pieces of 3 chunks; 2 pieces (one of 2 chunks, one of 1);
+# 15 pieces of 2 chunks and two of 1; 7 pieces of 4 chunks and two of 2
+SHAPES = [(4, 8, 2048), (2, 12, 777), (8, 12, 1100), (10, 14, 300), (2, 8, 4096), (4, 8, 4096)]
 
 
 @pytest.mark.parametrize("B,H,n", SHAPES)
@@ -34,7 +35,7 @@ def test_many_pairs_forward(B, H, n, normalize):
     assert_parity(o, o_ref, st, st_ref, TOL_BF16, f"pairs B{B}H{H}n{n} norm={normalize}")
 
 
-@pytest.mark.parametrize("B,H,n", [(4, 8, 2048), (2, 12, 777)])
+@pytest.mark.parametrize("B,H,n", [(4, 8, 2048), (2, 12, 777), (2, 8, 4096)])
 def test_many_pairs_forward_resume(B, H, n):
     """state_in from the oracle's state of a first part (piece 0 folds it in), no state out."""
     w = wl(B=B, H=H, n=n + 333, seed=72)
