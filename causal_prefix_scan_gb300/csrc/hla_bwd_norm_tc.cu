@@ -113,23 +113,19 @@ __device__ __forceinline__ void store_hilo16(uint8_t *hi, uint8_t *lo, int r, in
     tile_store_row16(lo, 64, r, c0, l);
 }
 
-// L rows of 64 bf16, row r scaled by s[r] (fp32), into hi and lo tiles; rows >= L zero.
-__device__ __forceinline__ void load_tile_rowscaled_hilo(const __nv_bfloat16 *src, int L, const float *s,
-                                                         uint8_t *hi, uint8_t *lo) {
+// A bf16 tile (rows r >= L zero) with row r scaled by s[r], in place as the hi part and
+// into `lo` as the rest: each thread rewrites only the elements it read.
+__device__ __forceinline__ void rowscale_hilo_inplace(uint8_t *hi, uint8_t *lo, const float *s, int L) {
     for (int e = threadIdx.x; e < 64 * 4; e += kTc) {
         const int r = e >> 2, c = (e & 3) * 16;
-        float v[16];
         const float w = r < L ? s[r] : 0.f;
+        float a[8], b[8], v[16];
+        tile_load_row8(hi, 64, r, c, a);
+        tile_load_row8(hi, 64, r, c + 8, b);
 #pragma unroll
-        for (int i = 0; i < 16; i += 8) {
-            uint4 u = make_uint4(0, 0, 0, 0);
-            if (r < L) u = *reinterpret_cast<const uint4 *>(src + (size_t)r * 64 + c + i);
-            const uint32_t p[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                v[i + 2 * j] = w * __uint_as_float(p[j] << 16);
-                v[i + 2 * j + 1] = w * __uint_as_float(p[j] & 0xFFFF0000u);
-            }
+        for (int i = 0; i < 8; ++i) {
+            v[i] = w * a[i];
+            v[8 + i] = w * b[i];
         }
         store_hilo16(hi, lo, r, c, v);
     }
@@ -160,7 +156,8 @@ __device__ __forceinline__ float tile_colsum(const uint8_t *tile, int i, const f
 // ======================================================================= 1. fwd_local
 enum { F_Q, F_K, F_V, F_A, F_UW, F_KW1, F_QW2, F_N };
 
-__global__ void __launch_bounds__(kTc, 2) fwd_local_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kTc, 2) fwd_local_kernel(const __grid_constant__ BwdArgs a,
+                                                             const __grid_constant__ ChunkMaps tm) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Ctx x;
     if (!setup(x, smem_raw, F_N, a.err)) return;
@@ -169,26 +166,25 @@ __global__ void __launch_bounds__(kTc, 2) fwd_local_kernel(const __grid_constant
     const int nch = (a.n + 63) / 64, u = blockIdx.x / nch, ch = blockIdx.x % nch;
     const int t0 = ch * 64, L = min(64, a.n - t0);
     const bool decay = (a.flags & HLA_DECAY) != 0;
-    const size_t r0 = ((size_t)u * a.n + t0) * 64, rk = (bwd::kv_unit(a, u) * a.n + t0) * 64;
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q) + r0;
-    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k) + rk;
-    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v) + rk;
-    fill_gp(gp, a, u);
     {
-        const __nv_bfloat16 *src[3] = {q, k, v};
+        const CUtensorMap *m[3] = {&tm.q, &tm.k, &tm.v};
+        const int kvu = (int)bwd::kv_unit(a, u), un[3] = {u, kvu, kvu};
         uint8_t *dst[3] = {x.tile(F_Q), x.tile(F_K), x.tile(F_V)};
-        load_tiles_bf16<3>(src, L, dst);
+        tma_issue<3>(x, m, un, t0, dst);
     }
+    fill_gp(gp, a, u);
     __syncthreads();
-    const uint8_t *kw1 = x.tile(F_K), *qw2 = x.tile(F_Q);
-    if (decay) {  // weighted copies: g^{L-1-s} K, g^{2L-1-s} Q
+    if (decay) {  // token weights of the copies: g^{L-1-s} K, g^{2L-1-s} Q
         for (int s = threadIdx.x; s < 64; s += kTc) {
             w[s] = s < L ? gp[L - 1 - s] : 0.f;
             w[64 + s] = s < L ? gp[2 * L - 1 - s] : 0.f;
         }
-        __syncthreads();
-        load_tile_scaled(k, L, w, x.tile(F_KW1));
-        load_tile_scaled(q, L, w + 64, x.tile(F_QW2));
+    }
+    const bool loaded = tma_wait(x);
+    const uint8_t *kw1 = x.tile(F_K), *qw2 = x.tile(F_Q);
+    if (decay && loaded) {
+        scale_tile(x.tile(F_K), L, w, x.tile(F_KW1));
+        scale_tile(x.tile(F_Q), L, w + 64, x.tile(F_QW2));
         kw1 = x.tile(F_KW1);
         qw2 = x.tile(F_QW2);
     }
@@ -197,6 +193,7 @@ __global__ void __launch_bounds__(kTc, 2) fwd_local_kernel(const __grid_constant
     const size_t ro = (size_t)x.row * 64 + x.c0;
     float r[16];
     do {
+        if (!loaded) break;
         if (x.tid == 0) mma_kk(x.tb + 0, x.tile(F_Q), x.tile(F_K), false);  // Q K^T
         x.commit();
         if (!x.wait()) break;
@@ -301,7 +298,8 @@ __global__ void __launch_bounds__(kTc, 2) incr_kernel(const __grid_constant__ Bw
 //   XB: X_p lo, then g^{2L-s} Q;  T0: A~, then M, then P;  T1: U, then the weighted dU_loc.
 enum { O_Q, O_K, O_V, O_G, O_SA, O_SB, O_XA, O_XB, O_T0, O_T1, O_N };
 
-__global__ void __launch_bounds__(kTc, 2) out_local_kernel(const __grid_constant__ BwdArgs a, float eps) {
+__global__ void __launch_bounds__(kTc, 2) out_local_kernel(const __grid_constant__ BwdArgs a,
+                                                             const __grid_constant__ ChunkMaps tm, float eps) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Ctx x;
     if (!setup(x, smem_raw, O_N, a.err)) return;
@@ -314,27 +312,28 @@ __global__ void __launch_bounds__(kTc, 2) out_local_kernel(const __grid_constant
     const int nch = (a.n + 63) / 64, u = blockIdx.x / nch, ch = blockIdx.x % nch;
     const int t0 = ch * 64, L = min(64, a.n - t0);
     const bool decay = (a.flags & HLA_DECAY) != 0;
-    const size_t r0 = ((size_t)u * a.n + t0) * 64, rk = (bwd::kv_unit(a, u) * a.n + t0) * 64;
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q) + r0;
     const Ptrs R = regions(a);
     float *lc = R.loc + ((size_t)u * nch + ch) * NWs::LOC;
     const float *so = R.st + ((size_t)u * nch + ch) * NWs::ST;
+    {  // the bf16 inputs by TMA while the threads convert the states
+        const CUtensorMap *m[4] = {&tm.q, &tm.k, &tm.v, &tm.g};
+        const int kvu = (int)bwd::kv_unit(a, u), un[4] = {u, kvu, kvu, u};
+        uint8_t *dst[4] = {x.tile(O_Q), x.tile(O_K), x.tile(O_V), x.tile(O_G)};
+        tma_issue<4>(x, m, un, t0, dst);
+    }
     fill_gp(gp, a, u);
     {
-        const __nv_bfloat16 *src[4] = {q, static_cast<const __nv_bfloat16 *>(a.k) + rk,
-                                       static_cast<const __nv_bfloat16 *>(a.v) + rk,
-                                       static_cast<const __nv_bfloat16 *>(a.go) + r0};
-        uint8_t *dst[4] = {x.tile(O_Q), x.tile(O_K), x.tile(O_V), x.tile(O_G)};
-        load_tiles_bf16<4>(src, L, dst);
         const float *ss[2] = {so + NWs::S_SP, so + NWs::S_XP};
         uint8_t *hi[2] = {x.tile(O_SA), x.tile(O_XA)}, *lo[2] = {x.tile(O_SB), x.tile(O_XB)};
         load_tiles_hilo<2>(ss, hi, lo);
     }
+    __syncthreads();  // gp
     for (int i = threadIdx.x; i < 64; i += kTc) {
         yp[i] = so[NWs::S_YP + i];
         w[i] = i < L ? gp[2 * i] : 0.f;
         w[64 + i] = i < L ? gp[2 * L - i] : 0.f;
     }
+    const bool loaded = tma_wait(x);
     x.publish();
     const int t = x.row;
     const bool in = t < L;
@@ -342,6 +341,7 @@ __global__ void __launch_bounds__(kTc, 2) out_local_kernel(const __grid_constant
     const size_t ro = (size_t)t * 64 + x.c0;
     float r[16], s[16];
     do {
+        if (!loaded) break;
         // stage 1: Q K^T; Q S_p; Q X_p
         if (x.tid == 0) {
             mma_kk(x.tb + 0, x.tile(O_Q), x.tile(O_K), false);
@@ -442,8 +442,8 @@ __global__ void __launch_bounds__(kTc, 2) out_local_kernel(const __grid_constant
         x.commit();
         const uint8_t *qw4 = x.tile(O_Q), *qw5 = x.tile(O_Q);
         if (decay) {
-            load_tile_scaled(q, L, w, x.tile(O_XA));
-            load_tile_scaled(q, L, w + 64, x.tile(O_XB));
+            scale_tile(x.tile(O_Q), L, w, x.tile(O_XA));
+            scale_tile(x.tile(O_Q), L, w + 64, x.tile(O_XB));
             qw4 = x.tile(O_XA);
             qw5 = x.tile(O_XB);
         }
@@ -502,7 +502,8 @@ __global__ void __launch_bounds__(kTc, 2) out_local_kernel(const __grid_constant
 enum { G_Q, G_K, G_V, G_AH, G_AL, G_SH, G_SL, G_XH, G_XL, G_LH, G_LL, G_P, G_U, G_N };
 constexpr int G_DU = G_V, G_A = G_LL, G_M = G_SH, G_OH = G_SL, G_B = G_XH, G_OL = G_XL;
 
-__global__ void __launch_bounds__(kTc, 2) grad_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kTc, 2) grad_kernel(const __grid_constant__ BwdArgs a,
+                                                        const __grid_constant__ ChunkMaps tm) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Ctx x;
     if (!setup(x, smem_raw, G_N, a.err)) return;
@@ -514,6 +515,13 @@ __global__ void __launch_bounds__(kTc, 2) grad_kernel(const __grid_constant__ Bw
     const size_t r0 = ((size_t)u * a.n + t0) * 64;
     const Ptrs R = regions(a);
     const float *so = R.st + ((size_t)u * nch + ch) * NWs::ST;
+    {  // the bf16 inputs by TMA (the output gradient into A's hi tile) while the threads
+       // convert the states
+        const CUtensorMap *m[4] = {&tm.q, &tm.k, &tm.v, &tm.g};
+        const int kvu = (int)bwd::kv_unit(a, u), un[4] = {u, kvu, kvu, u};
+        uint8_t *dst[4] = {x.tile(G_Q), x.tile(G_K), x.tile(G_V), x.tile(G_AH)};
+        tma_issue<4>(x, m, un, t0, dst);
+    }
     fill_gp(gp, a, u);
     for (int i = threadIdx.x; i < 64; i += kTc) {
         const bool ok = i < L;
@@ -523,18 +531,12 @@ __global__ void __launch_bounds__(kTc, 2) grad_kernel(const __grid_constant__ Bw
         ln[i] = so[NWs::S_LN + i];
     }
     {
-        const size_t rk = (bwd::kv_unit(a, u) * a.n + t0) * 64;
-        const __nv_bfloat16 *src[3] = {static_cast<const __nv_bfloat16 *>(a.q) + r0,
-                                       static_cast<const __nv_bfloat16 *>(a.k) + rk,
-                                       static_cast<const __nv_bfloat16 *>(a.v) + rk};
-        uint8_t *dst[3] = {x.tile(G_Q), x.tile(G_K), x.tile(G_V)};
-        load_tiles_bf16<3>(src, L, dst);
         const float *ss[3] = {so + NWs::S_SP, so + NWs::S_XP, so + NWs::S_LAM};
         uint8_t *hi[3] = {x.tile(G_SH), x.tile(G_XH), x.tile(G_LH)}, *lo[3] = {x.tile(G_SL), x.tile(G_XL), x.tile(G_LL)};
         load_tiles_hilo<3>(ss, hi, lo);
     }
-    __syncthreads();  // rr is read by the A tiles
-    load_tile_rowscaled_hilo(static_cast<const __nv_bfloat16 *>(a.go) + r0, L, rr, x.tile(G_AH), x.tile(G_AL));
+    const bool loaded = tma_wait(x);  // also orders rr for the A tiles
+    if (loaded) rowscale_hilo_inplace(x.tile(G_AH), x.tile(G_AL), rr, L);
     x.publish();
     const int t = x.row;
     const bool in = t < L;
@@ -543,6 +545,7 @@ __global__ void __launch_bounds__(kTc, 2) grad_kernel(const __grid_constant__ Bw
     const size_t ro = r0 + (size_t)t * 64 + x.c0;
     float r[16], s[16];
     do {
+        if (!loaded) break;
         // stage 1: A~ raw; P raw = A V^T (hi + lo); Q S_p; V Lam_n^T
         if (x.tid == 0) {
             mma_kk(x.tb + 0, x.tile(G_Q), x.tile(G_K), false);
@@ -711,7 +714,9 @@ hla_status bwd_norm_tc_launch(const hla_params &p, const BwdArgs &a0, cudaStream
     pa.units = units; pa.nch = nch; pa.n = a.n; pa.chunk = 64; pa.H = a.H; pa.gamma = gamma;
     if ((e = mark(0)) != cudaSuccess) return fail(e, "event");
     // forward: local sums, S_p, increments, X_p and Y_p, then the outputs and the backward local sums
-    fwd_local_kernel<<<units * nch, kTc, kFwdLocalSmem, st>>>(a);
+    ChunkMaps maps;
+    if (!chunk_maps(maps, a.q, a.k, a.v, a.go, a.n, units, a.B * a.Hkv)) return fail(cudaErrorInvalidValue, "tensor maps");
+    fwd_local_kernel<<<units * nch, kTc, kFwdLocalSmem, st>>>(a, maps);
     pa.njobs = 1;
     pa.job[0] = job(NWs::L_SLOC, NWs::S_SP, 64 * 64, 0, 1);
     if ((e = chunk_prefix(pa, st)) != cudaSuccess) return fail(e, "S prefix");
@@ -720,7 +725,7 @@ hla_status bwd_norm_tc_launch(const hla_params &p, const BwdArgs &a0, cudaStream
     pa.job[0] = job(NWs::L_XLOC, NWs::S_XP, 64 * 64, 0, 2);
     pa.job[1] = job(NWs::L_YLOC, NWs::S_YP, 64, 0, 2);
     if ((e = chunk_prefix(pa, st)) != cudaSuccess) return fail(e, "X prefix");
-    out_local_kernel<<<units * nch, kTc, kOutSmem, st>>>(a, p.eps);
+    out_local_kernel<<<units * nch, kTc, kOutSmem, st>>>(a, maps, p.eps);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail(e, "outputs");
     if ((e = mark(1)) != cudaSuccess) return fail(e, "event");
     // backward scan: Lam_n and lam_n, the increments of Om, then Om_n
@@ -732,7 +737,7 @@ hla_status bwd_norm_tc_launch(const hla_params &p, const BwdArgs &a0, cudaStream
     pa.job[0] = job(NWs::L_OLOC, NWs::S_OM, 64 * 64, 1, 1);
     if ((e = chunk_prefix(pa, st)) != cudaSuccess) return fail(e, "Om suffix");
     if ((e = mark(2)) != cudaSuccess) return fail(e, "event");
-    grad_kernel<<<units * nch, kTc, kGradSmem, st>>>(a);
+    grad_kernel<<<units * nch, kTc, kGradSmem, st>>>(a, maps);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail(e, "gradients");
     if (a.dk_pair) {  // shared key/value heads: sum each group's gradients
         const size_t elems = (size_t)a.B * a.Hkv * a.n * 64;

@@ -38,7 +38,8 @@ enum { L_Q, L_K, L_V, L_G, L_A, L_P, L_UW, L_DUW, L_KW1, L_QW2, L_QW4, L_VW5, L_
 enum { G_Q, G_K, G_V, G_G, G_SH, G_SL, G_XH, G_XL, G_LH, G_LL, G_A, G_P, G_U, G_N };
 constexpr int G_DU = G_V, G_M = G_SH, G_OH = G_SL, G_B = G_XH, G_OL = G_XL;
 
-__global__ void __launch_bounds__(kTc, 2) bwd_local_tc_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kTc, 2) bwd_local_tc_kernel(const __grid_constant__ BwdArgs a,
+                                                                const __grid_constant__ ChunkMaps tm) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Ctx x;
     if (!setup(x, smem_raw, L_N, a.err)) return;
@@ -47,21 +48,15 @@ __global__ void __launch_bounds__(kTc, 2) bwd_local_tc_kernel(const __grid_const
     const int nch = (a.n + 63) / 64, u = blockIdx.x / nch, ch = blockIdx.x % nch;
     const int t0 = ch * 64, L = min(64, a.n - t0);
     const bool decay = (a.flags & HLA_DECAY) != 0;
-    const size_t r0 = ((size_t)u * a.n + t0) * 64;
-    const size_t rk = (bwd::kv_unit(a, u) * a.n + t0) * 64;  // rows of the key/value head
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q) + r0;
-    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k) + rk;
-    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v) + rk;
-    const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(a.go) + r0;
-    fill_gp(gp, a, u);
     {
-        const __nv_bfloat16 *src[4] = {q, k, v, g};
+        const CUtensorMap *m[4] = {&tm.q, &tm.k, &tm.v, &tm.g};
+        const int kvu = (int)bwd::kv_unit(a, u), un[4] = {u, kvu, kvu, u};
         uint8_t *dst[4] = {x.tile(L_Q), x.tile(L_K), x.tile(L_V), x.tile(L_G)};
-        load_tiles_bf16<4>(src, L, dst);
+        tma_issue<4>(x, m, un, t0, dst);
     }
+    fill_gp(gp, a, u);
     __syncthreads();
-    const uint8_t *kw1 = x.tile(L_K), *qw2 = x.tile(L_Q), *qw4 = x.tile(L_Q), *vw5 = x.tile(L_V);
-    if (decay) {  // weighted copies: g^{L-1-s} K, g^{2L-1-s} Q, g^{2s} Q, g^{2L-s} V
+    if (decay) {  // token weights of the copies: g^{L-1-s} K, g^{2L-1-s} Q, g^{2s} Q, g^{2L-s} V
         for (int s = threadIdx.x; s < 64; s += kTc) {
             const bool in = s < L;
             w[s] = in ? gp[L - 1 - s] : 0.f;
@@ -69,11 +64,14 @@ __global__ void __launch_bounds__(kTc, 2) bwd_local_tc_kernel(const __grid_const
             w[128 + s] = in ? gp[2 * s] : 0.f;
             w[192 + s] = in ? gp[2 * L - s] : 0.f;
         }
-        __syncthreads();
-        load_tile_scaled(k, L, w, x.tile(L_KW1));
-        load_tile_scaled(q, L, w + 64, x.tile(L_QW2));
-        load_tile_scaled(q, L, w + 128, x.tile(L_QW4));
-        load_tile_scaled(v, L, w + 192, x.tile(L_VW5));
+    }
+    const bool loaded = tma_wait(x);
+    const uint8_t *kw1 = x.tile(L_K), *qw2 = x.tile(L_Q), *qw4 = x.tile(L_Q), *vw5 = x.tile(L_V);
+    if (decay && loaded) {  // the weighted copies, from the tiles
+        scale_tile(x.tile(L_K), L, w, x.tile(L_KW1));
+        scale_tile(x.tile(L_Q), L, w + 64, x.tile(L_QW2));
+        scale_tile(x.tile(L_Q), L, w + 128, x.tile(L_QW4));
+        scale_tile(x.tile(L_V), L, w + 192, x.tile(L_VW5));
         kw1 = x.tile(L_KW1); qw2 = x.tile(L_QW2); qw4 = x.tile(L_QW4); vw5 = x.tile(L_VW5);
     }
     x.publish();
@@ -82,6 +80,7 @@ __global__ void __launch_bounds__(kTc, 2) bwd_local_tc_kernel(const __grid_const
     const size_t ro = (size_t)x.row * 64 + x.c0;
     float r[16];
     do {
+        if (!loaded) break;
         // A~ = Q K^T, P = G V^T
         if (x.tid == 0) {
             mma_kk(x.tb + 0, x.tile(L_Q), x.tile(L_K), false);
@@ -163,7 +162,8 @@ __device__ __forceinline__ void load_sym_hilo(const float *src, uint8_t *hi, uin
     }
 }
 
-__global__ void __launch_bounds__(kTc, 2) bwd_grad_tc_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kTc, 2) bwd_grad_tc_kernel(const __grid_constant__ BwdArgs a,
+                                                               const __grid_constant__ ChunkMaps tm) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Ctx x;
     if (!setup(x, smem_raw, G_N, a.err)) return;
@@ -174,19 +174,19 @@ __global__ void __launch_bounds__(kTc, 2) bwd_grad_tc_kernel(const __grid_consta
     const BwdWs ws{64, 64};
     const float *so =
         a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
+    {  // the bf16 inputs by TMA while the threads convert the states
+        const CUtensorMap *m[4] = {&tm.q, &tm.k, &tm.v, &tm.g};
+        const int kvu = (int)bwd::kv_unit(a, u), un[4] = {u, kvu, kvu, u};
+        uint8_t *dst[4] = {x.tile(G_Q), x.tile(G_K), x.tile(G_V), x.tile(G_G)};
+        tma_issue<4>(x, m, un, t0, dst);
+    }
     fill_gp(gp, a, u);
     {
-        const size_t rk = (bwd::kv_unit(a, u) * a.n + t0) * 64;  // rows of the key/value head
-        const __nv_bfloat16 *src[4] = {static_cast<const __nv_bfloat16 *>(a.q) + r0,
-                                       static_cast<const __nv_bfloat16 *>(a.k) + rk,
-                                       static_cast<const __nv_bfloat16 *>(a.v) + rk,
-                                       static_cast<const __nv_bfloat16 *>(a.go) + r0};
-        uint8_t *dst[4] = {x.tile(G_Q), x.tile(G_K), x.tile(G_V), x.tile(G_G)};
-        load_tiles_bf16<4>(src, L, dst);
         const float *ss[3] = {so + ws.o_sp(), so + ws.o_xp(), so + ws.o_lam()};
         uint8_t *hi[3] = {x.tile(G_SH), x.tile(G_XH), x.tile(G_LH)}, *lo[3] = {x.tile(G_SL), x.tile(G_XL), x.tile(G_LL)};
         load_tiles_hilo<3>(ss, hi, lo);
     }
+    const bool loaded = tma_wait(x);
     x.publish();
     // row scales of this thread's token row t
     const int t = x.row;
@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(kTc, 2) bwd_grad_tc_kernel(const __grid_consta
     const size_t ro = r0 + (size_t)t * 64 + x.c0;
     float r[16], s[16];
     do {
+        if (!loaded) break;
         // stage 1: A~, P raw; Q S_p; V Lam^T
         if (x.tid == 0) {
             mma_kk(x.tb + 0, x.tile(G_Q), x.tile(G_K), false);
@@ -308,7 +309,9 @@ cudaError_t local_tc(const BwdArgs &a, cudaStream_t st) {
     cudaError_t e =
         cudaFuncSetAttribute(bwd_local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLocalSmem);
     if (e != cudaSuccess) return e;
-    bwd_local_tc_kernel<<<a.B * a.H * ((a.n + 63) / 64), kTc, kLocalSmem, st>>>(a);
+    ChunkMaps m;
+    if (!chunk_maps(m, a.q, a.k, a.v, a.go, a.n, a.B * a.H, a.B * a.Hkv)) return cudaErrorInvalidValue;
+    bwd_local_tc_kernel<<<a.B * a.H * ((a.n + 63) / 64), kTc, kLocalSmem, st>>>(a, m);
     return cudaGetLastError();
 }
 
@@ -316,7 +319,9 @@ cudaError_t grad_tc(const BwdArgs &a, cudaStream_t st) {
     cudaError_t e =
         cudaFuncSetAttribute(bwd_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem);
     if (e != cudaSuccess) return e;
-    bwd_grad_tc_kernel<<<a.B * a.H * ((a.n + 63) / 64), kTc, kGradSmem, st>>>(a);
+    ChunkMaps m;
+    if (!chunk_maps(m, a.q, a.k, a.v, a.go, a.n, a.B * a.H, a.B * a.Hkv)) return cudaErrorInvalidValue;
+    bwd_grad_tc_kernel<<<a.B * a.H * ((a.n + 63) / 64), kTc, kGradSmem, st>>>(a, m);
     return cudaGetLastError();
 }
 

@@ -1,13 +1,27 @@
 // hla_chunk_tc.cuh -- shared machinery of the per-chunk tensor-core kernels (third
 // order, backward): one CTA of 8 warps (two per TMEM lane quadrant) per chunk of 64
-// tokens, 64 x 64 bf16 operand tiles in 128-byte-swizzled shared memory, 64-row
-// tcgen05.mma groups issued by thread 0 into 64-column TMEM accumulators, bounded
-// mbarrier waits that raise the sticky status flag instead of hanging.
+// tokens, 64 x 64 bf16 operand tiles in 128-byte-swizzled shared memory (the bf16 inputs
+// brought in by TMA, the fp32 states converted by the threads), 64-row tcgen05.mma groups
+// issued by thread 0 into 64-column TMEM accumulators, bounded mbarrier waits that raise
+// the sticky status flag instead of hanging.
 #pragma once
 #include "hla_internal.h"
+#include "hla_tmap.h"
 
 namespace hla {
 namespace chunktc {
+
+// Tensor maps of the bf16 inputs a chunk kernel loads: [units][n][64], boxes of 64 token
+// rows of one unit (q and the output gradient over query heads, k and v over key/value heads).
+struct ChunkMaps {
+    CUtensorMap q, k, v, g;
+};
+// false if the driver's encoder is unavailable or rejects a tensor; g may be null
+inline bool chunk_maps(ChunkMaps &m, const void *q, const void *k, const void *v, const void *g, int n, int units,
+                       int kv_units) {
+    return tc::encode_3d(&m.q, q, 64, n, units, 64) && tc::encode_3d(&m.k, k, 64, n, kv_units, 64) &&
+           tc::encode_3d(&m.v, v, 64, n, kv_units, 64) && (!g || tc::encode_3d(&m.g, g, 64, n, units, 64));
+}
 
 // One elementwise scan over the chunks of every pair: out[ch] = R, R = f_ch R + in[ch],
 // f_ch = g^{power * L_ch} (1 without decay), in chunk order (reverse: last chunk first).
@@ -39,8 +53,8 @@ constexpr uint32_t kCols = 256;    // TMEM columns: four 64-column accumulators
 
 struct Ctx {
     uint8_t *base;
-    uint64_t *bar;
-    uint32_t tb, ph;
+    uint64_t *bar, *tbar;  // MMA completion; TMA tile arrival
+    uint32_t tb, ph, tph;
     int tid, warp, lane, quad, half;
     int row, c0;  // the accumulator row this thread reads and its first of 16 columns
     unsigned *err;
@@ -101,41 +115,12 @@ __device__ __forceinline__ void mma_mm(uint32_t d, const uint8_t *a, const uint8
         umma_f16(d, da + (uint32_t)(k * 8), db + (uint32_t)(k * 8), id, (acc || k > 0) ? 1u : 0u);
 }
 
-// L rows of 64 bf16 (row-major) into a swizzled tile; rows >= L are zero.
-__device__ __forceinline__ void load_tile_bf16(const __nv_bfloat16 *src, int L, uint8_t *tile) {
-    for (int e = threadIdx.x; e < 64 * 8; e += kTc) {
-        const int r = e >> 3, c = (e & 7) * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (r < L) v = *reinterpret_cast<const uint4 *>(src + (size_t)r * 64 + c);
-        *reinterpret_cast<uint4 *>(tile + tile_off(64, r, c)) = v;
-    }
-}
-// A 64 x 64 fp32 matrix (row-major) into bf16 hi and lo tiles (hi + lo = the value to
-// about 2^-17 relative).
-__device__ __forceinline__ void load_tile_hilo(const float *src, uint8_t *hi, uint8_t *lo) {
-    for (int e = threadIdx.x; e < 64 * 4; e += kTc) {
-        const int r = e >> 2, c = (e & 3) * 16;
-        float v[16], h[16], l[16];
-#pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(src + (size_t)r * 64 + c + i);
-            v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            h[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
-            l[i] = v[i] - h[i];
-        }
-        tile_store_row16(hi, 64, r, c, h);
-        tile_store_row16(lo, 64, r, c, l);
-    }
-}
-
 // Block setup shared by both kernels: barrier, TMEM allocation.  Returns false if
 // the shared window is not 1024-byte aligned (then nothing was allocated).
 __device__ bool setup(Ctx &x, uint8_t *smem, int ntiles, unsigned *err) {
     x.base = smem;
     x.bar = reinterpret_cast<uint64_t *>(smem + ntiles * TILE);
+    x.tbar = reinterpret_cast<uint64_t *>(smem + ntiles * TILE + 16);
     uint32_t *tptr = reinterpret_cast<uint32_t *>(smem + ntiles * TILE + 8);
     int *bad = reinterpret_cast<int *>(smem + ntiles * TILE + 12);
     x.tid = threadIdx.x;
@@ -146,10 +131,12 @@ __device__ bool setup(Ctx &x, uint8_t *smem, int ntiles, unsigned *err) {
     x.row = 16 * x.quad + (x.lane & 15);
     x.c0 = x.half * 32 + (x.lane >> 4) * 16;
     x.ph = 0;
+    x.tph = 0;
     x.err = err;
     if (x.tid == 0) {
         *bad = (smem_u32(smem) & 1023u) != 0;
         mbar_init(x.bar, 1);
+        mbar_init(x.tbar, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -168,6 +155,40 @@ __device__ bool setup(Ctx &x, uint8_t *smem, int ntiles, unsigned *err) {
     return true;
 }
 
+// N tiles of 64 token rows by TMA (thread 0 issues): map m[i] at (feature 0, token t0,
+// unit u[i]) into tile d[i]; rows past the sequence arrive as zeros.  Wait with tma_wait.
+template <int N>
+__device__ __forceinline__ void tma_issue(const Ctx &x, const CUtensorMap *const (&m)[N], const int (&u)[N], int t0,
+                                          uint8_t *const (&d)[N]) {
+    if (x.tid == 0) {
+        mbar_expect_tx(x.tbar, N * TILE);
+#pragma unroll
+        for (int i = 0; i < N; ++i) tma_load_3d(d[i], m[i], x.tbar, 0, t0, u[i]);
+    }
+}
+// Every thread: bounded wait for the tiles of the last tma_issue; false (uniform) if it expired.
+__device__ __forceinline__ bool tma_wait(Ctx &x) {
+    const bool ok = mbar_wait(x.tbar, x.tph, x.err);
+    x.tph ^= 1u;
+    return !__syncthreads_or(!ok);
+}
+// A bf16 tile with row r scaled by w[r] (zero for r >= L) into another tile.
+__device__ __forceinline__ void scale_tile(const uint8_t *src, int L, const float *w, uint8_t *dst) {
+    for (int e = threadIdx.x; e < 64 * 4; e += kTc) {
+        const int r = e >> 2, c = (e & 3) * 16;
+        const float s = r < L ? w[r] : 0.f;
+        float a[8], b[8], v[16];
+        tile_load_row8(src, 64, r, c, a);
+        tile_load_row8(src, 64, r, c + 8, b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[i] = s * a[i];
+            v[8 + i] = s * b[i];
+        }
+        tile_store_row16(dst, 64, r, c, v);
+    }
+}
+
 __device__ void teardown(const Ctx &x) {
     tc_fence_before();
     __syncthreads();
@@ -183,26 +204,6 @@ __device__ __forceinline__ void store_tril(const Ctx &x, uint8_t *tile, float (&
     tile_store_row16(tile, 64, x.row, x.c0, v);
 }
 
-// N tiles of L rows of 64 bf16 each (row-major) into swizzled tiles, rows >= L zero;
-// every global load of the batch is issued before the first shared store.
-template <int N>
-__device__ __forceinline__ void load_tiles_bf16(const __nv_bfloat16 *const (&src)[N], int L, uint8_t *const (&tile)[N]) {
-    uint4 v[N][2];
-#pragma unroll
-    for (int t = 0; t < N; ++t)
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            const int e = threadIdx.x + p * kTc, r = e >> 3, c = (e & 7) * 8;
-            v[t][p] = r < L ? *reinterpret_cast<const uint4 *>(src[t] + (size_t)r * 64 + c) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-    for (int t = 0; t < N; ++t)
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            const int e = threadIdx.x + p * kTc, r = e >> 3, c = (e & 7) * 8;
-            *reinterpret_cast<uint4 *>(tile[t] + tile_off(64, r, c)) = v[t][p];
-        }
-}
 // N fp32 64 x 64 matrices (row-major) into bf16 hi and lo tiles; all loads first.
 template <int N>
 __device__ __forceinline__ void load_tiles_hilo(const float *const (&src)[N], uint8_t *const (&hi)[N],
@@ -230,26 +231,6 @@ __device__ __forceinline__ void load_tiles_hilo(const float *const (&src)[N], ui
     }
 }
 
-// L rows of 64 bf16 scaled by w[r] into a swizzled tile (bf16 after scaling); rows >= L zero.
-__device__ __forceinline__ void load_tile_scaled(const __nv_bfloat16 *src, int L, const float *w, uint8_t *tile) {
-    for (int e = threadIdx.x; e < 64 * 4; e += kTc) {
-        const int r = e >> 2, c = (e & 3) * 16;
-        float v[16];
-        const float s = r < L ? w[r] : 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; i += 8) {
-            uint4 u = make_uint4(0, 0, 0, 0);
-            if (r < L) u = *reinterpret_cast<const uint4 *>(src + (size_t)r * 64 + c + i);
-            const uint32_t p[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                v[i + 2 * j] = s * __uint_as_float(p[j] << 16);
-                v[i + 2 * j + 1] = s * __uint_as_float(p[j] & 0xFFFF0000u);
-            }
-        }
-        tile_store_row16(tile, 64, r, c, v);
-    }
-}
 // 16 accumulator values of this thread's row into a tile, lower triangle kept and
 // weighted by gp[step * (row - col)] (powers of the decay factor)
 __device__ __forceinline__ void store_tril_decay(const Ctx &x, uint8_t *tile, float (&v)[16], const float *gp, int step) {

@@ -25,7 +25,8 @@ enum { L_Q, L_K, L_V, L_A, L_U, L_W, L_N };
 // tiles of the output kernel
 enum { O_Q, O_K, O_V, O_SH, O_SL, O_PH, O_PL, O_TH, O_TL, O_A, O_U, O_W, O_N };
 
-__global__ void __launch_bounds__(kTc, 2) fwd3_local_tc_kernel(const __grid_constant__ Fwd3Args a) {
+__global__ void __launch_bounds__(kTc, 2) fwd3_local_tc_kernel(const __grid_constant__ Fwd3Args a,
+                                                                 const __grid_constant__ ChunkMaps tm) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Ctx x;
     if (!setup(x, smem_raw, L_N, a.err)) return;
@@ -33,15 +34,16 @@ __global__ void __launch_bounds__(kTc, 2) fwd3_local_tc_kernel(const __grid_cons
     const int t0 = ch * 64, L = min(64, a.n - t0);
     const size_t r0 = ((size_t)u * a.n + t0) * 64;
     {
-        const __nv_bfloat16 *src[3] = {static_cast<const __nv_bfloat16 *>(a.q) + r0,
-                                       static_cast<const __nv_bfloat16 *>(a.k) + r0,
-                                       static_cast<const __nv_bfloat16 *>(a.v) + r0};
+        const CUtensorMap *m[3] = {&tm.q, &tm.k, &tm.v};
+        const int un[3] = {u, u, u};
         uint8_t *dst[3] = {x.tile(L_Q), x.tile(L_K), x.tile(L_V)};
-        load_tiles_bf16<3>(src, L, dst);
+        tma_issue<3>(x, m, un, t0, dst);
     }
+    const bool loaded = tma_wait(x);
     x.publish();
     float v[16];
     do {
+        if (!loaded) break;
         // A~ = tril(Q K^T)
         if (x.tid == 0) mma_kk(x.tb, x.tile(L_Q), x.tile(L_K), false);
         x.commit();
@@ -97,7 +99,8 @@ __global__ void __launch_bounds__(kTc, 2) fwd3_local_tc_kernel(const __grid_cons
     teardown(x);
 }
 
-__global__ void __launch_bounds__(kTc, 2) fwd3_out_tc_kernel(const __grid_constant__ Fwd3Args a) {
+__global__ void __launch_bounds__(kTc, 2) fwd3_out_tc_kernel(const __grid_constant__ Fwd3Args a,
+                                                               const __grid_constant__ ChunkMaps tm) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Ctx x;
     if (!setup(x, smem_raw, O_N, a.err)) return;
@@ -106,20 +109,21 @@ __global__ void __launch_bounds__(kTc, 2) fwd3_out_tc_kernel(const __grid_consta
     const size_t r0 = ((size_t)u * a.n + t0) * 64;
     const Ws3 ws{64, 64};
     const float *so = a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
-    {
-        const __nv_bfloat16 *src[3] = {static_cast<const __nv_bfloat16 *>(a.q) + r0,
-                                       static_cast<const __nv_bfloat16 *>(a.k) + r0,
-                                       static_cast<const __nv_bfloat16 *>(a.v) + r0};
+    {  // the bf16 inputs by TMA while the threads convert the states
+        const CUtensorMap *m[3] = {&tm.q, &tm.k, &tm.v};
+        const int un[3] = {u, u, u};
         uint8_t *dst[3] = {x.tile(O_Q), x.tile(O_K), x.tile(O_V)};
-        load_tiles_bf16<3>(src, L, dst);
+        tma_issue<3>(x, m, un, t0, dst);
         const float *ss[3] = {so + ws.s_sk(), so + ws.s_p(), so + ws.s_t()};
         uint8_t *hi[3] = {x.tile(O_SH), x.tile(O_PH), x.tile(O_TH)}, *lo[3] = {x.tile(O_SL), x.tile(O_PL), x.tile(O_TL)};
         load_tiles_hilo<3>(ss, hi, lo);
     }
+    const bool loaded = tma_wait(x);
     x.publish();
     constexpr uint32_t SA = 0, SU = 64, SW = 128, SO = 192;
     float v[16];
     do {
+        if (!loaded) break;
         // A~ = Q K^T, and the prefix-state terms Q S^K_p, Q P_p, Q T_p
         if (x.tid == 0) {
             mma_kk(x.tb + SA, x.tile(O_Q), x.tile(O_K), false);
@@ -182,7 +186,9 @@ cudaError_t local_tc(const Fwd3Args &a, cudaStream_t st) {
                                          (int)kLocalSmem);
     if (e != cudaSuccess) return e;
     const int nch = (a.n + 63) / 64;
-    fwd3_local_tc_kernel<<<a.B * a.H * nch, kTc, kLocalSmem, st>>>(a);
+    ChunkMaps m;
+    if (!chunk_maps(m, a.q, a.k, a.v, nullptr, a.n, a.B * a.H, a.B * a.H)) return cudaErrorInvalidValue;
+    fwd3_local_tc_kernel<<<a.B * a.H * nch, kTc, kLocalSmem, st>>>(a, m);
     return cudaGetLastError();
 }
 
@@ -191,7 +197,9 @@ cudaError_t out_tc(const Fwd3Args &a, cudaStream_t st) {
         cudaFuncSetAttribute(fwd3_out_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
     if (e != cudaSuccess) return e;
     const int nch = (a.n + 63) / 64;
-    fwd3_out_tc_kernel<<<a.B * a.H * nch, kTc, kOutSmem, st>>>(a);
+    ChunkMaps m;
+    if (!chunk_maps(m, a.q, a.k, a.v, nullptr, a.n, a.B * a.H, a.B * a.H)) return cudaErrorInvalidValue;
+    fwd3_out_tc_kernel<<<a.B * a.H * nch, kTc, kOutSmem, st>>>(a, m);
     return cudaGetLastError();
 }
 

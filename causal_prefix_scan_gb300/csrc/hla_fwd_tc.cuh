@@ -53,6 +53,7 @@
 #include <cstring>
 
 #include "hla_internal.h"
+#include "hla_tmap.h"
 
 namespace hla {
 namespace tc {
@@ -2144,31 +2145,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<C, D, DV>::CTAS) fwd_tc_kernel(c
 }
 
 // ============================================================================ host side
-inline PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        cudaDriverEntryPointQueryResult q;
-        void *p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-inline bool encode_3d(CUtensorMap *tm, const void *ptr, int width, int n, int BH, int box_rows) {
-    auto enc = get_encoder();
-    if (!enc) return false;
-    cuuint64_t gdim[3] = {(cuuint64_t)width, (cuuint64_t)n, (cuuint64_t)BH};
-    cuuint64_t gstr[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * (cuuint64_t)n};
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), gdim, gstr, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 struct Plan {
     int nchunks;  // chunks per sequence
     int cpc;      // chunks per CTA (a run in the end-to-end order of all sequences)
