@@ -621,7 +621,8 @@ hla_status hla_state3_combine(int count, int d, int dv, unsigned flags, const hl
                               const hla_state3 *out, const float *decay_pow, void *stream) {
     if (count < 0) return fail(HLA_ERR_ARG, "need count >= 0");
     auto ok = [](int x) { return x == 16 || x == 32 || x == 64; };
-    if (!ok(d) || !ok(dv)) return fail(HLA_ERR_UNSUPPORTED, "d, dv must be in {16,32,64} (got %d, %d)", d, dv);
+    if (!ok(d) || !(ok(dv) || dv == 128))
+        return fail(HLA_ERR_UNSUPPORTED, "d must be in {16,32,64} and dv in {16,32,64,128} (got %d, %d)", d, dv);
     if (flags & ~(unsigned)HLA_NORMALIZE) return fail(HLA_ERR_UNSUPPORTED, "flags must be 0 or HLA_NORMALIZE");
     if (!A || !B || !out) return fail(HLA_ERR_ARG, "A, B, out must be set");
     const bool norm = (flags & HLA_NORMALIZE) != 0;

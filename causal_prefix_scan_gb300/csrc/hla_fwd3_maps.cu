@@ -227,6 +227,14 @@ cudaError_t state3_combine_launch(int count, int d, int dv, bool norm, const hla
                                   const hla_state3 &out, const float *decay_pow, cudaStream_t st) {
     if (count == 0) return cudaSuccess;
     fwd3::Comb3 c{count, d, dv, norm, A, B, out, decay_pow};
+    if (dv == 128) {  // the concatenation at dv = 128 (the forward reaches it through value halves)
+        switch (d) {
+            case 16: return fwd3::combine_t<16, 128>(c, st);
+            case 32: return fwd3::combine_t<32, 128>(c, st);
+            case 64: return fwd3::combine_t<64, 128>(c, st);
+        }
+        return cudaErrorInvalidValue;
+    }
     return fwd3::by_width<fwd3::CombFn>(d, dv, c, st);
 }
 

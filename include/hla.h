@@ -376,7 +376,7 @@ HLA_API hla_status hla_decode3_step(int N, int H, int d, int dv, hla_dtype dtype
  * and with HLA_NORMALIZE the unit column likewise (m as P, h as T, mqm as M^QP).
  * A, B, out: hla_state3 with S, P, T, SQ, MQP, MKQ (and m, h, mqm with HLA_NORMALIZE),
  * fp32 [count][...]; out may alias A or B (each item is read whole before it is
- * written).  flags: 0 or HLA_NORMALIZE; d, dv in {16, 32, 64}.  One launch on `stream`.
+ * written).  flags: 0 or HLA_NORMALIZE; d in {16, 32, 64}, dv in {16, 32, 64, 128}.  One launch on `stream`.
  */
 HLA_API hla_status hla_state3_combine(int count, int d, int dv, unsigned flags, const hla_state3 *A,
                                       const hla_state3 *B, const hla_state3 *out, const float *decay_pow,

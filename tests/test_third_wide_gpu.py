@@ -87,3 +87,23 @@ def test_forward3_chunk_128_is_chunk_64():
     for name in ("SQ", "MQP", "MKQ", "mqm"):
         a, b = getattr(s128, name).double(), getattr(s64, name).double()
         assert float((a - b).norm() / b.norm()) < 1e-6, name
+
+
+@pytest.mark.parametrize("normalize", [False, True])
+def test_concatenation_at_value_width_128(normalize):
+    """Two dv = 128 segments summarised independently (with their maps) and concatenated on
+    the GPU equal the summary of the joined sequence."""
+    w, x = case(32, 32, 190, "f32", True, normalize, 94)
+    cut = 83
+    _, A = gpu3(x, w, normalize, part=(0, cut))
+    _, Bs = gpu3(x, w, normalize, part=(cut, w.n))
+    units = w.B * w.H
+    g = np.asarray(x["gamma"], np.float64)
+    fpow = torch.from_numpy((g[np.arange(units) % w.H] ** (w.n - cut)).astype(np.float32)).cuda()
+    AB = hla.state3_combine(A, Bs, decay_pow=fpow, normalize=normalize)
+    hla.hla_sync_status()
+    o_ref, st_ref = oracle.forward3(x["q"], x["k"], x["v"], chunk=16, gamma=x["gamma"], normalize=normalize, eps=1e-3)
+    for name, want in expect(st_ref, units, w.d, 128, normalize).items():
+        got = getattr(AB, name).double().cpu().numpy().reshape(want.shape[0], 1, -1)
+        e = per_pair_errors(got, want.reshape(want.shape[0], 1, -1)).max()
+        assert e <= TOL_F32, f"combine dv128: {name} {e:.3e}"
