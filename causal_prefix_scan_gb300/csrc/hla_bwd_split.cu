@@ -1,4 +1,6 @@
-// hla_bwd_split.cu -- the copies around a backward pass split over value columns.
+// hla_bwd_split.cu -- the copies around a call split over value columns (the backward
+// pass, and the third-order forward, whose output and value-width state columns split the
+// same way: column j depends on the values' column j only).
 //
 // The loss sum_t dout_t . o_t is a sum over value columns, and column j of the output
 // depends on column j of the values only (o_t[j] = q_t^T X_t[:, j], X_t[:, j] built from

@@ -115,7 +115,8 @@ struct NormLayout {
 };
 NormLayout bwd_norm_layout(const hla_params &p);
 hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a, void *workspace, cudaStream_t st);
-// A backward pass split over value columns (hla_bwd_split.cu): columns [64 half, 64 half + 64)
+// A call split over value columns (hla_bwd_split.cu; the backward and the third-order
+// forward at dv = 128): columns [64 half, 64 half + 64)
 // of [rows][128] elements of type dt gathered into [rows][64] (or scattered back), and
 // the fp32 sum of the halves' dq, dk (first: overwrite) with its final rounding.
 cudaError_t cols_half_copy(const void *src, void *dst, size_t rows, hla_dtype dt, int half, bool gather,
