@@ -979,7 +979,7 @@ struct Fwd2 {
     // Scan, step 2 (ts_bh is cleared: pass 2 moves TS on): the pass-2 start state TS = S_pre(k), TX = X_pre(k), Yrun = Y_pre(k);
     // for a sequence's last piece with state_out also Y_end = Y_pre + Y_k + S_pre m_k
     // (in state_out.h until the export replaces it by h).
-    __device__ void ah_setup_pass2(int k, bool last, bool want_out, uint32_t &aux_ph) {
+    __device__ void ah_setup_pass2(int k, bool last, bool want_out, uint32_t &aux_ph, bool atilde, uint32_t &ph) {
         const bool sin = P.sin.S != nullptr;
         const int row = srow(), cv = shc<DV>();
         constexpr int NV = shr<DV>();
@@ -1005,6 +1005,7 @@ struct Fwd2 {
             ah_sync();
             if (part == 1) t_sp_tile();
         }
+        if (atilde && part == 0) e_atilde(ph);  // the first pass-2 chunk's A-tilde (E warps)
         if (last && want_out) {  // C_end = C_in + sum_{r<=k} C_r, m_end likewise -> state_out
             float *Co = P.sout.C + ((size_t)bh * D + row) * DV;
 #pragma unroll
@@ -1292,14 +1293,13 @@ __global__ void __launch_bounds__(kThreads, Lay<DV, NORM>::CTAS) fwd_ws2_kernel(
             x.ah_sync();
             x.ah_store_summary(P.summ + ((size_t)bh * P.kmax + pc.k) * L_::SUM);
             x.ah_sync();
-            if (x.ah == 0 && !pc.last) {
+            if (x.ah == 128 && !pc.last) {  // (a T thread: the release waits for the stores to drain)
                 unsigned *f = P.flagA + (size_t)bh * P.kmax + pc.k;
                 asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(x.tag) : "memory");
             }
             last_p1 = bh;
         }
-        if (isE) x.e_atilde(ph);  // the first pass-2 chunk's A-tilde, while the scan waits
-        bool atilde_done = isE;
+        bool atilde_done = isE;  // packed in the first setup, while T hands over S_p
         for (int bh = bh_lo; bh <= bh_hi; ++bh) {
             const Piece pc = piece(bh);
             if (pc.last) continue;
@@ -1309,7 +1309,7 @@ __global__ void __launch_bounds__(kThreads, Lay<DV, NORM>::CTAS) fwd_ws2_kernel(
         for (int bh = bh_lo; bh <= bh_hi; ++bh) {
             const Piece pc = piece(bh);
             select(bh);
-            x.ah_setup_pass2(pc.k, pc.last, want_out, aux_ph);
+            x.ah_setup_pass2(pc.k, pc.last, want_out, aux_ph, atilde_done, ph);
             for (int j = pc.jb; j < pc.je; ++j) {
                 const int L = min(CT, P.n - j * CT);
                 if (isE) x.e_pass2(it, j, L, ph, gt, atilde_done);
