@@ -140,6 +140,17 @@ def test_backward_tensor_core_short_sequences(n):
     check(run_backward(x, g, "bf16", 64), run_oracle(x, g), TOL_BF16, f"bwd tc n{n}")
 
 
+@pytest.mark.parametrize("n", [1, 5, 64, 65])
+@pytest.mark.parametrize("Hkv", [2, 1])
+def test_backward_normalised_tensor_core_short_sequences(n, Hkv):
+    """The tensor-core normalised backward on sequences of one partial chunk, one full chunk
+    and a chunk plus one token (the TMA tiles past the sequence read as zeros)."""
+    w = small(n=n, d=64, dv=64, chunk=64, decay=True, dtype="bf16", qk="elu1", Hkv=Hkv, seed=39)
+    x = W.make_inputs(w)
+    g = W.make_dout(w)
+    check(run_backward(x, g, "bf16", 64, eps=1e-3), run_oracle(x, g, eps=1e-3), TOL_BF16, f"bwd norm tc n{n} Hkv{Hkv}")
+
+
 @pytest.mark.parametrize("d,dv,chunk,dtype", [(64, 64, 64, "bf16"), (32, 16, 32, "f32")])
 @pytest.mark.parametrize("Hkv", [1, 2])
 def test_backward_shared_kv_heads(d, dv, chunk, dtype, Hkv):
