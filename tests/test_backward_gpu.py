@@ -140,11 +140,13 @@ def test_backward_tensor_core_short_sequences(n):
     check(run_backward(x, g, "bf16", 64), run_oracle(x, g), TOL_BF16, f"bwd tc n{n}")
 
 
-@pytest.mark.parametrize("n", [1, 5, 64, 65])
+@pytest.mark.parametrize("n", [2, 5, 64, 65])
 @pytest.mark.parametrize("Hkv", [2, 1])
 def test_backward_normalised_tensor_core_short_sequences(n, Hkv):
     """The tensor-core normalised backward on sequences of one partial chunk, one full chunk
-    and a chunk plus one token (the TMA tiles past the sequence read as zeros)."""
+    and a chunk plus one token (the TMA tiles past the sequence read as zeros).  Not n = 1:
+    a single token's normalised output is its own value up to eps, so dq and dk are
+    O(eps) remainders of O(1) parts and no relative bound applies to them."""
     w = small(n=n, d=64, dv=64, chunk=64, decay=True, dtype="bf16", qk="elu1", Hkv=Hkv, seed=39)
     x = W.make_inputs(w)
     g = W.make_dout(w)
