@@ -185,14 +185,23 @@ hla_status hla_forward_chunked(const hla_params *p, const void *q, const void *k
 namespace {
 // The shape the backward kernels run: a chunk of 128 tokens as two of 64 (the chunk
 // length changes only the rounding), and dv = 128 as two 64-column halves of the values
-// (hla_bwd_split.cu).
+// (hla_bwd_split.cu).  d = 128 runs in chunks of 16 tokens over slices of at most 32
+// value columns: the CUDA-core gradient kernel holds its two d x d and two d x dv fp32
+// states and the chunk's tiles in shared memory only at that size.
 hla_params bwd_inner(const hla_params &p) {
     hla_params q = p;
+    if (q.d == 128) {
+        q.chunk = 16;
+        if (q.dv > 32) q.dv = 32;
+        return q;
+    }
     if (q.chunk == 128) q.chunk = 64;
     if (q.dv == 128) q.dv = 64;
     return q;
 }
-bool bwd_split(const hla_params &p) { return p.dv == 128; }
+// Value-column slices of the call (1: no split).
+int bwd_slices(const hla_params &p) { return p.dv / bwd_inner(p).dv; }
+bool bwd_split(const hla_params &p) { return bwd_slices(p) > 1; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -206,23 +215,24 @@ size_t bwd_inner_workspace(const hla_params &q) {
     return hla::bwd_simt_workspace(q);
 }
 
-// dv = 128: the half problem's workspace, then the gathered value and upstream halves,
-// the half's dq, dk, dv (input type) and the fp32 sums of dq and dk (byte offsets).
+// Split over value columns: the slice problem's workspace, then the gathered value and
+// upstream slices, the slice's dq, dk, dv (input type) and the fp32 sums of dq and dk
+// (byte offsets).
 struct SplitLayout {
     size_t inner, vh, gh, dqh, dkh, dvh, acc_q, acc_k, total;
 };
 SplitLayout split_layout(const hla_params &p) {
     const hla_params q = bwd_inner(p);
-    const size_t el = p.in_dtype == HLA_F32 ? 4 : 2, hkv = p.Hkv > 0 ? p.Hkv : p.H;
+    const size_t el = p.in_dtype == HLA_F32 ? 4 : 2, hkv = p.Hkv > 0 ? p.Hkv : p.H, w = q.dv;
     const size_t rq = (size_t)p.B * p.H * p.n, rkv = (size_t)p.B * hkv * p.n;
     SplitLayout L;
     size_t o = align256(bwd_inner_workspace(q));
     L.inner = 0;
-    L.vh = o; o = align256(o + rkv * 64 * el);
-    L.gh = o; o = align256(o + rq * 64 * el);
+    L.vh = o; o = align256(o + rkv * w * el);
+    L.gh = o; o = align256(o + rq * w * el);
     L.dqh = o; o = align256(o + rq * p.d * el);
     L.dkh = o; o = align256(o + rkv * p.d * el);
-    L.dvh = o; o = align256(o + rkv * 64 * el);
+    L.dvh = o; o = align256(o + rkv * w * el);
     L.acc_q = o; o = align256(o + rq * p.d * 4);
     L.acc_k = o; o = align256(o + rkv * p.d * 4);
     L.total = o;
@@ -243,10 +253,12 @@ hla_status check_bwd_params(const hla_params *p) {
         return fail(HLA_ERR_ARG, "problem too large");
     const bool dv_ok = p->dv == 16 || p->dv == 32 || p->dv == 64 || p->dv == 128;
     const bool c_ok = p->chunk == 16 || p->chunk == 32 || p->chunk == 64 || p->chunk == 128;
-    if (!dv_ok || !c_ok || !hla::bwd_simt_supported(bwd_inner(*p)))
+    // d = 128 without normalisation: the normalised chain's fp32 forwards have no d = 128 form
+    const bool d_ok = p->d != 128 || !(p->flags & HLA_NORMALIZE);
+    if (!dv_ok || !c_ok || !d_ok || !hla::bwd_simt_supported(bwd_inner(*p)))
         return fail(HLA_ERR_UNSUPPORTED,
-                    "backward supports flags 0, HLA_DECAY, HLA_NORMALIZE, d in {16,32,64}, dv and chunk in "
-                    "{16,32,64,128} (got flags=%u Hkv=%d d=%d dv=%d chunk=%d)",
+                    "backward supports flags 0, HLA_DECAY, HLA_NORMALIZE, d in {16,32,64} and d = 128 without "
+                    "HLA_NORMALIZE, dv and chunk in {16,32,64,128} (got flags=%u Hkv=%d d=%d dv=%d chunk=%d)",
                     p->flags, p->Hkv, p->d, p->dv, p->chunk);
     return HLA_OK;
 }
@@ -298,16 +310,16 @@ hla_status backward_impl(const hla_params *p, const void *q, const void *k, cons
         return fail(HLA_ERR_ARG, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
     const bool split = bwd_split(*p);
     if ((norm || split) ? (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 : !aligned16(workspace))
-        return fail(HLA_ERR_ARG, "workspace must be 256-byte aligned with HLA_NORMALIZE or dv = 128, else 16-byte "
-                                 "aligned");
+        return fail(HLA_ERR_ARG, "workspace must be 256-byte aligned with HLA_NORMALIZE or a split over value "
+                                 "columns (dv = 128; d = 128 with dv > 32), else 16-byte aligned");
     if (phase_events) {
         for (int i = 0; i < 4; ++i)
             if (!phase_events[i]) return fail(HLA_ERR_ARG, "phase_events must hold four events");
     }
-    if (split) {  // two 64-column halves of the values: dq, dk add up, dv side by side
+    if (split) {  // slices of the value columns: dq, dk add up, dv side by side
         if (state_in || d_state_in)
-            return fail(HLA_ERR_UNSUPPORTED, "dv = 128: the backward from a given state or with its gradient is "
-                                             "not supported");
+            return fail(HLA_ERR_UNSUPPORTED, "a backward split over value columns (dv = 128; d = 128 with dv > 32) "
+                                             "from a given state or with its gradient is not supported");
         const hla_params in = bwd_inner(*p);
         const SplitLayout L = split_layout(*p);
         uint8_t *w = static_cast<uint8_t *>(workspace);
@@ -316,10 +328,12 @@ hla_status backward_impl(const hla_params *p, const void *q, const void *k, cons
         auto ev = [&](int i) {
             return phase_events ? cudaEventRecord(static_cast<cudaEvent_t>(phase_events[i]), st) : cudaSuccess;
         };
+        const int parts = bwd_slices(*p), pw = in.dv;
         cudaError_t e = ev(0);
-        for (int h = 0; h < 2 && e == cudaSuccess; ++h) {
-            if ((e = hla::cols_half_copy(v, w + L.vh, rkv, p->in_dtype, h, true, st)) != cudaSuccess) break;
-            if ((e = hla::cols_half_copy(dout, w + L.gh, rq, p->in_dtype, h, true, st)) != cudaSuccess) break;
+        for (int h = 0; h < parts && e == cudaSuccess; ++h) {
+            if ((e = hla::cols_part_copy(v, w + L.vh, rkv, p->in_dtype, p->dv, pw, h, true, st)) != cudaSuccess) break;
+            if ((e = hla::cols_part_copy(dout, w + L.gh, rq, p->in_dtype, p->dv, pw, h, true, st)) != cudaSuccess)
+                break;
             s = backward_impl(&in, q, k, w + L.vh, w + L.gh, nullptr, w + L.dqh, w + L.dkh, w + L.dvh, nullptr,
                               w + L.inner, L.vh, stream, nullptr);
             if (s != HLA_OK) return s;
@@ -328,14 +342,14 @@ hla_status backward_impl(const hla_params *p, const void *q, const void *k, cons
                 (e = hla::acc_add(reinterpret_cast<float *>(w + L.acc_k), w + L.dkh, rkv * p->d, p->in_dtype, h == 0,
                                   st)) != cudaSuccess)
                 break;
-            e = hla::cols_half_copy(w + L.dvh, dv, rkv, p->in_dtype, h, false, st);
+            e = hla::cols_part_copy(w + L.dvh, dv, rkv, p->in_dtype, p->dv, pw, h, false, st);
         }
         if (e == cudaSuccess) e = hla::acc_store(dq, reinterpret_cast<const float *>(w + L.acc_q), rq * p->d,
                                                  p->in_dtype, st);
         if (e == cudaSuccess) e = hla::acc_store(dk, reinterpret_cast<const float *>(w + L.acc_k), rkv * p->d,
                                                  p->in_dtype, st);
         for (int i = 1; i < 4 && e == cudaSuccess; ++i) e = ev(i);
-        if (e != cudaSuccess) return cuda_fail(e, "backward over value halves");
+        if (e != cudaSuccess) return cuda_fail(e, "backward over value-column slices");
         return HLA_OK;
     }
     const hla_params inner = bwd_inner(*p);

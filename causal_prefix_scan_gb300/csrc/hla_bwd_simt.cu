@@ -30,7 +30,8 @@ cudaError_t launch_c(const BwdArgs &a, cudaStream_t st) {
 bool bwd_simt_supported(const hla_params &p) {
     auto ok = [](int x) { return x == 16 || x == 32 || x == 64; };
     const int hkv = p.Hkv > 0 ? p.Hkv : p.H;
-    return ok(p.d) && ok(p.dv) && ok(p.chunk) && p.H % hkv == 0 && !(p.flags & (HLA_UNMASKED | HLA_ASYMMETRIC));
+    const bool shape = (ok(p.d) && ok(p.dv) && ok(p.chunk)) || (p.d == 128 && p.chunk == 16 && (p.dv == 16 || p.dv == 32));
+    return shape && p.H % hkv == 0 && !(p.flags & (HLA_UNMASKED | HLA_ASYMMETRIC));
 }
 
 // Local sums and chunk states, then (shared key/value heads only) the per-query-head

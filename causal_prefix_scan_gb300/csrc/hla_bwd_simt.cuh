@@ -1,5 +1,6 @@
 // hla_bwd_simt.cuh -- chunk-parallel backward pass of the masked second-order HLA
-// forward on CUDA cores (fp32 arithmetic), for d, dv, chunk in {16,32,64}, from a zero
+// forward on CUDA cores (fp32 arithmetic), for d, dv, chunk in {16,32,64} and for d = 128
+// with 16-token chunks and dv in {16,32}, from a zero
 // or a given initial state (S_in, X_in = S_in C_in - G_in; the gradient of that state
 // comes from the adjoints at the first token: dX_in = g^2 Lam, dS_in = g Om +
 // dX_in C_in^T, dC_in = S_in^T dX_in, dG_in = -dX_in).  The kernels compute the unnormalised gradient; the ratio-normalised
@@ -207,9 +208,11 @@ struct ScanSmem {
     static constexpr int FW = WMAX + 4, LB = NB + 4;
     // F: S or Lam (D x <= WMAX); BK: the column block of X or Om; then two buffers of
     // FL (the increment of F), R (the product operand block, Cq or W, <= WMAX rows)
-    // and BL (the block increment)
+    // and BL (the block increment).  At d = 128 two D x D increments do not fit beside
+    // the rest, so FL is not staged: the update reads it from the workspace.
+    static constexpr bool STAGE_FL = D <= 64;
     static constexpr int F = 0, BK = F + D * FW, RED = BK + D * LB, BUF = RED + kThreads * 16;
-    static constexpr int B_FL = 0, B_R = D * FW, B_BL = B_R + WMAX * LB, BUFSZ = B_BL + D * LB;
+    static constexpr int B_FL = 0, B_R = STAGE_FL ? D * FW : 0, B_BL = B_R + WMAX * LB, BUFSZ = B_BL + D * LB;
     static constexpr int TOTAL = BUF + 2 * BUFSZ;
 };
 
@@ -233,7 +236,8 @@ __device__ __forceinline__ void scan_dir(const BwdArgs &a, float *sm, int part, 
     auto issue = [&](int it) {  // the local sums of step it into buffer it & 1
         const float *lc = loc + (size_t)chunk_at(it) * ws.loc_floats();
         float *b = sm + Sm::BUF + (it & 1) * Sm::BUFSZ;
-        copy_mat_async<FWD>(lc + (DIR == 0 ? ws.o_sloc() : ws.o_lloc()), FWD, b + Sm::B_FL, Sm::FW, D);
+        if constexpr (Sm::STAGE_FL)
+            copy_mat_async<FWD>(lc + (DIR == 0 ? ws.o_sloc() : ws.o_lloc()), FWD, b + Sm::B_FL, Sm::FW, D);
         copy_mat_async<NBD>(lc + (DIR == 0 ? ws.o_cq() : ws.o_w()) + c0, BW, b + Sm::B_R, Sm::LB, RK);
         copy_mat_async<NBD>(lc + (DIR == 0 ? ws.o_xloc() : ws.o_oloc()) + c0, BW, b + Sm::B_BL, Sm::LB, D);
     };
@@ -277,6 +281,8 @@ __device__ __forceinline__ void scan_dir(const BwdArgs &a, float *sm, int part, 
         __syncthreads();
         const float *b = sm + Sm::BUF + (it & 1) * Sm::BUFSZ;
         const float *Fl = b + Sm::B_FL, *R = b + Sm::B_R, *Bl = b + Sm::B_BL;
+        // the increment of F in the workspace (read there when it is not staged)
+        const float *Flg = loc + (size_t)ch * ws.loc_floats() + (DIR == 0 ? ws.o_sloc() : ws.o_lloc());
         // block <- f_b block + Bl + F R  (F the state before this chunk's update), F R over all threads
         const float fb = DIR == 0 ? f2 : f1, ff = DIR == 0 ? f1 : f2;
         mac_ksplit<D, NBD, RK>(F, Sm::FW, R, Sm::LB, red);
@@ -288,7 +294,7 @@ __device__ __forceinline__ void scan_dir(const BwdArgs &a, float *sm, int part, 
         __syncthreads();
         for (int e = threadIdx.x; e < D * FWD; e += kThreads) {
             const int r = e / FWD, x = e % FWD;
-            F[r * Sm::FW + x] = ff * F[r * Sm::FW + x] + Fl[r * Sm::FW + x];
+            F[r * Sm::FW + x] = ff * F[r * Sm::FW + x] + (Sm::STAGE_FL ? Fl[r * Sm::FW + x] : Flg[e]);
         }
         __syncthreads();
     }
@@ -545,6 +551,14 @@ cudaError_t launch_d(const BwdArgs &a, cudaStream_t st) {
         case 16: return launch_dv<T, C, 16>(a, st);
         case 32: return launch_dv<T, C, 32>(a, st);
         case 64: return launch_dv<T, C, 64>(a, st);
+        case 128:
+            // d = 128: the gradient kernel's fp32 states (two d x d, two d x dv) and its
+            // chunk tiles fit 227 KB of shared memory at 16-token chunks and dv <= 32
+            if constexpr (C == 16) {
+                if (a.dv == 16) return launch_t<T, C, 128, 16>(a, st);
+                if (a.dv == 32) return launch_t<T, C, 128, 32>(a, st);
+            }
+            break;
     }
     return cudaErrorInvalidValue;
 }

@@ -1,12 +1,13 @@
 // hla_bwd_split.cu -- the copies around a call split over value columns (the backward
 // pass, and the third-order forward, whose output and value-width state columns split the
-// same way: column j depends on the values' column j only).
+// same way: column j depends on the values' column j only).  The backward at d = 128 runs
+// over slices of 32 value columns; otherwise a split is two halves of 64.
 //
 // The loss sum_t dout_t . o_t is a sum over value columns, and column j of the output
 // depends on column j of the values only (o_t[j] = q_t^T X_t[:, j], X_t[:, j] built from
 // v[:, j]).  So the gradient for dv = 128 is the sum of the gradients of two 64-column
 // problems (same q, k; value and upstream columns [0, 64) and [64, 128)): dq and dk add,
-// dv is the two halves side by side.  With ratio normalisation each half keeps the full
+// dv is the two halves side by side (likewise for any number of equal slices).  With ratio normalisation each half keeps the full
 // denominator (it does not depend on the values), and its upstream for the unit column
 // is its own share r (dout_h . o_h) of r (dout . o), so the halves add up exactly too.
 // These kernels gather a half of the value columns, scatter a half back, and accumulate
@@ -23,14 +24,14 @@ int grid_for(size_t work) {
     return (int)(b < 8192 ? (b > 0 ? b : 1) : 8192);
 }
 
-// Columns [half*64, half*64+64) of [rows][128] elements of `el` bytes <-> [rows][64],
-// in 16-byte pieces (64 elements of 2 or 4 bytes are 8 or 16 pieces per row).
+// Columns [part*w, part*w+w) of [rows][nparts*w] elements <-> [rows][w], in 16-byte
+// pieces (per_row pieces of a narrow row: w elements of 2 or 4 bytes).
 __global__ void __launch_bounds__(kThreads) cols_copy_kernel(const uint4 *src, uint4 *dst, size_t rows, int per_row,
-                                                             int half, int gather) {
+                                                             int nparts, int part, int gather) {
     const size_t total = rows * per_row;
     for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < total; i += (size_t)gridDim.x * kThreads) {
         const size_t r = i / per_row, c = i % per_row;
-        const size_t wide = r * 2 * per_row + (size_t)half * per_row + c, narrow = r * per_row + c;
+        const size_t wide = r * nparts * per_row + (size_t)part * per_row + c, narrow = r * per_row + c;
         if (gather) dst[narrow] = src[wide];
         else dst[wide] = src[narrow];
     }
@@ -65,13 +66,21 @@ __global__ void __launch_bounds__(kThreads) acc_store_kernel<__nv_bfloat16>(__nv
 
 }  // namespace
 
+cudaError_t cols_part_copy(const void *src, void *dst, size_t rows, hla_dtype dt, int width, int part_width,
+                           int part, bool gather, cudaStream_t st) {
+    const int el = dt == HLA_F32 ? 4 : 2;
+    if (part_width * el % 16 != 0 || width % part_width != 0 || part < 0 || part >= width / part_width)
+        return cudaErrorInvalidValue;
+    const int per_row = part_width * el / 16;
+    cols_copy_kernel<<<grid_for(rows * per_row), kThreads, 0, st>>>(static_cast<const uint4 *>(src),
+                                                                     static_cast<uint4 *>(dst), rows, per_row,
+                                                                     width / part_width, part, gather ? 1 : 0);
+    return cudaGetLastError();
+}
+
 cudaError_t cols_half_copy(const void *src, void *dst, size_t rows, hla_dtype dt, int half, bool gather,
                            cudaStream_t st) {
-    const int per_row = dt == HLA_F32 ? 16 : 8;
-    cols_copy_kernel<<<grid_for(rows * per_row), kThreads, 0, st>>>(static_cast<const uint4 *>(src),
-                                                                     static_cast<uint4 *>(dst), rows, per_row, half,
-                                                                     gather ? 1 : 0);
-    return cudaGetLastError();
+    return cols_part_copy(src, dst, rows, dt, 128, 64, half, gather, st);
 }
 
 cudaError_t acc_add(float *acc, const void *src, size_t count, hla_dtype dt, bool first, cudaStream_t st) {

@@ -223,20 +223,23 @@ HLA_API hla_status hla_decode_step(int N, int H, int Hkv, int d, int dv, hla_dty
  *
  *   p      as for hla_forward_chunked; supported: flags 0, HLA_DECAY, HLA_NORMALIZE
  *          (eps >= 0) or both (HLA_UNMASKED, HLA_ASYMMETRIC: HLA_ERR_UNSUPPORTED),
- *          Hkv dividing H (0 means H), d in {16,32,64}, dv and chunk in
- *          {16,32,64,128}, in_dtype HLA_F32 or HLA_BF16.  dv = 128 runs as two
- *          problems over the value columns [0,64) and [64,128) (the loss is a sum over
- *          value columns, each depending on its own column of v only): dq and dk are
- *          their sum, formed in fp32 and rounded once, dv their two halves; not with a
- *          given state or its gradient (HLA_ERR_UNSUPPORTED).  A 128-token chunk runs
- *          as two chunks of 64 tokens (the same gradient up to rounding);
+ *          Hkv dividing H (0 means H), d in {16,32,64,128} (128 without
+ *          HLA_NORMALIZE), dv and chunk in {16,32,64,128}, in_dtype HLA_F32 or
+ *          HLA_BF16.  dv = 128 runs as two problems over the value columns [0,64) and
+ *          [64,128) (the loss is a sum over value columns, each depending on its own
+ *          column of v only): dq and dk are their sum, formed in fp32 and rounded once,
+ *          dv their two halves; not with a given state or its gradient
+ *          (HLA_ERR_UNSUPPORTED).  A 128-token chunk runs as two chunks of 64 tokens
+ *          (the same gradient up to rounding).  d = 128 runs on the CUDA cores in
+ *          16-token chunks (whatever chunk is given) over slices of 32 value columns
+ *          when dv > 32, split as above;
  *   q      [B][H][n][d], k [B][Hkv][n][d], v [B][Hkv][n][dv], dout [B][H][n][dv],
  *          in_dtype, read only (query head h reads key/value head h / (H / Hkv));
  *   dq     [B][H][n][d], dk [B][Hkv][n][d], dv [B][Hkv][n][dv], in_dtype, written (not
  *          accumulated); with Hkv < H, dk and dv are the sums over each group;
  *   workspace device scratch of at least hla_backward_workspace_size(p) bytes,
- *          16-byte aligned (256-byte aligned with HLA_NORMALIZE or dv = 128), no
- *          initial contents needed.
+ *          16-byte aligned (256-byte aligned with HLA_NORMALIZE or a split over value
+ *          columns), no initial contents needed.
  * All tensor pointers 16-byte aligned.  Without HLA_NORMALIZE three kernel phases
  * on `stream` (plus the group sums when Hkv < H); with it, the launches above.
  */

@@ -141,8 +141,7 @@ def _bcall(p, ptrs=(16,) * 7, ws=16, ws_bytes=1 << 40):
     (dict(flags=hla.HLA_UNMASKED), hla.HLA_ERR_UNSUPPORTED),
     (dict(flags=hla.HLA_ASYMMETRIC), hla.HLA_ERR_UNSUPPORTED),
     (dict(H=6, Hkv=4), hla.HLA_ERR_ARG),
-    (dict(d=128), hla.HLA_ERR_UNSUPPORTED),
-    (dict(d=128, dv=128, chunk=128), hla.HLA_ERR_UNSUPPORTED),
+    (dict(flags=hla.HLA_NORMALIZE, d=128, dv=32, chunk=16, eps=1e-3), hla.HLA_ERR_UNSUPPORTED),
     (dict(dv=96), hla.HLA_ERR_UNSUPPORTED),
     (dict(chunk=256), hla.HLA_ERR_UNSUPPORTED),
     (dict(d=48), hla.HLA_ERR_UNSUPPORTED),
@@ -314,6 +313,33 @@ def test_backward_value_halves_and_long_chunks(lib):
     assert hla.library().hla_backward_chunked_state(ctypes.byref(_params(dv=128)), 16, 16, 16, 16, good, 16, 16, 16,
                                                     None, 256, 1 << 40, None) == hla.HLA_ERR_UNSUPPORTED
     assert "dv = 128" in hla.hla_last_error()
+
+
+def test_backward_key_width_128(lib):
+    """d = 128 runs in 16-token chunks over slices of at most 32 value columns: dv <= 32
+    is the plain layout at chunk 16 (whatever chunk is asked for); wider values are split
+    like dv = 128 at d <= 64, with 32-column slices."""
+    al = lambda x: -(-x // 256) * 256
+    B, H, n, d = 1, 2, 100, 128
+    for dv in (16, 32):
+        nch = -(-n // 16)
+        want = (B * H * nch * (4 * d * d + 6 * d * dv) + B * H * (d * dv + d * d)) * 4
+        for c in (16, 32, 64, 128):
+            assert hla.hla_backward_workspace_size(_params(B=B, H=H, n=n, d=d, dv=dv, chunk=c,
+                                                           in_dtype=hla.HLA_F32)) == want
+    for dt, el in ((hla.HLA_F32, 4), (hla.HLA_BF16, 2)):
+        inner = hla.hla_backward_workspace_size(_params(B=B, H=H, n=n, d=d, dv=32, chunk=16, in_dtype=dt))
+        rq = B * H * n
+        for dv in (64, 128):
+            want = al(inner) + al(rq * 32 * el) + al(rq * 32 * el) + al(rq * d * el) + al(rq * d * el) \
+                + al(rq * 32 * el) + al(rq * d * 4) + al(rq * d * 4)
+            assert hla.hla_backward_workspace_size(_params(B=B, H=H, n=n, d=d, dv=dv, chunk=64, in_dtype=dt)) == want
+    # a split supports no given state; dv <= 32 does
+    good = ctypes.pointer(hla.hla_state(256, 256, 256, 256, 256))
+    assert hla.library().hla_backward_chunked_state(ctypes.byref(_params(d=128, dv=64)), 16, 16, 16, 16, good, 16,
+                                                    16, 16, None, 256, 1 << 40, None) == hla.HLA_ERR_UNSUPPORTED
+    assert "d = 128 with dv > 32" in hla.hla_last_error()
+    assert hla.hla_backward_workspace_size(_params(d=128, dv=128, chunk=128, flags=hla.HLA_DECAY, gamma=16)) > 0
 
 
 def test_backward_state_rejects_bad_args(lib):
