@@ -73,7 +73,7 @@ hla_status check_params(const hla_params *p) {
         return fail(HLA_ERR_UNSUPPORTED, "unsupported shape: dtype=%d d=%d dv=%d chunk=%d", (int)p->in_dtype, p->d,
                     p->dv, p->chunk);
     if (p->in_dtype == HLA_F32 && !hla::fwd_simt_supported(*p))
-        return fail(HLA_ERR_UNSUPPORTED, "fp32 inputs need d, dv, chunk in {16,32,64}");
+        return fail(HLA_ERR_UNSUPPORTED, "fp32 inputs need d, dv, chunk in {16,32,64,128} (d, dv <= 64 for the unmasked and asymmetric variants)");
     return HLA_OK;
 }
 
@@ -253,12 +253,10 @@ hla_status check_bwd_params(const hla_params *p) {
         return fail(HLA_ERR_ARG, "problem too large");
     const bool dv_ok = p->dv == 16 || p->dv == 32 || p->dv == 64 || p->dv == 128;
     const bool c_ok = p->chunk == 16 || p->chunk == 32 || p->chunk == 64 || p->chunk == 128;
-    // d = 128 without normalisation: the normalised chain's fp32 forwards have no d = 128 form
-    const bool d_ok = p->d != 128 || !(p->flags & HLA_NORMALIZE);
-    if (!dv_ok || !c_ok || !d_ok || !hla::bwd_simt_supported(bwd_inner(*p)))
+    if (!dv_ok || !c_ok || !hla::bwd_simt_supported(bwd_inner(*p)))
         return fail(HLA_ERR_UNSUPPORTED,
-                    "backward supports flags 0, HLA_DECAY, HLA_NORMALIZE, d in {16,32,64} and d = 128 without "
-                    "HLA_NORMALIZE, dv and chunk in {16,32,64,128} (got flags=%u Hkv=%d d=%d dv=%d chunk=%d)",
+                    "backward supports flags 0, HLA_DECAY, HLA_NORMALIZE, d in {16,32,64,128}, dv and chunk in "
+                    "{16,32,64,128} (got flags=%u Hkv=%d d=%d dv=%d chunk=%d)",
                     p->flags, p->Hkv, p->d, p->dv, p->chunk);
     return HLA_OK;
 }

@@ -86,12 +86,14 @@ __global__ void __launch_bounds__(kEwThreads) norm_upstream_kernel(const float *
 // Item i = sequence * P + s.  CTA (sequence, row block) writes rows [r0, r0 + kScanRows)
 // of every state; each keeps its own copy of the whole prefix C and m (the right
 // factor of the cross terms) in shared memory.
-constexpr int kScanMaxD = 64, kScanRows = 16;
+// Capacity: d <= 128 and d * dv <= 4096 (d <= 64 with dv <= 64; d = 128 runs over value
+// slices of at most 32 columns).
+constexpr int kScanMaxD = 128, kScanMaxC = 4096, kScanRows = 16;
 // init: the state before the first segment of every sequence (init.S NULL: zeros).
 __global__ void __launch_bounds__(kEwThreads) segment_scan_kernel(StatePtrs seg, StatePtrs pre, StatePtrs init, int P,
                                                                    int d, int dv, int H, const float *gamma,
                                                                    int seg_len) {
-    __shared__ float sb[kScanRows * kScanMaxD], ca[kScanMaxD * kScanMaxD], ma[kScanMaxD];
+    __shared__ float sb[kScanRows * kScanMaxD], ca[kScanMaxC], ma[kScanMaxD];
     const int seq = blockIdx.x, r0 = blockIdx.y * kScanRows, tid = threadIdx.x;
     const size_t nS = (size_t)d * d, nC = (size_t)d * dv;
     const float f = gamma ? exp2f(log2f(gamma[seq % H]) * (float)seg_len) : 1.f, f2 = f * f;
@@ -341,6 +343,8 @@ hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a0, void *workspa
             if (s != HLA_OK) return s;
             StatePtrs init{};
             if (given) init = to_ptrs(part == 0 ? &sv : &se);
+            if (p.d > kScanMaxD || (size_t)p.d * dvp > (size_t)kScanMaxC)
+                return hla::report(HLA_ERR_UNSUPPORTED, "normalised backward: state too wide for the segment scan");
             segment_scan_kernel<<<dim3(p.B * p.H, p.d / kScanRows), kEwThreads, 0, st>>>(
                 to_ptrs(&sg), to_ptrs(&pr), init, P, p.d, dvp, p.H, (p.flags & HLA_DECAY) ? p.gamma : nullptr, p.n / P);
             if ((e = cudaGetLastError()) != cudaSuccess) return cuda_err(e, "segment scan");

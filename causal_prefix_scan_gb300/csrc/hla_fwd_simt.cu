@@ -1,5 +1,6 @@
 // hla_fwd_simt.cu -- chunked masked second-order HLA forward on CUDA cores, fp32
-// arithmetic, for fp32 inputs and for widths d, dv <= 64 (any input dtype).
+// arithmetic, for fp32 inputs and for widths the tensor-core kernels do not take (any
+// input dtype): d, dv in {16,32,64,128} (128 for the masked variant only).
 //
 // One CTA per (b,h) pair walks the chunks in order, keeping the pair's state on
 // chip.  Instead of G and h it carries X = S C - G (d x dv) and Y = S m - h (d),
@@ -322,16 +323,29 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
 // (leading dimensions = width + 4 floats, so that row-wise float4 reads of different
 // rows fall in different banks).  Products whose right operand is read transposed
 // (Q K^T, Q U^T) use column-strided tiles for the same reason.
-template <int D, int DV>
+// MC: the longest chunk the layout holds.  The pair's state (S, X, C: d x d and two
+// d x dv fp32 arrays) stays in shared memory, so wide states leave room for shorter
+// chunks only: a longer chunk runs as several of MC tokens (the chunk length changes
+// only the rounding).
+template <int D, int DV, int MC>
 struct TiledLayout {
-    static constexpr int LD = D + 4, LV = DV + 4, LC = kMaxChunk + 4;
+    static constexpr int LD = D + 4, LV = DV + 4, LC = MC + 4;
     static constexpr int S = 0, X = S + D * LD, Cs = X + D * LV, m = Cs + D * LV, Y = m + D;
-    static constexpr int Q = Y + D, K = Q + kMaxChunk * LD, U = K + kMaxChunk * LD, V = U + kMaxChunk * LD;
-    static constexpr int A = V + kMaxChunk * LV, gp = A + kMaxChunk * LC;
-    static constexpr int w1 = gp + 2 * kMaxChunk + 4, w2 = w1 + kMaxChunk, rden = w2 + kMaxChunk;
-    static constexpr int floats = rden + kMaxChunk;
+    static constexpr int Q = Y + D, K = Q + MC * LD, U = K + MC * LD, V = U + MC * LD;
+    static constexpr int A = V + MC * LV, gp = A + MC * LC;
+    static constexpr int w1 = gp + 2 * MC + 4, w2 = w1 + MC, rden = w2 + MC;
+    static constexpr int floats = rden + MC;
     static_assert(D % 4 == 0 && DV % 4 == 0 && X % 4 == 0 && Q % 4 == 0 && V % 4 == 0 && A % 4 == 0, "alignment");
 };
+constexpr int kSmemFloats = 227 * 1024 / 4;
+template <int D, int DV>
+constexpr int tiled_max_chunk() {
+    return TiledLayout<D, DV, 64>::floats <= kSmemFloats   ? 64
+           : TiledLayout<D, DV, 32>::floats <= kSmemFloats ? 32
+           : TiledLayout<D, DV, 16>::floats <= kSmemFloats ? 16
+                                                           : 8;
+}
+static_assert(TiledLayout<128, 128, tiled_max_chunk<128, 128>()>::floats <= kSmemFloats, "d = dv = 128 layout");
 
 template <class Body>
 __device__ __forceinline__ void tiles_rt(int M, int N, bool strided, Body body) {
@@ -344,9 +358,9 @@ __device__ __forceinline__ void tiles_rt(int M, int N, bool strided, Body body) 
     }
 }
 
-template <typename T, int D, int DV>
+template <typename T, int D, int DV, int MC>
 __global__ void __launch_bounds__(kThreads) fwd_simt_tiled_kernel(FwdArgs a) {
-    using Lt = TiledLayout<D, DV>;
+    using Lt = TiledLayout<D, DV, MC>;
     constexpr int LD = Lt::LD, LV = Lt::LV, LC = Lt::LC;
     extern __shared__ __align__(16) float sm[];
     float *S = sm + Lt::S, *X = sm + Lt::X, *Cs = sm + Lt::Cs, *m = sm + Lt::m, *Y = sm + Lt::Y;
@@ -499,17 +513,12 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_tiled_kernel(FwdArgs a) {
     }
 }
 
+// The unmasked and asymmetric variants (d, dv <= 64; chunks of at most kMaxChunk tokens).
 template <typename T, int D, int DV>
-cudaError_t launch_t(const FwdArgs &a, cudaStream_t st) {
-    if (!(a.flags & (HLA_UNMASKED | HLA_ASYMMETRIC))) {
-        const size_t bytes = (size_t)TiledLayout<D, DV>::floats * sizeof(float);
-        auto kern = fwd_simt_tiled_kernel<T, D, DV>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        if (e != cudaSuccess) return e;
-        kern<<<a.B * a.H, kThreads, bytes, st>>>(a);
-        return cudaGetLastError();
-    }
+cudaError_t launch_general(const FwdArgs &a0, cudaStream_t st) {
     constexpr int DU = D > DV ? D : DV;
+    FwdArgs a = a0;
+    if (a.chunk > kMaxChunk) a.chunk = kMaxChunk;
     const size_t floats = (size_t)D * D + 2 * (size_t)D * DV + 2 * D + (size_t)kMaxChunk * (2 * D + DV + DU) +
                           (size_t)kMaxChunk * kMaxChunk + kMaxChunk + 2 * kMaxChunk + 2;
     const size_t bytes = floats * sizeof(float);
@@ -520,12 +529,33 @@ cudaError_t launch_t(const FwdArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+template <typename T, int D, int DV>
+cudaError_t launch_t(const FwdArgs &a0, cudaStream_t st) {
+    if (!(a0.flags & (HLA_UNMASKED | HLA_ASYMMETRIC))) {
+        constexpr int MC = tiled_max_chunk<D, DV>();
+        FwdArgs a = a0;
+        if (a.chunk > MC) a.chunk = MC;
+        const size_t bytes = (size_t)TiledLayout<D, DV, MC>::floats * sizeof(float);
+        auto kern = fwd_simt_tiled_kernel<T, D, DV, MC>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e != cudaSuccess) return e;
+        kern<<<a.B * a.H, kThreads, bytes, st>>>(a);
+        return cudaGetLastError();
+    }
+    if constexpr (D > 64 || DV > 64) {  // the unmasked and asymmetric kernel holds d, dv <= 64
+        return cudaErrorInvalidValue;
+    } else {
+        return launch_general<T, D, DV>(a0, st);
+    }
+}
+
 template <typename T, int D>
 cudaError_t launch_dv(const FwdArgs &a, cudaStream_t st) {
     switch (a.dv) {
         case 16: return launch_t<T, D, 16>(a, st);
         case 32: return launch_t<T, D, 32>(a, st);
         case 64: return launch_t<T, D, 64>(a, st);
+        case 128: return launch_t<T, D, 128>(a, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -536,6 +566,7 @@ cudaError_t launch_d(const FwdArgs &a, cudaStream_t st) {
         case 16: return launch_dv<T, 16>(a, st);
         case 32: return launch_dv<T, 32>(a, st);
         case 64: return launch_dv<T, 64>(a, st);
+        case 128: return launch_dv<T, 128>(a, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -544,7 +575,10 @@ cudaError_t launch_d(const FwdArgs &a, cudaStream_t st) {
 
 bool fwd_simt_supported(const hla_params &p) {
     auto ok = [](int x) { return x == 16 || x == 32 || x == 64; };
-    return ok(p.d) && ok(p.dv) && ok(p.chunk) && p.chunk <= kMaxChunk;
+    auto wide = [&](int x) { return ok(x) || x == 128; };
+    // the masked variant at every width; the unmasked and asymmetric ones at d, dv <= 64
+    const bool general = (p.flags & (HLA_UNMASKED | HLA_ASYMMETRIC)) != 0;
+    return (general ? ok(p.d) && ok(p.dv) : wide(p.d) && wide(p.dv)) && wide(p.chunk);
 }
 
 cudaError_t fwd_simt_launch(const FwdArgs &a, cudaStream_t st) {

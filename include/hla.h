@@ -115,8 +115,12 @@ typedef struct {
  *   in_dtype HLA_BF16, d in {64,128}, dv in {64,128}, chunk in {64,128}:
  *       tensor-core path (tcgen05 MMA, TMEM accumulators, TMA tile loads);
  *       with HLA_ASYMMETRIC only dv <= d.
- *   in_dtype HLA_F32 or HLA_BF16 with d, dv in {16,32,64} and chunk in
- *       {16,32,64}: CUDA-core fp32 path (fp32 inputs keep full precision).
+ *   in_dtype HLA_F32 or HLA_BF16 with d, dv, chunk in {16,32,64,128} (d, dv in
+ *       {16,32,64} for HLA_UNMASKED and HLA_ASYMMETRIC), the shapes above excepted:
+ *       CUDA-core fp32 path (fp32 inputs keep full precision).  One CTA per pair
+ *       holds the pair's state in shared memory; where that leaves too little room,
+ *       a chunk runs as several shorter ones (64 tokens at most; 32 at d = 128 with
+ *       dv = 32 or 64, 8 at d = dv = 128), which changes only the rounding.
  *   Anything else: HLA_ERR_UNSUPPORTED.  Any n >= 0; a final partial chunk is
  *   handled exactly (decay is applied only over the tokens present).
  */
@@ -223,9 +227,8 @@ HLA_API hla_status hla_decode_step(int N, int H, int Hkv, int d, int dv, hla_dty
  *
  *   p      as for hla_forward_chunked; supported: flags 0, HLA_DECAY, HLA_NORMALIZE
  *          (eps >= 0) or both (HLA_UNMASKED, HLA_ASYMMETRIC: HLA_ERR_UNSUPPORTED),
- *          Hkv dividing H (0 means H), d in {16,32,64,128} (128 without
- *          HLA_NORMALIZE), dv and chunk in {16,32,64,128}, in_dtype HLA_F32 or
- *          HLA_BF16.  dv = 128 runs as two problems over the value columns [0,64) and
+ *          Hkv dividing H (0 means H), d, dv and chunk in {16,32,64,128}, in_dtype
+ *          HLA_F32 or HLA_BF16.  dv = 128 runs as two problems over the value columns [0,64) and
  *          [64,128) (the loss is a sum over value columns, each depending on its own
  *          column of v only): dq and dk are their sum, formed in fp32 and rounded once,
  *          dv their two halves; not with a given state or its gradient

@@ -70,7 +70,8 @@ def _call(p, q=16, k=16, v=16, o=16, sin=None, sout=None, ws=None, ws_bytes=0):
     (dict(flags=hla.HLA_NORMALIZE, eps=-1.0), hla.HLA_ERR_ARG),
     (dict(d=48), hla.HLA_ERR_UNSUPPORTED),
     (dict(chunk=256), hla.HLA_ERR_UNSUPPORTED),
-    (dict(in_dtype=hla.HLA_F32, d=128, dv=128, chunk=128), hla.HLA_ERR_UNSUPPORTED),
+    (dict(in_dtype=hla.HLA_F32, d=128, flags=hla.HLA_UNMASKED), hla.HLA_ERR_UNSUPPORTED),
+    (dict(in_dtype=hla.HLA_F32, dv=96), hla.HLA_ERR_UNSUPPORTED),
 ])
 def test_forward_rejects_bad_params(lib, kw, status):
     assert _call(_params(**kw)) == status
@@ -137,11 +138,9 @@ def _bcall(p, ptrs=(16,) * 7, ws=16, ws_bytes=1 << 40):
     (dict(flags=16), hla.HLA_ERR_ARG),
     (dict(flags=hla.HLA_DECAY), hla.HLA_ERR_ARG),            # decay without gamma
     (dict(flags=hla.HLA_NORMALIZE, eps=-1.0), hla.HLA_ERR_ARG),
-    (dict(flags=hla.HLA_NORMALIZE, d=128), hla.HLA_ERR_UNSUPPORTED),
     (dict(flags=hla.HLA_UNMASKED), hla.HLA_ERR_UNSUPPORTED),
     (dict(flags=hla.HLA_ASYMMETRIC), hla.HLA_ERR_UNSUPPORTED),
     (dict(H=6, Hkv=4), hla.HLA_ERR_ARG),
-    (dict(flags=hla.HLA_NORMALIZE, d=128, dv=32, chunk=16, eps=1e-3), hla.HLA_ERR_UNSUPPORTED),
     (dict(dv=96), hla.HLA_ERR_UNSUPPORTED),
     (dict(chunk=256), hla.HLA_ERR_UNSUPPORTED),
     (dict(d=48), hla.HLA_ERR_UNSUPPORTED),
@@ -340,6 +339,7 @@ def test_backward_key_width_128(lib):
                                                     16, 16, None, 256, 1 << 40, None) == hla.HLA_ERR_UNSUPPORTED
     assert "d = 128 with dv > 32" in hla.hla_last_error()
     assert hla.hla_backward_workspace_size(_params(d=128, dv=128, chunk=128, flags=hla.HLA_DECAY, gamma=16)) > 0
+    assert hla.hla_backward_workspace_size(_params(d=128, dv=128, chunk=64, flags=hla.HLA_NORMALIZE, eps=1e-3)) > 0
 
 
 def test_backward_state_rejects_bad_args(lib):
