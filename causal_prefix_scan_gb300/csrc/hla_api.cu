@@ -411,28 +411,39 @@ namespace {
 // two 64-column halves of the values (the output's column j and the state's P, T, M^QP
 // columns j depend on the values' column j only; S^K, S^Q, M^KQ and the unit column's
 // m, h, mqm on none), each half written into its columns (hla_bwd_split.cu copies).
+// d = 128 runs in 16-token chunks over slices of at most 32 value columns: the CUDA-core
+// output kernel holds S^K_p (128 x 128 fp32) beside P_p, T_p and the chunk's tiles only
+// at that size.
 hla_params fwd3_inner(const hla_params &p) {
     hla_params q = p;
+    if (q.d == 128) {
+        q.chunk = 16;
+        if (q.dv > 32) q.dv = 32;
+        return q;
+    }
     if (q.chunk == 128) q.chunk = 64;
     if (q.dv == 128) q.dv = 64;
     return q;
 }
+// Value-column slices of the call (1: no split).
+int fwd3_slices(const hla_params &p) { return p.dv / fwd3_inner(p).dv; }
 
-// dv = 128: the half problem's workspace, the gathered value half, the output half, and
-// the value-column halves (P, T, M^QP, fp32) of state_in and of state_out (byte offsets).
+// Split over value columns: the slice problem's workspace, the gathered value slice, the
+// output slice, and the value-column slices (P, T, M^QP, fp32) of state_in and of
+// state_out (byte offsets).
 struct Split3 {
     size_t vh, oh, sin, sout, total;
 };
 Split3 split3_layout(const hla_params &p) {
     const hla_params q = fwd3_inner(p);
-    const size_t el = p.in_dtype == HLA_F32 ? 4 : 2, rows = (size_t)p.B * p.H * p.n;
-    const size_t half_state = (size_t)p.B * p.H * p.d * 64 * 4;
+    const size_t el = p.in_dtype == HLA_F32 ? 4 : 2, rows = (size_t)p.B * p.H * p.n, w = q.dv;
+    const size_t slice_state = (size_t)p.B * p.H * p.d * w * 4;
     Split3 L;
     size_t o = align256(hla::fwd3_workspace(q));
-    L.vh = o; o = align256(o + rows * 64 * el);
-    L.oh = o; o = align256(o + rows * 64 * el);
-    L.sin = o; o = align256(o + 3 * half_state);
-    L.sout = o; o = align256(o + 3 * half_state);
+    L.vh = o; o = align256(o + rows * w * el);
+    L.oh = o; o = align256(o + rows * w * el);
+    L.sin = o; o = align256(o + 3 * slice_state);
+    L.sout = o; o = align256(o + 3 * slice_state);
     L.total = o;
     return L;
 }
@@ -455,8 +466,8 @@ hla_status check_fwd3_params(const hla_params *p) {
     const bool c_ok = p->chunk == 16 || p->chunk == 32 || p->chunk == 64 || p->chunk == 128;
     if (!dv_ok || !c_ok || !hla::fwd3_supported(fwd3_inner(*p)))
         return fail(HLA_ERR_UNSUPPORTED,
-                    "third order supports flags HLA_DECAY, HLA_NORMALIZE, Hkv = H, d in {16,32,64}, dv and chunk "
-                    "in {16,32,64,128} (got flags=%u Hkv=%d d=%d dv=%d chunk=%d)",
+                    "third order supports flags HLA_DECAY, HLA_NORMALIZE, Hkv = H, d, dv and chunk in "
+                    "{16,32,64,128} (got flags=%u Hkv=%d d=%d dv=%d chunk=%d)",
                     p->flags, p->Hkv, p->d, p->dv, p->chunk);
     if ((p->flags & HLA_NORMALIZE) && !(p->eps >= 0.f)) return fail(HLA_ERR_ARG, "need eps >= 0");
     if ((p->flags & HLA_DECAY) && !p->gamma) return fail(HLA_ERR_ARG, "HLA_DECAY needs gamma");
@@ -477,7 +488,7 @@ hla_status check_state3(const hla_state3 *s, const char *name, bool normalize, b
 
 size_t hla_forward3_workspace_size(const hla_params *p) {
     if (check_fwd3_params(p) != HLA_OK) return 0;
-    if (p->dv == 128) return split3_layout(*p).total;
+    if (fwd3_slices(*p) > 1) return split3_layout(*p).total;
     return hla::fwd3_workspace(fwd3_inner(*p));
 }
 
@@ -537,26 +548,29 @@ hla_status forward3_impl(const hla_params *p, const void *q, const void *k, cons
     if (!workspace || workspace_bytes < need)
         return fail(HLA_ERR_ARG, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
     if (!aligned16(workspace)) return fail(HLA_ERR_ARG, "workspace must be 16-byte aligned");
-    const bool split = p->dv == 128;
+    const bool split = fwd3_slices(*p) > 1;
     if ((norm || split) && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return fail(HLA_ERR_ARG, "workspace must be 256-byte aligned with HLA_NORMALIZE or dv = 128");
+        return fail(HLA_ERR_ARG, "workspace must be 256-byte aligned with HLA_NORMALIZE or a split over value "
+                                 "columns (dv = 128; d = 128 with dv > 32)");
     if (phase_events) {
         for (int i = 0; i < 4; ++i)
             if (!phase_events[i]) return fail(HLA_ERR_ARG, "phase_events must hold four events");
     }
-    if (split) {  // two 64-column halves of the values, each written into its columns
+    if (split) {  // slices of the value columns, each written into its columns
         const hla_params in = fwd3_inner(*p);
         const Split3 L = split3_layout(*p);
+        const int parts = fwd3_slices(*p), pw = in.dv;
         uint8_t *w = static_cast<uint8_t *>(workspace);
         const size_t rows = (size_t)p->B * p->H * p->n, srows = (size_t)p->B * p->H * p->d;
-        const size_t hs = srows * 64;  // floats of one half array of the state
+        const size_t hs = srows * pw;  // floats of one slice array of the state
         float *ti = reinterpret_cast<float *>(w + L.sin), *to = reinterpret_cast<float *>(w + L.sout);
         auto ev = [&](int i) {
             return phase_events ? cudaEventRecord(static_cast<cudaEvent_t>(phase_events[i]), st) : cudaSuccess;
         };
         cudaError_t e = ev(0);
-        for (int h = 0; h < 2 && e == cudaSuccess; ++h) {
-            if ((e = hla::cols_half_copy(v, w + L.vh, rows, p->in_dtype, h, true, st)) != cudaSuccess) break;
+        for (int h = 0; h < parts && e == cudaSuccess; ++h) {
+            if ((e = hla::cols_part_copy(v, w + L.vh, rows, p->in_dtype, p->dv, pw, h, true, st)) != cudaSuccess)
+                break;
             hla_state3 si{}, so{};
             if (state_in) {
                 si = *state_in;
@@ -565,7 +579,7 @@ hla_status forward3_impl(const hla_params *p, const void *q, const void *k, cons
                 si.MQP = maps ? ti + 2 * hs : nullptr;
                 const float *src[3] = {state_in->P, state_in->T, state_in->MQP};
                 for (int i = 0; i < (maps ? 3 : 2) && e == cudaSuccess; ++i)
-                    e = hla::cols_half_copy(src[i], ti + i * hs, srows, HLA_F32, h, true, st);
+                    e = hla::cols_part_copy(src[i], ti + i * hs, srows, HLA_F32, p->dv, pw, h, true, st);
                 if (e != cudaSuccess) break;
             }
             if (state_out) {
@@ -577,15 +591,16 @@ hla_status forward3_impl(const hla_params *p, const void *q, const void *k, cons
             s = forward3_impl(&in, q, k, w + L.vh, w + L.oh, state_in ? &si : nullptr, state_out ? &so : nullptr, w,
                               L.vh, stream, nullptr);
             if (s != HLA_OK) return s;
-            if ((e = hla::cols_half_copy(w + L.oh, o, rows, p->in_dtype, h, false, st)) != cudaSuccess) break;
+            if ((e = hla::cols_part_copy(w + L.oh, o, rows, p->in_dtype, p->dv, pw, h, false, st)) != cudaSuccess)
+                break;
             if (state_out) {
                 float *dst[3] = {state_out->P, state_out->T, state_out->MQP};
                 for (int i = 0; i < (maps ? 3 : 2) && e == cudaSuccess; ++i)
-                    e = hla::cols_half_copy(to + i * hs, dst[i], srows, HLA_F32, h, false, st);
+                    e = hla::cols_part_copy(to + i * hs, dst[i], srows, HLA_F32, p->dv, pw, h, false, st);
             }
         }
         for (int i = 1; i < 4 && e == cudaSuccess; ++i) e = ev(i);
-        if (e != cudaSuccess) return cuda_fail(e, "third-order forward over value halves");
+        if (e != cudaSuccess) return cuda_fail(e, "third-order forward over value-column slices");
         return HLA_OK;
     }
     const hla_params inner = fwd3_inner(*p);
@@ -632,9 +647,8 @@ hla_status forward3_impl(const hla_params *p, const void *q, const void *k, cons
 hla_status hla_state3_combine(int count, int d, int dv, unsigned flags, const hla_state3 *A, const hla_state3 *B,
                               const hla_state3 *out, const float *decay_pow, void *stream) {
     if (count < 0) return fail(HLA_ERR_ARG, "need count >= 0");
-    auto ok = [](int x) { return x == 16 || x == 32 || x == 64; };
-    if (!ok(d) || !(ok(dv) || dv == 128))
-        return fail(HLA_ERR_UNSUPPORTED, "d must be in {16,32,64} and dv in {16,32,64,128} (got %d, %d)", d, dv);
+    if (!width_ok(d) || !width_ok(dv))
+        return fail(HLA_ERR_UNSUPPORTED, "d and dv must be in {16,32,64,128} (got %d, %d)", d, dv);
     if (flags & ~(unsigned)HLA_NORMALIZE) return fail(HLA_ERR_UNSUPPORTED, "flags must be 0 or HLA_NORMALIZE");
     if (!A || !B || !out) return fail(HLA_ERR_ARG, "A, B, out must be set");
     const bool norm = (flags & HLA_NORMALIZE) != 0;

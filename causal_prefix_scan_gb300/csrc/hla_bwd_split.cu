@@ -78,11 +78,6 @@ cudaError_t cols_part_copy(const void *src, void *dst, size_t rows, hla_dtype dt
     return cudaGetLastError();
 }
 
-cudaError_t cols_half_copy(const void *src, void *dst, size_t rows, hla_dtype dt, int half, bool gather,
-                           cudaStream_t st) {
-    return cols_part_copy(src, dst, rows, dt, 128, 64, half, gather, st);
-}
-
 cudaError_t acc_add(float *acc, const void *src, size_t count, hla_dtype dt, bool first, cudaStream_t st) {
     if (dt == HLA_F32)
         acc_add_kernel<float><<<grid_for(count), kThreads, 0, st>>>(acc, static_cast<const float *>(src), count, first);

@@ -181,6 +181,120 @@ __global__ void __launch_bounds__(kThreads) combine3_kernel(Comb3 c) {
     }
 }
 
+// d = 128: the four d x d operands of the kernel above (128 x 132 floats each) do not fit
+// one CTA's shared memory beside P_A and M^QP_B, so the concatenation runs in two phases
+// that each stage only what is overwritten while it is read (out may alias A or B).
+// Phase 1 forms P, T, M^QP (and m, h, mqm) with S^Q_B P_A staged, using
+// S^K_A (S^Q_B P_A) for the W P_A term and S^K_A (S^Q_B m_A) for W m_A; the d x d operands
+// stay in global memory, which phase 1 does not write.  Phase 2 stages S^K_A and S^Q_B
+// and writes S, S^Q and M^KQ, forming W tile by tile.
+template <int DV>
+struct WideSmem {
+    static constexpr int D = 128, LD = D + 4, LV = DV + 4;
+    static constexpr int PA = 0, MQPB = PA + D * LV, SQP = MQPB + D * LV, VEC = SQP + D * LV, P1 = VEC + 3 * D;
+    static constexpr int SKA = 0, SQB = SKA + D * LD, P2 = SQB + D * LD;
+    static constexpr int TOTAL = P1 > P2 ? P1 : P2;
+};
+
+template <int DV>
+__global__ void __launch_bounds__(kThreads) combine3_wide_kernel(Comb3 c) {
+    using Sm = WideSmem<DV>;
+    constexpr int D = Sm::D;
+    extern __shared__ __align__(16) float sm[];
+    const int i0 = blockIdx.x;
+    const float f = c.decay_pow ? c.decay_pow[i0] : 1.f, f2 = f * f, f3 = f2 * f;
+    const size_t oD = (size_t)i0 * D * D, oV = (size_t)i0 * D * DV, od = (size_t)i0 * D;
+    const float *SKA_g = c.A.S + oD, *SQB_g = c.B.SQ + oD, *MKQB_g = c.B.MKQ + oD;
+    // ---- phase 1: P, T, M^QP and the unit column
+    float *PA = sm + Sm::PA, *MQPB = sm + Sm::MQPB, *SQP = sm + Sm::SQP;
+    float *mA = sm + Sm::VEC, *mqmB = mA + D, *sqm = mqmB + D;
+    for (int e = threadIdx.x; e < D * DV; e += kThreads) {
+        const int o = (e / DV) * Sm::LV + e % DV;
+        PA[o] = c.A.P[oV + e];
+        MQPB[o] = c.B.MQP[oV + e];
+    }
+    if (c.norm)
+        for (int e = threadIdx.x; e < D; e += kThreads) {
+            mA[e] = c.A.m[od + e];
+            mqmB[e] = c.B.mqm[od + e];
+        }
+    __syncthreads();
+    // S^Q_B P_A and S^Q_B m_A
+    tiles<false, D, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, false>(acc, SQB_g, D, PA, Sm::LV, m0, n0, ns, D);
+        each(acc, m0, n0, ns, [&](int i, int j, float x) { SQP[i * Sm::LV + j] = x; });
+    });
+    if (c.norm)
+        for (int i = threadIdx.x; i < D; i += kThreads) {
+            float acc = 0.f;
+            for (int l = 0; l < D; ++l) acc = fmaf(SQB_g[(size_t)i * D + l], mA[l], acc);
+            sqm[i] = acc;
+        }
+    __syncthreads();
+    tiles<false, D, DV>([&](float (&acc)[4][4], int m0, int n0, int ns) {
+        float t[4][4] = {};
+        mac<false, false>(t, SKA_g, D, MQPB, Sm::LV, m0, n0, ns, D);  // S^K_A M^QP_B
+        mac<false, false>(t, MKQB_g, D, PA, Sm::LV, m0, n0, ns, D);   // + M^KQ_B P_A
+        mac<false, false>(acc, SKA_g, D, SQP, Sm::LV, m0, n0, ns, D); // S^K_A S^Q_B P_A
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int r = m0 + i, col = n0 + j * ns;
+                const size_t g = oV + (size_t)r * DV + col;
+                const float tA = c.A.T[g], tB = c.B.T[g], qA = c.A.MQP[g], qB = MQPB[r * Sm::LV + col];
+                const float pA = PA[r * Sm::LV + col], pB = c.B.P[g];
+                c.out.T[g] = f3 * tA + tB + f * t[i][j] + f2 * acc[i][j];
+                c.out.MQP[g] = f2 * qA + qB + f * SQP[r * Sm::LV + col];
+                c.out.P[g] = f * pA + pB;
+            }
+    });
+    if (c.norm) {
+        for (int i = threadIdx.x; i < D; i += kThreads) {
+            float skq = 0.f, mkm = 0.f, wmm = 0.f;
+            for (int l = 0; l < D; ++l) {
+                skq = fmaf(SKA_g[(size_t)i * D + l], mqmB[l], skq);
+                mkm = fmaf(MKQB_g[(size_t)i * D + l], mA[l], mkm);
+                wmm = fmaf(SKA_g[(size_t)i * D + l], sqm[l], wmm);
+            }
+            const float hA = c.A.h[od + i], hB = c.B.h[od + i], mAi = mA[i], mB = c.B.m[od + i];
+            const float qA = c.A.mqm[od + i], qB = mqmB[i];
+            c.out.h[od + i] = f3 * hA + hB + f * (skq + mkm) + f2 * wmm;
+            c.out.m[od + i] = f * mAi + mB;
+            c.out.mqm[od + i] = f2 * qA + qB + f * sqm[i];
+        }
+    }
+    __syncthreads();  // every read of phase 1 is done before phase 2 writes S, S^Q, M^KQ
+    // ---- phase 2: S, S^Q, M^KQ
+    float *SKA = sm + Sm::SKA, *SQB = sm + Sm::SQB;
+    for (int e = threadIdx.x; e < D * D; e += kThreads) {
+        const int o = (e / D) * Sm::LD + e % D;
+        SKA[o] = SKA_g[e];
+        SQB[o] = SQB_g[e];
+    }
+    __syncthreads();
+    tiles<false, D, D>([&](float (&acc)[4][4], int m0, int n0, int ns) {
+        mac<false, false>(acc, SKA, Sm::LD, SQB, Sm::LD, m0, n0, ns, D);  // W = S^K_A S^Q_B
+        each(acc, m0, n0, ns, [&](int i, int j, float x) {
+            const size_t g = oD + (size_t)i * D + j;
+            const float kA = c.A.MKQ[g], kB = c.B.MKQ[g], qA = c.A.SQ[g], qB = SQB[i * Sm::LD + j];
+            c.out.S[g] = f * SKA[i * Sm::LD + j] + c.B.S[g];
+            c.out.SQ[g] = f * qA + qB;
+            c.out.MKQ[g] = f2 * kA + kB + f * x;
+        });
+    });
+}
+
+template <int DV>
+cudaError_t combine_wide_t(const Comb3 &c, cudaStream_t st) {
+    constexpr size_t bytes = WideSmem<DV>::TOTAL * sizeof(float);
+    static_assert(bytes <= 227 * 1024, "shared memory");
+    cudaError_t e = smem_attr(combine3_wide_kernel<DV>, bytes);
+    if (e != cudaSuccess) return e;
+    combine3_wide_kernel<DV><<<c.count, kThreads, bytes, st>>>(c);
+    return cudaGetLastError();
+}
+
 template <int D, int DV>
 cudaError_t combine_t(const Comb3 &c, cudaStream_t st) {
     constexpr size_t bytes = CombSmem<D, DV>::TOTAL * sizeof(float);
@@ -220,6 +334,11 @@ struct CombFn {
 }  // namespace fwd3
 
 cudaError_t fwd3_maps_launch(const Fwd3Args &a, cudaStream_t st) {
+    if (a.d == 128) {
+        if (a.dv == 16) return fwd3::maps_t<128, 16>(a, st);
+        if (a.dv == 32) return fwd3::maps_t<128, 32>(a, st);
+        return cudaErrorInvalidValue;
+    }
     return fwd3::by_width<fwd3::MapsFn>(a.d, a.dv, a, st);
 }
 
@@ -227,6 +346,15 @@ cudaError_t state3_combine_launch(int count, int d, int dv, bool norm, const hla
                                   const hla_state3 &out, const float *decay_pow, cudaStream_t st) {
     if (count == 0) return cudaSuccess;
     fwd3::Comb3 c{count, d, dv, norm, A, B, out, decay_pow};
+    if (d == 128) {
+        switch (dv) {
+            case 16: return fwd3::combine_wide_t<16>(c, st);
+            case 32: return fwd3::combine_wide_t<32>(c, st);
+            case 64: return fwd3::combine_wide_t<64>(c, st);
+            case 128: return fwd3::combine_wide_t<128>(c, st);
+        }
+        return cudaErrorInvalidValue;
+    }
     if (dv == 128) {  // the concatenation at dv = 128 (the forward reaches it through value halves)
         switch (d) {
             case 16: return fwd3::combine_t<16, 128>(c, st);

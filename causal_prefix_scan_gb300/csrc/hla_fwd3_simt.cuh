@@ -1,5 +1,6 @@
 // hla_fwd3_simt.cuh -- chunk-parallel forward of masked third-order HLA on CUDA
-// cores (fp32 arithmetic), for d, dv, chunk in {16,32,64}.
+// cores (fp32 arithmetic), for d, dv, chunk in {16,32,64} and for d = 128 with
+// 16-token chunks and dv in {16,32}.
 //
 // "Higher-order Linear Attention", gist.science summary, section 3 "Derde-orde HLA":
 // the operator A A^T A (A = Q K^T) with every factor causal,
@@ -166,8 +167,12 @@ struct ScanSmem3 {
     static constexpr int NB = DV / kSplit, LF = D + 4, LB = NB + 4;
     static constexpr int SK = 0, PB = SK + D * LF, TB = PB + D * LB, X = TB + D * LB, Y = X + D * LB,
                          RED = Y + D * LB, RSZ = kThreads * 16, BUF = RED + 2 * RSZ;
-    // one buffer: S^K_B, S^Q_B, M^KQ_B (D x LF each), then the column blocks of P_B, T_B, M^QP_B
-    static constexpr int B_SK = 0, B_SQ = D * LF, B_MKQ = 2 * D * LF, B_P = 3 * D * LF, B_T = B_P + D * LB,
+    // one buffer: S^K_B, S^Q_B, M^KQ_B (D x LF each), then the column blocks of P_B, T_B,
+    // M^QP_B.  At d = 128 two buffers of three d x d sums do not fit beside the running
+    // S^K: the d x d sums are then read from the workspace where they are used.
+    static constexpr bool STAGE_DD = D <= 64;
+    static constexpr int DD = STAGE_DD ? D * LF : 0;
+    static constexpr int B_SK = 0, B_SQ = DD, B_MKQ = 2 * DD, B_P = 3 * DD, B_T = B_P + D * LB,
                          B_MQP = B_T + D * LB, BUFSZ = B_MQP + D * LB;
     static constexpr int TOTAL = BUF + 2 * BUFSZ;
 };
@@ -191,9 +196,11 @@ __global__ void __launch_bounds__(kThreads) fwd3_scan_kernel(Fwd3Args a) {
     auto issue = [&](int ch) {  // the local sums of chunk ch into buffer ch & 1
         const float *lc = loc + (size_t)ch * ws.loc_floats();
         float *b = sm + Sm::BUF + (ch & 1) * Sm::BUFSZ;
-        copy_mat_async<D>(lc + ws.o_sk(), D, b + Sm::B_SK, LF, D);
-        copy_mat_async<D>(lc + ws.o_sq(), D, b + Sm::B_SQ, LF, D);
-        copy_mat_async<D>(lc + ws.o_mkq(), D, b + Sm::B_MKQ, LF, D);
+        if constexpr (Sm::STAGE_DD) {
+            copy_mat_async<D>(lc + ws.o_sk(), D, b + Sm::B_SK, LF, D);
+            copy_mat_async<D>(lc + ws.o_sq(), D, b + Sm::B_SQ, LF, D);
+            copy_mat_async<D>(lc + ws.o_mkq(), D, b + Sm::B_MKQ, LF, D);
+        }
         copy_mat_async<NB>(lc + ws.o_p() + c0, DV, b + Sm::B_P, LB, D);
         copy_mat_async<NB>(lc + ws.o_t() + c0, DV, b + Sm::B_T, LB, D);
         copy_mat_async<NB>(lc + ws.o_mqp() + c0, DV, b + Sm::B_MQP, LB, D);
@@ -227,13 +234,18 @@ __global__ void __launch_bounds__(kThreads) fwd3_scan_kernel(Fwd3Args a) {
         cp_async_wait<1>();  // chunk ch's copies (the group before the one just committed)
         __syncthreads();
         const float *b = sm + Sm::BUF + (ch & 1) * Sm::BUFSZ;
-        const float *SKl = b + Sm::B_SK, *SQl = b + Sm::B_SQ, *MKQl = b + Sm::B_MKQ;
+        const float *lc = loc + (size_t)ch * ws.loc_floats();
+        // the d x d sums: staged (row stride LF) or in the workspace (row stride D)
+        constexpr int LDD = Sm::STAGE_DD ? LF : D;
+        const float *SKl = Sm::STAGE_DD ? b + Sm::B_SK : lc + ws.o_sk();
+        const float *SQl = Sm::STAGE_DD ? b + Sm::B_SQ : lc + ws.o_sq();
+        const float *MKQl = Sm::STAGE_DD ? b + Sm::B_MKQ : lc + ws.o_mkq();
         const float *Pl = b + Sm::B_P, *Tl = b + Sm::B_T, *MQPl = b + Sm::B_MQP;
         const int L = min(C, a.n - ch * C);
         const float f = decay ? gpow(lg, (float)L) : 1.f, f3 = f * f * f;
         // S^Q_B P_A and M^KQ_B P_A (block columns), each over all threads
-        mac_ksplit<D, NB, D>(SQl, LF, Pb, LB, red1);
-        mac_ksplit<D, NB, D>(MKQl, LF, Pb, LB, red2);
+        mac_ksplit<D, NB, D>(SQl, LDD, Pb, LB, red1);
+        mac_ksplit<D, NB, D>(MKQl, LDD, Pb, LB, red2);
         __syncthreads();
         // X = M^QP_B + f S^Q_B P_A,  Y = M^KQ_B P_A
         for (int e = threadIdx.x; e < D * NB; e += kThreads) {
@@ -253,7 +265,7 @@ __global__ void __launch_bounds__(kThreads) fwd3_scan_kernel(Fwd3Args a) {
         // S^K <- f S^K + S^K_B
         for (int e = threadIdx.x; e < D * D; e += kThreads) {
             const int r = e / D, x = e % D;
-            SK[r * LF + x] = f * SK[r * LF + x] + SKl[r * LF + x];
+            SK[r * LF + x] = f * SK[r * LF + x] + SKl[r * LDD + x];
         }
         __syncthreads();
     }
@@ -401,6 +413,14 @@ cudaError_t launch_d(const Fwd3Args &a, cudaStream_t st) {
         case 16: return launch_dv<T, C, 16>(a, st);
         case 32: return launch_dv<T, C, 32>(a, st);
         case 64: return launch_dv<T, C, 64>(a, st);
+        case 128:
+            // d = 128: the output kernel's S^K_p (128 x 128 fp32), P_p, T_p and chunk tiles
+            // fit 227 KB of shared memory at 16-token chunks and dv <= 32
+            if constexpr (C == 16) {
+                if (a.dv == 16) return launch_t<T, C, 128, 16>(a, st);
+                if (a.dv == 32) return launch_t<T, C, 128, 32>(a, st);
+            }
+            break;
     }
     return cudaErrorInvalidValue;
 }

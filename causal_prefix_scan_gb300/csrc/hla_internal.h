@@ -116,15 +116,12 @@ struct NormLayout {
 NormLayout bwd_norm_layout(const hla_params &p);
 hla_status bwd_norm_launch(const hla_params &p, const BwdArgs &a, void *workspace, cudaStream_t st);
 // A call split over value columns (hla_bwd_split.cu; the backward and the third-order
-// forward at dv = 128, the backward at d = 128): columns [part_width part, part_width
-// (part + 1)) of [rows][width] elements of type dt gathered into [rows][part_width] (or
-// scattered back; part_width elements a multiple of 16 bytes), the same for the two
-// halves of 128 columns, and the fp32 sum of the slices' dq, dk (first: overwrite) with
-// its final rounding.
+// forward at dv = 128 or d = 128): columns [part_width part, part_width (part + 1)) of
+// [rows][width] elements of type dt gathered into [rows][part_width] (or scattered back;
+// part_width elements a multiple of 16 bytes), and the fp32 sum of the slices' dq, dk
+// (first: overwrite) with its final rounding.
 cudaError_t cols_part_copy(const void *src, void *dst, size_t rows, hla_dtype dt, int width, int part_width,
                            int part, bool gather, cudaStream_t st);
-cudaError_t cols_half_copy(const void *src, void *dst, size_t rows, hla_dtype dt, int half, bool gather,
-                           cudaStream_t st);
 cudaError_t acc_add(float *acc, const void *src, size_t count, hla_dtype dt, bool first, cudaStream_t st);
 cudaError_t acc_store(void *dst, const float *acc, size_t count, hla_dtype dt, cudaStream_t st);
 // The same on the tensor cores (hla_bwd_norm_tc.cu): bf16, d = dv = chunk = 64 (the shape),

@@ -328,21 +328,22 @@ HLA_API size_t hla_forward3_workspace_size(const hla_params *p);
  * (section 4, "Derde-orde scans"): chunk-local sums, a scan over chunks that composes
  * states with the segment-level linear maps M^KQ and M^QP, then per-chunk outputs.
  *   p         flags 0, HLA_DECAY (gamma [H], values in [0, 1]), HLA_NORMALIZE
- *             (eps >= 0) or both; Hkv 0 or H; d in {16,32,64}, dv and chunk in
- *             {16,32,64,128}; in_dtype HLA_F32 or HLA_BF16 (fp32 arithmetic).
- *             dv = 128 runs as two problems over the value columns [0,64) and
- *             [64,128): the output's column j and the state's P, T, M^QP columns j
- *             depend on column j of v only, while S, S^Q, M^KQ, m, h, mqm depend on
- *             no value column; each half writes its columns of o and of state_out.
- *             A 128-token chunk runs as two of 64 tokens (the same result up to
- *             rounding);
+ *             (eps >= 0) or both; Hkv 0 or H; d, dv and chunk in {16,32,64,128};
+ *             in_dtype HLA_F32 or HLA_BF16 (fp32 arithmetic).  dv = 128 runs as two
+ *             problems over the value columns [0,64) and [64,128): the output's
+ *             column j and the state's P, T, M^QP columns j depend on column j of v
+ *             only, while S, S^Q, M^KQ, m, h, mqm depend on no value column; each half
+ *             writes its columns of o and of state_out.  A 128-token chunk runs as two
+ *             of 64 tokens (the same result up to rounding).  d = 128 runs on the CUDA
+ *             cores in 16-token chunks (whatever chunk is given) over slices of 32
+ *             value columns when dv > 32, split as above;
  *   q, k      [B][H][n][d]; v, o [B][H][n][dv]; in_dtype;
  *   state_in  (S, P, T; with HLA_NORMALIZE also m, h) before the first token, or NULL
  *             for zeros;
  *   state_out (S, P, T; with HLA_NORMALIZE also m, h) after the last token, or NULL;
  *             may not alias state_in;
  *   workspace at least hla_forward3_workspace_size(p) bytes, 16-byte aligned (256-byte
- *             aligned with HLA_NORMALIZE or dv = 128).
+ *             aligned with HLA_NORMALIZE or a split over value columns).
  * Three kernel launches on `stream` (tensor cores for bf16 at 64/64/64 without decay,
  * CUDA cores otherwise).  With HLA_NORMALIZE the numerator and the denominator (a
  * 16-wide unit-value tile with the same S) are two such forwards, followed by an
@@ -354,7 +355,7 @@ HLA_API hla_status hla_forward3_chunked(const hla_params *p, const void *q, cons
 
 /* hla_forward3_chunked recording four caller-owned events on `stream` (NULL: none):
  * before the local-sums kernel, after it, after the scan and after the output kernel
- * (with dv = 128: the first before the call, the other three after it). */
+ * (with a split over value columns: the first before the call, the other three after it). */
 HLA_API hla_status hla_forward3_chunked_traced(const hla_params *p, const void *q, const void *k, const void *v,
                                                void *o, const hla_state3 *state_in, const hla_state3 *state_out,
                                                void *workspace, size_t workspace_bytes, void *stream,
@@ -382,7 +383,9 @@ HLA_API hla_status hla_decode3_step(int N, int H, int d, int dv, hla_dtype dtype
  * and with HLA_NORMALIZE the unit column likewise (m as P, h as T, mqm as M^QP).
  * A, B, out: hla_state3 with S, P, T, SQ, MQP, MKQ (and m, h, mqm with HLA_NORMALIZE),
  * fp32 [count][...]; out may alias A or B (each item is read whole before it is
- * written).  flags: 0 or HLA_NORMALIZE; d in {16, 32, 64}, dv in {16, 32, 64, 128}.  One launch on `stream`.
+ * written).  flags: 0 or HLA_NORMALIZE; d and dv in {16, 32, 64, 128}.  One launch on
+ * `stream` (at d = 128 in two phases inside it: P, T, M^QP and the unit column, then
+ * S, S^Q, M^KQ, each staging what it overwrites).
  */
 HLA_API hla_status hla_state3_combine(int count, int d, int dv, unsigned flags, const hla_state3 *A,
                                       const hla_state3 *B, const hla_state3 *out, const float *decay_pow,

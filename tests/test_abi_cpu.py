@@ -233,7 +233,7 @@ def _f3call(p, ptrs=(16,) * 4, sin=None, sout=None, ws=16, ws_bytes=1 << 40):
     (dict(flags=hla.HLA_UNMASKED), hla.HLA_ERR_UNSUPPORTED),
     (dict(flags=hla.HLA_ASYMMETRIC), hla.HLA_ERR_UNSUPPORTED),
     (dict(H=4, Hkv=2), hla.HLA_ERR_UNSUPPORTED),
-    (dict(d=128), hla.HLA_ERR_UNSUPPORTED),
+    (dict(d=48), hla.HLA_ERR_UNSUPPORTED),
     (dict(chunk=256), hla.HLA_ERR_UNSUPPORTED),
     (dict(dv=48), hla.HLA_ERR_UNSUPPORTED),
     (dict(dv=96), hla.HLA_ERR_UNSUPPORTED),
@@ -261,6 +261,24 @@ def test_forward3_value_halves_and_long_chunks(lib):
             hla.hla_forward3_workspace_size(_params(chunk=64, in_dtype=dt))
     assert _f3call(_params(dv=128), ws=16) == hla.HLA_ERR_ARG
     assert "256" in hla.hla_last_error()
+
+
+def test_forward3_key_width_128(lib):
+    """d = 128 runs in 16-token chunks over slices of at most 32 value columns: dv <= 32
+    is the plain layout at chunk 16 (whatever chunk is asked for), wider values split like
+    dv = 128 at d <= 64 with 32-column slices."""
+    al = lambda x: -(-x // 256) * 256
+    B, H, n, d = 1, 2, 100, 128
+    for dv in (16, 32):
+        want = B * H * (-(-n // 16)) * (4 * d * d + 5 * d * dv) * 4
+        for c in (16, 32, 64, 128):
+            assert hla.hla_forward3_workspace_size(_params(B=B, H=H, n=n, d=d, dv=dv, chunk=c)) == want
+    for dt, el in ((hla.HLA_F32, 4), (hla.HLA_BF16, 2)):
+        inner = hla.hla_forward3_workspace_size(_params(B=B, H=H, n=n, d=d, dv=32, chunk=16, in_dtype=dt))
+        rows, part = B * H * n, B * H * d * 32 * 4
+        for dv in (64, 128):
+            want = al(inner) + 2 * al(rows * 32 * el) + 2 * al(3 * part)
+            assert hla.hla_forward3_workspace_size(_params(B=B, H=H, n=n, d=d, dv=dv, chunk=64, in_dtype=dt)) == want
 
 
 def test_forward3_rejects_null_misaligned_short_workspace_and_aliasing(lib):
@@ -360,7 +378,8 @@ def test_state3_combine_rejects_bad_args(lib):
     call = lambda count=2, d=64, dv=64, fl=0, A=full, B=full, out=full: L.hla_state3_combine(count, d, dv, fl, A, B,
                                                                                              out, None, None)
     assert call(count=-1) == hla.HLA_ERR_ARG
-    assert call(d=128) == hla.HLA_ERR_UNSUPPORTED
+    assert call(d=48) == hla.HLA_ERR_UNSUPPORTED
+    assert call(d=128, dv=96) == hla.HLA_ERR_UNSUPPORTED
     assert call(fl=hla.HLA_DECAY) == hla.HLA_ERR_UNSUPPORTED
     assert call(A=None) == hla.HLA_ERR_ARG
     assert call(B=nomaps) == hla.HLA_ERR_ARG
