@@ -287,11 +287,18 @@ def forward3(q, k, v, state_in=None, chunk=None, want_state=True, nthreads=None,
     columns, the unit column last (its P is the key mass m^K, its G1..G3 are h^(1..3)).
     state_in / the returned state: dict with the fields of STATE3_FIELDS, each
     [B*H, d, d] or [B*H, d, dve] (T is derived and ignored on input).
+    Key/value heads may be shared: k [B,Hkv,n,d], v [B,Hkv,n,dv] with H a multiple of
+    Hkv, query head h reading key/value head h // (H // Hkv) (each group's keys and
+    values are given to every query head of the group before the recurrence runs).
     Returns (o [B,H,n,dv], state or None)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, n, d = q.shape
     dv = v.shape[-1]
-    assert k.shape == q.shape and v.shape == (B, H, n, dv)
+    Hkv = k.shape[1]
+    assert k.shape == (B, Hkv, n, d) and v.shape == (B, Hkv, n, dv) and H % Hkv == 0
+    if Hkv != H:
+        k = np.ascontiguousarray(np.repeat(k, H // Hkv, axis=1))
+        v = np.ascontiguousarray(np.repeat(v, H // Hkv, axis=1))
     dve = dv + (1 if normalize else 0)
     units = B * H
     g = None if gamma is None else np.ascontiguousarray(np.asarray(gamma, np.float64).reshape(H))

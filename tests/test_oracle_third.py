@@ -46,6 +46,20 @@ def test_brute_force(n, d, dv):
         assert rel(o[0, h], brute3(q[0, h], k[0, h], v[0, h])) < 1e-12
 
 
+def test_shared_key_value_heads_brute_force():
+    """Four query heads on two key/value heads: query head h uses key/value head h // 2
+    (not h % 2) in the four-index sum."""
+    rng = np.random.default_rng(17)
+    q = rng.standard_normal((1, 4, 7, 3))
+    k = rng.standard_normal((1, 2, 7, 3))
+    v = rng.standard_normal((1, 2, 7, 2))
+    o, _ = oracle.forward3(q, k, v)
+    for h in range(4):
+        assert rel(o[0, h], brute3(q[0, h], k[0, h // 2], v[0, h // 2])) < 1e-12
+    oc, _ = oracle.forward3(q, k, v, chunk=2)
+    assert rel(oc, o) < 1e-12
+
+
 def test_dense_form():
     rng = np.random.default_rng(2)
     n, d, dv = 40, 5, 3
