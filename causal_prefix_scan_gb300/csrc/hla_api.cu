@@ -466,7 +466,7 @@ hla_status check_fwd3_params(const hla_params *p) {
     const bool c_ok = p->chunk == 16 || p->chunk == 32 || p->chunk == 64 || p->chunk == 128;
     if (!dv_ok || !c_ok || !hla::fwd3_supported(fwd3_inner(*p)))
         return fail(HLA_ERR_UNSUPPORTED,
-                    "third order supports flags HLA_DECAY, HLA_NORMALIZE, Hkv = H, d, dv and chunk in "
+                    "third order supports flags HLA_DECAY, HLA_NORMALIZE, Hkv dividing H, d, dv and chunk in "
                     "{16,32,64,128} (got flags=%u Hkv=%d d=%d dv=%d chunk=%d)",
                     p->flags, p->Hkv, p->d, p->dv, p->chunk);
     if ((p->flags & HLA_NORMALIZE) && !(p->eps >= 0.f)) return fail(HLA_ERR_ARG, "need eps >= 0");
@@ -562,6 +562,7 @@ hla_status forward3_impl(const hla_params *p, const void *q, const void *k, cons
         const int parts = fwd3_slices(*p), pw = in.dv;
         uint8_t *w = static_cast<uint8_t *>(workspace);
         const size_t rows = (size_t)p->B * p->H * p->n, srows = (size_t)p->B * p->H * p->d;
+        const size_t kv_rows = (size_t)p->B * (p->Hkv > 0 ? p->Hkv : p->H) * p->n;
         const size_t hs = srows * pw;  // floats of one slice array of the state
         float *ti = reinterpret_cast<float *>(w + L.sin), *to = reinterpret_cast<float *>(w + L.sout);
         auto ev = [&](int i) {
@@ -569,7 +570,7 @@ hla_status forward3_impl(const hla_params *p, const void *q, const void *k, cons
         };
         cudaError_t e = ev(0);
         for (int h = 0; h < parts && e == cudaSuccess; ++h) {
-            if ((e = hla::cols_part_copy(v, w + L.vh, rows, p->in_dtype, p->dv, pw, h, true, st)) != cudaSuccess)
+            if ((e = hla::cols_part_copy(v, w + L.vh, kv_rows, p->in_dtype, p->dv, pw, h, true, st)) != cudaSuccess)
                 break;
             hla_state3 si{}, so{};
             if (state_in) {
@@ -607,6 +608,7 @@ hla_status forward3_impl(const hla_params *p, const void *q, const void *k, cons
     p = &inner;
     hla::Fwd3Args a;
     a.B = p->B; a.H = p->H; a.n = p->n; a.d = p->d; a.dv = p->dv; a.chunk = p->chunk;
+    a.Hkv = p->Hkv > 0 ? p->Hkv : p->H;
     a.in_dtype = p->in_dtype;
     a.gamma = (p->flags & HLA_DECAY) ? p->gamma : nullptr;
     a.q = q; a.k = k; a.v = v; a.o = o;

@@ -219,7 +219,7 @@ bool fwd3_supported(const hla_params &p) {
     auto ok = [](int x) { return x == 16 || x == 32 || x == 64; };
     const int hkv = p.Hkv > 0 ? p.Hkv : p.H;
     const bool shape = (ok(p.d) && ok(p.dv) && ok(p.chunk)) || (p.d == 128 && p.chunk == 16 && (p.dv == 16 || p.dv == 32));
-    return shape && hkv == p.H && (p.flags & ~(unsigned)(HLA_DECAY | HLA_NORMALIZE)) == 0;
+    return shape && p.H % hkv == 0 && (p.flags & ~(unsigned)(HLA_DECAY | HLA_NORMALIZE)) == 0;
 }
 
 namespace fwd3 {

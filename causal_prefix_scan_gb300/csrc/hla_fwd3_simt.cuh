@@ -28,6 +28,9 @@
 // f = g^L:  S^K = f S^K_A + S^K_B (P likewise),  X = M^QP_B + f S^Q_B P_A,
 //   T = f^3 T_A + T_B + f M^KQ_B P_A + f S^K_A X.
 //
+// Key/value heads may be shared: query head h reads key/value head h / (H / Hkv); the
+// state stays per query head.
+//
 // Three launches: (1) one CTA per chunk writes the local sums; (2) the scan, one CTA
 // per (b,h) and column block of dv, walks the chunks and writes each chunk's prefix
 // state (and the final state); (3) one CTA per chunk forms the outputs.  For bf16
@@ -72,6 +75,11 @@ struct Ws3 {
     __host__ __device__ size_t s_t() const { return (size_t)d * d + (size_t)d * dv; }
 };
 
+// Key/value head read by query pair u = b*H + h: b*Hkv + h / (H / Hkv).
+__device__ __forceinline__ size_t kv_unit(const Fwd3Args &a, int u) {
+    return (size_t)(u / a.H) * a.Hkv + (u % a.H) / (a.H / a.Hkv);
+}
+
 // ---- (1) chunk-local sums --------------------------------------------------------
 // Powers g^x, x = 0 .. 3C (gp[x]); all ones without decay.
 constexpr int gp_count(int C) { return 3 * C + 4; }
@@ -99,8 +107,9 @@ __global__ void __launch_bounds__(kThreads) fwd3_local_kernel(Fwd3Args a) {
     const size_t rq = ((size_t)u * a.n + t0) * D, rv = ((size_t)u * a.n + t0) * DV;
     fill_powers(gp, gp_count(C), a, u);
     load_rows<D>(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L);
-    load_rows<D>(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L);
-    load_rows<DV>(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L);
+    const size_t kvu = kv_unit(a, u), rk = (kvu * a.n + t0) * D, rkv = (kvu * a.n + t0) * DV;
+    load_rows<D>(static_cast<const T *>(a.k) + rk, K, Sm::LQ, C, L);
+    load_rows<DV>(static_cast<const T *>(a.v) + rkv, V, Sm::LV, C, L);
     __syncthreads();
     // token weights of the local sums, relative to the chunk's last token e = L - 1
     for (int b = threadIdx.x; b < C; b += kThreads) {
@@ -314,8 +323,9 @@ __global__ void __launch_bounds__(kThreads) fwd3_out_kernel(Fwd3Args a) {
     copy_mat_async<DV>(so + ws.s_t(), DV, Tp, Sm::LV, D);
     cp_async_commit();
     load_rows<D>(static_cast<const T *>(a.q) + rq, Q, Sm::LQ, C, L);
-    load_rows<D>(static_cast<const T *>(a.k) + rq, K, Sm::LQ, C, L);
-    load_rows<DV>(static_cast<const T *>(a.v) + rv, V, Sm::LV, C, L);
+    const size_t kvu = kv_unit(a, u), rk = (kvu * a.n + t0) * D, rkv = (kvu * a.n + t0) * DV;
+    load_rows<D>(static_cast<const T *>(a.k) + rk, K, Sm::LQ, C, L);
+    load_rows<DV>(static_cast<const T *>(a.v) + rkv, V, Sm::LV, C, L);
     __syncthreads();
     for (int t = threadIdx.x; t < C; t += kThreads) {  // row scales of the prefix-state terms
         r1[t] = gp[t + 1];

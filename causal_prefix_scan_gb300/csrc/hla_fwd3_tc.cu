@@ -35,7 +35,8 @@ __global__ void __launch_bounds__(kTc, 2) fwd3_local_tc_kernel(const __grid_cons
     const size_t r0 = ((size_t)u * a.n + t0) * 64;
     {
         const CUtensorMap *m[3] = {&tm.q, &tm.k, &tm.v};
-        const int un[3] = {u, u, u};
+        const int kvu = (u / a.H) * a.Hkv + (u % a.H) / (a.H / a.Hkv);  // key/value head
+        const int un[3] = {u, kvu, kvu};
         uint8_t *dst[3] = {x.tile(L_Q), x.tile(L_K), x.tile(L_V)};
         tma_issue<3>(x, m, un, t0, dst);
     }
@@ -111,7 +112,8 @@ __global__ void __launch_bounds__(kTc, 2) fwd3_out_tc_kernel(const __grid_consta
     const float *so = a.workspace + (size_t)a.B * a.H * nch * ws.loc_floats() + ((size_t)u * nch + ch) * ws.st_floats();
     {  // the bf16 inputs by TMA while the threads convert the states
         const CUtensorMap *m[3] = {&tm.q, &tm.k, &tm.v};
-        const int un[3] = {u, u, u};
+        const int kvu = (u / a.H) * a.Hkv + (u % a.H) / (a.H / a.Hkv);  // key/value head
+        const int un[3] = {u, kvu, kvu};
         uint8_t *dst[3] = {x.tile(O_Q), x.tile(O_K), x.tile(O_V)};
         tma_issue<3>(x, m, un, t0, dst);
         const float *ss[3] = {so + ws.s_sk(), so + ws.s_p(), so + ws.s_t()};
@@ -187,7 +189,7 @@ cudaError_t local_tc(const Fwd3Args &a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     const int nch = (a.n + 63) / 64;
     ChunkMaps m;
-    if (!chunk_maps(m, a.q, a.k, a.v, nullptr, a.n, a.B * a.H, a.B * a.H)) return cudaErrorInvalidValue;
+    if (!chunk_maps(m, a.q, a.k, a.v, nullptr, a.n, a.B * a.H, a.B * a.Hkv)) return cudaErrorInvalidValue;
     fwd3_local_tc_kernel<<<a.B * a.H * nch, kTc, kLocalSmem, st>>>(a, m);
     return cudaGetLastError();
 }
@@ -198,7 +200,7 @@ cudaError_t out_tc(const Fwd3Args &a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     const int nch = (a.n + 63) / 64;
     ChunkMaps m;
-    if (!chunk_maps(m, a.q, a.k, a.v, nullptr, a.n, a.B * a.H, a.B * a.H)) return cudaErrorInvalidValue;
+    if (!chunk_maps(m, a.q, a.k, a.v, nullptr, a.n, a.B * a.H, a.B * a.Hkv)) return cudaErrorInvalidValue;
     fwd3_out_tc_kernel<<<a.B * a.H * nch, kTc, kOutSmem, st>>>(a, m);
     return cudaGetLastError();
 }

@@ -133,6 +133,7 @@ hla_status bwd_norm_tc_launch(const hla_params &p, const BwdArgs &a, cudaStream_
 
 struct Fwd3Args {
     int B, H, n, d, dv, chunk;
+    int Hkv;  // key/value heads (query head h reads h / (H / Hkv))
     hla_dtype in_dtype;
     const float *gamma;  // [H] decay per head, or NULL (none)
     const void *q, *k, *v;

@@ -328,7 +328,7 @@ HLA_API size_t hla_forward3_workspace_size(const hla_params *p);
  * (section 4, "Derde-orde scans"): chunk-local sums, a scan over chunks that composes
  * states with the segment-level linear maps M^KQ and M^QP, then per-chunk outputs.
  *   p         flags 0, HLA_DECAY (gamma [H], values in [0, 1]), HLA_NORMALIZE
- *             (eps >= 0) or both; Hkv 0 or H; d, dv and chunk in {16,32,64,128};
+ *             (eps >= 0) or both; Hkv dividing H (0 means H); d, dv and chunk in {16,32,64,128};
  *             in_dtype HLA_F32 or HLA_BF16 (fp32 arithmetic).  dv = 128 runs as two
  *             problems over the value columns [0,64) and [64,128): the output's
  *             column j and the state's P, T, M^QP columns j depend on column j of v
@@ -337,7 +337,8 @@ HLA_API size_t hla_forward3_workspace_size(const hla_params *p);
  *             of 64 tokens (the same result up to rounding).  d = 128 runs on the CUDA
  *             cores in 16-token chunks (whatever chunk is given) over slices of 32
  *             value columns when dv > 32, split as above;
- *   q, k      [B][H][n][d]; v, o [B][H][n][dv]; in_dtype;
+ *   q         [B][H][n][d], k [B][Hkv][n][d], v [B][Hkv][n][dv], o [B][H][n][dv]; in_dtype
+ *             (query head h reads key/value head h / (H / Hkv); the state is per query head);
  *   state_in  (S, P, T; with HLA_NORMALIZE also m, h) before the first token, or NULL
  *             for zeros;
  *   state_out (S, P, T; with HLA_NORMALIZE also m, h) after the last token, or NULL;

@@ -232,7 +232,7 @@ def _f3call(p, ptrs=(16,) * 4, sin=None, sout=None, ws=16, ws_bytes=1 << 40):
     (dict(flags=hla.HLA_DECAY), hla.HLA_ERR_ARG),  # decay without rates
     (dict(flags=hla.HLA_UNMASKED), hla.HLA_ERR_UNSUPPORTED),
     (dict(flags=hla.HLA_ASYMMETRIC), hla.HLA_ERR_UNSUPPORTED),
-    (dict(H=4, Hkv=2), hla.HLA_ERR_UNSUPPORTED),
+    (dict(H=6, Hkv=4), hla.HLA_ERR_ARG),
     (dict(d=48), hla.HLA_ERR_UNSUPPORTED),
     (dict(chunk=256), hla.HLA_ERR_UNSUPPORTED),
     (dict(dv=48), hla.HLA_ERR_UNSUPPORTED),
