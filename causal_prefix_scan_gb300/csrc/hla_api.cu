@@ -54,6 +54,21 @@ hla_status check_state(const hla_state *s, const char *name) {
     return HLA_OK;
 }
 
+// AHLA at dv = 128 with d <= 64, which neither the tensor-core path (dv <= d) nor the
+// CUDA-core one (dv <= 64 for this variant) takes whole: two problems over the value
+// columns [0,64) and [64,128).  The output's column j and the state's P, E columns j (in
+// C, G) depend on column j of v only; R, m^K and n (in S, m, h) on none.
+hla_params fwd_half(const hla_params &p) {
+    hla_params q = p;
+    q.dv = 64;
+    return q;
+}
+bool fwd_asym_split(const hla_params &p) {
+    if (!(p.flags & HLA_ASYMMETRIC) || p.dv != 128 || p.d > 64) return false;
+    const hla_params h = fwd_half(p);
+    return hla::fwd_tc_supported(h) || hla::fwd_simt_supported(h);
+}
+
 hla_status check_params(const hla_params *p) {
     if (!p) return fail(HLA_ERR_ARG, "params is NULL");
     if (p->B < 1 || p->H < 1 || p->n < 0) return fail(HLA_ERR_ARG, "need B >= 1, H >= 1, n >= 0");
@@ -69,6 +84,7 @@ hla_status check_params(const hla_params *p) {
     if ((p->flags & HLA_NORMALIZE) && !(p->eps >= 0.f)) return fail(HLA_ERR_ARG, "eps must be >= 0");
     if ((long long)p->B * p->H * (long long)p->n * (p->d > p->dv ? p->d : p->dv) > (1LL << 40))
         return fail(HLA_ERR_ARG, "problem too large");
+    if (fwd_asym_split(*p)) return HLA_OK;
     if (!hla::fwd_tc_supported(*p) && !hla::fwd_simt_supported(*p))
         return fail(HLA_ERR_UNSUPPORTED, "unsupported shape: dtype=%d d=%d dv=%d chunk=%d", (int)p->in_dtype, p->d,
                     p->dv, p->chunk);
@@ -112,14 +128,46 @@ const char *hla_status_string(hla_status s) {
 
 const char *hla_last_error(void) { return g_msg; }
 
+}  // extern "C"
+
+namespace {
+size_t fwd_align256(size_t x) { return (x + 255) & ~size_t(255); }
+// The split AHLA forward's workspace: the half problem's, then the gathered value half,
+// the output half (input type), and the C, G halves (fp32) of state_in and state_out.
+struct FwdSplit {
+    size_t vh, oh, sin, sout, total;
+};
+FwdSplit fwd_split_layout(const hla_params &p, int nsm) {
+    const hla_params h = fwd_half(p);
+    const size_t el = p.in_dtype == HLA_F32 ? 4 : 2, hkv = p.Hkv > 0 ? p.Hkv : p.H;
+    const size_t rq = (size_t)p.B * p.H * p.n, rkv = (size_t)p.B * hkv * p.n;
+    const size_t half_cg = (size_t)p.B * p.H * p.d * 64 * 4;  // one half of C or G
+    FwdSplit L;
+    size_t o = fwd_align256(hla::fwd_tc_supported(h) && p.n > 0 ? hla::fwd_tc_workspace(h, nsm) : 0);
+    L.vh = o; o = fwd_align256(o + rkv * 64 * el);
+    L.oh = o; o = fwd_align256(o + rq * 64 * el);
+    L.sin = o; o = fwd_align256(o + 2 * half_cg);
+    L.sout = o; o = fwd_align256(o + 2 * half_cg);
+    L.total = o;
+    return L;
+}
+}  // namespace
+
+extern "C" {
+
 size_t hla_forward_workspace_size(const hla_params *p) {
     if (check_params(p) != HLA_OK) return 0;
+    if (fwd_asym_split(*p)) return p->n > 0 ? fwd_split_layout(*p, num_sms_current()).total : 0;
     if (hla::fwd_tc_supported(*p)) return hla::fwd_tc_workspace(*p, num_sms_current());
     return 0;
 }
 
 const char *hla_forward_kernel(const hla_params *p) {
     if (check_params(p) != HLA_OK || p->n == 0) return nullptr;
+    if (fwd_asym_split(*p)) {  // the kernel of each value half
+        const hla_params h = fwd_half(*p);
+        return hla::fwd_tc_supported(h) ? hla::fwd_tc_kernel_name(h) : "fwd_simt_kernel";
+    }
     return hla::fwd_tc_supported(*p) ? hla::fwd_tc_kernel_name(*p) : "fwd_simt_kernel";
 }
 
@@ -141,7 +189,7 @@ hla_status hla_forward_chunked(const hla_params *p, const void *q, const void *k
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool tc = hla::fwd_tc_supported(*p);
     const int nsm = num_sms_current();
-    if (tc && p->n > 0) {
+    if (tc && p->n > 0 && !fwd_asym_split(*p)) {
         const size_t need = hla::fwd_tc_workspace(*p, nsm);
         if (!workspace || workspace_bytes < need)
             return fail(HLA_ERR_ARG, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
@@ -164,6 +212,47 @@ hla_status hla_forward_chunked(const hla_params *p, const void *q, const void *k
             }
             if (e != cudaSuccess) return cuda_fail(e, "state copy");
         }
+        return HLA_OK;
+    }
+    if (fwd_asym_split(*p)) {  // two 64-column halves of the values, each written into its columns
+        const FwdSplit L = fwd_split_layout(*p, nsm);
+        if (!workspace || workspace_bytes < L.total)
+            return fail(HLA_ERR_ARG, "workspace too small: need %zu bytes, got %zu", L.total, workspace_bytes);
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return fail(HLA_ERR_ARG, "workspace must be 256-byte aligned");
+        const hla_params h = fwd_half(*p);
+        uint8_t *w = static_cast<uint8_t *>(workspace);
+        const size_t hkv = p->Hkv > 0 ? p->Hkv : p->H;
+        const size_t rq = (size_t)p->B * p->H * p->n, rkv = (size_t)p->B * hkv * p->n;
+        const size_t srows = (size_t)p->B * p->H * p->d, hs = srows * 64;
+        float *ci = reinterpret_cast<float *>(w + L.sin), *co = reinterpret_cast<float *>(w + L.sout);
+        cudaError_t e = cudaSuccess;
+        for (int half = 0; half < 2 && e == cudaSuccess; ++half) {
+            if ((e = hla::cols_part_copy(v, w + L.vh, rkv, p->in_dtype, 128, 64, half, true, st)) != cudaSuccess) break;
+            hla_state si{}, so{};
+            if (state_in) {
+                si = *state_in;
+                si.C = ci;
+                si.G = ci + hs;
+                if ((e = hla::cols_part_copy(state_in->C, si.C, srows, HLA_F32, 128, 64, half, true, st)) != cudaSuccess ||
+                    (e = hla::cols_part_copy(state_in->G, si.G, srows, HLA_F32, 128, 64, half, true, st)) != cudaSuccess)
+                    break;
+            }
+            if (state_out) {  // S, m, h (R, m^K, n) come out the same from both halves
+                so = *state_out;
+                so.C = co;
+                so.G = co + hs;
+            }
+            s = hla_forward_chunked(&h, q, k, w + L.vh, w + L.oh, state_in ? &si : nullptr,
+                                    state_out ? &so : nullptr, w, L.vh, stream);
+            if (s != HLA_OK) return s;
+            if ((e = hla::cols_part_copy(w + L.oh, o, rq, p->in_dtype, 128, 64, half, false, st)) != cudaSuccess) break;
+            if (state_out &&
+                ((e = hla::cols_part_copy(so.C, state_out->C, srows, HLA_F32, 128, 64, half, false, st)) != cudaSuccess ||
+                 (e = hla::cols_part_copy(so.G, state_out->G, srows, HLA_F32, 128, 64, half, false, st)) != cudaSuccess))
+                break;
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "forward over value halves");
         return HLA_OK;
     }
     hla::FwdArgs a;

@@ -63,7 +63,7 @@ def _call(p, q=16, k=16, v=16, o=16, sin=None, sout=None, ws=None, ws_bytes=0):
     (dict(in_dtype=7), hla.HLA_ERR_ARG),
     (dict(flags=16), hla.HLA_ERR_ARG),
     (dict(flags=hla.HLA_UNMASKED | hla.HLA_ASYMMETRIC), hla.HLA_ERR_ARG),
-    (dict(flags=hla.HLA_ASYMMETRIC, d=64, dv=128), hla.HLA_ERR_UNSUPPORTED),  # needs dv <= d on tensor cores
+    (dict(flags=hla.HLA_ASYMMETRIC, d=128, dv=96), hla.HLA_ERR_UNSUPPORTED),
     (dict(H=6, Hkv=4), hla.HLA_ERR_ARG),                    # key/value heads must divide H
     (dict(Hkv=-1), hla.HLA_ERR_ARG),
     (dict(flags=hla.HLA_DECAY), hla.HLA_ERR_ARG),          # decay without gamma
@@ -76,6 +76,24 @@ def _call(p, q=16, k=16, v=16, o=16, sin=None, sout=None, ws=None, ws_bytes=0):
 def test_forward_rejects_bad_params(lib, kw, status):
     assert _call(_params(**kw)) == status
     assert hla.hla_last_error()
+
+
+def test_forward_asymmetric_value_halves(lib):
+    """AHLA at dv = 128, d <= 64 runs as two 64-column value halves: the half problem's
+    workspace, then the gathered value half, the output half (input type) and the C, G
+    halves of state_in and state_out (fp32), in 256-byte aligned regions."""
+    al = lambda x: -(-x // 256) * 256
+    for dt, el in ((hla.HLA_F32, 4), (hla.HLA_BF16, 2)):
+        for d in (16, 32, 64):
+            B, H, Hkv, n = 2, 4, 2, 100
+            kw = dict(B=B, H=H, Hkv=Hkv, n=n, d=d, chunk=64, in_dtype=dt, flags=hla.HLA_ASYMMETRIC)
+            inner = hla.hla_forward_workspace_size(_params(dv=64, **kw))
+            rq, rkv, cg = B * H * n, B * Hkv * n, B * H * d * 64 * 4
+            want = al(inner) + al(rkv * 64 * el) + al(rq * 64 * el) + 2 * al(2 * cg)
+            assert hla.hla_forward_workspace_size(_params(dv=128, **kw)) == want
+            assert hla.hla_forward_kernel(_params(dv=128, **kw)) == hla.hla_forward_kernel(_params(dv=64, **kw))
+    assert _call(_params(flags=hla.HLA_ASYMMETRIC, dv=128), ws=16, ws_bytes=1 << 40) == hla.HLA_ERR_ARG
+    assert "256" in hla.hla_last_error()
 
 
 def test_forward_rejects_null_and_misaligned(lib):

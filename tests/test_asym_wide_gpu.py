@@ -1,0 +1,54 @@
+"""GPU parity of the asymmetric variant AHLA (section 2) at value width dv = 128 with
+d <= 64, which runs as two problems over the value columns [0, 64) and [64, 128): the
+output's column j and the state's P, E columns j depend on column j of v only, R, m^K
+and n on none.  Each half takes the tensor-core path (bf16, d = 64) or the CUDA-core
+one.  Against the fp64 oracle; tolerance per (b,h) relative L2: 1e-4 for fp32 inputs,
+2e-2 for bf16."""
+import numpy as np
+import pytest
+import torch
+
+import causal_prefix_scan_gb300 as hla
+from causal_prefix_scan_gb300 import workloads as W
+from gpu_helpers import TOL_BF16, TOL_F32, assert_parity, run_forward, run_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def wl(**kw):
+    base = dict(B=1, H=2, n=200, d=64, dv=128, chunk=64, dtype="bf16", qk="elu1", seed=201, gamma_lo=0.9,
+                gamma_hi=0.999)
+    base.update(kw)
+    return W.Workload("asym128", **base)
+
+
+@pytest.mark.parametrize("d,chunk,dtype", [(64, 64, "bf16"), (64, 128, "bf16"), (32, 32, "f32"), (16, 64, "bf16")])
+@pytest.mark.parametrize("decay,normalize", [(False, False), (True, False), (True, True)])
+def test_asym_value_width_128(d, chunk, dtype, decay, normalize):
+    w = wl(d=d, chunk=chunk, dtype=dtype, decay=decay, n=3 * chunk + 21, seed=201 + d)
+    x = W.make_inputs(w)
+    o, st = run_forward(x, dtype, chunk, normalize=normalize, eps=1e-6, asymmetric=True)
+    o_ref, st_ref = run_oracle(x, normalize=normalize, eps=1e-6, asymmetric=True)
+    assert_parity(o, o_ref, st, st_ref, tol=TOL_F32 if dtype == "f32" else TOL_BF16,
+                  what=f"asym dv128 d{d} c{chunk} {dtype}", asymmetric=True)
+
+
+def test_asym_value_width_128_resumed_shared_heads():
+    """Four query heads on two key/value heads, continued from the oracle's state."""
+    w = wl(B=2, H=4, Hkv=2, n=330, decay=True, seed=210)
+    x = W.make_inputs(w)
+    n1 = 131
+    x1 = {kk: (vv[:, :, :n1] if kk != "gamma" else vv) for kk, vv in x.items()}
+    x2 = {kk: (vv[:, :, n1:] if kk != "gamma" else vv) for kk, vv in x.items()}
+    _, st1 = run_oracle(x1, normalize=True, eps=1e-6, asymmetric=True)
+    o2, st2 = run_forward(x2, "bf16", 64, normalize=True, eps=1e-6, state_in=st1, asymmetric=True)
+    o2_ref, st2_ref = run_oracle(x2, normalize=True, eps=1e-6, state_in=st1, asymmetric=True)
+    assert_parity(o2, o2_ref, st2, st2_ref, what="asym dv128 resumed, shared heads", asymmetric=True)
+
+
+def test_asym_value_width_128_kernel_name():
+    q = to_dev(np.zeros((1, 2, 64, 64), np.float32), "bf16")
+    v = to_dev(np.zeros((1, 2, 64, 128), np.float32), "bf16")
+    p = hla.make_params(q, v, 64, None, False, 0.0, False, True)
+    assert hla.hla_forward_kernel(p) == "fwd_tc_kernel"
+    assert hla.hla_forward_workspace_size(p) > 0
