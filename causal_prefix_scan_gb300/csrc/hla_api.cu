@@ -54,17 +54,19 @@ hla_status check_state(const hla_state *s, const char *name) {
     return HLA_OK;
 }
 
-// AHLA at dv = 128 with d <= 64, which neither the tensor-core path (dv <= d) nor the
-// CUDA-core one (dv <= 64 for this variant) takes whole: two problems over the value
-// columns [0,64) and [64,128).  The output's column j and the state's P, E columns j (in
-// C, G) depend on column j of v only; R, m^K and n (in S, m, h) on none.
+// The unmasked and asymmetric variants at dv = 128 with d <= 64 where no kernel takes the
+// shape whole (the tensor-core AHLA needs dv <= d, the tensor cores d >= 64 and bf16, the
+// CUDA-core kernel of these variants dv <= 64): two problems over the value columns
+// [0,64) and [64,128).  The output's column j and the state's C, G columns j (C, and P, E
+// of AHLA) depend on column j of v only; S, m, h (R, m^K, n of AHLA) on none.
 hla_params fwd_half(const hla_params &p) {
     hla_params q = p;
     q.dv = 64;
     return q;
 }
-bool fwd_asym_split(const hla_params &p) {
-    if (!(p.flags & HLA_ASYMMETRIC) || p.dv != 128 || p.d > 64) return false;
+bool fwd_value_split(const hla_params &p) {
+    if (!(p.flags & (HLA_ASYMMETRIC | HLA_UNMASKED)) || p.dv != 128 || p.d > 64) return false;
+    if (hla::fwd_tc_supported(p) || hla::fwd_simt_supported(p)) return false;
     const hla_params h = fwd_half(p);
     return hla::fwd_tc_supported(h) || hla::fwd_simt_supported(h);
 }
@@ -84,7 +86,7 @@ hla_status check_params(const hla_params *p) {
     if ((p->flags & HLA_NORMALIZE) && !(p->eps >= 0.f)) return fail(HLA_ERR_ARG, "eps must be >= 0");
     if ((long long)p->B * p->H * (long long)p->n * (p->d > p->dv ? p->d : p->dv) > (1LL << 40))
         return fail(HLA_ERR_ARG, "problem too large");
-    if (fwd_asym_split(*p)) return HLA_OK;
+    if (fwd_value_split(*p)) return HLA_OK;
     if (!hla::fwd_tc_supported(*p) && !hla::fwd_simt_supported(*p))
         return fail(HLA_ERR_UNSUPPORTED, "unsupported shape: dtype=%d d=%d dv=%d chunk=%d", (int)p->in_dtype, p->d,
                     p->dv, p->chunk);
@@ -132,7 +134,7 @@ const char *hla_last_error(void) { return g_msg; }
 
 namespace {
 size_t fwd_align256(size_t x) { return (x + 255) & ~size_t(255); }
-// The split AHLA forward's workspace: the half problem's, then the gathered value half,
+// The forward split over value halves: the half problem's workspace, the gathered value half,
 // the output half (input type), and the C, G halves (fp32) of state_in and state_out.
 struct FwdSplit {
     size_t vh, oh, sin, sout, total;
@@ -157,14 +159,14 @@ extern "C" {
 
 size_t hla_forward_workspace_size(const hla_params *p) {
     if (check_params(p) != HLA_OK) return 0;
-    if (fwd_asym_split(*p)) return p->n > 0 ? fwd_split_layout(*p, num_sms_current()).total : 0;
+    if (fwd_value_split(*p)) return p->n > 0 ? fwd_split_layout(*p, num_sms_current()).total : 0;
     if (hla::fwd_tc_supported(*p)) return hla::fwd_tc_workspace(*p, num_sms_current());
     return 0;
 }
 
 const char *hla_forward_kernel(const hla_params *p) {
     if (check_params(p) != HLA_OK || p->n == 0) return nullptr;
-    if (fwd_asym_split(*p)) {  // the kernel of each value half
+    if (fwd_value_split(*p)) {  // the kernel of each value half
         const hla_params h = fwd_half(*p);
         return hla::fwd_tc_supported(h) ? hla::fwd_tc_kernel_name(h) : "fwd_simt_kernel";
     }
@@ -189,7 +191,7 @@ hla_status hla_forward_chunked(const hla_params *p, const void *q, const void *k
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool tc = hla::fwd_tc_supported(*p);
     const int nsm = num_sms_current();
-    if (tc && p->n > 0 && !fwd_asym_split(*p)) {
+    if (tc && p->n > 0 && !fwd_value_split(*p)) {
         const size_t need = hla::fwd_tc_workspace(*p, nsm);
         if (!workspace || workspace_bytes < need)
             return fail(HLA_ERR_ARG, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
@@ -214,7 +216,7 @@ hla_status hla_forward_chunked(const hla_params *p, const void *q, const void *k
         }
         return HLA_OK;
     }
-    if (fwd_asym_split(*p)) {  // two 64-column halves of the values, each written into its columns
+    if (fwd_value_split(*p)) {  // two 64-column halves of the values, each written into its columns
         const FwdSplit L = fwd_split_layout(*p, nsm);
         if (!workspace || workspace_bytes < L.total)
             return fail(HLA_ERR_ARG, "workspace too small: need %zu bytes, got %zu", L.total, workspace_bytes);
@@ -238,7 +240,7 @@ hla_status hla_forward_chunked(const hla_params *p, const void *q, const void *k
                     (e = hla::cols_part_copy(state_in->G, si.G, srows, HLA_F32, 128, 64, half, true, st)) != cudaSuccess)
                     break;
             }
-            if (state_out) {  // S, m, h (R, m^K, n) come out the same from both halves
+            if (state_out) {  // S, m, h come out the same from both halves
                 so = *state_out;
                 so.C = co;
                 so.G = co + hs;

@@ -121,10 +121,11 @@ typedef struct {
  *       holds the pair's state in shared memory; where that leaves too little room,
  *       a chunk runs as several shorter ones (64 tokens at most; 32 at d = 128 with
  *       dv = 32 or 64, 8 at d = dv = 128), which changes only the rounding.
- *   HLA_ASYMMETRIC with dv = 128 and d in {16,32,64}: two problems over the value
- *       columns [0,64) and [64,128), each on the path above for its shape (the
- *       output's and the state's C, G columns j depend on column j of v only; S, m,
- *       h on none); the workspace then also holds the gathered halves.
+ *   HLA_ASYMMETRIC or HLA_UNMASKED with dv = 128 and d in {16,32,64} where neither
+ *       path above takes the shape: two problems over the value columns [0,64) and
+ *       [64,128), each on the path above for its shape (the output's and the state's
+ *       C, G columns j depend on column j of v only; S, m, h on none); the workspace
+ *       then also holds the gathered halves.
  *   Anything else: HLA_ERR_UNSUPPORTED.  Any n >= 0; a final partial chunk is
  *   handled exactly (decay is applied only over the tokens present).
  */

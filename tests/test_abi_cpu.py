@@ -94,6 +94,12 @@ def test_forward_asymmetric_value_halves(lib):
             assert hla.hla_forward_kernel(_params(dv=128, **kw)) == hla.hla_forward_kernel(_params(dv=64, **kw))
     assert _call(_params(flags=hla.HLA_ASYMMETRIC, dv=128), ws=16, ws_bytes=1 << 40) == hla.HLA_ERR_ARG
     assert "256" in hla.hla_last_error()
+    # the unmasked variant splits only where no kernel takes the shape whole
+    um = dict(flags=hla.HLA_UNMASKED, dv=128, n=100)
+    assert hla.hla_forward_workspace_size(_params(d=64, **um)) == \
+        hla.hla_forward_workspace_size(_params(d=64, **um, in_dtype=hla.HLA_BF16))  # tensor cores, no split
+    for d in (16, 32, 64):
+        assert hla.hla_forward_workspace_size(_params(d=d, in_dtype=hla.HLA_F32, **um)) > 0
 
 
 def test_forward_rejects_null_and_misaligned(lib):

@@ -1,9 +1,9 @@
-"""GPU parity of the asymmetric variant AHLA (section 2) at value width dv = 128 with
-d <= 64, which runs as two problems over the value columns [0, 64) and [64, 128): the
-output's column j and the state's P, E columns j depend on column j of v only, R, m^K
-and n on none.  Each half takes the tensor-core path (bf16, d = 64) or the CUDA-core
-one.  Against the fp64 oracle; tolerance per (b,h) relative L2: 1e-4 for fp32 inputs,
-2e-2 for bf16."""
+"""GPU parity of the asymmetric variant AHLA (section 2) and of the unmasked variant at
+value width dv = 128 with d <= 64 where no kernel takes the shape whole: two problems
+over the value columns [0, 64) and [64, 128) (the output's column j and the state's
+value-width columns j depend on column j of v only, the rest on none).  Each half takes
+the tensor-core path (bf16, d = 64) or the CUDA-core one.  Against the fp64 oracle;
+tolerance per (b,h) relative L2: 1e-4 for fp32 inputs, 2e-2 for bf16."""
 import numpy as np
 import pytest
 import torch
@@ -52,3 +52,14 @@ def test_asym_value_width_128_kernel_name():
     p = hla.make_params(q, v, 64, None, False, 0.0, False, True)
     assert hla.hla_forward_kernel(p) == "fwd_tc_kernel"
     assert hla.hla_forward_workspace_size(p) > 0
+
+
+@pytest.mark.parametrize("d,dtype", [(64, "f32"), (32, "f32"), (32, "bf16")])
+@pytest.mark.parametrize("decay,normalize", [(False, False), (True, True)])
+def test_unmasked_value_width_128(d, dtype, decay, normalize):
+    w = wl(d=d, chunk=32, dtype=dtype, decay=decay, n=117, seed=220 + d, qk="elu1" if normalize else "l2")
+    x = W.make_inputs(w)
+    o, st = run_forward(x, dtype, 32, normalize=normalize, eps=1e-6, unmasked=True)
+    o_ref, st_ref = run_oracle(x, normalize=normalize, eps=1e-6, unmasked=True)
+    assert_parity(o, o_ref, st, st_ref, tol=TOL_F32 if dtype == "f32" else TOL_BF16,
+                  what=f"unmasked dv128 d{d} {dtype}")
