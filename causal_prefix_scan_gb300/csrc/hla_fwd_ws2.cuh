@@ -431,6 +431,10 @@ struct Fwd2 {
         const int t0 = j * CT, qs = it & 1;
         const int pk = (pbh / P.H) * P.Hkv + (pbh % P.H) / (P.H / P.Hkv);
         const int ks = kslot(it);
+        // The second chunk's loads wait until the first chunk's Q and K have landed: at the
+        // start of the launch every CTA requests its inputs at once, and the first chunk's
+        // tiles, which the chain needs first, then do not share DRAM with the second's.
+        if (it == 1 && (!wait1(B_KF + kslot(0), kpar(0)) || !wait1(B_QF, qpar(0)))) return false;
         if (!wait1(B_KE + ks, kpar(it) ^ 1u)) return false;
         fence_async_smem();  // earlier generic reads of the buffer precede the overwrite
         mbar_expect_tx(bar(B_KF + ks), L_::SK);
