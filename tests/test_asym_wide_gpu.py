@@ -63,3 +63,26 @@ def test_unmasked_value_width_128(d, dtype, decay, normalize):
     o_ref, st_ref = run_oracle(x, normalize=normalize, eps=1e-6, unmasked=True)
     assert_parity(o, o_ref, st, st_ref, tol=TOL_F32 if dtype == "f32" else TOL_BF16,
                   what=f"unmasked dv128 d{d} {dtype}")
+
+
+@pytest.mark.parametrize("n", [1, 7, 64, 65])
+def test_asym_value_width_128_short_sequences(n):
+    """Sequences of one token, shorter than a chunk, exactly one chunk and one token more."""
+    w = wl(n=n, decay=True, seed=230 + n)
+    x = W.make_inputs(w)
+    o, st = run_forward(x, "bf16", 64, normalize=True, eps=1e-6, asymmetric=True)
+    o_ref, st_ref = run_oracle(x, normalize=True, eps=1e-6, asymmetric=True)
+    assert_parity(o, o_ref, st, st_ref, tol=TOL_BF16, what=f"asym dv128 n{n}", asymmetric=True)
+
+
+def test_asym_value_width_128_empty_sequence_copies_the_state():
+    """n = 0: state_out is state_in, all 128 value columns."""
+    w = wl(n=40, decay=True, seed=240)
+    x = W.make_inputs(w)
+    _, st1 = run_oracle(x, normalize=True, eps=1e-6, asymmetric=True)
+    empty = {kk: (vv[:, :, :0] if kk != "gamma" else vv) for kk, vv in x.items()}
+    o, st = run_forward(empty, "bf16", 64, normalize=True, eps=1e-6, state_in=st1, asymmetric=True)
+    assert o.shape == (1, 2, 0, 128)
+    for name in ("S", "C", "m", "G", "h"):
+        a, b = getattr(st, name), np.asarray(getattr(st1, name), np.float32)
+        assert np.array_equal(np.asarray(a, np.float32).reshape(b.shape), b), name

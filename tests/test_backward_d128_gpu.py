@@ -112,3 +112,10 @@ def test_backward_key_width_128_empty_sequence():
     w, x, g = case(64, 64, 0, "bf16", False, seed=52)
     dq, dk, dv = gpu_grads(w, x, g)
     assert dq.shape == (1, 2, 0, 128) and dv.shape == (1, 2, 0, 64)
+
+
+@pytest.mark.parametrize("n", [1, 15, 16, 17])
+def test_backward_key_width_128_short_sequences(n):
+    """One token, shorter than the 16-token inner chunk, exactly one and one token more."""
+    w, x, g = case(64, 64, n, "f32", True, seed=270 + n)
+    check(gpu_grads(w, x, g), oracle_grads(x, g), TOL_F32, f"bwd d128 n{n}")

@@ -101,3 +101,15 @@ def test_backward_normalised_key_width_128(dv, chunk, n, dtype, decay):
         assert np.all(np.isfinite(a)), name
         e = per_pair_errors(a, b).max()
         assert e <= tol, f"norm bwd d128 dv{dv} {dtype}: {name} {e:.3e}"
+
+
+@pytest.mark.parametrize("n", [1, 5, 32, 33])
+def test_fp32_forward_d128_short_sequences(n):
+    """d = dv = 128 (8-token inner chunks) and d = 128, dv = 64 (32-token) on sequences of
+    one token, shorter than a chunk, one chunk and one token more."""
+    for dv in (128, 64):
+        w = wl(dv=dv, chunk=64, n=n, decay=True, qk="elu1", seed=250 + n + dv)
+        x = W.make_inputs(w)
+        o, st = run_forward(x, "f32", 64, normalize=True, eps=1e-6)
+        o_ref, st_ref = run_oracle(x, normalize=True, eps=1e-6)
+        assert_parity(o, o_ref, st, st_ref, tol=TOL_F32, what=f"fp32 d128 dv{dv} n{n}")

@@ -115,3 +115,13 @@ def test_concatenation_at_key_width_128(dv, normalize):
         AB = hla.state3_combine(A, Bs, decay_pow=fpow, normalize=normalize, out=out)
         hla.hla_sync_status()
         check_state(AB, st_ref, w, normalize, TOL_F32, f"combine d128 dv{dv} into {where}")
+
+
+@pytest.mark.parametrize("n", [1, 15, 16, 17])
+def test_forward3_key_width_128_short_sequences(n):
+    """One token, shorter than the 16-token inner chunk, exactly one and one token more."""
+    w, x = case(64, 64, n, "f32", True, True, seed=260 + n)
+    o, st = gpu3(x, w, True)
+    o_ref, st_ref = oracle3(x, True)
+    assert per_pair_errors(o, o_ref).max() <= TOL_F32
+    check_state(st, st_ref, w, True, TOL_F32, f"fwd3 d128 n{n}")
