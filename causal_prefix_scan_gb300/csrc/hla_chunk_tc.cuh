@@ -16,7 +16,7 @@ namespace chunktc {
 struct ChunkMaps {
     CUtensorMap q, k, v, g;
 };
-// false if the driver's encoder is unavailable or rejects a tensor; g may be null
+// false if the CUDA driver's tensor-map encoder is unavailable or rejects a tensor; g may be null
 inline bool chunk_maps(ChunkMaps &m, const void *q, const void *k, const void *v, const void *g, int n, int units,
                        int kv_units) {
     return tc::encode_3d(&m.q, q, 64, n, units, 64) && tc::encode_3d(&m.k, k, 64, n, kv_units, 64) &&

@@ -31,7 +31,7 @@ struct Cached {
 };
 Cached g_scratch[kMaxDevices];
 
-// The driver's cuCtxGetCurrent, reached through the runtime (no link to libcuda).
+// The CUDA driver's cuCtxGetCurrent, reached through the runtime (no link to libcuda).
 PFN_cuCtxGetCurrent_v4000 ctx_getter() {
     static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
     if (!fn) {
