@@ -102,3 +102,30 @@ def test_the_last_tag_clears_header_and_flags(i):
     assert header(ws) == (0, 0, 0)
     assert same(run(c, ws), ref)
     assert header(ws) == (0, 1, 0)
+
+
+def test_split_call_shares_the_workspace_across_the_generation_wrap():
+    """The AHLA forward at dv = 128 runs two tensor-core launches per call on the same
+    workspace (one per value half): results equal those on a fresh workspace, bit for bit,
+    also when the first half's launch carries the last 32-bit tag."""
+    w = W.Workload("ws_asym", B=2, H=3, n=500, d=64, dv=128, chunk=64, dtype="bf16", qk="elu1", seed=111,
+                   decay=True, gamma_lo=0.9, gamma_hi=0.999, asymmetric=True)
+    x = W.make_inputs(w)
+    q, k, v = (to_dev(x[n], "bf16") for n in ("q", "k", "v"))
+    g = torch.from_numpy(np.asarray(x["gamma"], np.float32)).cuda()
+
+    def run_asym(ws=None):
+        o, st = hla.forward(q, k, v, chunk=64, gamma=g, normalize=True, eps=1e-6, return_state=True, workspace=ws,
+                            asymmetric=True)
+        hla.hla_sync_status()
+        return [o] + list(st.astuple())
+
+    ref = run_asym()
+    p = hla.make_params(q, v, 64, g, True, 1e-6, False, True)
+    ws = hla.new_workspace(hla.hla_forward_workspace_size(p))
+    assert same(run_asym(ws), ref)
+    assert same(run_asym(ws), ref)
+    assert header(ws) == (0, 4, 0)  # two calls of two launches
+    ws[4:8] = torch.from_numpy(np.array([0xFFFFFFFE], np.uint32).view(np.uint8).copy()).to(ws.device)
+    assert same(run_asym(ws), ref)
+    assert header(ws) == (0, 1, 0)  # the first half's launch cleared the header, the second took generation 1
