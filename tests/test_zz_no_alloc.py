@@ -61,3 +61,24 @@ def test_noalloc_rejects_oversized_problem():
     st = hla.library().hla_forward_chunked_noalloc(ctypes.byref(p), 16, 16, 16, 16, None, None, None)
     assert st == hla.HLA_ERR_UNSUPPORTED
     assert "scratch" in hla.hla_last_error()
+
+
+def test_noalloc_split_call():
+    """The AHLA forward at dv = 128 (two value-half launches) through the no-alloc entry:
+    the same results, bit for bit, as with a caller workspace, on two calls in a row."""
+    w = W.Workload("noalloc_asym", 1, 2, 3 * 64 + 9, 64, 128, 64, "bf16", "elu1", normalize=True, eps=1e-6, seed=43,
+                   decay=True, asymmetric=True)
+    q, k, v, g = _inputs(w)
+    units = w.B * w.H
+    o_ref, st_ref = hla.forward(q, k, v, chunk=64, gamma=g, normalize=True, eps=1e-6, return_state=True,
+                                asymmetric=True)
+    hla.hla_sync_status()
+    p = hla.make_params(q, v, 64, g, True, 1e-6, False, True)
+    assert 0 < hla.hla_forward_workspace_size(p) <= 32 << 20
+    for call in range(2):
+        o = torch.full(q.shape[:3] + (w.dv,), float("nan"), dtype=torch.bfloat16, device="cuda")
+        st = hla.State.empty(units, w.d, w.dv)
+        hla.hla_forward_chunked_noalloc(p, q, k, v, o, None, st)
+        hla.hla_sync_status()
+        assert torch.equal(o, o_ref), f"call {call}"
+        assert all(torch.equal(a, b) for a, b in zip(st.astuple(), st_ref.astuple())), f"call {call}"
